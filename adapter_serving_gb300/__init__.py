@@ -1,0 +1,259 @@
+"""GB300 (sm_103a) multi-tenant LoRA adapted linear layer.
+
+``y_i = W x_i + s * B_a (A_a x_i)`` for a batch whose rows each carry their own adapter id,
+with the base W read once per call and every distinct adapter's factors gathered once
+through a paged pool ("m07 -- Multi-Adapter (LoRA) Serving", section 6 "Deep Dive A:
+Batching Heterogeneous Adapters"; "LoRA, quotas and noisy neighbours", section "One weight
+read, many adapters").
+
+This module is the Python binding of the C ABI in ``include/lora_gb300.h``: it marshals
+arguments (torch tensors -> device pointers, the current CUDA stream) and nothing else;
+every step of the forward runs in the CUDA library ``_build/liblora_gb300.so``. Importing
+the package loads that library and fails loudly if it is missing -- there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = ["Pool", "LoraError", "build_segments", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF16"]
+
+LIB_PATH = _build.LIB
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"CUDA library not built: {LIB_PATH} is missing. Run `python adapter_serving_gb300/build.py` "
+        "(or __graft_entry__.build()) first.")
+lib = ctypes.CDLL(LIB_PATH)
+
+OK, EINVAL, ENOTLOADED, ENOMEM, ECUDA, EUNSUPPORTED, EDEVICE = 0, -1, -2, -3, -5, -6, -7
+DTYPE_F32, DTYPE_BF16 = 0, 1
+MAX_MODULES, MAX_RANK, PAGE_ROWS, MAX_DECODE_ROWS = 8, 64, 64, 256
+DEVERR = {0: "none", 1: "bad adapter id", 2: "adapter not loaded", 3: "in-kernel wait timed out",
+          4: "bad segment table"}
+
+_P, _I32, _I64, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+
+
+class lora_pool_desc(ctypes.Structure):
+    _fields_ = [("n_modules", _I32), ("d_in", ctypes.POINTER(_I32)), ("d_out", ctypes.POINTER(_I32)),
+                ("max_adapters", _I32), ("max_rank", _I32), ("pages", ctypes.POINTER(_I64)), ("max_rows", _I32)]
+
+
+class lora_module_io(ctypes.Structure):
+    _fields_ = [("module", _I32), ("x", _P), ("W", _P), ("y", _P)]
+
+
+def _sig(name, res, *args):
+    f = getattr(lib, name)
+    f.restype = res
+    f.argtypes = list(args)
+    return f
+
+
+_sig("lora_pool_create", ctypes.c_int, ctypes.POINTER(lora_pool_desc), ctypes.POINTER(_P))
+_sig("lora_pool_destroy", ctypes.c_int, _P)
+_sig("lora_pool_load", ctypes.c_int, _P, _I32, _I32, _P, _P, _I32, _P)
+_sig("lora_pool_unload", ctypes.c_int, _P, _I32, _P)
+_sig("lora_pool_query", ctypes.c_int, _P, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I64))
+_sig("lora_pool_free_rows", ctypes.c_int, _P, _I32, ctypes.POINTER(_I64))
+_sig("lora_build_segments", ctypes.c_int, _P, _I32, _P, _P, _P, ctypes.POINTER(_I32))
+_sig("lora_layer_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _I32, _F, _I32, _P)
+_sig("lora_linear_forward", ctypes.c_int, _P, _I32, _P, _P, _P, _I32, _F, _P, _I32, _P)
+_sig("lora_segment_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _P, _I32, _I32, _F,
+     _I32, _P)
+_sig("lora_pool_last_segments", ctypes.c_int, _P, _P, _P, _P, ctypes.POINTER(_I32), ctypes.POINTER(_I32))
+_sig("lora_last_device_error", ctypes.c_int, _P, ctypes.POINTER(_I32), ctypes.POINTER(_I32))
+_sig("lora_profile_enable", ctypes.c_int, _P, _I32)
+_sig("lora_profile_read", ctypes.c_int, _P, _I32, ctypes.POINTER(_I32), ctypes.POINTER(ctypes.c_double))
+_sig("lora_last_cuda_error", ctypes.c_char_p)
+_sig("lora_status_string", ctypes.c_char_p, ctypes.c_int)
+_sig("lora_version", ctypes.c_int)
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status, what):
+        msg = f"{what}: {lib.lora_status_string(status).decode()} ({status})"
+        if status == ECUDA:
+            msg += f" [{lib.lora_last_cuda_error().decode()}]"
+        super().__init__(msg)
+        self.status = status
+
+
+def _check(rc, what):
+    if rc != OK:
+        raise LoraError(rc, what)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _dev_bf16(t, what):
+    import torch
+    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+        raise ValueError(f"{what}: need a contiguous CUDA bf16 tensor")
+    return t
+
+
+def _dev_i32(t, what):
+    import torch
+    if not (t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()):
+        raise ValueError(f"{what}: need a contiguous CUDA int32 tensor")
+    return t
+
+
+def _y_dtype(y):
+    import torch
+    if not (y.is_cuda and y.is_contiguous()):
+        raise ValueError("y: need a contiguous CUDA tensor")
+    if y.dtype == torch.float32:
+        return DTYPE_F32
+    if y.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise ValueError("y: float32 or bfloat16")
+
+
+def build_segments(ids):
+    """Host-side stable grouping of rows by adapter id (lora_build_segments)."""
+    import numpy as np
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    n = len(ids)
+    perm = np.empty(max(1, n), np.int32)
+    seg_start = np.empty(n + 1, np.int32)
+    seg_adapter = np.empty(max(1, n), np.int32)
+    ns = _I32(0)
+    _check(lib.lora_build_segments(ids.ctypes.data, n, perm.ctypes.data, seg_start.ctypes.data,
+                                   seg_adapter.ctypes.data, ctypes.byref(ns)), "lora_build_segments")
+    k = ns.value
+    return perm[:n].copy(), seg_start[:k + 1].copy(), seg_adapter[:k].copy()
+
+
+class Pool:
+    """A paged adapter pool on the current CUDA device (lora_pool_create / _destroy)."""
+
+    def __init__(self, d_in, d_out, max_adapters, max_rank=MAX_RANK, pages=None, max_rows=MAX_DECODE_ROWS):
+        n = len(d_in)
+        self.d_in, self.d_out = list(map(int, d_in)), list(map(int, d_out))
+        self._din = (_I32 * n)(*self.d_in)
+        self._dout = (_I32 * n)(*self.d_out)
+        self._pages = None if pages is None else (_I64 * n)(*map(int, pages))
+        desc = lora_pool_desc(n, self._din, self._dout, int(max_adapters), int(max_rank),
+                              self._pages, int(max_rows))
+        h = _P()
+        _check(lib.lora_pool_create(ctypes.byref(desc), ctypes.byref(h)), "lora_pool_create")
+        self.handle = h
+        self.max_adapters, self.max_rank, self.max_rows = int(max_adapters), int(max_rank), int(max_rows)
+
+    def close(self):
+        if self.handle:
+            lib.lora_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- residency
+    def load(self, adapter_id, module, A, B, stream=None):
+        """A: bf16 [rank, d_in], B: bf16 [d_out, rank]; host (pinned or pageable) or CUDA tensors."""
+        import torch
+        for t, nm in ((A, "A"), (B, "B")):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError(f"{nm}: need a contiguous bf16 tensor")
+        rank = A.shape[0]
+        if B.shape != (self.d_out[module], rank) or A.shape != (rank, self.d_in[module]):
+            raise ValueError(f"factor shapes {tuple(A.shape)} / {tuple(B.shape)} do not match module {module}")
+        _check(lib.lora_pool_load(self.handle, int(adapter_id), int(module), _ptr(A), _ptr(B), int(rank),
+                                  _stream(stream)), "lora_pool_load")
+
+    def unload(self, adapter_id, stream=None):
+        _check(lib.lora_pool_unload(self.handle, int(adapter_id), _stream(stream)), "lora_pool_unload")
+
+    def query(self, adapter_id, module):
+        r, off = _I32(0), _I64(0)
+        _check(lib.lora_pool_query(self.handle, int(adapter_id), int(module), ctypes.byref(r), ctypes.byref(off)),
+               "lora_pool_query")
+        return r.value, off.value
+
+    def free_rows(self, module):
+        f = _I64(0)
+        _check(lib.lora_pool_free_rows(self.handle, int(module), ctypes.byref(f)), "lora_pool_free_rows")
+        return f.value
+
+    # ---- forward
+    @staticmethod
+    def _ios(ios):
+        arr = (lora_module_io * len(ios))()
+        dt = None
+        for i, (module, x, W, y) in enumerate(ios):
+            _dev_bf16(x, "x"), _dev_bf16(W, "W")
+            d = _y_dtype(y)
+            if dt is not None and d != dt:
+                raise ValueError("all outputs of one call share a dtype")
+            dt = d
+            arr[i] = lora_module_io(int(module), x.data_ptr(), W.data_ptr(), y.data_ptr())
+        return arr, dt
+
+    def layer_forward(self, ios, row_adapter_ids, scale, stream=None):
+        """ios: [(module, x, W, y)], row_adapter_ids: CUDA int32 [n] (-1 = base only)."""
+        arr, dt = self._ios(ios)
+        ids = _dev_i32(row_adapter_ids, "row_adapter_ids")
+        _check(lib.lora_layer_forward(self.handle, len(ios), arr, _ptr(ids), ids.numel(), float(scale), dt,
+                                      _stream(stream)), "lora_layer_forward")
+
+    def linear_forward(self, module, x, W, row_adapter_ids, scale, y, stream=None):
+        _dev_bf16(x, "x"), _dev_bf16(W, "W")
+        ids = _dev_i32(row_adapter_ids, "row_adapter_ids")
+        _check(lib.lora_linear_forward(self.handle, int(module), _ptr(x), _ptr(W), _ptr(ids), ids.numel(),
+                                       float(scale), _ptr(y), _y_dtype(y), _stream(stream)), "lora_linear_forward")
+
+    def segment_forward(self, ios, seg_start, seg_adapter, n, scale, stream=None):
+        """Grouped rows: seg_start CUDA int32 [n_seg+1], seg_adapter CUDA int32 [n_seg]."""
+        arr, dt = self._ios(ios)
+        ss, sa = _dev_i32(seg_start, "seg_start"), _dev_i32(seg_adapter, "seg_adapter")
+        _check(lib.lora_segment_forward(self.handle, len(ios), arr, _ptr(ss), _ptr(sa), sa.numel(), int(n),
+                                        float(scale), dt, _stream(stream)), "lora_segment_forward")
+
+    def last_segments(self):
+        """(perm or None, seg_start, seg_adapter) of the most recent forward, read back from the device."""
+        import numpy as np
+        n, ns = _I32(0), _I32(0)
+        _check(lib.lora_pool_last_segments(self.handle, None, None, None, ctypes.byref(ns), ctypes.byref(n)),
+               "lora_pool_last_segments")
+        perm = np.full(max(1, n.value), -7, np.int32)
+        ss = np.empty(ns.value + 1, np.int32)
+        sa = np.empty(max(1, ns.value), np.int32)
+        _check(lib.lora_pool_last_segments(self.handle, perm.ctypes.data, ss.ctypes.data, sa.ctypes.data,
+                                           ctypes.byref(ns), ctypes.byref(n)), "lora_pool_last_segments")
+        decoded = n.value <= MAX_DECODE_ROWS
+        return (perm[:n.value].copy() if decoded else None), ss, sa[:ns.value].copy()
+
+    KERNELS = {"prep": 0, "shrink": 1, "gemm": 2}
+
+    def profile(self, enable=True):
+        _check(lib.lora_profile_enable(self.handle, 1 if enable else 0), "lora_profile_enable")
+
+    def profile_read(self, kernel):
+        """(launches, total device ms) of one kernel kind since the last read."""
+        n, ms = _I32(0), ctypes.c_double(0)
+        _check(lib.lora_profile_read(self.handle, self.KERNELS[kernel], ctypes.byref(n), ctypes.byref(ms)),
+               "lora_profile_read")
+        return n.value, ms.value
+
+    def last_device_error(self):
+        c, d = _I32(0), _I32(0)
+        _check(lib.lora_last_device_error(self.handle, ctypes.byref(c), ctypes.byref(d)), "lora_last_device_error")
+        return c.value, d.value

@@ -1,0 +1,626 @@
+// lora_api.cu -- host side of the C ABI declared in include/lora_gb300.h: the paged adapter
+// pool (64-row pages per projection, carved into power-of-two runs of rank-vectors by a
+// buddy allocator), the device-side (pointer, rank) table, the workspace, and the forward
+// entry points that queue the prep / shrink / tcgen05 kernels.
+//
+// Paging follows "LoRA, quotas and noisy neighbours", section "Adapter weights and KV in one
+// pool", and "12. Adapter Serving and Multi-Tenant Customization", sections "S-LoRA's unified
+// paging" (fixed-size pages, gathered through indirection) and "vLLM's pre-allocated LoRA
+// buffers" (capacity fixed at creation: max adapters, max rank).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "lora_internal.h"
+
+using namespace lora;
+
+namespace {
+
+thread_local std::string g_last_cuda_error;
+
+int cuda_fail(cudaError_t e, const char *what) {
+    g_last_cuda_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return LORA_ECUDA;
+}
+
+#define LORA_CUDA(call)                                 \
+    do {                                                \
+        cudaError_t e_ = (call);                        \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+    } while (0)
+
+int storage_rank(int r) {
+    int rp = 8;
+    while (rp < r) rp <<= 1;
+    return rp;
+}
+int order_of(int rp) { return rp == 8 ? 0 : rp == 16 ? 1 : rp == 32 ? 2 : 3; }
+
+// Buddy allocator over one projection's pages: runs of 8/16/32/64 rows, aligned to their size,
+// never crossing a 64-row page.
+struct RowAllocator {
+    std::set<int64_t> free_[4];
+    int64_t free_rows = 0;
+    void init(int64_t pages) {
+        for (auto &f : free_) f.clear();
+        for (int64_t p = 0; p < pages; ++p) free_[3].insert(p * LORA_PAGE_ROWS);
+        free_rows = pages * LORA_PAGE_ROWS;
+    }
+    int64_t alloc(int order) {
+        int o = order;
+        while (o < 4 && free_[o].empty()) ++o;
+        if (o == 4) return -1;
+        int64_t off = *free_[o].begin();
+        free_[o].erase(free_[o].begin());
+        while (o > order) {  // split, keep the lower half
+            --o;
+            free_[o].insert(off + (int64_t(8) << o));
+        }
+        free_rows -= int64_t(8) << order;
+        return off;
+    }
+    void release(int64_t off, int order) {
+        free_rows += int64_t(8) << order;
+        while (order < 3) {
+            const int64_t buddy = off ^ (int64_t(8) << order);
+            auto it = free_[order].find(buddy);
+            if (it == free_[order].end()) break;
+            free_[order].erase(it);
+            off = std::min(off, buddy);
+            ++order;
+        }
+        free_[order].insert(off);
+    }
+};
+
+struct ModuleStore {
+    int d_in = 0, d_out = 0;
+    int64_t pages = 0;
+    uint16_t *A = nullptr;  // [pages * 64, d_in]
+    uint16_t *B = nullptr;  // [pages * 64 * d_out] (rank-major runs of [d_out, rp])
+    RowAllocator rows;
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (row-major), box {64 cols, box_rows rows}, 128-byte swizzle.
+int make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled unavailable";
+        return LORA_ECUDA;
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
+        return LORA_ECUDA;
+    }
+    return LORA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+struct lora_pool {
+    int device = 0;
+    int num_sms = 0;
+    int n_modules = 0;
+    ModuleStore mod[LORA_MAX_MODULES];
+    int max_adapters = 0, max_rank = 0, max_rows = 0;
+    PoolEntry *d_table = nullptr;     // [n_modules][max_adapters]
+    std::vector<PoolEntry> h_table;
+    std::vector<int> rp_count;        // loaded entries per storage-rank order (for rpmax)
+    // workspace
+    int32_t *perm = nullptr, *seg_start = nullptr, *seg_adapter = nullptr, *n_seg = nullptr, *err = nullptr;
+    float *T = nullptr;               // [LORA_MAX_MODULES][max_rows][64]
+    float *shrink_part = nullptr;     // [LORA_MAX_MODULES][ks_cap][256][64]
+    int32_t *shrink_cnt = nullptr;    // [LORA_MAX_MODULES][256]
+    float *gemm_part = nullptr;       // [num_sms][2][128 * 256]
+    int32_t *tile_cnt = nullptr;      // [tile_cap]
+    int ks_cap = 0, tile_cap = 0;
+    // kernel timing: pending event pairs per kernel kind
+    bool profiling = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> prof_pending[3];
+    std::vector<cudaEvent_t> prof_free;
+    int last_n = 0;                   // rows of the most recent forward
+    bool last_decode = false;
+    std::vector<void *> allocations;
+
+    PoolEntry &entry(int m, int a) { return h_table[(size_t)m * max_adapters + a]; }
+    int rpmax() const {
+        for (int o = 3; o >= 0; --o)
+            if (rp_count[o] > 0) return 8 << o;
+        return 8;
+    }
+};
+
+static int dev_alloc(lora_pool *p, void **ptr, size_t bytes) {
+    cudaError_t e = cudaMalloc(ptr, std::max<size_t>(bytes, 256));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        g_last_cuda_error = std::string("cudaMalloc: ") + cudaGetErrorString(e);
+        return LORA_ENOMEM;
+    }
+    p->allocations.push_back(*ptr);
+    return LORA_OK;
+}
+
+extern "C" {
+
+int lora_version(void) { return 10000; }
+
+const char *lora_status_string(int s) {
+    switch (s) {
+        case LORA_OK: return "ok";
+        case LORA_EINVAL: return "invalid argument";
+        case LORA_ENOTLOADED: return "adapter not resident";
+        case LORA_ENOMEM: return "out of pool pages or device memory";
+        case LORA_ECUDA: return "CUDA error";
+        case LORA_EUNSUPPORTED: return "unsupported request";
+        case LORA_EDEVICE: return "device-side error recorded";
+        default: return "unknown status";
+    }
+}
+
+const char *lora_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+int lora_pool_destroy(lora_pool *p) {
+    if (!p) return LORA_EINVAL;
+    cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    for (void *a : p->allocations) cudaFree(a);
+    for (auto &v : p->prof_pending)
+        for (auto &e : v) {
+            cudaEventDestroy(e.first);
+            cudaEventDestroy(e.second);
+        }
+    for (auto e : p->prof_free) cudaEventDestroy(e);
+    delete p;
+    return LORA_OK;
+}
+
+int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
+    if (!d || !out || !d->d_in || !d->d_out) return LORA_EINVAL;
+    if (d->n_modules < 1 || d->n_modules > LORA_MAX_MODULES) return LORA_EINVAL;
+    if (d->max_adapters < 1 || d->max_rank < 1 || d->max_rank > LORA_MAX_RANK || d->max_rows < 1) return LORA_EINVAL;
+    for (int m = 0; m < d->n_modules; ++m) {
+        if (d->d_in[m] < 8 || d->d_out[m] < 8 || d->d_in[m] % 8 || d->d_out[m] % 8) return LORA_EINVAL;
+        if (d->pages && d->pages[m] < 0) return LORA_EINVAL;
+    }
+    *out = nullptr;
+    int device = 0, num_sms = 0;
+    LORA_CUDA(cudaGetDevice(&device));
+    LORA_CUDA(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device));
+    lora_pool *p = new lora_pool();
+    p->device = device;
+    p->num_sms = num_sms;
+    p->n_modules = d->n_modules;
+    p->max_adapters = d->max_adapters;
+    p->max_rank = d->max_rank;
+    p->max_rows = d->max_rows;
+    p->rp_count.assign(4, 0);
+    const int rp_cap = storage_rank(d->max_rank);
+    int rc;
+    for (int m = 0; m < p->n_modules; ++m) {
+        ModuleStore &s = p->mod[m];
+        s.d_in = d->d_in[m];
+        s.d_out = d->d_out[m];
+        s.pages = d->pages ? d->pages[m]
+                           : ((int64_t)d->max_adapters * rp_cap + LORA_PAGE_ROWS - 1) / LORA_PAGE_ROWS;
+        const size_t rows = (size_t)s.pages * LORA_PAGE_ROWS;
+        if ((rc = dev_alloc(p, (void **)&s.A, rows * s.d_in * 2)) ||
+            (rc = dev_alloc(p, (void **)&s.B, rows * s.d_out * 2))) {
+            lora_pool_destroy(p);
+            return rc;
+        }
+        s.rows.init(s.pages);
+    }
+    p->h_table.assign((size_t)p->n_modules * p->max_adapters, PoolEntry{nullptr, nullptr, 0, 0, -1});
+    const size_t tbytes = p->h_table.size() * sizeof(PoolEntry);
+    if ((rc = dev_alloc(p, (void **)&p->d_table, tbytes))) {
+        lora_pool_destroy(p);
+        return rc;
+    }
+    // workspace
+    int max_din = 0, max_dout = 0;
+    for (int m = 0; m < p->n_modules; ++m) {
+        max_din = std::max(max_din, p->mod[m].d_in);
+        max_dout = std::max(max_dout, p->mod[m].d_out);
+    }
+    p->ks_cap = (max_din + 511) / 512;
+    p->tile_cap = LORA_MAX_MODULES * ((max_dout + kBM - 1) / kBM);
+    const size_t R = (size_t)p->max_rows;
+    if ((rc = dev_alloc(p, (void **)&p->perm, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->seg_start, (R + 2) * 4)) ||
+        (rc = dev_alloc(p, (void **)&p->seg_adapter, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->n_seg, 16)) ||
+        (rc = dev_alloc(p, (void **)&p->err, 16)) ||
+        (rc = dev_alloc(p, (void **)&p->T, (size_t)LORA_MAX_MODULES * R * LORA_MAX_RANK * 4)) ||
+        (rc = dev_alloc(p, (void **)&p->shrink_part,
+                        (size_t)LORA_MAX_MODULES * p->ks_cap * LORA_MAX_DECODE_ROWS * LORA_MAX_RANK * 4)) ||
+        (rc = dev_alloc(p, (void **)&p->shrink_cnt, (size_t)LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS * 4)) ||
+        (rc = dev_alloc(p, (void **)&p->gemm_part, (size_t)p->num_sms * 2 * kBM * 256 * 4)) ||
+        (rc = dev_alloc(p, (void **)&p->tile_cnt, (size_t)p->tile_cap * 4))) {
+        lora_pool_destroy(p);
+        return rc;
+    }
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = cudaMemset(p->d_table, 0, tbytes);
+    if (e == cudaSuccess) e = cudaMemset(p->err, 0, 16);
+    if (e == cudaSuccess) e = cudaMemset(p->n_seg, 0, 16);
+    if (e == cudaSuccess) e = cudaMemset(p->shrink_cnt, 0, (size_t)LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS * 4);
+    if (e == cudaSuccess) e = cudaMemset(p->tile_cnt, 0, (size_t)p->tile_cap * 4);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        lora_pool_destroy(p);
+        return cuda_fail(e, "pool init");
+    }
+    *out = p;
+    return LORA_OK;
+}
+
+int lora_pool_query(const lora_pool *p, int32_t a, int32_t m, int32_t *rank, int64_t *row_off) {
+    if (!p || m < 0 || m >= p->n_modules || a < 0 || a >= p->max_adapters) return LORA_EINVAL;
+    const PoolEntry &e = p->h_table[(size_t)m * p->max_adapters + a];
+    if (rank) *rank = e.rank;
+    if (row_off) *row_off = e.rank > 0 ? e.row_off : -1;
+    return LORA_OK;
+}
+
+int lora_pool_free_rows(const lora_pool *p, int32_t m, int64_t *free_rows) {
+    if (!p || !free_rows || m < 0 || m >= p->n_modules) return LORA_EINVAL;
+    *free_rows = p->mod[m].rows.free_rows;
+    return LORA_OK;
+}
+
+static void release_entry(lora_pool *p, int m, int a) {
+    PoolEntry &e = p->entry(m, a);
+    if (e.rank > 0) {
+        p->mod[m].rows.release(e.row_off, order_of(e.rp));
+        p->rp_count[order_of(e.rp)]--;
+    }
+    e = PoolEntry{nullptr, nullptr, 0, 0, -1};
+}
+
+int lora_pool_load(lora_pool *p, int32_t a, int32_t m, const void *A, const void *B, int32_t rank,
+                   lora_stream_t stream) {
+    if (!p || !A || !B || m < 0 || m >= p->n_modules || a < 0 || a >= p->max_adapters) return LORA_EINVAL;
+    if (rank < 1 || rank > p->max_rank) return LORA_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    ModuleStore &ms = p->mod[m];
+    const int rp = storage_rank(rank);
+    // a reload replaces the old factors; free first so the rows can be reused
+    release_entry(p, m, a);
+    const int64_t off = ms.rows.alloc(order_of(rp));
+    if (off < 0) {
+        LORA_CUDA(launch_table_write(p->d_table + (size_t)m * p->max_adapters + a, p->entry(m, a), s));
+        return LORA_ENOMEM;
+    }
+    uint16_t *Ad = ms.A + (size_t)off * ms.d_in;
+    uint16_t *Bd = ms.B + (size_t)off * ms.d_out;
+    LORA_CUDA(cudaMemcpyAsync(Ad, A, (size_t)rank * ms.d_in * 2, cudaMemcpyDefault, s));
+    if (rank < rp) LORA_CUDA(cudaMemsetAsync(Ad + (size_t)rank * ms.d_in, 0, (size_t)(rp - rank) * ms.d_in * 2, s));
+    if (rank == rp) {
+        LORA_CUDA(cudaMemcpyAsync(Bd, B, (size_t)ms.d_out * rank * 2, cudaMemcpyDefault, s));
+    } else {
+        LORA_CUDA(cudaMemsetAsync(Bd, 0, (size_t)ms.d_out * rp * 2, s));
+        LORA_CUDA(cudaMemcpy2DAsync(Bd, (size_t)rp * 2, B, (size_t)rank * 2, (size_t)rank * 2, ms.d_out,
+                                    cudaMemcpyDefault, s));
+    }
+    PoolEntry e{Ad, Bd, rank, rp, off};
+    p->entry(m, a) = e;
+    p->rp_count[order_of(rp)]++;
+    LORA_CUDA(launch_table_write(p->d_table + (size_t)m * p->max_adapters + a, e, s));
+    return LORA_OK;
+}
+
+int lora_pool_unload(lora_pool *p, int32_t a, lora_stream_t stream) {
+    if (!p || a < 0 || a >= p->max_adapters) return LORA_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    bool any = false;
+    for (int m = 0; m < p->n_modules; ++m) {
+        if (p->entry(m, a).rank > 0) {
+            any = true;
+            release_entry(p, m, a);
+            LORA_CUDA(launch_table_write(p->d_table + (size_t)m * p->max_adapters + a, p->entry(m, a), s));
+        }
+    }
+    return any ? LORA_OK : LORA_ENOTLOADED;
+}
+
+int lora_build_segments(const int32_t *ids, int32_t n, int32_t *perm, int32_t *seg_start, int32_t *seg_adapter,
+                        int32_t *n_seg) {
+    if (n < 0 || !seg_start || !n_seg || (n > 0 && (!ids || !perm || !seg_adapter))) return LORA_EINVAL;
+    std::vector<int32_t> order(n);
+    for (int i = 0; i < n; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return ids[x] < ids[y]; });
+    int ns = 0;
+    for (int q = 0; q < n; ++q) {
+        perm[q] = order[q];
+        if (q == 0 || ids[order[q]] != ids[order[q - 1]]) {
+            seg_start[ns] = q;
+            seg_adapter[ns] = ids[order[q]];
+            ++ns;
+        }
+    }
+    seg_start[ns] = n;
+    *n_seg = ns;
+    return LORA_OK;
+}
+
+int lora_pool_last_segments(lora_pool *p, int32_t *perm, int32_t *seg_start, int32_t *seg_adapter, int32_t *n_seg,
+                            int32_t *n) {
+    if (!p) return LORA_EINVAL;
+    LORA_CUDA(cudaSetDevice(p->device));
+    LORA_CUDA(cudaDeviceSynchronize());
+    int32_t ns = 0;
+    LORA_CUDA(cudaMemcpy(&ns, p->n_seg, 4, cudaMemcpyDeviceToHost));
+    if (ns < 0 || ns > p->max_rows + 1) ns = 0;
+    if (n) *n = p->last_n;
+    if (n_seg) *n_seg = ns;
+    if (perm && p->last_decode && p->last_n > 0)
+        LORA_CUDA(cudaMemcpy(perm, p->perm, (size_t)p->last_n * 4, cudaMemcpyDeviceToHost));
+    if (seg_start) LORA_CUDA(cudaMemcpy(seg_start, p->seg_start, (size_t)(ns + 1) * 4, cudaMemcpyDeviceToHost));
+    if (seg_adapter && ns > 0) LORA_CUDA(cudaMemcpy(seg_adapter, p->seg_adapter, (size_t)ns * 4, cudaMemcpyDeviceToHost));
+    return LORA_OK;
+}
+
+int lora_last_device_error(lora_pool *p, int32_t *code, int32_t *detail) {
+    if (!p) return LORA_EINVAL;
+    LORA_CUDA(cudaSetDevice(p->device));
+    LORA_CUDA(cudaDeviceSynchronize());
+    int32_t h[2] = {0, 0};
+    LORA_CUDA(cudaMemcpy(h, p->err, 8, cudaMemcpyDeviceToHost));
+    LORA_CUDA(cudaMemset(p->err, 0, 8));
+    if (code) *code = h[0];
+    if (detail) *detail = h[1];
+    return LORA_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ profiling --------------
+
+static cudaEvent_t prof_event(lora_pool *p) {
+    if (!p->prof_free.empty()) {
+        cudaEvent_t e = p->prof_free.back();
+        p->prof_free.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Runs `launch` between two recorded events when profiling is on.
+template <class F>
+static cudaError_t timed_launch(lora_pool *p, int kind, cudaStream_t s, F &&launch) {
+    if (!p->profiling) return launch();
+    cudaEvent_t a = prof_event(p), b = prof_event(p);
+    if (!a || !b) return launch();
+    cudaEventRecord(a, s);
+    cudaError_t e = launch();
+    cudaEventRecord(b, s);
+    p->prof_pending[kind].push_back({a, b});
+    return e;
+}
+
+extern "C" int lora_profile_enable(lora_pool *p, int32_t enable) {
+    if (!p) return LORA_EINVAL;
+    p->profiling = enable != 0;
+    return LORA_OK;
+}
+
+extern "C" int lora_profile_read(lora_pool *p, int32_t kind, int32_t *launches, double *total_ms) {
+    if (!p || kind < 0 || kind > 2) return LORA_EINVAL;
+    LORA_CUDA(cudaSetDevice(p->device));
+    LORA_CUDA(cudaDeviceSynchronize());
+    double tot = 0;
+    for (auto &pr : p->prof_pending[kind]) {
+        float ms = 0;
+        LORA_CUDA(cudaEventElapsedTime(&ms, pr.first, pr.second));
+        tot += ms;
+        p->prof_free.push_back(pr.first);
+        p->prof_free.push_back(pr.second);
+    }
+    if (launches) *launches = (int32_t)p->prof_pending[kind].size();
+    if (total_ms) *total_ms = tot;
+    p->prof_pending[kind].clear();
+    return LORA_OK;
+}
+
+// ------------------------------------------------------------------ forward ----------------
+
+static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const int32_t *ids,
+                        const int32_t *seg_start, const int32_t *seg_adapter, int n_seg, int n, float scale,
+                        int y_dtype, cudaStream_t s) {
+    if (!p || !io || n_io < 1 || n_io > LORA_MAX_MODULES || n < 0 || n > p->max_rows) return LORA_EINVAL;
+    if (y_dtype != LORA_DTYPE_F32 && y_dtype != LORA_DTYPE_BF16) return LORA_EINVAL;
+    for (int i = 0; i < n_io; ++i) {
+        const lora_module_io &m = io[i];
+        if (m.module < 0 || m.module >= p->n_modules || !m.x || !m.W || !m.y) return LORA_EINVAL;
+        if (!aligned16(m.x) || !aligned16(m.W) || !aligned16(m.y)) return LORA_EINVAL;
+    }
+    if (ids == nullptr && (!seg_start || !seg_adapter || n_seg < 1 || n_seg > n + 1)) {
+        if (!(n == 0 && seg_start && seg_adapter)) return LORA_EINVAL;
+    }
+    if (n == 0) return LORA_OK;
+    const bool decode = n <= LORA_MAX_DECODE_ROWS;
+    if (ids && !decode) return LORA_EUNSUPPORTED;
+    cudaError_t e;
+
+    // ---- prep: row grouping / checks
+    PrepParams pp{};
+    pp.ids = ids;
+    pp.seg_start_in = seg_start;
+    pp.seg_adapter_in = seg_adapter;
+    pp.n_seg_in = n_seg;
+    pp.n = n;
+    pp.max_adapters = p->max_adapters;
+    pp.n_mod = n_io;
+    for (int i = 0; i < n_io; ++i) pp.table[i] = p->d_table + (size_t)io[i].module * p->max_adapters;
+    pp.perm = p->perm;
+    pp.seg_start = p->seg_start;
+    pp.seg_adapter = p->seg_adapter;
+    pp.n_seg = p->n_seg;
+    pp.err = p->err;
+    e = timed_launch(p, LORA_KERNEL_PREP, s,
+                     [&] { return decode ? launch_prep_decode(pp, s) : launch_prep_segments(pp, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "prep kernel");
+    p->last_n = n;
+    p->last_decode = decode;
+
+    const int rpmax = p->rpmax();
+
+    // ---- shrink: T[m][q][:] = s * A_a x_row(q)
+    ShrinkParams sp{};
+    sp.n_mod = n_io;
+    sp.n = n;
+    sp.rpmax = rpmax;
+    sp.by_segment = decode ? 1 : 0;
+    sp.max_units = LORA_MAX_DECODE_ROWS;
+    sp.ks_max = p->ks_cap;
+    sp.scale = scale;
+    sp.perm = decode ? p->perm : nullptr;
+    sp.seg_start = p->seg_start;
+    sp.seg_adapter = p->seg_adapter;
+    sp.n_seg = p->n_seg;
+    sp.partials = p->shrink_part;
+    sp.counters = p->shrink_cnt;
+    const int kc_dec = rpmax <= 8 ? 2048 : rpmax <= 16 ? 1024 : 512;
+    int splits = 0;
+    for (int i = 0; i < n_io; ++i) {
+        const ModuleStore &ms = p->mod[io[i].module];
+        sp.x[i] = static_cast<const uint16_t *>(io[i].x);
+        sp.table[i] = pp.table[i];
+        sp.T[i] = p->T + (size_t)i * p->max_rows * LORA_MAX_RANK;
+        sp.d_in[i] = ms.d_in;
+        sp.kc[i] = decode ? std::min(kc_dec, ms.d_in) : ms.d_in;
+        sp.ksplit[i] = (ms.d_in + sp.kc[i] - 1) / sp.kc[i];
+        sp.split_begin[i] = splits;
+        splits += sp.ksplit[i];
+    }
+    sp.split_begin[n_io] = splits;
+    const int units = decode ? n : (n + kShrinkGroupRows - 1) / kShrinkGroupRows;
+    e = timed_launch(p, LORA_KERNEL_SHRINK, s, [&] { return launch_shrink(sp, units, splits, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "shrink kernel");
+
+    // ---- base + expand on tcgen05
+    GemmParams gp;
+    memset(&gp, 0, sizeof gp);
+    gp.n_mod = n_io;
+    gp.n = n;
+    gp.nt = decode ? ((n + 15) & ~15) : 256;
+    gp.n_chunks = (n + gp.nt - 1) / gp.nt;
+    gp.decode = decode ? 1 : 0;
+    gp.stream_k = gp.n_chunks == 1 ? 1 : 0;
+    gp.rpmax = rpmax;
+    gp.unit_rows = rpmax >= 64 ? 8 : 32;
+    gp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
+    gp.raster_group = 8;
+    int64_t iters = 0;
+    int tiles = 0;
+    for (int i = 0; i < n_io; ++i) {
+        const ModuleStore &ms = p->mod[io[i].module];
+        GemmModule &gm = gp.mod[i];
+        int rc = make_tmap(&gm.tmW, io[i].W, ms.d_out, ms.d_in, kBM);
+        if (rc) return rc;
+        rc = make_tmap(&gm.tmX, io[i].x, n, ms.d_in, gp.nt);
+        if (rc) return rc;
+        gm.y = io[i].y;
+        gm.T = sp.T[i];
+        gm.table = pp.table[i];
+        gm.d_in = ms.d_in;
+        gm.d_out = ms.d_out;
+        gm.m_tiles = (ms.d_out + kBM - 1) / kBM;
+        gm.k_blocks = (ms.d_in + kBK - 1) / kBK;
+        gm.iter_begin = iters;
+        gm.tile_begin = tiles;
+        const int mt = gm.m_tiles * gp.n_chunks;
+        tiles += mt;
+        iters += (int64_t)mt * gm.k_blocks;
+    }
+    if (gp.stream_k && tiles > p->tile_cap) return LORA_EUNSUPPORTED;
+    gp.total_tiles = tiles;
+    gp.total_iters = iters;
+    if (gp.stream_k) {
+        // every CTA gets at least 4 k-blocks, so all ranges are non-empty
+        gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(p->num_sms, iters / 4));
+    } else {
+        gp.n_cta = std::min(p->num_sms, tiles);
+    }
+    gp.tmem_cols = 32;
+    while (gp.tmem_cols < 2 * gp.nt) gp.tmem_cols <<= 1;
+    gp.slot_bytes = (kBM * rpmax * 2 + gp.unit_rows * rpmax * 4 + 127) & ~127;
+    const int ring_target = rpmax <= 16 ? 48 * 1024 : 72 * 1024;
+    gp.n_slots = std::max(2, std::min(kMaxSlots, ring_target / gp.slot_bytes));
+    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)gp.nt * kBK * 2;
+    const size_t budget = 227 * 1024;
+    const size_t fixed = gemm_smem_bytes(gp.nt, 0, gp.n_slots, gp.slot_bytes);
+    int stages = (int)std::min<size_t>(kMaxStages, (budget - fixed - 16 * kMaxStages) / stage);
+    if (stages < 2) return LORA_EUNSUPPORTED;
+    gp.n_stages = stages;
+    gp.perm = p->perm;
+    gp.seg_start = p->seg_start;
+    gp.seg_adapter = p->seg_adapter;
+    gp.n_seg = p->n_seg;
+    gp.partials = p->gemm_part;
+    gp.tile_counters = p->tile_cnt;
+    gp.err = p->err;
+    const size_t smem = gemm_smem_bytes(gp.nt, gp.n_stages, gp.n_slots, gp.slot_bytes);
+    e = timed_launch(p, LORA_KERNEL_GEMM, s, [&] { return launch_gemm(gp, smem, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "gemm kernel");
+    return LORA_OK;
+}
+
+extern "C" {
+
+int lora_layer_forward(lora_pool *p, int32_t n_io, const lora_module_io *io, const int32_t *ids, int32_t n,
+                       float scale, int32_t y_dtype, lora_stream_t stream) {
+    if (!ids && n > 0) return LORA_EINVAL;
+    if (n > LORA_MAX_DECODE_ROWS) return LORA_EUNSUPPORTED;
+    return forward_impl(p, n_io, io, ids, nullptr, nullptr, 0, n, scale, y_dtype,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lora_linear_forward(lora_pool *p, int32_t module, const void *x, const void *W, const int32_t *ids, int32_t n,
+                        float scale, void *y, int32_t y_dtype, lora_stream_t stream) {
+    lora_module_io io{module, x, W, y};
+    return lora_layer_forward(p, 1, &io, ids, n, scale, y_dtype, stream);
+}
+
+int lora_segment_forward(lora_pool *p, int32_t n_io, const lora_module_io *io, const int32_t *seg_start,
+                         const int32_t *seg_adapter, int32_t n_seg, int32_t n, float scale, int32_t y_dtype,
+                         lora_stream_t stream) {
+    if (!seg_start || !seg_adapter) return LORA_EINVAL;
+    return forward_impl(p, n_io, io, nullptr, seg_start, seg_adapter, n_seg, n, scale, y_dtype,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

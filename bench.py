@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""Benchmark: multi-tenant LoRA adapted-layer decode on one GB300 (or N replicas).
+
+Workload: the pages' 70B attention layer at decode -- q/o 8192->8192, k/v 8192->1024, 128
+rows each carrying its own adapter (128 distinct rank-8 adapters on all four projections),
+scale 1 ("m07 -- Multi-Adapter (LoRA) Serving", section 2 "Scale Numbers", the batch-128
+distinct-adapter case).  One step = the whole hot path for one batch: q/k/v in one call
+(they read the same x), then o, each call = row grouping + shrink + tcgen05 base/expand.
+
+Printed (rank 0, one JSON line): tokens/s (rows/s) over all GPUs, ms per step, HBM GB/s of
+algorithmic bytes, the dominant kernel's roofline fraction (CUDA events on the launch
+stream), the end-to-end number through the C ABI with host buffers, the CPU oracle as a
+reported baseline, and SM clocks sampled during the timed region.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica (the path has no
+exchange step), value = rows of all ranks / max step time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "adapted-layer decode tokens/s & HBM GB/s at batch 128, distinct adapters, 1 GB300"
+UNIT = "tokens/s"
+FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="timed loop only (for profiler launch lists)")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def algorithmic_bytes(w):
+    """Algorithmic bytes of one step: W once, each distinct adapter's factors once, x once per
+    stage, y written once (fp32)."""
+    ids = w.row_adapters()
+    distinct = sorted(set(int(a) for a in ids if a >= 0))
+    mods = w.module_names()
+    W = sum(w.modules[m][0] * w.modules[m][1] * 2 for m in mods)
+    A = sum(int(w.ranks[a]) * w.modules[m][0] * 2 for a in distinct for m in mods)
+    B = sum(int(w.ranks[a]) * w.modules[m][1] * 2 for a in distinct for m in mods)
+    X = sum(w.n_rows * w.modules[st[0]][0] * 2 for st in w.stages)
+    Y = sum(w.n_rows * w.modules[m][1] * 4 for m in mods)
+    return {"W": W, "A": A, "B": B, "x": X, "y": Y, "total": W + A + B + X + Y,
+            "gemm": W + B + X + Y, "shrink": A + X, "distinct": len(distinct)}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.gpu = gpu
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------------------------
+def cpu_baseline(w, xs, Ws, factors, budget_s=10.0):
+    """The oracle as it stands, on this host's cores: whole steps (every row, every projection)
+    repeated until ~budget_s of work; returns rows/s."""
+    import oracle
+    rows = np.arange(w.n_rows)
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        for st, mods in enumerate(w.stages):
+            for m in mods:
+                oracle.workload_module(w, m, rows=rows, stage_x=xs[st], W=Ws[m], factors=factors)
+        done += w.n_rows
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{done // w.n_rows} full step(s) of the workload ({done} rows x 4 projections), fp64",
+            "seconds": round(dt, 2)}
+
+
+def make_inputs(w):
+    xs = [w.x(i) for i in range(len(w.stages))]
+    Ws = {m: w.W(m) for m in w.module_names()}
+    factors = {(int(a), m): (w.A(int(a), m), w.B(int(a), m)) for a in w.used_adapters() for m in w.module_names()}
+    return xs, Ws, factors
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    xs, Ws, factors = make_inputs(w)
+    import oracle
+    rows = np.arange(16)  # each step: a bounded 16-row sample of the batch, all four projections
+    def step():
+        for st, mods in enumerate(w.stages):
+            for m in mods:
+                oracle.workload_module(w, m, rows=rows, stage_x=xs[st], W=Ws[m], factors=factors)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    v = len(rows) * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "rows_per_step": int(len(rows)), "batch_rows": w.n_rows},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"{len(rows)} of {w.n_rows} rows per step, all four projections"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    import adapter_serving_gb300 as L
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    names = w.module_names()
+    xs, Ws, factors = make_inputs(w)
+
+    # ---- pool with the batch's adapters resident
+    adapters = w.used_adapters()
+    pages = (sum(max(8, int(w.ranks[a])) for a in adapters) + 63) // 64 + 4
+    pool = L.Pool([w.modules[m][0] for m in names], [w.modules[m][1] for m in names], w.n_adapters,
+                  max_rank=64, pages=[pages] * len(names), max_rows=w.n_rows)
+    for a in adapters:
+        for mi, m in enumerate(names):
+            A, B = factors[(int(a), m)]
+            pool.load(int(a), mi, torch.from_numpy(A).view(torch.bfloat16), torch.from_numpy(B).view(torch.bfloat16))
+    bf = lambda b: torch.from_numpy(b).view(torch.bfloat16).to(dev)
+    xd = [bf(x) for x in xs]
+    Wd = {m: bf(Ws[m]) for m in names}
+    yd = {m: torch.empty(w.n_rows, w.modules[m][1], device=dev) for m in names}
+    ids = torch.from_numpy(w.ids).to(dev)
+    ids_base = torch.full_like(ids, -1)
+    stage_io = [[(names.index(m), xd[st], Wd[m], yd[m]) for m in mods] for st, mods in enumerate(w.stages)]
+    stream = torch.cuda.current_stream()
+
+    def step(id_t):
+        for io in stage_io:
+            pool.layer_forward(io, id_t, w.scale, stream=stream)
+
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def timed(n, id_t, per_step=None):
+        """Device time of n steps, L2 flushed before each (the flush is outside the events)."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            evs[i][0].record(stream)
+            (per_step or step)(id_t)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step(ids)
+    torch.cuda.synchronize()
+    code, detail = pool.last_device_error()
+    if code:
+        raise RuntimeError(f"device error {L.DEVERR.get(code)} at {detail}")
+
+    sampler = ClockSampler(local)
+    if not args.no_clocks:
+        sampler.start()
+        time.sleep(0.3)
+    barrier()
+    total_ms = timed(args.steps, ids)
+    barrier()
+    clocks = None
+    if not args.no_clocks:
+        # keep the same load running so the 100 ms sampler sees the clocks under it
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 1.5:
+            timed(20, ids)
+        clocks = sampler.stop()
+    ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ab = algorithmic_bytes(w)
+    value = world * w.n_rows / (ms / 1e3)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "batch_rows": w.n_rows, "distinct_adapters": ab["distinct"], "rank": 8,
+                       "projections": "q 8192x8192, k 8192->1024, v 8192->1024, o 8192x8192",
+                       "calls_per_step": len(w.stages), "output": "fp32",
+                       "l2": "flushed before every timed step (256 MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "hbm_gbs": ab["total"] / (ms / 1e3) / 1e9,
+            "algorithmic_bytes_per_step": ab["total"],
+            "gpu_launches": 3 * len(w.stages) * args.steps}
+    if clocks:
+        line["clocks"] = clocks
+
+    if not args.no_extras:
+        # ---- per-kernel device time on the launch stream (library event pairs)
+        pool.profile(True)
+        timed(args.steps, ids)
+        kt = {k: pool.profile_read(k) for k in ("prep", "shrink", "gemm")}
+        pool.profile(False)
+        hbm, src = peaks()
+        g_launch, g_ms = kt["gemm"]
+        achieved = ab["gemm"] * args.steps / (g_ms / 1e3) / 1e9
+        line["roofline"] = {"kernel": "gemm_kernel (tcgen05 base + fused expand)", "bound": "hbm",
+                            "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                            "peak_source": src, "traffic": None,
+                            "algorithmic_bytes_per_step": ab["gemm"], "launches_per_step": g_launch / args.steps}
+        line["kernel_ms_per_step"] = {k: v[1] / args.steps for k, v in kt.items()}
+        s_ms = kt["shrink"][1] / args.steps
+        line["shrink_roofline"] = {"achieved": ab["shrink"] / (s_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                                   "frac": ab["shrink"] / (s_ms / 1e3) / 1e9 / hbm}
+        # ---- the base-only layer on the same W and x (every row id -1)
+        base_ms = timed(args.steps, ids_base) / args.steps
+        line["base_only_ms_per_step"] = base_ms
+        line["overhead_vs_base"] = ms / base_ms - 1
+        line["byte_ratio_adapters_vs_base"] = (ab["A"] + ab["B"]) / ab["W"]
+        # ---- end to end through the C ABI with host buffers (pinned), copies inside the timing
+        hx = [torch.from_numpy(x).view(torch.bfloat16).pin_memory() for x in xs]
+        hid = torch.from_numpy(w.ids).pin_memory()
+        hy = {m: torch.empty(w.n_rows, w.modules[m][1], dtype=torch.float32).pin_memory() for m in names}
+        h2d = sum(x.numel() * 2 for x in hx) + hid.numel() * 4
+        d2h = sum(y.numel() * 4 for y in hy.values())
+
+        def e2e_step(_):
+            for x_h, x_d in zip(hx, xd):
+                x_d.copy_(x_h, non_blocking=True)
+            ids.copy_(hid, non_blocking=True)
+            step(ids)
+            for m in names:
+                hy[m].copy_(yd[m], non_blocking=True)
+
+        barrier()
+        e_ms = timed(args.steps, None, per_step=e2e_step) / args.steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        line["e2e"] = {"value": world * w.n_rows / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+        code, detail = pool.last_device_error()
+        if code:
+            raise RuntimeError(f"device error {L.DEVERR.get(code)} at {detail}")
+        if rank == 0 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, xs, Ws, factors)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    pool.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _build():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("_lora_build", os.path.join(ROOT, "adapter_serving_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+
+
+def main():
+    args = parse()
+    if args.impl == "ours":
+        _build()
+    w = wl.attn70b_decode()
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

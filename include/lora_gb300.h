@@ -1,0 +1,243 @@
+/*
+ * lora_gb300.h -- C ABI of the GB300 (sm_103a) multi-tenant LoRA adapted linear layer.
+ *
+ * The operation.  One adapted linear layer over a batch whose rows each carry their own
+ * adapter id:
+ *
+ *     y_i = W x_i + s * B_a (A_a x_i),      a = adapter of row i,
+ *
+ * with W: [d_out, d_in], A_a: [r, d_in], B_a: [d_out, r]
+ * ("m07 -- Multi-Adapter (LoRA) Serving", section 2 "Scale Numbers", the factor shapes, and
+ * section 6 "Deep Dive A: Batching Heterogeneous Adapters", y = Wx + (B.A)x.(alpha/r) -- the
+ * scale s is passed in directly; "12. Adapter Serving and Multi-Tenant Customization",
+ * section "What an adapter adds to a forward pass").  A row whose adapter id is -1 is a
+ * base-only request and gets W x_i alone ("12. Adapter Serving ...", section "Scheduling
+ * with adapter awareness", the base-only group).  The base projection reads W once per call
+ * for the whole batch; every DISTINCT adapter's factors are read once per call ("m07",
+ * section 6, "The cost is bandwidth, not compute").  Factors are gathered inside the kernels
+ * through a device-side indirection table, so a captured CUDA graph stays valid across
+ * loads ("12. Adapter Serving ...", section "CUDA graphs": adapter addresses are read from a
+ * buffer, not baked into the graph).  Factor storage is paged ("LoRA, quotas and noisy
+ * neighbours", section "Adapter weights and KV in one pool"; "12. Adapter Serving ...",
+ * section "S-LoRA's unified paging").
+ *
+ * Conventions for every entry point:
+ *  - Return value: LORA_OK (0) or a negative LORA_E* status; nothing aborts the process and
+ *    no kernel traps.  lora_status_string() names a status.
+ *  - Tensors are dense row-major; bf16 means IEEE bfloat16 (16-bit) values.
+ *  - "device" pointers are CUDA device memory (or managed memory) of the current device;
+ *    "host or device" pointers may be either (copied with UVA).  Pointers passed to the
+ *    forward calls must be 16-byte aligned.
+ *  - Caller-owned buffers are only borrowed for the duration of the call (for asynchronous
+ *    calls: until the work queued on `stream` has run).  The pool owns its factor pages,
+ *    its table and its workspace.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls that take a
+ *    stream are asynchronous with respect to the host.  All calls on one pool must be
+ *    ordered with each other (one stream, or explicit events): the pool's workspace and
+ *    table are shared by its calls.
+ *  - Shapes: d_in and d_out must be multiples of 8; 1 <= rank <= 64.
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lora_pool lora_pool;
+typedef struct CUstream_st *lora_stream_t; /* == cudaStream_t */
+
+/* status codes */
+#define LORA_OK 0
+#define LORA_EINVAL (-1)       /* bad argument: null pointer, shape, rank, id out of range */
+#define LORA_ENOTLOADED (-2)   /* adapter (or a module of it) is not resident */
+#define LORA_ENOMEM (-3)       /* no free pages in the pool, or a device allocation failed */
+#define LORA_ECUDA (-5)        /* a CUDA runtime call failed (see lora_last_cuda_error) */
+#define LORA_EUNSUPPORTED (-6) /* valid request this build does not handle (see each call) */
+#define LORA_EDEVICE (-7)      /* a kernel recorded an error (see lora_last_device_error) */
+
+/* output element types */
+#define LORA_DTYPE_F32 0
+#define LORA_DTYPE_BF16 1
+
+#define LORA_MAX_MODULES 8     /* projections per pool and per layer call */
+#define LORA_MAX_RANK 64
+#define LORA_PAGE_ROWS 64      /* rank-vectors per page */
+#define LORA_MAX_DECODE_ROWS 256
+
+/* device-side error codes reported by lora_last_device_error */
+#define LORA_DEVERR_NONE 0
+#define LORA_DEVERR_BAD_ADAPTER 1 /* row/segment names an id outside [-1, max_adapters) */
+#define LORA_DEVERR_NOT_LOADED 2  /* row/segment names an adapter not resident for a module */
+#define LORA_DEVERR_TIMEOUT 3     /* a bounded in-kernel wait gave up (kernel returned early) */
+#define LORA_DEVERR_BAD_SEGMENTS 4 /* segment table not increasing / not covering the rows */
+
+/*
+ * Pool geometry, fixed at creation.
+ *  n_modules       number of projections (1..LORA_MAX_MODULES)
+ *  d_in, d_out     [n_modules] host arrays: projection m maps d_in[m] -> d_out[m]
+ *  max_adapters    adapter ids are 0 .. max_adapters-1
+ *  max_rank        largest rank a load may use (1..64)
+ *  pages           [n_modules] host array or NULL: number of 64-row pages reserved for
+ *                  module m.  A rank-r factor pair takes ceil-pow2(max(r, 8)) rows of one
+ *                  page (A rows d_in wide, B stored as [d_out, rows]).  NULL reserves
+ *                  enough for every adapter at max_rank.
+ *  max_rows        largest row count (decode rows or prefill tokens) one forward may pass;
+ *                  sizes the workspace.
+ */
+typedef struct {
+    int32_t n_modules;
+    const int32_t *d_in;
+    const int32_t *d_out;
+    int32_t max_adapters;
+    int32_t max_rank;
+    const int64_t *pages;
+    int32_t max_rows;
+} lora_pool_desc;
+
+/*
+ * lora_pool_create -- allocate the paged factor pool, its (pointer, rank) table and the
+ * workspace on the current CUDA device.  *out receives the pool.  Synchronous.
+ * Errors: EINVAL (bad desc), ENOMEM, ECUDA.
+ */
+int lora_pool_create(const lora_pool_desc *desc, lora_pool **out);
+
+/* lora_pool_destroy -- synchronize the device and free everything the pool owns. */
+int lora_pool_destroy(lora_pool *pool);
+
+/*
+ * lora_pool_load -- make adapter `adapter_id` resident for projection `module`.
+ *  A     host or device bf16 [rank, d_in]     (copied; caller keeps ownership)
+ *  B     host or device bf16 [d_out, rank]
+ * Pages are taken from the module's free list; the factors are copied in on `stream`
+ * (zero-padded to the storage rank) and the table entry is written on `stream` after the
+ * copy, so forwards queued later on `stream` see the adapter.  Loading an id that is
+ * already resident for this module replaces it.  Host-side bookkeeping is synchronous.
+ * Errors: EINVAL (id, module, rank, null), ENOMEM (no free rows), ECUDA.
+ */
+int lora_pool_load(lora_pool *pool, int32_t adapter_id, int32_t module, const void *A,
+                   const void *B, int32_t rank, lora_stream_t stream);
+
+/*
+ * lora_pool_unload -- release adapter `adapter_id` from every module.  The table entries
+ * are cleared on `stream`; the rows return to the free lists at once, so a later load may
+ * reuse them: order it after every forward that still reads the adapter.
+ * Errors: EINVAL, ENOTLOADED (resident in no module).
+ */
+int lora_pool_unload(lora_pool *pool, int32_t adapter_id, lora_stream_t stream);
+
+/*
+ * lora_pool_query -- host-side view of one table entry: *rank (0 if not resident) and
+ * *row_offset (first pool row of its pages).  Either output may be NULL.
+ */
+int lora_pool_query(const lora_pool *pool, int32_t adapter_id, int32_t module, int32_t *rank,
+                    int64_t *row_offset);
+
+/* lora_pool_free_rows -- free (rank-vector) rows left in module `module`'s pages. */
+int lora_pool_free_rows(const lora_pool *pool, int32_t module, int64_t *free_rows);
+
+/*
+ * lora_build_segments -- host-side row grouping: a stable sort of rows by adapter id
+ * (ascending, -1 first, ties keep row order).  ("m07", section 6: the index vector
+ * sequence -> adapter slot; "LoRA, quotas and noisy neighbours", section "One weight read,
+ * many adapters": rows tagged with their adapter and grouped.)
+ *  row_ids      host int32 [n]
+ *  perm         host int32 [n]     out: perm[p] = row at sorted position p
+ *  seg_start    host int32 [n+1]   out: group s covers sorted positions [seg_start[s], seg_start[s+1])
+ *  seg_adapter  host int32 [n]     out: adapter id of group s
+ *  n_seg        host int32         out: number of groups
+ * The same grouping is computed on the device inside lora_layer_forward.  Errors: EINVAL.
+ */
+int lora_build_segments(const int32_t *row_ids, int32_t n, int32_t *perm, int32_t *seg_start,
+                        int32_t *seg_adapter, int32_t *n_seg);
+
+/* One projection of a layer call. */
+typedef struct {
+    int32_t module;  /* pool module index */
+    const void *x;   /* device bf16 [n, d_in]; projections may share x */
+    const void *W;   /* device bf16 [d_out, d_in] */
+    void *y;         /* device [n, d_out], element type y_dtype (fp32 or bf16) */
+} lora_module_io;
+
+/*
+ * lora_layer_forward -- decode step: y = W x + s B_a A_a x for every projection in `io`,
+ * rows tagged by `row_adapter_ids` (device int32 [n], -1 = base only).  The rows are
+ * grouped by adapter on the device; every distinct adapter's factors are read once.
+ *  n_io       1..LORA_MAX_MODULES projections, each with its own W and y (x may be shared)
+ *  n          rows, 0 <= n <= min(LORA_MAX_DECODE_ROWS, max_rows); n == 0 does nothing
+ *  scale      s
+ *  y_dtype    LORA_DTYPE_F32 or LORA_DTYPE_BF16 (fp32 accumulate either way)
+ * Asynchronous on `stream`.  An id outside [-1, max_adapters) or an adapter not resident
+ * for one of the modules is recorded in the device error word (lora_last_device_error) and
+ * that row gets the base term only.  Errors: EINVAL, EUNSUPPORTED (n > 256: use
+ * lora_segment_forward with grouped rows), ECUDA.
+ */
+int lora_layer_forward(lora_pool *pool, int32_t n_io, const lora_module_io *io,
+                       const int32_t *row_adapter_ids, int32_t n, float scale, int32_t y_dtype,
+                       lora_stream_t stream);
+
+/* lora_linear_forward -- lora_layer_forward for one projection. */
+int lora_linear_forward(lora_pool *pool, int32_t module, const void *x, const void *W,
+                        const int32_t *row_adapter_ids, int32_t n, float scale, void *y,
+                        int32_t y_dtype, lora_stream_t stream);
+
+/*
+ * lora_segment_forward -- prefill / grouped rows: rows come as contiguous segments, one
+ * adapter per segment ("m07", section 6 "Prefill is different, and worse": variable-length
+ * segments; "LoRA, quotas and noisy neighbours", section "One weight read, many adapters").
+ *  seg_start    device int32 [n_seg+1], seg_start[0] = 0, non-decreasing, seg_start[n_seg] = n
+ *  seg_adapter  device int32 [n_seg], -1 = base only
+ *  n            rows (tokens), 0 <= n <= max_rows
+ * Same outputs and error reporting as lora_layer_forward; any n up to max_rows.
+ */
+int lora_segment_forward(lora_pool *pool, int32_t n_io, const lora_module_io *io,
+                         const int32_t *seg_start, const int32_t *seg_adapter, int32_t n_seg,
+                         int32_t n, float scale, int32_t y_dtype, lora_stream_t stream);
+
+/*
+ * lora_pool_last_segments -- synchronize the device and copy out the row grouping the most
+ * recent forward on this pool used (computed on the device for lora_layer_forward; the
+ * checked copy of the given table for lora_segment_forward).  Host outputs:
+ *  perm         int32 [n]      sorted position -> row (identity for grouped rows with n > 256;
+ *                              left untouched then)
+ *  seg_start    int32 [n+1], seg_adapter int32 [n], *n_seg, *n (rows of that forward).
+ * Any output pointer may be NULL.  Errors: EINVAL, ECUDA.
+ */
+int lora_pool_last_segments(lora_pool *pool, int32_t *perm, int32_t *seg_start, int32_t *seg_adapter,
+                            int32_t *n_seg, int32_t *n);
+
+/*
+ * lora_last_device_error -- synchronize the device, then read and clear the pool's device
+ * error word.  *code is a LORA_DEVERR_* value, *detail the row/segment it concerns.
+ */
+int lora_last_device_error(lora_pool *pool, int32_t *code, int32_t *detail);
+
+/*
+ * Kernel timing.  While enabled, every forward on this pool records a CUDA event pair on its
+ * stream around each kernel it launches (LORA_KERNEL_PREP: row grouping / checks,
+ * LORA_KERNEL_SHRINK: t = s A x, LORA_KERNEL_GEMM: tcgen05 base + expand).
+ * lora_profile_read synchronizes, returns the number of launches and their summed device
+ * time in milliseconds for one kind, and clears that kind.  Timing adds two event records
+ * per launch; leave it off for throughput runs.  Errors: EINVAL, ECUDA.
+ */
+#define LORA_KERNEL_PREP 0
+#define LORA_KERNEL_SHRINK 1
+#define LORA_KERNEL_GEMM 2
+int lora_profile_enable(lora_pool *pool, int32_t enable);
+int lora_profile_read(lora_pool *pool, int32_t kernel, int32_t *launches, double *total_ms);
+
+/* lora_last_cuda_error -- the last CUDA error string seen by this library (thread-local). */
+const char *lora_last_cuda_error(void);
+
+/* lora_status_string -- a constant string naming a LORA_* status. */
+const char *lora_status_string(int status);
+
+/* lora_version -- ABI version (major * 10000 + minor * 100 + patch). */
+int lora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LORA_GB300_H */
