@@ -462,15 +462,15 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
                         int y_dtype, cudaStream_t s) {
     if (!p || !io || n_io < 1 || n_io > LORA_MAX_MODULES || n < 0 || n > p->max_rows) return LORA_EINVAL;
     if (y_dtype != LORA_DTYPE_F32 && y_dtype != LORA_DTYPE_BF16) return LORA_EINVAL;
+    for (int i = 0; i < n_io; ++i)
+        if (io[i].module < 0 || io[i].module >= p->n_modules) return LORA_EINVAL;
+    if (n == 0) return LORA_OK;  // empty batch: nothing to read or write
     for (int i = 0; i < n_io; ++i) {
         const lora_module_io &m = io[i];
         if (m.module < 0 || m.module >= p->n_modules || !m.x || !m.W || !m.y) return LORA_EINVAL;
         if (!aligned16(m.x) || !aligned16(m.W) || !aligned16(m.y)) return LORA_EINVAL;
     }
-    if (ids == nullptr && (!seg_start || !seg_adapter || n_seg < 1 || n_seg > n + 1)) {
-        if (!(n == 0 && seg_start && seg_adapter)) return LORA_EINVAL;
-    }
-    if (n == 0) return LORA_OK;
+    if (ids == nullptr && (!seg_start || !seg_adapter || n_seg < 1 || n_seg > n)) return LORA_EINVAL;
     const bool decode = n <= LORA_MAX_DECODE_ROWS;
     if (ids && !decode) return LORA_EUNSUPPORTED;
     cudaError_t e;
@@ -513,7 +513,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     sp.n_seg = p->n_seg;
     sp.partials = p->shrink_part;
     sp.counters = p->shrink_cnt;
-    const int kc_dec = rpmax <= 8 ? 2048 : rpmax <= 16 ? 1024 : 512;
+    const int kc_dec = kShrinkDecKC;
     int splits = 0;
     for (int i = 0; i < n_io; ++i) {
         const ModuleStore &ms = p->mod[io[i].module];
@@ -575,8 +575,10 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     } else {
         gp.n_cta = std::min(p->num_sms, tiles);
     }
+    // TMEM: n_acc accumulator buffers of nt columns, then nt columns for the expand delta
+    gp.n_acc = 3 * gp.nt <= 512 ? 2 : 1;
     gp.tmem_cols = 32;
-    while (gp.tmem_cols < 2 * gp.nt) gp.tmem_cols <<= 1;
+    while (gp.tmem_cols < (gp.n_acc + 1) * gp.nt) gp.tmem_cols <<= 1;
     gp.slot_bytes = (kBM * rpmax * 2 + gp.unit_rows * rpmax * 4 + 127) & ~127;
     const int ring_target = rpmax <= 16 ? 48 * 1024 : 72 * 1024;
     gp.n_slots = std::max(2, std::min(kMaxSlots, ring_target / gp.slot_bytes));
@@ -604,6 +606,7 @@ extern "C" {
 int lora_layer_forward(lora_pool *p, int32_t n_io, const lora_module_io *io, const int32_t *ids, int32_t n,
                        float scale, int32_t y_dtype, lora_stream_t stream) {
     if (!ids && n > 0) return LORA_EINVAL;
+    if (n == 0) return forward_impl(p, n_io, io, nullptr, nullptr, nullptr, 0, 0, scale, y_dtype, nullptr);
     if (n > LORA_MAX_DECODE_ROWS) return LORA_EUNSUPPORTED;
     return forward_impl(p, n_io, io, ids, nullptr, nullptr, 0, n, scale, y_dtype,
                         reinterpret_cast<cudaStream_t>(stream));
@@ -618,6 +621,7 @@ int lora_linear_forward(lora_pool *p, int32_t module, const void *x, const void 
 int lora_segment_forward(lora_pool *p, int32_t n_io, const lora_module_io *io, const int32_t *seg_start,
                          const int32_t *seg_adapter, int32_t n_seg, int32_t n, float scale, int32_t y_dtype,
                          lora_stream_t stream) {
+    if (n == 0) return forward_impl(p, n_io, io, nullptr, nullptr, nullptr, 0, 0, scale, y_dtype, nullptr);
     if (!seg_start || !seg_adapter) return LORA_EINVAL;
     return forward_impl(p, n_io, io, nullptr, seg_start, seg_adapter, n_seg, n, scale, y_dtype,
                         reinterpret_cast<cudaStream_t>(stream));

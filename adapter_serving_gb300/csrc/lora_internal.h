@@ -24,11 +24,15 @@ constexpr int kBK = 64;        // K per pipeline stage (one 128-byte swizzle row
 constexpr int kEpiWarps = 4;   // epilogue warps (one per TMEM lane quarter)
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxSlots = 32;
+constexpr int kMaxWin = 256;        // segments one tile's expand can touch (= max rows per tile)
 constexpr int kMaxStages = 8;
 constexpr int kShrinkThreads = 256;
 constexpr int kShrinkRows = 8;      // rows per register block in the shrink
 constexpr int kShrinkKSub = 1024;   // K elements staged in shared memory per step
 constexpr int kShrinkGroupRows = 64;  // rows per shrink block on the grouped (prefill) path
+constexpr int kShrinkDecCh = 8;       // decode shrink: 16-byte chunks of A per lane and pass
+constexpr int kShrinkDecKC = 256 * kShrinkDecCh;  // decode shrink: K per block (split width)
+constexpr int kShrinkDecRows = 4;     // decode shrink: rows sharing one register load of A
 
 struct GemmModule {
     CUtensorMap tmW;  // W [d_out, d_in]: box {64, 128}, 128B swizzle
@@ -62,6 +66,7 @@ struct GemmParams {
     int32_t slot_bytes;
     int32_t raster_group;  // W tiles per raster group (round robin)
     int32_t tmem_cols;
+    int32_t n_acc;         // accumulator buffers in TMEM (2 when 3 * nt <= 512, else 1)
     const int32_t *perm;
     const int32_t *seg_start;
     const int32_t *seg_adapter;

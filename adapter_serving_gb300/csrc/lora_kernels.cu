@@ -304,6 +304,96 @@ __global__ void __launch_bounds__(kShrinkThreads) shrink_kernel(const __grid_con
     if (tid == 0) p.counters[m * p.max_units + u] = 0;
 }
 
+// Decode shrink: one block per (segment, 2048-wide K split, module).  Each warp takes one rank
+// row per pass and every lane issues its eight 16-byte loads of A up front (32 KiB of A in
+// flight per block and pass), then reads the segment's x rows straight from L2.  Partial sums
+// of the splits are combined by the last block of the segment, in split order.
+__global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const __grid_constant__ ShrinkParams p) {
+    __shared__ int s_last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int m = 0;
+    while (m + 1 < p.n_mod && p.split_begin[m + 1] <= (int)blockIdx.y) ++m;
+    const int kc = blockIdx.y - p.split_begin[m];
+    const int ks = p.ksplit[m];
+    if (kc >= ks) return;
+    const int u = blockIdx.x;
+    if (u >= *p.n_seg) return;
+    const int qlo = p.seg_start[u], qhi = p.seg_start[u + 1];
+    const int a = p.seg_adapter[u];
+    const int d_in = p.d_in[m];
+    const int kbeg = kc * p.kc[m];
+    const int kend = min(d_in, kbeg + p.kc[m]);
+    const uint16_t *x = p.x[m];
+    const int rpmax = p.rpmax;
+    int r = 0, rp = 0;
+    const uint16_t *A = nullptr;
+    if (a >= 0) {
+        const PoolEntry *e = p.table[m] + a;
+        r = e->rank;
+        rp = e->rp;
+        A = e->A;
+    }
+    for (int j0 = 0; j0 < r; j0 += kShrinkThreads / 32) {
+        const int j = j0 + warp;
+        if (j >= r) break;  // warp-uniform
+        uint4 av[kShrinkDecCh];
+#pragma unroll
+        for (int c = 0; c < kShrinkDecCh; ++c) {
+            const int kk = kbeg + lane * 8 + 256 * c;
+            av[c] = kk < kend ? __ldg(reinterpret_cast<const uint4 *>(A + (size_t)j * d_in + kk)) : make_uint4(0, 0, 0, 0);
+        }
+        for (int qb = qlo; qb < qhi; qb += kShrinkDecRows) {
+            float acc[kShrinkDecRows];
+#pragma unroll
+            for (int rr = 0; rr < kShrinkDecRows; ++rr) {
+                acc[rr] = 0.f;
+                if (qb + rr < qhi) {
+                    const uint16_t *xr = x + (size_t)p.perm[qb + rr] * d_in;
+                    uint4 xv[kShrinkDecCh];
+#pragma unroll
+                    for (int c = 0; c < kShrinkDecCh; ++c) {
+                        const int kk = kbeg + lane * 8 + 256 * c;
+                        xv[c] = kk < kend ? __ldg(reinterpret_cast<const uint4 *>(xr + kk)) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int c = 0; c < kShrinkDecCh; ++c) acc[rr] += dot8_bf16(av[c], xv[c]);
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < kShrinkDecRows; ++rr) {
+                if (qb + rr < qhi) {
+                    const float v = warp_sum(acc[rr]);
+                    if (lane == 0) {
+                        if (ks == 1)
+                            p.T[m][(size_t)(qb + rr) * rpmax + j] = p.scale * v;
+                        else
+                            p.partials[(((size_t)m * p.ks_max + kc) * p.n + (qb + rr)) * rpmax + j] = v;
+                    }
+                }
+            }
+        }
+    }
+    if (ks == 1) {
+        for (int idx = tid; idx < (qhi - qlo) * (rp - r); idx += kShrinkThreads)
+            p.T[m][(size_t)(qlo + idx / (rp - r)) * rpmax + r + idx % (rp - r)] = 0.f;
+        return;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(p.counters + m * p.max_units + u, 1) == ks - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int idx = tid; idx < (qhi - qlo) * rp; idx += kShrinkThreads) {
+        const int q = qlo + idx / rp, j = idx % rp;
+        float v = 0.f;
+        if (j < r)
+            for (int c = 0; c < ks; ++c) v += __ldcg(p.partials + (((size_t)m * p.ks_max + c) * p.n + q) * rpmax + j);
+        p.T[m][(size_t)q * rpmax + j] = p.scale * v;
+    }
+    if (tid == 0) p.counters[m * p.max_units + u] = 0;
+}
+
 // ============================================================================ gemm ==========
 
 struct Item {
@@ -372,26 +462,36 @@ __device__ __forceinline__ int cta_of(const GemmParams &p, int64_t x) {
     return (int)(((x + 1) * p.n_cta - 1) / p.total_iters);
 }
 
-struct Unit {
-    int32_t a, qa, qe;
+// Expand metadata staged in shared memory by the epilogue warps (no global-latency chains in
+// the per-unit loop): the row order (decode) and, for the segments the current tile touches,
+// their first position, B factor address and storage rank.
+struct EpiMeta {
+    uint64_t wB[kMaxWin];      // B factor base of the window's segments (0 = base only)
+    int32_t perm[kMaxWin];     // decode: sorted position -> row
+    int32_t wss[kMaxWin + 4];  // window segment starts (clipped to the tile), wss[count] = qhi
+    int32_t wrp[kMaxWin];      // storage rank (0 = base only)
+    int32_t count;             // segments in the window
+    int32_t module;            // module the window was built for (decode caching)
+    int32_t qlo, qhi;
 };
 
-// Walks the expand units of one tile: runs of at most unit_rows sorted positions that share
-// a segment (one adapter), restricted to the tile's positions [q, qhi).
+struct Unit {
+    int32_t k, qa, qe;  // window segment, positions [qa, qe)
+};
+
+// Expand units of one tile: runs of at most unit_rows positions inside one window segment.
 struct UnitCursor {
-    int32_t s, q, qhi, n_seg;
-    __device__ void begin(const GemmParams &p, int qlo, int qhi_, int n_seg_) {
-        q = qlo;
-        qhi = qhi_;
-        n_seg = n_seg_;
-        s = p.decode ? 0 : seg_of(p.seg_start, n_seg_, qlo);
+    int32_t k, q;
+    __device__ void begin(const EpiMeta &w) {
+        k = 0;
+        q = w.qlo;
     }
-    __device__ bool next(const GemmParams &p, Unit &u) {
-        if (q >= qhi) return false;
-        while (s + 1 < n_seg && __ldg(p.seg_start + s + 1) <= q) ++s;
-        int qe = min(min(__ldg(p.seg_start + s + 1), qhi), q + p.unit_rows);
+    __device__ bool next(const GemmParams &p, const EpiMeta &w, Unit &u) {
+        if (q >= w.qhi) return false;
+        while (k + 1 < w.count && w.wss[k + 1] <= q) ++k;
+        int qe = min(min(w.wss[k + 1], w.qhi), q + p.unit_rows);
         if (qe <= q) qe = q + 1;  // inconsistent table: still make progress, stay in bounds
-        u.a = __ldg(p.seg_adapter + s);
+        u.k = k;
         u.qa = q;
         u.qe = qe;
         q = qe;
@@ -403,16 +503,61 @@ struct EpiCtx {
     const GemmParams *p;
     uint8_t *ring;
     uint64_t *slot_bar;
+    EpiMeta *meta;
     uint32_t tmem_base;
-    int etid;       // 0..127 among epilogue threads
-    int o;          // TMEM lane = W row within the tile
-    int lane_base;  // first TMEM lane of this warp
+    uint32_t delta_col;  // first TMEM column of the expand (delta) region
+    int etid;            // 0..127 among epilogue threads
+    int o;               // TMEM lane = W row within the tile
+    int lane_base;       // first TMEM lane of this warp
     int lane;
-    uint32_t g_unit;  // expand units processed by this CTA so far (ring slot / parity)
+    uint32_t g_unit;     // expand units processed by this CTA so far (ring slot / parity)
 };
 
-__device__ __forceinline__ const PoolEntry *entry_of(const GemmParams &p, int m, int a) {
-    return p.mod[m].table + a;
+// (Re)build the segment window for a tile: every segment overlapping its positions
+// [qlo, qhi), with the factor addresses of module m.  Decode tiles of one module share the
+// window, so it is rebuilt only when the module changes.
+__device__ void build_window(EpiCtx &c, const Item &it) {
+    const GemmParams &p = *c.p;
+    EpiMeta &w = *c.meta;
+    const int row0 = it.chunk * p.nt;
+    if (p.decode && w.module == it.m) return;
+    named_bar_sync(1, 128);  // nobody still reads the old window
+    const int n_seg = *p.n_seg;
+    int s0, cnt, qlo, qhi;
+    if (p.decode) {
+        qlo = 0;
+        qhi = p.n;
+        s0 = 0;
+        cnt = min(n_seg, kMaxWin);
+    } else {
+        qlo = row0;
+        qhi = min(p.n, row0 + p.nt);
+        s0 = seg_of(p.seg_start, n_seg, qlo);
+        const int s1 = seg_of(p.seg_start, n_seg, qhi - 1);
+        cnt = min(s1 - s0 + 1, kMaxWin);
+    }
+    const PoolEntry *table = p.mod[it.m].table;
+    for (int i = c.etid; i < cnt; i += 128) {
+        const int s = s0 + i;
+        const int a = __ldg(p.seg_adapter + s);
+        w.wss[i] = max(__ldg(p.seg_start + s), qlo);
+        uint64_t b = 0;
+        int rp = 0;
+        if (a >= 0) {
+            b = reinterpret_cast<uint64_t>(table[a].B);
+            rp = table[a].rp;
+        }
+        w.wB[i] = b;
+        w.wrp[i] = rp;
+    }
+    if (c.etid == 0) {
+        w.wss[cnt] = qhi;
+        w.count = cnt;
+        w.qlo = qlo;
+        w.qhi = qhi;
+        w.module = it.m;
+    }
+    named_bar_sync(1, 128);
 }
 
 // Stage one expand unit into a ring slot: the adapter's B rows [o0, o0 + 128) (cp.async,
@@ -422,50 +567,46 @@ __device__ __forceinline__ const PoolEntry *entry_of(const GemmParams &p, int m,
 __device__ void issue_unit(EpiCtx &c, const Item &it, const Unit &u, int slot) {
     const GemmParams &p = *c.p;
     const GemmModule &M = p.mod[it.m];
-    uint8_t *sb = c.ring + (size_t)slot * p.slot_bytes;
-    if (u.a >= 0) {
-        const PoolEntry *e = entry_of(p, it.m, u.a);
-        const int rp = e->rp;
-        const uint16_t *B = e->B;
-        if (rp > 0) {
-            const int lg = __ffs(rp >> 3) - 1;  // log2(rp / 8)
-            const int nch = 1 << lg;
-            const int sh = 3 - lg;
-            const int o0 = it.w_tile * kBM;
-            const uint32_t sbase = smem_u32(sb);
-            for (int idx = c.etid; idx < (kBM << lg); idx += 128) {
-                const int row = idx >> lg, ch = idx & (nch - 1);
-                const int o = o0 + row;
-                const bool v = o < M.d_out;
-                const uint16_t *src = v ? B + (size_t)o * rp + ch * 8 : B;
-                cp_async_16(sbase + (uint32_t)(((row << lg) + (ch ^ ((row >> sh) & (nch - 1)))) * 16), src,
-                            v ? 16u : 0u);
-            }
-            const int tch = rp >> 2;
-            const int rows = u.qe - u.qa;
-            const float *Tsrc = M.T + (size_t)u.qa * p.rpmax;
-            const uint32_t tbase = sbase + (uint32_t)(kBM * p.rpmax * 2);
-            for (int idx = c.etid; idx < rows * tch; idx += 128) {
-                const int r = idx / tch, ch = idx - r * tch;
-                cp_async_16(tbase + (uint32_t)((r * rp + ch * 4) * 4), Tsrc + (size_t)r * p.rpmax + ch * 4, 16u);
-            }
+    const EpiMeta &w = *c.meta;
+    const int rp = w.wrp[u.k];
+    if (rp > 0) {
+        const uint16_t *B = reinterpret_cast<const uint16_t *>(w.wB[u.k]);
+        const uint32_t sbase = smem_u32(c.ring + (size_t)slot * p.slot_bytes);
+        const int lg = __ffs(rp >> 3) - 1;  // log2(rp / 8)
+        const int nch = 1 << lg;
+        const int sh = 3 - lg;
+        const int o0 = it.w_tile * kBM;
+        for (int idx = c.etid; idx < (kBM << lg); idx += 128) {
+            const int row = idx >> lg, ch = idx & (nch - 1);
+            const int o = o0 + row;
+            const bool v = o < M.d_out;
+            const uint16_t *src = v ? B + (size_t)o * rp + ch * 8 : B;
+            cp_async_16(sbase + (uint32_t)(((row << lg) + (ch ^ ((row >> sh) & (nch - 1)))) * 16), src,
+                        v ? 16u : 0u);
+        }
+        const int tch = rp >> 2;
+        const int rows = u.qe - u.qa;
+        const float *Tsrc = M.T + (size_t)u.qa * p.rpmax;
+        const uint32_t tbase = sbase + (uint32_t)(kBM * p.rpmax * 2);
+        for (int idx = c.etid; idx < rows * tch; idx += 128) {
+            const int r = idx / tch, ch = idx - r * tch;
+            cp_async_16(tbase + (uint32_t)((r * rp + ch * 4) * 4), Tsrc + (size_t)r * p.rpmax + ch * 4, 16u);
         }
     }
     cp_async_arrive_noinc(c.slot_bar + slot);
 }
 
 template <int RP>
-__device__ __forceinline__ void apply_unit(EpiCtx &c, const Item &it, const Unit &u, const uint8_t *sb,
-                                           uint32_t tcol0, int row0) {
+__device__ __forceinline__ void apply_unit(EpiCtx &c, const Unit &u, const uint8_t *sb, uint32_t tcol0, int row0) {
     constexpr int LG = (RP == 8) ? 0 : (RP == 16) ? 1 : (RP == 32) ? 2 : 3;
     constexpr int NCH = 1 << LG;
     constexpr int SH = 3 - LG;
     const GemmParams &p = *c.p;
+    const EpiMeta &w = *c.meta;
     uint32_t b[RP / 2];
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(
-            sb + ((c.o << LG) + (ch ^ ((c.o >> SH) & (NCH - 1)))) * 16);
+        const uint4 v = *reinterpret_cast<const uint4 *>(sb + ((c.o << LG) + (ch ^ ((c.o >> SH) & (NCH - 1)))) * 16);
         b[4 * ch + 0] = v.x;
         b[4 * ch + 1] = v.y;
         b[4 * ch + 2] = v.z;
@@ -483,50 +624,47 @@ __device__ __forceinline__ void apply_unit(EpiCtx &c, const Item &it, const Unit
             acc = fmaf(bf16lo(b[2 * j4 + 1]), tv.z, acc);
             acc = fmaf(bf16hi(b[2 * j4 + 1]), tv.w, acc);
         }
-        const int col = p.decode ? __ldg(p.perm + q) : q - row0;
+        const int col = p.decode ? w.perm[q] : q - row0;
         tmem_st1(tcol0 + (uint32_t)col, acc);
     }
 }
 
-// Expand for a tile this CTA heads: D[o, col(q)] = sum_j B_a[o0 + o, j] * t_q[j] for every
-// position q of the tile (0 for base-only rows).  Runs while the MMA warp is still busy with
-// the previous tile; the MMAs of this tile then accumulate the base term on top.
-__device__ bool init_expand(EpiCtx &c, const Item &it, int buf, volatile int *abort_flag) {
+// Expand for a tile this CTA heads: delta[o, col(q)] = sum_j B_a[o0 + o, j] * t_q[j] for every
+// position q of the tile (0 for base-only rows), written into the TMEM delta region.  It runs
+// while the MMA warp works on the same tile; the drain adds it to the accumulator.
+__device__ bool init_expand(EpiCtx &c, const Item &it, volatile int *abort_flag) {
     const GemmParams &p = *c.p;
+    build_window(c, it);
+    const EpiMeta &w = *c.meta;
     const int row0 = it.chunk * p.nt;
-    const int qlo = p.decode ? 0 : row0;
-    const int qhi = p.decode ? p.n : min(p.n, row0 + p.nt);
-    const int n_seg = *p.n_seg;
-    const uint32_t tcol0 = c.tmem_base + ((uint32_t)c.lane_base << 16) + (uint32_t)(buf * p.nt);
+    const uint32_t tcol0 = c.tmem_base + ((uint32_t)c.lane_base << 16) + c.delta_col;
     UnitCursor ic, cc;
-    ic.begin(p, qlo, qhi, n_seg);
-    cc.begin(p, qlo, qhi, n_seg);
+    ic.begin(w);
+    cc.begin(w);
     const uint32_t base = c.g_unit;
     uint32_t issued = 0, consumed = 0;
     Unit u;
-    while (issued < (uint32_t)p.n_slots && ic.next(p, u)) {
+    while (issued < (uint32_t)p.n_slots && ic.next(p, w, u)) {
         issue_unit(c, it, u, (base + issued) % p.n_slots);
         ++issued;
     }
     bool ok = true;
-    while (cc.next(p, u)) {
+    while (cc.next(p, w, u)) {
         const uint32_t k = base + consumed;
         const int slot = k % p.n_slots;
         const bool landed = mbar_wait(c.slot_bar + slot, (k / p.n_slots) & 1, abort_flag, p.err);
         {
-            // runs even if the wait gave up (the warp-wide TMEM stores need every lane);
-            // the values are then meaningless but every access stays in bounds
+            // runs even if the wait gave up (the warp-wide TMEM stores need every lane); the
+            // values are then meaningless but every access stays in bounds
             const uint8_t *sb = c.ring + (size_t)slot * p.slot_bytes;
-            int rp = 0;
-            if (u.a >= 0) rp = entry_of(p, it.m, u.a)->rp;
-            switch (rp) {
-                case 8: apply_unit<8>(c, it, u, sb, tcol0, row0); break;
-                case 16: apply_unit<16>(c, it, u, sb, tcol0, row0); break;
-                case 32: apply_unit<32>(c, it, u, sb, tcol0, row0); break;
-                case 64: apply_unit<64>(c, it, u, sb, tcol0, row0); break;
+            switch (w.wrp[u.k]) {
+                case 8: apply_unit<8>(c, u, sb, tcol0, row0); break;
+                case 16: apply_unit<16>(c, u, sb, tcol0, row0); break;
+                case 32: apply_unit<32>(c, u, sb, tcol0, row0); break;
+                case 64: apply_unit<64>(c, u, sb, tcol0, row0); break;
                 default:
                     for (int q = u.qa; q < u.qe; ++q) {
-                        const int col = p.decode ? __ldg(p.perm + q) : q - row0;
+                        const int col = p.decode ? w.perm[q] : q - row0;
                         tmem_st1(tcol0 + (uint32_t)col, 0.f);
                     }
             }
@@ -538,7 +676,7 @@ __device__ bool init_expand(EpiCtx &c, const Item &it, int buf, volatile int *ab
             ok = false;
             break;
         }
-        if (ic.next(p, u)) {
+        if (ic.next(p, w, u)) {
             issue_unit(c, it, u, (base + issued) % p.n_slots);
             ++issued;
         }
@@ -570,6 +708,17 @@ __device__ __forceinline__ void ld_cols16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// This CTA's share of a tile: accumulator (+ the expand delta when it heads the tile).
+__device__ __forceinline__ void own_cols16(const EpiCtx &c, uint32_t tacc, bool head, int c0, float (&v)[16]) {
+    ld_cols16(tacc + c0, v);
+    if (head) {
+        float d[16];
+        ld_cols16(c.tmem_base + ((uint32_t)c.lane_base << 16) + c.delta_col + c0, d);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] += d[i];
+    }
+}
+
 // Accumulator -> y.  A tile split over several CTAs (stream-K) is finished by the last CTA
 // to get there (atomic counter); it adds the pieces in k order, so the sum never depends on
 // timing.  No CTA ever waits for another.
@@ -581,13 +730,14 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
     const int ncols16 = (ncols + 15) & ~15;
     const int oo = it.w_tile * kBM + c.o;
     const bool o_ok = oo < M.d_out;
-    const uint32_t tcol0 = c.tmem_base + ((uint32_t)c.lane_base << 16) + (uint32_t)(buf * p.nt);
+    const bool head = it.kb0 == 0;
+    const uint32_t tacc = c.tmem_base + ((uint32_t)c.lane_base << 16) + (uint32_t)(buf * p.nt);
     const size_t slot_elems = (size_t)kBM * p.nt;
 
-    if (it.kb0 == 0 && it.kb1 == it.kbn) {
+    if (head && it.kb1 == it.kbn) {
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
-            ld_cols16(tcol0 + c0, v);
+            own_cols16(c, tacc, true, c0, v);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int col = c0 + i;
@@ -603,7 +753,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
     const int nc = c_last - c_first + 1;
     int32_t *counter = p.tile_counters + it.tile;
     bool finalize = false;
-    if (it.kb0 == 0) {  // the head usually arrives last: finish directly if everyone else is in
+    if (head) {  // the head usually arrives last: finish directly if everyone else is in
         if (c.etid == 0) *misc_flag = (atomicAdd(counter, 0) == nc - 1);
         named_bar_sync(1, 128);
         finalize = *misc_flag != 0;
@@ -615,7 +765,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
         float *dst = p.partials + ((size_t)blockIdx.x * 2 + my_slot) * slot_elems;
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
-            ld_cols16(tcol0 + c0, v);
+            own_cols16(c, tacc, head, c0, v);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 if (c0 + i < ncols) dst[(size_t)(c0 + i) * kBM + c.o] = v[i];
@@ -631,7 +781,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
     __threadfence();
     for (int c0 = 0; c0 < ncols16; c0 += 16) {
         float own[16], sum[16];
-        ld_cols16(tcol0 + c0, own);
+        own_cols16(c, tacc, head, c0, own);
         for (int jc = 0; jc < nc; ++jc) {
             const int cc = c_first + jc;
             float v[16];
@@ -662,15 +812,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.n_stages;
+    const int NB = p.n_acc;
     const uint32_t a_bytes = kBM * kBK * 2;
     const uint32_t b_bytes = (uint32_t)p.nt * kBK * 2;
     const uint32_t stage_bytes = a_bytes + b_bytes;
     uint8_t *ring = smem + (size_t)S * stage_bytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.n_slots * p.slot_bytes);
+    EpiMeta *meta = reinterpret_cast<EpiMeta *>(ring + (size_t)p.n_slots * p.slot_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(meta + 1);
     uint64_t *empty = full + S;
     uint64_t *acc_full = empty + S;
-    uint64_t *acc_ready = acc_full + 2;
-    uint64_t *mma_done = acc_ready + 2;
+    uint64_t *acc_free = acc_full + 2;
+    uint64_t *mma_done = acc_free + 2;
     uint64_t *slot_bar = mma_done + 1;
     uint32_t *misc = reinterpret_cast<uint32_t *>(slot_bar + p.n_slots);  // [0] tmem, [1] abort, [2] flag
 
@@ -682,12 +834,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
-            mbar_init(acc_ready + b, kEpiWarps);
+            mbar_init(acc_free + b, kEpiWarps);
         }
         mbar_init(mma_done, 1);
         for (int s = 0; s < p.n_slots; ++s) mbar_init(slot_bar + s, 128);
         misc[1] = 0;
         misc[2] = 0;
+        meta->module = -1;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -746,11 +899,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             uint32_t k = 0, li = 0;
             bool ok = true;
             while (ok && sc.next(p, it)) {
-                const int buf = li & 1;
-                if (!mbar_wait(acc_ready + buf, (li >> 1) & 1, abort_flag, p.err)) break;
+                const int buf = li % NB;
+                const uint32_t use = li / NB;
+                if (!mbar_wait(acc_free + buf, (use & 1) ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * p.nt);
-                const bool head = it.kb0 == 0;  // the accumulator holds the expand already
                 for (int kb = it.kb0; kb < it.kb1; ++kb, ++k) {
                     const int s = k % S;
                     if (!mbar_wait(full + s, (k / S) & 1, abort_flag, p.err)) {
@@ -763,7 +916,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint32_t accum = (head || kb > it.kb0 || kk > 0) ? 1u : 0u;
+                        const uint32_t accum = (kb > it.kb0 || kk > 0) ? 1u : 0u;
                         umma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, accum);
                     }
                     umma_commit(empty + s);
@@ -784,43 +937,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         c.p = &p;
         c.ring = ring;
         c.slot_bar = slot_bar;
+        c.meta = meta;
         c.tmem_base = tmem_base;
+        c.delta_col = (uint32_t)(NB * p.nt);
         c.etid = threadIdx.x - 64;
         c.lane = lane;
         c.lane_base = (warp & 3) * 32;
         c.o = c.lane_base + lane;
         c.g_unit = 0;
+        if (p.decode)
+            for (int i = c.etid; i < p.n; i += 128) meta->perm[i] = __ldg(p.perm + i);
         volatile int *flag = reinterpret_cast<volatile int *>(misc + 2);
         Sched sc;
         sc.begin(p, blockIdx.x);
-        Item cur, nxt;
-        bool has_cur = sc.next(p, cur);
+        Item it;
         uint32_t li = 0;
-        bool ok = true;
-        auto prepare = [&](const Item &it, uint32_t idx) {
-            const int buf = idx & 1;
-            if (it.kb0 == 0) ok = init_expand(c, it, buf, abort_flag) && ok;
+        while (sc.next(p, it)) {
+            const int buf = li % NB;
+            bool ok = true;
+            if (it.kb0 == 0) ok = init_expand(c, it, abort_flag);
+            const bool full_ok = mbar_wait(acc_full + buf, (li / NB) & 1, abort_flag, p.err);
+            if (named_bar_or(1, 128, !(full_ok && ok))) break;
+            tc_fence_after();
+            drain(c, it, buf, flag);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_ready + buf);
-        };
-        if (has_cur) prepare(cur, 0);
-        while (has_cur && ok) {
-            const bool has_nxt = sc.next(p, nxt);
-            if (has_nxt) prepare(nxt, li + 1);
-            const int buf = li & 1;
-            const bool full_ok = mbar_wait(acc_full + buf, (li >> 1) & 1, abort_flag, p.err);
-            if (named_bar_or(1, 128, !full_ok)) break;
-            tc_fence_after();
-            drain(c, cur, buf, flag);
-            cur = nxt;
-            has_cur = has_nxt;
+            if (lane == 0) mbar_arrive(acc_free + buf);
             ++li;
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
     }
@@ -830,7 +979,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
 size_t gemm_smem_bytes(int nt, int n_stages, int n_slots, int slot_bytes) {
     const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2;
-    return 1024 + stage * n_stages + (size_t)n_slots * slot_bytes +
+    return 1024 + stage * n_stages + (size_t)n_slots * slot_bytes + sizeof(EpiMeta) +
            8 * (2 * (size_t)n_stages + 5 + n_slots) + 16;
 }
 
@@ -845,7 +994,10 @@ cudaError_t launch_prep_segments(const PrepParams &p, cudaStream_t s) {
 }
 
 cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStream_t s) {
-    shrink_kernel<<<dim3(grid_x, grid_y), kShrinkThreads, 0, s>>>(p);
+    if (p.by_segment)
+        shrink_decode_kernel<<<dim3(grid_x, grid_y), kShrinkThreads, 0, s>>>(p);
+    else
+        shrink_kernel<<<dim3(grid_x, grid_y), kShrinkThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
