@@ -63,6 +63,8 @@ _sig("lora_layer_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io
 _sig("lora_linear_forward", ctypes.c_int, _P, _I32, _P, _P, _P, _I32, _F, _P, _I32, _P)
 _sig("lora_segment_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _P, _I32, _I32, _F,
      _I32, _P)
+_sig("lora_linear_forward_static", ctypes.c_int, _P, _P, _I32, _I32, _P, _I32, _P, _P, _I32, _I32, _F, _P, _I32,
+     _P)
 _sig("lora_pool_last_segments", ctypes.c_int, _P, _P, _P, _P, ctypes.POINTER(_I32), ctypes.POINTER(_I32))
 _sig("lora_last_device_error", ctypes.c_int, _P, ctypes.POINTER(_I32), ctypes.POINTER(_I32))
 _sig("lora_profile_enable", ctypes.c_int, _P, _I32)

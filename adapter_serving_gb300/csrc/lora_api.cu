@@ -173,6 +173,8 @@ static int dev_alloc(lora_pool *p, void **ptr, size_t bytes) {
     return LORA_OK;
 }
 
+void lora::set_last_error(const char *why) { g_last_cuda_error = why; }
+
 extern "C" {
 
 int lora_version(void) { return 10000; }

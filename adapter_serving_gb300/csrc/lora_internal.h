@@ -1,6 +1,7 @@
 // lora_internal.h -- structures shared by the host side (pool, API) and the kernels.
 #pragma once
 #include <cstdint>
+#include <string>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -122,5 +123,9 @@ cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStr
 cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s);
 size_t gemm_smem_bytes(int nt, int n_stages, int n_slots, int slot_bytes);
+
+// lora_api.cu: sets the string lora_last_cuda_error() returns on this thread
+void set_last_error(const char *why);
+inline void set_last_error(const std::string &why) { set_last_error(why.c_str()); }
 
 }  // namespace lora

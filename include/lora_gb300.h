@@ -197,6 +197,39 @@ int lora_segment_forward(lora_pool *pool, int32_t n_io, const lora_module_io *io
                          int32_t n, float scale, int32_t y_dtype, lora_stream_t stream);
 
 /*
+ * lora_linear_forward_static -- lora_linear_forward for callers that must not allocate device
+ * memory.  The pages have no counterpart to this call.
+ *
+ * Who needs it: a caller that cannot call cudaMalloc -- a serving runtime that has already
+ * handed all of HBM to its own allocator (KV cache, its own fixed LoRA buffers), where an extra
+ * allocation would fail or break its accounting, or code embedded in a framework that forbids
+ * raw device allocations.  Such a caller cannot create a lora_pool either, so it passes its
+ * adapters as stacked buffers it already owns.  Every per-call scratch buffer (row grouping,
+ * shrink result and partial sums, stream-K partial tiles, counters, the factor table) lives in
+ * one file-scope device array of this library, at most 24 MiB, which every GPU that loads the
+ * library keeps until the process exits.  Nothing is allocated by this call.
+ *
+ *  x, W, y        as lora_linear_forward (device, 16-byte aligned); d_in, d_out multiples of 8
+ *  row_adapter_ids device int32 [n]; -1 = base only; an id outside [-1, n_adapters) is served
+ *                 base only (this call has no device error report)
+ *  A_stack        device bf16 [n_adapters, rank, d_in]   (adapter a's A at offset a*rank*d_in)
+ *  B_stack        device bf16 [n_adapters, d_out, rank]  (adapter a's B at offset a*d_out*rank)
+ *  rank           8, 16, 32 or 64, the same for every adapter (zero-pad smaller ranks)
+ * Limits of the scratch: n <= 128, d_in <= 16384, d_out <= 32768, n_adapters <= 4096; larger
+ * requests return LORA_EUNSUPPORTED, bad arguments LORA_EINVAL, and lora_last_cuda_error()
+ * then names the reason.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) for that device, so make that first call before any stream capture.
+ * All calls share the one array and it keeps the previous call's contents (the counters in it
+ * are cleared by every call): calls that can overlap on the GPU -- on different streams, or
+ * from several host threads -- race and corrupt each other's results; order them.
+ * Asynchronous on `stream`.
+ */
+int lora_linear_forward_static(const void *x, const void *W, int32_t d_in, int32_t d_out,
+                               const int32_t *row_adapter_ids, int32_t n, const void *A_stack,
+                               const void *B_stack, int32_t n_adapters, int32_t rank, float scale,
+                               void *y, int32_t y_dtype, lora_stream_t stream);
+
+/*
  * lora_pool_last_segments -- synchronize the device and copy out the row grouping the most
  * recent forward on this pool used (computed on the device for lora_layer_forward; the
  * checked copy of the given table for lora_segment_forward).  Host outputs:
