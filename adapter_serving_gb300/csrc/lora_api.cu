@@ -515,7 +515,9 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     sp.n_seg = p->n_seg;
     sp.partials = p->shrink_part;
     sp.counters = p->shrink_cnt;
-    const int kc_dec = kShrinkDecKC;
+    // decode split width: about 128 KiB of A per block, in whole 2048-wide steps
+    int kc_dec = kShrinkDecKC;
+    while (kc_dec * rpmax * 2 < 128 * 1024) kc_dec += kShrinkDecKC;
     int splits = 0;
     for (int i = 0; i < n_io; ++i) {
         const ModuleStore &ms = p->mod[io[i].module];
@@ -543,7 +545,6 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     gp.decode = decode ? 1 : 0;
     gp.stream_k = gp.n_chunks == 1 ? 1 : 0;
     gp.rpmax = rpmax;
-    gp.unit_rows = rpmax >= 64 ? 8 : 32;
     gp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
     gp.raster_group = 8;
     int64_t iters = 0;
@@ -577,19 +578,16 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     } else {
         gp.n_cta = std::min(p->num_sms, tiles);
     }
-    // TMEM: n_acc accumulator buffers of nt columns, then nt columns for the expand delta
-    gp.n_acc = 3 * gp.nt <= 512 ? 2 : 1;
+    // TMEM: n_acc accumulator buffers of nt columns, then one expand-delta buffer per accumulator
+    gp.n_acc = 4 * gp.nt <= 512 ? 2 : 1;
     gp.tmem_cols = 32;
-    while (gp.tmem_cols < (gp.n_acc + 1) * gp.nt) gp.tmem_cols <<= 1;
-    gp.slot_bytes = (kBM * rpmax * 2 + gp.unit_rows * rpmax * 4 + 127) & ~127;
-    const int ring_target = rpmax <= 16 ? 48 * 1024 : 72 * 1024;
-    gp.n_slots = std::max(2, std::min(kMaxSlots, ring_target / gp.slot_bytes));
+    while (gp.tmem_cols < 2 * gp.n_acc * gp.nt) gp.tmem_cols <<= 1;
+    // per-thread staging for the expand's B rows: small for low ranks, more for rank 64
+    gp.ring_chunks = rpmax <= 16 ? 16 : 32;
     const size_t stage = (size_t)kBM * kBK * 2 + (size_t)gp.nt * kBK * 2;
-    const size_t budget = 227 * 1024;
-    const size_t fixed = gemm_smem_bytes(gp.nt, 0, gp.n_slots, gp.slot_bytes);
-    int stages = (int)std::min<size_t>(kMaxStages, (budget - fixed - 16 * kMaxStages) / stage);
-    if (stages < 2) return LORA_EUNSUPPORTED;
-    gp.n_stages = stages;
+    const size_t fixed = gemm_smem_bytes(gp.nt, 0, gp.ring_chunks, rpmax);
+    gp.n_stages = (int)std::min<size_t>(kMaxStages, (227 * 1024 - fixed - 16 * kMaxStages) / stage);
+    if (gp.n_stages < 2) return LORA_EUNSUPPORTED;
     gp.perm = p->perm;
     gp.seg_start = p->seg_start;
     gp.seg_adapter = p->seg_adapter;
@@ -597,7 +595,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     gp.partials = p->gemm_part;
     gp.tile_counters = p->tile_cnt;
     gp.err = p->err;
-    const size_t smem = gemm_smem_bytes(gp.nt, gp.n_stages, gp.n_slots, gp.slot_bytes);
+    const size_t smem = gemm_smem_bytes(gp.nt, gp.n_stages, gp.ring_chunks, rpmax);
     e = timed_launch(p, LORA_KERNEL_GEMM, s, [&] { return launch_gemm(gp, smem, s); });
     if (e != cudaSuccess) return cuda_fail(e, "gemm kernel");
     return LORA_OK;

@@ -24,7 +24,6 @@ constexpr int kBM = 128;       // W rows per tile (MMA M)
 constexpr int kBK = 64;        // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kEpiWarps = 4;   // epilogue warps (one per TMEM lane quarter)
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
-constexpr int kMaxSlots = 32;
 constexpr int kMaxWin = 256;        // segments one tile's expand can touch (= max rows per tile)
 constexpr int kMaxStages = 8;
 constexpr int kShrinkThreads = 256;
@@ -60,14 +59,12 @@ struct GemmParams {
     int32_t total_tiles;
     int64_t total_iters;
     int32_t rpmax;         // T row stride
-    int32_t unit_rows;     // rows per expand unit
     int32_t y_bf16;
     int32_t n_stages;
-    int32_t n_slots;
-    int32_t slot_bytes;
+    int32_t ring_chunks;   // per epilogue thread: 16-byte pieces of B rows staged per batch
     int32_t raster_group;  // W tiles per raster group (round robin)
     int32_t tmem_cols;
-    int32_t n_acc;         // accumulator buffers in TMEM (2 when 3 * nt <= 512, else 1)
+    int32_t n_acc;         // accumulator + delta buffer pairs in TMEM (2 when 4 * nt <= 512, else 1)
     const int32_t *perm;
     const int32_t *seg_start;
     const int32_t *seg_adapter;
@@ -122,7 +119,7 @@ cudaError_t launch_prep_segments(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStream_t s);
 cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s);
-size_t gemm_smem_bytes(int nt, int n_stages, int n_slots, int slot_bytes);
+size_t gemm_smem_bytes(int nt, int n_stages, int ring_chunks, int rpmax);
 
 // lora_api.cu: sets the string lora_last_cuda_error() returns on this thread
 void set_last_error(const char *why);

@@ -304,10 +304,11 @@ __global__ void __launch_bounds__(kShrinkThreads) shrink_kernel(const __grid_con
     if (tid == 0) p.counters[m * p.max_units + u] = 0;
 }
 
-// Decode shrink: one block per (segment, 2048-wide K split, module).  Each warp takes one rank
-// row per pass and every lane issues its eight 16-byte loads of A up front (32 KiB of A in
-// flight per block and pass), then reads the segment's x rows straight from L2.  Partial sums
-// of the splits are combined by the last block of the segment, in split order.
+// Decode shrink: one block per (segment, K split, module); a split covers the whole K for low
+// ranks and is cut so one block reads about 128 KiB of A otherwise.  Each warp takes one rank
+// row per pass and walks the split in 2048-wide steps: every lane issues its eight 16-byte
+// loads of A up front, then reads the segment's x rows straight from L2.  Partial sums of the
+// splits are combined by the last block of the segment, in split order.
 __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const __grid_constant__ ShrinkParams p) {
     __shared__ int s_last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -324,6 +325,11 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const 
     const int kbeg = kc * p.kc[m];
     const int kend = min(d_in, kbeg + p.kc[m]);
     const uint16_t *x = p.x[m];
+    float *const T = p.T[m];
+    const int32_t *const perm = p.perm;
+    float *const partials = p.partials;
+    const float scale = p.scale;
+    const int ks_max = p.ks_max, n = p.n;
     const int rpmax = p.rpmax;
     int r = 0, rp = 0;
     const uint16_t *A = nullptr;
@@ -336,27 +342,34 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const 
     for (int j0 = 0; j0 < r; j0 += kShrinkThreads / 32) {
         const int j = j0 + warp;
         if (j >= r) break;  // warp-uniform
-        uint4 av[kShrinkDecCh];
-#pragma unroll
-        for (int c = 0; c < kShrinkDecCh; ++c) {
-            const int kk = kbeg + lane * 8 + 256 * c;
-            av[c] = kk < kend ? __ldg(reinterpret_cast<const uint4 *>(A + (size_t)j * d_in + kk)) : make_uint4(0, 0, 0, 0);
-        }
         for (int qb = qlo; qb < qhi; qb += kShrinkDecRows) {
             float acc[kShrinkDecRows];
 #pragma unroll
-            for (int rr = 0; rr < kShrinkDecRows; ++rr) {
-                acc[rr] = 0.f;
-                if (qb + rr < qhi) {
-                    const uint16_t *xr = x + (size_t)p.perm[qb + rr] * d_in;
-                    uint4 xv[kShrinkDecCh];
+            for (int rr = 0; rr < kShrinkDecRows; ++rr) acc[rr] = 0.f;
+            int row[kShrinkDecRows];
 #pragma unroll
-                    for (int c = 0; c < kShrinkDecCh; ++c) {
-                        const int kk = kbeg + lane * 8 + 256 * c;
-                        xv[c] = kk < kend ? __ldg(reinterpret_cast<const uint4 *>(xr + kk)) : make_uint4(0, 0, 0, 0);
+            for (int rr = 0; rr < kShrinkDecRows; ++rr) row[rr] = qb + rr < qhi ? perm[qb + rr] : -1;
+            // the block's K range in 2048-wide steps: 8 loads of A per lane, then x, then FMAs
+            for (int k0 = kbeg; k0 < kend; k0 += kShrinkDecKC) {
+                uint4 av[kShrinkDecCh];
+#pragma unroll
+                for (int c = 0; c < kShrinkDecCh; ++c) {
+                    const int kk = k0 + lane * 8 + 256 * c;
+                    av[c] = kk < kend ? __ldg(reinterpret_cast<const uint4 *>(A + (size_t)j * d_in + kk)) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int rr = 0; rr < kShrinkDecRows; ++rr) {
+                    if (row[rr] >= 0) {
+                        const uint16_t *xr = x + (size_t)row[rr] * d_in;
+                        uint4 xv[kShrinkDecCh];
+#pragma unroll
+                        for (int c = 0; c < kShrinkDecCh; ++c) {
+                            const int kk = k0 + lane * 8 + 256 * c;
+                            xv[c] = kk < kend ? __ldg(reinterpret_cast<const uint4 *>(xr + kk)) : make_uint4(0, 0, 0, 0);
+                        }
+#pragma unroll
+                        for (int c = 0; c < kShrinkDecCh; ++c) acc[rr] += dot8_bf16(av[c], xv[c]);
                     }
-#pragma unroll
-                    for (int c = 0; c < kShrinkDecCh; ++c) acc[rr] += dot8_bf16(av[c], xv[c]);
                 }
             }
 #pragma unroll
@@ -365,9 +378,9 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const 
                     const float v = warp_sum(acc[rr]);
                     if (lane == 0) {
                         if (ks == 1)
-                            p.T[m][(size_t)(qb + rr) * rpmax + j] = p.scale * v;
+                            T[(size_t)row[rr] * rpmax + j] = scale * v;
                         else
-                            p.partials[(((size_t)m * p.ks_max + kc) * p.n + (qb + rr)) * rpmax + j] = v;
+                            partials[(((size_t)m * ks_max + kc) * n + (qb + rr)) * rpmax + j] = v;
                     }
                 }
             }
@@ -375,7 +388,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const 
     }
     if (ks == 1) {
         for (int idx = tid; idx < (qhi - qlo) * (rp - r); idx += kShrinkThreads)
-            p.T[m][(size_t)(qlo + idx / (rp - r)) * rpmax + r + idx % (rp - r)] = 0.f;
+            T[(size_t)perm[qlo + idx / (rp - r)] * rpmax + r + idx % (rp - r)] = 0.f;
         return;
     }
     __threadfence();
@@ -388,8 +401,8 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const 
         const int q = qlo + idx / rp, j = idx % rp;
         float v = 0.f;
         if (j < r)
-            for (int c = 0; c < ks; ++c) v += __ldcg(p.partials + (((size_t)m * p.ks_max + c) * p.n + q) * rpmax + j);
-        p.T[m][(size_t)q * rpmax + j] = p.scale * v;
+            for (int c = 0; c < ks; ++c) v += __ldcg(partials + (((size_t)m * ks_max + c) * n + q) * rpmax + j);
+        T[(size_t)perm[q] * rpmax + j] = scale * v;
     }
     if (tid == 0) p.counters[m * p.max_units + u] = 0;
 }
@@ -462,296 +475,254 @@ __device__ __forceinline__ int cta_of(const GemmParams &p, int64_t x) {
     return (int)(((x + 1) * p.n_cta - 1) / p.total_iters);
 }
 
-// Expand metadata staged in shared memory by the epilogue warps (no global-latency chains in
-// the per-unit loop): the row order (decode) and, for the segments the current tile touches,
-// their first position, B factor address and storage rank.
+// Expand metadata staged in shared memory by the epilogue warps: for every TMEM column of the
+// tile (a row of the batch), the B factor of its adapter and the storage rank (0 = base only).
 struct EpiMeta {
-    uint64_t wB[kMaxWin];      // B factor base of the window's segments (0 = base only)
-    int32_t perm[kMaxWin];     // decode: sorted position -> row
-    int32_t wss[kMaxWin + 4];  // window segment starts (clipped to the tile), wss[count] = qhi
-    int32_t wrp[kMaxWin];      // storage rank (0 = base only)
-    int32_t count;             // segments in the window
-    int32_t module;            // module the window was built for (decode caching)
-    int32_t qlo, qhi;
+    uint64_t colB[kMaxWin];  // B factor base ([d_out, rp]) of the column's adapter
+    int32_t colrp[kMaxWin];  // storage rank of that adapter, 0 for base-only rows
+    int32_t ncols;           // columns set up
+    int32_t module;          // module the columns were set up for (decode caching)
+    int32_t maxrp;           // largest storage rank among them (0: base-only tile)
+    int32_t pad_;
 };
 
-struct Unit {
-    int32_t k, qa, qe;  // window segment, positions [qa, qe)
-};
-
-// Expand units of one tile: runs of at most unit_rows positions inside one window segment.
-struct UnitCursor {
-    int32_t k, q;
-    __device__ void begin(const EpiMeta &w) {
-        k = 0;
-        q = w.qlo;
-    }
-    __device__ bool next(const GemmParams &p, const EpiMeta &w, Unit &u) {
-        if (q >= w.qhi) return false;
-        while (k + 1 < w.count && w.wss[k + 1] <= q) ++k;
-        int qe = min(min(w.wss[k + 1], w.qhi), q + p.unit_rows);
-        if (qe <= q) qe = q + 1;  // inconsistent table: still make progress, stay in bounds
-        u.k = k;
-        u.qa = q;
-        u.qe = qe;
-        q = qe;
-        return true;
-    }
-};
-
+// Everything the epilogue reads per call, copied out of the kernel parameters once.  Parameters
+// reached through a runtime module index are generic loads that the compiler must repeat after
+// every store (they might alias); locals never are.
 struct EpiCtx {
     const GemmParams *p;
-    uint8_t *ring;
-    uint64_t *slot_bar;
+    uint8_t *ring;       // per-thread staging of B rows: chunk i of thread t at (i * 128 + t) * 16
+    float *tstage;       // t rows of the current batch of columns, [16][rpmax]
     EpiMeta *meta;
+    int decode, n, nt, y_bf16, n_cta, rpmax;
+    int64_t total_iters;
+    float *partials;
+    int32_t *tile_counters;
+    const int32_t *perm, *seg_start, *seg_adapter, *n_seg;
     uint32_t tmem_base;
-    uint32_t delta_col;  // first TMEM column of the expand (delta) region
+    uint32_t delta_col;  // first TMEM column of the expand (delta) buffers (one per accumulator)
     int etid;            // 0..127 among epilogue threads
     int o;               // TMEM lane = W row within the tile
     int lane_base;       // first TMEM lane of this warp
     int lane;
-    uint32_t g_unit;     // expand units processed by this CTA so far (ring slot / parity)
 };
 
-// (Re)build the segment window for a tile: every segment overlapping its positions
-// [qlo, qhi), with the factor addresses of module m.  Decode tiles of one module share the
-// window, so it is rebuilt only when the module changes.
-__device__ void build_window(EpiCtx &c, const Item &it) {
-    const GemmParams &p = *c.p;
+struct ModLocal {
+    void *y;
+    const float *T;
+    const PoolEntry *table;
+    int d_out;
+};
+__device__ __forceinline__ ModLocal mod_local(const GemmParams &p, int m) {
+    const GemmModule &M = p.mod[m];
+    return ModLocal{M.y, M.T, M.table, M.d_out};
+}
+
+// (Re)build the per-column metadata of a tile from the segment table: every row of the tile's
+// positions gets its segment's adapter.  Decode tiles of one module share it, so it is rebuilt
+// only when the module changes; for grouped rows it is built per tile.
+__device__ void setup_columns(EpiCtx &c, const Item &it) {
     EpiMeta &w = *c.meta;
-    const int row0 = it.chunk * p.nt;
-    if (p.decode && w.module == it.m) return;
-    named_bar_sync(1, 128);  // nobody still reads the old window
-    const int n_seg = *p.n_seg;
-    int s0, cnt, qlo, qhi;
-    if (p.decode) {
-        qlo = 0;
-        qhi = p.n;
-        s0 = 0;
-        cnt = min(n_seg, kMaxWin);
-    } else {
-        qlo = row0;
-        qhi = min(p.n, row0 + p.nt);
-        s0 = seg_of(p.seg_start, n_seg, qlo);
-        const int s1 = seg_of(p.seg_start, n_seg, qhi - 1);
-        cnt = min(s1 - s0 + 1, kMaxWin);
-    }
-    const PoolEntry *table = p.mod[it.m].table;
-    for (int i = c.etid; i < cnt; i += 128) {
-        const int s = s0 + i;
-        const int a = __ldg(p.seg_adapter + s);
-        w.wss[i] = max(__ldg(p.seg_start + s), qlo);
+    if (c.decode && w.module == it.m) return;
+    named_bar_sync(1, 128);  // nobody still reads the old columns
+    if (c.etid == 0) w.maxrp = 0;
+    named_bar_sync(1, 128);
+    const int n_seg = *c.n_seg;
+    const int row0 = it.chunk * c.nt;
+    const int qlo = c.decode ? 0 : row0;
+    const int qhi = c.decode ? c.n : min(c.n, row0 + c.nt);
+    const int32_t *seg_start = c.seg_start, *seg_adapter = c.seg_adapter, *perm = c.perm;
+    const int decode = c.decode;
+    const int s0 = decode ? 0 : seg_of(seg_start, n_seg, qlo);
+    const int s1 = decode ? n_seg - 1 : seg_of(seg_start, n_seg, qhi - 1);
+    const PoolEntry *table = mod_local(*c.p, it.m).table;
+    // one thread per position: find its segment (binary search in [s0, s1]), then its column
+    for (int q = qlo + c.etid; q < qhi; q += 128) {
+        int lo = s0, hi = s1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(seg_start + mid) <= q) lo = mid; else hi = mid - 1;
+        }
+        const int a = __ldg(seg_adapter + lo);
         uint64_t b = 0;
         int rp = 0;
         if (a >= 0) {
             b = reinterpret_cast<uint64_t>(table[a].B);
             rp = table[a].rp;
         }
-        w.wB[i] = b;
-        w.wrp[i] = rp;
+        const int col = decode ? __ldg(perm + q) : q - row0;
+        if (col >= 0 && col < kMaxWin) {
+            w.colB[col] = b;
+            w.colrp[col] = rp;
+        }
+        if (rp > 0) atomicMax(&w.maxrp, rp);
     }
     if (c.etid == 0) {
-        w.wss[cnt] = qhi;
-        w.count = cnt;
-        w.qlo = qlo;
-        w.qhi = qhi;
+        w.ncols = qhi - qlo;
         w.module = it.m;
     }
     named_bar_sync(1, 128);
 }
 
-// Stage one expand unit into a ring slot: the adapter's B rows [o0, o0 + 128) (cp.async,
-// 16-byte chunks XOR-swizzled by row so each thread later reads its own row without bank
-// conflicts) and the unit's t rows.  Every epilogue thread arrives on the slot barrier once
-// its copies land.
-__device__ void issue_unit(EpiCtx &c, const Item &it, const Unit &u, int slot) {
-    const GemmParams &p = *c.p;
-    const GemmModule &M = p.mod[it.m];
+// Expand for a tile this CTA heads: delta[o, col] = sum_j B_a[o0 + o, j] * t_col[j] for every
+// column (row of the batch) of the tile, 0 for base-only rows, written into the TMEM delta
+// buffer paired with the tile's accumulator.  It runs while the MMA warp works (on this tile or
+// the one before); the drain adds it to the accumulator.
+//
+// Columns go in blocks of 16 (one 16-column TMEM store per block), each block in batches of CB
+// columns.  Column i of a batch owns NCH fixed 16-byte slots of the per-thread ring, so every
+// address is known without a running counter and all loads and dot products of a batch are
+// independent: each thread copies its own B row pieces with cp.async (it then waits only for
+// its own copies), the 128 threads copy the batch's t rows together, one wait, one barrier,
+// then the batch is computed.  NCH = storage rank / 8 of the largest rank among the columns.
+template <int NCH>
+__device__ void expand_blocks(EpiCtx &c, const Item &it, uint32_t tcol0) {
+    constexpr int CB = (NCH <= 2) ? 16 / NCH : 32 / NCH;  // columns per batch (ring: CB * NCH slots)
+    constexpr int NB16 = 16 / CB;                       // batches per 16-column block
     const EpiMeta &w = *c.meta;
-    const int rp = w.wrp[u.k];
-    if (rp > 0) {
-        const uint16_t *B = reinterpret_cast<const uint16_t *>(w.wB[u.k]);
-        const uint32_t sbase = smem_u32(c.ring + (size_t)slot * p.slot_bytes);
-        const int lg = __ffs(rp >> 3) - 1;  // log2(rp / 8)
-        const int nch = 1 << lg;
-        const int sh = 3 - lg;
-        const int o0 = it.w_tile * kBM;
-        for (int idx = c.etid; idx < (kBM << lg); idx += 128) {
-            const int row = idx >> lg, ch = idx & (nch - 1);
-            const int o = o0 + row;
-            const bool v = o < M.d_out;
-            const uint16_t *src = v ? B + (size_t)o * rp + ch * 8 : B;
-            cp_async_16(sbase + (uint32_t)(((row << lg) + (ch ^ ((row >> sh) & (nch - 1)))) * 16), src,
-                        v ? 16u : 0u);
-        }
-        const int tch = rp >> 2;
-        const int rows = u.qe - u.qa;
-        const float *Tsrc = M.T + (size_t)u.qa * p.rpmax;
-        const uint32_t tbase = sbase + (uint32_t)(kBM * p.rpmax * 2);
-        for (int idx = c.etid; idx < rows * tch; idx += 128) {
-            const int r = idx / tch, ch = idx - r * tch;
-            cp_async_16(tbase + (uint32_t)((r * rp + ch * 4) * 4), Tsrc + (size_t)r * p.rpmax + ch * 4, 16u);
-        }
-    }
-    cp_async_arrive_noinc(c.slot_bar + slot);
-}
-
-template <int RP>
-__device__ __forceinline__ void apply_unit(EpiCtx &c, const Unit &u, const uint8_t *sb, uint32_t tcol0, int row0) {
-    constexpr int LG = (RP == 8) ? 0 : (RP == 16) ? 1 : (RP == 32) ? 2 : 3;
-    constexpr int NCH = 1 << LG;
-    constexpr int SH = 3 - LG;
-    const GemmParams &p = *c.p;
-    const EpiMeta &w = *c.meta;
-    uint32_t b[RP / 2];
+    const ModLocal M = mod_local(*c.p, it.m);
+    const int row0 = it.chunk * c.nt;
+    const int ncols = w.ncols;
+    const int rpmax = c.rpmax;
+    const int oo = it.w_tile * kBM + c.o;
+    const bool o_ok = oo < M.d_out;
+    const uint32_t ring_me = smem_u32(c.ring) + (uint32_t)c.o * 16;
+    const uint32_t tst = smem_u32(c.tstage);
+    const float *Tg = M.T + (size_t)row0 * rpmax;  // t rows in row order
+    for (int b0 = 0; b0 < ncols; b0 += 16) {
+        float d[16];
 #pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(sb + ((c.o << LG) + (ch ^ ((c.o >> SH) & (NCH - 1)))) * 16);
-        b[4 * ch + 0] = v.x;
-        b[4 * ch + 1] = v.y;
-        b[4 * ch + 2] = v.z;
-        b[4 * ch + 3] = v.w;
-    }
-    const float *Ts = reinterpret_cast<const float *>(sb + kBM * p.rpmax * 2);
-    for (int q = u.qa; q < u.qe; ++q) {
-        const float4 *t4 = reinterpret_cast<const float4 *>(Ts + (q - u.qa) * RP);
-        float acc = 0.f;
+        for (int k = 0; k < NB16; ++k) {
+            const int cb = b0 + k * CB;
+            int rp[CB];
 #pragma unroll
-        for (int j4 = 0; j4 < RP / 4; ++j4) {
-            const float4 tv = t4[j4];
-            acc = fmaf(bf16lo(b[2 * j4]), tv.x, acc);
-            acc = fmaf(bf16hi(b[2 * j4]), tv.y, acc);
-            acc = fmaf(bf16lo(b[2 * j4 + 1]), tv.z, acc);
-            acc = fmaf(bf16hi(b[2 * j4 + 1]), tv.w, acc);
-        }
-        const int col = p.decode ? w.perm[q] : q - row0;
-        tmem_st1(tcol0 + (uint32_t)col, acc);
-    }
-}
-
-// Expand for a tile this CTA heads: delta[o, col(q)] = sum_j B_a[o0 + o, j] * t_q[j] for every
-// position q of the tile (0 for base-only rows), written into the TMEM delta region.  It runs
-// while the MMA warp works on the same tile; the drain adds it to the accumulator.
-__device__ bool init_expand(EpiCtx &c, const Item &it, volatile int *abort_flag) {
-    const GemmParams &p = *c.p;
-    build_window(c, it);
-    const EpiMeta &w = *c.meta;
-    const int row0 = it.chunk * p.nt;
-    const uint32_t tcol0 = c.tmem_base + ((uint32_t)c.lane_base << 16) + c.delta_col;
-    UnitCursor ic, cc;
-    ic.begin(w);
-    cc.begin(w);
-    const uint32_t base = c.g_unit;
-    uint32_t issued = 0, consumed = 0;
-    Unit u;
-    while (issued < (uint32_t)p.n_slots && ic.next(p, w, u)) {
-        issue_unit(c, it, u, (base + issued) % p.n_slots);
-        ++issued;
-    }
-    bool ok = true;
-    while (cc.next(p, w, u)) {
-        const uint32_t k = base + consumed;
-        const int slot = k % p.n_slots;
-        const bool landed = mbar_wait(c.slot_bar + slot, (k / p.n_slots) & 1, abort_flag, p.err);
-        {
-            // runs even if the wait gave up (the warp-wide TMEM stores need every lane); the
-            // values are then meaningless but every access stays in bounds
-            const uint8_t *sb = c.ring + (size_t)slot * p.slot_bytes;
-            switch (w.wrp[u.k]) {
-                case 8: apply_unit<8>(c, u, sb, tcol0, row0); break;
-                case 16: apply_unit<16>(c, u, sb, tcol0, row0); break;
-                case 32: apply_unit<32>(c, u, sb, tcol0, row0); break;
-                case 64: apply_unit<64>(c, u, sb, tcol0, row0); break;
-                default:
-                    for (int q = u.qa; q < u.qe; ++q) {
-                        const int col = p.decode ? w.perm[q] : q - row0;
-                        tmem_st1(tcol0 + (uint32_t)col, 0.f);
-                    }
+            for (int i = 0; i < CB; ++i) rp[i] = cb + i < ncols ? w.colrp[cb + i] : 0;
+#pragma unroll
+            for (int i = 0; i < CB; ++i) {
+                if (rp[i] > 0) {
+                    const uint16_t *src =
+                        reinterpret_cast<const uint16_t *>(w.colB[cb + i]) + (size_t)(o_ok ? oo : 0) * rp[i];
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch)
+                        if (ch * 8 < rp[i])
+                            cp_async_16(ring_me + (uint32_t)((i * NCH + ch) * 128 * 16), src + ch * 8, o_ok ? 16u : 0u);
+                }
             }
+            const int nrow = min(CB, ncols - cb);
+            if (nrow > 0) {
+                const int tchunks = nrow * (rpmax >> 2);
+                for (int idx = c.etid; idx < tchunks; idx += 128)
+                    cp_async_16(tst + (uint32_t)idx * 16, Tg + (size_t)cb * rpmax + idx * 4, 16u);
+            }
+            cp_async_commit();
+            cp_async_wait_all();
+            named_bar_sync(1, 128);  // everyone's t rows have landed
+#pragma unroll
+            for (int i = 0; i < CB; ++i) {
+                const float *t = c.tstage + i * rpmax;
+                float acc = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    if (ch * 8 < rp[i]) {
+                        const uint4 bv = *reinterpret_cast<const uint4 *>(c.ring + ((size_t)(i * NCH + ch) * 128 + c.o) * 16);
+                        const float4 ta = *reinterpret_cast<const float4 *>(t + ch * 8);
+                        const float4 tb = *reinterpret_cast<const float4 *>(t + ch * 8 + 4);
+                        acc = fmaf(bf16lo(bv.x), ta.x, acc);
+                        acc = fmaf(bf16hi(bv.x), ta.y, acc);
+                        acc = fmaf(bf16lo(bv.y), ta.z, acc);
+                        acc = fmaf(bf16hi(bv.y), ta.w, acc);
+                        acc = fmaf(bf16lo(bv.z), tb.x, acc);
+                        acc = fmaf(bf16hi(bv.z), tb.y, acc);
+                        acc = fmaf(bf16lo(bv.w), tb.z, acc);
+                        acc = fmaf(bf16hi(bv.w), tb.w, acc);
+                    }
+                }
+                d[k * CB + i] = acc;
+            }
+            named_bar_sync(1, 128);  // the t rows may be overwritten by the next batch
         }
-        // every thread is done with the slot; leave together if any wait gave up
-        const bool any_failed = named_bar_or(1, 128, !landed);
-        ++consumed;
-        if (any_failed) {
-            ok = false;
-            break;
-        }
-        if (ic.next(p, w, u)) {
-            issue_unit(c, it, u, (base + issued) % p.n_slots);
-            ++issued;
+        tmem_st16(tcol0 + (uint32_t)b0, d);
+    }
+}
+
+__device__ void init_expand(EpiCtx &c, const Item &it, int buf) {
+    setup_columns(c, it);
+    const uint32_t tcol0 = c.tmem_base + ((uint32_t)c.lane_base << 16) + c.delta_col + (uint32_t)(buf * c.nt);
+    switch (c.meta->maxrp) {
+        case 8: expand_blocks<1>(c, it, tcol0); break;
+        case 16: expand_blocks<2>(c, it, tcol0); break;
+        case 32: expand_blocks<4>(c, it, tcol0); break;
+        case 64: expand_blocks<8>(c, it, tcol0); break;
+        default: {  // base-only tile
+            float z[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z[i] = 0.f;
+            for (int b0 = 0; b0 < c.meta->ncols; b0 += 16) tmem_st16(tcol0 + (uint32_t)b0, z);
         }
     }
-    // A timed-out wait can leave copies in flight: let them land before the slot is reused.
-    while (consumed < issued) {
-        const uint32_t k = base + consumed;
-        mbar_wait(c.slot_bar + (k % p.n_slots), (k / p.n_slots) & 1, abort_flag, p.err);
-        ++consumed;
-    }
-    c.g_unit = base + consumed;
     tmem_st_wait();
-    return ok;
 }
 
-__device__ __forceinline__ void store_y(const GemmParams &p, const GemmModule &M, int row, int oo, float v) {
-    if (p.y_bf16) {
-        reinterpret_cast<uint16_t *>(M.y)[(size_t)row * M.d_out + oo] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+__device__ __forceinline__ void store_y(void *y, int d_out, int y_bf16, int row, int oo, float v) {
+    if (y_bf16) {
+        reinterpret_cast<uint16_t *>(y)[(size_t)row * d_out + oo] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
     } else {
-        reinterpret_cast<float *>(M.y)[(size_t)row * M.d_out + oo] = v;
+        reinterpret_cast<float *>(y)[(size_t)row * d_out + oo] = v;
     }
 }
 
-__device__ __forceinline__ void ld_cols16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    tmem_ld16(taddr, r);
+// This CTA's share of 16 columns of a tile: accumulator (+ the expand delta when it heads the
+// tile), both TMEM loads in flight before the one wait.
+__device__ __forceinline__ void own_cols16(const EpiCtx &c, uint32_t tacc, uint32_t tdel, bool head, int c0,
+                                           float (&v)[16]) {
+    uint32_t r[16], d[16];
+    tmem_ld16(tacc + c0, r);
+    if (head) tmem_ld16(tdel + c0, d);
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + (head ? __uint_as_float(d[i]) : 0.f);
 }
 
-// This CTA's share of a tile: accumulator (+ the expand delta when it heads the tile).
-__device__ __forceinline__ void own_cols16(const EpiCtx &c, uint32_t tacc, bool head, int c0, float (&v)[16]) {
-    ld_cols16(tacc + c0, v);
-    if (head) {
-        float d[16];
-        ld_cols16(c.tmem_base + ((uint32_t)c.lane_base << 16) + c.delta_col + c0, d);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] += d[i];
-    }
-}
+constexpr int kPrefetchParts = 1;  // partial tiles read ahead per 16-column chunk when finishing
 
 // Accumulator -> y.  A tile split over several CTAs (stream-K) is finished by the last CTA
 // to get there (atomic counter); it adds the pieces in k order, so the sum never depends on
-// timing.  No CTA ever waits for another.
+// timing.  No CTA ever waits for another.  Partial tiles are stored row-major per TMEM lane
+// ([o][column]) so each thread moves its 16 columns with four 16-byte accesses.
 __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_flag) {
-    const GemmParams &p = *c.p;
-    const GemmModule &M = p.mod[it.m];
-    const int row0 = it.chunk * p.nt;
-    const int ncols = p.decode ? p.n : min(p.nt, p.n - row0);
+    const ModLocal M = mod_local(*c.p, it.m);
+    const int nt = c.nt, decode = c.decode, y_bf16 = c.y_bf16, n_cta = c.n_cta;
+    const int64_t total_iters = c.total_iters;
+    float *const partials = c.partials;
+    const int row0 = it.chunk * nt;
+    const int ncols = decode ? c.n : min(nt, c.n - row0);
     const int ncols16 = (ncols + 15) & ~15;
     const int oo = it.w_tile * kBM + c.o;
     const bool o_ok = oo < M.d_out;
     const bool head = it.kb0 == 0;
-    const uint32_t tacc = c.tmem_base + ((uint32_t)c.lane_base << 16) + (uint32_t)(buf * p.nt);
-    const size_t slot_elems = (size_t)kBM * p.nt;
+    const uint32_t lane_off = (uint32_t)c.lane_base << 16;
+    const uint32_t tacc = c.tmem_base + lane_off + (uint32_t)(buf * nt);
+    const uint32_t tdel = c.tmem_base + lane_off + c.delta_col + (uint32_t)(buf * nt);
+    const size_t slot_elems = (size_t)kBM * nt;
 
     if (head && it.kb1 == it.kbn) {
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
-            own_cols16(c, tacc, true, c0, v);
+            own_cols16(c, tacc, tdel, true, c0, v);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int col = c0 + i;
-                if (col < ncols && o_ok) store_y(p, M, p.decode ? col : row0 + col, oo, v[i]);
+                if (col < ncols && o_ok) store_y(M.y, M.d_out, y_bf16, decode ? col : row0 + col, oo, v[i]);
             }
         }
         return;
     }
 
     // ---- partial tile (stream-K) ----
-    const int c_first = cta_of(p, it.it0);
-    const int c_last = cta_of(p, it.it0 + it.kbn - 1);
+    const int c_first = (int)(((it.it0 + 1) * n_cta - 1) / total_iters);  // CTA holding iteration it0
+    const int c_last = (int)(((it.it0 + it.kbn) * n_cta - 1) / total_iters);
     const int nc = c_last - c_first + 1;
-    int32_t *counter = p.tile_counters + it.tile;
+    int32_t *counter = c.tile_counters + it.tile;
     bool finalize = false;
     if (head) {  // the head usually arrives last: finish directly if everyone else is in
         if (c.etid == 0) *misc_flag = (atomicAdd(counter, 0) == nc - 1);
@@ -759,16 +730,18 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
         finalize = *misc_flag != 0;
         named_bar_sync(1, 128);
     }
+    auto part_row = [&](int cta) -> float * {
+        const int64_t b_c = (int64_t)cta * total_iters / n_cta;
+        const int sl = (b_c >= it.it0) ? 0 : 1;
+        return partials + ((size_t)cta * 2 + sl) * slot_elems + (size_t)c.o * nt;
+    };
     if (!finalize) {
-        const int64_t my_b = (int64_t)blockIdx.x * p.total_iters / p.n_cta;
-        const int my_slot = (my_b >= it.it0) ? 0 : 1;
-        float *dst = p.partials + ((size_t)blockIdx.x * 2 + my_slot) * slot_elems;
+        float4 *dst = reinterpret_cast<float4 *>(part_row(blockIdx.x));
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
-            own_cols16(c, tacc, head, c0, v);
+            own_cols16(c, tacc, tdel, head, c0, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (c0 + i < ncols) dst[(size_t)(c0 + i) * kBM + c.o] = v[i];
+            for (int i = 0; i < 4; ++i) dst[c0 / 4 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         __threadfence();
         named_bar_sync(1, 128);
@@ -779,22 +752,56 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
     }
     if (!finalize) return;
     __threadfence();
+    // the other pieces' loads for chunk c0 + 16 are issued before chunk c0 is added up
+    float4 cur[kPrefetchParts][4], nxt[kPrefetchParts][4];
+    // k-th contributor other than this CTA (this CTA is one of c_first..c_last)
+    const int self_idx = (int)blockIdx.x - c_first;
+    auto other = [&](int k) { return c_first + k + (k >= self_idx ? 1 : 0); };
+    auto fetch = [&](int c0, float4 (&dst)[kPrefetchParts][4]) {
+#pragma unroll
+        for (int k = 0; k < kPrefetchParts; ++k) {
+            if (k < nc - 1 && c0 < ncols16) {
+                const float4 *src = reinterpret_cast<const float4 *>(part_row(other(k))) + c0 / 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dst[k][i] = __ldcg(src + i);
+            }
+        }
+    };
+    fetch(0, cur);
     for (int c0 = 0; c0 < ncols16; c0 += 16) {
+        fetch(c0 + 16, nxt);
         float own[16], sum[16];
-        own_cols16(c, tacc, head, c0, own);
+        own_cols16(c, tacc, tdel, head, c0, own);
         for (int jc = 0; jc < nc; ++jc) {
             const int cc = c_first + jc;
             float v[16];
+            const int k_other = jc - (jc > self_idx ? 1 : 0);
             if (cc == (int)blockIdx.x) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = own[i];
-            } else {
-                const int64_t b_c = (int64_t)cc * p.total_iters / p.n_cta;
-                const int sl = (b_c >= it.it0) ? 0 : 1;
-                const float *src = p.partials + ((size_t)cc * 2 + sl) * slot_elems;
+            } else if (k_other < kPrefetchParts) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    v[i] = (c0 + i < ncols) ? __ldcg(src + (size_t)(c0 + i) * kBM + c.o) : 0.f;
+                for (int jp = 0; jp < kPrefetchParts; ++jp) {
+                    if (jp == k_other) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            v[4 * i] = cur[jp][i].x;
+                            v[4 * i + 1] = cur[jp][i].y;
+                            v[4 * i + 2] = cur[jp][i].z;
+                            v[4 * i + 3] = cur[jp][i].w;
+                        }
+                    }
+                }
+            } else {
+                const float4 *src = reinterpret_cast<const float4 *>(part_row(cc)) + c0 / 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 t = __ldcg(src + i);
+                    v[4 * i] = t.x;
+                    v[4 * i + 1] = t.y;
+                    v[4 * i + 2] = t.z;
+                    v[4 * i + 3] = t.w;
+                }
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) sum[i] = (jc == 0) ? v[i] : sum[i] + v[i];
@@ -802,8 +809,12 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int col = c0 + i;
-            if (col < ncols && o_ok) store_y(p, M, p.decode ? col : row0 + col, oo, sum[i]);
+            if (col < ncols && o_ok) store_y(M.y, M.d_out, y_bf16, decode ? col : row0 + col, oo, sum[i]);
         }
+#pragma unroll
+        for (int jc = 0; jc < kPrefetchParts; ++jc)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cur[jc][i] = nxt[jc][i];
     }
     if (c.etid == 0) *counter = 0;
 }
@@ -816,15 +827,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const uint32_t a_bytes = kBM * kBK * 2;
     const uint32_t b_bytes = (uint32_t)p.nt * kBK * 2;
     const uint32_t stage_bytes = a_bytes + b_bytes;
-    uint8_t *ring = smem + (size_t)S * stage_bytes;
-    EpiMeta *meta = reinterpret_cast<EpiMeta *>(ring + (size_t)p.n_slots * p.slot_bytes);
+    uint8_t *ring = smem + (size_t)S * stage_bytes;  // per-thread B staging, ring_chunks * 2 KiB
+    float *tstage = reinterpret_cast<float *>(ring + (size_t)p.ring_chunks * 128 * 16);  // [16][rpmax]
+    EpiMeta *meta = reinterpret_cast<EpiMeta *>(tstage + 16 * p.rpmax);
     uint64_t *full = reinterpret_cast<uint64_t *>(meta + 1);
     uint64_t *empty = full + S;
     uint64_t *acc_full = empty + S;
     uint64_t *acc_free = acc_full + 2;
     uint64_t *mma_done = acc_free + 2;
-    uint64_t *slot_bar = mma_done + 1;
-    uint32_t *misc = reinterpret_cast<uint32_t *>(slot_bar + p.n_slots);  // [0] tmem, [1] abort, [2] flag
+    uint32_t *misc = reinterpret_cast<uint32_t *>(mma_done + 1);  // [0] tmem, [1] abort, [2] flag
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -837,7 +848,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             mbar_init(acc_free + b, kEpiWarps);
         }
         mbar_init(mma_done, 1);
-        for (int s = 0; s < p.n_slots; ++s) mbar_init(slot_bar + s, 128);
         misc[1] = 0;
         misc[2] = 0;
         meta->module = -1;
@@ -936,7 +946,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         EpiCtx c;
         c.p = &p;
         c.ring = ring;
-        c.slot_bar = slot_bar;
+        c.tstage = tstage;
         c.meta = meta;
         c.tmem_base = tmem_base;
         c.delta_col = (uint32_t)(NB * p.nt);
@@ -944,25 +954,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         c.lane = lane;
         c.lane_base = (warp & 3) * 32;
         c.o = c.lane_base + lane;
-        c.g_unit = 0;
-        if (p.decode)
-            for (int i = c.etid; i < p.n; i += 128) meta->perm[i] = __ldg(p.perm + i);
+        c.decode = p.decode;
+        c.n = p.n;
+        c.nt = p.nt;
+        c.y_bf16 = p.y_bf16;
+        c.n_cta = p.n_cta;
+        c.rpmax = p.rpmax;
+        c.total_iters = p.total_iters;
+        c.partials = p.partials;
+        c.tile_counters = p.tile_counters;
+        c.perm = p.perm;
+        c.seg_start = p.seg_start;
+        c.seg_adapter = p.seg_adapter;
+        c.n_seg = p.n_seg;
         volatile int *flag = reinterpret_cast<volatile int *>(misc + 2);
+        // The expand of a tile this CTA heads is prepared one item ahead when there are two
+        // accumulator/delta buffer pairs, so it overlaps the MMAs of the item before it.
         Sched sc;
         sc.begin(p, blockIdx.x);
-        Item it;
+        Item cur, nxt;
+        bool has_cur = sc.next(p, cur);
         uint32_t li = 0;
-        while (sc.next(p, it)) {
+        if (has_cur && cur.kb0 == 0) init_expand(c, cur, 0);
+        while (has_cur) {
             const int buf = li % NB;
-            bool ok = true;
-            if (it.kb0 == 0) ok = init_expand(c, it, abort_flag);
+            const bool has_nxt = sc.next(p, nxt);
+            if (has_nxt && NB == 2 && nxt.kb0 == 0) init_expand(c, nxt, (li + 1) % 2);
             const bool full_ok = mbar_wait(acc_full + buf, (li / NB) & 1, abort_flag, p.err);
-            if (named_bar_or(1, 128, !(full_ok && ok))) break;
+            if (named_bar_or(1, 128, !full_ok)) break;
             tc_fence_after();
-            drain(c, it, buf, flag);
+            drain(c, cur, buf, flag);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_free + buf);
+            if (has_nxt && NB == 1 && nxt.kb0 == 0) init_expand(c, nxt, 0);
+            cur = nxt;
+            has_cur = has_nxt;
             ++li;
         }
     }
@@ -977,10 +1004,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
 // ====================================================================== launchers ==========
 
-size_t gemm_smem_bytes(int nt, int n_stages, int n_slots, int slot_bytes) {
+size_t gemm_smem_bytes(int nt, int n_stages, int ring_chunks, int rpmax) {
     const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2;
-    return 1024 + stage * n_stages + (size_t)n_slots * slot_bytes + sizeof(EpiMeta) +
-           8 * (2 * (size_t)n_stages + 5 + n_slots) + 16;
+    return 1024 + stage * n_stages + (size_t)ring_chunks * 128 * 16 + (size_t)16 * rpmax * 4 + sizeof(EpiMeta) +
+           8 * (2 * (size_t)n_stages + 5) + 16;
 }
 
 cudaError_t launch_prep_decode(const PrepParams &p, cudaStream_t s) {

@@ -214,7 +214,6 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     gp.decode = 1;
     gp.stream_k = 1;
     gp.rpmax = rpmax;
-    gp.unit_rows = rpmax >= 64 ? 8 : 32;
     gp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
     gp.raster_group = 8;
     GemmModule &gm = gp.mod[0];
@@ -232,15 +231,15 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     gp.total_tiles = gm.m_tiles;
     gp.total_iters = (int64_t)gm.m_tiles * gm.k_blocks;
     gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, gp.total_iters / 4));
-    gp.n_acc = 3 * gp.nt <= 512 ? 2 : 1;
+    gp.n_acc = 4 * gp.nt <= 512 ? 2 : 1;
     gp.tmem_cols = 32;
-    while (gp.tmem_cols < (gp.n_acc + 1) * gp.nt) gp.tmem_cols <<= 1;
-    gp.slot_bytes = (kBM * rpmax * 2 + gp.unit_rows * rpmax * 4 + 127) & ~127;
-    const int ring_target = rpmax <= 16 ? 48 * 1024 : 72 * 1024;
-    gp.n_slots = std::max(2, std::min(kMaxSlots, ring_target / gp.slot_bytes));
+    while (gp.tmem_cols < 2 * gp.n_acc * gp.nt) gp.tmem_cols <<= 1;
+    // per-thread staging for the expand's B rows: small for low ranks, more for rank 64
+    gp.ring_chunks = rpmax <= 16 ? 16 : 32;
     const size_t stage = (size_t)kBM * kBK * 2 + (size_t)gp.nt * kBK * 2;
-    const size_t fixed = gemm_smem_bytes(gp.nt, 0, gp.n_slots, gp.slot_bytes);
+    const size_t fixed = gemm_smem_bytes(gp.nt, 0, gp.ring_chunks, rpmax);
     gp.n_stages = (int)std::min<size_t>(kMaxStages, (227 * 1024 - fixed - 16 * kMaxStages) / stage);
+    if (gp.n_stages < 2) return LORA_EUNSUPPORTED;
     gp.perm = perm;
     gp.seg_start = seg_start;
     gp.seg_adapter = seg_adapter;
@@ -248,7 +247,7 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     gp.partials = reinterpret_cast<float *>(scratch + kOffGemmPart);
     gp.tile_counters = reinterpret_cast<int32_t *>(scratch + kOffTileCnt);
     gp.err = err;
-    const size_t smem = gemm_smem_bytes(gp.nt, gp.n_stages, gp.n_slots, gp.slot_bytes);
+    const size_t smem = gemm_smem_bytes(gp.nt, gp.n_stages, gp.ring_chunks, rpmax);
     if ((e = launch_gemm(gp, smem, s)) != cudaSuccess)
         return fail(LORA_ECUDA, std::string("gemm kernel: ") + cudaGetErrorString(e));
     return LORA_OK;
