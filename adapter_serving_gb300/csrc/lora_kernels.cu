@@ -494,7 +494,7 @@ struct EpiCtx {
     uint8_t *ring;       // per-thread staging of B rows: chunk i of thread t at (i * 128 + t) * 16
     float *tstage;       // t rows of the current batch of columns, [16][rpmax]
     EpiMeta *meta;
-    int decode, n, nt, y_bf16, n_cta, rpmax;
+    int decode, n, nt, y_bf16, n_cta, rpmax, ring_chunks;
     int64_t total_iters;
     float *partials;
     int32_t *tile_counters;
@@ -663,13 +663,6 @@ __device__ void init_expand(EpiCtx &c, const Item &it, int buf) {
     tmem_st_wait();
 }
 
-__device__ __forceinline__ void store_y(void *y, int d_out, int y_bf16, int row, int oo, float v) {
-    if (y_bf16) {
-        reinterpret_cast<uint16_t *>(y)[(size_t)row * d_out + oo] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-    } else {
-        reinterpret_cast<float *>(y)[(size_t)row * d_out + oo] = v;
-    }
-}
 
 // This CTA's share of 16 columns of a tile: accumulator (+ the expand delta when it heads the
 // tile), both TMEM loads in flight before the one wait.
@@ -683,13 +676,27 @@ __device__ __forceinline__ void own_cols16(const EpiCtx &c, uint32_t tacc, uint3
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + (head ? __uint_as_float(d[i]) : 0.f);
 }
 
-constexpr int kPrefetchParts = 1;  // partial tiles read ahead per 16-column chunk when finishing
 
-// Accumulator -> y.  A tile split over several CTAs (stream-K) is finished by the last CTA
-// to get there (atomic counter); it adds the pieces in k order, so the sum never depends on
-// timing.  No CTA ever waits for another.  Partial tiles are stored row-major per TMEM lane
-// ([o][column]) so each thread moves its 16 columns with four 16-byte accesses.
-__device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_flag) {
+// Drain: accumulator (+ expand delta when this CTA heads the tile) -> y.  Output goes through
+// shared memory and the TMA engine: the 128 lanes of a 16-column chunk are written to a
+// [column][lane] buffer and one thread issues bulk stores (a y row segment per column, or one
+// contiguous 8 KiB block of a partial tile), double-buffered.  A tile split over several CTAs
+// (stream-K) is finished by one CTA that adds the pieces in k order, so the sum never depends
+// on timing.  The piece holding k-block 0 is always the last item of its CTA and the other
+// pieces are the first items of theirs, so that CTA waits (bounded) for the others and then
+// finishes the tile without writing its own piece; if the wait runs out it falls back to
+// "write your piece, last to arrive finishes".
+struct DrainBufs {
+    uint8_t *obuf[2];   // output staging, 8 KiB each
+    uint8_t *ibuf[2];   // other pieces' chunks, 8 KiB each
+    uint64_t *ld_bar;   // [2] completion of the ibuf loads
+    uint32_t *ld_count; // loads issued so far by this CTA (parity of ld_bar)
+};
+
+constexpr uint64_t kHeadWaitNs = 50000;  // how long a finishing CTA waits for the other pieces
+
+__device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_flag, volatile int *abort_flag,
+                      DrainBufs &db, uint32_t &n_out) {
     const ModLocal M = mod_local(*c.p, it.m);
     const int nt = c.nt, decode = c.decode, y_bf16 = c.y_bf16, n_cta = c.n_cta;
     const int64_t total_iters = c.total_iters;
@@ -697,23 +704,53 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
     const int row0 = it.chunk * nt;
     const int ncols = decode ? c.n : min(nt, c.n - row0);
     const int ncols16 = (ncols + 15) & ~15;
-    const int oo = it.w_tile * kBM + c.o;
-    const bool o_ok = oo < M.d_out;
+    const int o0 = it.w_tile * kBM;
+    const int orows = min(kBM, M.d_out - o0);  // valid lanes of this tile
     const bool head = it.kb0 == 0;
     const uint32_t lane_off = (uint32_t)c.lane_base << 16;
     const uint32_t tacc = c.tmem_base + lane_off + (uint32_t)(buf * nt);
     const uint32_t tdel = c.tmem_base + lane_off + c.delta_col + (uint32_t)(buf * nt);
     const size_t slot_elems = (size_t)kBM * nt;
+    const bool leader = c.etid == 0;
+
+    // one 16-column chunk of values -> staging buffer -> bulk store(s)
+    auto emit = [&](int c0, const float (&v)[16], float *part_dst) {
+        const int b = n_out & 1;
+        if (n_out >= 2 && leader) bulk_wait_read<1>();  // the store from two chunks ago has read b
+        named_bar_sync(1, 128);
+        uint8_t *ob = b ? db.obuf[1] : db.obuf[0];
+        if (part_dst || !y_bf16) {
+            float *f = reinterpret_cast<float *>(ob);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i * kBM + c.o] = v[i];
+        } else {
+            uint16_t *h = reinterpret_cast<uint16_t *>(ob);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) h[i * kBM + c.o] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+            if (part_dst) {
+                bulk_store(part_dst + (size_t)c0 * kBM, ob, 16 * kBM * 4);
+            } else {
+                const int esz = y_bf16 ? 2 : 4;
+                for (int i = 0; i < 16 && c0 + i < ncols; ++i) {
+                    const int row = decode ? c0 + i : row0 + c0 + i;
+                    uint8_t *dst = reinterpret_cast<uint8_t *>(M.y) + ((size_t)row * M.d_out + o0) * esz;
+                    bulk_store(dst, ob + (size_t)i * kBM * esz, (uint32_t)(orows * esz));
+                }
+            }
+            bulk_commit();
+        }
+        ++n_out;
+    };
 
     if (head && it.kb1 == it.kbn) {
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
             own_cols16(c, tacc, tdel, true, c0, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int col = c0 + i;
-                if (col < ncols && o_ok) store_y(M.y, M.d_out, y_bf16, decode ? col : row0 + col, oo, v[i]);
-            }
+            emit(c0, v, nullptr);
         }
         return;
     }
@@ -722,101 +759,87 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
     const int c_first = (int)(((it.it0 + 1) * n_cta - 1) / total_iters);  // CTA holding iteration it0
     const int c_last = (int)(((it.it0 + it.kbn) * n_cta - 1) / total_iters);
     const int nc = c_last - c_first + 1;
+    const int self_idx = (int)blockIdx.x - c_first;
     int32_t *counter = c.tile_counters + it.tile;
+    auto part_of = [&](int cta) -> float * {  // [column][lane] piece of CTA `cta`
+        const int64_t b_c = (int64_t)cta * total_iters / n_cta;
+        return partials + ((size_t)cta * 2 + ((b_c >= it.it0) ? 0 : 1)) * slot_elems;
+    };
     bool finalize = false;
-    if (head) {  // the head usually arrives last: finish directly if everyone else is in
-        if (c.etid == 0) *misc_flag = (atomicAdd(counter, 0) == nc - 1);
+    if (head) {
+        if (leader) {
+            const uint64_t t0 = globaltimer();
+            int seen = ld_acquire_gpu(counter);
+            while (seen != nc - 1 && globaltimer() - t0 < kHeadWaitNs) seen = ld_acquire_gpu(counter);
+            *misc_flag = (seen == nc - 1);
+        }
         named_bar_sync(1, 128);
         finalize = *misc_flag != 0;
         named_bar_sync(1, 128);
     }
-    auto part_row = [&](int cta) -> float * {
-        const int64_t b_c = (int64_t)cta * total_iters / n_cta;
-        const int sl = (b_c >= it.it0) ? 0 : 1;
-        return partials + ((size_t)cta * 2 + sl) * slot_elems + (size_t)c.o * nt;
-    };
     if (!finalize) {
-        float4 *dst = reinterpret_cast<float4 *>(part_row(blockIdx.x));
+        float *dst = part_of(blockIdx.x);
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
             own_cols16(c, tacc, tdel, head, c0, v);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[c0 / 4 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            emit(c0, v, dst);
         }
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (c.etid == 0) *misc_flag = (atomicAdd(counter, 1) == nc - 1);
+        if (leader) {
+            bulk_wait<0>();  // the piece is in global memory
+            fence_proxy_async_global();
+            __threadfence();
+            *misc_flag = (atomicAdd(counter, 1) == nc - 1);
+        }
         named_bar_sync(1, 128);
         finalize = *misc_flag != 0;
         named_bar_sync(1, 128);
     }
     if (!finalize) return;
     __threadfence();
-    // the other pieces' loads for chunk c0 + 16 are issued before chunk c0 is added up
-    float4 cur[kPrefetchParts][4], nxt[kPrefetchParts][4];
-    // k-th contributor other than this CTA (this CTA is one of c_first..c_last)
-    const int self_idx = (int)blockIdx.x - c_first;
-    auto other = [&](int k) { return c_first + k + (k >= self_idx ? 1 : 0); };
-    auto fetch = [&](int c0, float4 (&dst)[kPrefetchParts][4]) {
-#pragma unroll
-        for (int k = 0; k < kPrefetchParts; ++k) {
-            if (k < nc - 1 && c0 < ncols16) {
-                const float4 *src = reinterpret_cast<const float4 *>(part_row(other(k))) + c0 / 4;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dst[k][i] = __ldcg(src + i);
-            }
-        }
+    fence_proxy_async_global();  // the pieces were written through the async proxy
+
+    // finish: other pieces arrive chunk by chunk through ibuf[2] (bulk loads, one ahead)
+    const int others = nc - 1;
+    const int n_loads = others * (ncols16 / 16);
+    auto issue_load = [&](int l) {  // load l = (chunk l / others, other l % others)
+        if (!leader || l >= n_loads) return;
+        const uint32_t g = *db.ld_count + (uint32_t)l;
+        const int k = l % others, c0 = (l / others) * 16;
+        const float *src = part_of(c_first + k + (k >= self_idx ? 1 : 0)) + (size_t)c0 * kBM;
+        uint64_t *bar = db.ld_bar + (g & 1);
+        mbar_arrive_expect_tx(bar, 16 * kBM * 4);
+        bulk_load((g & 1) ? db.ibuf[1] : db.ibuf[0], src, 16 * kBM * 4, bar);
     };
-    fetch(0, cur);
+    issue_load(0);
+    issue_load(1);
+    int l = 0;
     for (int c0 = 0; c0 < ncols16; c0 += 16) {
-        fetch(c0 + 16, nxt);
         float own[16], sum[16];
         own_cols16(c, tacc, tdel, head, c0, own);
         for (int jc = 0; jc < nc; ++jc) {
-            const int cc = c_first + jc;
-            float v[16];
-            const int k_other = jc - (jc > self_idx ? 1 : 0);
-            if (cc == (int)blockIdx.x) {
+            if (jc == self_idx) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = own[i];
-            } else if (k_other < kPrefetchParts) {
-#pragma unroll
-                for (int jp = 0; jp < kPrefetchParts; ++jp) {
-                    if (jp == k_other) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            v[4 * i] = cur[jp][i].x;
-                            v[4 * i + 1] = cur[jp][i].y;
-                            v[4 * i + 2] = cur[jp][i].z;
-                            v[4 * i + 3] = cur[jp][i].w;
-                        }
-                    }
-                }
+                for (int i = 0; i < 16; ++i) sum[i] = (jc == 0) ? own[i] : sum[i] + own[i];
             } else {
-                const float4 *src = reinterpret_cast<const float4 *>(part_row(cc)) + c0 / 4;
+                const uint32_t g = *db.ld_count + (uint32_t)l;
+                // bounded wait; a timeout has already raised the abort flag and recorded it
+                mbar_wait(db.ld_bar + (g & 1), (g >> 1) & 1, abort_flag, nullptr);
+                const float *f = reinterpret_cast<const float *>((g & 1) ? db.ibuf[1] : db.ibuf[0]);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float4 t = __ldcg(src + i);
-                    v[4 * i] = t.x;
-                    v[4 * i + 1] = t.y;
-                    v[4 * i + 2] = t.z;
-                    v[4 * i + 3] = t.w;
+                for (int i = 0; i < 16; ++i) {
+                    const float v = f[i * kBM + c.o];
+                    sum[i] = (jc == 0) ? v : sum[i] + v;
                 }
+                named_bar_sync(1, 128);  // everyone has read the buffer
+                issue_load(l + 2);
+                ++l;
             }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) sum[i] = (jc == 0) ? v[i] : sum[i] + v[i];
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int col = c0 + i;
-            if (col < ncols && o_ok) store_y(M.y, M.d_out, y_bf16, decode ? col : row0 + col, oo, sum[i]);
-        }
-#pragma unroll
-        for (int jc = 0; jc < kPrefetchParts; ++jc)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) cur[jc][i] = nxt[jc][i];
+        emit(c0, sum, nullptr);
     }
-    if (c.etid == 0) *counter = 0;
+    if (leader) *db.ld_count += (uint32_t)n_loads;
+    named_bar_sync(1, 128);
+    if (leader) *counter = 0;
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -835,7 +858,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     uint64_t *acc_full = empty + S;
     uint64_t *acc_free = acc_full + 2;
     uint64_t *mma_done = acc_free + 2;
-    uint32_t *misc = reinterpret_cast<uint32_t *>(mma_done + 1);  // [0] tmem, [1] abort, [2] flag
+    uint64_t *ld_bar = mma_done + 1;  // [2] drain: other pieces' chunk loads
+    uint32_t *misc = reinterpret_cast<uint32_t *>(ld_bar + 2);  // [0] tmem, [1] abort, [2] flag, [3] loads
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -848,6 +872,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             mbar_init(acc_free + b, kEpiWarps);
         }
         mbar_init(mma_done, 1);
+        mbar_init(ld_bar, 1);
+        mbar_init(ld_bar + 1, 1);
+        misc[3] = 0;
         misc[1] = 0;
         misc[2] = 0;
         meta->module = -1;
@@ -960,6 +987,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         c.y_bf16 = p.y_bf16;
         c.n_cta = p.n_cta;
         c.rpmax = p.rpmax;
+        c.ring_chunks = p.ring_chunks;
         c.total_iters = p.total_iters;
         c.partials = p.partials;
         c.tile_counters = p.tile_counters;
@@ -968,6 +996,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         c.seg_adapter = p.seg_adapter;
         c.n_seg = p.n_seg;
         volatile int *flag = reinterpret_cast<volatile int *>(misc + 2);
+        DrainBufs db;
+        db.obuf[0] = ring;
+        db.obuf[1] = ring + 8192;
+        db.ibuf[0] = ring + 16384;
+        db.ibuf[1] = ring + 24576;
+        db.ld_bar = ld_bar;
+        db.ld_count = misc + 3;
+        uint32_t n_out = 0;
         // The expand of a tile this CTA heads is prepared one item ahead when there are two
         // accumulator/delta buffer pairs, so it overlaps the MMAs of the item before it.
         Sched sc;
@@ -983,15 +1019,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             const bool full_ok = mbar_wait(acc_full + buf, (li / NB) & 1, abort_flag, p.err);
             if (named_bar_or(1, 128, !full_ok)) break;
             tc_fence_after();
-            drain(c, cur, buf, flag);
+            drain(c, cur, buf, flag, abort_flag, db, n_out);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_free + buf);
+            // the staging buffers live in the ring, which the next expand reuses
+            if (c.etid == 0) bulk_wait_read<0>();
+            named_bar_sync(1, 128);
             if (has_nxt && NB == 1 && nxt.kb0 == 0) init_expand(c, nxt, 0);
             cur = nxt;
             has_cur = has_nxt;
             ++li;
         }
+        if (c.etid == 0) bulk_wait<0>();  // every output store has been performed
     }
     tc_fence_before();
     __syncthreads();
@@ -1007,7 +1047,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 size_t gemm_smem_bytes(int nt, int n_stages, int ring_chunks, int rpmax) {
     const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2;
     return 1024 + stage * n_stages + (size_t)ring_chunks * 128 * 16 + (size_t)16 * rpmax * 4 + sizeof(EpiMeta) +
-           8 * (2 * (size_t)n_stages + 5) + 16;
+           8 * (2 * (size_t)n_stages + 7) + 16;
 }
 
 cudaError_t launch_prep_decode(const PrepParams &p, cudaStream_t s) {
