@@ -104,8 +104,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
 // 2-D bf16 tensor [rows, cols] (row-major), box {64 cols, box_rows rows}, 128-byte swizzle.
-int make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_rows) {
+int lora::make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_rows) {
     auto fn = encode_fn();
     if (!fn) {
         g_last_cuda_error = "cuTensorMapEncodeTiled unavailable";
@@ -125,9 +129,28 @@ int make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int
     return LORA_OK;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
-}  // namespace
+// Output y [n, d_out] (row-major, fp32 or bf16), box {128 outputs, 16 rows}, no swizzle: the
+// shared-memory side is a dense [16][128] block.  Rows past n and columns past d_out are clipped.
+int lora::make_tmap_y(CUtensorMap *tm, void *y, int64_t n, int64_t d_out, bool bf16) {
+    auto fn = encode_fn();
+    if (!fn) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled unavailable";
+        return LORA_ECUDA;
+    }
+    const int esz = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)d_out, (cuuint64_t)(n > 0 ? n : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)d_out * esz};
+    cuuint32_t box[2] = {128, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled (y) failed (" + std::to_string((int)r) + ")";
+        return LORA_ECUDA;
+    }
+    return LORA_OK;
+}
 
 struct lora_pool {
     int device = 0;
@@ -555,6 +578,8 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
         int rc = make_tmap(&gm.tmW, io[i].W, ms.d_out, ms.d_in, kBM);
         if (rc) return rc;
         rc = make_tmap(&gm.tmX, io[i].x, n, ms.d_in, gp.nt);
+        if (rc) return rc;
+        rc = make_tmap_y(&gm.tmY, io[i].y, n, ms.d_out, y_dtype == LORA_DTYPE_BF16);
         if (rc) return rc;
         gm.y = io[i].y;
         gm.T = sp.T[i];

@@ -37,6 +37,7 @@ constexpr int kShrinkDecRows = 4;     // decode shrink: rows sharing one registe
 struct GemmModule {
     CUtensorMap tmW;  // W [d_out, d_in]: box {64, 128}, 128B swizzle
     CUtensorMap tmX;  // X [n, d_in]:    box {64, nt},  128B swizzle
+    CUtensorMap tmY;  // y [n, d_out]:   box {128, 16}, fp32 or bf16, no swizzle (epilogue stores)
     void *y;
     const float *T;            // scaled shrink result, sorted positions, [n][rpmax]
     const PoolEntry *table;    // this module's entries [max_adapters]
@@ -112,6 +113,13 @@ struct PrepParams {
     int32_t *n_seg;
     int32_t *err;
 };
+
+static_assert(sizeof(GemmParams) <= 32764, "gemm parameters exceed the kernel parameter space");
+
+// tensor maps (lora_api.cu): bf16 [rows, cols] operand, box {64, box_rows}, 128-byte swizzle; and
+// the output y [n, d_out] (fp32 or bf16), box {128, 16}, for the epilogue's TMA stores
+int make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_rows);
+int make_tmap_y(CUtensorMap *tm, void *y, int64_t n, int64_t d_out, bool bf16);
 
 // launchers (lora_kernels.cu)
 cudaError_t launch_prep_decode(const PrepParams &p, cudaStream_t s);

@@ -508,6 +508,7 @@ struct EpiCtx {
 };
 
 struct ModLocal {
+    const CUtensorMap *tmY;
     void *y;
     const float *T;
     const PoolEntry *table;
@@ -515,7 +516,7 @@ struct ModLocal {
 };
 __device__ __forceinline__ ModLocal mod_local(const GemmParams &p, int m) {
     const GemmModule &M = p.mod[m];
-    return ModLocal{M.y, M.T, M.table, M.d_out};
+    return ModLocal{&M.tmY, M.y, M.T, M.table, M.d_out};
 }
 
 // (Re)build the per-column metadata of a tile from the segment table: every row of the tile's
@@ -677,26 +678,38 @@ __device__ __forceinline__ void own_cols16(const EpiCtx &c, uint32_t tacc, uint3
 }
 
 
-// Drain: accumulator (+ expand delta when this CTA heads the tile) -> y.  Output goes through
-// shared memory and the TMA engine: the 128 lanes of a 16-column chunk are written to a
-// [column][lane] buffer and one thread issues bulk stores (a y row segment per column, or one
-// contiguous 8 KiB block of a partial tile), double-buffered.  A tile split over several CTAs
-// (stream-K) is finished by one CTA that adds the pieces in k order, so the sum never depends
-// on timing.  The piece holding k-block 0 is always the last item of its CTA and the other
-// pieces are the first items of theirs, so that CTA waits (bounded) for the others and then
-// finishes the tile without writing its own piece; if the wait runs out it falls back to
-// "write your piece, last to arrive finishes".
+// Partial tiles (stream-K pieces) are kept in column quads: element (column c, lane o) at
+// ((c / 4) * 128 + o) * 4 + c % 4.  A thread's 16 columns are four 16-byte vectors and a warp
+// stores or loads 512 contiguous bytes per instruction.
+__device__ __forceinline__ float4 *piece_quads(float *piece, int c0, int o) {
+    return reinterpret_cast<float4 *>(piece) + (size_t)(c0 >> 2) * kBM + o;
+}
+
+// Drain: accumulator (+ expand delta when this CTA heads the tile) -> y.  y goes out through
+// shared memory and TMA tensor stores of [16 columns][128 lanes] blocks: the blocks of a round
+// are staged together (the round is as many blocks as the staging buffer holds), then one
+// barrier and the round's stores back to back.
+//
+// A tile split over several CTAs (stream-K) is finished by one CTA that adds the pieces in k
+// order, so the sum never depends on timing.  The piece holding k-block 0 is always the last
+// item of its CTA and the other pieces are the first items of theirs, so that CTA waits
+// (bounded) for the others and then finishes the tile without writing its own piece; if the
+// wait runs out it falls back to "write your piece, last to arrive finishes".  Pieces go to
+// global memory with plain vector stores; the finishing CTA pulls the other pieces into its idle
+// stage buffers with bulk copies when it can, else reads them with vector loads.
 struct DrainBufs {
-    uint8_t *obuf[2];   // output staging, 8 KiB each
-    uint8_t *ibuf[2];   // other pieces' chunks, 8 KiB each
-    uint64_t *ld_bar;   // [2] completion of the ibuf loads
-    uint32_t *ld_count; // loads issued so far by this CTA (parity of ld_bar)
+    uint8_t *ybuf;       // y staging (the expand ring, idle during a drain)
+    uint32_t ybuf_bytes;
+    uint8_t *stage;      // the stage buffers, free once the CTA's last item has been multiplied
+    uint32_t stage_bytes;
+    uint64_t *ld_bar;    // completion of the bulk copies of other pieces
+    uint32_t ld_phase;   // phases of ld_bar completed so far
 };
 
 constexpr uint64_t kHeadWaitNs = 50000;  // how long a finishing CTA waits for the other pieces
 
-__device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_flag, volatile int *abort_flag,
-                      DrainBufs &db, uint32_t &n_out) {
+__device__ void drain(EpiCtx &c, const Item &it, int buf, bool last, volatile int *misc_flag,
+                      volatile int *abort_flag, DrainBufs &db) {
     const ModLocal M = mod_local(*c.p, it.m);
     const int nt = c.nt, decode = c.decode, y_bf16 = c.y_bf16, n_cta = c.n_cta;
     const int64_t total_iters = c.total_iters;
@@ -705,52 +718,53 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
     const int ncols = decode ? c.n : min(nt, c.n - row0);
     const int ncols16 = (ncols + 15) & ~15;
     const int o0 = it.w_tile * kBM;
-    const int orows = min(kBM, M.d_out - o0);  // valid lanes of this tile
     const bool head = it.kb0 == 0;
     const uint32_t lane_off = (uint32_t)c.lane_base << 16;
     const uint32_t tacc = c.tmem_base + lane_off + (uint32_t)(buf * nt);
     const uint32_t tdel = c.tmem_base + lane_off + c.delta_col + (uint32_t)(buf * nt);
     const size_t slot_elems = (size_t)kBM * nt;
     const bool leader = c.etid == 0;
+    const uint32_t esz = y_bf16 ? 2u : 4u;
+    const uint32_t piece_bytes = (uint32_t)ncols16 * kBM * 4;
 
-    // one 16-column chunk of values -> staging buffer -> bulk store(s)
-    auto emit = [&](int c0, const float (&v)[16], float *part_dst) {
-        const int b = n_out & 1;
-        if (n_out >= 2 && leader) bulk_wait_read<1>();  // the store from two chunks ago has read b
-        named_bar_sync(1, 128);
-        uint8_t *ob = b ? db.obuf[1] : db.obuf[0];
-        if (part_dst || !y_bf16) {
-            float *f = reinterpret_cast<float *>(ob);
+    // y staging for a block of 16 columns at `dst` ([column][lane], fp32 or bf16)
+    auto put16 = [&](uint8_t *dst, const float (&v)[16]) {
+        if (!y_bf16) {
+            float *f = reinterpret_cast<float *>(dst);
 #pragma unroll
             for (int i = 0; i < 16; ++i) f[i * kBM + c.o] = v[i];
         } else {
-            uint16_t *h = reinterpret_cast<uint16_t *>(ob);
+            uint16_t *h = reinterpret_cast<uint16_t *>(dst);
 #pragma unroll
             for (int i = 0; i < 16; ++i) h[i * kBM + c.o] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
         }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (leader) {
-            if (part_dst) {
-                bulk_store(part_dst + (size_t)c0 * kBM, ob, 16 * kBM * 4);
-            } else {
-                const int esz = y_bf16 ? 2 : 4;
-                for (int i = 0; i < 16 && c0 + i < ncols; ++i) {
-                    const int row = decode ? c0 + i : row0 + c0 + i;
-                    uint8_t *dst = reinterpret_cast<uint8_t *>(M.y) + ((size_t)row * M.d_out + o0) * esz;
-                    bulk_store(dst, ob + (size_t)i * kBM * esz, (uint32_t)(orows * esz));
-                }
-            }
-            bulk_commit();
+    };
+    // block c0 of y: into its slot of the current round; the round's stores go out when it is full
+    const uint32_t block_bytes = 16u * kBM * esz;
+    const int round_blocks = (int)(db.ybuf_bytes / block_bytes);
+    auto emit = [&](int c0, const float (&v)[16]) {
+        const int slot = (c0 >> 4) % round_blocks;
+        if (slot == 0) {  // the previous round's stores must have read the buffer
+            if (leader) bulk_wait_read<0>();
+            named_bar_sync(1, 128);
         }
-        ++n_out;
+        put16(db.ybuf + (size_t)slot * block_bytes, v);
+        if (slot == round_blocks - 1 || c0 + 16 >= ncols16) {
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (leader) {
+                for (int k = 0; k <= slot; ++k)
+                    tma_store_2d(M.tmY, db.ybuf + (size_t)k * block_bytes, o0, row0 + c0 - 16 * (slot - k));
+                bulk_commit();
+            }
+        }
     };
 
     if (head && it.kb1 == it.kbn) {
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
             own_cols16(c, tacc, tdel, true, c0, v);
-            emit(c0, v, nullptr);
+            emit(c0, v);
         }
         return;
     }
@@ -761,7 +775,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
     const int nc = c_last - c_first + 1;
     const int self_idx = (int)blockIdx.x - c_first;
     int32_t *counter = c.tile_counters + it.tile;
-    auto part_of = [&](int cta) -> float * {  // [column][lane] piece of CTA `cta`
+    auto part_of = [&](int cta) -> float * {  // the piece of CTA `cta`
         const int64_t b_c = (int64_t)cta * total_iters / n_cta;
         return partials + ((size_t)cta * 2 + ((b_c >= it.it0) ? 0 : 1)) * slot_elems;
     };
@@ -782,63 +796,61 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, volatile int *misc_fla
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
             own_cols16(c, tacc, tdel, head, c0, v);
-            emit(c0, v, dst);
+            float4 *q = piece_quads(dst, c0, c.o);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) __stcg(q + k * kBM, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
         }
-        if (leader) {
-            bulk_wait<0>();  // the piece is in global memory
-            fence_proxy_async_global();
-            __threadfence();
-            *misc_flag = (atomicAdd(counter, 1) == nc - 1);
-        }
+        __threadfence();  // this thread's share of the piece is visible device-wide
+        named_bar_sync(1, 128);
+        if (leader) *misc_flag = (atomicAdd(counter, 1) == nc - 1);
         named_bar_sync(1, 128);
         finalize = *misc_flag != 0;
         named_bar_sync(1, 128);
+        if (!finalize) return;
     }
-    if (!finalize) return;
     __threadfence();
-    fence_proxy_async_global();  // the pieces were written through the async proxy
 
-    // finish: other pieces arrive chunk by chunk through ibuf[2] (bulk loads, one ahead)
-    const int others = nc - 1;
-    const int n_loads = others * (ncols16 / 16);
-    auto issue_load = [&](int l) {  // load l = (chunk l / others, other l % others)
-        if (!leader || l >= n_loads) return;
-        const uint32_t g = *db.ld_count + (uint32_t)l;
-        const int k = l % others, c0 = (l / others) * 16;
-        const float *src = part_of(c_first + k + (k >= self_idx ? 1 : 0)) + (size_t)c0 * kBM;
-        uint64_t *bar = db.ld_bar + (g & 1);
-        mbar_arrive_expect_tx(bar, 16 * kBM * 4);
-        bulk_load((g & 1) ? db.ibuf[1] : db.ibuf[0], src, 16 * kBM * 4, bar);
-    };
-    issue_load(0);
-    issue_load(1);
-    int l = 0;
+    // finish: the other pieces, staged in shared memory when the stage buffers are idle
+    const uint32_t others_bytes = (uint32_t)(nc - 1) * piece_bytes;
+    const bool staged = last && (uint64_t)others_bytes <= db.stage_bytes;
+    if (staged) {
+        fence_proxy_async_global();  // the pieces were written through the generic proxy
+        if (leader) {
+            mbar_arrive_expect_tx(db.ld_bar, others_bytes);
+            for (int k = 0, j = 0; k < nc; ++k)
+                if (k != self_idx) bulk_load(db.stage + (size_t)(j++) * piece_bytes, part_of(c_first + k), piece_bytes, db.ld_bar);
+        }
+        // bounded wait; a timeout has already raised the abort flag
+        mbar_wait(db.ld_bar, db.ld_phase & 1, abort_flag, nullptr);
+        ++db.ld_phase;
+    }
+    const uint32_t pbase = smem_u32(db.stage) + (uint32_t)c.o * 16;  // this lane's quad of piece 0, block 0
     for (int c0 = 0; c0 < ncols16; c0 += 16) {
         float own[16], sum[16];
         own_cols16(c, tacc, tdel, head, c0, own);
-        for (int jc = 0; jc < nc; ++jc) {
+        for (int jc = 0, j = 0; jc < nc; ++jc) {
+            float4 q[4];
             if (jc == self_idx) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) sum[i] = (jc == 0) ? own[i] : sum[i] + own[i];
-            } else {
-                const uint32_t g = *db.ld_count + (uint32_t)l;
-                // bounded wait; a timeout has already raised the abort flag and recorded it
-                mbar_wait(db.ld_bar + (g & 1), (g >> 1) & 1, abort_flag, nullptr);
-                const float *f = reinterpret_cast<const float *>((g & 1) ? db.ibuf[1] : db.ibuf[0]);
+                for (int k = 0; k < 4; ++k) q[k] = make_float4(own[4 * k], own[4 * k + 1], own[4 * k + 2], own[4 * k + 3]);
+            } else if (staged) {
+                const uint32_t a = pbase + (uint32_t)(j++) * piece_bytes + (uint32_t)(c0 >> 2) * kBM * 16;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float v = f[i * kBM + c.o];
-                    sum[i] = (jc == 0) ? v : sum[i] + v;
-                }
-                named_bar_sync(1, 128);  // everyone has read the buffer
-                issue_load(l + 2);
-                ++l;
+                for (int k = 0; k < 4; ++k) q[k] = lds128(a + (uint32_t)k * kBM * 16);
+            } else {
+                const float4 *src = piece_quads(part_of(c_first + jc), c0, c.o);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) q[k] = __ldcg(src + k * kBM);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float a[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sum[4 * k + e] = jc == 0 ? a[e] : sum[4 * k + e] + a[e];
             }
         }
-        emit(c0, sum, nullptr);
+        emit(c0, sum);
     }
-    if (leader) *db.ld_count += (uint32_t)n_loads;
-    named_bar_sync(1, 128);
     if (leader) *counter = 0;
 }
 
@@ -858,8 +870,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     uint64_t *acc_full = empty + S;
     uint64_t *acc_free = acc_full + 2;
     uint64_t *mma_done = acc_free + 2;
-    uint64_t *ld_bar = mma_done + 1;  // [2] drain: other pieces' chunk loads
-    uint32_t *misc = reinterpret_cast<uint32_t *>(ld_bar + 2);  // [0] tmem, [1] abort, [2] flag, [3] loads
+    uint64_t *ld_bar = mma_done + 1;  // drain: bulk copies of other pieces
+    uint32_t *misc = reinterpret_cast<uint32_t *>(ld_bar + 2);  // [0] tmem, [1] abort, [2] flag
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -873,8 +885,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
         mbar_init(mma_done, 1);
         mbar_init(ld_bar, 1);
-        mbar_init(ld_bar + 1, 1);
-        misc[3] = 0;
         misc[1] = 0;
         misc[2] = 0;
         meta->module = -1;
@@ -997,13 +1007,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         c.n_seg = p.n_seg;
         volatile int *flag = reinterpret_cast<volatile int *>(misc + 2);
         DrainBufs db;
-        db.obuf[0] = ring;
-        db.obuf[1] = ring + 8192;
-        db.ibuf[0] = ring + 16384;
-        db.ibuf[1] = ring + 24576;
+        db.ybuf = ring;
+        db.ybuf_bytes = (uint32_t)p.ring_chunks * 128 * 16;
+        db.stage = smem;
+        db.stage_bytes = (uint32_t)S * stage_bytes;
         db.ld_bar = ld_bar;
-        db.ld_count = misc + 3;
-        uint32_t n_out = 0;
+        db.ld_phase = 0;
         // The expand of a tile this CTA heads is prepared one item ahead when there are two
         // accumulator/delta buffer pairs, so it overlaps the MMAs of the item before it.
         Sched sc;
@@ -1019,7 +1028,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             const bool full_ok = mbar_wait(acc_full + buf, (li / NB) & 1, abort_flag, p.err);
             if (named_bar_or(1, 128, !full_ok)) break;
             tc_fence_after();
-            drain(c, cur, buf, flag, abort_flag, db, n_out);
+            drain(c, cur, buf, !has_nxt, flag, abort_flag, db);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_free + buf);

@@ -70,32 +70,6 @@ __global__ void static_table_kernel(PoolEntry *table, const uint16_t *A, const u
         table[a] = PoolEntry{A + (size_t)a * rank * d_in, B + (size_t)a * d_out * rank, rank, rank, 0};
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-bool tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Returns `status` and leaves the reason where lora_last_cuda_error() reads it.
 int fail(int status, const std::string &why) {
     set_last_error(why);
@@ -217,8 +191,9 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     gp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
     gp.raster_group = 8;
     GemmModule &gm = gp.mod[0];
-    if (!tmap(&gm.tmW, W, d_out, d_in, kBM) || !tmap(&gm.tmX, x, n, d_in, gp.nt))
-        return fail(LORA_ECUDA, "cuTensorMapEncodeTiled failed");
+    if (make_tmap(&gm.tmW, W, d_out, d_in, kBM) || make_tmap(&gm.tmX, x, n, d_in, gp.nt) ||
+        make_tmap_y(&gm.tmY, y, n, d_out, y_dtype == LORA_DTYPE_BF16))
+        return LORA_ECUDA;  // the reason is already recorded
     gm.y = y;
     gm.T = T;
     gm.table = table;
