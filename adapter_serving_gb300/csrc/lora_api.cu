@@ -168,6 +168,13 @@ struct lora_pool {
     int32_t *shrink_cnt = nullptr;    // [LORA_MAX_MODULES][256]
     float *gemm_part = nullptr;       // [num_sms][2][128 * 256]
     int32_t *tile_cnt = nullptr;      // [tile_cap]
+    BPackG *packs = nullptr;          // [LORA_MAX_MODULES][kMaxPacks] decode expand packs
+    int32_t *tpos = nullptr;          // [LORA_MAX_MODULES][256] decode: t row of each position
+    int32_t *n_packs = nullptr;       // [LORA_MAX_MODULES]
+    float *Tp = nullptr;              // [LORA_MAX_MODULES][kPackedTFloats] decode: packed t
+    int32_t *chunk_seg0 = nullptr;    // [chunk_cap] grouped rows: first segment of each chunk
+    int32_t *chunk_nb = nullptr;      // [chunk_cap] grouped rows: expand slots of each chunk
+    int chunk_cap = 0;
     int ks_cap = 0, tile_cap = 0;
     // kernel timing: pending event pairs per kernel kind
     bool profiling = false;
@@ -283,6 +290,7 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
     p->ks_cap = (max_din + 511) / 512;
     p->tile_cap = LORA_MAX_MODULES * ((max_dout + kBM - 1) / kBM);
     const size_t R = (size_t)p->max_rows;
+    p->chunk_cap = (int)(R / 256 + 2);
     if ((rc = dev_alloc(p, (void **)&p->perm, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->seg_start, (R + 2) * 4)) ||
         (rc = dev_alloc(p, (void **)&p->seg_adapter, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->n_seg, 16)) ||
         (rc = dev_alloc(p, (void **)&p->err, 16)) ||
@@ -291,7 +299,13 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
                         (size_t)LORA_MAX_MODULES * p->ks_cap * LORA_MAX_DECODE_ROWS * LORA_MAX_RANK * 4)) ||
         (rc = dev_alloc(p, (void **)&p->shrink_cnt, (size_t)LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS * 4)) ||
         (rc = dev_alloc(p, (void **)&p->gemm_part, (size_t)p->num_sms * 2 * kBM * 256 * 4)) ||
-        (rc = dev_alloc(p, (void **)&p->tile_cnt, (size_t)p->tile_cap * 4))) {
+        (rc = dev_alloc(p, (void **)&p->tile_cnt, (size_t)p->tile_cap * 4)) ||
+        (rc = dev_alloc(p, (void **)&p->packs, sizeof(BPackG) * LORA_MAX_MODULES * kMaxPacks)) ||
+        (rc = dev_alloc(p, (void **)&p->tpos, (size_t)4 * LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS)) ||
+        (rc = dev_alloc(p, (void **)&p->n_packs, (size_t)4 * LORA_MAX_MODULES)) ||
+        (rc = dev_alloc(p, (void **)&p->Tp, (size_t)4 * LORA_MAX_MODULES * kPackedTFloats)) ||
+        (rc = dev_alloc(p, (void **)&p->chunk_seg0, (size_t)4 * p->chunk_cap)) ||
+        (rc = dev_alloc(p, (void **)&p->chunk_nb, (size_t)4 * p->chunk_cap))) {
         lora_pool_destroy(p);
         return rc;
     }
@@ -515,13 +529,27 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     pp.seg_adapter = p->seg_adapter;
     pp.n_seg = p->n_seg;
     pp.err = p->err;
+    const int nt = decode ? ((n + 15) & ~15) : 256;  // rows per MMA tile (MMA N)
+    const int rpmax = p->rpmax();
+    if (decode) {
+        for (int i = 0; i < n_io; ++i) {
+            pp.packs[i] = p->packs + (size_t)i * kMaxPacks;
+            pp.tpos[i] = p->tpos + (size_t)i * LORA_MAX_DECODE_ROWS;
+        }
+        pp.n_packs = p->n_packs;
+        pp.pack_ch = pack_ch(nt);
+    } else {
+        if ((n + nt - 1) / nt > p->chunk_cap) return LORA_EUNSUPPORTED;
+        pp.nt = nt;
+        pp.pf_ch = pf_ch(nt, rpmax);
+        pp.chunk_seg0 = p->chunk_seg0;
+        pp.chunk_nb = p->chunk_nb;
+    }
     e = timed_launch(p, LORA_KERNEL_PREP, s,
                      [&] { return decode ? launch_prep_decode(pp, s) : launch_prep_segments(pp, s); });
     if (e != cudaSuccess) return cuda_fail(e, "prep kernel");
     p->last_n = n;
     p->last_decode = decode;
-
-    const int rpmax = p->rpmax();
 
     // ---- shrink: T[m][q][:] = s * A_a x_row(q)
     ShrinkParams sp{};
@@ -546,7 +574,8 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
         const ModuleStore &ms = p->mod[io[i].module];
         sp.x[i] = static_cast<const uint16_t *>(io[i].x);
         sp.table[i] = pp.table[i];
-        sp.T[i] = p->T + (size_t)i * p->max_rows * LORA_MAX_RANK;
+        sp.T[i] = decode ? p->Tp + (size_t)i * kPackedTFloats : p->T + (size_t)i * p->max_rows * LORA_MAX_RANK;
+        sp.tpos[i] = decode ? pp.tpos[i] : nullptr;
         sp.d_in[i] = ms.d_in;
         sp.kc[i] = decode ? std::min(kc_dec, ms.d_in) : ms.d_in;
         sp.ksplit[i] = (ms.d_in + sp.kc[i] - 1) / sp.kc[i];
@@ -563,7 +592,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     memset(&gp, 0, sizeof gp);
     gp.n_mod = n_io;
     gp.n = n;
-    gp.nt = decode ? ((n + 15) & ~15) : 256;
+    gp.nt = nt;
     gp.n_chunks = (n + gp.nt - 1) / gp.nt;
     gp.decode = decode ? 1 : 0;
     gp.stream_k = gp.n_chunks == 1 ? 1 : 0;
@@ -584,11 +613,11 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
         gm.y = io[i].y;
         gm.T = sp.T[i];
         gm.table = pp.table[i];
+        gm.packs = decode ? pp.packs[i] : nullptr;
         gm.d_in = ms.d_in;
         gm.d_out = ms.d_out;
         gm.m_tiles = (ms.d_out + kBM - 1) / kBM;
         gm.k_blocks = (ms.d_in + kBK - 1) / kBK;
-        gm.iter_begin = iters;
         gm.tile_begin = tiles;
         const int mt = gm.m_tiles * gp.n_chunks;
         tiles += mt;
@@ -596,23 +625,19 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     }
     if (gp.stream_k && tiles > p->tile_cap) return LORA_EUNSUPPORTED;
     gp.total_tiles = tiles;
-    gp.total_iters = iters;
     if (gp.stream_k) {
         // every CTA gets at least 4 k-blocks, so all ranges are non-empty
         gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(p->num_sms, iters / 4));
     } else {
         gp.n_cta = std::min(p->num_sms, tiles);
     }
-    // TMEM: n_acc accumulator buffers of nt columns, then one expand-delta buffer per accumulator
-    gp.n_acc = 4 * gp.nt <= 512 ? 2 : 1;
-    gp.tmem_cols = 32;
-    while (gp.tmem_cols < 2 * gp.n_acc * gp.nt) gp.tmem_cols <<= 1;
-    // per-thread staging for the expand's B rows: small for low ranks, more for rank 64
-    gp.ring_chunks = rpmax <= 16 ? 16 : 32;
-    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)gp.nt * kBK * 2;
-    const size_t fixed = gemm_smem_bytes(gp.nt, 0, gp.ring_chunks, rpmax);
-    gp.n_stages = (int)std::min<size_t>(kMaxStages, (227 * 1024 - fixed - 16 * kMaxStages) / stage);
-    if (gp.n_stages < 2) return LORA_EUNSUPPORTED;
+    gp.n_packs = decode ? p->n_packs : nullptr;
+    gp.chunk_seg0 = decode ? nullptr : p->chunk_seg0;
+    gp.chunk_nb = decode ? nullptr : p->chunk_nb;
+    gp.pack_ch = pack_ch(nt);
+    gp.pf_ch = pf_ch(nt, rpmax);
+    size_t smem = 0;
+    if (!plan_gemm(gp, &smem)) return LORA_EUNSUPPORTED;
     gp.perm = p->perm;
     gp.seg_start = p->seg_start;
     gp.seg_adapter = p->seg_adapter;
@@ -620,7 +645,6 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     gp.partials = p->gemm_part;
     gp.tile_counters = p->tile_cnt;
     gp.err = p->err;
-    const size_t smem = gemm_smem_bytes(gp.nt, gp.n_stages, gp.ring_chunks, rpmax);
     e = timed_launch(p, LORA_KERNEL_GEMM, s, [&] { return launch_gemm(gp, smem, s); });
     if (e != cudaSuccess) return cuda_fail(e, "gemm kernel");
     return LORA_OK;

@@ -34,16 +34,70 @@ constexpr int kShrinkDecCh = 8;       // decode shrink: 16-byte chunks of A per 
 constexpr int kShrinkDecKC = 256 * kShrinkDecCh;  // decode shrink: K per block (split width)
 constexpr int kShrinkDecRows = 4;     // decode shrink: rows sharing one register load of A
 
+// ---- expand stages --------------------------------------------------------------------
+// The expand (delta = B_a t) of a tile runs from "B stages" that follow the tile's W k-blocks in
+// the same TMA ring: a stage holds the 128-row slices of B of a group of slots (a slot is one
+// adapter with a run of positions that use it) and those positions' t rows; the epilogue warps
+// compute the dot products from shared memory into the tile's TMEM delta buffer.
+
+constexpr int kPackRanks = 64;     // storage ranks per B stage (the stage's 16 KiB A buffer)
+constexpr int kPackSlots = kPackRanks / 8;
+constexpr int kStageHdrBytes = 256;  // slot header at the start of a B stage's X buffer
+constexpr int kYBufBytes = 32768;    // epilogue y staging
+
+// decode: one group of slots ("pack"), written by prep, read by the TMA producer
+struct BSlotG {
+    const uint16_t *B;  // adapter's B for this module, [d_out, rp]
+    uint16_t q0;        // first sorted position of the slot
+    uint8_t nrows;      // positions in the slot (<= pack_ch)
+    uint8_t rp;         // storage rank
+    uint8_t off;        // rank offset within the pack
+    uint8_t pad_[3];
+};
+static_assert(sizeof(BSlotG) == 16, "BSlotG layout");
+struct BPackG {
+    int32_t tbegin;   // first float of the pack's t rows in the module's packed T
+    int32_t tfloats;  // floats of t rows
+    int32_t nslots;
+    int32_t pad_;
+    BSlotG slot[kPackSlots];
+};
+static_assert(sizeof(BPackG) == 16 * (1 + kPackSlots), "BPackG layout");
+
+// shared-memory slot header of a B stage, written by the producer, read by the epilogue
+struct BSlotS {
+    int32_t q0;       // first position (decode: sorted position; grouped rows: row)
+    int16_t nrows;
+    int16_t rp;
+    int16_t off;      // rank offset: the slot's B rows start at off * 256 bytes of the A buffer
+    int16_t tstride;  // floats between consecutive t rows
+    int32_t toff;     // first float of the slot's t rows in the stage's t area
+};
+struct BStageHdr {
+    int32_t nslots;
+    int32_t singles8;  // every slot has rank 8 and one row (the epilogue's fast path)
+    int32_t pad_[2];
+    BSlotS slot[kPackSlots];
+};
+static_assert(sizeof(BStageHdr) <= kStageHdrBytes, "B stage header");
+
+// rows per decode slot: the t rows of a full pack must fit the X buffer after the header
+__host__ __device__ constexpr int pack_ch(int nt) { return nt / 2 - 1 < 8 ? nt / 2 - 1 : 8; }
+// packs of one module (decode, n <= 256 rows): at most one per slot
+constexpr int kMaxPacks = LORA_MAX_DECODE_ROWS + LORA_MAX_DECODE_ROWS / 7 + 1;
+// packed t of one module: pack_ch floats per rank unit, 64 units per pack
+constexpr size_t kPackedTFloats = (size_t)8 * kPackRanks * kMaxPacks;
+
 struct GemmModule {
     CUtensorMap tmW;  // W [d_out, d_in]: box {64, 128}, 128B swizzle
     CUtensorMap tmX;  // X [n, d_in]:    box {64, nt},  128B swizzle
     CUtensorMap tmY;  // y [n, d_out]:   box {128, 16}, fp32 or bf16, no swizzle (epilogue stores)
     void *y;
-    const float *T;            // scaled shrink result, sorted positions, [n][rpmax]
+    const float *T;            // shrink result: decode packed per pack, grouped rows [n][rpmax]
     const PoolEntry *table;    // this module's entries [max_adapters]
+    const BPackG *packs;       // decode: this module's packs
     int32_t d_in, d_out;
     int32_t m_tiles, k_blocks;
-    int64_t iter_begin;        // flattened (tile, k-block) index where this module starts
     int32_t tile_begin;        // first global tile index of this module
     int32_t pad_;
 };
@@ -58,11 +112,9 @@ struct GemmParams {
     int32_t stream_k;      // 1: contiguous (tile, k-block) ranges per CTA; 0: whole tiles round robin
     int32_t n_cta;
     int32_t total_tiles;
-    int64_t total_iters;
     int32_t rpmax;         // T row stride
     int32_t y_bf16;
     int32_t n_stages;
-    int32_t ring_chunks;   // per epilogue thread: 16-byte pieces of B rows staged per batch
     int32_t raster_group;  // W tiles per raster group (round robin)
     int32_t tmem_cols;
     int32_t n_acc;         // accumulator + delta buffer pairs in TMEM (2 when 4 * nt <= 512, else 1)
@@ -70,6 +122,11 @@ struct GemmParams {
     const int32_t *seg_start;
     const int32_t *seg_adapter;
     const int32_t *n_seg;
+    const int32_t *n_packs;     // decode: [n_mod] B stages per tile of each module
+    const int32_t *chunk_seg0;  // grouped rows: first segment touching each row chunk
+    const int32_t *chunk_nb;    // grouped rows: B stages (slots) of each row chunk
+    int32_t pack_ch;            // decode: positions per slot
+    int32_t pf_ch;              // grouped rows: positions per slot
     float *partials;       // [n_cta][2][kBM * nt]
     int32_t *tile_counters;
     int32_t *err;          // [0] code, [1] detail
@@ -94,6 +151,7 @@ struct ShrinkParams {
     const int32_t *seg_start;
     const int32_t *seg_adapter;
     const int32_t *n_seg;
+    const int32_t *tpos[LORA_MAX_MODULES];  // decode: where position q's t row starts in T
     float *partials;      // [n_mod][ks_max][n][rpmax]
     int32_t *counters;    // [n_mod][max_units]
 };
@@ -112,6 +170,16 @@ struct PrepParams {
     int32_t *seg_adapter;
     int32_t *n_seg;
     int32_t *err;
+    // decode: expand packs per module
+    BPackG *packs[LORA_MAX_MODULES];
+    int32_t *tpos[LORA_MAX_MODULES];  // [n] float offset of position q's t row in the packed T
+    int32_t *n_packs;                 // [n_mod]
+    int32_t pack_ch;
+    // grouped rows: per row chunk of nt rows
+    int32_t nt;
+    int32_t pf_ch;
+    int32_t *chunk_seg0;
+    int32_t *chunk_nb;
 };
 
 static_assert(sizeof(GemmParams) <= 32764, "gemm parameters exceed the kernel parameter space");
@@ -127,7 +195,16 @@ cudaError_t launch_prep_segments(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStream_t s);
 cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s);
-size_t gemm_smem_bytes(int nt, int n_stages, int ring_chunks, int rpmax);
+size_t gemm_smem_bytes(int nt, int n_stages);
+// TMEM buffers, stage count and shared memory of a gemm launch; false if no two stages fit
+bool plan_gemm(GemmParams &gp, size_t *smem_bytes);
+// decode packs of one module: at most one pack per slot
+inline int pack_cap(int n, int ch) { return n + (n + ch - 1) / ch + 1; }
+// grouped rows: positions per slot so that a slot's t rows fit a B stage
+inline int pf_ch(int nt, int rpmax) {
+    const int c = (nt * 128 - kStageHdrBytes) / (rpmax * 4);
+    return c < nt ? c : nt;
+}
 
 // lora_api.cu: sets the string lora_last_cuda_error() returns on this thread
 void set_last_error(const char *why);

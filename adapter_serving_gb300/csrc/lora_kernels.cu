@@ -1,10 +1,13 @@
 // lora_kernels.cu -- the device side of the adapted linear layer y_i = W x_i + s B_a (A_a x_i).
 //
-//   prep_decode_kernel    row grouping: stable sort of the rows by adapter id, plus id checks
-//   prep_segments_kernel  checks a given contiguous segment table (prefill)
+//   prep_decode_kernel    row grouping: stable sort of the rows by adapter id, id checks, and
+//                         the expand packs (which adapters' B slices share one B stage)
+//   prep_segments_kernel  checks a given contiguous segment table (prefill), expand slots per
+//                         row chunk
 //   shrink_kernel         t_i = s * A_a x_i for every row (CUDA cores; bandwidth-bound)
-//   gemm_kernel           base W x_i on tcgen05 tensor cores, with the expand s B_a t_i written
-//                         into the TMEM accumulator before the base MMAs accumulate on top
+//   gemm_kernel           base W x_i on tcgen05 tensor cores into TMEM; the expand s B_a t_i from
+//                         B stages in the same TMA ring on CUDA cores into a second TMEM buffer;
+//                         both added on the way out
 //
 // The forward is the one on "m07 -- Multi-Adapter (LoRA) Serving", section 6 "Deep Dive A:
 // Batching Heterogeneous Adapters" (one batched base GEMM shared by the batch, plus a gathered
@@ -12,6 +15,7 @@
 // many adapters" (rows tagged with their adapter, grouped, one kernel per layer).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <cstdint>
 
 #include "lora_internal.h"
@@ -71,6 +75,103 @@ __device__ int checked_id(const PrepParams &p, int id, int where) {
     return id;
 }
 
+// Exclusive prefix sum over the 256 threads of a block; `total` receives the sum.
+__device__ int block_scan256(int v, int *s_warp, int &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    int before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const int t = s_warp[w];
+        before += w < warp ? t : 0;
+        tot += t;
+    }
+    __syncthreads();
+    total = tot;
+    return before + x - v;
+}
+
+// Expand packs of every module (decode).  A slot is one adapter segment's run of at most
+// pack_ch positions.  Slots are ordered by storage rank (descending), then segment, then
+// position, and laid end to end in rank units: as ranks are powers of two no slot crosses a
+// multiple of 64, so pack j (one B stage) is exactly the slots in units [64 j, 64 j + 64).
+// A slot at unit offset P keeps its t rows at floats [pack_ch * P, pack_ch * (P + rp)) of the
+// module's packed T, so a pack's t rows are one contiguous range too.
+__device__ void build_packs(const PrepParams &p, int ns) {
+    __shared__ int s_warp[8];
+    __shared__ int s_first[320];
+    const int tid = threadIdx.x;
+    const int ch = p.pack_ch;
+    for (int m = 0; m < p.n_mod; ++m) {
+        int q0 = 0, q1 = 0, rp = 0, nsl = 0, cls = 4;
+        const uint16_t *B = nullptr;
+        if (tid < ns) {
+            q0 = p.seg_start[tid];
+            q1 = p.seg_start[tid + 1];
+            const int a = p.seg_adapter[tid];
+            if (a >= 0) {
+                const PoolEntry e = p.table[m][a];
+                rp = e.rp;
+                B = e.B;
+            }
+            if (rp > 0) {
+                nsl = (q1 - q0 + ch - 1) / ch;
+                cls = rp == 64 ? 0 : rp == 32 ? 1 : rp == 16 ? 2 : 3;
+            }
+        }
+        int slot_base = 0, unit_base = 0, slots_tot = 0, units_tot = 0;
+        for (int c = 0; c < 4; ++c) {
+            int tot;
+            const int ex = block_scan256(cls == c ? nsl : 0, s_warp, tot);
+            if (cls == c) {
+                slot_base = slots_tot + ex;
+                unit_base = units_tot + ex * (64 >> c);
+            }
+            slots_tot += tot;
+            units_tot += tot * (64 >> c);
+        }
+        const int npk = (units_tot + kPackRanks - 1) / kPackRanks;
+        for (int k = 0; k < nsl; ++k) {
+            const int P = unit_base + k * rp;
+            if (P % kPackRanks == 0) s_first[P / kPackRanks] = slot_base + k;
+        }
+        if (tid == 0) s_first[npk] = slots_tot;
+        __syncthreads();
+        BPackG *packs = p.packs[m];
+        for (int k = 0; k < nsl; ++k) {
+            const int P = unit_base + k * rp, j = P / kPackRanks;
+            const int e = slot_base + k - s_first[j];
+            const int r0 = q0 + k * ch;
+            BSlotG sl;
+            sl.B = B;
+            sl.q0 = (uint16_t)r0;
+            sl.nrows = (uint8_t)min(ch, q1 - r0);
+            sl.rp = (uint8_t)rp;
+            sl.off = (uint8_t)(P % kPackRanks);
+            sl.pad_[0] = sl.pad_[1] = sl.pad_[2] = 0;
+            packs[j].slot[e] = sl;
+            if (e == 0) {
+                packs[j].tbegin = ch * kPackRanks * j;
+                packs[j].tfloats = ch * min(kPackRanks, units_tot - kPackRanks * j);
+                packs[j].nslots = s_first[j + 1] - s_first[j];
+                packs[j].pad_ = 0;
+            }
+        }
+        if (tid < ns)
+            for (int q = q0; q < q1; ++q)
+                p.tpos[m][q] = rp > 0 ? ch * (unit_base + ((q - q0) / ch) * rp) + ((q - q0) % ch) * rp : -1;
+        if (tid == 0) p.n_packs[m] = npk;
+        __syncthreads();  // s_first is reused by the next module
+    }
+}
+
 // One block of 256 threads, n <= 256 rows.  Position of row i in the stable order:
 // #{j : id_j < id_i} + #{j < i : id_j == id_i}.
 __global__ void __launch_bounds__(256) prep_decode_kernel(const PrepParams p) {
@@ -119,10 +220,14 @@ __global__ void __launch_bounds__(256) prep_decode_kernel(const PrepParams p) {
         p.seg_start[seg] = tid;
         p.seg_adapter[seg] = s_sorted[tid];
     }
+    const int ns = n > 0 ? s_scan[n - 1] : 0;
     if (tid == 0) {
-        int ns = n > 0 ? s_scan[n - 1] : 0;
         *p.n_seg = ns;
         p.seg_start[ns] = n;
+    }
+    if (p.packs[0] != nullptr) {
+        __syncthreads();  // the segment table is complete
+        build_packs(p, ns);
     }
 }
 
@@ -138,6 +243,11 @@ __global__ void __launch_bounds__(1024) prep_segments_kernel(const PrepParams p)
             p.seg_adapter[0] = -1;
             *p.n_seg = 1;
         }
+        if (p.chunk_nb != nullptr)
+            for (int c = threadIdx.x; c < (p.n + p.nt - 1) / p.nt; c += blockDim.x) {
+                p.chunk_seg0[c] = 0;
+                p.chunk_nb[c] = 0;
+            }
         return;
     }
     for (int s = threadIdx.x; s <= p.n_seg_in; s += blockDim.x) {
@@ -145,6 +255,22 @@ __global__ void __launch_bounds__(1024) prep_segments_kernel(const PrepParams p)
         if (s < p.n_seg_in) p.seg_adapter[s] = checked_id(p, p.seg_adapter_in[s], s);
     }
     if (threadIdx.x == 0) *p.n_seg = p.n_seg_in;
+    if (p.chunk_nb == nullptr) return;
+    // expand slots of every row chunk: each segment's rows in the chunk, in runs of pf_ch
+    __syncthreads();
+    const int ns = p.n_seg_in, nt = p.nt, chunks = (p.n + nt - 1) / nt;
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+        const int row0 = c * nt, row1 = min(p.n, row0 + nt);
+        int sg = seg_of(p.seg_start, ns, row0);
+        p.chunk_seg0[c] = sg;
+        int nb = 0;
+        for (; sg < ns && p.seg_start[sg] < row1; ++sg) {
+            if (p.seg_adapter[sg] < 0) continue;
+            const int rows = min(p.seg_start[sg + 1], row1) - max(p.seg_start[sg], row0);
+            nb += (rows + p.pf_ch - 1) / p.pf_ch;
+        }
+        p.chunk_nb[c] = nb;
+    }
 }
 
 __global__ void table_write_kernel(PoolEntry *dst, PoolEntry v) { *dst = v; }
@@ -327,6 +453,9 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const 
     const uint16_t *x = p.x[m];
     float *const T = p.T[m];
     const int32_t *const perm = p.perm;
+    const int32_t *const tpos = p.tpos[m];
+    // where position q's t row starts: its pack slot (expand packs) or its row
+    auto t_at = [&](int q) -> float * { return T + (tpos ? (size_t)tpos[q] : (size_t)perm[q] * p.rpmax); };
     float *const partials = p.partials;
     const float scale = p.scale;
     const int ks_max = p.ks_max, n = p.n;
@@ -378,7 +507,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const 
                     const float v = warp_sum(acc[rr]);
                     if (lane == 0) {
                         if (ks == 1)
-                            T[(size_t)row[rr] * rpmax + j] = scale * v;
+                            t_at(qb + rr)[j] = scale * v;
                         else
                             partials[(((size_t)m * ks_max + kc) * n + (qb + rr)) * rpmax + j] = v;
                     }
@@ -388,7 +517,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const 
     }
     if (ks == 1) {
         for (int idx = tid; idx < (qhi - qlo) * (rp - r); idx += kShrinkThreads)
-            T[(size_t)perm[qlo + idx / (rp - r)] * rpmax + r + idx % (rp - r)] = 0.f;
+            t_at(qlo + idx / (rp - r))[r + idx % (rp - r)] = 0.f;
         return;
     }
     __threadfence();
@@ -402,16 +531,30 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const 
         float v = 0.f;
         if (j < r)
             for (int c = 0; c < ks; ++c) v += __ldcg(partials + (((size_t)m * ks_max + c) * n + q) * rpmax + j);
-        T[(size_t)perm[q] * rpmax + j] = scale * v;
+        t_at(q)[j] = scale * v;
     }
     if (tid == 0) p.counters[m * p.max_units + u] = 0;
 }
 
 // ============================================================================ gemm ==========
+//
+// One persistent CTA per SM, four roles: warp 0 is the TMA producer, lane 0 of warp 1 issues
+// tcgen05.mma, warps 2-5 are the epilogue (TMEM lane quarter = warp % 4).  A tile is 128 rows
+// of W (MMA M) by the rows of the batch or of a row chunk (MMA N).  Its iterations are the
+// k-blocks of W (64 wide) followed by its B stages (the expand, see BStageHdr); decode spreads
+// the flattened (tile, iteration) space evenly over the CTAs (stream-K), grouped rows take whole
+// tiles round robin.
 
 struct Item {
-    int32_t m, w_tile, chunk, kb0, kb1, kbn, tile;
-    int64_t it0;  // flattened index of the tile's first k-block
+    int32_t m, w_tile, chunk, kb0, kb1, kbn, ext, tile;
+    int64_t it0;  // flattened index of the tile's first iteration
+};
+
+// Where each module's tiles start in the flattened iteration space; built by one thread at
+// kernel start because the number of B stages per tile comes from the prep kernel.
+struct SchedSmem {
+    int64_t iter_begin[LORA_MAX_MODULES + 1];
+    int32_t ext[LORA_MAX_MODULES];  // iterations of one tile: k-blocks + B stages
 };
 
 __device__ __forceinline__ void tile_coords(const GemmParams &p, int m, int lt, Item &it) {
@@ -427,28 +570,34 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int m, int lt, 
 struct Sched {
     int64_t x, e;
     int32_t j, cta;
-    __device__ void begin(const GemmParams &p, int c) {
+    __device__ void begin(const GemmParams &p, const SchedSmem &ss, int c) {
         cta = c;
         j = 0;
         if (p.stream_k) {
-            x = (int64_t)c * p.total_iters / p.n_cta;
-            e = (int64_t)(c + 1) * p.total_iters / p.n_cta;
+            const int64_t tot = ss.iter_begin[p.n_mod];
+            x = (int64_t)c * tot / p.n_cta;
+            e = (int64_t)(c + 1) * tot / p.n_cta;
         }
     }
-    __device__ bool next(const GemmParams &p, Item &it) {
+    // whether next() has another item to give
+    __device__ __forceinline__ bool more(const GemmParams &p) const {
+        return p.stream_k ? x < e : cta + j * p.n_cta < p.total_tiles;
+    }
+    __device__ bool next(const GemmParams &p, const SchedSmem &ss, Item &it) {
         if (p.stream_k) {
             if (x >= e) return false;
             int m = 0;
-            while (m + 1 < p.n_mod && p.mod[m + 1].iter_begin <= x) ++m;
-            const int kbn = p.mod[m].k_blocks;
-            const int64_t local = x - p.mod[m].iter_begin;
-            const int lt = (int)(local / kbn);
+            while (m + 1 < p.n_mod && ss.iter_begin[m + 1] <= x) ++m;
+            const int ext = ss.ext[m];
+            const int64_t local = x - ss.iter_begin[m];
+            const int lt = (int)(local / ext);
             it.m = m;
-            it.kbn = kbn;
-            it.kb0 = (int)(local - (int64_t)lt * kbn);
-            it.kb1 = (int)((e - x) < (int64_t)(kbn - it.kb0) ? it.kb0 + (e - x) : kbn);
+            it.kbn = p.mod[m].k_blocks;
+            it.ext = ext;
+            it.kb0 = (int)(local - (int64_t)lt * ext);
+            it.kb1 = (int)((e - x) < (int64_t)(ext - it.kb0) ? it.kb0 + (e - x) : ext);
             it.tile = p.mod[m].tile_begin + lt;
-            it.it0 = p.mod[m].iter_begin + (int64_t)lt * kbn;
+            it.it0 = ss.iter_begin[m] + (int64_t)lt * ext;
             tile_coords(p, m, lt, it);
             x += it.kb1 - it.kb0;
             return true;
@@ -461,29 +610,42 @@ struct Sched {
         const int lt = t - p.mod[m].tile_begin;
         it.m = m;
         it.kbn = p.mod[m].k_blocks;
-        it.kb0 = 0;
-        it.kb1 = it.kbn;
         it.tile = t;
         it.it0 = 0;
         tile_coords(p, m, lt, it);
+        it.ext = it.kbn + (p.chunk_nb ? p.chunk_nb[it.chunk] : 0);
+        it.kb0 = 0;
+        it.kb1 = it.ext;
         return true;
     }
 };
 
-// CTA whose stream-K range holds flattened iteration x.
-__device__ __forceinline__ int cta_of(const GemmParams &p, int64_t x) {
-    return (int)(((x + 1) * p.n_cta - 1) / p.total_iters);
-}
-
-// Expand metadata staged in shared memory by the epilogue warps: for every TMEM column of the
-// tile (a row of the batch), the B factor of its adapter and the storage rank (0 = base only).
-struct EpiMeta {
-    uint64_t colB[kMaxWin];  // B factor base ([d_out, rp]) of the column's adapter
-    int32_t colrp[kMaxWin];  // storage rank of that adapter, 0 for base-only rows
-    int32_t ncols;           // columns set up
-    int32_t module;          // module the columns were set up for (decode caching)
-    int32_t maxrp;           // largest storage rank among them (0: base-only tile)
-    int32_t pad_;
+// A tile's ext = kbn + nb iterations interleave its nb B stages evenly among its kbn W k-blocks:
+// iteration i is a B stage when floor((i + 1) nb / ext) > floor(i nb / ext).  Iteration 0 is always
+// a W k-block, so the piece holding k-block 0 is the one holding iteration 0.
+__device__ __forceinline__ int b_before(const Item &it, int i) { return i * (it.ext - it.kbn) / it.ext; }
+// W k-blocks and B stages of an item
+__device__ __forceinline__ int item_b(const Item &it) { return b_before(it, it.kb1) - b_before(it, it.kb0); }
+__device__ __forceinline__ int item_w(const Item &it) { return it.kb1 - it.kb0 - item_b(it); }
+// Walks an item's iterations without a division per step: acc = (i nb) mod ext, b = B stages
+// before iteration i.
+struct Mix {
+    int nb, ext, acc, b;
+    __device__ __forceinline__ void begin(const Item &it) {
+        nb = it.ext - it.kbn;
+        ext = it.ext;
+        const int t = it.kb0 * nb;
+        b = t / ext;
+        acc = t - b * ext;
+    }
+    // whether the current iteration is a B stage (its pack is `b` before the call); moves on
+    __device__ __forceinline__ bool step() {
+        acc += nb;
+        if (acc < ext) return false;
+        acc -= ext;
+        ++b;
+        return true;
+    }
 };
 
 // Everything the epilogue reads per call, copied out of the kernel parameters once.  Parameters
@@ -491,14 +653,11 @@ struct EpiMeta {
 // every store (they might alias); locals never are.
 struct EpiCtx {
     const GemmParams *p;
-    uint8_t *ring;       // per-thread staging of B rows: chunk i of thread t at (i * 128 + t) * 16
-    float *tstage;       // t rows of the current batch of columns, [16][rpmax]
-    EpiMeta *meta;
-    int decode, n, nt, y_bf16, n_cta, rpmax, ring_chunks;
+    const int32_t *perm_s;  // decode: sorted position -> row (shared memory copy)
+    int decode, n, nt, y_bf16, n_cta, pack_ch;
     int64_t total_iters;
     float *partials;
     int32_t *tile_counters;
-    const int32_t *perm, *seg_start, *seg_adapter, *n_seg;
     uint32_t tmem_base;
     uint32_t delta_col;  // first TMEM column of the expand (delta) buffers (one per accumulator)
     int etid;            // 0..127 among epilogue threads
@@ -509,174 +668,144 @@ struct EpiCtx {
 
 struct ModLocal {
     const CUtensorMap *tmY;
-    void *y;
-    const float *T;
-    const PoolEntry *table;
     int d_out;
 };
 __device__ __forceinline__ ModLocal mod_local(const GemmParams &p, int m) {
     const GemmModule &M = p.mod[m];
-    return ModLocal{&M.tmY, M.y, M.T, M.table, M.d_out};
+    return ModLocal{&M.tmY, M.d_out};
 }
 
-// (Re)build the per-column metadata of a tile from the segment table: every row of the tile's
-// positions gets its segment's adapter.  Decode tiles of one module share it, so it is rebuilt
-// only when the module changes; for grouped rows it is built per tile.
-__device__ void setup_columns(EpiCtx &c, const Item &it) {
-    EpiMeta &w = *c.meta;
-    if (c.decode && w.module == it.m) return;
-    named_bar_sync(1, 128);  // nobody still reads the old columns
-    if (c.etid == 0) w.maxrp = 0;
-    named_bar_sync(1, 128);
-    const int n_seg = *c.n_seg;
-    const int row0 = it.chunk * c.nt;
-    const int qlo = c.decode ? 0 : row0;
-    const int qhi = c.decode ? c.n : min(c.n, row0 + c.nt);
-    const int32_t *seg_start = c.seg_start, *seg_adapter = c.seg_adapter, *perm = c.perm;
-    const int decode = c.decode;
-    const int s0 = decode ? 0 : seg_of(seg_start, n_seg, qlo);
-    const int s1 = decode ? n_seg - 1 : seg_of(seg_start, n_seg, qhi - 1);
-    const PoolEntry *table = mod_local(*c.p, it.m).table;
-    // one thread per position: find its segment (binary search in [s0, s1]), then its column
-    for (int q = qlo + c.etid; q < qhi; q += 128) {
-        int lo = s0, hi = s1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(seg_start + mid) <= q) lo = mid; else hi = mid - 1;
-        }
-        const int a = __ldg(seg_adapter + lo);
-        uint64_t b = 0;
-        int rp = 0;
-        if (a >= 0) {
-            b = reinterpret_cast<uint64_t>(table[a].B);
-            rp = table[a].rp;
-        }
-        const int col = decode ? __ldg(perm + q) : q - row0;
-        if (col >= 0 && col < kMaxWin) {
-            w.colB[col] = b;
-            w.colrp[col] = rp;
-        }
-        if (rp > 0) atomicMax(&w.maxrp, rp);
-    }
-    if (c.etid == 0) {
-        w.ncols = qhi - qlo;
-        w.module = it.m;
-    }
-    named_bar_sync(1, 128);
-}
-
-// Expand for a tile this CTA heads: delta[o, col] = sum_j B_a[o0 + o, j] * t_col[j] for every
-// column (row of the batch) of the tile, 0 for base-only rows, written into the TMEM delta
-// buffer paired with the tile's accumulator.  It runs while the MMA warp works (on this tile or
-// the one before); the drain adds it to the accumulator.
+// ---- expand (B stages) ----------------------------------------------------------------
 //
-// Columns go in blocks of 16 (one 16-column TMEM store per block), each block in batches of CB
-// columns.  Column i of a batch owns NCH fixed 16-byte slots of the per-thread ring, so every
-// address is known without a running counter and all loads and dot products of a batch are
-// independent: each thread copies its own B row pieces with cp.async (it then waits only for
-// its own copies), the 128 threads copy the batch's t rows together, one wait, one barrier,
-// then the batch is computed.  NCH = storage rank / 8 of the largest rank among the columns.
-template <int NCH>
-__device__ void expand_blocks(EpiCtx &c, const Item &it, uint32_t tcol0) {
-    constexpr int CB = (NCH <= 2) ? 16 / NCH : 32 / NCH;  // columns per batch (ring: CB * NCH slots)
-    constexpr int NB16 = 16 / CB;                       // batches per 16-column block
-    const EpiMeta &w = *c.meta;
-    const ModLocal M = mod_local(*c.p, it.m);
-    const int row0 = it.chunk * c.nt;
-    const int ncols = w.ncols;
-    const int rpmax = c.rpmax;
-    const int oo = it.w_tile * kBM + c.o;
-    const bool o_ok = oo < M.d_out;
-    const uint32_t ring_me = smem_u32(c.ring) + (uint32_t)c.o * 16;
-    const uint32_t tst = smem_u32(c.tstage);
-    const float *Tg = M.T + (size_t)row0 * rpmax;  // t rows in row order
-    for (int b0 = 0; b0 < ncols; b0 += 16) {
-        float d[16];
+// Producer side: one B stage = the B slices (rows o0 .. o0+127 of each slot's adapter, [128][rp]
+// bf16, one bulk copy each, at rank offset `off` of the A buffer) and the slots' t rows (one bulk
+// copy after the header of the X buffer); the slot header is written with plain stores before
+// the arrive that opens the stage.
+
+// decode: pack j of module M, its 16-byte pieces held one per lane (lane 0: header, lane e + 1:
+// slot e), already loaded.  Returns the bytes the copies bring.
+__device__ __forceinline__ void produce_pack(const uint4 rec, const GemmModule &M, int o0, int orows, int pack_ch,
+                                             uint8_t *sa, uint8_t *sx, uint64_t *full_bar, int lane) {
+    const int nslots = __shfl_sync(0xffffffffu, (int)rec.z, 0);
+    const int tbegin = __shfl_sync(0xffffffffu, (int)rec.x, 0);
+    const int tfloats = __shfl_sync(0xffffffffu, (int)rec.y, 0);
+    BStageHdr *hdr = reinterpret_cast<BStageHdr *>(sx);
+    const bool mine = lane >= 1 && lane <= nslots;
+    const uint16_t *B = reinterpret_cast<const uint16_t *>((uint64_t)rec.x | ((uint64_t)rec.y << 32));
+    const int rp = (int)(rec.z >> 24), off = (int)(rec.w & 0xff);
+    uint32_t bytes = 0;
+    if (mine) {
+        BSlotS sl;
+        sl.q0 = (int)(rec.z & 0xffff);
+        sl.nrows = (int16_t)((rec.z >> 16) & 0xff);
+        sl.rp = (int16_t)rp;
+        sl.off = (int16_t)off;
+        sl.tstride = (int16_t)rp;
+        sl.toff = pack_ch * off;
+        hdr->slot[lane - 1] = sl;
+        bytes = (uint32_t)(orows * rp * 2);
+    }
+    const bool plain = !mine || (rp == 8 && ((rec.z >> 16) & 0xff) == 1);
+    const bool singles8 = __all_sync(0xffffffffu, plain);
+    if (lane == 0) {
+        hdr->nslots = nslots;
+        hdr->singles8 = singles8 ? 1 : 0;
+    }
+    fence_proxy_async_smem();  // the slot is refilled by TMA later
+    const uint32_t total = __reduce_add_sync(0xffffffffu, bytes) + (uint32_t)tfloats * 4;
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(full_bar, total);
+    __syncwarp();
+    if (mine) bulk_load(sa + off * 256, B + (size_t)o0 * rp, bytes, full_bar);
+    if (lane == 0 && tfloats > 0) bulk_load(sx + kStageHdrBytes, M.T + tbegin, (uint32_t)tfloats * 4, full_bar);
+}
+
+// Epilogue side: delta[o, col] = sum_j B_a[o0 + o, j] t_col[j] for every row of every slot of
+// the stage, written to the column of the TMEM delta buffer (32x32b.x1: this warp's 32 lanes).
+__device__ __forceinline__ float dot8_bf16_f32(uint4 b, float4 ta, float4 tb) {
+    float acc0 = bf16lo(b.x) * ta.x, acc1 = bf16hi(b.x) * ta.y;
+    acc0 = fmaf(bf16lo(b.y), ta.z, acc0);
+    acc1 = fmaf(bf16hi(b.y), ta.w, acc1);
+    acc0 = fmaf(bf16lo(b.z), tb.x, acc0);
+    acc1 = fmaf(bf16hi(b.z), tb.y, acc1);
+    acc0 = fmaf(bf16lo(b.w), tb.z, acc0);
+    acc1 = fmaf(bf16hi(b.w), tb.w, acc1);
+    return acc0 + acc1;
+}
+
+__device__ void expand_stage(const EpiCtx &c, const uint8_t *sa, const uint8_t *sx, uint32_t tdel, int row0) {
+    const BStageHdr *hdr = reinterpret_cast<const BStageHdr *>(sx);
+    const int nslots = min(hdr->nslots, kPackSlots);
+    const uint32_t a_base = smem_u32(sa), t_base = smem_u32(sx) + kStageHdrBytes;
+    if (hdr->singles8) {
+        // rank-8 slots of one row each (distinct adapters): slot e's B rows sit at rank offset 8 e
+        // and its t row at pack_ch * 8 e floats, so all loads go out before any arithmetic and
+        // only the column lookup waits on the slot header
+        for (int e0 = 0; e0 < nslots; e0 += 4) {
+            uint4 bv[4];
+            float4 ta[4], tb[4];
+            int q[4];
 #pragma unroll
-        for (int k = 0; k < NB16; ++k) {
-            const int cb = b0 + k * CB;
-            int rp[CB];
-#pragma unroll
-            for (int i = 0; i < CB; ++i) rp[i] = cb + i < ncols ? w.colrp[cb + i] : 0;
-#pragma unroll
-            for (int i = 0; i < CB; ++i) {
-                if (rp[i] > 0) {
-                    const uint16_t *src =
-                        reinterpret_cast<const uint16_t *>(w.colB[cb + i]) + (size_t)(o_ok ? oo : 0) * rp[i];
-#pragma unroll
-                    for (int ch = 0; ch < NCH; ++ch)
-                        if (ch * 8 < rp[i])
-                            cp_async_16(ring_me + (uint32_t)((i * NCH + ch) * 128 * 16), src + ch * 8, o_ok ? 16u : 0u);
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + u;
+                q[u] = -1;
+                if (e < nslots) {
+                    bv[u] = lds_u128(a_base + (uint32_t)e * 2048 + (uint32_t)c.o * 16);
+                    ta[u] = lds128(t_base + (uint32_t)(e * c.pack_ch * 32));
+                    tb[u] = lds128(t_base + (uint32_t)(e * c.pack_ch * 32) + 16);
+                    q[u] = hdr->slot[e].q0;
                 }
             }
-            const int nrow = min(CB, ncols - cb);
-            if (nrow > 0) {
-                const int tchunks = nrow * (rpmax >> 2);
-                for (int idx = c.etid; idx < tchunks; idx += 128)
-                    cp_async_16(tst + (uint32_t)idx * 16, Tg + (size_t)cb * rpmax + idx * 4, 16u);
-            }
-            cp_async_commit();
-            cp_async_wait_all();
-            named_bar_sync(1, 128);  // everyone's t rows have landed
 #pragma unroll
-            for (int i = 0; i < CB; ++i) {
-                const float *t = c.tstage + i * rpmax;
-                float acc = 0.f;
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch) {
-                    if (ch * 8 < rp[i]) {
-                        const uint4 bv = *reinterpret_cast<const uint4 *>(c.ring + ((size_t)(i * NCH + ch) * 128 + c.o) * 16);
-                        const float4 ta = *reinterpret_cast<const float4 *>(t + ch * 8);
-                        const float4 tb = *reinterpret_cast<const float4 *>(t + ch * 8 + 4);
-                        acc = fmaf(bf16lo(bv.x), ta.x, acc);
-                        acc = fmaf(bf16hi(bv.x), ta.y, acc);
-                        acc = fmaf(bf16lo(bv.y), ta.z, acc);
-                        acc = fmaf(bf16hi(bv.y), ta.w, acc);
-                        acc = fmaf(bf16lo(bv.z), tb.x, acc);
-                        acc = fmaf(bf16hi(bv.z), tb.y, acc);
-                        acc = fmaf(bf16lo(bv.w), tb.z, acc);
-                        acc = fmaf(bf16hi(bv.w), tb.w, acc);
-                    }
+            for (int u = 0; u < 4; ++u) {
+                if (q[u] >= 0 && q[u] < c.n) {  // the same for the whole warp
+                    const int col = c.decode ? c.perm_s[q[u]] : q[u] - row0;
+                    if (col >= 0 && col < c.nt) tmem_st1(tdel + (uint32_t)col, dot8_bf16_f32(bv[u], ta[u], tb[u]));
                 }
-                d[k * CB + i] = acc;
             }
-            named_bar_sync(1, 128);  // the t rows may be overwritten by the next batch
         }
-        tmem_st16(tcol0 + (uint32_t)b0, d);
+        return;
+    }
+    for (int e = 0; e < nslots; ++e) {
+        const BSlotS sl = hdr->slot[e];
+        const int rp = sl.rp;
+        const uint32_t brow = a_base + (uint32_t)sl.off * 256 + (uint32_t)(c.o * rp * 2);
+        for (int r = 0; r < sl.nrows; ++r) {
+            const uint32_t trow = t_base + (uint32_t)(sl.toff + r * sl.tstride) * 4;
+            float acc0 = 0.f, acc1 = 0.f;
+            for (int j = 0; j < rp; j += 8) {
+                const uint4 b = lds_u128(brow + j * 2);
+                const float4 ta = lds128(trow + j * 4), tb = lds128(trow + j * 4 + 16);
+                acc0 = fmaf(bf16lo(b.x), ta.x, acc0);
+                acc1 = fmaf(bf16hi(b.x), ta.y, acc1);
+                acc0 = fmaf(bf16lo(b.y), ta.z, acc0);
+                acc1 = fmaf(bf16hi(b.y), ta.w, acc1);
+                acc0 = fmaf(bf16lo(b.z), tb.x, acc0);
+                acc1 = fmaf(bf16hi(b.z), tb.y, acc1);
+                acc0 = fmaf(bf16lo(b.w), tb.z, acc0);
+                acc1 = fmaf(bf16hi(b.w), tb.w, acc1);
+            }
+            const int q = sl.q0 + r;  // the same for the whole warp: the guards below are uniform
+            if (q < 0 || q >= c.n) continue;
+            const int col = c.decode ? c.perm_s[q] : q - row0;
+            if (col < 0 || col >= c.nt) continue;
+            tmem_st1(tdel + (uint32_t)col, acc0 + acc1);
+        }
     }
 }
 
-__device__ void init_expand(EpiCtx &c, const Item &it, int buf) {
-    setup_columns(c, it);
-    const uint32_t tcol0 = c.tmem_base + ((uint32_t)c.lane_base << 16) + c.delta_col + (uint32_t)(buf * c.nt);
-    switch (c.meta->maxrp) {
-        case 8: expand_blocks<1>(c, it, tcol0); break;
-        case 16: expand_blocks<2>(c, it, tcol0); break;
-        case 32: expand_blocks<4>(c, it, tcol0); break;
-        case 64: expand_blocks<8>(c, it, tcol0); break;
-        default: {  // base-only tile
-            float z[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) z[i] = 0.f;
-            for (int b0 = 0; b0 < c.meta->ncols; b0 += 16) tmem_st16(tcol0 + (uint32_t)b0, z);
-        }
-    }
-    tmem_st_wait();
-}
-
-
-// This CTA's share of 16 columns of a tile: accumulator (+ the expand delta when it heads the
-// tile), both TMEM loads in flight before the one wait.
-__device__ __forceinline__ void own_cols16(const EpiCtx &c, uint32_t tacc, uint32_t tdel, bool head, int c0,
+// This CTA's share of 16 columns of a tile: accumulator and/or expand delta, both TMEM loads in
+// flight before the one wait.
+__device__ __forceinline__ void own_cols16(uint32_t tacc, uint32_t tdel, bool with_acc, bool with_delta, int c0,
                                            float (&v)[16]) {
     uint32_t r[16], d[16];
-    tmem_ld16(tacc + c0, r);
-    if (head) tmem_ld16(tdel + c0, d);
+    if (with_acc) tmem_ld16(tacc + c0, r);
+    if (with_delta) tmem_ld16(tdel + c0, d);
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + (head ? __uint_as_float(d[i]) : 0.f);
+    for (int i = 0; i < 16; ++i)
+        v[i] = (with_acc ? __uint_as_float(r[i]) : 0.f) + (with_delta ? __uint_as_float(d[i]) : 0.f);
 }
-
 
 // Partial tiles (stream-K pieces) are kept in column quads: element (column c, lane o) at
 // ((c / 4) * 128 + o) * 4 + c % 4.  A thread's 16 columns are four 16-byte vectors and a warp
@@ -708,8 +837,8 @@ struct DrainBufs {
 
 constexpr uint64_t kHeadWaitNs = 50000;  // how long a finishing CTA waits for the other pieces
 
-__device__ void drain(EpiCtx &c, const Item &it, int buf, bool last, volatile int *misc_flag,
-                      volatile int *abort_flag, DrainBufs &db) {
+__device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool with_delta, bool last,
+                      volatile int *misc_flag, volatile int *abort_flag, DrainBufs &db) {
     const ModLocal M = mod_local(*c.p, it.m);
     const int nt = c.nt, decode = c.decode, y_bf16 = c.y_bf16, n_cta = c.n_cta;
     const int64_t total_iters = c.total_iters;
@@ -760,10 +889,10 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool last, volatile in
         }
     };
 
-    if (head && it.kb1 == it.kbn) {
+    if (head && it.kb1 == it.ext) {
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
-            own_cols16(c, tacc, tdel, true, c0, v);
+            own_cols16(tacc, tdel, with_acc, with_delta, c0, v);
             emit(c0, v);
         }
         return;
@@ -771,7 +900,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool last, volatile in
 
     // ---- partial tile (stream-K) ----
     const int c_first = (int)(((it.it0 + 1) * n_cta - 1) / total_iters);  // CTA holding iteration it0
-    const int c_last = (int)(((it.it0 + it.kbn) * n_cta - 1) / total_iters);
+    const int c_last = (int)(((it.it0 + it.ext) * n_cta - 1) / total_iters);
     const int nc = c_last - c_first + 1;
     const int self_idx = (int)blockIdx.x - c_first;
     int32_t *counter = c.tile_counters + it.tile;
@@ -795,7 +924,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool last, volatile in
         float *dst = part_of(blockIdx.x);
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
-            own_cols16(c, tacc, tdel, head, c0, v);
+            own_cols16(tacc, tdel, with_acc, with_delta, c0, v);
             float4 *q = piece_quads(dst, c0, c.o);
 #pragma unroll
             for (int k = 0; k < 4; ++k) __stcg(q + k * kBM, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
@@ -827,7 +956,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool last, volatile in
     const uint32_t pbase = smem_u32(db.stage) + (uint32_t)c.o * 16;  // this lane's quad of piece 0, block 0
     for (int c0 = 0; c0 < ncols16; c0 += 16) {
         float own[16], sum[16];
-        own_cols16(c, tacc, tdel, head, c0, own);
+        own_cols16(tacc, tdel, with_acc, with_delta, c0, own);
         for (int jc = 0, j = 0; jc < nc; ++jc) {
             float4 q[4];
             if (jc == self_idx) {
@@ -862,21 +991,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const uint32_t a_bytes = kBM * kBK * 2;
     const uint32_t b_bytes = (uint32_t)p.nt * kBK * 2;
     const uint32_t stage_bytes = a_bytes + b_bytes;
-    uint8_t *ring = smem + (size_t)S * stage_bytes;  // per-thread B staging, ring_chunks * 2 KiB
-    float *tstage = reinterpret_cast<float *>(ring + (size_t)p.ring_chunks * 128 * 16);  // [16][rpmax]
-    EpiMeta *meta = reinterpret_cast<EpiMeta *>(tstage + 16 * p.rpmax);
-    uint64_t *full = reinterpret_cast<uint64_t *>(meta + 1);
-    uint64_t *empty = full + S;
+    uint8_t *ybuf = smem + (size_t)S * stage_bytes;  // epilogue y staging
+    int32_t *perm_s = reinterpret_cast<int32_t *>(ybuf + kYBufBytes);
+    SchedSmem *ss = reinterpret_cast<SchedSmem *>(perm_s + LORA_MAX_DECODE_ROWS);
+    // A stage slot is filled with either W k-blocks (wfull, consumed by the MMA warp) or a B stage
+    // (bfull, consumed by the epilogue).  Each consumer skips the other kind, so each kind has its
+    // own barrier and every consumer keeps its own per-slot parity: a parity wait is only sound
+    // when the waiter cannot fall two phases behind, which holds per kind but not across kinds.
+    uint64_t *wfull = reinterpret_cast<uint64_t *>(ss + 1);
+    uint64_t *bfull = wfull + S;
+    uint64_t *empty = bfull + S;
     uint64_t *acc_full = empty + S;
     uint64_t *acc_free = acc_full + 2;
     uint64_t *mma_done = acc_free + 2;
     uint64_t *ld_bar = mma_done + 1;  // drain: bulk copies of other pieces
-    uint32_t *misc = reinterpret_cast<uint32_t *>(ld_bar + 2);  // [0] tmem, [1] abort, [2] flag
+    uint32_t *misc = reinterpret_cast<uint32_t *>(ld_bar + 1);  // [0] tmem, [1] abort, [2] flag
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full + s, 1);
+            mbar_init(wfull + s, 1);
+            mbar_init(bfull + s, 1);
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -887,8 +1022,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         mbar_init(ld_bar, 1);
         misc[1] = 0;
         misc[2] = 0;
-        meta->module = -1;
         fence_mbar_init();
+        // the flattened schedule: per module, tiles x (k-blocks + B stages)
+        int64_t ib = 0;
+        for (int m = 0; m < p.n_mod; ++m) {
+            const int ext = p.mod[m].k_blocks + (p.stream_k && p.n_packs ? p.n_packs[m] : 0);
+            ss->ext[m] = ext;
+            ss->iter_begin[m] = ib;
+            ib += (int64_t)p.mod[m].m_tiles * p.n_chunks * ext;
+        }
+        ss->iter_begin[p.n_mod] = ib;
     }
     if (warp == 0 && lane == 0) {
         for (int m = 0; m < p.n_mod; ++m) {
@@ -904,72 +1047,167 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------------------ TMA producer
-            const uint64_t pol_w = p.decode ? l2_policy_evict_first() : l2_policy_evict_normal();
-            const uint64_t pol_x = l2_policy_evict_last();
-            Sched sc;
-            sc.begin(p, blockIdx.x);
-            Item it;
-            uint32_t k = 0;  // stage fills issued
-            bool ok = true;
-            while (ok && sc.next(p, it)) {
-                const GemmModule &M = p.mod[it.m];
-                const int o0 = it.w_tile * kBM, row0 = it.chunk * p.nt;
-                for (int kb = it.kb0; kb < it.kb1; ++kb, ++k) {
-                    const int s = k % S;
-                    if (!mbar_wait(empty + s, ((k / S) & 1) ^ 1, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *sa = smem + (size_t)s * stage_bytes;
-                    mbar_arrive_expect_tx(full + s, stage_bytes);
-                    tma_load_2d(sa, &M.tmW, full + s, kb * kBK, o0, pol_w);
-                    tma_load_2d(sa + a_bytes, &M.tmX, full + s, kb * kBK, row0, pol_x);
+        // ---------------------------------------------------------------- TMA producer (warp)
+        const uint64_t pol_w = p.decode ? l2_policy_evict_first() : l2_policy_evict_normal();
+        const uint64_t pol_x = l2_policy_evict_last();
+        Sched sc;
+        sc.begin(p, *ss, blockIdx.x);
+        Item it;
+        uint32_t k = 0;  // stage fills issued
+        bool ok = true;
+        // per slot (bit s): parity of the next W / B fill, kind and parity of the latest fill
+        uint32_t wpar = 0, bpar = 0, last_b = 0, last_par = 0, filled = 0;
+        auto note_fill = [&](int s, bool is_b) -> uint32_t {
+            const uint32_t bit = 1u << s;
+            const uint32_t par = ((is_b ? bpar : wpar) >> s) & 1u;
+            if (is_b) bpar ^= bit; else wpar ^= bit;
+            last_b = is_b ? (last_b | bit) : (last_b & ~bit);
+            last_par = (last_par & ~bit) | (par << s);
+            filled |= bit;
+            return par;
+        };
+        // one stage slot: wait until it is free (lane 0), the answer goes to the whole warp
+        auto acquire = [&](uint32_t kk) -> bool {
+            int got = 1;
+            if (lane == 0) got = mbar_wait(empty + kk % S, ((kk / S) & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
+            return __shfl_sync(0xffffffffu, got, 0) != 0;
+        };
+        while (ok && sc.next(p, *ss, it)) {
+            const GemmModule &M = p.mod[it.m];
+            const int o0 = it.w_tile * kBM, row0 = it.chunk * p.nt;
+            const int orows = min(kBM, M.d_out - o0);
+            const int b0 = b_before(it, it.kb0), b1 = b_before(it, it.kb1);  // the item's packs
+            // decode: the first pack of the item's B stages, fetched ahead
+            uint4 rec = make_uint4(0, 0, 0, 0);
+            if (p.stream_k && b1 > b0 && lane <= kPackSlots)
+                rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + b0) + lane);
+            // grouped rows: the chunk's slots in order (segment, run of pf_ch rows)
+            int sg = 0, r = row0;
+            const int row1 = min(p.n, row0 + p.nt);
+            if (!p.stream_k && b1 > b0) sg = p.chunk_seg0[it.chunk];
+            Mix mx;
+            mx.begin(it);
+            for (int i = it.kb0; i < it.kb1; ++i, ++k) {
+                if (!acquire(k)) {
+                    ok = false;
+                    break;
                 }
-            }
-            // never leave the block with copies still landing in its shared memory
-            for (uint32_t q = (k > (uint32_t)S ? k - S : 0); q < k; ++q) {
-                const uint32_t a = smem_u32(full + (q % S));
-                const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(a, (q / S) & 1) && globaltimer() - t0 < kWaitBudgetNs) {
+                uint8_t *sa = smem + (size_t)(k % S) * stage_bytes;
+                uint8_t *sx = sa + a_bytes;
+                const int jb = mx.b;
+                if (!mx.step()) {
+                    // ---- W k-block i - jb
+                    const int kb = i - jb;
+                    note_fill(k % S, false);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(wfull + k % S, stage_bytes);
+                        tma_load_2d(sa, &M.tmW, wfull + k % S, kb * kBK, o0, pol_w);
+                        tma_load_2d(sa + a_bytes, &M.tmX, wfull + k % S, kb * kBK, row0, pol_x);
+                    }
+                    continue;
+                }
+                // ---- B stage jb
+                uint64_t *bar = bfull + k % S;
+                note_fill(k % S, true);
+                if (p.stream_k) {
+                    const uint4 cur = rec;
+                    if (jb + 1 < b1 && lane <= kPackSlots)
+                        rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + jb + 1) + lane);
+                    produce_pack(cur, M, o0, orows, p.pack_ch, sa, sx, bar, lane);
+                } else if (lane == 0) {
+                    const int ns = *p.n_seg;
+                    int s1 = 0, a = -1;
+                    for (; sg < ns; ++sg) {  // the next segment with an adapter and rows left in the chunk
+                        s1 = min(p.seg_start[sg + 1], row1);
+                        a = p.seg_adapter[sg];
+                        r = max(r, p.seg_start[sg]);
+                        if (a >= 0 && r < s1) break;
+                    }
+                    BStageHdr *hdr = reinterpret_cast<BStageHdr *>(sx);
+                    if (sg >= ns) {  // the chunk has fewer slots than counted: an empty stage
+                        report(p.err, LORA_DEVERR_BAD_SEGMENTS, it.chunk);
+                        hdr->nslots = 0;
+                        hdr->singles8 = 0;
+                        fence_proxy_async_smem();
+                        mbar_arrive(bar);
+                        continue;
+                    }
+                    const int nr = min(p.pf_ch, s1 - r);
+                    const PoolEntry e = M.table[a];
+                    BSlotS sl;
+                    sl.q0 = r;
+                    sl.nrows = (int16_t)nr;
+                    sl.rp = (int16_t)e.rp;
+                    sl.off = 0;
+                    sl.tstride = (int16_t)p.rpmax;
+                    sl.toff = 0;
+                    hdr->nslots = 1;
+                    hdr->singles8 = 0;
+                    hdr->slot[0] = sl;
+                    fence_proxy_async_smem();  // the slot is refilled by TMA later
+                    const uint32_t bb = (uint32_t)(orows * e.rp * 2), tb = (uint32_t)(nr * p.rpmax * 4);
+                    mbar_arrive_expect_tx(bar, bb + tb);
+                    bulk_load(sa, e.B + (size_t)o0 * e.rp, bb, bar);
+                    bulk_load(sx + kStageHdrBytes, M.T + (size_t)r * p.rpmax, tb, bar);
+                    r += nr;
                 }
             }
         }
+        // never leave the block with copies still landing in its shared memory: wait for the
+        // latest fill of every slot
+        if (lane == 0)
+            for (int q = 0; q < S; ++q) {
+                if (!((filled >> q) & 1u)) continue;
+                const uint32_t a = smem_u32(((last_b >> q) & 1u) ? bfull + q : wfull + q);
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(a, (last_par >> q) & 1u) && globaltimer() - t0 < kWaitBudgetNs) {
+                }
+            }
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
             const uint32_t idesc = idesc_bf16_f32(kBM, (uint32_t)p.nt);
             Sched sc;
-            sc.begin(p, blockIdx.x);
+            sc.begin(p, *ss, blockIdx.x);
             Item it;
-            uint32_t k = 0, li = 0;
+            uint32_t k = 0, li = 0, use0 = 0, use1 = 0, wpar = 0;
             bool ok = true;
-            while (ok && sc.next(p, it)) {
+            while (ok && sc.next(p, *ss, it)) {
                 const int buf = li % NB;
-                const uint32_t use = li / NB;
-                if (!mbar_wait(acc_free + buf, (use & 1) ^ 1, abort_flag, p.err)) break;
-                tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(buf * p.nt);
-                for (int kb = it.kb0; kb < it.kb1; ++kb, ++k) {
-                    const int s = k % S;
-                    if (!mbar_wait(full + s, (k / S) & 1, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
+                if (item_w(it) > 0) {
+                    const uint32_t use = buf ? use1 : use0;
+                    if (!mbar_wait(acc_free + buf, (use & 1) ^ 1, abort_flag, p.err)) break;
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-                    const uint64_t da = sdesc_kmajor_sw128(sa);
-                    const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes);
+                    const uint32_t d = tmem_base + (uint32_t)(buf * p.nt);
+                    bool first = true;
+                    Mix mx;
+                    mx.begin(it);
+                    for (int i = it.kb0; i < it.kb1; ++i, ++k) {
+                        if (mx.step()) continue;  // B stages go to the epilogue
+                        const int s = k % S;
+                        if (!mbar_wait(wfull + s, (wpar >> s) & 1u, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        wpar ^= 1u << s;
+                        tc_fence_after();
+                        const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+                        const uint64_t da = sdesc_kmajor_sw128(sa);
+                        const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint32_t accum = (kb > it.kb0 || kk > 0) ? 1u : 0u;
-                        umma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, accum);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint32_t accum = (!first || kk > 0) ? 1u : 0u;
+                            umma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, accum);
+                        }
+                        first = false;
+                        umma_commit(empty + s);
                     }
-                    umma_commit(empty + s);
+                    if (!ok) break;
+                    umma_commit(acc_full + buf);
+                    if (buf) ++use1; else ++use0;
+                } else {
+                    k += (uint32_t)(it.kb1 - it.kb0);  // only B stages
                 }
-                if (!ok) break;
-                umma_commit(acc_full + buf);
                 ++li;
             }
             umma_commit(mma_done);
@@ -982,9 +1220,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         // ---------------------------------------------------------------- epilogue
         EpiCtx c;
         c.p = &p;
-        c.ring = ring;
-        c.tstage = tstage;
-        c.meta = meta;
+        c.perm_s = perm_s;
         c.tmem_base = tmem_base;
         c.delta_col = (uint32_t)(NB * p.nt);
         c.etid = threadIdx.x - 64;
@@ -996,48 +1232,74 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         c.nt = p.nt;
         c.y_bf16 = p.y_bf16;
         c.n_cta = p.n_cta;
-        c.rpmax = p.rpmax;
-        c.ring_chunks = p.ring_chunks;
-        c.total_iters = p.total_iters;
+        c.pack_ch = p.pack_ch;
+        c.total_iters = ss->iter_begin[p.n_mod];
         c.partials = p.partials;
         c.tile_counters = p.tile_counters;
-        c.perm = p.perm;
-        c.seg_start = p.seg_start;
-        c.seg_adapter = p.seg_adapter;
-        c.n_seg = p.n_seg;
         volatile int *flag = reinterpret_cast<volatile int *>(misc + 2);
+        if (p.decode)
+            for (int q = c.etid; q < p.n; q += 128) perm_s[q] = p.perm[q];
+        named_bar_sync(1, 128);
         DrainBufs db;
-        db.ybuf = ring;
-        db.ybuf_bytes = (uint32_t)p.ring_chunks * 128 * 16;
+        db.ybuf = ybuf;
+        db.ybuf_bytes = kYBufBytes;
         db.stage = smem;
         db.stage_bytes = (uint32_t)S * stage_bytes;
         db.ld_bar = ld_bar;
         db.ld_phase = 0;
-        // The expand of a tile this CTA heads is prepared one item ahead when there are two
-        // accumulator/delta buffer pairs, so it overlaps the MMAs of the item before it.
+        const uint32_t lane_off = (uint32_t)c.lane_base << 16;
         Sched sc;
-        sc.begin(p, blockIdx.x);
-        Item cur, nxt;
-        bool has_cur = sc.next(p, cur);
-        uint32_t li = 0;
-        if (has_cur && cur.kb0 == 0) init_expand(c, cur, 0);
+        sc.begin(p, *ss, blockIdx.x);
+        Item cur;
+        bool has_cur = sc.next(p, *ss, cur);
+        uint32_t k = 0, li = 0, use0 = 0, use1 = 0, bpar = 0;
         while (has_cur) {
             const int buf = li % NB;
-            const bool has_nxt = sc.next(p, nxt);
-            if (has_nxt && NB == 2 && nxt.kb0 == 0) init_expand(c, nxt, (li + 1) % 2);
-            const bool full_ok = mbar_wait(acc_full + buf, (li / NB) & 1, abort_flag, p.err);
-            if (named_bar_or(1, 128, !full_ok)) break;
+            const bool last = !sc.more(p);
+            const int nw = item_w(cur), nbs = item_b(cur);
+            bool ok = true;
+            if (nbs > 0) {
+                // expand: zero this item's delta columns, then every B stage adds its slots' rows
+                const uint32_t tdel = tmem_base + lane_off + c.delta_col + (uint32_t)(buf * p.nt);
+                const int row0 = cur.chunk * p.nt;
+                const int ncols = p.decode ? p.n : min(p.nt, p.n - row0);
+                float z[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) z[i] = 0.f;
+                for (int c0 = 0; c0 < ncols; c0 += 16) tmem_st16(tdel + (uint32_t)c0, z);
+                tmem_st_wait();
+                Mix mx;
+                mx.begin(cur);
+                for (int i = cur.kb0; i < cur.kb1 && ok; ++i, ++k) {
+                    if (!mx.step()) continue;  // W k-blocks go to the MMA warp
+                    const int s = k % S;
+                    ok = !named_bar_or(1, 128, !mbar_wait(bfull + s, (bpar >> s) & 1u, abort_flag, p.err));
+                    if (!ok) break;
+                    bpar ^= 1u << s;
+                    const uint8_t *sa = smem + (size_t)s * stage_bytes;
+                    expand_stage(c, sa, sa + a_bytes, tdel, row0);
+                    named_bar_sync(1, 128);  // every warp is done with the stage
+                    if (c.etid == 0) mbar_arrive(empty + s);
+                }
+                tmem_st_wait();
+            } else {
+                k += (uint32_t)nw;
+            }
+            if (!ok) break;
+            if (nw > 0) {
+                const uint32_t use = buf ? use1 : use0;
+                ok = mbar_wait(acc_full + buf, use & 1, abort_flag, p.err);
+            }
+            if (named_bar_or(1, 128, !ok)) break;
             tc_fence_after();
-            drain(c, cur, buf, !has_nxt, flag, abort_flag, db);
+            drain(c, cur, buf, nw > 0, nbs > 0, last, flag, abort_flag, db);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_free + buf);
-            // the staging buffers live in the ring, which the next expand reuses
-            if (c.etid == 0) bulk_wait_read<0>();
-            named_bar_sync(1, 128);
-            if (has_nxt && NB == 1 && nxt.kb0 == 0) init_expand(c, nxt, 0);
-            cur = nxt;
-            has_cur = has_nxt;
+            if (nw > 0) {
+                if (lane == 0) mbar_arrive(acc_free + buf);
+                if (buf) ++use1; else ++use0;
+            }
+            has_cur = sc.next(p, *ss, cur);
             ++li;
         }
         if (c.etid == 0) bulk_wait<0>();  // every output store has been performed
@@ -1053,10 +1315,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
 // ====================================================================== launchers ==========
 
-size_t gemm_smem_bytes(int nt, int n_stages, int ring_chunks, int rpmax) {
+size_t gemm_smem_bytes(int nt, int n_stages) {
     const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2;
-    return 1024 + stage * n_stages + (size_t)ring_chunks * 128 * 16 + (size_t)16 * rpmax * 4 + sizeof(EpiMeta) +
-           8 * (2 * (size_t)n_stages + 7) + 16;
+    return 1024 + stage * n_stages + kYBufBytes + 4 * LORA_MAX_DECODE_ROWS + sizeof(SchedSmem) +
+           8 * (3 * (size_t)n_stages + 6) + 16;
+}
+
+bool plan_gemm(GemmParams &gp, size_t *smem_bytes) {
+    // TMEM: n_acc accumulator buffers of nt columns, then one expand-delta buffer per accumulator
+    gp.n_acc = 4 * gp.nt <= 512 ? 2 : 1;
+    gp.tmem_cols = 32;
+    while (gp.tmem_cols < 2 * gp.n_acc * gp.nt) gp.tmem_cols <<= 1;
+    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)gp.nt * kBK * 2;
+    const size_t fixed = gemm_smem_bytes(gp.nt, 0);
+    gp.n_stages = (int)std::min<size_t>(kMaxStages, (227 * 1024 - fixed - 16 * kMaxStages) / stage);
+    *smem_bytes = gemm_smem_bytes(gp.nt, gp.n_stages);
+    return gp.n_stages >= 2;
 }
 
 cudaError_t launch_prep_decode(const PrepParams &p, cudaStream_t s) {

@@ -44,8 +44,11 @@ constexpr size_t kOffNSeg = al(kOffSegAdapter + 4 * 256);
 constexpr size_t kOffErr = al(kOffNSeg + 16);                     // from here up to kOffT:
 constexpr size_t kOffShrinkCnt = al(kOffErr + 16);                // cleared at every call
 constexpr size_t kOffTileCnt = al(kOffShrinkCnt + 4 * kStMaxUnits);
-constexpr size_t kOffT = al(kOffTileCnt + 4 * (kStMaxDout / kBM));
-constexpr size_t kOffShrinkPart = al(kOffT + 4 * (size_t)kStMaxRows * LORA_MAX_RANK);
+constexpr size_t kOffT = al(kOffTileCnt + 4 * (kStMaxDout / kBM));  // packed t of the expand
+constexpr size_t kOffPacks = al(kOffT + 4 * kPackedTFloats);
+constexpr size_t kOffTpos = al(kOffPacks + sizeof(BPackG) * kMaxPacks);
+constexpr size_t kOffNPacks = al(kOffTpos + 4 * LORA_MAX_DECODE_ROWS);
+constexpr size_t kOffShrinkPart = al(kOffNPacks + 16);
 constexpr size_t kOffGemmPart = al(kOffShrinkPart + 4 * (size_t)kStKsMax * kStMaxRows * LORA_MAX_RANK);
 constexpr size_t kStaticBytes = al(kOffGemmPart + 4 * (size_t)kStMaxCta * 2 * kBM * kStMaxRows);
 static_assert(kOffT % 256 == 0 && kOffShrinkPart % 256 == 0 && kOffGemmPart % 256 == 0, "alignment");
@@ -127,6 +130,10 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     int32_t *n_seg = reinterpret_cast<int32_t *>(scratch + kOffNSeg);
     int32_t *err = reinterpret_cast<int32_t *>(scratch + kOffErr);
     float *T = reinterpret_cast<float *>(scratch + kOffT);
+    BPackG *packs = reinterpret_cast<BPackG *>(scratch + kOffPacks);
+    int32_t *tpos = reinterpret_cast<int32_t *>(scratch + kOffTpos);
+    int32_t *n_packs = reinterpret_cast<int32_t *>(scratch + kOffNPacks);
+    const int nt = (n + 15) & ~15;
 
     // the previous call leaves its contents behind: zero the counters and the error word
     e = cudaMemsetAsync(scratch + kOffErr, 0, kOffT - kOffErr, s);
@@ -150,6 +157,10 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     pp.seg_adapter = seg_adapter;
     pp.n_seg = n_seg;
     pp.err = err;
+    pp.packs[0] = packs;
+    pp.tpos[0] = tpos;
+    pp.n_packs = n_packs;
+    pp.pack_ch = pack_ch(nt);
     if ((e = launch_prep_decode(pp, s)) != cudaSuccess)
         return fail(LORA_ECUDA, std::string("prep kernel: ") + cudaGetErrorString(e));
 
@@ -171,6 +182,7 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     sp.x[0] = static_cast<const uint16_t *>(x);
     sp.table[0] = table;
     sp.T[0] = T;
+    sp.tpos[0] = tpos;
     sp.d_in[0] = d_in;
     sp.kc[0] = std::min(kShrinkDecKC, d_in);
     sp.ksplit[0] = (d_in + sp.kc[0] - 1) / sp.kc[0];
@@ -183,7 +195,7 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     memset(&gp, 0, sizeof gp);
     gp.n_mod = 1;
     gp.n = n;
-    gp.nt = (n + 15) & ~15;
+    gp.nt = nt;
     gp.n_chunks = 1;
     gp.decode = 1;
     gp.stream_k = 1;
@@ -201,20 +213,14 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     gm.d_out = d_out;
     gm.m_tiles = (d_out + kBM - 1) / kBM;
     gm.k_blocks = (d_in + kBK - 1) / kBK;
-    gm.iter_begin = 0;
     gm.tile_begin = 0;
+    gm.packs = packs;
     gp.total_tiles = gm.m_tiles;
-    gp.total_iters = (int64_t)gm.m_tiles * gm.k_blocks;
-    gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, gp.total_iters / 4));
-    gp.n_acc = 4 * gp.nt <= 512 ? 2 : 1;
-    gp.tmem_cols = 32;
-    while (gp.tmem_cols < 2 * gp.n_acc * gp.nt) gp.tmem_cols <<= 1;
-    // per-thread staging for the expand's B rows: small for low ranks, more for rank 64
-    gp.ring_chunks = rpmax <= 16 ? 16 : 32;
-    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)gp.nt * kBK * 2;
-    const size_t fixed = gemm_smem_bytes(gp.nt, 0, gp.ring_chunks, rpmax);
-    gp.n_stages = (int)std::min<size_t>(kMaxStages, (227 * 1024 - fixed - 16 * kMaxStages) / stage);
-    if (gp.n_stages < 2) return LORA_EUNSUPPORTED;
+    gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, (int64_t)gm.m_tiles * gm.k_blocks / 4));
+    gp.n_packs = n_packs;
+    gp.pack_ch = pack_ch(nt);
+    size_t smem = 0;
+    if (!plan_gemm(gp, &smem)) return fail(LORA_EUNSUPPORTED, "no two pipeline stages fit shared memory");
     gp.perm = perm;
     gp.seg_start = seg_start;
     gp.seg_adapter = seg_adapter;
@@ -222,7 +228,6 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     gp.partials = reinterpret_cast<float *>(scratch + kOffGemmPart);
     gp.tile_counters = reinterpret_cast<int32_t *>(scratch + kOffTileCnt);
     gp.err = err;
-    const size_t smem = gemm_smem_bytes(gp.nt, gp.n_stages, gp.ring_chunks, rpmax);
     if ((e = launch_gemm(gp, smem, s)) != cudaSuccess)
         return fail(LORA_ECUDA, std::string("gemm kernel: ") + cudaGetErrorString(e));
     return LORA_OK;
