@@ -618,6 +618,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
         gm.d_out = ms.d_out;
         gm.m_tiles = (ms.d_out + kBM - 1) / kBM;
         gm.k_blocks = (ms.d_in + kBK - 1) / kBK;
+        gm.iter_begin = iters;
         gm.tile_begin = tiles;
         const int mt = gm.m_tiles * gp.n_chunks;
         tiles += mt;
@@ -625,6 +626,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     }
     if (gp.stream_k && tiles > p->tile_cap) return LORA_EUNSUPPORTED;
     gp.total_tiles = tiles;
+    gp.total_iters = iters;
     if (gp.stream_k) {
         // every CTA gets at least 4 k-blocks, so all ranges are non-empty
         gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(p->num_sms, iters / 4));

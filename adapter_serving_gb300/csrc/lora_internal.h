@@ -98,6 +98,7 @@ struct GemmModule {
     const BPackG *packs;       // decode: this module's packs
     int32_t d_in, d_out;
     int32_t m_tiles, k_blocks;
+    int64_t iter_begin;        // flattened (tile, W k-block) index where this module starts
     int32_t tile_begin;        // first global tile index of this module
     int32_t pad_;
 };
@@ -112,6 +113,7 @@ struct GemmParams {
     int32_t stream_k;      // 1: contiguous (tile, k-block) ranges per CTA; 0: whole tiles round robin
     int32_t n_cta;
     int32_t total_tiles;
+    int64_t total_iters;       // W k-blocks of all tiles (the stream-K space)
     int32_t rpmax;         // T row stride
     int32_t y_bf16;
     int32_t n_stages;

@@ -540,21 +540,17 @@ __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const 
 //
 // One persistent CTA per SM, four roles: warp 0 is the TMA producer, lane 0 of warp 1 issues
 // tcgen05.mma, warps 2-5 are the epilogue (TMEM lane quarter = warp % 4).  A tile is 128 rows
-// of W (MMA M) by the rows of the batch or of a row chunk (MMA N).  Its iterations are the
-// k-blocks of W (64 wide) followed by its B stages (the expand, see BStageHdr); decode spreads
-// the flattened (tile, iteration) space evenly over the CTAs (stream-K), grouped rows take whole
-// tiles round robin.
+// of W (MMA M) by the rows of the batch or of a row chunk (MMA N).  Decode spreads the flattened
+// (tile, W k-block) space evenly over the CTAs (stream-K), grouped rows take whole tiles round
+// robin.  A tile's nb B stages (the expand, see BStageHdr) ride along with its k-blocks: pack j
+// belongs to k-block floor(j kbn / nb) in the sense that the packs [P(kb), P(kb + 1)),
+// P(kb) = floor(kb nb / kbn), follow k-block kb in the stage ring.  So a piece of a tile carries
+// the packs in proportion to its k-blocks, and where the pieces split never depends on the
+// adapters of the batch.
 
 struct Item {
-    int32_t m, w_tile, chunk, kb0, kb1, kbn, ext, tile;
-    int64_t it0;  // flattened index of the tile's first iteration
-};
-
-// Where each module's tiles start in the flattened iteration space; built by one thread at
-// kernel start because the number of B stages per tile comes from the prep kernel.
-struct SchedSmem {
-    int64_t iter_begin[LORA_MAX_MODULES + 1];
-    int32_t ext[LORA_MAX_MODULES];  // iterations of one tile: k-blocks + B stages
+    int32_t m, w_tile, chunk, kb0, kb1, kbn, nbs, tile;
+    int64_t it0;  // flattened index of the tile's first W k-block
 };
 
 __device__ __forceinline__ void tile_coords(const GemmParams &p, int m, int lt, Item &it) {
@@ -570,34 +566,34 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int m, int lt, 
 struct Sched {
     int64_t x, e;
     int32_t j, cta;
-    __device__ void begin(const GemmParams &p, const SchedSmem &ss, int c) {
+    __device__ void begin(const GemmParams &p, int c) {
         cta = c;
         j = 0;
         if (p.stream_k) {
-            const int64_t tot = ss.iter_begin[p.n_mod];
-            x = (int64_t)c * tot / p.n_cta;
-            e = (int64_t)(c + 1) * tot / p.n_cta;
+            x = (int64_t)c * p.total_iters / p.n_cta;
+            e = (int64_t)(c + 1) * p.total_iters / p.n_cta;
         }
     }
     // whether next() has another item to give
     __device__ __forceinline__ bool more(const GemmParams &p) const {
         return p.stream_k ? x < e : cta + j * p.n_cta < p.total_tiles;
     }
-    __device__ bool next(const GemmParams &p, const SchedSmem &ss, Item &it) {
+    // `npk`: B stages per tile of each module (decode, shared memory)
+    __device__ bool next(const GemmParams &p, const int32_t *npk, Item &it) {
         if (p.stream_k) {
             if (x >= e) return false;
             int m = 0;
-            while (m + 1 < p.n_mod && ss.iter_begin[m + 1] <= x) ++m;
-            const int ext = ss.ext[m];
-            const int64_t local = x - ss.iter_begin[m];
-            const int lt = (int)(local / ext);
+            while (m + 1 < p.n_mod && p.mod[m + 1].iter_begin <= x) ++m;
+            const int kbn = p.mod[m].k_blocks;
+            const int64_t local = x - p.mod[m].iter_begin;
+            const int lt = (int)(local / kbn);
             it.m = m;
-            it.kbn = p.mod[m].k_blocks;
-            it.ext = ext;
-            it.kb0 = (int)(local - (int64_t)lt * ext);
-            it.kb1 = (int)((e - x) < (int64_t)(ext - it.kb0) ? it.kb0 + (e - x) : ext);
+            it.kbn = kbn;
+            it.nbs = npk[m];
+            it.kb0 = (int)(local - (int64_t)lt * kbn);
+            it.kb1 = (int)((e - x) < (int64_t)(kbn - it.kb0) ? it.kb0 + (e - x) : kbn);
             it.tile = p.mod[m].tile_begin + lt;
-            it.it0 = ss.iter_begin[m] + (int64_t)lt * ext;
+            it.it0 = p.mod[m].iter_begin + (int64_t)lt * kbn;
             tile_coords(p, m, lt, it);
             x += it.kb1 - it.kb0;
             return true;
@@ -610,41 +606,40 @@ struct Sched {
         const int lt = t - p.mod[m].tile_begin;
         it.m = m;
         it.kbn = p.mod[m].k_blocks;
+        it.kb0 = 0;
+        it.kb1 = it.kbn;
         it.tile = t;
         it.it0 = 0;
         tile_coords(p, m, lt, it);
-        it.ext = it.kbn + (p.chunk_nb ? p.chunk_nb[it.chunk] : 0);
-        it.kb0 = 0;
-        it.kb1 = it.ext;
+        it.nbs = p.chunk_nb ? p.chunk_nb[it.chunk] : 0;
         return true;
     }
 };
 
-// A tile's ext = kbn + nb iterations interleave its nb B stages evenly among its kbn W k-blocks:
-// iteration i is a B stage when floor((i + 1) nb / ext) > floor(i nb / ext).  Iteration 0 is always
-// a W k-block, so the piece holding k-block 0 is the one holding iteration 0.
-__device__ __forceinline__ int b_before(const Item &it, int i) { return i * (it.ext - it.kbn) / it.ext; }
-// W k-blocks and B stages of an item
-__device__ __forceinline__ int item_b(const Item &it) { return b_before(it, it.kb1) - b_before(it, it.kb0); }
-__device__ __forceinline__ int item_w(const Item &it) { return it.kb1 - it.kb0 - item_b(it); }
-// Walks an item's iterations without a division per step: acc = (i nb) mod ext, b = B stages
-// before iteration i.
+// The item's packs: [P(kb0), P(kb1)) with P(kb) = floor(kb nb / kbn).
+__device__ __forceinline__ int pack_of(const Item &it, int kb) { return kb * it.nbs / it.kbn; }
+__device__ __forceinline__ int item_b(const Item &it) { return pack_of(it, it.kb1) - pack_of(it, it.kb0); }
+
+// Walks an item's k-blocks without a division per step: after k-block kb the packs
+// [P(kb), P(kb + 1)) follow; acc = (kb nb) mod kbn, b = P(kb).
 struct Mix {
-    int nb, ext, acc, b;
+    int nb, kbn, acc, b;
     __device__ __forceinline__ void begin(const Item &it) {
-        nb = it.ext - it.kbn;
-        ext = it.ext;
+        nb = it.nbs;
+        kbn = it.kbn;
         const int t = it.kb0 * nb;
-        b = t / ext;
-        acc = t - b * ext;
+        b = t / kbn;
+        acc = t - b * kbn;
     }
-    // whether the current iteration is a B stage (its pack is `b` before the call); moves on
-    __device__ __forceinline__ bool step() {
+    // number of packs that follow the current k-block (they start at `b` before the call)
+    __device__ __forceinline__ int after_w() {
         acc += nb;
-        if (acc < ext) return false;
-        acc -= ext;
-        ++b;
-        return true;
+        int cnt = 0;
+        while (acc >= kbn) {
+            acc -= kbn;
+            ++cnt;
+        }
+        return cnt;
     }
 };
 
@@ -889,7 +884,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool wi
         }
     };
 
-    if (head && it.kb1 == it.ext) {
+    if (head && it.kb1 == it.kbn) {
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
             own_cols16(tacc, tdel, with_acc, with_delta, c0, v);
@@ -900,7 +895,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool wi
 
     // ---- partial tile (stream-K) ----
     const int c_first = (int)(((it.it0 + 1) * n_cta - 1) / total_iters);  // CTA holding iteration it0
-    const int c_last = (int)(((it.it0 + it.ext) * n_cta - 1) / total_iters);
+    const int c_last = (int)(((it.it0 + it.kbn) * n_cta - 1) / total_iters);
     const int nc = c_last - c_first + 1;
     const int self_idx = (int)blockIdx.x - c_first;
     int32_t *counter = c.tile_counters + it.tile;
@@ -993,12 +988,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const uint32_t stage_bytes = a_bytes + b_bytes;
     uint8_t *ybuf = smem + (size_t)S * stage_bytes;  // epilogue y staging
     int32_t *perm_s = reinterpret_cast<int32_t *>(ybuf + kYBufBytes);
-    SchedSmem *ss = reinterpret_cast<SchedSmem *>(perm_s + LORA_MAX_DECODE_ROWS);
+    int32_t *npk = perm_s + LORA_MAX_DECODE_ROWS;  // [LORA_MAX_MODULES] packs per tile (decode)
     // A stage slot is filled with either W k-blocks (wfull, consumed by the MMA warp) or a B stage
     // (bfull, consumed by the epilogue).  Each consumer skips the other kind, so each kind has its
     // own barrier and every consumer keeps its own per-slot parity: a parity wait is only sound
     // when the waiter cannot fall two phases behind, which holds per kind but not across kinds.
-    uint64_t *wfull = reinterpret_cast<uint64_t *>(ss + 1);
+    uint64_t *wfull = reinterpret_cast<uint64_t *>(npk + LORA_MAX_MODULES);
     uint64_t *bfull = wfull + S;
     uint64_t *empty = bfull + S;
     uint64_t *acc_full = empty + S;
@@ -1023,15 +1018,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         misc[1] = 0;
         misc[2] = 0;
         fence_mbar_init();
-        // the flattened schedule: per module, tiles x (k-blocks + B stages)
-        int64_t ib = 0;
-        for (int m = 0; m < p.n_mod; ++m) {
-            const int ext = p.mod[m].k_blocks + (p.stream_k && p.n_packs ? p.n_packs[m] : 0);
-            ss->ext[m] = ext;
-            ss->iter_begin[m] = ib;
-            ib += (int64_t)p.mod[m].m_tiles * p.n_chunks * ext;
-        }
-        ss->iter_begin[p.n_mod] = ib;
+        for (int m = 0; m < p.n_mod; ++m) npk[m] = (p.stream_k && p.n_packs) ? p.n_packs[m] : 0;
     }
     if (warp == 0 && lane == 0) {
         for (int m = 0; m < p.n_mod; ++m) {
@@ -1051,7 +1038,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const uint64_t pol_w = p.decode ? l2_policy_evict_first() : l2_policy_evict_normal();
         const uint64_t pol_x = l2_policy_evict_last();
         Sched sc;
-        sc.begin(p, *ss, blockIdx.x);
+        sc.begin(p, blockIdx.x);
         Item it;
         uint32_t k = 0;  // stage fills issued
         bool ok = true;
@@ -1072,84 +1059,89 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             if (lane == 0) got = mbar_wait(empty + kk % S, ((kk / S) & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
             return __shfl_sync(0xffffffffu, got, 0) != 0;
         };
-        while (ok && sc.next(p, *ss, it)) {
+        while (ok && sc.next(p, npk, it)) {
             const GemmModule &M = p.mod[it.m];
             const int o0 = it.w_tile * kBM, row0 = it.chunk * p.nt;
             const int orows = min(kBM, M.d_out - o0);
-            const int b0 = b_before(it, it.kb0), b1 = b_before(it, it.kb1);  // the item's packs
+            const int b1 = pack_of(it, it.kb1);
+            Mix mx;
+            mx.begin(it);
             // decode: the first pack of the item's B stages, fetched ahead
             uint4 rec = make_uint4(0, 0, 0, 0);
-            if (p.stream_k && b1 > b0 && lane <= kPackSlots)
-                rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + b0) + lane);
+            if (p.stream_k && b1 > mx.b && lane <= kPackSlots)
+                rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + mx.b) + lane);
             // grouped rows: the chunk's slots in order (segment, run of pf_ch rows)
             int sg = 0, r = row0;
             const int row1 = min(p.n, row0 + p.nt);
-            if (!p.stream_k && b1 > b0) sg = p.chunk_seg0[it.chunk];
-            Mix mx;
-            mx.begin(it);
-            for (int i = it.kb0; i < it.kb1; ++i, ++k) {
+            if (!p.stream_k && b1 > mx.b) sg = p.chunk_seg0[it.chunk];
+            for (int kb = it.kb0; kb < it.kb1 && ok; ++kb) {
+                // ---- W k-block kb
                 if (!acquire(k)) {
                     ok = false;
                     break;
                 }
-                uint8_t *sa = smem + (size_t)(k % S) * stage_bytes;
-                uint8_t *sx = sa + a_bytes;
-                const int jb = mx.b;
-                if (!mx.step()) {
-                    // ---- W k-block i - jb
-                    const int kb = i - jb;
-                    note_fill(k % S, false);
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(wfull + k % S, stage_bytes);
-                        tma_load_2d(sa, &M.tmW, wfull + k % S, kb * kBK, o0, pol_w);
-                        tma_load_2d(sa + a_bytes, &M.tmX, wfull + k % S, kb * kBK, row0, pol_x);
-                    }
-                    continue;
+                note_fill(k % S, false);
+                if (lane == 0) {
+                    uint8_t *sa = smem + (size_t)(k % S) * stage_bytes;
+                    mbar_arrive_expect_tx(wfull + k % S, stage_bytes);
+                    tma_load_2d(sa, &M.tmW, wfull + k % S, kb * kBK, o0, pol_w);
+                    tma_load_2d(sa + a_bytes, &M.tmX, wfull + k % S, kb * kBK, row0, pol_x);
                 }
-                // ---- B stage jb
-                uint64_t *bar = bfull + k % S;
-                note_fill(k % S, true);
-                if (p.stream_k) {
-                    const uint4 cur = rec;
-                    if (jb + 1 < b1 && lane <= kPackSlots)
-                        rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + jb + 1) + lane);
-                    produce_pack(cur, M, o0, orows, p.pack_ch, sa, sx, bar, lane);
-                } else if (lane == 0) {
-                    const int ns = *p.n_seg;
-                    int s1 = 0, a = -1;
-                    for (; sg < ns; ++sg) {  // the next segment with an adapter and rows left in the chunk
-                        s1 = min(p.seg_start[sg + 1], row1);
-                        a = p.seg_adapter[sg];
-                        r = max(r, p.seg_start[sg]);
-                        if (a >= 0 && r < s1) break;
+                ++k;
+                // ---- the packs that follow it
+                const int nb = mx.after_w();
+                for (int q = 0; q < nb; ++q, ++mx.b, ++k) {
+                    const int jb = mx.b;
+                    if (!acquire(k)) {
+                        ok = false;
+                        break;
                     }
-                    BStageHdr *hdr = reinterpret_cast<BStageHdr *>(sx);
-                    if (sg >= ns) {  // the chunk has fewer slots than counted: an empty stage
-                        report(p.err, LORA_DEVERR_BAD_SEGMENTS, it.chunk);
-                        hdr->nslots = 0;
+                    uint8_t *sa = smem + (size_t)(k % S) * stage_bytes;
+                    uint8_t *sx = sa + a_bytes;
+                    uint64_t *bar = bfull + k % S;
+                    note_fill(k % S, true);
+                    if (p.stream_k) {
+                        const uint4 cur = rec;
+                        if (jb + 1 < b1 && lane <= kPackSlots)
+                            rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + jb + 1) + lane);
+                        produce_pack(cur, M, o0, orows, p.pack_ch, sa, sx, bar, lane);
+                    } else if (lane == 0) {
+                        const int ns = *p.n_seg;
+                        int s1 = 0, a = -1;
+                        for (; sg < ns; ++sg) {  // the next segment with an adapter and rows left in the chunk
+                            s1 = min(p.seg_start[sg + 1], row1);
+                            a = p.seg_adapter[sg];
+                            r = max(r, p.seg_start[sg]);
+                            if (a >= 0 && r < s1) break;
+                        }
+                        BStageHdr *hdr = reinterpret_cast<BStageHdr *>(sx);
+                        if (sg >= ns) {  // the chunk has fewer slots than counted: an empty stage
+                            report(p.err, LORA_DEVERR_BAD_SEGMENTS, it.chunk);
+                            hdr->nslots = 0;
+                            hdr->singles8 = 0;
+                            fence_proxy_async_smem();
+                            mbar_arrive(bar);
+                            continue;
+                        }
+                        const int nr = min(p.pf_ch, s1 - r);
+                        const PoolEntry e = M.table[a];
+                        BSlotS sl;
+                        sl.q0 = r;
+                        sl.nrows = (int16_t)nr;
+                        sl.rp = (int16_t)e.rp;
+                        sl.off = 0;
+                        sl.tstride = (int16_t)p.rpmax;
+                        sl.toff = 0;
+                        hdr->nslots = 1;
                         hdr->singles8 = 0;
-                        fence_proxy_async_smem();
-                        mbar_arrive(bar);
-                        continue;
+                        hdr->slot[0] = sl;
+                        fence_proxy_async_smem();  // the slot is refilled by TMA later
+                        const uint32_t bb = (uint32_t)(orows * e.rp * 2), tb = (uint32_t)(nr * p.rpmax * 4);
+                        mbar_arrive_expect_tx(bar, bb + tb);
+                        bulk_load(sa, e.B + (size_t)o0 * e.rp, bb, bar);
+                        bulk_load(sx + kStageHdrBytes, M.T + (size_t)r * p.rpmax, tb, bar);
+                        r += nr;
                     }
-                    const int nr = min(p.pf_ch, s1 - r);
-                    const PoolEntry e = M.table[a];
-                    BSlotS sl;
-                    sl.q0 = r;
-                    sl.nrows = (int16_t)nr;
-                    sl.rp = (int16_t)e.rp;
-                    sl.off = 0;
-                    sl.tstride = (int16_t)p.rpmax;
-                    sl.toff = 0;
-                    hdr->nslots = 1;
-                    hdr->singles8 = 0;
-                    hdr->slot[0] = sl;
-                    fence_proxy_async_smem();  // the slot is refilled by TMA later
-                    const uint32_t bb = (uint32_t)(orows * e.rp * 2), tb = (uint32_t)(nr * p.rpmax * 4);
-                    mbar_arrive_expect_tx(bar, bb + tb);
-                    bulk_load(sa, e.B + (size_t)o0 * e.rp, bb, bar);
-                    bulk_load(sx + kStageHdrBytes, M.T + (size_t)r * p.rpmax, tb, bar);
-                    r += nr;
                 }
             }
         }
@@ -1168,46 +1160,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             // ------------------------------------------------------------ MMA issuer
             const uint32_t idesc = idesc_bf16_f32(kBM, (uint32_t)p.nt);
             Sched sc;
-            sc.begin(p, *ss, blockIdx.x);
+            sc.begin(p, blockIdx.x);
             Item it;
             uint32_t k = 0, li = 0, use0 = 0, use1 = 0, wpar = 0;
             bool ok = true;
-            while (ok && sc.next(p, *ss, it)) {
+            while (ok && sc.next(p, npk, it)) {
                 const int buf = li % NB;
-                if (item_w(it) > 0) {
-                    const uint32_t use = buf ? use1 : use0;
-                    if (!mbar_wait(acc_free + buf, (use & 1) ^ 1, abort_flag, p.err)) break;
-                    tc_fence_after();
-                    const uint32_t d = tmem_base + (uint32_t)(buf * p.nt);
-                    bool first = true;
-                    Mix mx;
-                    mx.begin(it);
-                    for (int i = it.kb0; i < it.kb1; ++i, ++k) {
-                        if (mx.step()) continue;  // B stages go to the epilogue
-                        const int s = k % S;
-                        if (!mbar_wait(wfull + s, (wpar >> s) & 1u, abort_flag, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        wpar ^= 1u << s;
-                        tc_fence_after();
-                        const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-                        const uint64_t da = sdesc_kmajor_sw128(sa);
-                        const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes);
-#pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint32_t accum = (!first || kk > 0) ? 1u : 0u;
-                            umma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, accum);
-                        }
-                        first = false;
-                        umma_commit(empty + s);
+                const uint32_t use = buf ? use1 : use0;
+                if (!mbar_wait(acc_free + buf, (use & 1) ^ 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(buf * p.nt);
+                Mix mx;
+                mx.begin(it);
+                for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                    const int s = k % S;
+                    if (!mbar_wait(wfull + s, (wpar >> s) & 1u, abort_flag, p.err)) {
+                        ok = false;
+                        break;
                     }
-                    if (!ok) break;
-                    umma_commit(acc_full + buf);
-                    if (buf) ++use1; else ++use0;
-                } else {
-                    k += (uint32_t)(it.kb1 - it.kb0);  // only B stages
+                    wpar ^= 1u << s;
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+                    const uint64_t da = sdesc_kmajor_sw128(sa);
+                    const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint32_t accum = (kb > it.kb0 || kk > 0) ? 1u : 0u;
+                        umma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, accum);
+                    }
+                    umma_commit(empty + s);
+                    k += 1 + (uint32_t)mx.after_w();  // the packs after it go to the epilogue
                 }
+                if (!ok) break;
+                umma_commit(acc_full + buf);
+                if (buf) ++use1; else ++use0;
                 ++li;
             }
             umma_commit(mma_done);
@@ -1233,7 +1219,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         c.y_bf16 = p.y_bf16;
         c.n_cta = p.n_cta;
         c.pack_ch = p.pack_ch;
-        c.total_iters = ss->iter_begin[p.n_mod];
+        c.total_iters = p.total_iters;
         c.partials = p.partials;
         c.tile_counters = p.tile_counters;
         volatile int *flag = reinterpret_cast<volatile int *>(misc + 2);
@@ -1249,14 +1235,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         db.ld_phase = 0;
         const uint32_t lane_off = (uint32_t)c.lane_base << 16;
         Sched sc;
-        sc.begin(p, *ss, blockIdx.x);
+        sc.begin(p, blockIdx.x);
         Item cur;
-        bool has_cur = sc.next(p, *ss, cur);
+        bool has_cur = sc.next(p, npk, cur);
         uint32_t k = 0, li = 0, use0 = 0, use1 = 0, bpar = 0;
         while (has_cur) {
             const int buf = li % NB;
             const bool last = !sc.more(p);
-            const int nw = item_w(cur), nbs = item_b(cur);
+            const int nbs = item_b(cur);
             bool ok = true;
             if (nbs > 0) {
                 // expand: zero this item's delta columns, then every B stage adds its slots' rows
@@ -1270,36 +1256,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 tmem_st_wait();
                 Mix mx;
                 mx.begin(cur);
-                for (int i = cur.kb0; i < cur.kb1 && ok; ++i, ++k) {
-                    if (!mx.step()) continue;  // W k-blocks go to the MMA warp
-                    const int s = k % S;
-                    ok = !named_bar_or(1, 128, !mbar_wait(bfull + s, (bpar >> s) & 1u, abort_flag, p.err));
-                    if (!ok) break;
-                    bpar ^= 1u << s;
-                    const uint8_t *sa = smem + (size_t)s * stage_bytes;
-                    expand_stage(c, sa, sa + a_bytes, tdel, row0);
-                    named_bar_sync(1, 128);  // every warp is done with the stage
-                    if (c.etid == 0) mbar_arrive(empty + s);
+                for (int kb = cur.kb0; kb < cur.kb1 && ok; ++kb) {
+                    ++k;  // the W k-block goes to the MMA warp
+                    const int nb = mx.after_w();
+                    for (int q = 0; q < nb; ++q, ++k) {
+                        const int s = k % S;
+                        ok = !named_bar_or(1, 128, !mbar_wait(bfull + s, (bpar >> s) & 1u, abort_flag, p.err));
+                        if (!ok) break;
+                        bpar ^= 1u << s;
+                        const uint8_t *sa = smem + (size_t)s * stage_bytes;
+                        expand_stage(c, sa, sa + a_bytes, tdel, row0);
+                        named_bar_sync(1, 128);  // every warp is done with the stage
+                        if (c.etid == 0) mbar_arrive(empty + s);
+                    }
                 }
                 tmem_st_wait();
             } else {
-                k += (uint32_t)nw;
+                k += (uint32_t)(cur.kb1 - cur.kb0);
             }
             if (!ok) break;
-            if (nw > 0) {
-                const uint32_t use = buf ? use1 : use0;
-                ok = mbar_wait(acc_full + buf, use & 1, abort_flag, p.err);
-            }
+            const uint32_t use = buf ? use1 : use0;
+            ok = mbar_wait(acc_full + buf, use & 1, abort_flag, p.err);
             if (named_bar_or(1, 128, !ok)) break;
             tc_fence_after();
-            drain(c, cur, buf, nw > 0, nbs > 0, last, flag, abort_flag, db);
+            drain(c, cur, buf, true, nbs > 0, last, flag, abort_flag, db);
             tc_fence_before();
             __syncwarp();
-            if (nw > 0) {
-                if (lane == 0) mbar_arrive(acc_free + buf);
-                if (buf) ++use1; else ++use0;
-            }
-            has_cur = sc.next(p, *ss, cur);
+            if (lane == 0) mbar_arrive(acc_free + buf);
+            if (buf) ++use1; else ++use0;
+            has_cur = sc.next(p, npk, cur);
             ++li;
         }
         if (c.etid == 0) bulk_wait<0>();  // every output store has been performed
@@ -1317,7 +1302,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
 size_t gemm_smem_bytes(int nt, int n_stages) {
     const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2;
-    return 1024 + stage * n_stages + kYBufBytes + 4 * LORA_MAX_DECODE_ROWS + sizeof(SchedSmem) +
+    return 1024 + stage * n_stages + kYBufBytes + 4 * LORA_MAX_DECODE_ROWS + 4 * LORA_MAX_MODULES +
            8 * (3 * (size_t)n_stages + 6) + 16;
 }
 

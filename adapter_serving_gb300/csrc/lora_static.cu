@@ -213,10 +213,12 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     gm.d_out = d_out;
     gm.m_tiles = (d_out + kBM - 1) / kBM;
     gm.k_blocks = (d_in + kBK - 1) / kBK;
+    gm.iter_begin = 0;
     gm.tile_begin = 0;
     gm.packs = packs;
     gp.total_tiles = gm.m_tiles;
-    gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, (int64_t)gm.m_tiles * gm.k_blocks / 4));
+    gp.total_iters = (int64_t)gm.m_tiles * gm.k_blocks;
+    gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, gp.total_iters / 4));
     gp.n_packs = n_packs;
     gp.pack_ch = pack_ch(nt);
     size_t smem = 0;
