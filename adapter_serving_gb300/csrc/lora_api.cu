@@ -290,7 +290,7 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
     p->ks_cap = (max_din + 511) / 512;
     p->tile_cap = LORA_MAX_MODULES * ((max_dout + kBM - 1) / kBM);
     const size_t R = (size_t)p->max_rows;
-    p->chunk_cap = (int)(R / 256 + 2);
+    p->chunk_cap = (int)(R / 256 + 2);  // row chunks of 256 (grouped rows)
     if ((rc = dev_alloc(p, (void **)&p->perm, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->seg_start, (R + 2) * 4)) ||
         (rc = dev_alloc(p, (void **)&p->seg_adapter, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->n_seg, 16)) ||
         (rc = dev_alloc(p, (void **)&p->err, 16)) ||

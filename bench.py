@@ -47,7 +47,14 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="timed loop only (for profiler launch lists)")
+    ap.add_argument("--workload", default="attn70b", choices=sorted(WORKLOADS),
+                    help="attn70b (the headline) or another of the pages' configurations")
     return ap.parse_args()
+
+
+# name -> (constructor, kind); the headline is attn70b
+WORKLOADS = {"attn70b": (wl.attn70b_decode, "decode"), "all70b": (wl.all70b_decode, "decode"),
+             "zipf": (wl.zipf_pool, "decode"), "prefill": (wl.prefill_segments, "prefill")}
 
 
 def dist_env():
@@ -76,6 +83,25 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 TFLOP/s for a kernel inside a long step (the sustained figure)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 1700.0, "fallback"
+
+
+def step_flops(w):
+    """Dense flops of one step: base 2 n d_in d_out per projection plus the LoRA shrink and
+    expand, 2 n r (d_in + d_out), each row with its own adapter's rank."""
+    ranks = np.array([int(w.ranks[a]) if a >= 0 else 0 for a in w.row_adapters()], np.int64)
+    base = sum(2 * w.n_rows * w.modules[m][0] * w.modules[m][1] for m in w.module_names())
+    lora = sum(int(2 * ranks.sum() * (w.modules[m][0] + w.modules[m][1])) for m in w.module_names())
+    return base, lora
 
 
 class ClockSampler:
@@ -213,14 +239,22 @@ def run_ours(args, w):
     xd = [bf(x) for x in xs]
     Wd = {m: bf(Ws[m]) for m in names}
     yd = {m: torch.empty(w.n_rows, w.modules[m][1], device=dev) for m in names}
-    ids = torch.from_numpy(w.ids).to(dev)
+    grouped = w.ids is None
+    if grouped:  # prefill: contiguous request segments; the base-only run gives every segment -1
+        ids = torch.from_numpy(w.seg_adapter).to(dev)
+        ss_d = torch.from_numpy(w.seg_start).to(dev)
+    else:
+        ids = torch.from_numpy(w.ids).to(dev)
     ids_base = torch.full_like(ids, -1)
     stage_io = [[(names.index(m), xd[st], Wd[m], yd[m]) for m in mods] for st, mods in enumerate(w.stages)]
     stream = torch.cuda.current_stream()
 
     def step(id_t):
         for io in stage_io:
-            pool.layer_forward(io, id_t, w.scale, stream=stream)
+            if grouped:
+                pool.segment_forward(io, ss_d, id_t, w.n_rows, w.scale, stream=stream)
+            else:
+                pool.layer_forward(io, id_t, w.scale, stream=stream)
 
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -268,21 +302,30 @@ def run_ours(args, w):
         ms = float(t.item())
     ab = algorithmic_bytes(w)
     value = world * w.n_rows / (ms / 1e3)
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+    ranks = sorted(set(int(w.ranks[a]) for a in w.used_adapters()))
+    line = {"metric": METRIC if args.workload == "attn70b" else f"{args.workload}: tokens/s", "value": value,
+            "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "batch_rows": w.n_rows, "distinct_adapters": ab["distinct"], "rank": 8,
-                       "projections": "q 8192x8192, k 8192->1024, v 8192->1024, o 8192x8192",
+            "config": {"workload": w.name, "batch_rows": w.n_rows, "distinct_adapters": ab["distinct"],
+                       "ranks": ranks,
+                       "projections": ", ".join(f"{m} {w.modules[m][0]}->{w.modules[m][1]}" for m in names),
                        "calls_per_step": len(w.stages), "output": "fp32",
                        "l2": "flushed before every timed step (256 MiB write)",
                        "parallelism": f"replicas x{world}"},
             "hbm_gbs": ab["total"] / (ms / 1e3) / 1e9,
             "algorithmic_bytes_per_step": ab["total"],
             "gpu_launches": 3 * len(w.stages) * args.steps}
+    if grouped:
+        base_f, lora_f = step_flops(w)
+        tp, tsrc = tensor_peak()
+        line["tensor"] = {"tflops": (base_f + lora_f) / (ms / 1e3) / 1e12, "peak": tp, "peak_source": tsrc,
+                          "frac": (base_f + lora_f) / (ms / 1e3) / 1e12 / tp, "flops_per_step": base_f + lora_f,
+                          "lora_flops_per_step": lora_f}
     if clocks:
         line["clocks"] = clocks
 
-    if not args.no_extras:
+    if not args.no_extras and not grouped:
         # ---- per-kernel device time on the launch stream (library event pairs)
         pool.profile(True)
         timed(args.steps, ids)
@@ -293,7 +336,8 @@ def run_ours(args, w):
         achieved = ab["gemm"] * args.steps / (g_ms / 1e3) / 1e9
         line["roofline"] = {"kernel": "gemm_kernel (tcgen05 base + fused expand)", "bound": "hbm",
                             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                            "peak_source": src, "traffic": GEMM_DRAM_BYTES_PER_LAUNCH,
+                            "peak_source": src,
+                            "traffic": GEMM_DRAM_BYTES_PER_LAUNCH if args.workload == "attn70b" else None,
                             "algorithmic_bytes_per_step": ab["gemm"], "launches_per_step": g_launch / args.steps}
         line["kernel_ms_per_step"] = {k: v[1] / args.steps for k, v in kt.items()}
         s_ms = kt["shrink"][1] / args.steps
@@ -330,7 +374,7 @@ def run_ours(args, w):
         code, detail = pool.last_device_error()
         if code:
             raise RuntimeError(f"device error {L.DEVERR.get(code)} at {detail}")
-        if rank == 0 and not args.no_cpu_baseline:
+        if rank == 0 and not args.no_cpu_baseline and args.workload == "attn70b":
             line["cpu_baseline"] = cpu_baseline(w, xs, Ws, factors)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -350,14 +394,14 @@ def _build():
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per gemm launch, mean of the qkv and
 # o launches of this workload, from an ncu capture of the current gemm kernel; None whenever the
 # kernel has changed since the last capture.
-GEMM_DRAM_BYTES_PER_LAUNCH = 176_051_200
+GEMM_DRAM_BYTES_PER_LAUNCH = None
 
 
 def main():
     args = parse()
     if args.impl == "ours":
         _build()
-    w = wl.attn70b_decode()
+    w = WORKLOADS[args.workload][0]()
     if args.impl == "reference":
         run_reference(args, w)
     else:
