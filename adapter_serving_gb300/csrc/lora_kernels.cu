@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>
+#include <utility>
 
 #include "lora_internal.h"
 #include "ptx.cuh"
@@ -76,8 +77,10 @@ __device__ int checked_id(const PrepParams &p, int id, int where) {
 }
 
 // Exclusive prefix sum over the 256 threads of a block; `total` receives the sum.
-__device__ int block_scan256(int v, int *s_warp, int &total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Exclusive prefix sum over a group of 256 threads (8 warps) that synchronises on named barrier
+// `bar`; `total` receives the sum.
+__device__ int group_scan256(int v, int *s_warp, int &total, int bar) {
+    const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) & 7;
     int x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -85,7 +88,7 @@ __device__ int block_scan256(int v, int *s_warp, int &total) {
         if (lane >= o) x += y;
     }
     if (lane == 31) s_warp[warp] = x;
-    __syncthreads();
+    named_bar_sync(bar, 256);
     int before = 0, tot = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
@@ -93,7 +96,7 @@ __device__ int block_scan256(int v, int *s_warp, int &total) {
         before += w < warp ? t : 0;
         tot += t;
     }
-    __syncthreads();
+    named_bar_sync(bar, 256);
     total = tot;
     return before + x - v;
 }
@@ -104,12 +107,18 @@ __device__ int block_scan256(int v, int *s_warp, int &total) {
 // multiple of 64, so pack j (one B stage) is exactly the slots in units [64 j, 64 j + 64).
 // A slot at unit offset P keeps its t rows at floats [pack_ch * P, pack_ch * (P + rp)) of the
 // module's packed T, so a pack's t rows are one contiguous range too.
+// The prep block has kPrepGroups groups of 256 threads; group g builds the packs of modules
+// g, g + kPrepGroups, ..., synchronising on its own named barrier.
+constexpr int kPrepGroups = 4;
+
 __device__ void build_packs(const PrepParams &p, int ns) {
-    __shared__ int s_warp[8];
-    __shared__ int s_first[320];
-    const int tid = threadIdx.x;
+    __shared__ int s_warp_all[kPrepGroups][8];
+    __shared__ int s_first_all[kPrepGroups][320];
+    const int g = threadIdx.x >> 8, tid = threadIdx.x & 255;
+    const int bar = 1 + g;
+    int *s_warp = s_warp_all[g], *s_first = s_first_all[g];
     const int ch = p.pack_ch;
-    for (int m = 0; m < p.n_mod; ++m) {
+    for (int m = g; m < p.n_mod; m += kPrepGroups) {
         int q0 = 0, q1 = 0, rp = 0, nsl = 0, cls = 4;
         const uint16_t *B = nullptr;
         if (tid < ns) {
@@ -129,7 +138,7 @@ __device__ void build_packs(const PrepParams &p, int ns) {
         int slot_base = 0, unit_base = 0, slots_tot = 0, units_tot = 0;
         for (int c = 0; c < 4; ++c) {
             int tot;
-            const int ex = block_scan256(cls == c ? nsl : 0, s_warp, tot);
+            const int ex = group_scan256(cls == c ? nsl : 0, s_warp, tot, bar);
             if (cls == c) {
                 slot_base = slots_tot + ex;
                 unit_base = units_tot + ex * (64 >> c);
@@ -143,7 +152,7 @@ __device__ void build_packs(const PrepParams &p, int ns) {
             if (P % kPackRanks == 0) s_first[P / kPackRanks] = slot_base + k;
         }
         if (tid == 0) s_first[npk] = slots_tot;
-        __syncthreads();
+        named_bar_sync(bar, 256);
         BPackG *packs = p.packs[m];
         for (int k = 0; k < nsl; ++k) {
             const int P = unit_base + k * rp, j = P / kPackRanks;
@@ -168,18 +177,20 @@ __device__ void build_packs(const PrepParams &p, int ns) {
             for (int q = q0; q < q1; ++q)
                 p.tpos[m][q] = rp > 0 ? ch * (unit_base + ((q - q0) / ch) * rp) + ((q - q0) % ch) * rp : -1;
         if (tid == 0) p.n_packs[m] = npk;
-        __syncthreads();  // s_first is reused by the next module
+        named_bar_sync(bar, 256);  // s_first is reused by the group's next module
     }
 }
 
 // One block of 256 threads, n <= 256 rows.  Position of row i in the stable order:
 // #{j : id_j < id_i} + #{j < i : id_j == id_i}.
-__global__ void __launch_bounds__(256) prep_decode_kernel(const PrepParams p) {
+__global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const PrepParams p) {
     __shared__ int s_id[256];
     __shared__ int s_sorted[256];
     __shared__ int s_scan[256];
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x;  // the row grouping uses threads 0..255; all of them build packs
     const int n = p.n;
+    grid_dep_wait();
+    grid_dep_launch();
     bool seg_ok = true;
     if (p.ids == nullptr) {
         seg_ok = segments_valid(p);
@@ -206,13 +217,16 @@ __global__ void __launch_bounds__(256) prep_decode_kernel(const PrepParams p) {
         s_sorted[pos] = id;
     }
     __syncthreads();
-    int flag = (tid < n) && (tid == 0 || s_sorted[tid] != s_sorted[tid - 1]);
-    s_scan[tid] = flag;
+    int flag = 0;
+    if (tid < 256) {
+        flag = (tid < n) && (tid == 0 || s_sorted[tid] != s_sorted[tid - 1]);
+        s_scan[tid] = flag;
+    }
     __syncthreads();
     for (int off = 1; off < 256; off <<= 1) {
-        int v = tid >= off ? s_scan[tid - off] : 0;
+        const int v = (tid < 256 && tid >= off) ? s_scan[tid - off] : 0;
         __syncthreads();
-        s_scan[tid] += v;
+        if (tid < 256) s_scan[tid] += v;
         __syncthreads();
     }
     if (flag) {
@@ -234,6 +248,8 @@ __global__ void __launch_bounds__(256) prep_decode_kernel(const PrepParams p) {
 // Grouped rows (prefill): validate the table, copy it into the workspace with unusable
 // adapters replaced by -1 (base only).  A malformed table becomes one base-only segment.
 __global__ void __launch_bounds__(1024) prep_segments_kernel(const PrepParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
     const bool ok = segments_valid(p);
     if (!ok) {
         if (threadIdx.x == 0) {
@@ -304,6 +320,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(kShrinkThreads) shrink_kernel(const __grid_constant__ ShrinkParams p) {
     __shared__ __align__(16) uint16_t xs[kShrinkRows * kShrinkKSub];
     __shared__ int s_last;
+    grid_dep_wait();
+    grid_dep_launch();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int m = 0;
     while (m + 1 < p.n_mod && p.split_begin[m + 1] <= (int)blockIdx.y) ++m;
@@ -437,6 +455,8 @@ __global__ void __launch_bounds__(kShrinkThreads) shrink_kernel(const __grid_con
 // splits are combined by the last block of the segment, in split order.
 __global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const __grid_constant__ ShrinkParams p) {
     __shared__ int s_last;
+    grid_dep_wait();
+    grid_dep_launch();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int m = 0;
     while (m + 1 < p.n_mod && p.split_begin[m + 1] <= (int)blockIdx.y) ++m;
@@ -1018,7 +1038,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         misc[1] = 0;
         misc[2] = 0;
         fence_mbar_init();
-        for (int m = 0; m < p.n_mod; ++m) npk[m] = (p.stream_k && p.n_packs) ? p.n_packs[m] : 0;
     }
     if (warp == 0 && lane == 0) {
         for (int m = 0; m < p.n_mod; ++m) {
@@ -1027,6 +1046,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
     }
     if (warp == 1) tmem_alloc(misc, (uint32_t)p.tmem_cols);
+    // everything above overlaps the previous kernel on the stream; from here on its outputs
+    // (segments, packs, t) and the inputs written before it are read
+    grid_dep_wait();
+    grid_dep_launch();
+    if (threadIdx.x == 0)
+        for (int m = 0; m < p.n_mod; ++m) npk[m] = (p.stream_k && p.n_packs) ? p.n_packs[m] : 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1318,22 +1343,36 @@ bool plan_gemm(GemmParams &gp, size_t *smem_bytes) {
     return gp.n_stages >= 2;
 }
 
+// Every hot-path kernel is launched as a programmatic dependent of the one before it on the
+// stream: it may start (and run its prologue) while that one drains, and waits for it with
+// griddepcontrol.wait before reading anything.
+template <class... KArgs, class... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_prep_decode(const PrepParams &p, cudaStream_t s) {
-    prep_decode_kernel<<<1, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(prep_decode_kernel, dim3(1), dim3(256 * kPrepGroups), 0, s, p);
 }
 
 cudaError_t launch_prep_segments(const PrepParams &p, cudaStream_t s) {
-    prep_segments_kernel<<<1, 1024, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(prep_segments_kernel, dim3(1), dim3(1024), 0, s, p);
 }
 
 cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStream_t s) {
-    if (p.by_segment)
-        shrink_decode_kernel<<<dim3(grid_x, grid_y), kShrinkThreads, 0, s>>>(p);
-    else
-        shrink_kernel<<<dim3(grid_x, grid_y), kShrinkThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    if (p.by_segment) return launch_pdl(shrink_decode_kernel, dim3(grid_x, grid_y), dim3(kShrinkThreads), 0, s, p);
+    return launch_pdl(shrink_kernel, dim3(grid_x, grid_y), dim3(kShrinkThreads), 0, s, p);
 }
 
 cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s) {
@@ -1343,8 +1382,7 @@ cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s) 
         if (e != cudaSuccess) return e;
         configured = smem_bytes;
     }
-    gemm_kernel<<<p.n_cta, kGemmThreads, smem_bytes, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_kernel, dim3(p.n_cta), dim3(kGemmThreads), smem_bytes, s, p);
 }
 
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s) {

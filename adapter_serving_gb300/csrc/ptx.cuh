@@ -166,6 +166,14 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
     return v;
 }
 
+// ------------------------------------------------- programmatic dependent launch ------
+// Wait until the grids this one depends on (launched before it on the stream) have completed
+// and their memory is visible; a no-op when the kernel was launched without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel on the stream start launching (its own grid_dep_wait still waits for
+// this whole grid).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- cp.async -----------
 // 16-byte global->shared copy; src_bytes < 16 zero-fills the rest (0 = pure zero fill).
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
