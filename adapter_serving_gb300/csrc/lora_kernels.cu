@@ -66,11 +66,15 @@ __device__ int checked_id(const PrepParams &p, int id, int where) {
         return -1;
     }
     if (id >= 0) {
-        for (int m = 0; m < p.n_mod; ++m) {
-            if (p.table[m][id].rank <= 0) {
-                report(p.err, LORA_DEVERR_NOT_LOADED, where);
-                return -1;
-            }
+        int rank[LORA_MAX_MODULES];  // all loads in flight before the first test
+#pragma unroll
+        for (int m = 0; m < LORA_MAX_MODULES; ++m) rank[m] = m < p.n_mod ? p.table[m][id].rank : 1;
+        bool ok = true;
+#pragma unroll
+        for (int m = 0; m < LORA_MAX_MODULES; ++m) ok = ok && rank[m] > 0;
+        if (!ok) {
+            report(p.err, LORA_DEVERR_NOT_LOADED, where);
+            return -1;
         }
     }
     return id;
@@ -217,24 +221,31 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
         s_sorted[pos] = id;
     }
     __syncthreads();
+    // segment starts: positions whose id differs from the one before; inclusive scan of the
+    // flags (warp shuffles, then the 8 warp totals)
     int flag = 0;
-    if (tid < 256) {
-        flag = (tid < n) && (tid == 0 || s_sorted[tid] != s_sorted[tid - 1]);
-        s_scan[tid] = flag;
+    if (tid < 256) flag = (tid < n) && (tid == 0 || s_sorted[tid] != s_sorted[tid - 1]);
+    int incl = flag;
+    const int lane = tid & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
     }
+    if (tid < 256 && lane == 31) s_scan[tid >> 5] = incl;
     __syncthreads();
-    for (int off = 1; off < 256; off <<= 1) {
-        const int v = (tid < 256 && tid >= off) ? s_scan[tid - off] : 0;
-        __syncthreads();
-        if (tid < 256) s_scan[tid] += v;
-        __syncthreads();
+    int before = 0, ns = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const int t = s_scan[w];
+        before += w < (tid >> 5) ? t : 0;
+        ns += t;
     }
     if (flag) {
-        int seg = s_scan[tid] - 1;
+        const int seg = before + incl - 1;
         p.seg_start[seg] = tid;
         p.seg_adapter[seg] = s_sorted[tid];
     }
-    const int ns = n > 0 ? s_scan[n - 1] : 0;
     if (tid == 0) {
         *p.n_seg = ns;
         p.seg_start[ns] = n;
@@ -453,7 +464,7 @@ __global__ void __launch_bounds__(kShrinkThreads) shrink_kernel(const __grid_con
 // row per pass and walks the split in 2048-wide steps: every lane issues its eight 16-byte
 // loads of A up front, then reads the segment's x rows straight from L2.  Partial sums of the
 // splits are combined by the last block of the segment, in split order.
-__global__ void __launch_bounds__(kShrinkThreads, 2) shrink_decode_kernel(const __grid_constant__ ShrinkParams p) {
+__global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const __grid_constant__ ShrinkParams p) {
     __shared__ int s_last;
     grid_dep_wait();
     grid_dep_launch();
