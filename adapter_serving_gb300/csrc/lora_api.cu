@@ -163,6 +163,7 @@ struct lora_pool {
     std::vector<int> rp_count;        // loaded entries per storage-rank order (for rpmax)
     // workspace
     int32_t *perm = nullptr, *seg_start = nullptr, *seg_adapter = nullptr, *n_seg = nullptr, *err = nullptr;
+    int32_t *qadapter = nullptr;      // [max_rows] decode: adapter of each sorted position
     float *T = nullptr;               // [LORA_MAX_MODULES][max_rows][64]
     float *shrink_part = nullptr;     // [LORA_MAX_MODULES][ks_cap][256][64]
     int32_t *shrink_cnt = nullptr;    // [LORA_MAX_MODULES][256]
@@ -293,6 +294,7 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
     p->chunk_cap = (int)(R / 256 + 2);  // row chunks of 256 (grouped rows)
     if ((rc = dev_alloc(p, (void **)&p->perm, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->seg_start, (R + 2) * 4)) ||
         (rc = dev_alloc(p, (void **)&p->seg_adapter, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->n_seg, 16)) ||
+        (rc = dev_alloc(p, (void **)&p->qadapter, (R + 1) * 4)) ||
         (rc = dev_alloc(p, (void **)&p->err, 16)) ||
         (rc = dev_alloc(p, (void **)&p->T, (size_t)LORA_MAX_MODULES * R * LORA_MAX_RANK * 4)) ||
         (rc = dev_alloc(p, (void **)&p->shrink_part,
@@ -529,6 +531,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     pp.seg_adapter = p->seg_adapter;
     pp.n_seg = p->n_seg;
     pp.err = p->err;
+    pp.qadapter = p->qadapter;
     const int nt = decode ? ((n + 15) & ~15) : 256;  // rows per MMA tile (MMA N)
     const int rpmax = p->rpmax();
     if (decode) {
@@ -564,6 +567,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     sp.seg_start = p->seg_start;
     sp.seg_adapter = p->seg_adapter;
     sp.n_seg = p->n_seg;
+    sp.qadapter = p->qadapter;
     sp.partials = p->shrink_part;
     sp.counters = p->shrink_cnt;
     // decode split width: about 128 KiB of A per block, in whole 2048-wide steps

@@ -154,6 +154,7 @@ struct ShrinkParams {
     const int32_t *seg_adapter;
     const int32_t *n_seg;
     const int32_t *tpos[LORA_MAX_MODULES];  // decode: where position q's t row starts in T
+    const int32_t *qadapter;                // decode: adapter of each sorted position
     float *partials;      // [n_mod][ks_max][n][rpmax]
     int32_t *counters;    // [n_mod][max_units]
 };
@@ -172,6 +173,7 @@ struct PrepParams {
     int32_t *seg_adapter;
     int32_t *n_seg;
     int32_t *err;
+    int32_t *qadapter;                // decode: [n] adapter of each sorted position
     // decode: expand packs per module
     BPackG *packs[LORA_MAX_MODULES];
     int32_t *tpos[LORA_MAX_MODULES];  // [n] float offset of position q's t row in the packed T

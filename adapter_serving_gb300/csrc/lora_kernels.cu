@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
             pos += (v < id) || (v == id && j < tid);
         }
         p.perm[pos] = tid;
+        p.qadapter[pos] = id;
         s_sorted[pos] = id;
     }
     __syncthreads();
@@ -474,10 +475,12 @@ __global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const 
     const int kc = blockIdx.y - p.split_begin[m];
     const int ks = p.ksplit[m];
     if (kc >= ks) return;
+    // one block per sorted position: rows of a shared adapter spread over blocks (its A is read
+    // from L2 after the first), so blocks stay balanced
     const int u = blockIdx.x;
-    if (u >= *p.n_seg) return;
-    const int qlo = p.seg_start[u], qhi = p.seg_start[u + 1];
-    const int a = p.seg_adapter[u];
+    if (u >= p.n) return;
+    const int qlo = u, qhi = u + 1;
+    const int a = p.qadapter[u];
     const int d_in = p.d_in[m];
     const int kbeg = kc * p.kc[m];
     const int kend = min(d_in, kbeg + p.kc[m]);

@@ -41,7 +41,8 @@ constexpr size_t kOffPerm = al(kOffTable + sizeof(PoolEntry) * kStMaxAdapters);
 constexpr size_t kOffSegStart = al(kOffPerm + 4 * 256);
 constexpr size_t kOffSegAdapter = al(kOffSegStart + 4 * 272);
 constexpr size_t kOffNSeg = al(kOffSegAdapter + 4 * 256);
-constexpr size_t kOffErr = al(kOffNSeg + 16);                     // from here up to kOffT:
+constexpr size_t kOffQAdapter = al(kOffNSeg + 16);
+constexpr size_t kOffErr = al(kOffQAdapter + 4 * 256);                     // from here up to kOffT:
 constexpr size_t kOffShrinkCnt = al(kOffErr + 16);                // cleared at every call
 constexpr size_t kOffTileCnt = al(kOffShrinkCnt + 4 * kStMaxUnits);
 constexpr size_t kOffT = al(kOffTileCnt + 4 * (kStMaxDout / kBM));  // packed t of the expand
@@ -129,6 +130,7 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     int32_t *seg_adapter = reinterpret_cast<int32_t *>(scratch + kOffSegAdapter);
     int32_t *n_seg = reinterpret_cast<int32_t *>(scratch + kOffNSeg);
     int32_t *err = reinterpret_cast<int32_t *>(scratch + kOffErr);
+    int32_t *qadapter = reinterpret_cast<int32_t *>(scratch + kOffQAdapter);
     float *T = reinterpret_cast<float *>(scratch + kOffT);
     BPackG *packs = reinterpret_cast<BPackG *>(scratch + kOffPacks);
     int32_t *tpos = reinterpret_cast<int32_t *>(scratch + kOffTpos);
@@ -157,6 +159,7 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     pp.seg_adapter = seg_adapter;
     pp.n_seg = n_seg;
     pp.err = err;
+    pp.qadapter = qadapter;
     pp.packs[0] = packs;
     pp.tpos[0] = tpos;
     pp.n_packs = n_packs;
@@ -177,6 +180,7 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     sp.seg_start = seg_start;
     sp.seg_adapter = seg_adapter;
     sp.n_seg = n_seg;
+    sp.qadapter = qadapter;
     sp.partials = reinterpret_cast<float *>(scratch + kOffShrinkPart);
     sp.counters = reinterpret_cast<int32_t *>(scratch + kOffShrinkCnt);
     sp.x[0] = static_cast<const uint16_t *>(x);
