@@ -762,6 +762,32 @@ __device__ __forceinline__ float dot8_bf16_f32(uint4 b, float4 ta, float4 tb) {
     return acc0 + acc1;
 }
 
+// One slot of a B stage: this lane's row of the slot's B (NCH 16-byte chunks, storage rank 8 NCH)
+// is loaded once, then every position of the slot streams its t row against it.
+template <int NCH>
+__device__ __forceinline__ void expand_slot(const EpiCtx &c, uint32_t brow, uint32_t tslot, int tstride, int nrows,
+                                            int q0, uint32_t tdel, int row0) {
+    uint4 b[NCH];
+    const uint32_t mine = brow + (uint32_t)(c.o * NCH * 16);
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) b[ch] = lds_u128(mine + ch * 16);
+    for (int r = 0; r < nrows; ++r) {
+        const uint32_t trow = tslot + (uint32_t)(r * tstride * 4);
+        float acc[NCH];
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) acc[ch] = dot8_bf16_f32(b[ch], lds128(trow + ch * 32), lds128(trow + ch * 32 + 16));
+#pragma unroll
+        for (int w = 1; w < NCH; w <<= 1)
+#pragma unroll
+            for (int ch = 0; ch + w < NCH; ch += 2 * w) acc[ch] += acc[ch + w];  // fixed pairwise order
+        const int q = q0 + r;  // the same for the whole warp: the guards below are uniform
+        if (q < 0 || q >= c.n) continue;
+        const int col = c.decode ? c.perm_s[q] : q - row0;
+        if (col < 0 || col >= c.nt) continue;
+        tmem_st1(tdel + (uint32_t)col, acc[0]);
+    }
+}
+
 __device__ void expand_stage(const EpiCtx &c, const uint8_t *sa, const uint8_t *sx, uint32_t tdel, int row0) {
     const BStageHdr *hdr = reinterpret_cast<const BStageHdr *>(sx);
     const int nslots = min(hdr->nslots, kPackSlots);
@@ -797,28 +823,14 @@ __device__ void expand_stage(const EpiCtx &c, const uint8_t *sa, const uint8_t *
     }
     for (int e = 0; e < nslots; ++e) {
         const BSlotS sl = hdr->slot[e];
-        const int rp = sl.rp;
-        const uint32_t brow = a_base + (uint32_t)sl.off * 256 + (uint32_t)(c.o * rp * 2);
-        for (int r = 0; r < sl.nrows; ++r) {
-            const uint32_t trow = t_base + (uint32_t)(sl.toff + r * sl.tstride) * 4;
-            float acc0 = 0.f, acc1 = 0.f;
-            for (int j = 0; j < rp; j += 8) {
-                const uint4 b = lds_u128(brow + j * 2);
-                const float4 ta = lds128(trow + j * 4), tb = lds128(trow + j * 4 + 16);
-                acc0 = fmaf(bf16lo(b.x), ta.x, acc0);
-                acc1 = fmaf(bf16hi(b.x), ta.y, acc1);
-                acc0 = fmaf(bf16lo(b.y), ta.z, acc0);
-                acc1 = fmaf(bf16hi(b.y), ta.w, acc1);
-                acc0 = fmaf(bf16lo(b.z), tb.x, acc0);
-                acc1 = fmaf(bf16hi(b.z), tb.y, acc1);
-                acc0 = fmaf(bf16lo(b.w), tb.z, acc0);
-                acc1 = fmaf(bf16hi(b.w), tb.w, acc1);
-            }
-            const int q = sl.q0 + r;  // the same for the whole warp: the guards below are uniform
-            if (q < 0 || q >= c.n) continue;
-            const int col = c.decode ? c.perm_s[q] : q - row0;
-            if (col < 0 || col >= c.nt) continue;
-            tmem_st1(tdel + (uint32_t)col, acc0 + acc1);
+        const uint32_t brow = a_base + (uint32_t)sl.off * 256;
+        const uint32_t tslot = t_base + (uint32_t)sl.toff * 4;
+        switch (sl.rp) {
+            case 8: expand_slot<1>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
+            case 16: expand_slot<2>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
+            case 32: expand_slot<4>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
+            case 64: expand_slot<8>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
+            default: break;
         }
     }
 }
