@@ -767,15 +767,21 @@ __device__ __forceinline__ float dot8_bf16_f32(uint4 b, float4 ta, float4 tb) {
 template <int NCH>
 __device__ __forceinline__ void expand_slot(const EpiCtx &c, uint32_t brow, uint32_t tslot, int tstride, int nrows,
                                             int q0, uint32_t tdel, int row0) {
+    // lane o starts at chunk rot = o / (8 / NCH): the eight lanes of a quarter warp then hit eight
+    // different 16-byte bank groups of their rows (rows are NCH * 16 bytes apart)
+    const int rot = (c.o * NCH / 8) & (NCH - 1);
     uint4 b[NCH];
     const uint32_t mine = brow + (uint32_t)(c.o * NCH * 16);
 #pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) b[ch] = lds_u128(mine + ch * 16);
+    for (int ch = 0; ch < NCH; ++ch) b[ch] = lds_u128(mine + ((ch + rot) & (NCH - 1)) * 16);
     for (int r = 0; r < nrows; ++r) {
         const uint32_t trow = tslot + (uint32_t)(r * tstride * 4);
         float acc[NCH];
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) acc[ch] = dot8_bf16_f32(b[ch], lds128(trow + ch * 32), lds128(trow + ch * 32 + 16));
+        for (int ch = 0; ch < NCH; ++ch) {
+            const uint32_t tc = trow + ((ch + rot) & (NCH - 1)) * 32;
+            acc[ch] = dot8_bf16_f32(b[ch], lds128(tc), lds128(tc + 16));
+        }
 #pragma unroll
         for (int w = 1; w < NCH; w <<= 1)
 #pragma unroll
