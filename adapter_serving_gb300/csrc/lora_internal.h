@@ -120,6 +120,7 @@ struct GemmParams {
     int32_t raster_group;  // W tiles per raster group (round robin)
     int32_t tmem_cols;
     int32_t n_acc;         // accumulator + delta buffer pairs in TMEM (2 when 4 * nt <= 512, else 1)
+    int32_t ybuf_bytes;    // dedicated y staging in shared memory (0: stage buffers / plain stores)
     const int32_t *perm;
     const int32_t *seg_start;
     const int32_t *seg_adapter;
@@ -199,7 +200,7 @@ cudaError_t launch_prep_segments(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStream_t s);
 cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s);
-size_t gemm_smem_bytes(int nt, int n_stages);
+size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes);
 // TMEM buffers, stage count and shared memory of a gemm launch; false if no two stages fit
 bool plan_gemm(GemmParams &gp, size_t *smem_bytes);
 // decode packs of one module: at most one pack per slot

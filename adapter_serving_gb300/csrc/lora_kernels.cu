@@ -697,11 +697,12 @@ struct EpiCtx {
 
 struct ModLocal {
     const CUtensorMap *tmY;
+    void *y;
     int d_out;
 };
 __device__ __forceinline__ ModLocal mod_local(const GemmParams &p, int m) {
     const GemmModule &M = p.mod[m];
-    return ModLocal{&M.tmY, M.d_out};
+    return ModLocal{&M.tmY, M.y, M.d_out};
 }
 
 // ---- expand (B stages) ----------------------------------------------------------------
@@ -915,28 +916,53 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool wi
             for (int i = 0; i < 16; ++i) h[i * kBM + c.o] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
         }
     };
-    // block c0 of y: into its slot of the current round; the round's stores go out when it is full
+    // Where y is staged: on the CTA's last item the stage buffers are idle (after any pieces pulled
+    // in there); otherwise the kernel's y buffer if it has one.  With neither, plain stores.
     const uint32_t block_bytes = 16u * kBM * esz;
-    const int round_blocks = (int)(db.ybuf_bytes / block_bytes);
+    uint8_t *ys = nullptr;
+    int round_blocks = 0;
+    auto set_staging = [&](uint32_t used) {
+        if (last && used < db.stage_bytes) {
+            ys = db.stage + used;
+            round_blocks = (int)((db.stage_bytes - used) / block_bytes);
+        } else {
+            ys = db.ybuf;
+            round_blocks = (int)(db.ybuf_bytes / block_bytes);
+        }
+    };
+    const bool o_ok = o0 + c.o < M.d_out;
+    // block c0 of y: into its slot of the current round; the round's stores go out when it is full
     auto emit = [&](int c0, const float (&v)[16]) {
+        if (round_blocks == 0) {  // plain stores: lane o writes output o0 + o of 16 rows
+            if (!o_ok) return;
+            const size_t base = (size_t)(row0 + c0) * M.d_out + o0 + c.o;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (c0 + i >= ncols) continue;
+                if (!y_bf16) static_cast<float *>(M.y)[base + (size_t)i * M.d_out] = v[i];
+                else static_cast<__nv_bfloat16 *>(M.y)[base + (size_t)i * M.d_out] = __float2bfloat16_rn(v[i]);
+            }
+            return;
+        }
         const int slot = (c0 >> 4) % round_blocks;
         if (slot == 0) {  // the previous round's stores must have read the buffer
             if (leader) bulk_wait_read<0>();
             named_bar_sync(1, 128);
         }
-        put16(db.ybuf + (size_t)slot * block_bytes, v);
+        put16(ys + (size_t)slot * block_bytes, v);
         if (slot == round_blocks - 1 || c0 + 16 >= ncols16) {
             fence_proxy_async_smem();
             named_bar_sync(1, 128);
             if (leader) {
                 for (int k = 0; k <= slot; ++k)
-                    tma_store_2d(M.tmY, db.ybuf + (size_t)k * block_bytes, o0, row0 + c0 - 16 * (slot - k));
+                    tma_store_2d(M.tmY, ys + (size_t)k * block_bytes, o0, row0 + c0 - 16 * (slot - k));
                 bulk_commit();
             }
         }
     };
 
     if (head && it.kb1 == it.kbn) {
+        set_staging(0);
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
             own_cols16(tacc, tdel, with_acc, with_delta, c0, v);
@@ -989,6 +1015,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool wi
     // finish: the other pieces, staged in shared memory when the stage buffers are idle
     const uint32_t others_bytes = (uint32_t)(nc - 1) * piece_bytes;
     const bool staged = last && (uint64_t)others_bytes <= db.stage_bytes;
+    set_staging(staged ? others_bytes : 0);
     if (staged) {
         fence_proxy_async_global();  // the pieces were written through the generic proxy
         if (leader) {
@@ -1038,8 +1065,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const uint32_t a_bytes = kBM * kBK * 2;
     const uint32_t b_bytes = (uint32_t)p.nt * kBK * 2;
     const uint32_t stage_bytes = a_bytes + b_bytes;
-    uint8_t *ybuf = smem + (size_t)S * stage_bytes;  // epilogue y staging
-    int32_t *perm_s = reinterpret_cast<int32_t *>(ybuf + kYBufBytes);
+    uint8_t *ybuf = smem + (size_t)S * stage_bytes;  // epilogue y staging (may be empty)
+    int32_t *perm_s = reinterpret_cast<int32_t *>(ybuf + p.ybuf_bytes);
     int32_t *npk = perm_s + LORA_MAX_DECODE_ROWS;  // [LORA_MAX_MODULES] packs per tile (decode)
     // A stage slot is filled with either W k-blocks (wfull, consumed by the MMA warp) or a B stage
     // (bfull, consumed by the epilogue).  Each consumer skips the other kind, so each kind has its
@@ -1285,7 +1312,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         named_bar_sync(1, 128);
         DrainBufs db;
         db.ybuf = ybuf;
-        db.ybuf_bytes = kYBufBytes;
+        db.ybuf_bytes = (uint32_t)p.ybuf_bytes;
         db.stage = smem;
         db.stage_bytes = (uint32_t)S * stage_bytes;
         db.ld_bar = ld_bar;
@@ -1357,9 +1384,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
 // ====================================================================== launchers ==========
 
-size_t gemm_smem_bytes(int nt, int n_stages) {
+size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes) {
     const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2;
-    return 1024 + stage * n_stages + kYBufBytes + 4 * LORA_MAX_DECODE_ROWS + 4 * LORA_MAX_MODULES +
+    return 1024 + stage * n_stages + (size_t)ybuf_bytes + 4 * LORA_MAX_DECODE_ROWS + 4 * LORA_MAX_MODULES +
            8 * (3 * (size_t)n_stages + 6) + 16;
 }
 
@@ -1368,10 +1395,14 @@ bool plan_gemm(GemmParams &gp, size_t *smem_bytes) {
     gp.n_acc = 4 * gp.nt <= 512 ? 2 : 1;
     gp.tmem_cols = 32;
     while (gp.tmem_cols < 2 * gp.n_acc * gp.nt) gp.tmem_cols <<= 1;
+    // y staging: decode drains stage y in the idle stage buffers (the finishing CTA's last item)
+    // or store it plainly, which buys one more stage; grouped rows drain every tile while the next
+    // one streams, so they keep a dedicated buffer
+    gp.ybuf_bytes = gp.stream_k ? 0 : kYBufBytes;
     const size_t stage = (size_t)kBM * kBK * 2 + (size_t)gp.nt * kBK * 2;
-    const size_t fixed = gemm_smem_bytes(gp.nt, 0);
-    gp.n_stages = (int)std::min<size_t>(kMaxStages, (227 * 1024 - fixed - 16 * kMaxStages) / stage);
-    *smem_bytes = gemm_smem_bytes(gp.nt, gp.n_stages);
+    const size_t fixed = gemm_smem_bytes(gp.nt, 0, gp.ybuf_bytes);
+    gp.n_stages = (int)std::min<size_t>(kMaxStages, (227 * 1024 - fixed - 24 * kMaxStages) / stage);
+    *smem_bytes = gemm_smem_bytes(gp.nt, gp.n_stages, gp.ybuf_bytes);
     return gp.n_stages >= 2;
 }
 
