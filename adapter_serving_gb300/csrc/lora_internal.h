@@ -205,9 +205,10 @@ size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes);
 bool plan_gemm(GemmParams &gp, size_t *smem_bytes);
 // decode packs of one module: at most one pack per slot
 inline int pack_cap(int n, int ch) { return n + (n + ch - 1) / ch + 1; }
-// grouped rows: positions per slot so that a slot's t rows fit a B stage
+// grouped rows: positions per slot so that a slot's B rows, header and t rows fit the y buffer the
+// epilogue copies a B stage into (and the t rows fit the stage's X buffer)
 inline int pf_ch(int nt, int rpmax) {
-    const int c = (nt * 128 - kStageHdrBytes) / (rpmax * 4);
+    const int c = (kYBufBytes - kStageHdrBytes - kBM * rpmax * 2) / (rpmax * 4);
     return c < nt ? c : nt;
 }
 

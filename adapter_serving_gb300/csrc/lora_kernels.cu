@@ -650,6 +650,28 @@ struct Sched {
     }
 };
 
+// Grouped rows (round robin): the j-th tile of CTA `cta`, whole K, its expand slots from the
+// per-chunk table.
+__device__ bool rr_item(const GemmParams &p, int cta, int j, Item &it) {
+    const int t = cta + j * p.n_cta;
+    if (t >= p.total_tiles) return false;
+    int m = 0;
+    while (m + 1 < p.n_mod && p.mod[m + 1].tile_begin <= t) ++m;
+    it.m = m;
+    it.kbn = p.mod[m].k_blocks;
+    it.kb0 = 0;
+    it.kb1 = it.kbn;
+    it.tile = t;
+    it.it0 = 0;
+    tile_coords(p, m, t - p.mod[m].tile_begin, it);
+    it.nbs = p.chunk_nb ? p.chunk_nb[it.chunk] : 0;
+    return true;
+}
+
+// Grouped rows: tile j+1's B stages enter the ring after the first kGroupedLead k-blocks of tile
+// j, so its expand runs while tile j is multiplied; tile 0's come first.
+constexpr int kGroupedLead = 4;
+
 // The item's packs: [P(kb0), P(kb1)) with P(kb) = floor(kb nb / kbn).
 __device__ __forceinline__ int pack_of(const Item &it, int kb) { return kb * it.nbs / it.kbn; }
 __device__ __forceinline__ int item_b(const Item &it) { return pack_of(it, it.kb1) - pack_of(it, it.kb0); }
@@ -1143,90 +1165,136 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             if (lane == 0) got = mbar_wait(empty + kk % S, ((kk / S) & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
             return __shfl_sync(0xffffffffu, got, 0) != 0;
         };
-        while (ok && sc.next(p, npk, it)) {
-            const GemmModule &M = p.mod[it.m];
-            const int o0 = it.w_tile * kBM, row0 = it.chunk * p.nt;
-            const int orows = min(kBM, M.d_out - o0);
-            const int b1 = pack_of(it, it.kb1);
-            Mix mx;
-            mx.begin(it);
-            // decode: the first pack of the item's B stages, fetched ahead
-            uint4 rec = make_uint4(0, 0, 0, 0);
-            if (p.stream_k && b1 > mx.b && lane <= kPackSlots)
-                rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + mx.b) + lane);
-            // grouped rows: the chunk's slots in order (segment, run of pf_ch rows)
-            int sg = 0, r = row0;
-            const int row1 = min(p.n, row0 + p.nt);
-            if (!p.stream_k && b1 > mx.b) sg = p.chunk_seg0[it.chunk];
-            for (int kb = it.kb0; kb < it.kb1 && ok; ++kb) {
-                // ---- W k-block kb
-                if (!acquire(k)) {
-                    ok = false;
-                    break;
-                }
-                note_fill(k % S, false);
-                if (lane == 0) {
-                    uint8_t *sa = smem + (size_t)(k % S) * stage_bytes;
-                    mbar_arrive_expect_tx(wfull + k % S, stage_bytes);
-                    tma_load_2d(sa, &M.tmW, wfull + k % S, kb * kBK, o0, pol_w);
-                    tma_load_2d(sa + a_bytes, &M.tmX, wfull + k % S, kb * kBK, row0, pol_x);
-                }
-                ++k;
-                // ---- the packs that follow it
-                const int nb = mx.after_w();
-                for (int q = 0; q < nb; ++q, ++mx.b, ++k) {
-                    const int jb = mx.b;
+        // one W k-block of item t into stage kk
+        auto issue_w = [&](const Item &t, int kb, uint32_t kk) {
+            const GemmModule &M = p.mod[t.m];
+            note_fill(kk % S, false);
+            if (lane == 0) {
+                uint8_t *sa = smem + (size_t)(kk % S) * stage_bytes;
+                mbar_arrive_expect_tx(wfull + kk % S, stage_bytes);
+                tma_load_2d(sa, &M.tmW, wfull + kk % S, kb * kBK, t.w_tile * kBM, pol_w);
+                tma_load_2d(sa + a_bytes, &M.tmX, wfull + kk % S, kb * kBK, t.chunk * p.nt, pol_x);
+            }
+        };
+        if (p.stream_k) {
+            // ---- decode: stream-K items, packs after their k-blocks
+            while (ok && sc.next(p, npk, it)) {
+                const GemmModule &M = p.mod[it.m];
+                const int o0 = it.w_tile * kBM;
+                const int orows = min(kBM, M.d_out - o0);
+                const int b1 = pack_of(it, it.kb1);
+                Mix mx;
+                mx.begin(it);
+                // the first pack of the item's B stages, fetched ahead
+                uint4 rec = make_uint4(0, 0, 0, 0);
+                if (b1 > mx.b && lane <= kPackSlots) rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + mx.b) + lane);
+                for (int kb = it.kb0; kb < it.kb1 && ok; ++kb) {
                     if (!acquire(k)) {
                         ok = false;
                         break;
                     }
-                    uint8_t *sa = smem + (size_t)(k % S) * stage_bytes;
-                    uint8_t *sx = sa + a_bytes;
-                    uint64_t *bar = bfull + k % S;
-                    note_fill(k % S, true);
-                    if (p.stream_k) {
+                    issue_w(it, kb, k);
+                    ++k;
+                    const int nb = mx.after_w();
+                    for (int q = 0; q < nb; ++q, ++mx.b, ++k) {
+                        const int jb = mx.b;
+                        if (!acquire(k)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *sa = smem + (size_t)(k % S) * stage_bytes;
+                        note_fill(k % S, true);
                         const uint4 cur = rec;
                         if (jb + 1 < b1 && lane <= kPackSlots)
                             rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + jb + 1) + lane);
-                        produce_pack(cur, M, o0, orows, p.pack_ch, sa, sx, bar, lane);
-                    } else if (lane == 0) {
-                        const int ns = *p.n_seg;
-                        int s1 = 0, a = -1;
-                        for (; sg < ns; ++sg) {  // the next segment with an adapter and rows left in the chunk
-                            s1 = min(p.seg_start[sg + 1], row1);
-                            a = p.seg_adapter[sg];
-                            r = max(r, p.seg_start[sg]);
-                            if (a >= 0 && r < s1) break;
-                        }
-                        BStageHdr *hdr = reinterpret_cast<BStageHdr *>(sx);
-                        if (sg >= ns) {  // the chunk has fewer slots than counted: an empty stage
-                            report(p.err, LORA_DEVERR_BAD_SEGMENTS, it.chunk);
-                            hdr->nslots = 0;
-                            hdr->singles8 = 0;
-                            fence_proxy_async_smem();
-                            mbar_arrive(bar);
-                            continue;
-                        }
-                        const int nr = min(p.pf_ch, s1 - r);
-                        const PoolEntry e = M.table[a];
-                        BSlotS sl;
-                        sl.q0 = r;
-                        sl.nrows = (int16_t)nr;
-                        sl.rp = (int16_t)e.rp;
-                        sl.off = 0;
-                        sl.tstride = (int16_t)p.rpmax;
-                        sl.toff = 0;
-                        hdr->nslots = 1;
-                        hdr->singles8 = 0;
-                        hdr->slot[0] = sl;
-                        fence_proxy_async_smem();  // the slot is refilled by TMA later
-                        const uint32_t bb = (uint32_t)(orows * e.rp * 2), tb = (uint32_t)(nr * p.rpmax * 4);
-                        mbar_arrive_expect_tx(bar, bb + tb);
-                        bulk_load(sa, e.B + (size_t)o0 * e.rp, bb, bar);
-                        bulk_load(sx + kStageHdrBytes, M.T + (size_t)r * p.rpmax, tb, bar);
-                        r += nr;
+                        produce_pack(cur, M, o0, orows, p.pack_ch, sa, sa + a_bytes, bfull + k % S, lane);
                     }
                 }
+            }
+        } else {
+            // ---- grouped rows: whole tiles round robin, each tile's slots one per B stage: a
+            // segment's rows in the chunk in runs of pf_ch (walked with sg / r)
+            auto issue_b = [&](const Item &t, int &sg, int &r, uint32_t kk) {
+                const GemmModule &M = p.mod[t.m];
+                const int o0 = t.w_tile * kBM, row0 = t.chunk * p.nt;
+                const int orows = min(kBM, M.d_out - o0);
+                const int row1 = min(p.n, row0 + p.nt);
+                uint8_t *sa = smem + (size_t)(kk % S) * stage_bytes;
+                uint8_t *sx = sa + a_bytes;
+                uint64_t *bar = bfull + kk % S;
+                note_fill(kk % S, true);
+                if (lane != 0) return;
+                const int ns = *p.n_seg;
+                int s1 = 0, a = -1;
+                for (; sg < ns; ++sg) {  // the next segment with an adapter and rows left in the chunk
+                    s1 = min(p.seg_start[sg + 1], row1);
+                    a = p.seg_adapter[sg];
+                    r = max(r, p.seg_start[sg]);
+                    if (a >= 0 && r < s1) break;
+                }
+                BStageHdr *hdr = reinterpret_cast<BStageHdr *>(sx);
+                if (sg >= ns) {  // the chunk has fewer slots than counted: an empty stage
+                    report(p.err, LORA_DEVERR_BAD_SEGMENTS, t.chunk);
+                    hdr->nslots = 0;
+                    hdr->singles8 = 0;
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar);
+                    return;
+                }
+                const int nr = min(p.pf_ch, s1 - r);
+                const PoolEntry e = M.table[a];
+                BSlotS sl;
+                sl.q0 = r;
+                sl.nrows = (int16_t)nr;
+                sl.rp = (int16_t)e.rp;
+                sl.off = 0;
+                sl.tstride = (int16_t)p.rpmax;
+                sl.toff = 0;
+                hdr->nslots = 1;
+                hdr->singles8 = 0;
+                hdr->slot[0] = sl;
+                fence_proxy_async_smem();  // the slot is refilled by TMA later
+                const uint32_t bb = (uint32_t)(orows * e.rp * 2), tb = (uint32_t)(nr * p.rpmax * 4);
+                mbar_arrive_expect_tx(bar, bb + tb);
+                bulk_load(sa, e.B + (size_t)o0 * e.rp, bb, bar);
+                bulk_load(sx + kStageHdrBytes, M.T + (size_t)r * p.rpmax, tb, bar);
+                r += nr;
+            };
+            Item cur, nxt;
+            bool has = rr_item(p, blockIdx.x, 0, cur);
+            if (has) {
+                int sg = p.chunk_seg0[cur.chunk], r = cur.chunk * p.nt;
+                for (int q = 0; q < cur.nbs && ok; ++q, ++k) {
+                    if (!acquire(k)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_b(cur, sg, r, k);
+                }
+            }
+            for (int jt = 0; has && ok; ++jt) {
+                const bool has_nxt = rr_item(p, blockIdx.x, jt + 1, nxt);
+                const int lead = min(kGroupedLead, cur.kbn);
+                int sg = has_nxt ? p.chunk_seg0[nxt.chunk] : 0, r = has_nxt ? nxt.chunk * p.nt : 0;
+                for (int kb = 0; kb <= cur.kbn && ok; ++kb) {
+                    if (kb == lead && has_nxt)
+                        for (int q = 0; q < nxt.nbs && ok; ++q, ++k) {
+                            if (!acquire(k)) {
+                                ok = false;
+                                break;
+                            }
+                            issue_b(nxt, sg, r, k);
+                        }
+                    if (kb == cur.kbn || !ok) continue;
+                    if (!acquire(k)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_w(cur, kb, k);
+                    ++k;
+                }
+                cur = nxt;
+                has = has_nxt;
             }
         }
         // never leave the block with copies still landing in its shared memory: wait for the
@@ -1243,42 +1311,76 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
             const uint32_t idesc = idesc_bf16_f32(kBM, (uint32_t)p.nt);
-            Sched sc;
-            sc.begin(p, blockIdx.x);
-            Item it;
             uint32_t k = 0, li = 0, use0 = 0, use1 = 0, wpar = 0;
             bool ok = true;
-            while (ok && sc.next(p, npk, it)) {
-                const int buf = li % NB;
-                const uint32_t use = buf ? use1 : use0;
-                if (!mbar_wait(acc_free + buf, (use & 1) ^ 1, abort_flag, p.err)) break;
+            // one W k-block at stage k into accumulator column d
+            auto mma_stage = [&](uint32_t d, bool accumulate) -> bool {
+                const int s = k % S;
+                if (!mbar_wait(wfull + s, (wpar >> s) & 1u, abort_flag, p.err)) return false;
+                wpar ^= 1u << s;
                 tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(buf * p.nt);
-                Mix mx;
-                mx.begin(it);
-                for (int kb = it.kb0; kb < it.kb1; ++kb) {
-                    const int s = k % S;
-                    if (!mbar_wait(wfull + s, (wpar >> s) & 1u, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    wpar ^= 1u << s;
-                    tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-                    const uint64_t da = sdesc_kmajor_sw128(sa);
-                    const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes);
+                const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+                const uint64_t da = sdesc_kmajor_sw128(sa);
+                const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint32_t accum = (kb > it.kb0 || kk > 0) ? 1u : 0u;
-                        umma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, accum);
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    umma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, (accumulate || kk > 0) ? 1u : 0u);
+                umma_commit(empty + s);
+                return true;
+            };
+            if (p.stream_k) {
+                Sched sc;
+                sc.begin(p, blockIdx.x);
+                Item it;
+                while (ok && sc.next(p, npk, it)) {
+                    const int buf = li % NB;
+                    const uint32_t use = buf ? use1 : use0;
+                    if (!mbar_wait(acc_free + buf, (use & 1) ^ 1, abort_flag, p.err)) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + (uint32_t)(buf * p.nt);
+                    Mix mx;
+                    mx.begin(it);
+                    for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                        if (!mma_stage(d, kb > it.kb0)) {
+                            ok = false;
+                            break;
+                        }
+                        k += 1 + (uint32_t)mx.after_w();  // the packs after it go to the epilogue
                     }
-                    umma_commit(empty + s);
-                    k += 1 + (uint32_t)mx.after_w();  // the packs after it go to the epilogue
+                    if (!ok) break;
+                    umma_commit(acc_full + buf);
+                    if (buf) ++use1; else ++use0;
+                    ++li;
                 }
-                if (!ok) break;
-                umma_commit(acc_full + buf);
-                if (buf) ++use1; else ++use0;
-                ++li;
+            } else {
+                // grouped rows: the epilogue writes each tile's expand into the accumulator first
+                // and then arrives on acc_free, so every k-block accumulates on top of it
+                Item cur, nxt;
+                bool has = rr_item(p, blockIdx.x, 0, cur);
+                if (has) k += (uint32_t)cur.nbs;
+                for (int jt = 0; has && ok; ++jt) {
+                    const bool has_nxt = rr_item(p, blockIdx.x, jt + 1, nxt);
+                    const int buf = jt & 1;
+                    const uint32_t use = buf ? use1 : use0;
+                    if (!mbar_wait(acc_free + buf, use & 1, abort_flag, p.err)) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + (uint32_t)(buf * p.nt);
+                    const int lead = min(kGroupedLead, cur.kbn);
+                    for (int kb = 0; kb < cur.kbn; ++kb) {
+                        if (kb == lead && has_nxt) k += (uint32_t)nxt.nbs;
+                        if (!mma_stage(d, true)) {
+                            ok = false;
+                            break;
+                        }
+                        ++k;
+                    }
+                    if (!ok) break;
+                    if (lead == cur.kbn && has_nxt) k += (uint32_t)nxt.nbs;
+                    umma_commit(acc_full + buf);
+                    if (buf) ++use1; else ++use0;
+                    cur = nxt;
+                    has = has_nxt;
+                }
             }
             umma_commit(mma_done);
             const uint32_t a = smem_u32(mma_done);
@@ -1318,58 +1420,132 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         db.ld_bar = ld_bar;
         db.ld_phase = 0;
         const uint32_t lane_off = (uint32_t)c.lane_base << 16;
-        Sched sc;
-        sc.begin(p, blockIdx.x);
-        Item cur;
-        bool has_cur = sc.next(p, npk, cur);
-        uint32_t k = 0, li = 0, use0 = 0, use1 = 0, bpar = 0;
-        while (has_cur) {
-            const int buf = li % NB;
-            const bool last = !sc.more(p);
-            const int nbs = item_b(cur);
-            bool ok = true;
-            if (nbs > 0) {
-                // expand: zero this item's delta columns, then every B stage adds its slots' rows
-                const uint32_t tdel = tmem_base + lane_off + c.delta_col + (uint32_t)(buf * p.nt);
-                const int row0 = cur.chunk * p.nt;
-                const int ncols = p.decode ? p.n : min(p.nt, p.n - row0);
-                float z[16];
+        uint32_t bpar = 0;
+        // wait for the B stage at ring slot kk (all 128 threads); false if the wait gave up
+        auto wait_b = [&](uint32_t kk) -> bool {
+            const int s = kk % S;
+            const bool ok = !named_bar_or(1, 128, !mbar_wait(bfull + s, (bpar >> s) & 1u, abort_flag, p.err));
+            if (ok) bpar ^= 1u << s;
+            return ok;
+        };
+        float z[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) z[i] = 0.f;
-                for (int c0 = 0; c0 < ncols; c0 += 16) tmem_st16(tdel + (uint32_t)c0, z);
-                tmem_st_wait();
-                Mix mx;
-                mx.begin(cur);
-                for (int kb = cur.kb0; kb < cur.kb1 && ok; ++kb) {
-                    ++k;  // the W k-block goes to the MMA warp
-                    const int nb = mx.after_w();
-                    for (int q = 0; q < nb; ++q, ++k) {
-                        const int s = k % S;
-                        ok = !named_bar_or(1, 128, !mbar_wait(bfull + s, (bpar >> s) & 1u, abort_flag, p.err));
-                        if (!ok) break;
-                        bpar ^= 1u << s;
-                        const uint8_t *sa = smem + (size_t)s * stage_bytes;
-                        expand_stage(c, sa, sa + a_bytes, tdel, row0);
-                        named_bar_sync(1, 128);  // every warp is done with the stage
-                        if (c.etid == 0) mbar_arrive(empty + s);
+        for (int i = 0; i < 16; ++i) z[i] = 0.f;
+        if (p.stream_k) {
+            Sched sc;
+            sc.begin(p, blockIdx.x);
+            Item cur;
+            bool has_cur = sc.next(p, npk, cur);
+            uint32_t k = 0, li = 0, use0 = 0, use1 = 0;
+            while (has_cur) {
+                const int buf = li % NB;
+                const bool last = !sc.more(p);
+                const int nbs = item_b(cur);
+                bool ok = true;
+                if (nbs > 0) {
+                    // expand: zero this item's delta columns, then every B stage adds its slots' rows
+                    const uint32_t tdel = tmem_base + lane_off + c.delta_col + (uint32_t)(buf * p.nt);
+                    const int row0 = cur.chunk * p.nt;
+                    const int ncols = p.decode ? p.n : min(p.nt, p.n - row0);
+                    float z[16];
+    #pragma unroll
+                    for (int i = 0; i < 16; ++i) z[i] = 0.f;
+                    for (int c0 = 0; c0 < ncols; c0 += 16) tmem_st16(tdel + (uint32_t)c0, z);
+                    tmem_st_wait();
+                    Mix mx;
+                    mx.begin(cur);
+                    for (int kb = cur.kb0; kb < cur.kb1 && ok; ++kb) {
+                        ++k;  // the W k-block goes to the MMA warp
+                        const int nb = mx.after_w();
+                        for (int q = 0; q < nb; ++q, ++k) {
+                            const int s = k % S;
+                            ok = wait_b(k);
+                            if (!ok) break;
+                            const uint8_t *sa = smem + (size_t)s * stage_bytes;
+                            expand_stage(c, sa, sa + a_bytes, tdel, row0);
+                            named_bar_sync(1, 128);  // every warp is done with the stage
+                            if (c.etid == 0) mbar_arrive(empty + s);
+                        }
                     }
+                    tmem_st_wait();
+                } else {
+                    k += (uint32_t)(cur.kb1 - cur.kb0);
+                }
+                if (!ok) break;
+                const uint32_t use = buf ? use1 : use0;
+                ok = mbar_wait(acc_full + buf, use & 1, abort_flag, p.err);
+                if (named_bar_or(1, 128, !ok)) break;
+                tc_fence_after();
+                drain(c, cur, buf, true, nbs > 0, last, flag, abort_flag, db);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_free + buf);
+                if (buf) ++use1; else ++use0;
+                has_cur = sc.next(p, npk, cur);
+                ++li;
+            }
+        } else {
+            // ---- grouped rows: the expand of tile j+1 is written into its accumulator (zeros +
+            // delta) while tile j is multiplied, then acc_free tells the MMA warp to start on it.
+            // A B stage is copied into the y buffer first, so its ring slot is given back at once.
+            uint32_t use0 = 0, use1 = 0;
+            auto pre = [&](const Item &t, int buf, uint32_t k0) -> bool {
+                const uint32_t tacc = tmem_base + lane_off + (uint32_t)(buf * p.nt);
+                const int row0 = t.chunk * p.nt;
+                for (int c0 = 0; c0 < p.nt; c0 += 16) tmem_st16(tacc + (uint32_t)c0, z);
+                tmem_st_wait();
+                for (int q = 0; q < t.nbs; ++q) {
+                    const uint32_t kk = k0 + (uint32_t)q;
+                    if (!wait_b(kk)) return false;
+                    const uint8_t *sa = smem + (size_t)(kk % S) * stage_bytes;
+                    const uint8_t *sx = sa + a_bytes;
+                    const BStageHdr *hdr = reinterpret_cast<const BStageHdr *>(sx);
+                    // the slot's B rows ([128][rp], rank offset 0), then header and t rows
+                    const uint32_t bbytes = hdr->nslots > 0 ? (uint32_t)(kBM * hdr->slot[0].rp * 2) : 0u;
+                    const uint32_t tbytes = hdr->nslots > 0 ? (uint32_t)(hdr->slot[0].nrows * p.rpmax * 4) : 0u;
+                    if (c.etid == 0) bulk_wait_read<0>();  // y stores of the last drain have read the buffer
+                    named_bar_sync(1, 128);
+                    for (uint32_t off = (uint32_t)c.etid * 16; off < bbytes; off += 128 * 16)
+                        *reinterpret_cast<uint4 *>(ybuf + off) = *reinterpret_cast<const uint4 *>(sa + off);
+                    for (uint32_t off = (uint32_t)c.etid * 16; off < kStageHdrBytes + tbytes; off += 128 * 16)
+                        *reinterpret_cast<uint4 *>(ybuf + bbytes + off) = *reinterpret_cast<const uint4 *>(sx + off);
+                    named_bar_sync(1, 128);  // the copy is complete: the slot goes back
+                    if (c.etid == 0) mbar_arrive(empty + kk % S);
+                    expand_stage(c, ybuf, ybuf + bbytes, tacc, row0);
+                    named_bar_sync(1, 128);  // before the buffer is overwritten
                 }
                 tmem_st_wait();
-            } else {
-                k += (uint32_t)(cur.kb1 - cur.kb0);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_free + buf);
+                return true;
+            };
+            Item cur, nxt;
+            bool has = rr_item(p, blockIdx.x, 0, cur);
+            bool ok = true;
+            uint32_t kw = 0;  // ring position of the current tile's first k-block
+            if (has) {
+                ok = pre(cur, 0, 0);
+                kw = (uint32_t)cur.nbs;
             }
-            if (!ok) break;
-            const uint32_t use = buf ? use1 : use0;
-            ok = mbar_wait(acc_full + buf, use & 1, abort_flag, p.err);
-            if (named_bar_or(1, 128, !ok)) break;
-            tc_fence_after();
-            drain(c, cur, buf, true, nbs > 0, last, flag, abort_flag, db);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_free + buf);
-            if (buf) ++use1; else ++use0;
-            has_cur = sc.next(p, npk, cur);
-            ++li;
+            for (int jt = 0; has && ok; ++jt) {
+                const bool has_nxt = rr_item(p, blockIdx.x, jt + 1, nxt);
+                const int buf = jt & 1;
+                const int lead = min(kGroupedLead, cur.kbn);
+                if (has_nxt) ok = pre(nxt, buf ^ 1, kw + (uint32_t)lead);
+                if (!ok) break;
+                const uint32_t use = buf ? use1 : use0;
+                ok = mbar_wait(acc_full + buf, use & 1, abort_flag, p.err);
+                if (named_bar_or(1, 128, !ok)) break;
+                tc_fence_after();
+                drain(c, cur, buf, true, false, !has_nxt, flag, abort_flag, db);
+                tc_fence_before();
+                __syncwarp();
+                if (buf) ++use1; else ++use0;
+                kw += (uint32_t)cur.kbn + (has_nxt ? (uint32_t)nxt.nbs : 0u);
+                cur = nxt;
+                has = has_nxt;
+            }
         }
         if (c.etid == 0) bulk_wait<0>();  // every output store has been performed
     }
@@ -1391,10 +1567,13 @@ size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes) {
 }
 
 bool plan_gemm(GemmParams &gp, size_t *smem_bytes) {
-    // TMEM: n_acc accumulator buffers of nt columns, then one expand-delta buffer per accumulator
-    gp.n_acc = 4 * gp.nt <= 512 ? 2 : 1;
+    // TMEM.  Decode: n_acc accumulator buffers of nt columns, then one expand-delta buffer per
+    // accumulator.  Grouped rows: two accumulators and no delta buffer (the expand is written into
+    // the accumulator before the tile's MMAs).
+    gp.n_acc = (!gp.stream_k || 4 * gp.nt <= 512) ? 2 : 1;
+    const int cols = gp.stream_k ? 2 * gp.n_acc * gp.nt : gp.n_acc * gp.nt;
     gp.tmem_cols = 32;
-    while (gp.tmem_cols < 2 * gp.n_acc * gp.nt) gp.tmem_cols <<= 1;
+    while (gp.tmem_cols < cols) gp.tmem_cols <<= 1;
     // y staging: decode drains stage y in the idle stage buffers (the finishing CTA's last item)
     // or store it plainly, which buys one more stage; grouped rows drain every tile while the next
     // one streams, so they keep a dedicated buffer
