@@ -54,7 +54,9 @@ def parse():
 
 # name -> (constructor, kind); the headline is attn70b
 WORKLOADS = {"attn70b": (wl.attn70b_decode, "decode"), "all70b": (wl.all70b_decode, "decode"),
-             "zipf": (wl.zipf_pool, "decode"), "prefill": (wl.prefill_segments, "prefill")}
+             "zipf": (wl.zipf_pool, "decode"), "prefill": (wl.prefill_segments, "prefill"),
+             # the prefill path at a size a profiler capture can replay (8 requests, ~8.7k tokens)
+             "prefill_small": (lambda: wl.prefill_segments(n_req=8), "prefill")}
 
 
 def dist_env():
