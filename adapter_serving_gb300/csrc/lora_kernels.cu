@@ -80,30 +80,41 @@ __device__ int checked_id(const PrepParams &p, int id, int where) {
     return id;
 }
 
-// Exclusive prefix sum over the 256 threads of a block; `total` receives the sum.
-// Exclusive prefix sum over a group of 256 threads (8 warps) that synchronises on named barrier
+// Exclusive prefix sum of 64-bit values over a group of 256 threads (8 warps) on named barrier
 // `bar`; `total` receives the sum.
-__device__ int group_scan256(int v, int *s_warp, int &total, int bar) {
+__device__ uint64_t group_scan256_u64(uint64_t v, uint64_t *s_warp, uint64_t &total, int bar) {
     const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) & 7;
-    int x = v;
+    uint64_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) s_warp[warp] = x;
     named_bar_sync(bar, 256);
-    int before = 0, tot = 0;
+    uint64_t before = 0, tot = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-        const int t = s_warp[w];
+        const uint64_t t = s_warp[w];
         before += w < warp ? t : 0;
         tot += t;
     }
-    named_bar_sync(bar, 256);
+    named_bar_sync(bar, 256);  // s_warp may be reused
     total = tot;
     return before + x - v;
 }
+
+// Row grouping state the prep block keeps in shared memory (decode, n <= 256 rows).
+struct PrepShared {
+    int id[LORA_MAX_DECODE_ROWS];                          // adapter id of row r (-1 = base only)
+    int sorted[LORA_MAX_DECODE_ROWS];                      // adapter id at sorted position q
+    int cnt[4][LORA_MAX_DECODE_ROWS];                      // partial position counts
+    int seg_of[LORA_MAX_DECODE_ROWS];                      // segment of position q
+    int seg_q0[LORA_MAX_DECODE_ROWS + 1];                  // first position of segment s
+    int rp[LORA_MAX_MODULES][LORA_MAX_DECODE_ROWS];        // storage rank at position q (0 = none)
+    const uint16_t *B[LORA_MAX_MODULES][LORA_MAX_DECODE_ROWS];  // B of the adapter at position q
+    int scan[8];
+};
 
 // Expand packs of every module (decode).  A slot is one adapter segment's run of at most
 // pack_ch positions.  Slots are ordered by storage rank (descending), then segment, then
@@ -112,38 +123,41 @@ __device__ int group_scan256(int v, int *s_warp, int &total, int bar) {
 // A slot at unit offset P keeps its t rows at floats [pack_ch * P, pack_ch * (P + rp)) of the
 // module's packed T, so a pack's t rows are one contiguous range too.
 // The prep block has kPrepGroups groups of 256 threads; group g builds the packs of modules
-// g, g + kPrepGroups, ..., synchronising on its own named barrier.
+// g, g + kPrepGroups, ..., synchronising on its own named barrier.  Everything it needs about
+// the segments (first position, rank, B) is already in shared memory.
 constexpr int kPrepGroups = 4;
 
-__device__ void build_packs(const PrepParams &p, int ns) {
-    __shared__ int s_warp_all[kPrepGroups][8];
+__device__ void build_packs(const PrepParams &p, const PrepShared &sh, int ns) {
+    __shared__ uint64_t s_warp_all[kPrepGroups][8];
     __shared__ int s_first_all[kPrepGroups][320];
+    __shared__ int s_unit_all[kPrepGroups][LORA_MAX_DECODE_ROWS];
     const int g = threadIdx.x >> 8, tid = threadIdx.x & 255;
     const int bar = 1 + g;
-    int *s_warp = s_warp_all[g], *s_first = s_first_all[g];
+    uint64_t *s_warp = s_warp_all[g];
+    int *s_first = s_first_all[g], *s_unit = s_unit_all[g];
     const int ch = p.pack_ch;
     for (int m = g; m < p.n_mod; m += kPrepGroups) {
         int q0 = 0, q1 = 0, rp = 0, nsl = 0, cls = 4;
         const uint16_t *B = nullptr;
         if (tid < ns) {
-            q0 = p.seg_start[tid];
-            q1 = p.seg_start[tid + 1];
-            const int a = p.seg_adapter[tid];
-            if (a >= 0) {
-                const PoolEntry e = p.table[m][a];
-                rp = e.rp;
-                B = e.B;
-            }
+            q0 = sh.seg_q0[tid];
+            q1 = sh.seg_q0[tid + 1];
+            rp = sh.rp[m][q0];
+            B = sh.B[m][q0];
             if (rp > 0) {
                 nsl = (q1 - q0 + ch - 1) / ch;
                 cls = rp == 64 ? 0 : rp == 32 ? 1 : rp == 16 ? 2 : 3;
             }
         }
-        int slot_base = 0, unit_base = 0, slots_tot = 0, units_tot = 0;
+        // slots before this segment's, per rank class, in one scan of four 16-bit counts
+        uint64_t tot4;
+        const uint64_t ex4 = group_scan256_u64(cls < 4 ? (uint64_t)nsl << (16 * cls) : 0, s_warp, tot4, bar);
+        int slots_tot = 0, units_tot = 0, slot_base = 0, unit_base = 0;
+#pragma unroll
         for (int c = 0; c < 4; ++c) {
-            int tot;
-            const int ex = group_scan256(cls == c ? nsl : 0, s_warp, tot, bar);
+            const int tot = (int)((tot4 >> (16 * c)) & 0xffff);
             if (cls == c) {
+                const int ex = (int)((ex4 >> (16 * c)) & 0xffff);
                 slot_base = slots_tot + ex;
                 unit_base = units_tot + ex * (64 >> c);
             }
@@ -155,6 +169,7 @@ __device__ void build_packs(const PrepParams &p, int ns) {
             const int P = unit_base + k * rp;
             if (P % kPackRanks == 0) s_first[P / kPackRanks] = slot_base + k;
         }
+        if (tid < ns) s_unit[tid] = rp > 0 ? unit_base : -1;
         if (tid == 0) s_first[npk] = slots_tot;
         named_bar_sync(bar, 256);
         BPackG *packs = p.packs[m];
@@ -177,21 +192,23 @@ __device__ void build_packs(const PrepParams &p, int ns) {
                 packs[j].pad_ = 0;
             }
         }
-        if (tid < ns)
-            for (int q = q0; q < q1; ++q)
-                p.tpos[m][q] = rp > 0 ? ch * (unit_base + ((q - q0) / ch) * rp) + ((q - q0) % ch) * rp : -1;
+        // where each position's t row goes: one thread per position
+        for (int q = tid; q < p.n; q += 256) {
+            const int sg = sh.seg_of[q], ub = s_unit[sg], r = sh.rp[m][q];
+            const int d = q - sh.seg_q0[sg];
+            p.tpos[m][q] = ub >= 0 ? ch * (ub + (d / ch) * r) + (d % ch) * r : -1;
+        }
         if (tid == 0) p.n_packs[m] = npk;
-        named_bar_sync(bar, 256);  // s_first is reused by the group's next module
+        named_bar_sync(bar, 256);  // s_first and s_unit are reused by the group's next module
     }
 }
 
-// One block of 256 threads, n <= 256 rows.  Position of row i in the stable order:
-// #{j : id_j < id_i} + #{j < i : id_j == id_i}.
+// One block of 1024 threads, n <= 256 rows.  Position of row i in the stable order:
+// #{j : id_j < id_i} + #{j < i : id_j == id_i}, counted by four threads per row over a quarter
+// of the rows each.
 __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const PrepParams p) {
-    __shared__ int s_id[256];
-    __shared__ int s_sorted[256];
-    __shared__ int s_scan[256];
-    const int tid = threadIdx.x;  // the row grouping uses threads 0..255; all of them build packs
+    __shared__ PrepShared sh;
+    const int tid = threadIdx.x;
     const int n = p.n;
     grid_dep_wait();
     grid_dep_launch();
@@ -200,32 +217,83 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
         seg_ok = segments_valid(p);
         if (!seg_ok && tid == 0) report(p.err, LORA_DEVERR_BAD_SEGMENTS, 0);
     }
+    // ---- ids, checked; every module's rank and B of the row's adapter (all loads in flight first)
     int id = -1;
+    int rp_row[LORA_MAX_MODULES];
+    const uint16_t *B_row[LORA_MAX_MODULES];
     if (tid < n) {
+        int where = tid;
         if (p.ids) {
-            id = checked_id(p, p.ids[tid], tid);
+            id = p.ids[tid];
         } else if (seg_ok) {
-            int s = seg_of(p.seg_start_in, p.n_seg_in, tid);
-            id = checked_id(p, p.seg_adapter_in[s], s);
+            where = seg_of(p.seg_start_in, p.n_seg_in, tid);
+            id = p.seg_adapter_in[where];
         }
-        s_id[tid] = id;
+        if (id < -1 || id >= p.max_adapters) {
+            report(p.err, LORA_DEVERR_BAD_ADAPTER, where);
+            id = -1;
+        }
+        int rank[LORA_MAX_MODULES];
+#pragma unroll
+        for (int m = 0; m < LORA_MAX_MODULES; ++m) {
+            rank[m] = 1;
+            rp_row[m] = 0;
+            B_row[m] = nullptr;
+            if (id >= 0 && m < p.n_mod) {
+                const PoolEntry *e = p.table[m] + id;
+                rank[m] = e->rank;
+                rp_row[m] = e->rp;
+                B_row[m] = e->B;
+            }
+        }
+        bool ok = true;
+#pragma unroll
+        for (int m = 0; m < LORA_MAX_MODULES; ++m) ok = ok && rank[m] > 0;
+        if (!ok) {
+            report(p.err, LORA_DEVERR_NOT_LOADED, where);
+            id = -1;
+        }
+        if (id < 0) {
+#pragma unroll
+            for (int m = 0; m < LORA_MAX_MODULES; ++m) {
+                rp_row[m] = 0;
+                B_row[m] = nullptr;
+            }
+        }
+        sh.id[tid] = id;
+    }
+    __syncthreads();
+    // ---- stable sort: four partial counts per row
+    {
+        const int row = tid & 255, part = tid >> 8;
+        if (row < n) {
+            const int v = sh.id[row];
+            const int j0 = part * n / 4, j1 = (part + 1) * n / 4;
+            int c = 0;
+            for (int j = j0; j < j1; ++j) {
+                const int u = sh.id[j];
+                c += (u < v) || (u == v && j < row);
+            }
+            sh.cnt[part][row] = c;
+        }
     }
     __syncthreads();
     if (tid < n) {
-        int pos = 0;
-        for (int j = 0; j < n; ++j) {
-            int v = s_id[j];
-            pos += (v < id) || (v == id && j < tid);
-        }
+        const int pos = sh.cnt[0][tid] + sh.cnt[1][tid] + sh.cnt[2][tid] + sh.cnt[3][tid];
         p.perm[pos] = tid;
         p.qadapter[pos] = id;
-        s_sorted[pos] = id;
+        sh.sorted[pos] = id;
+#pragma unroll
+        for (int m = 0; m < LORA_MAX_MODULES; ++m) {
+            sh.rp[m][pos] = rp_row[m];
+            sh.B[m][pos] = B_row[m];
+        }
     }
     __syncthreads();
-    // segment starts: positions whose id differs from the one before; inclusive scan of the
+    // ---- segment starts: positions whose id differs from the one before; inclusive scan of the
     // flags (warp shuffles, then the 8 warp totals)
     int flag = 0;
-    if (tid < 256) flag = (tid < n) && (tid == 0 || s_sorted[tid] != s_sorted[tid - 1]);
+    if (tid < 256) flag = (tid < n) && (tid == 0 || sh.sorted[tid] != sh.sorted[tid - 1]);
     int incl = flag;
     const int lane = tid & 31;
 #pragma unroll
@@ -233,27 +301,30 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
-    if (tid < 256 && lane == 31) s_scan[tid >> 5] = incl;
+    if (tid < 256 && lane == 31) sh.scan[tid >> 5] = incl;
     __syncthreads();
     int before = 0, ns = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-        const int t = s_scan[w];
+        const int t = sh.scan[w];
         before += w < (tid >> 5) ? t : 0;
         ns += t;
     }
+    if (tid < n) sh.seg_of[tid] = before + incl - 1;
     if (flag) {
         const int seg = before + incl - 1;
         p.seg_start[seg] = tid;
-        p.seg_adapter[seg] = s_sorted[tid];
+        p.seg_adapter[seg] = sh.sorted[tid];
+        sh.seg_q0[seg] = tid;
     }
     if (tid == 0) {
         *p.n_seg = ns;
         p.seg_start[ns] = n;
+        sh.seg_q0[ns] = n;
     }
     if (p.packs[0] != nullptr) {
         __syncthreads();  // the segment table is complete
-        build_packs(p, ns);
+        build_packs(p, sh, ns);
     }
 }
 
