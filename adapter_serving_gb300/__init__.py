@@ -18,7 +18,7 @@ import os
 
 from . import build as _build
 
-__all__ = ["Pool", "LoraError", "build_segments", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF16"]
+__all__ = ["Pool", "LoraError", "build_segments", "form_batch", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF16"]
 
 LIB_PATH = _build.LIB
 if not os.path.exists(LIB_PATH):
@@ -45,6 +45,11 @@ class lora_module_io(ctypes.Structure):
     _fields_ = [("module", _I32), ("x", _P), ("W", _P), ("y", _P)]
 
 
+class lora_batch_policy(ctypes.Structure):
+    _fields_ = [("max_batch", _I32), ("max_distinct", _I32), ("min_batch", _I32), ("tail_slots", _I32),
+                ("max_queue_ms", ctypes.c_double)]
+
+
 def _sig(name, res, *args):
     f = getattr(lib, name)
     f.restype = res
@@ -59,6 +64,8 @@ _sig("lora_pool_unload", ctypes.c_int, _P, _I32, _P)
 _sig("lora_pool_query", ctypes.c_int, _P, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I64))
 _sig("lora_pool_free_rows", ctypes.c_int, _P, _I32, ctypes.POINTER(_I64))
 _sig("lora_build_segments", ctypes.c_int, _P, _I32, _P, _P, _P, ctypes.POINTER(_I32))
+_sig("lora_form_batch", ctypes.c_int, _P, _P, _I32, ctypes.POINTER(lora_batch_policy), _P, ctypes.POINTER(_I32),
+     ctypes.POINTER(_I32))
 _sig("lora_layer_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _I32, _F, _I32, _P)
 _sig("lora_linear_forward", ctypes.c_int, _P, _I32, _P, _P, _P, _I32, _F, _P, _I32, _P)
 _sig("lora_segment_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _P, _I32, _I32, _F,
@@ -139,6 +146,24 @@ def build_segments(ids):
                                    seg_adapter.ctypes.data, ctypes.byref(ns)), "lora_build_segments")
     k = ns.value
     return perm[:n].copy(), seg_start[:k + 1].copy(), seg_adapter[:k].copy()
+
+
+def form_batch(queue_adapter, queue_waited_ms, max_batch, max_distinct=32, min_batch=1, tail_slots=4,
+               max_queue_ms=200.0):
+    """Adapter-aware batch former (lora_form_batch): returns (queue indices of the next step's
+    requests in batch order, distinct adapters among them).  Defaults are the pages' values: a cap
+    of 32 adapters, 4 reserved tail slots, a 200 ms age deadline."""
+    import numpy as np
+    qa = np.ascontiguousarray(queue_adapter, dtype=np.int32)
+    qw = np.ascontiguousarray(queue_waited_ms, dtype=np.float64)
+    if qa.shape != qw.shape or qa.ndim != 1:
+        raise ValueError("queue_adapter and queue_waited_ms: need two 1-D arrays of one length")
+    pol = lora_batch_policy(int(max_batch), int(max_distinct), int(min_batch), int(tail_slots), float(max_queue_ms))
+    out = np.empty(max(1, min(len(qa), int(max_batch))), np.int32)
+    n, d = _I32(0), _I32(0)
+    _check(lib.lora_form_batch(qa.ctypes.data, qw.ctypes.data, len(qa), ctypes.byref(pol), out.ctypes.data,
+                               ctypes.byref(n), ctypes.byref(d)), "lora_form_batch")
+    return out[:n.value].copy(), d.value
 
 
 class Pool:

@@ -153,6 +153,43 @@ int lora_pool_free_rows(const lora_pool *pool, int32_t module, int64_t *free_row
 int lora_build_segments(const int32_t *row_ids, int32_t n, int32_t *perm, int32_t *seg_start,
                         int32_t *seg_adapter, int32_t *n_seg);
 
+/* Policy of the adapter-aware batch former (lora_form_batch). */
+typedef struct {
+    int32_t max_batch;     /* most requests in one step, >= 1 */
+    int32_t max_distinct;  /* cap on the adapters of one step ("m07", section 6: 32), >= 0 */
+    int32_t min_batch;     /* the cap binds only once the batch holds this many requests, >= 0 */
+    int32_t tail_slots;    /* places reserved for the oldest single-request adapters
+                              ("m07", revision R1: 4 of the 32); 0 = none */
+    double max_queue_ms;   /* age deadline: older requests are admitted first ("m07", section 6,
+                              "The fairness cost": 200 ms); <= 0 = no deadline */
+} lora_batch_policy;
+
+/*
+ * lora_form_batch -- host-side batch former: picks the requests of the next step from the
+ * waiting queue so that the step reads few distinct adapters.  ("m07 -- Multi-Adapter (LoRA)
+ * Serving", section 6 "Deep Dive A", "The adapter-aware scheduler" and "The fairness cost, which
+ * must be stated"; revision R1, reserved tail slots; "12. Adapter Serving and Multi-Tenant
+ * Customization", section "Scheduling with adapter awareness".)  In batch order it admits
+ *   1. every request older than max_queue_ms (oldest first);
+ *   2. up to tail_slots of the oldest remaining requests whose adapter has exactly one waiting
+ *      request;
+ *   3. the remaining requests grouped by adapter, largest group first (ties: first arrival),
+ *      each group whole while there is room.  Once the batch holds max_distinct adapters and at
+ *      least min_batch requests, groups that would add a new adapter are passed over; groups of
+ *      adapters already admitted and the base-only group (-1) still come in.
+ *  queue_adapter    host int32 [n_queue]   adapter id of each waiting request (-1 = base only),
+ *                                          in arrival order
+ *  queue_waited_ms  host double [n_queue]  how long each request has waited
+ *  out_idx          host int32 [min(n_queue, max_batch)]  out: queue indices of the batch, in
+ *                                          batch order
+ *  out_n            out: requests in the batch
+ *  out_distinct     out: distinct adapters (ids >= 0) in the batch
+ * Pure host code; no device is touched.  Errors: EINVAL (null pointer, negative count, a policy
+ * field out of range, an id < -1, a NaN wait).
+ */
+int lora_form_batch(const int32_t *queue_adapter, const double *queue_waited_ms, int32_t n_queue,
+                    const lora_batch_policy *policy, int32_t *out_idx, int32_t *out_n, int32_t *out_distinct);
+
 /* One projection of a layer call. */
 typedef struct {
     int32_t module;  /* pool module index */

@@ -27,7 +27,7 @@ import numpy as np
 _CHUNK = 1 << 22
 
 # seed-key tags, one per kind of array
-_TAG_W, _TAG_X, _TAG_A, _TAG_B, _TAG_IDS, _TAG_RANKS, _TAG_LENS = 1, 2, 3, 4, 5, 6, 7
+_TAG_W, _TAG_X, _TAG_A, _TAG_B, _TAG_IDS, _TAG_RANKS, _TAG_LENS, _TAG_QUEUE = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -213,6 +213,22 @@ def random_ids(n, n_adapters, seed, p_base=0.0):
     if p_base > 0:
         ids[g.random(n) < p_base] = -1
     return ids
+
+
+def request_queue(n, seed=0, n_adapters=5000, zipf_s=1.1, max_wait_ms=400.0, p_base=0.0):
+    """A waiting queue for the batch former: n requests in arrival order whose adapters follow the
+    bounded Zipf(1.1) over n_adapters of ``zipf_pool`` (a fraction ``p_base`` base-only, -1), and
+    how long each has waited: arrival times uniform over the last ``max_wait_ms``, so the queue's
+    first request has waited longest.  Returns (adapter ids int32 [n], waited ms float64 [n])."""
+    g = np.random.default_rng([seed, _TAG_QUEUE])
+    k = np.arange(1, n_adapters + 1, dtype=np.float64)
+    p = k ** (-zipf_s)
+    cdf = np.cumsum(p / p.sum())
+    ids = np.minimum(np.searchsorted(cdf, g.random(n), side="right"), n_adapters - 1).astype(np.int32)
+    if p_base > 0:
+        ids[g.random(n) < p_base] = -1
+    waited = np.sort(g.random(n) * max_wait_ms)[::-1].copy()
+    return ids, waited
 
 
 ALL = {"tiny": tiny, "attn70b": attn70b_decode, "all70b": all70b_decode, "zipf": zipf_pool,
