@@ -18,7 +18,7 @@ import os
 
 from . import build as _build
 
-__all__ = ["Pool", "LoraError", "build_segments", "form_batch", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF16"]
+__all__ = ["Pool", "AdapterCache", "LoraError", "build_segments", "form_batch", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF16"]
 
 LIB_PATH = _build.LIB
 if not os.path.exists(LIB_PATH):
@@ -27,7 +27,7 @@ if not os.path.exists(LIB_PATH):
         "(or __graft_entry__.build()) first.")
 lib = ctypes.CDLL(LIB_PATH)
 
-OK, EINVAL, ENOTLOADED, ENOMEM, ECUDA, EUNSUPPORTED, EDEVICE = 0, -1, -2, -3, -5, -6, -7
+OK, EINVAL, ENOTLOADED, ENOMEM, ECUDA, EUNSUPPORTED, EDEVICE, EPINNED = 0, -1, -2, -3, -5, -6, -7, -8
 DTYPE_F32, DTYPE_BF16 = 0, 1
 MAX_MODULES, MAX_RANK, PAGE_ROWS, MAX_DECODE_ROWS = 8, 64, 64, 256
 DEVERR = {0: "none", 1: "bad adapter id", 2: "adapter not loaded", 3: "in-kernel wait timed out",
@@ -64,6 +64,13 @@ _sig("lora_pool_unload", ctypes.c_int, _P, _I32, _P)
 _sig("lora_pool_query", ctypes.c_int, _P, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I64))
 _sig("lora_pool_free_rows", ctypes.c_int, _P, _I32, ctypes.POINTER(_I64))
 _sig("lora_build_segments", ctypes.c_int, _P, _I32, _P, _P, _P, ctypes.POINTER(_I32))
+_sig("lora_cache_create", ctypes.c_int, _I64, ctypes.c_double, ctypes.c_double, ctypes.POINTER(_P))
+_sig("lora_cache_destroy", ctypes.c_int, _P)
+_sig("lora_cache_acquire", ctypes.c_int, _P, _I32, _I64, ctypes.c_double, _P, _I32, ctypes.POINTER(_I32),
+     ctypes.POINTER(_I32))
+_sig("lora_cache_release", ctypes.c_int, _P, _I32)
+_sig("lora_cache_stats", ctypes.c_int, _P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I32))
+_sig("lora_cache_resident", ctypes.c_int, _P, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32))
 _sig("lora_form_batch", ctypes.c_int, _P, _P, _I32, ctypes.POINTER(lora_batch_policy), _P, ctypes.POINTER(_I32),
      ctypes.POINTER(_I32))
 _sig("lora_layer_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _I32, _F, _I32, _P)
@@ -164,6 +171,54 @@ def form_batch(queue_adapter, queue_waited_ms, max_batch, max_distinct=32, min_b
     _check(lib.lora_form_batch(qa.ctypes.data, qw.ctypes.data, len(qa), ctypes.byref(pol), out.ctypes.data,
                                ctypes.byref(n), ctypes.byref(d)), "lora_form_batch")
     return out[:n.value].copy(), d.value
+
+
+class AdapterCache:
+    """Residency decisions for a pool (lora_cache_*): value-per-byte eviction, reference counts,
+    the pinning guard.  Host only; the caller applies the decisions to the pool."""
+
+    def __init__(self, budget_bytes, guard_fraction=0.8, window_s=3600.0):
+        h = _P()
+        _check(lib.lora_cache_create(int(budget_bytes), float(guard_fraction), float(window_s), ctypes.byref(h)),
+               "lora_cache_create")
+        self.handle = h
+
+    def acquire(self, adapter, nbytes, now_s):
+        """Returns (adapters to unload first, whether `adapter` must be loaded); raises LoraError
+        with status EPINNED (guard) or ENOMEM (no room)."""
+        cap = 4096
+        ev = (_I32 * cap)()
+        n, load = _I32(0), _I32(0)
+        _check(lib.lora_cache_acquire(self.handle, int(adapter), int(nbytes), float(now_s), ev, cap, ctypes.byref(n),
+                                      ctypes.byref(load)), "lora_cache_acquire")
+        return [ev[i] for i in range(n.value)], bool(load.value)
+
+    def release(self, adapter):
+        _check(lib.lora_cache_release(self.handle, int(adapter)), "lora_cache_release")
+
+    def stats(self):
+        """(resident bytes, pinned bytes, resident adapters)"""
+        u, p, r = _I64(0), _I64(0), _I32(0)
+        _check(lib.lora_cache_stats(self.handle, ctypes.byref(u), ctypes.byref(p), ctypes.byref(r)), "lora_cache_stats")
+        return u.value, p.value, r.value
+
+    def resident(self, adapter):
+        """(resident, references)"""
+        r, k = _I32(0), _I32(0)
+        _check(lib.lora_cache_resident(self.handle, int(adapter), ctypes.byref(r), ctypes.byref(k)),
+               "lora_cache_resident")
+        return bool(r.value), k.value
+
+    def close(self):
+        if self.handle:
+            lib.lora_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Pool:

@@ -219,6 +219,7 @@ const char *lora_status_string(int s) {
         case LORA_ECUDA: return "CUDA error";
         case LORA_EUNSUPPORTED: return "unsupported request";
         case LORA_EDEVICE: return "device-side error recorded";
+        case LORA_EPINNED: return "pinning guard: no new adapters while the cache is pinned";
         default: return "unknown status";
     }
 }

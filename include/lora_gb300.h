@@ -57,6 +57,7 @@ typedef struct CUstream_st *lora_stream_t; /* == cudaStream_t */
 #define LORA_ECUDA (-5)        /* a CUDA runtime call failed (see lora_last_cuda_error) */
 #define LORA_EUNSUPPORTED (-6) /* valid request this build does not handle (see each call) */
 #define LORA_EDEVICE (-7)      /* a kernel recorded an error (see lora_last_device_error) */
+#define LORA_EPINNED (-8)      /* the adapter cache's pinning guard refuses a new adapter */
 
 /* output element types */
 #define LORA_DTYPE_F32 0
@@ -189,6 +190,40 @@ typedef struct {
  */
 int lora_form_batch(const int32_t *queue_adapter, const double *queue_waited_ms, int32_t n_queue,
                     const lora_batch_policy *policy, int32_t *out_idx, int32_t *out_n, int32_t *out_distinct);
+
+/*
+ * Adapter cache -- host-side residency decisions for the device pool.  ("m07 -- Multi-Adapter
+ * (LoRA) Serving", section 7 "Deep Dive B", "Eviction, and the trap in it": value =
+ * requests_last_hour / size_bytes, evict lowest value first, never an adapter with in-flight
+ * requests, and stop admitting new adapters while pinned bytes exceed a share of the budget;
+ * revision R3: that share is 80% once the budget is sized by Little's law.)  The cache only
+ * decides; the caller unloads and loads on the pool (lora_pool_unload / lora_pool_load, any
+ * stream).  Pure host code; one cache per pool, not thread-safe.
+ *
+ * lora_cache_create   budget_bytes >= 0, guard_fraction in [0, 1], window_s > 0 (the pages: an
+ *                     hour).  Errors: EINVAL.
+ * lora_cache_acquire  a sequence starts on `adapter` (bytes = what it holds in the pool) at time
+ *                     now_s: counts one request, and takes a reference.  If the adapter is
+ *                     resident nothing else happens (*must_load = 0).  Otherwise, unless the
+ *                     pinning guard refuses (EPINNED), room is made by evicting unreferenced
+ *                     adapters lowest value first (ties: older latest request, then smaller id);
+ *                     their ids go to evict[0 .. *n_evict) and the caller must unload them before
+ *                     loading `adapter` (*must_load = 1).  ENOMEM: even evicting every
+ *                     unreferenced adapter would not make room; nothing changed.  EINVAL: bad
+ *                     argument, a time earlier than the previous call's, a resident adapter
+ *                     acquired with another size, or more evictions than evict_cap.
+ * lora_cache_release  a sequence on `adapter` ended: drops one reference.  EINVAL if it holds none.
+ * lora_cache_stats    resident bytes, pinned bytes (resident with references), resident adapters.
+ * lora_cache_resident whether `adapter` is resident, and its references.
+ */
+typedef struct lora_cache lora_cache;
+int lora_cache_create(int64_t budget_bytes, double guard_fraction, double window_s, lora_cache **out);
+int lora_cache_destroy(lora_cache *cache);
+int lora_cache_acquire(lora_cache *cache, int32_t adapter, int64_t bytes, double now_s, int32_t *evict,
+                       int32_t evict_cap, int32_t *n_evict, int32_t *must_load);
+int lora_cache_release(lora_cache *cache, int32_t adapter);
+int lora_cache_stats(const lora_cache *cache, int64_t *used_bytes, int64_t *pinned_bytes, int32_t *resident);
+int lora_cache_resident(const lora_cache *cache, int32_t adapter, int32_t *resident, int32_t *ref);
 
 /* One projection of a layer call. */
 typedef struct {

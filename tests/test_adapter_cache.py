@@ -1,0 +1,268 @@
+"""The adapter cache: value-per-byte eviction, reference counts and the pinning guard
+("m07 -- Multi-Adapter (LoRA) Serving", section 7 "Deep Dive B", "Eviction, and the trap in it";
+revision R3 "The pinning guard was inconsistent").
+
+* the oracle against hand-worked scenarios, each the rule it is named after, and against the
+  pages' Little's-law numbers (180 pinned adapters, 11.7 GB, ~23 GB);
+* properties of a long seeded Zipf(1.1) simulation (budget never exceeded, no referenced adapter
+  evicted, the guard refuses exactly when pinned bytes exceed its share);
+* the library's lora_cache_* decision for decision against the oracle on the same traffic;
+* (GPU) the cache driving loads and unloads of a real pool -- loads on a side stream, each step's
+  forward waiting on them -- with every step's output checked against the fp64 forward.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from oracle import adapter_cache as OC
+
+ATTN = [(8192, 8192), (8192, 1024), (8192, 1024), (8192, 8192)]
+
+
+def _lib():
+    import adapter_serving_gb300 as L
+    return L
+
+
+# ------------------------------------------------------------------- hand-worked scenarios ---
+
+def test_value_per_byte_keeps_the_hot_adapter_that_lru_would_evict():
+    """A one-shot cold adapter must not push out a hot one: LRU would evict H (its latest request is
+    older), value per byte evicts C (1 request per 100 B against H's 10)."""
+    c = OC.AdapterCache(300, guard_fraction=1.0)
+    for t in range(10):
+        assert c.acquire("H", 100, float(t))[0] == "ok"
+        c.release("H")
+    assert c.acquire("C", 100, 10.0) == ("ok", [], True)
+    c.release("C")
+    assert c.acquire("N", 200, 11.0) == ("ok", ["C"], True)
+
+
+def test_referenced_adapter_is_never_evicted():
+    c = OC.AdapterCache(300, guard_fraction=1.0)
+    for t in range(10):
+        c.acquire("H", 100, float(t))
+        c.release("H")
+    c.acquire("C", 100, 10.0)  # still generating: keeps its reference
+    assert c.acquire("N", 200, 11.0) == ("ok", ["H"], True)
+
+
+def test_pinning_guard_refuses_new_adapters_but_not_resident_ones():
+    c = OC.AdapterCache(100, guard_fraction=0.5)
+    assert c.acquire("A", 60, 0.0) == ("ok", [], True)  # pinned 60 > 50
+    assert c.acquire("B", 10, 1.0) == ("pinned", [], False)
+    assert c.acquire("A", 60, 2.0) == ("ok", [], False)  # existing sequences' adapter still serves
+    c.release("A")
+    c.release("A")
+    assert c.acquire("B", 10, 3.0) == ("ok", [], True)
+
+
+def test_value_counts_only_the_window():
+    """Requests older than the window no longer count: H's ten early requests expire."""
+    c = OC.AdapterCache(200, guard_fraction=1.0, window_s=10.0)
+    for t in range(10):
+        c.acquire("H", 100, float(t))
+        c.release("H")
+    for t in (25.0, 26.0):
+        c.acquire("C", 100, t)
+        c.release("C")
+    assert c.acquire("N", 100, 30.0) == ("ok", ["H"], True)
+
+
+def test_no_room_changes_nothing():
+    c = OC.AdapterCache(100, guard_fraction=1.0)
+    c.acquire("A", 80, 0.0)
+    assert c.acquire("B", 50, 1.0) == ("nomem", [], False)
+    assert c.resident == {"A"} and c.used_bytes() == 80
+    assert c.acquire("B", 101, 2.0) == ("nomem", [], False)
+
+
+def test_ties_go_to_the_older_latest_request_then_the_smaller_id():
+    c = OC.AdapterCache(300, guard_fraction=1.0)
+    for a, t in ((5, 0.0), (3, 1.0), (4, 1.0)):
+        c.acquire(a, 100, t)
+        c.release(a)
+    assert c.acquire(9, 100, 2.0) == ("ok", [5], True)   # equal values: 5's request is oldest
+    c.release(9)
+    assert c.acquire(8, 100, 3.0) == ("ok", [3], True)   # 3 and 4 tie on time too: smaller id
+
+
+def test_evicts_the_fewest_adapters_in_value_order():
+    c = OC.AdapterCache(400, guard_fraction=1.0)
+    for a, n in ((1, 3), (2, 1), (3, 2), (4, 5)):
+        for k in range(n):
+            c.acquire(a, 100, float(10 * a + k))
+            c.release(a)
+    assert c.acquire(5, 150, 100.0) == ("ok", [2, 3], True)
+
+
+def test_little_law_sizing_matches_the_pages():
+    """R3: 3 distinct adapters/s x 60 s = 180 pinned; x 65 MB = 11.7 GB; budget 2x = ~23 GB."""
+    adapter = oracle.adapter_bytes(ATTN, 8, 80)  # the 65 MB attention rank-8 adapter
+    assert adapter // 10**6 == 65
+    assert OC.little_pinned_adapters(3, 60) == 180
+    assert round(180 * 65e6 / 1e9, 1) == 11.7
+    assert round(OC.little_cache_bytes(3, 60, 65e6) / 1e9) == 23
+    # with the cache sized so, the steady state pins half of it -- which is why R3 moves the guard to 80%
+    assert OC.little_pinned_adapters(3, 60) * 65e6 / OC.little_cache_bytes(3, 60, 65e6) == 0.5
+
+
+# ------------------------------------------------------------ simulation on Zipf traffic ---
+
+def _traffic(seed, n_events=3000, n_adapters=400):
+    """Requests arriving on Zipf(1.1) adapters; each runs for a seeded number of steps."""
+    ids, _ = wl.request_queue(n_events, seed=seed, n_adapters=n_adapters)
+    g = np.random.default_rng([seed, 77])
+    ranks = g.choice(np.array([8, 16, 32, 64]), n_adapters, p=[0.4, 0.3, 0.2, 0.1])
+    size = {a: int(ranks[a]) * 1000 for a in range(n_adapters)}
+    durations = g.integers(1, 40, n_events)
+    return ids, size, durations
+
+
+def _simulate(cache_acquire, cache_release, seed, per_step=4):
+    """Replays the traffic: every step `per_step` requests arrive and finished sequences end.
+    Returns the list of decisions."""
+    ids, size, durations = _traffic(seed)
+    ending = {}
+    log = []
+    step = 0
+    for i, a in enumerate(ids.tolist()):
+        if i % per_step == 0:
+            step += 1
+            for b in ending.pop(step, []):
+                cache_release(b)
+        d = cache_acquire(a, size[a], step * 0.5)
+        log.append(d)
+        if d[0] == "ok":
+            ending.setdefault(step + int(durations[i]), []).append(a)
+    return log
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_oracle_properties_on_zipf_traffic(seed):
+    c = OC.AdapterCache(120_000, guard_fraction=0.8, window_s=200.0)
+    seen = {"pinned": 0, "ok": 0, "nomem": 0}
+
+    def acquire(a, n, t):
+        pinned_before = c.pinned_bytes()
+        refs_before = {b for b in c.resident if c.ref.get(b, 0) > 0}
+        d = c.acquire(a, n, t)
+        seen[d[0]] += 1
+        assert c.used_bytes() <= c.budget
+        assert not set(d[1]) & refs_before, "evicted an adapter with in-flight sequences"
+        if d[0] == "pinned":
+            assert pinned_before > 0.8 * c.budget
+        elif d[2]:
+            assert pinned_before <= 0.8 * c.budget
+        return d
+
+    _simulate(acquire, c.release, seed)
+    assert seen["ok"] > 1000 and seen["pinned"] > 0  # the guard does fire under this load
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("guard,window", [(0.8, 200.0), (0.5, 30.0), (1.0, 3600.0)])
+def test_library_matches_oracle_decision_for_decision(seed, guard, window):
+    L = _lib()
+    ref = OC.AdapterCache(120_000, guard_fraction=guard, window_s=window)
+    lib = L.AdapterCache(120_000, guard_fraction=guard, window_s=window)
+
+    def lib_acquire(a, n, t):
+        try:
+            ev, load = lib.acquire(a, n, t)
+            return "ok", ev, load
+        except L.LoraError as e:
+            return {L.EPINNED: "pinned", L.ENOMEM: "nomem"}[e.status], [], False
+
+    got = _simulate(lib_acquire, lib.release, seed)
+    want = _simulate(ref.acquire, ref.release, seed)
+    assert got == want
+    u, p, r = lib.stats()
+    assert (u, p, r) == (ref.used_bytes(), ref.pinned_bytes(), len(ref.resident))
+    lib.close()
+
+
+def test_library_argument_checks():
+    L = _lib()
+    with pytest.raises(L.LoraError):
+        L.AdapterCache(100, guard_fraction=1.5)
+    with pytest.raises(L.LoraError):
+        L.AdapterCache(100, window_s=0.0)
+    c = L.AdapterCache(100)
+    with pytest.raises(L.LoraError):
+        c.release(3)  # never acquired
+    c.acquire(3, 10, 5.0)
+    with pytest.raises(L.LoraError):
+        c.acquire(4, 10, 4.0)  # time went back
+    with pytest.raises(L.LoraError):
+        c.acquire(3, 20, 6.0)  # resident with another size
+    with pytest.raises(L.LoraError):
+        c.acquire(-1, 10, 7.0)
+    assert c.resident(3) == (True, 1)
+    c.close()
+
+
+# ------------------------------------------------------------------------------ on the GPU ---
+
+@pytest.mark.gpu
+def test_cache_drives_a_real_pool_with_side_stream_loads():
+    """Sequences arrive on Zipf adapters; the cache decides residency for a pool too small for all
+    of them.  Evictions and loads run on a copy stream; each step's forward waits for them with an
+    event, and every step's y is checked against the fp64 forward."""
+    import torch
+    from harness import check_close, oracle_rows, run_stage, to_host_bf16
+    L = _lib()
+    n_adapters, d_in, d_out = 40, 1024, 1024
+    # one rank: the pool's buddy allocator then never fragments, so the cache's byte count is exact
+    ranks = np.full(n_adapters, 16, np.int32)
+    arrivals, _ = wl.request_queue(120, seed=5, n_adapters=n_adapters)
+    pages = 5                                  # 320 rows per module: room for 20 of the 40 adapters
+    row_bytes = (d_in + d_out) * 2
+    pool = L.Pool([d_in], [d_out], n_adapters, max_rank=64, pages=[pages], max_rows=64)
+    cache = L.AdapterCache(pages * 64 * row_bytes, guard_fraction=0.8, window_s=50.0)
+    base = wl.custom("cache_pool", {"proj": (d_in, d_out)}, [["proj"]], 1, ranks, 1.0, seed=9)
+    factors = {a: (to_host_bf16(base.A(a, "proj")).pin_memory(), to_host_bf16(base.B(a, "proj")).pin_memory())
+               for a in range(n_adapters)}
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    active = []   # (adapter, steps left)
+    loads = evictions = 0
+    g = np.random.default_rng(13)
+    for step in range(30):
+        for _ in range(4):  # arrivals
+            a = int(arrivals[(4 * step + _) % len(arrivals)])
+            try:
+                ev, must_load = cache.acquire(a, 16 * row_bytes, float(step))
+            except L.LoraError as e:
+                assert e.status in (L.EPINNED, L.ENOMEM)
+                continue
+            if ev or must_load:
+                copy.wait_stream(compute)  # the pool's rows are reused only after the steps that read them
+                for b in ev:
+                    pool.unload(b, stream=copy)
+                    evictions += 1
+                if must_load:
+                    pool.load(a, 0, *factors[a], stream=copy)
+                    loads += 1
+            active.append([a, int(g.integers(2, 8))])
+        if not active:
+            continue
+        done = torch.cuda.Event()
+        done.record(copy)
+        compute.wait_event(done)
+        ids = np.array([a for a, _ in active], np.int32)
+        w = wl.custom("cache_pool", {"proj": (d_in, d_out)}, [["proj"]], len(ids), ranks, 1.0, seed=9, ids=ids)
+        y = run_stage(pool, w, 0)["proj"].cpu().double().numpy()
+        check_close(y, oracle_rows(w, "proj", 0), what=f"step {step}")
+        for s in active:
+            s[1] -= 1
+        for a, left in active:
+            if left == 0:
+                cache.release(a)
+        active = [s for s in active if s[1] > 0]
+    assert loads > 20 and evictions > 0
+    code, _ = pool.last_device_error()
+    assert code == 0
+    pool.close()
+    cache.close()
