@@ -18,7 +18,7 @@ import os
 
 from . import build as _build
 
-__all__ = ["Pool", "AdapterCache", "LoraError", "build_segments", "form_batch", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF16"]
+__all__ = ["Pool", "AdapterCache", "LoraError", "build_segments", "form_batch", "quantize_rows_int8", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF16"]
 
 LIB_PATH = _build.LIB
 if not os.path.exists(LIB_PATH):
@@ -38,7 +38,8 @@ _P, _I32, _I64, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_f
 
 class lora_pool_desc(ctypes.Structure):
     _fields_ = [("n_modules", _I32), ("d_in", ctypes.POINTER(_I32)), ("d_out", ctypes.POINTER(_I32)),
-                ("max_adapters", _I32), ("max_rank", _I32), ("pages", ctypes.POINTER(_I64)), ("max_rows", _I32)]
+                ("max_adapters", _I32), ("max_rank", _I32), ("pages", ctypes.POINTER(_I64)), ("max_rows", _I32),
+                ("factor_dtype", _I32)]
 
 
 class lora_module_io(ctypes.Structure):
@@ -61,6 +62,8 @@ _sig("lora_pool_create", ctypes.c_int, ctypes.POINTER(lora_pool_desc), ctypes.PO
 _sig("lora_pool_destroy", ctypes.c_int, _P)
 _sig("lora_pool_load", ctypes.c_int, _P, _I32, _I32, _P, _P, _I32, _P)
 _sig("lora_pool_unload", ctypes.c_int, _P, _I32, _P)
+_sig("lora_pool_load_i8", ctypes.c_int, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P)
+_sig("lora_quantize_rows_int8", ctypes.c_int, _P, _I64, _I64, _P, _P)
 _sig("lora_pool_query", ctypes.c_int, _P, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I64))
 _sig("lora_pool_free_rows", ctypes.c_int, _P, _I32, ctypes.POINTER(_I64))
 _sig("lora_build_segments", ctypes.c_int, _P, _I32, _P, _P, _P, ctypes.POINTER(_I32))
@@ -155,6 +158,24 @@ def build_segments(ids):
     return perm[:n].copy(), seg_start[:k + 1].copy(), seg_adapter[:k].copy()
 
 
+def quantize_rows_int8(bits):
+    """Host int8 quantization, one fp32 scale per row (lora_quantize_rows_int8): ``bits`` are bf16
+    values (uint16 numpy array or bf16 torch tensor) [rows, cols]; returns (int8 codes, fp32 scales)
+    as numpy arrays."""
+    import numpy as np
+    if hasattr(bits, "view") and not isinstance(bits, np.ndarray):  # torch bf16 tensor
+        import torch
+        bits = bits.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    if b.ndim != 2:
+        raise ValueError("need a 2-D array")
+    codes = np.empty(b.shape, np.int8)
+    scales = np.empty(b.shape[0], np.float32)
+    _check(lib.lora_quantize_rows_int8(b.ctypes.data, b.shape[0], b.shape[1], codes.ctypes.data, scales.ctypes.data),
+           "lora_quantize_rows_int8")
+    return codes, scales
+
+
 def form_batch(queue_adapter, queue_waited_ms, max_batch, max_distinct=32, min_batch=1, tail_slots=4,
                max_queue_ms=200.0):
     """Adapter-aware batch former (lora_form_batch): returns (queue indices of the next step's
@@ -224,14 +245,19 @@ class AdapterCache:
 class Pool:
     """A paged adapter pool on the current CUDA device (lora_pool_create / _destroy)."""
 
-    def __init__(self, d_in, d_out, max_adapters, max_rank=MAX_RANK, pages=None, max_rows=MAX_DECODE_ROWS):
+    def __init__(self, d_in, d_out, max_adapters, max_rank=MAX_RANK, pages=None, max_rows=MAX_DECODE_ROWS,
+                 factor_dtype="bf16"):
+        """factor_dtype: "bf16" (load) or "int8" (load_i8: codes + per-rank-row scales; decode only)."""
+        if factor_dtype not in ("bf16", "int8"):
+            raise ValueError("factor_dtype: 'bf16' or 'int8'")
         n = len(d_in)
         self.d_in, self.d_out = list(map(int, d_in)), list(map(int, d_out))
         self._din = (_I32 * n)(*self.d_in)
         self._dout = (_I32 * n)(*self.d_out)
         self._pages = None if pages is None else (_I64 * n)(*map(int, pages))
         desc = lora_pool_desc(n, self._din, self._dout, int(max_adapters), int(max_rank),
-                              self._pages, int(max_rows))
+                              self._pages, int(max_rows), 1 if factor_dtype == "int8" else 0)
+        self.factor_dtype = factor_dtype
         h = _P()
         _check(lib.lora_pool_create(ctypes.byref(desc), ctypes.byref(h)), "lora_pool_create")
         self.handle = h
@@ -260,6 +286,27 @@ class Pool:
             raise ValueError(f"factor shapes {tuple(A.shape)} / {tuple(B.shape)} do not match module {module}")
         _check(lib.lora_pool_load(self.handle, int(adapter_id), int(module), _ptr(A), _ptr(B), int(rank),
                                   _stream(stream)), "lora_pool_load")
+
+    def load_i8(self, adapter_id, module, qA, sA, qB, sB, stream=None):
+        """int8 pool: qA int8 [rank, d_in], sA fp32 [rank], qB int8 [d_out, rank], sB fp32 [rank]
+        (numpy arrays or host/CUDA tensors for the codes; the scales on the host)."""
+        import numpy as np
+
+        def _arr(a, dt):
+            if hasattr(a, "data_ptr"):
+                return a, a.data_ptr()
+            a = np.ascontiguousarray(a, dtype=dt)
+            return a, a.ctypes.data
+        qA, pa = _arr(qA, np.int8)
+        qB, pb = _arr(qB, np.int8)
+        sA = np.ascontiguousarray(sA, dtype=np.float32)
+        sB = np.ascontiguousarray(sB, dtype=np.float32)
+        rank = int(qA.shape[0])
+        if tuple(qA.shape) != (rank, self.d_in[module]) or tuple(qB.shape) != (self.d_out[module], rank) or \
+                sA.shape != (rank,) or sB.shape != (rank,):
+            raise ValueError(f"int8 factor shapes do not match module {module}")
+        _check(lib.lora_pool_load_i8(self.handle, int(adapter_id), int(module), ctypes.c_void_p(pa), sA.ctypes.data,
+                                     ctypes.c_void_p(pb), sB.ctypes.data, rank, _stream(stream)), "lora_pool_load_i8")
 
     def unload(self, adapter_id, stream=None):
         _check(lib.lora_pool_unload(self.handle, int(adapter_id), _stream(stream)), "lora_pool_unload")

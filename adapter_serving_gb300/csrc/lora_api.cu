@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -85,8 +86,9 @@ struct RowAllocator {
 struct ModuleStore {
     int d_in = 0, d_out = 0;
     int64_t pages = 0;
-    uint16_t *A = nullptr;  // [pages * 64, d_in]
+    uint16_t *A = nullptr;  // [pages * 64, d_in] (bf16, or int8 codes in an int8 pool)
     uint16_t *B = nullptr;  // [pages * 64 * d_out] (rank-major runs of [d_out, rp])
+    float *fold = nullptr;  // int8 pool: [pages * 64] scale of each stored row (A scale x B scale)
     RowAllocator rows;
 };
 
@@ -158,6 +160,7 @@ struct lora_pool {
     int n_modules = 0;
     ModuleStore mod[LORA_MAX_MODULES];
     int max_adapters = 0, max_rank = 0, max_rows = 0;
+    bool i8 = false;                  // factors stored as int8 codes + per-row scales
     PoolEntry *d_table = nullptr;     // [n_modules][max_adapters]
     std::vector<PoolEntry> h_table;
     std::vector<int> rp_count;        // loaded entries per storage-rank order (for rpmax)
@@ -245,6 +248,7 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
     if (!d || !out || !d->d_in || !d->d_out) return LORA_EINVAL;
     if (d->n_modules < 1 || d->n_modules > LORA_MAX_MODULES) return LORA_EINVAL;
     if (d->max_adapters < 1 || d->max_rank < 1 || d->max_rank > LORA_MAX_RANK || d->max_rows < 1) return LORA_EINVAL;
+    if (d->factor_dtype != LORA_FACTOR_BF16 && d->factor_dtype != LORA_FACTOR_I8) return LORA_EINVAL;
     for (int m = 0; m < d->n_modules; ++m) {
         if (d->d_in[m] < 8 || d->d_out[m] < 8 || d->d_in[m] % 8 || d->d_out[m] % 8) return LORA_EINVAL;
         if (d->pages && d->pages[m] < 0) return LORA_EINVAL;
@@ -260,7 +264,9 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
     p->max_adapters = d->max_adapters;
     p->max_rank = d->max_rank;
     p->max_rows = d->max_rows;
+    p->i8 = d->factor_dtype == LORA_FACTOR_I8;
     p->rp_count.assign(4, 0);
+    const size_t esize = p->i8 ? 1 : 2;
     const int rp_cap = storage_rank(d->max_rank);
     int rc;
     for (int m = 0; m < p->n_modules; ++m) {
@@ -270,8 +276,9 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
         s.pages = d->pages ? d->pages[m]
                            : ((int64_t)d->max_adapters * rp_cap + LORA_PAGE_ROWS - 1) / LORA_PAGE_ROWS;
         const size_t rows = (size_t)s.pages * LORA_PAGE_ROWS;
-        if ((rc = dev_alloc(p, (void **)&s.A, rows * s.d_in * 2)) ||
-            (rc = dev_alloc(p, (void **)&s.B, rows * s.d_out * 2))) {
+        if ((rc = dev_alloc(p, (void **)&s.A, rows * s.d_in * esize)) ||
+            (rc = dev_alloc(p, (void **)&s.B, rows * s.d_out * esize)) ||
+            (p->i8 && (rc = dev_alloc(p, (void **)&s.fold, rows * 4)))) {
             lora_pool_destroy(p);
             return rc;
         }
@@ -353,7 +360,7 @@ static void release_entry(lora_pool *p, int m, int a) {
 int lora_pool_load(lora_pool *p, int32_t a, int32_t m, const void *A, const void *B, int32_t rank,
                    lora_stream_t stream) {
     if (!p || !A || !B || m < 0 || m >= p->n_modules || a < 0 || a >= p->max_adapters) return LORA_EINVAL;
-    if (rank < 1 || rank > p->max_rank) return LORA_EINVAL;
+    if (rank < 1 || rank > p->max_rank || p->i8) return LORA_EINVAL;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     ModuleStore &ms = p->mod[m];
     const int rp = storage_rank(rank);
@@ -379,6 +386,65 @@ int lora_pool_load(lora_pool *p, int32_t a, int32_t m, const void *A, const void
     p->entry(m, a) = e;
     p->rp_count[order_of(rp)]++;
     LORA_CUDA(launch_table_write(p->d_table + (size_t)m * p->max_adapters + a, e, s));
+    return LORA_OK;
+}
+
+int lora_pool_load_i8(lora_pool *p, int32_t a, int32_t m, const int8_t *qA, const float *sA, const int8_t *qB,
+                      const float *sB, int32_t rank, lora_stream_t stream) {
+    if (!p || !qA || !qB || !sA || !sB || m < 0 || m >= p->n_modules || a < 0 || a >= p->max_adapters)
+        return LORA_EINVAL;
+    if (rank < 1 || rank > p->max_rank || !p->i8) return LORA_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    ModuleStore &ms = p->mod[m];
+    const int rp = storage_rank(rank);
+    release_entry(p, m, a);
+    const int64_t off = ms.rows.alloc(order_of(rp));
+    if (off < 0) {
+        LORA_CUDA(launch_table_write(p->d_table + (size_t)m * p->max_adapters + a, p->entry(m, a), s));
+        return LORA_ENOMEM;
+    }
+    int8_t *Ad = reinterpret_cast<int8_t *>(ms.A) + (size_t)off * ms.d_in;
+    int8_t *Bd = reinterpret_cast<int8_t *>(ms.B) + (size_t)off * ms.d_out;
+    LORA_CUDA(cudaMemcpyAsync(Ad, qA, (size_t)rank * ms.d_in, cudaMemcpyDefault, s));
+    if (rank < rp) LORA_CUDA(cudaMemsetAsync(Ad + (size_t)rank * ms.d_in, 0, (size_t)(rp - rank) * ms.d_in, s));
+    if (rank == rp) {
+        LORA_CUDA(cudaMemcpyAsync(Bd, qB, (size_t)ms.d_out * rank, cudaMemcpyDefault, s));
+    } else {
+        LORA_CUDA(cudaMemsetAsync(Bd, 0, (size_t)ms.d_out * rp, s));
+        LORA_CUDA(cudaMemcpy2DAsync(Bd, (size_t)rp, qB, (size_t)rank, (size_t)rank, ms.d_out, cudaMemcpyDefault, s));
+    }
+    // one fp32 scale per stored row; pageable source, so the call returns once it is staged
+    std::vector<float> fold((size_t)rp, 0.f);
+    for (int j = 0; j < rank; ++j) fold[(size_t)j] = sA[j] * sB[j];
+    LORA_CUDA(cudaMemcpyAsync(ms.fold + off, fold.data(), (size_t)rp * 4, cudaMemcpyHostToDevice, s));
+    PoolEntry e{reinterpret_cast<const uint16_t *>(Ad), reinterpret_cast<const uint16_t *>(Bd), rank, rp, off};
+    p->entry(m, a) = e;
+    p->rp_count[order_of(rp)]++;
+    LORA_CUDA(launch_table_write(p->d_table + (size_t)m * p->max_adapters + a, e, s));
+    return LORA_OK;
+}
+
+int lora_quantize_rows_int8(const void *src, int64_t rows, int64_t cols, int8_t *codes, float *scales) {
+    if (rows < 0 || cols < 1 || (rows > 0 && (!src || !codes || !scales))) return LORA_EINVAL;
+    const uint16_t *b = static_cast<const uint16_t *>(src);
+    auto f32 = [](uint16_t h) {
+        const uint32_t u = (uint32_t)h << 16;
+        float f;
+        std::memcpy(&f, &u, 4);
+        return f;
+    };
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *row = b + r * cols;
+        float mx = 0.f;
+        for (int64_t c = 0; c < cols; ++c) mx = std::max(mx, std::fabs(f32(row[c])));
+        const float sc = mx / 127.0f;
+        scales[r] = sc;
+        for (int64_t c = 0; c < cols; ++c) {
+            float q = 0.f;
+            if (sc > 0.f) q = std::min(127.0f, std::max(-127.0f, std::nearbyint(f32(row[c]) / sc)));
+            codes[r * cols + c] = (int8_t)q;
+        }
+    }
     return LORA_OK;
 }
 
@@ -514,7 +580,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     }
     if (ids == nullptr && (!seg_start || !seg_adapter || n_seg < 1 || n_seg > n)) return LORA_EINVAL;
     const bool decode = n <= LORA_MAX_DECODE_ROWS;
-    if (ids && !decode) return LORA_EUNSUPPORTED;
+    if ((ids || p->i8) && !decode) return LORA_EUNSUPPORTED;
     cudaError_t e;
 
     // ---- prep: row grouping / checks
@@ -564,6 +630,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     sp.max_units = LORA_MAX_DECODE_ROWS;
     sp.ks_max = p->ks_cap;
     sp.scale = scale;
+    sp.i8 = p->i8 ? 1 : 0;
     sp.perm = decode ? p->perm : nullptr;
     sp.seg_start = p->seg_start;
     sp.seg_adapter = p->seg_adapter;
@@ -573,12 +640,13 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     sp.counters = p->shrink_cnt;
     // decode split width: about 128 KiB of A per block, in whole 2048-wide steps
     int kc_dec = kShrinkDecKC;
-    while (kc_dec * rpmax * 2 < 128 * 1024) kc_dec += kShrinkDecKC;
+    while (kc_dec * rpmax * (p->i8 ? 1 : 2) < 128 * 1024) kc_dec += kShrinkDecKC;
     int splits = 0;
     for (int i = 0; i < n_io; ++i) {
         const ModuleStore &ms = p->mod[io[i].module];
         sp.x[i] = static_cast<const uint16_t *>(io[i].x);
         sp.table[i] = pp.table[i];
+        sp.fold[i] = ms.fold;
         sp.T[i] = decode ? p->Tp + (size_t)i * kPackedTFloats : p->T + (size_t)i * p->max_rows * LORA_MAX_RANK;
         sp.tpos[i] = decode ? pp.tpos[i] : nullptr;
         sp.d_in[i] = ms.d_in;
@@ -603,6 +671,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     gp.stream_k = gp.n_chunks == 1 ? 1 : 0;
     gp.rpmax = rpmax;
     gp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
+    gp.i8 = p->i8 ? 1 : 0;
     gp.raster_group = 8;
     int64_t iters = 0;
     int tiles = 0;

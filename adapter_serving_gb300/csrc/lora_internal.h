@@ -116,6 +116,7 @@ struct GemmParams {
     int64_t total_iters;       // W k-blocks of all tiles (the stream-K space)
     int32_t rpmax;         // T row stride
     int32_t y_bf16;
+    int32_t i8;            // factors are int8 codes (B stages carry 1-byte elements)
     int32_t n_stages;
     int32_t raster_group;  // W tiles per raster group (round robin)
     int32_t tmem_cols;
@@ -158,6 +159,10 @@ struct ShrinkParams {
     const int32_t *qadapter;                // decode: adapter of each sorted position
     float *partials;      // [n_mod][ks_max][n][rpmax]
     int32_t *counters;    // [n_mod][max_units]
+    // int8 factors: A rows are int8 codes and t_j is multiplied by fold[m][row_off + j] (the
+    // product of the rank row's A and B scales)
+    int32_t i8;
+    const float *fold[LORA_MAX_MODULES];
 };
 
 struct PrepParams {
@@ -198,7 +203,7 @@ int make_tmap_y(CUtensorMap *tm, void *y, int64_t n, int64_t d_out, bool bf16);
 cudaError_t launch_prep_decode(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_prep_segments(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStream_t s);
-cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s);
+cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s);  // p.i8 picks the instantiation
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s);
 size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes);
 // TMEM buffers, stage count and shared memory of a gemm launch; false if no two stages fit

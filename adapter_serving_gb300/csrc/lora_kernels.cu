@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>
+#include <type_traits>
 #include <utility>
 
 #include "lora_internal.h"
@@ -394,6 +395,31 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b) {
     return r;
 }
 
+// Four signed bytes as floats, exactly: bias each code to 0..255 (xor 0x80), place it in the low
+// mantissa bits of 2^23 (byte permute), subtract 2^23 + 128.  Two full-rate operations per code.
+__device__ __forceinline__ float4 i8x4(uint32_t v) {
+    const uint32_t u = v ^ 0x80808080u;
+    constexpr float kBias = 8388736.0f;  // 2^23 + 128
+    return make_float4(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - kBias,
+                       __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - kBias,
+                       __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - kBias,
+                       __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - kBias);
+}
+
+// 8 int8 codes of A (a.x bytes 0..3, a.y bytes 0..3) against 8 bf16 values of x
+__device__ __forceinline__ float dot8_bf16(uint2 a, uint4 b) {
+    const float4 lo = i8x4(a.x), hi = i8x4(a.y);
+    float r = lo.x * bf16lo(b.x);
+    r = fmaf(lo.y, bf16hi(b.x), r);
+    r = fmaf(lo.z, bf16lo(b.y), r);
+    r = fmaf(lo.w, bf16hi(b.y), r);
+    r = fmaf(hi.x, bf16lo(b.z), r);
+    r = fmaf(hi.y, bf16hi(b.z), r);
+    r = fmaf(hi.z, bf16lo(b.w), r);
+    r = fmaf(hi.w, bf16hi(b.w), r);
+    return r;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -536,7 +562,10 @@ __global__ void __launch_bounds__(kShrinkThreads) shrink_kernel(const __grid_con
 // row per pass and walks the split in 2048-wide steps: every lane issues its eight 16-byte
 // loads of A up front, then reads the segment's x rows straight from L2.  Partial sums of the
 // splits are combined by the last block of the segment, in split order.
+// I8: A holds int8 codes (8 per 8-byte load) and t_j is scaled by the row's fold scale.
+template <bool I8>
 __global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const __grid_constant__ ShrinkParams p) {
+    using AChunk = typename std::conditional<I8, uint2, uint4>::type;  // 8 elements of A
     __shared__ int s_last;
     grid_dep_wait();
     grid_dep_launch();
@@ -566,12 +595,14 @@ __global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const 
     const int ks_max = p.ks_max, n = p.n;
     const int rpmax = p.rpmax;
     int r = 0, rp = 0;
-    const uint16_t *A = nullptr;
+    const uint8_t *A = nullptr;  // bytes: bf16 elements or int8 codes
+    const float *fold = nullptr;  // I8: scale of each of the adapter's rows
     if (a >= 0) {
         const PoolEntry *e = p.table[m] + a;
         r = e->rank;
         rp = e->rp;
-        A = e->A;
+        A = reinterpret_cast<const uint8_t *>(e->A);
+        if (I8) fold = p.fold[m] + e->row_off;
     }
     for (int j0 = 0; j0 < r; j0 += kShrinkThreads / 32) {
         const int j = j0 + warp;
@@ -585,11 +616,13 @@ __global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const 
             for (int rr = 0; rr < kShrinkDecRows; ++rr) row[rr] = qb + rr < qhi ? perm[qb + rr] : -1;
             // the block's K range in 2048-wide steps: 8 loads of A per lane, then x, then FMAs
             for (int k0 = kbeg; k0 < kend; k0 += kShrinkDecKC) {
-                uint4 av[kShrinkDecCh];
+                AChunk av[kShrinkDecCh];
 #pragma unroll
                 for (int c = 0; c < kShrinkDecCh; ++c) {
                     const int kk = k0 + lane * 8 + 256 * c;
-                    av[c] = kk < kend ? __ldg(reinterpret_cast<const uint4 *>(A + (size_t)j * d_in + kk)) : make_uint4(0, 0, 0, 0);
+                    const size_t at = ((size_t)j * d_in + kk) * (I8 ? 1 : 2);
+                    if (kk < kend) av[c] = __ldg(reinterpret_cast<const AChunk *>(A + at));
+                    else av[c] = AChunk{};
                 }
 #pragma unroll
                 for (int rr = 0; rr < kShrinkDecRows; ++rr) {
@@ -612,7 +645,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const 
                     const float v = warp_sum(acc[rr]);
                     if (lane == 0) {
                         if (ks == 1)
-                            t_at(qb + rr)[j] = scale * v;
+                            t_at(qb + rr)[j] = (I8 ? scale * fold[j] : scale) * v;
                         else
                             partials[(((size_t)m * ks_max + kc) * n + (qb + rr)) * rpmax + j] = v;
                     }
@@ -636,7 +669,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const 
         float v = 0.f;
         if (j < r)
             for (int c = 0; c < ks; ++c) v += __ldcg(partials + (((size_t)m * ks_max + c) * n + q) * rpmax + j);
-        t_at(q)[j] = scale * v;
+        t_at(q)[j] = (I8 && j < r ? scale * fold[j] : scale) * v;
     }
     if (tid == 0) p.counters[m * p.max_units + u] = 0;
 }
@@ -808,13 +841,13 @@ __device__ __forceinline__ ModLocal mod_local(const GemmParams &p, int m) {
 // decode: pack j of module M, its 16-byte pieces held one per lane (lane 0: header, lane e + 1:
 // slot e), already loaded.  Returns the bytes the copies bring.
 __device__ __forceinline__ void produce_pack(const uint4 rec, const GemmModule &M, int o0, int orows, int pack_ch,
-                                             uint8_t *sa, uint8_t *sx, uint64_t *full_bar, int lane) {
+                                             uint8_t *sa, uint8_t *sx, uint64_t *full_bar, int lane, int esize) {
     const int nslots = __shfl_sync(0xffffffffu, (int)rec.z, 0);
     const int tbegin = __shfl_sync(0xffffffffu, (int)rec.x, 0);
     const int tfloats = __shfl_sync(0xffffffffu, (int)rec.y, 0);
     BStageHdr *hdr = reinterpret_cast<BStageHdr *>(sx);
     const bool mine = lane >= 1 && lane <= nslots;
-    const uint16_t *B = reinterpret_cast<const uint16_t *>((uint64_t)rec.x | ((uint64_t)rec.y << 32));
+    const uint8_t *B = reinterpret_cast<const uint8_t *>((uint64_t)rec.x | ((uint64_t)rec.y << 32));
     const int rp = (int)(rec.z >> 24), off = (int)(rec.w & 0xff);
     uint32_t bytes = 0;
     if (mine) {
@@ -826,7 +859,7 @@ __device__ __forceinline__ void produce_pack(const uint4 rec, const GemmModule &
         sl.tstride = (int16_t)rp;
         sl.toff = pack_ch * off;
         hdr->slot[lane - 1] = sl;
-        bytes = (uint32_t)(orows * rp * 2);
+        bytes = (uint32_t)(orows * rp * esize);
     }
     const bool plain = !mine || (rp == 8 && ((rec.z >> 16) & 0xff) == 1);
     const bool singles8 = __all_sync(0xffffffffu, plain);
@@ -839,7 +872,7 @@ __device__ __forceinline__ void produce_pack(const uint4 rec, const GemmModule &
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(full_bar, total);
     __syncwarp();
-    if (mine) bulk_load(sa + off * 256, B + (size_t)o0 * rp, bytes, full_bar);
+    if (mine) bulk_load(sa + off * kBM * esize, B + (size_t)o0 * rp * esize, bytes, full_bar);
     if (lane == 0 && tfloats > 0) bulk_load(sx + kStageHdrBytes, M.T + tbegin, (uint32_t)tfloats * 4, full_bar);
 }
 
@@ -856,25 +889,46 @@ __device__ __forceinline__ float dot8_bf16_f32(uint4 b, float4 ta, float4 tb) {
     return acc0 + acc1;
 }
 
+// 8 int8 codes of B against 8 fp32 t values (the int8 scales are already folded into t)
+__device__ __forceinline__ float dot8_i8_f32(uint2 b, float4 ta, float4 tb) {
+    const float4 lo = i8x4(b.x), hi = i8x4(b.y);
+    float acc0 = lo.x * ta.x, acc1 = lo.y * ta.y;
+    acc0 = fmaf(lo.z, ta.z, acc0);
+    acc1 = fmaf(lo.w, ta.w, acc1);
+    acc0 = fmaf(hi.x, tb.x, acc0);
+    acc1 = fmaf(hi.y, tb.y, acc1);
+    acc0 = fmaf(hi.z, tb.z, acc0);
+    acc1 = fmaf(hi.w, tb.w, acc1);
+    return acc0 + acc1;
+}
+
 // One slot of a B stage: this lane's row of the slot's B (NCH 16-byte chunks, storage rank 8 NCH)
 // is loaded once, then every position of the slot streams its t row against it.
-template <int NCH>
+// I8: a row holds int8 codes, 8 per 8-byte chunk.
+template <int NCH, bool I8>
 __device__ __forceinline__ void expand_slot(const EpiCtx &c, uint32_t brow, uint32_t tslot, int tstride, int nrows,
                                             int q0, uint32_t tdel, int row0) {
+    using BChunk = typename std::conditional<I8, uint2, uint4>::type;
+    constexpr uint32_t kChunk = I8 ? 8 : 16;
     // lane o starts at chunk rot = o / (8 / NCH): the eight lanes of a quarter warp then hit eight
     // different 16-byte bank groups of their rows (rows are NCH * 16 bytes apart)
     const int rot = (c.o * NCH / 8) & (NCH - 1);
-    uint4 b[NCH];
-    const uint32_t mine = brow + (uint32_t)(c.o * NCH * 16);
+    BChunk b[NCH];
+    const uint32_t mine = brow + (uint32_t)(c.o * NCH) * kChunk;
 #pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) b[ch] = lds_u128(mine + ((ch + rot) & (NCH - 1)) * 16);
+    for (int ch = 0; ch < NCH; ++ch) {
+        const uint32_t at = mine + (uint32_t)((ch + rot) & (NCH - 1)) * kChunk;
+        if constexpr (I8) b[ch] = lds_u64(at);
+        else b[ch] = lds_u128(at);
+    }
     for (int r = 0; r < nrows; ++r) {
         const uint32_t trow = tslot + (uint32_t)(r * tstride * 4);
         float acc[NCH];
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
             const uint32_t tc = trow + ((ch + rot) & (NCH - 1)) * 32;
-            acc[ch] = dot8_bf16_f32(b[ch], lds128(tc), lds128(tc + 16));
+            if constexpr (I8) acc[ch] = dot8_i8_f32(b[ch], lds128(tc), lds128(tc + 16));
+            else acc[ch] = dot8_bf16_f32(b[ch], lds128(tc), lds128(tc + 16));
         }
 #pragma unroll
         for (int w = 1; w < NCH; w <<= 1)
@@ -888,7 +942,9 @@ __device__ __forceinline__ void expand_slot(const EpiCtx &c, uint32_t brow, uint
     }
 }
 
+template <bool I8>
 __device__ void expand_stage(const EpiCtx &c, const uint8_t *sa, const uint8_t *sx, uint32_t tdel, int row0) {
+    constexpr uint32_t kEsize = I8 ? 1 : 2;
     const BStageHdr *hdr = reinterpret_cast<const BStageHdr *>(sx);
     const int nslots = min(hdr->nslots, kPackSlots);
     const uint32_t a_base = smem_u32(sa), t_base = smem_u32(sx) + kStageHdrBytes;
@@ -897,7 +953,7 @@ __device__ void expand_stage(const EpiCtx &c, const uint8_t *sa, const uint8_t *
         // and its t row at pack_ch * 8 e floats, so all loads go out before any arithmetic and
         // only the column lookup waits on the slot header
         for (int e0 = 0; e0 < nslots; e0 += 4) {
-            uint4 bv[4];
+            typename std::conditional<I8, uint2, uint4>::type bv[4];
             float4 ta[4], tb[4];
             int q[4];
 #pragma unroll
@@ -905,7 +961,8 @@ __device__ void expand_stage(const EpiCtx &c, const uint8_t *sa, const uint8_t *
                 const int e = e0 + u;
                 q[u] = -1;
                 if (e < nslots) {
-                    bv[u] = lds_u128(a_base + (uint32_t)e * 2048 + (uint32_t)c.o * 16);
+                    if constexpr (I8) bv[u] = lds_u64(a_base + (uint32_t)e * 1024 + (uint32_t)c.o * 8);
+                    else bv[u] = lds_u128(a_base + (uint32_t)e * 2048 + (uint32_t)c.o * 16);
                     ta[u] = lds128(t_base + (uint32_t)(e * c.pack_ch * 32));
                     tb[u] = lds128(t_base + (uint32_t)(e * c.pack_ch * 32) + 16);
                     q[u] = hdr->slot[e].q0;
@@ -915,7 +972,12 @@ __device__ void expand_stage(const EpiCtx &c, const uint8_t *sa, const uint8_t *
             for (int u = 0; u < 4; ++u) {
                 if (q[u] >= 0 && q[u] < c.n) {  // the same for the whole warp
                     const int col = c.decode ? c.perm_s[q[u]] : q[u] - row0;
-                    if (col >= 0 && col < c.nt) tmem_st1(tdel + (uint32_t)col, dot8_bf16_f32(bv[u], ta[u], tb[u]));
+                    if (col >= 0 && col < c.nt) {
+                        float v;
+                        if constexpr (I8) v = dot8_i8_f32(bv[u], ta[u], tb[u]);
+                        else v = dot8_bf16_f32(bv[u], ta[u], tb[u]);
+                        tmem_st1(tdel + (uint32_t)col, v);
+                    }
                 }
             }
         }
@@ -923,13 +985,13 @@ __device__ void expand_stage(const EpiCtx &c, const uint8_t *sa, const uint8_t *
     }
     for (int e = 0; e < nslots; ++e) {
         const BSlotS sl = hdr->slot[e];
-        const uint32_t brow = a_base + (uint32_t)sl.off * 256;
+        const uint32_t brow = a_base + (uint32_t)sl.off * kBM * kEsize;
         const uint32_t tslot = t_base + (uint32_t)sl.toff * 4;
         switch (sl.rp) {
-            case 8: expand_slot<1>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
-            case 16: expand_slot<2>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
-            case 32: expand_slot<4>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
-            case 64: expand_slot<8>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
+            case 8: expand_slot<1, I8>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
+            case 16: expand_slot<2, I8>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
+            case 32: expand_slot<4, I8>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
+            case 64: expand_slot<8, I8>(c, brow, tslot, sl.tstride, sl.nrows, sl.q0, tdel, row0); break;
             default: break;
         }
     }
@@ -1150,6 +1212,8 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool wi
     if (leader) *counter = 0;
 }
 
+// I8: the adapters' B factors are int8 codes (their scales are folded into t by the shrink).
+template <bool I8>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1247,7 +1311,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 tma_load_2d(sa + a_bytes, &M.tmX, wfull + kk % S, kb * kBK, t.chunk * p.nt, pol_x);
             }
         };
-        if (p.stream_k) {
+        if (I8 || p.stream_k) {  // int8 factors: decode only
             // ---- decode: stream-K items, packs after their k-blocks
             while (ok && sc.next(p, npk, it)) {
                 const GemmModule &M = p.mod[it.m];
@@ -1278,7 +1342,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                         const uint4 cur = rec;
                         if (jb + 1 < b1 && lane <= kPackSlots)
                             rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + jb + 1) + lane);
-                        produce_pack(cur, M, o0, orows, p.pack_ch, sa, sa + a_bytes, bfull + k % S, lane);
+                        produce_pack(cur, M, o0, orows, p.pack_ch, sa, sa + a_bytes, bfull + k % S, lane, I8 ? 1 : 2);
                     }
                 }
             }
@@ -1399,7 +1463,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 umma_commit(empty + s);
                 return true;
             };
-            if (p.stream_k) {
+            if (I8 || p.stream_k) {  // int8 factors: decode only
                 Sched sc;
                 sc.begin(p, blockIdx.x);
                 Item it;
@@ -1502,7 +1566,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         float z[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[i] = 0.f;
-        if (p.stream_k) {
+        if (I8 || p.stream_k) {  // int8 factors: decode only
             Sched sc;
             sc.begin(p, blockIdx.x);
             Item cur;
@@ -1533,7 +1597,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                             ok = wait_b(k);
                             if (!ok) break;
                             const uint8_t *sa = smem + (size_t)s * stage_bytes;
-                            expand_stage(c, sa, sa + a_bytes, tdel, row0);
+                            expand_stage<I8>(c, sa, sa + a_bytes, tdel, row0);
                             named_bar_sync(1, 128);  // every warp is done with the stage
                             if (c.etid == 0) mbar_arrive(empty + s);
                         }
@@ -1582,7 +1646,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                         *reinterpret_cast<uint4 *>(ybuf + bbytes + off) = *reinterpret_cast<const uint4 *>(sx + off);
                     named_bar_sync(1, 128);  // the copy is complete: the slot goes back
                     if (c.etid == 0) mbar_arrive(empty + kk % S);
-                    expand_stage(c, ybuf, ybuf + bbytes, tacc, row0);
+                    expand_stage<I8>(c, ybuf, ybuf + bbytes, tacc, row0);
                     named_bar_sync(1, 128);  // before the buffer is overwritten
                 }
                 tmem_st_wait();
@@ -1684,18 +1748,22 @@ cudaError_t launch_prep_segments(const PrepParams &p, cudaStream_t s) {
 }
 
 cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStream_t s) {
-    if (p.by_segment) return launch_pdl(shrink_decode_kernel, dim3(grid_x, grid_y), dim3(kShrinkThreads), 0, s, p);
+    if (p.by_segment && p.i8)
+        return launch_pdl(shrink_decode_kernel<true>, dim3(grid_x, grid_y), dim3(kShrinkThreads), 0, s, p);
+    if (p.by_segment) return launch_pdl(shrink_decode_kernel<false>, dim3(grid_x, grid_y), dim3(kShrinkThreads), 0, s, p);
     return launch_pdl(shrink_kernel, dim3(grid_x, grid_y), dim3(kShrinkThreads), 0, s, p);
 }
 
 cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s) {
-    static size_t configured = 0;
-    if (smem_bytes > configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+    static size_t configured[2] = {0, 0};
+    const int v = p.i8 ? 1 : 0;
+    auto kernel = p.i8 ? gemm_kernel<true> : gemm_kernel<false>;
+    if (smem_bytes > configured[v]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
         if (e != cudaSuccess) return e;
-        configured = smem_bytes;
+        configured[v] = smem_bytes;
     }
-    return launch_pdl(gemm_kernel, dim3(p.n_cta), dim3(kGemmThreads), smem_bytes, s, p);
+    return launch_pdl(kernel, dim3(p.n_cta), dim3(kGemmThreads), smem_bytes, s, p);
 }
 
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s) {

@@ -56,22 +56,27 @@ def parse():
 WORKLOADS = {"attn70b": (wl.attn70b_decode, "decode"), "all70b": (wl.all70b_decode, "decode"),
              "zipf": (wl.zipf_pool, "decode"), "prefill": (wl.prefill_segments, "prefill"),
              # the prefill path at a size a profiler capture can replay (8 requests, ~8.7k tokens)
-             "prefill_small": (lambda: wl.prefill_segments(n_req=8), "prefill")}
+             "prefill_small": (lambda: wl.prefill_segments(n_req=8), "prefill"),
+             # the same decode batches with int8 adapter factors (codes + per-rank-row scales)
+             "attn70b_i8": (wl.attn70b_decode, "decode"), "all70b_i8": (wl.all70b_decode, "decode")}
+INT8 = {"attn70b_i8", "all70b_i8"}
 
 
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
-def algorithmic_bytes(w):
-    """Algorithmic bytes of one step: W once, each distinct adapter's factors once, x once per
-    stage, y written once (fp32)."""
+def algorithmic_bytes(w, int8=False):
+    """Algorithmic bytes of one step: W once, each distinct adapter's factors once (int8: one byte
+    per code plus the fp32 scale of each rank row, counted with A), x once per stage, y written
+    once (fp32)."""
     ids = w.row_adapters()
     distinct = sorted(set(int(a) for a in ids if a >= 0))
     mods = w.module_names()
+    e = 1 if int8 else 2
     W = sum(w.modules[m][0] * w.modules[m][1] * 2 for m in mods)
-    A = sum(int(w.ranks[a]) * w.modules[m][0] * 2 for a in distinct for m in mods)
-    B = sum(int(w.ranks[a]) * w.modules[m][1] * 2 for a in distinct for m in mods)
+    A = sum(int(w.ranks[a]) * (w.modules[m][0] * e + (4 if int8 else 0)) for a in distinct for m in mods)
+    B = sum(int(w.ranks[a]) * w.modules[m][1] * e for a in distinct for m in mods)
     X = sum(w.n_rows * w.modules[st[0]][0] * 2 for st in w.stages)
     Y = sum(w.n_rows * w.modules[m][1] * 4 for m in mods)
     return {"W": W, "A": A, "B": B, "x": X, "y": Y, "total": W + A + B + X + Y,
@@ -231,12 +236,19 @@ def run_ours(args, w):
     # ---- pool with the batch's adapters resident
     adapters = w.used_adapters()
     pages = (sum(max(8, int(w.ranks[a])) for a in adapters) + 63) // 64 + 4
+    int8 = args.workload in INT8
     pool = L.Pool([w.modules[m][0] for m in names], [w.modules[m][1] for m in names], w.n_adapters,
-                  max_rank=64, pages=[pages] * len(names), max_rows=w.n_rows)
+                  max_rank=64, pages=[pages] * len(names), max_rows=w.n_rows,
+                  factor_dtype="int8" if int8 else "bf16")
     for a in adapters:
         for mi, m in enumerate(names):
             A, B = factors[(int(a), m)]
-            pool.load(int(a), mi, torch.from_numpy(A).view(torch.bfloat16), torch.from_numpy(B).view(torch.bfloat16))
+            if int8:  # the library's quantizer: one scale per rank row of A and of B transposed
+                qA, sA = L.quantize_rows_int8(A)
+                qBt, sB = L.quantize_rows_int8(np.ascontiguousarray(B.T))
+                pool.load_i8(int(a), mi, qA, sA, np.ascontiguousarray(qBt.T), sB)
+            else:
+                pool.load(int(a), mi, torch.from_numpy(A).view(torch.bfloat16), torch.from_numpy(B).view(torch.bfloat16))
     bf = lambda b: torch.from_numpy(b).view(torch.bfloat16).to(dev)
     xd = [bf(x) for x in xs]
     Wd = {m: bf(Ws[m]) for m in names}
@@ -302,14 +314,14 @@ def run_ours(args, w):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    ab = algorithmic_bytes(w)
+    ab = algorithmic_bytes(w, int8)
     value = world * w.n_rows / (ms / 1e3)
     ranks = sorted(set(int(w.ranks[a]) for a in w.used_adapters()))
     line = {"metric": METRIC if args.workload == "attn70b" else f"{args.workload}: tokens/s", "value": value,
             "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "batch_rows": w.n_rows, "distinct_adapters": ab["distinct"],
+            "vs_baseline": None, "dtype": "bf16, int8 adapter factors" if int8 else "bf16", "data": "synthetic",
+            "config": {"workload": w.name + ("_int8_factors" if int8 else ""), "batch_rows": w.n_rows, "distinct_adapters": ab["distinct"],
                        "ranks": ranks,
                        "projections": ", ".join(f"{m} {w.modules[m][0]}->{w.modules[m][1]}" for m in names),
                        "calls_per_step": len(w.stages), "output": "fp32",

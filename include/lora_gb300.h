@@ -87,6 +87,9 @@ typedef struct CUstream_st *lora_stream_t; /* == cudaStream_t */
  *                  enough for every adapter at max_rank.
  *  max_rows        largest row count (decode rows or prefill tokens) one forward may pass;
  *                  sizes the workspace.
+ *  factor_dtype    LORA_FACTOR_BF16 (0: bf16 factors, lora_pool_load) or LORA_FACTOR_I8 (int8
+ *                  codes with one fp32 scale per rank row of A and of B transposed,
+ *                  lora_pool_load_i8; decode forwards only)
  */
 typedef struct {
     int32_t n_modules;
@@ -96,7 +99,11 @@ typedef struct {
     int32_t max_rank;
     const int64_t *pages;
     int32_t max_rows;
+    int32_t factor_dtype;
 } lora_pool_desc;
+
+#define LORA_FACTOR_BF16 0
+#define LORA_FACTOR_I8 1
 
 /*
  * lora_pool_create -- allocate the paged factor pool, its (pointer, rank) table and the
@@ -153,6 +160,30 @@ int lora_pool_free_rows(const lora_pool *pool, int32_t module, int64_t *free_row
  */
 int lora_build_segments(const int32_t *row_ids, int32_t n, int32_t *perm, int32_t *seg_start,
                         int32_t *seg_adapter, int32_t *n_seg);
+
+/*
+ * lora_quantize_rows_int8 -- host-side symmetric int8 quantization with one scale per row
+ * ("m07 -- Multi-Adapter (LoRA) Serving", section 9 "Bottlenecks and Evolution", item 3:
+ * adapters tolerate int8; half the bytes).  For each row, in fp32: scale = max|v| / 127,
+ * code = round-half-to-even(v / scale) clipped to [-127, 127]; a zero row gets scale 0.
+ *  src     host bf16 [rows, cols]
+ *  codes   host int8 [rows, cols]    out
+ *  scales  host fp32 [rows]          out
+ * For an adapter, quantize A [r, d_in] by rows and B transposed ([r, d_out]) by rows, so both
+ * scales belong to one rank index.  Errors: EINVAL.
+ */
+int lora_quantize_rows_int8(const void *src, int64_t rows, int64_t cols, int8_t *codes, float *scales);
+
+/*
+ * lora_pool_load_i8 -- lora_pool_load for an int8 pool: the adapter's factors as codes and
+ * scales, factor = code * scale.
+ *  qA      host or device int8 [rank, d_in]     sA  host fp32 [rank]  (scale of A's row j)
+ *  qB      host or device int8 [d_out, rank]    sB  host fp32 [rank]  (scale of B's column j)
+ * Stored like the bf16 factors (rows >= rank zero) plus, per stored row, sA[j] * sB[j] in fp32,
+ * which the shrink applies to t_j.  Errors: EINVAL (bf16 pool, shapes, rank), ENOMEM, ECUDA.
+ */
+int lora_pool_load_i8(lora_pool *pool, int32_t adapter_id, int32_t module, const int8_t *qA, const float *sA,
+                      const int8_t *qB, const float *sB, int32_t rank, lora_stream_t stream);
 
 /* Policy of the adapter-aware batch former (lora_form_batch). */
 typedef struct {

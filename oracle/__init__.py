@@ -116,6 +116,48 @@ def adapted_linear(x, W, ids, A, B, scale, rows=None, threads=0, return_t=False)
     return (y, t) if return_t else y
 
 
+def quantize_rows_int8(bits):
+    """Symmetric int8 codes with one fp32 scale per row ("m07 -- Multi-Adapter (LoRA) Serving",
+    section 9 "Bottlenecks and Evolution", item 3: quantize adapters to int8).  For each row:
+    scale = max|v| / 127 and code = round-half-even(v / scale), clipped to [-127, 127], all in fp32
+    (a zero row gets scale 0 and codes 0).  ``bits``: uint16 bf16 bits [rows, cols]; returns
+    (int8 [rows, cols], float32 [rows]).  For an adapter the rows are A's rank rows and B's rank
+    columns (the rows of B transposed), so both scales belong to one rank index."""
+    v = (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    v = v.reshape(np.shape(bits))
+    scale = (np.abs(v).max(axis=1) / np.float32(127.0)).astype(np.float32)
+    codes = np.zeros(v.shape, np.int8)
+    nz = scale > 0
+    q = np.rint(v[nz] / scale[nz, None])  # float32 / float32: one IEEE rounding, then half-to-even
+    codes[nz] = np.clip(q, -127, 127).astype(np.int8)
+    return codes, scale
+
+
+def dequantize_rows_int8(codes, scale):
+    """The factor the int8 codes stand for, exactly: code * scale in fp64."""
+    return np.asarray(codes, np.float64) * np.asarray(scale, np.float64)[:, None]
+
+
+def adapted_linear_factors64(x, W, ids, A64, B64, scale, rows=None, threads=0):
+    """fp64 ``y_i = W x_i + s * B_a (A_a x_i)`` with the factors given as fp64 arrays (the int8
+    codes times their scales).  The base term comes from ``adapted_linear`` with every row
+    base-only; the adapter term is the plain definition in numpy fp64, row by row."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    n = len(ids)
+    rows = np.arange(n, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    y = adapted_linear(x, W, np.full(n, -1, np.int32), [None] * max(1, len(A64)), [None] * max(1, len(A64)),
+                       scale, rows=rows, threads=threads)
+    xf = (np.ascontiguousarray(x, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    xf = xf.reshape(np.shape(x))
+    for k, i in enumerate(rows):
+        a = int(ids[i])
+        if a < 0:
+            continue
+        t = A64[a] @ xf[i]
+        y[k] += scale * (B64[a] @ t)
+    return y
+
+
 def segments(ids):
     """(perm, seg_start, seg_adapter): rows stably grouped by ascending adapter id."""
     lib = _load()
