@@ -77,6 +77,8 @@ _sig("lora_cache_resident", ctypes.c_int, _P, _I32, ctypes.POINTER(_I32), ctypes
 _sig("lora_form_batch", ctypes.c_int, _P, _P, _I32, ctypes.POINTER(lora_batch_policy), _P, ctypes.POINTER(_I32),
      ctypes.POINTER(_I32))
 _sig("lora_layer_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _I32, _F, _I32, _P)
+_sig("lora_plan_rows", ctypes.c_int, _P, _P, _I32, _P)
+_sig("lora_layer_forward_planned", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _F, _I32, _P)
 _sig("lora_linear_forward", ctypes.c_int, _P, _I32, _P, _P, _P, _I32, _F, _P, _I32, _P)
 _sig("lora_segment_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _P, _I32, _I32, _F,
      _I32, _P)
@@ -342,6 +344,17 @@ class Pool:
         ids = _dev_i32(row_adapter_ids, "row_adapter_ids")
         _check(lib.lora_layer_forward(self.handle, len(ios), arr, _ptr(ids), ids.numel(), float(scale), dt,
                                       _stream(stream)), "lora_layer_forward")
+
+    def plan_rows(self, row_adapter_ids, stream=None):
+        """Group a decode batch once for every module (lora_plan_rows); then layer_forward_planned."""
+        ids = _dev_i32(row_adapter_ids, "row_adapter_ids")
+        _check(lib.lora_plan_rows(self.handle, _ptr(ids), ids.numel(), _stream(stream)), "lora_plan_rows")
+
+    def layer_forward_planned(self, ios, scale, stream=None):
+        """ios: [(module, x, W, y)] on the rows of the last plan_rows."""
+        arr, dt = self._ios(ios)
+        _check(lib.lora_layer_forward_planned(self.handle, len(ios), arr, float(scale), dt, _stream(stream)),
+               "lora_layer_forward_planned")
 
     def linear_forward(self, module, x, W, row_adapter_ids, scale, y, stream=None):
         _dev_bf16(x, "x"), _dev_bf16(W, "W")

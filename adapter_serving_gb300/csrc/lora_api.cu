@@ -161,6 +161,10 @@ struct lora_pool {
     ModuleStore mod[LORA_MAX_MODULES];
     int max_adapters = 0, max_rank = 0, max_rows = 0;
     bool i8 = false;                  // factors stored as int8 codes + per-row scales
+    // a row plan (lora_plan_rows) stays usable while `gen` is unchanged: loads, unloads and
+    // forwards that build their own grouping advance it
+    uint64_t gen = 1, plan_gen = 0;
+    int plan_n = 0;
     PoolEntry *d_table = nullptr;     // [n_modules][max_adapters]
     std::vector<PoolEntry> h_table;
     std::vector<int> rp_count;        // loaded entries per storage-rank order (for rpmax)
@@ -361,6 +365,7 @@ int lora_pool_load(lora_pool *p, int32_t a, int32_t m, const void *A, const void
                    lora_stream_t stream) {
     if (!p || !A || !B || m < 0 || m >= p->n_modules || a < 0 || a >= p->max_adapters) return LORA_EINVAL;
     if (rank < 1 || rank > p->max_rank || p->i8) return LORA_EINVAL;
+    ++p->gen;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     ModuleStore &ms = p->mod[m];
     const int rp = storage_rank(rank);
@@ -394,6 +399,7 @@ int lora_pool_load_i8(lora_pool *p, int32_t a, int32_t m, const int8_t *qA, cons
     if (!p || !qA || !qB || !sA || !sB || m < 0 || m >= p->n_modules || a < 0 || a >= p->max_adapters)
         return LORA_EINVAL;
     if (rank < 1 || rank > p->max_rank || !p->i8) return LORA_EINVAL;
+    ++p->gen;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     ModuleStore &ms = p->mod[m];
     const int rp = storage_rank(rank);
@@ -450,6 +456,7 @@ int lora_quantize_rows_int8(const void *src, int64_t rows, int64_t cols, int8_t 
 
 int lora_pool_unload(lora_pool *p, int32_t a, lora_stream_t stream) {
     if (!p || a < 0 || a >= p->max_adapters) return LORA_EINVAL;
+    ++p->gen;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     bool any = false;
     for (int m = 0; m < p->n_modules; ++m) {
@@ -565,21 +572,47 @@ extern "C" int lora_profile_read(lora_pool *p, int32_t kind, int32_t *launches, 
 
 // ------------------------------------------------------------------ forward ----------------
 
+// mode: kOwnGrouping (group the rows, then shrink and gemm), kBuildPlan (group the rows and build
+// the packs of every module of the pool, nothing else), kUsePlan (shrink and gemm on the last plan)
+enum { kOwnGrouping = 0, kBuildPlan = 1, kUsePlan = 2 };
+
 static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const int32_t *ids,
                         const int32_t *seg_start, const int32_t *seg_adapter, int n_seg, int n, float scale,
-                        int y_dtype, cudaStream_t s) {
-    if (!p || !io || n_io < 1 || n_io > LORA_MAX_MODULES || n < 0 || n > p->max_rows) return LORA_EINVAL;
-    if (y_dtype != LORA_DTYPE_F32 && y_dtype != LORA_DTYPE_BF16) return LORA_EINVAL;
-    for (int i = 0; i < n_io; ++i)
-        if (io[i].module < 0 || io[i].module >= p->n_modules) return LORA_EINVAL;
+                        int y_dtype, cudaStream_t s, int mode = kOwnGrouping) {
+    if (!p) return LORA_EINVAL;
+    if (mode == kUsePlan) {
+        if (p->plan_gen != p->gen) return LORA_EINVAL;  // no plan, or the pool changed since
+        n = p->plan_n;
+    }
+    if (mode == kBuildPlan) {
+        if (!ids || n < 0 || n > std::min(p->max_rows, LORA_MAX_DECODE_ROWS)) return LORA_EINVAL;
+        ++p->gen;
+        p->plan_gen = 0;
+        if (n == 0) {
+            p->plan_gen = p->gen;
+            p->plan_n = 0;
+            return LORA_OK;
+        }
+    } else {
+        if (!io || n_io < 1 || n_io > LORA_MAX_MODULES || n < 0 || n > p->max_rows) return LORA_EINVAL;
+        if (y_dtype != LORA_DTYPE_F32 && y_dtype != LORA_DTYPE_BF16) return LORA_EINVAL;
+        for (int i = 0; i < n_io; ++i)
+            if (io[i].module < 0 || io[i].module >= p->n_modules) return LORA_EINVAL;
+        if (mode == kOwnGrouping) ++p->gen;  // this call's grouping overwrites any plan
+    }
     if (n == 0) return LORA_OK;  // empty batch: nothing to read or write
-    for (int i = 0; i < n_io; ++i) {
+    for (int i = 0; mode != kBuildPlan && i < n_io; ++i) {
         const lora_module_io &m = io[i];
         if (m.module < 0 || m.module >= p->n_modules || !m.x || !m.W || !m.y) return LORA_EINVAL;
         if (!aligned16(m.x) || !aligned16(m.W) || !aligned16(m.y)) return LORA_EINVAL;
     }
-    if (ids == nullptr && (!seg_start || !seg_adapter || n_seg < 1 || n_seg > n)) return LORA_EINVAL;
+    if (mode == kOwnGrouping && ids == nullptr && (!seg_start || !seg_adapter || n_seg < 1 || n_seg > n))
+        return LORA_EINVAL;
     const bool decode = n <= LORA_MAX_DECODE_ROWS;
+    // the plan covers every module of the pool; a planned call finds module m's packs at slot m
+    const int n_prep = mode == kBuildPlan ? p->n_modules : n_io;
+    auto pool_module = [&](int i) { return mode == kBuildPlan ? i : io[i].module; };
+    auto slot = [&](int i) { return mode == kOwnGrouping ? i : pool_module(i); };
     if ((ids || p->i8) && !decode) return LORA_EUNSUPPORTED;
     cudaError_t e;
 
@@ -591,8 +624,8 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     pp.n_seg_in = n_seg;
     pp.n = n;
     pp.max_adapters = p->max_adapters;
-    pp.n_mod = n_io;
-    for (int i = 0; i < n_io; ++i) pp.table[i] = p->d_table + (size_t)io[i].module * p->max_adapters;
+    pp.n_mod = n_prep;
+    for (int i = 0; i < n_prep; ++i) pp.table[i] = p->d_table + (size_t)pool_module(i) * p->max_adapters;
     pp.perm = p->perm;
     pp.seg_start = p->seg_start;
     pp.seg_adapter = p->seg_adapter;
@@ -602,9 +635,9 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     const int nt = decode ? ((n + 15) & ~15) : 256;  // rows per MMA tile (MMA N)
     const int rpmax = p->rpmax();
     if (decode) {
-        for (int i = 0; i < n_io; ++i) {
-            pp.packs[i] = p->packs + (size_t)i * kMaxPacks;
-            pp.tpos[i] = p->tpos + (size_t)i * LORA_MAX_DECODE_ROWS;
+        for (int i = 0; i < n_prep; ++i) {
+            pp.packs[i] = p->packs + (size_t)slot(i) * kMaxPacks;
+            pp.tpos[i] = p->tpos + (size_t)slot(i) * LORA_MAX_DECODE_ROWS;
         }
         pp.n_packs = p->n_packs;
         pp.pack_ch = pack_ch(nt);
@@ -615,11 +648,18 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
         pp.chunk_seg0 = p->chunk_seg0;
         pp.chunk_nb = p->chunk_nb;
     }
-    e = timed_launch(p, LORA_KERNEL_PREP, s,
-                     [&] { return decode ? launch_prep_decode(pp, s) : launch_prep_segments(pp, s); });
-    if (e != cudaSuccess) return cuda_fail(e, "prep kernel");
-    p->last_n = n;
-    p->last_decode = decode;
+    if (mode != kUsePlan) {
+        e = timed_launch(p, LORA_KERNEL_PREP, s,
+                         [&] { return decode ? launch_prep_decode(pp, s) : launch_prep_segments(pp, s); });
+        if (e != cudaSuccess) return cuda_fail(e, "prep kernel");
+        p->last_n = n;
+        p->last_decode = decode;
+    }
+    if (mode == kBuildPlan) {
+        p->plan_gen = p->gen;
+        p->plan_n = n;
+        return LORA_OK;
+    }
 
     // ---- shrink: T[m][q][:] = s * A_a x_row(q)
     ShrinkParams sp{};
@@ -688,6 +728,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
         gm.T = sp.T[i];
         gm.table = pp.table[i];
         gm.packs = decode ? pp.packs[i] : nullptr;
+        gm.npk_index = slot(i);
         gm.d_in = ms.d_in;
         gm.d_out = ms.d_out;
         gm.m_tiles = (ms.d_out + kBM - 1) / kBM;
@@ -741,6 +782,17 @@ int lora_linear_forward(lora_pool *p, int32_t module, const void *x, const void 
                         float scale, void *y, int32_t y_dtype, lora_stream_t stream) {
     lora_module_io io{module, x, W, y};
     return lora_layer_forward(p, 1, &io, ids, n, scale, y_dtype, stream);
+}
+
+int lora_plan_rows(lora_pool *p, const int32_t *ids, int32_t n, lora_stream_t stream) {
+    return forward_impl(p, 0, nullptr, ids, nullptr, nullptr, 0, n, 1.f, LORA_DTYPE_F32,
+                        reinterpret_cast<cudaStream_t>(stream), kBuildPlan);
+}
+
+int lora_layer_forward_planned(lora_pool *p, int32_t n_io, const lora_module_io *io, float scale, int32_t y_dtype,
+                               lora_stream_t stream) {
+    return forward_impl(p, n_io, io, nullptr, nullptr, nullptr, 0, 0, scale, y_dtype,
+                        reinterpret_cast<cudaStream_t>(stream), kUsePlan);
 }
 
 int lora_segment_forward(lora_pool *p, int32_t n_io, const lora_module_io *io, const int32_t *seg_start,

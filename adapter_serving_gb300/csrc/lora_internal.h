@@ -100,7 +100,7 @@ struct GemmModule {
     int32_t m_tiles, k_blocks;
     int64_t iter_begin;        // flattened (tile, W k-block) index where this module starts
     int32_t tile_begin;        // first global tile index of this module
-    int32_t pad_;
+    int32_t npk_index;         // decode: this module's entry of GemmParams::n_packs
 };
 
 struct GemmParams {

@@ -1263,11 +1263,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
     if (warp == 1) tmem_alloc(misc, (uint32_t)p.tmem_cols);
     // everything above overlaps the previous kernel on the stream; from here on its outputs
-    // (segments, packs, t) and the inputs written before it are read
+    // (segments, packs, t) and the inputs written before it are read.  The next kernel is let in
+    // only as CTAs exit (no early trigger): launched early, a shrink's blocks would crowd three
+    // to an SM onto the first SMs this grid's tail frees instead of spreading over all of them.
     grid_dep_wait();
-    grid_dep_launch();
     if (threadIdx.x == 0)
-        for (int m = 0; m < p.n_mod; ++m) npk[m] = (p.stream_k && p.n_packs) ? p.n_packs[m] : 0;
+        for (int m = 0; m < p.n_mod; ++m) npk[m] = (p.stream_k && p.n_packs) ? p.n_packs[p.mod[m].npk_index] : 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -5,7 +5,8 @@ Workload: the pages' 70B attention layer at decode -- q/o 8192->8192, k/v 8192->
 rows each carrying its own adapter (128 distinct rank-8 adapters on all four projections),
 scale 1 ("m07 -- Multi-Adapter (LoRA) Serving", section 2 "Scale Numbers", the batch-128
 distinct-adapter case).  One step = the whole hot path for one batch: q/k/v in one call
-(they read the same x), then o, each call = row grouping + shrink + tcgen05 base/expand.
+(they read the same x), then o.  The batch's rows are grouped once per step for every projection
+(lora_plan_rows), then each call is shrink + tcgen05 base/expand (lora_layer_forward_planned).
 
 Printed (rank 0, one JSON line): tokens/s (rows/s) over all GPUs, ms per step, HBM GB/s of
 algorithmic bytes, the dominant kernel's roofline fraction (CUDA events on the launch
@@ -264,11 +265,13 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
 
     def step(id_t):
+        if not grouped:  # decode: one row grouping per batch serves every call of the step
+            pool.plan_rows(id_t, stream=stream)
         for io in stage_io:
             if grouped:
                 pool.segment_forward(io, ss_d, id_t, w.n_rows, w.scale, stream=stream)
             else:
-                pool.layer_forward(io, id_t, w.scale, stream=stream)
+                pool.layer_forward_planned(io, w.scale, stream=stream)
 
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -329,7 +332,7 @@ def run_ours(args, w):
                        "parallelism": f"replicas x{world}"},
             "hbm_gbs": ab["total"] / (ms / 1e3) / 1e9,
             "algorithmic_bytes_per_step": ab["total"],
-            "gpu_launches": 3 * len(w.stages) * args.steps}
+            "gpu_launches": (3 * len(w.stages) if grouped else 1 + 2 * len(w.stages)) * args.steps}
     if grouped:
         base_f, lora_f = step_flops(w)
         tp, tsrc = tensor_peak()
@@ -377,6 +380,7 @@ def run_ours(args, w):
 
         def e2e_step(_):
             ids.copy_(hid, non_blocking=True)
+            pool.plan_rows(ids, stream=stream)
             xd[0].copy_(hx[0], non_blocking=True)
             x_ready = []
             with torch.cuda.stream(copy_stream):
@@ -389,7 +393,7 @@ def run_ours(args, w):
             for st, io in enumerate(stage_io):
                 if st > 0:
                     stream.wait_event(x_ready[st - 1])
-                pool.layer_forward(io, ids, w.scale, stream=stream)
+                pool.layer_forward_planned(io, w.scale, stream=stream)
                 done = torch.cuda.Event()
                 done.record(stream)
                 copy_stream.wait_event(done)

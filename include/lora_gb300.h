@@ -333,6 +333,26 @@ int lora_linear_forward_static(const void *x, const void *W, int32_t d_in, int32
                                void *y, int32_t y_dtype, lora_stream_t stream);
 
 /*
+ * lora_plan_rows -- group a decode batch's rows once for every projection of the pool (the
+ * index vector of "m07", section 6, is one per batch): stable sort by adapter id, id checks
+ * (device error word), and every module's expand packs.  Then lora_layer_forward_planned runs
+ * any projections of the pool on that batch without grouping again.
+ *  row_adapter_ids  device int32 [n], -1 = base only; 0 <= n <= min(LORA_MAX_DECODE_ROWS, max_rows)
+ * Asynchronous on `stream`.  The plan lives in the pool's workspace: lora_pool_load / _load_i8 /
+ * _unload and every forward that groups its own rows end it.  Errors: EINVAL, ECUDA.
+ */
+int lora_plan_rows(lora_pool *pool, const int32_t *row_adapter_ids, int32_t n, lora_stream_t stream);
+
+/*
+ * lora_layer_forward_planned -- lora_layer_forward on the rows of the last lora_plan_rows (same
+ * n, same ids): shrink and base + expand only.  `io` may name any modules of the pool, in any
+ * calls, as long as the plan is current.  Errors: EINVAL (no current plan, or as
+ * lora_layer_forward), EUNSUPPORTED, ECUDA.
+ */
+int lora_layer_forward_planned(lora_pool *pool, int32_t n_io, const lora_module_io *io, float scale,
+                               int32_t y_dtype, lora_stream_t stream);
+
+/*
  * lora_pool_last_segments -- synchronize the device and copy out the row grouping the most
  * recent forward on this pool used (computed on the device for lora_layer_forward; the
  * checked copy of the given table for lora_segment_forward).  Host outputs:

@@ -295,3 +295,40 @@ def test_prefill_segments_full_size_sampled():
     rows = np.unique(np.concatenate([ss[:-1], ss[1:] - 1, _sample_rows(w.n_rows, 24, 4)]))
     rows = rows[:: max(1, len(rows) // 48)]
     _check_all(w, pool, f, rows=rows, segments=True)
+
+
+def test_planned_forward_equals_own_grouping_bit_for_bit():
+    """One plan per batch (lora_plan_rows) serves both calls of the layer; the kernels then see the
+    same grouping and packs as a call that groups its own rows, so the outputs are identical."""
+    import adapter_serving_gb300 as L
+    w = _reduced_attn(n=96, n_ad=20, seed=33, p_base=0.15)
+    pool, f = make_pool(w)
+    own = {}
+    for st in range(len(w.stages)):
+        own.update(run_stage(pool, w, st))
+    names = w.module_names()
+    ids = torch.from_numpy(w.ids).cuda()
+    pool.plan_rows(ids)
+    planned = {}
+    for st in range(len(w.stages)):
+        x = to_dev_bf16(w.x(st))
+        ios = []
+        for m in w.stages[st]:
+            y = torch.full((w.n_rows, w.modules[m][1]), float("nan"), device="cuda")
+            ios.append((names.index(m), x, to_dev_bf16(w.W(m)), y))
+            planned[m] = y
+        pool.layer_forward_planned(ios, w.scale)
+    torch.cuda.synchronize()
+    for m in names:
+        assert torch.equal(planned[m], own[m]), m
+    # the plan ends with a load, and with a call that groups its own rows
+    st0 = [(names.index(m), to_dev_bf16(w.x(0)), to_dev_bf16(w.W(m)), planned[m]) for m in w.stages[0]]
+    a0 = int(w.used_adapters()[0])
+    pool.load(a0, 0, to_host_bf16(f[(a0, names[0])][0]), to_host_bf16(f[(a0, names[0])][1]))
+    with pytest.raises(L.LoraError):
+        pool.layer_forward_planned(st0, w.scale)
+    pool.plan_rows(ids)
+    run_stage(pool, w, 0)
+    with pytest.raises(L.LoraError):
+        pool.layer_forward_planned(st0, w.scale)
+    pool.close()
