@@ -372,27 +372,25 @@ def run_ours(args, w):
         h2d = sum(x.numel() * 2 for x in hx) + hid.numel() * 4
         d2h = sum(y.numel() * 4 for y in hy.values())
 
-        # The copies are pipelined the way a serving loop would: the ids and the first call's x go
-        # up first; every later call's x goes up on a copy stream while the calls before it run,
-        # and each call's outputs come back on that stream while the next call runs.  The timed
+        # The copies are pipelined the way a serving loop would: the ids go up first and the rows
+        # are grouped while every call's x goes up on a copy stream; each call waits for its own
+        # x, and its outputs come back on that stream while the next call runs.  The timed
         # region still holds every byte of both directions.
         copy_stream = torch.cuda.Stream(device=dev)
 
         def e2e_step(_):
             ids.copy_(hid, non_blocking=True)
-            pool.plan_rows(ids, stream=stream)
-            xd[0].copy_(hx[0], non_blocking=True)
             x_ready = []
             with torch.cuda.stream(copy_stream):
-                copy_stream.wait_stream(stream)
-                for st in range(1, len(hx)):
+                copy_stream.wait_stream(stream)  # the previous step has read x
+                for st in range(len(hx)):
                     xd[st].copy_(hx[st], non_blocking=True)
                     ev = torch.cuda.Event()
                     ev.record(copy_stream)
                     x_ready.append(ev)
+            pool.plan_rows(ids, stream=stream)  # groups the rows while x goes up
             for st, io in enumerate(stage_io):
-                if st > 0:
-                    stream.wait_event(x_ready[st - 1])
+                stream.wait_event(x_ready[st])
                 pool.layer_forward_planned(io, w.scale, stream=stream)
                 done = torch.cuda.Event()
                 done.record(stream)
