@@ -640,7 +640,8 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
             pp.tpos[i] = p->tpos + (size_t)slot(i) * LORA_MAX_DECODE_ROWS;
         }
         pp.n_packs = p->n_packs;
-        pp.pack_ch = pack_ch(nt);
+        pp.pack_ranks = p->i8 ? kPackRanksI8 : kPackRanks;
+        pp.pack_ch = pack_ch(nt, pp.pack_ranks);
     } else {
         if ((n + nt - 1) / nt > p->chunk_cap) return LORA_EUNSUPPORTED;
         pp.nt = nt;
@@ -751,7 +752,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     gp.n_packs = decode ? p->n_packs : nullptr;
     gp.chunk_seg0 = decode ? nullptr : p->chunk_seg0;
     gp.chunk_nb = decode ? nullptr : p->chunk_nb;
-    gp.pack_ch = pack_ch(nt);
+    gp.pack_ch = pack_ch(nt, p->i8 ? kPackRanksI8 : kPackRanks);
     gp.pf_ch = pf_ch(nt, rpmax);
     size_t smem = 0;
     if (!plan_gemm(gp, &smem)) return LORA_EUNSUPPORTED;

@@ -40,9 +40,11 @@ constexpr int kShrinkDecRows = 4;     // decode shrink: rows sharing one registe
 // adapter with a run of positions that use it) and those positions' t rows; the epilogue warps
 // compute the dot products from shared memory into the tile's TMEM delta buffer.
 
-constexpr int kPackRanks = 64;     // storage ranks per B stage (the stage's 16 KiB A buffer)
-constexpr int kPackSlots = kPackRanks / 8;
-constexpr int kStageHdrBytes = 256;  // slot header at the start of a B stage's X buffer
+// storage ranks per B stage: as many 128-row B slices as the stage's 16 KiB A buffer holds
+constexpr int kPackRanks = 64;       // bf16 factors
+constexpr int kPackRanksI8 = 128;    // int8 factors
+constexpr int kPackSlots = kPackRanksI8 / 8;
+constexpr int kStageHdrBytes = 512;  // slot header at the start of a B stage's X buffer
 constexpr int kYBufBytes = 32768;    // epilogue y staging
 
 // decode: one group of slots ("pack"), written by prep, read by the TMA producer
@@ -69,7 +71,7 @@ struct BSlotS {
     int32_t q0;       // first position (decode: sorted position; grouped rows: row)
     int16_t nrows;
     int16_t rp;
-    int16_t off;      // rank offset: the slot's B rows start at off * 256 bytes of the A buffer
+    int16_t off;      // rank offset: the slot's B rows start at off * 128 * (element bytes) of the A buffer
     int16_t tstride;  // floats between consecutive t rows
     int32_t toff;     // first float of the slot's t rows in the stage's t area
 };
@@ -81,8 +83,11 @@ struct BStageHdr {
 };
 static_assert(sizeof(BStageHdr) <= kStageHdrBytes, "B stage header");
 
-// rows per decode slot: the t rows of a full pack must fit the X buffer after the header
-__host__ __device__ constexpr int pack_ch(int nt) { return nt / 2 - 1 < 8 ? nt / 2 - 1 : 8; }
+// rows per decode slot: the t rows of a full pack (pack_ranks fp32 per row) must fit the X buffer
+// (nt * 128 bytes) after the header
+__host__ __device__ constexpr int pack_ch(int nt, int pack_ranks) {
+    return (nt * 128 - kStageHdrBytes) / (pack_ranks * 4) < 8 ? (nt * 128 - kStageHdrBytes) / (pack_ranks * 4) : 8;
+}
 // packs of one module (decode, n <= 256 rows): at most one per slot
 constexpr int kMaxPacks = LORA_MAX_DECODE_ROWS + LORA_MAX_DECODE_ROWS / 7 + 1;
 // packed t of one module: pack_ch floats per rank unit, 64 units per pack
@@ -185,6 +190,7 @@ struct PrepParams {
     int32_t *tpos[LORA_MAX_MODULES];  // [n] float offset of position q's t row in the packed T
     int32_t *n_packs;                 // [n_mod]
     int32_t pack_ch;
+    int32_t pack_ranks;               // decode: storage ranks per pack (kPackRanks or kPackRanksI8)
     // grouped rows: per row chunk of nt rows
     int32_t nt;
     int32_t pf_ch;

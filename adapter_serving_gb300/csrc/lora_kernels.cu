@@ -165,17 +165,18 @@ __device__ void build_packs(const PrepParams &p, const PrepShared &sh, int ns) {
             slots_tot += tot;
             units_tot += tot * (64 >> c);
         }
-        const int npk = (units_tot + kPackRanks - 1) / kPackRanks;
+        const int PR = p.pack_ranks;
+        const int npk = (units_tot + PR - 1) / PR;
         for (int k = 0; k < nsl; ++k) {
             const int P = unit_base + k * rp;
-            if (P % kPackRanks == 0) s_first[P / kPackRanks] = slot_base + k;
+            if (P % PR == 0) s_first[P / PR] = slot_base + k;
         }
         if (tid < ns) s_unit[tid] = rp > 0 ? unit_base : -1;
         if (tid == 0) s_first[npk] = slots_tot;
         named_bar_sync(bar, 256);
         BPackG *packs = p.packs[m];
         for (int k = 0; k < nsl; ++k) {
-            const int P = unit_base + k * rp, j = P / kPackRanks;
+            const int P = unit_base + k * rp, j = P / PR;
             const int e = slot_base + k - s_first[j];
             const int r0 = q0 + k * ch;
             BSlotG sl;
@@ -183,12 +184,12 @@ __device__ void build_packs(const PrepParams &p, const PrepShared &sh, int ns) {
             sl.q0 = (uint16_t)r0;
             sl.nrows = (uint8_t)min(ch, q1 - r0);
             sl.rp = (uint8_t)rp;
-            sl.off = (uint8_t)(P % kPackRanks);
+            sl.off = (uint8_t)(P % PR);
             sl.pad_[0] = sl.pad_[1] = sl.pad_[2] = 0;
             packs[j].slot[e] = sl;
             if (e == 0) {
-                packs[j].tbegin = ch * kPackRanks * j;
-                packs[j].tfloats = ch * min(kPackRanks, units_tot - kPackRanks * j);
+                packs[j].tbegin = ch * PR * j;
+                packs[j].tfloats = ch * min(PR, units_tot - PR * j);
                 packs[j].nslots = s_first[j + 1] - s_first[j];
                 packs[j].pad_ = 0;
             }

@@ -163,7 +163,8 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     pp.packs[0] = packs;
     pp.tpos[0] = tpos;
     pp.n_packs = n_packs;
-    pp.pack_ch = pack_ch(nt);
+    pp.pack_ranks = kPackRanks;
+    pp.pack_ch = pack_ch(nt, kPackRanks);
     if ((e = launch_prep_decode(pp, s)) != cudaSuccess)
         return fail(LORA_ECUDA, std::string("prep kernel: ") + cudaGetErrorString(e));
 
@@ -224,7 +225,7 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     gp.total_iters = (int64_t)gm.m_tiles * gm.k_blocks;
     gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, gp.total_iters / 4));
     gp.n_packs = n_packs;
-    gp.pack_ch = pack_ch(nt);
+    gp.pack_ch = pack_ch(nt, kPackRanks);
     size_t smem = 0;
     if (!plan_gemm(gp, &smem)) return fail(LORA_EUNSUPPORTED, "no two pipeline stages fit shared memory");
     gp.perm = perm;
