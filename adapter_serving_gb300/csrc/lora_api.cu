@@ -175,7 +175,6 @@ struct lora_pool {
     float *shrink_part = nullptr;     // [LORA_MAX_MODULES][ks_cap][256][64]
     int32_t *shrink_cnt = nullptr;    // [LORA_MAX_MODULES][256]
     float *gemm_part = nullptr;       // [num_sms][2][128 * 256]
-    int32_t *tile_cnt = nullptr;      // [tile_cap]
     BPackG *packs = nullptr;          // [LORA_MAX_MODULES][kMaxPacks] decode expand packs
     int32_t *tpos = nullptr;          // [LORA_MAX_MODULES][256] decode: t row of each position
     int32_t *n_packs = nullptr;       // [LORA_MAX_MODULES]
@@ -183,7 +182,7 @@ struct lora_pool {
     int32_t *chunk_seg0 = nullptr;    // [chunk_cap] grouped rows: first segment of each chunk
     int32_t *chunk_nb = nullptr;      // [chunk_cap] grouped rows: expand slots of each chunk
     int chunk_cap = 0;
-    int ks_cap = 0, tile_cap = 0;
+    int ks_cap = 0;
     // kernel timing: pending event pairs per kernel kind
     bool profiling = false;
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> prof_pending[3];
@@ -301,7 +300,6 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
         max_dout = std::max(max_dout, p->mod[m].d_out);
     }
     p->ks_cap = (max_din + 511) / 512;
-    p->tile_cap = LORA_MAX_MODULES * ((max_dout + kBM - 1) / kBM);
     const size_t R = (size_t)p->max_rows;
     p->chunk_cap = (int)(R / 256 + 2);  // row chunks of 256 (grouped rows)
     if ((rc = dev_alloc(p, (void **)&p->perm, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->seg_start, (R + 2) * 4)) ||
@@ -313,7 +311,6 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
                         (size_t)LORA_MAX_MODULES * p->ks_cap * LORA_MAX_DECODE_ROWS * LORA_MAX_RANK * 4)) ||
         (rc = dev_alloc(p, (void **)&p->shrink_cnt, (size_t)LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS * 4)) ||
         (rc = dev_alloc(p, (void **)&p->gemm_part, (size_t)p->num_sms * 2 * kBM * 256 * 4)) ||
-        (rc = dev_alloc(p, (void **)&p->tile_cnt, (size_t)p->tile_cap * 4)) ||
         (rc = dev_alloc(p, (void **)&p->packs, sizeof(BPackG) * LORA_MAX_MODULES * kMaxPacks)) ||
         (rc = dev_alloc(p, (void **)&p->tpos, (size_t)4 * LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS)) ||
         (rc = dev_alloc(p, (void **)&p->n_packs, (size_t)4 * LORA_MAX_MODULES)) ||
@@ -328,7 +325,6 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
     if (e == cudaSuccess) e = cudaMemset(p->err, 0, 16);
     if (e == cudaSuccess) e = cudaMemset(p->n_seg, 0, 16);
     if (e == cudaSuccess) e = cudaMemset(p->shrink_cnt, 0, (size_t)LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS * 4);
-    if (e == cudaSuccess) e = cudaMemset(p->tile_cnt, 0, (size_t)p->tile_cap * 4);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         lora_pool_destroy(p);
@@ -740,7 +736,6 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
         tiles += mt;
         iters += (int64_t)mt * gm.k_blocks;
     }
-    if (gp.stream_k && tiles > p->tile_cap) return LORA_EUNSUPPORTED;
     gp.total_tiles = tiles;
     gp.total_iters = iters;
     if (gp.stream_k) {
@@ -761,9 +756,13 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     gp.seg_adapter = p->seg_adapter;
     gp.n_seg = p->n_seg;
     gp.partials = p->gemm_part;
-    gp.tile_counters = p->tile_cnt;
     gp.err = p->err;
-    e = timed_launch(p, LORA_KERNEL_GEMM, s, [&] { return launch_gemm(gp, smem, s); });
+    // the decode gemm leaves split tiles to finalize_kernel (timed with it, as one gemm launch)
+    e = timed_launch(p, LORA_KERNEL_GEMM, s, [&] {
+        cudaError_t r = launch_gemm(gp, smem, s);
+        if (r == cudaSuccess && gp.stream_k) r = launch_finalize(gp, s);
+        return r;
+    });
     if (e != cudaSuccess) return cuda_fail(e, "gemm kernel");
     return LORA_OK;
 }

@@ -136,8 +136,7 @@ struct GemmParams {
     const int32_t *chunk_nb;    // grouped rows: B stages (slots) of each row chunk
     int32_t pack_ch;            // decode: positions per slot
     int32_t pf_ch;              // grouped rows: positions per slot
-    float *partials;       // [n_cta][2][kBM * nt]
-    int32_t *tile_counters;
+    float *partials;       // [n_cta][2][kBM * nt] stream-K pieces (a CTA's first and later item)
     int32_t *err;          // [0] code, [1] detail
 };
 
@@ -210,6 +209,7 @@ cudaError_t launch_prep_decode(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_prep_segments(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStream_t s);
 cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s);  // p.i8 picks the instantiation
+cudaError_t launch_finalize(const GemmParams &p, cudaStream_t s);  // decode: sum split tiles' pieces into y
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s);
 size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes);
 // TMEM buffers, stage count and shared memory of a gemm launch; false if no two stages fit

@@ -813,7 +813,6 @@ struct EpiCtx {
     int decode, n, nt, y_bf16, n_cta, pack_ch;
     int64_t total_iters;
     float *partials;
-    int32_t *tile_counters;
     uint32_t tmem_base;
     uint32_t delta_col;  // first TMEM column of the expand (delta) buffers (one per accumulator)
     int etid;            // 0..127 among epilogue threads
@@ -1018,18 +1017,16 @@ __device__ __forceinline__ float4 *piece_quads(float *piece, int c0, int o) {
     return reinterpret_cast<float4 *>(piece) + (size_t)(c0 >> 2) * kBM + o;
 }
 
-// Drain: accumulator (+ expand delta when this CTA heads the tile) -> y.  y goes out through
-// shared memory and TMA tensor stores of [16 columns][128 lanes] blocks: the blocks of a round
-// are staged together (the round is as many blocks as the staging buffer holds), then one
-// barrier and the round's stores back to back.
+// Drain: accumulator (+ expand delta) -> y.  y goes out through shared memory and TMA tensor
+// stores of [16 columns][128 lanes] blocks: the blocks of a round are staged together (the round
+// is as many blocks as the staging buffer holds), then one barrier and the round's stores back to
+// back.
 //
-// A tile split over several CTAs (stream-K) is finished by one CTA that adds the pieces in k
-// order, so the sum never depends on timing.  The piece holding k-block 0 is always the last
-// item of its CTA and the other pieces are the first items of theirs, so that CTA waits
-// (bounded) for the others and then finishes the tile without writing its own piece; if the
-// wait runs out it falls back to "write your piece, last to arrive finishes".  Pieces go to
-// global memory with plain vector stores; the finishing CTA pulls the other pieces into its idle
-// stage buffers with bulk copies when it can, else reads them with vector loads.
+// A tile split over several CTAs (stream-K) is not finished here: every CTA writes its piece of
+// the tile to its workspace slot with plain vector stores and moves on, and finalize_kernel, the
+// next launch, adds the pieces in k order (so the sum never depends on timing).  Finishing in the
+// gemm kept the CTAs that held a tile's first k-block waiting for the others and then summing
+// alone, 6-8 us after everyone else was done.
 struct DrainBufs {
     uint8_t *ybuf;       // y staging (the expand ring, idle during a drain)
     uint32_t ybuf_bytes;
@@ -1039,7 +1036,6 @@ struct DrainBufs {
     uint32_t ld_phase;   // phases of ld_bar completed so far
 };
 
-constexpr uint64_t kHeadWaitNs = 50000;  // how long a finishing CTA waits for the other pieces
 
 __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool with_delta, bool last,
                       volatile int *misc_flag, volatile int *abort_flag, DrainBufs &db) {
@@ -1058,7 +1054,6 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool wi
     const size_t slot_elems = (size_t)kBM * nt;
     const bool leader = c.etid == 0;
     const uint32_t esz = y_bf16 ? 2u : 4u;
-    const uint32_t piece_bytes = (uint32_t)ncols16 * kBM * 4;
 
     // y staging for a block of 16 columns at `dst` ([column][lane], fp32 or bf16)
     auto put16 = [&](uint8_t *dst, const float (&v)[16]) {
@@ -1127,90 +1122,17 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool wi
         return;
     }
 
-    // ---- partial tile (stream-K) ----
-    const int c_first = (int)(((it.it0 + 1) * n_cta - 1) / total_iters);  // CTA holding iteration it0
-    const int c_last = (int)(((it.it0 + it.kbn) * n_cta - 1) / total_iters);
-    const int nc = c_last - c_first + 1;
-    const int self_idx = (int)blockIdx.x - c_first;
-    int32_t *counter = c.tile_counters + it.tile;
-    auto part_of = [&](int cta) -> float * {  // the piece of CTA `cta`
-        const int64_t b_c = (int64_t)cta * total_iters / n_cta;
-        return partials + ((size_t)cta * 2 + ((b_c >= it.it0) ? 0 : 1)) * slot_elems;
-    };
-    bool finalize = false;
-    if (head) {
-        if (leader) {
-            const uint64_t t0 = globaltimer();
-            int seen = ld_acquire_gpu(counter);
-            while (seen != nc - 1 && globaltimer() - t0 < kHeadWaitNs) seen = ld_acquire_gpu(counter);
-            *misc_flag = (seen == nc - 1);
-        }
-        named_bar_sync(1, 128);
-        finalize = *misc_flag != 0;
-        named_bar_sync(1, 128);
-    }
-    if (!finalize) {
-        float *dst = part_of(blockIdx.x);
-        for (int c0 = 0; c0 < ncols16; c0 += 16) {
-            float v[16];
-            own_cols16(tacc, tdel, with_acc, with_delta, c0, v);
-            float4 *q = piece_quads(dst, c0, c.o);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) __stcg(q + k * kBM, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
-        }
-        __threadfence();  // this thread's share of the piece is visible device-wide
-        named_bar_sync(1, 128);
-        if (leader) *misc_flag = (atomicAdd(counter, 1) == nc - 1);
-        named_bar_sync(1, 128);
-        finalize = *misc_flag != 0;
-        named_bar_sync(1, 128);
-        if (!finalize) return;
-    }
-    __threadfence();
-
-    // finish: the other pieces, staged in shared memory when the stage buffers are idle
-    const uint32_t others_bytes = (uint32_t)(nc - 1) * piece_bytes;
-    const bool staged = last && (uint64_t)others_bytes <= db.stage_bytes;
-    set_staging(staged ? others_bytes : 0);
-    if (staged) {
-        fence_proxy_async_global();  // the pieces were written through the generic proxy
-        if (leader) {
-            mbar_arrive_expect_tx(db.ld_bar, others_bytes);
-            for (int k = 0, j = 0; k < nc; ++k)
-                if (k != self_idx) bulk_load(db.stage + (size_t)(j++) * piece_bytes, part_of(c_first + k), piece_bytes, db.ld_bar);
-        }
-        // bounded wait; a timeout has already raised the abort flag
-        mbar_wait(db.ld_bar, db.ld_phase & 1, abort_flag, nullptr);
-        ++db.ld_phase;
-    }
-    const uint32_t pbase = smem_u32(db.stage) + (uint32_t)c.o * 16;  // this lane's quad of piece 0, block 0
+    // ---- partial tile (stream-K): the piece goes to this CTA's workspace slot (first or later
+    // item of the CTA); finalize_kernel adds the pieces of the tile in k order once the grid is done
+    const int64_t b_c = (int64_t)blockIdx.x * total_iters / n_cta;
+    float *dst = partials + ((size_t)blockIdx.x * 2 + ((b_c >= it.it0) ? 0 : 1)) * slot_elems;
     for (int c0 = 0; c0 < ncols16; c0 += 16) {
-        float own[16], sum[16];
-        own_cols16(tacc, tdel, with_acc, with_delta, c0, own);
-        for (int jc = 0, j = 0; jc < nc; ++jc) {
-            float4 q[4];
-            if (jc == self_idx) {
+        float v[16];
+        own_cols16(tacc, tdel, with_acc, with_delta, c0, v);
+        float4 *q = piece_quads(dst, c0, c.o);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) q[k] = make_float4(own[4 * k], own[4 * k + 1], own[4 * k + 2], own[4 * k + 3]);
-            } else if (staged) {
-                const uint32_t a = pbase + (uint32_t)(j++) * piece_bytes + (uint32_t)(c0 >> 2) * kBM * 16;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) q[k] = lds128(a + (uint32_t)k * kBM * 16);
-            } else {
-                const float4 *src = piece_quads(part_of(c_first + jc), c0, c.o);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) q[k] = __ldcg(src + k * kBM);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float a[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sum[4 * k + e] = jc == 0 ? a[e] : sum[4 * k + e] + a[e];
-            }
-        }
-        emit(c0, sum);
+        for (int k = 0; k < 4; ++k) __stcg(q + k * kBM, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
     }
-    if (leader) *counter = 0;
 }
 
 // I8: the adapters' B factors are int8 codes (their scales are folded into t by the shrink).
@@ -1544,7 +1466,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         c.pack_ch = p.pack_ch;
         c.total_iters = p.total_iters;
         c.partials = p.partials;
-        c.tile_counters = p.tile_counters;
         volatile int *flag = reinterpret_cast<volatile int *>(misc + 2);
         if (p.decode)
             for (int q = c.etid; q < p.n; q += 128) perm_s[q] = p.perm[q];
@@ -1695,6 +1616,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
 }
 
+// Stream-K finish: block (tile, 16-column block) of every tile whose k range was split over
+// CTAs adds the CTAs' pieces in k order and writes those 16 columns of y (lane o of the block =
+// output row o0 + o: plain stores, 128 contiguous bytes per warp and column).  Tiles done by one
+// CTA were written by the gemm itself.  The CTAs of a split tile are found from the same
+// flattened (tile, k-block) split as the gemm's.
+__global__ void __launch_bounds__(kBM) finalize_kernel(const __grid_constant__ GemmParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int tile = blockIdx.x, c0 = blockIdx.y * 16, o = threadIdx.x;
+    int m = 0;
+    while (m + 1 < p.n_mod && p.mod[m + 1].tile_begin <= tile) ++m;
+    const GemmModule &M = p.mod[m];
+    const int lt = tile - M.tile_begin;
+    if (lt >= M.m_tiles || c0 >= p.n) return;
+    const int64_t it0 = M.iter_begin + (int64_t)lt * M.k_blocks;
+    const int c_first = (int)(((it0 + 1) * p.n_cta - 1) / p.total_iters);
+    const int c_last = (int)(((it0 + M.k_blocks) * p.n_cta - 1) / p.total_iters);
+    if (c_first == c_last) return;  // one CTA held the whole tile
+    const size_t slot_elems = (size_t)kBM * p.nt;
+    float v[16];
+    for (int cta = c_first; cta <= c_last; ++cta) {
+        const int64_t b_c = (int64_t)cta * p.total_iters / p.n_cta;
+        const float *piece = p.partials + ((size_t)cta * 2 + ((b_c >= it0) ? 0 : 1)) * slot_elems;
+        const float4 *q = reinterpret_cast<const float4 *>(piece) + (size_t)(c0 >> 2) * kBM + o;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 f = __ldcg(q + k * kBM);
+            const float a[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[4 * k + e] = cta == c_first ? a[e] : v[4 * k + e] + a[e];
+        }
+    }
+    const int orow = lt * kBM + o;  // decode: one row chunk, W tile = local tile index
+    if (orow >= M.d_out) return;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        if (c0 + i >= p.n) break;
+        const size_t at = (size_t)(c0 + i) * M.d_out + orow;
+        if (p.y_bf16) static_cast<__nv_bfloat16 *>(M.y)[at] = __float2bfloat16_rn(v[i]);
+        else static_cast<float *>(M.y)[at] = v[i];
+    }
+}
+
 // ====================================================================== launchers ==========
 
 size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes) {
@@ -1766,6 +1730,10 @@ cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s) 
         configured[v] = smem_bytes;
     }
     return launch_pdl(kernel, dim3(p.n_cta), dim3(kGemmThreads), smem_bytes, s, p);
+}
+
+cudaError_t launch_finalize(const GemmParams &p, cudaStream_t s) {
+    return launch_pdl(finalize_kernel, dim3(p.total_tiles, (p.n + 15) / 16), dim3(kBM), 0, s, p);
 }
 
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s) {

@@ -44,8 +44,7 @@ constexpr size_t kOffNSeg = al(kOffSegAdapter + 4 * 256);
 constexpr size_t kOffQAdapter = al(kOffNSeg + 16);
 constexpr size_t kOffErr = al(kOffQAdapter + 4 * 256);                     // from here up to kOffT:
 constexpr size_t kOffShrinkCnt = al(kOffErr + 16);                // cleared at every call
-constexpr size_t kOffTileCnt = al(kOffShrinkCnt + 4 * kStMaxUnits);
-constexpr size_t kOffT = al(kOffTileCnt + 4 * (kStMaxDout / kBM));  // packed t of the expand
+constexpr size_t kOffT = al(kOffShrinkCnt + 4 * kStMaxUnits);  // packed t of the expand
 constexpr size_t kOffPacks = al(kOffT + 4 * kPackedTFloats);
 constexpr size_t kOffTpos = al(kOffPacks + sizeof(BPackG) * kMaxPacks);
 constexpr size_t kOffNPacks = al(kOffTpos + 4 * LORA_MAX_DECODE_ROWS);
@@ -233,9 +232,10 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     gp.seg_adapter = seg_adapter;
     gp.n_seg = n_seg;
     gp.partials = reinterpret_cast<float *>(scratch + kOffGemmPart);
-    gp.tile_counters = reinterpret_cast<int32_t *>(scratch + kOffTileCnt);
     gp.err = err;
     if ((e = launch_gemm(gp, smem, s)) != cudaSuccess)
         return fail(LORA_ECUDA, std::string("gemm kernel: ") + cudaGetErrorString(e));
+    if ((e = launch_finalize(gp, s)) != cudaSuccess)  // split tiles' pieces -> y
+        return fail(LORA_ECUDA, std::string("finalize kernel: ") + cudaGetErrorString(e));
     return LORA_OK;
 }

@@ -332,7 +332,7 @@ def run_ours(args, w):
                        "parallelism": f"replicas x{world}"},
             "hbm_gbs": ab["total"] / (ms / 1e3) / 1e9,
             "algorithmic_bytes_per_step": ab["total"],
-            "gpu_launches": (3 * len(w.stages) if grouped else 1 + 2 * len(w.stages)) * args.steps}
+            "gpu_launches": (3 * len(w.stages) if grouped else 1 + 3 * len(w.stages)) * args.steps}
     if grouped:
         base_f, lora_f = step_flops(w)
         tp, tsrc = tensor_peak()
