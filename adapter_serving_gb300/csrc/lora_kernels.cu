@@ -1635,18 +1635,33 @@ __global__ void __launch_bounds__(kBM) finalize_kernel(const __grid_constant__ G
     const int c_last = (int)(((it0 + M.k_blocks) * p.n_cta - 1) / p.total_iters);
     if (c_first == c_last) return;  // one CTA held the whole tile
     const size_t slot_elems = (size_t)kBM * p.nt;
-    float v[16];
-    for (int cta = c_first; cta <= c_last; ++cta) {
+    auto quads = [&](int cta) {  // this thread's four column quads of CTA cta's piece
         const int64_t b_c = (int64_t)cta * p.total_iters / p.n_cta;
         const float *piece = p.partials + ((size_t)cta * 2 + ((b_c >= it0) ? 0 : 1)) * slot_elems;
-        const float4 *q = reinterpret_cast<const float4 *>(piece) + (size_t)(c0 >> 2) * kBM + o;
+        return reinterpret_cast<const float4 *>(piece) + (size_t)(c0 >> 2) * kBM + o;
+    };
+    // pieces in groups of up to three, every load of a group in flight before the adds (in k order)
+    float v[16];
+    for (int g0 = c_first; g0 <= c_last; g0 += 3) {
+        const int ng = min(3, c_last - g0 + 1);
+        float4 f[3][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 f = __ldcg(q + k * kBM);
-            const float a[4] = {f.x, f.y, f.z, f.w};
+        for (int j = 0; j < 3; ++j)
+            if (j < ng) {
+                const float4 *q = quads(g0 + j);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[4 * k + e] = cta == c_first ? a[e] : v[4 * k + e] + a[e];
-        }
+                for (int k = 0; k < 4; ++k) f[j][k] = __ldcg(q + k * kBM);
+            }
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+            if (j < ng) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float a[4] = {f[j][k].x, f[j][k].y, f[j][k].z, f[j][k].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[4 * k + e] = (g0 + j == c_first) ? a[e] : v[4 * k + e] + a[e];
+                }
+            }
     }
     const int orow = lt * kBM + o;  // decode: one row chunk, W tile = local tile index
     if (orow >= M.d_out) return;
