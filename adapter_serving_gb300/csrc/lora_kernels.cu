@@ -4,10 +4,12 @@
 //                         the expand packs (which adapters' B slices share one B stage)
 //   prep_segments_kernel  checks a given contiguous segment table (prefill), expand slots per
 //                         row chunk
-//   shrink_kernel         t_i = s * A_a x_i for every row (CUDA cores; bandwidth-bound)
+//   shrink_kernel         t_i = s * A_a x_i for every row (CUDA cores; bandwidth-bound), grouped
+//   shrink_decode_kernel  rows and decode batches; the decode one also reads int8 factors
 //   gemm_kernel           base W x_i on tcgen05 tensor cores into TMEM; the expand s B_a t_i from
 //                         B stages in the same TMA ring on CUDA cores into a second TMEM buffer;
 //                         both added on the way out
+//   finalize_kernel       decode: the stream-K tiles split over CTAs, their pieces added in k order
 //
 // The forward is the one on "m07 -- Multi-Adapter (LoRA) Serving", section 6 "Deep Dive A:
 // Batching Heterogeneous Adapters" (one batched base GEMM shared by the batch, plus a gathered
@@ -1032,13 +1034,10 @@ struct DrainBufs {
     uint32_t ybuf_bytes;
     uint8_t *stage;      // the stage buffers, free once the CTA's last item has been multiplied
     uint32_t stage_bytes;
-    uint64_t *ld_bar;    // completion of the bulk copies of other pieces
-    uint32_t ld_phase;   // phases of ld_bar completed so far
 };
 
 
-__device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool with_delta, bool last,
-                      volatile int *misc_flag, volatile int *abort_flag, DrainBufs &db) {
+__device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool with_delta, bool last, DrainBufs &db) {
     const ModLocal M = mod_local(*c.p, it.m);
     const int nt = c.nt, decode = c.decode, y_bf16 = c.y_bf16, n_cta = c.n_cta;
     const int64_t total_iters = c.total_iters;
@@ -1158,8 +1157,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     uint64_t *acc_full = empty + S;
     uint64_t *acc_free = acc_full + 2;
     uint64_t *mma_done = acc_free + 2;
-    uint64_t *ld_bar = mma_done + 1;  // drain: bulk copies of other pieces
-    uint32_t *misc = reinterpret_cast<uint32_t *>(ld_bar + 1);  // [0] tmem, [1] abort, [2] flag
+    uint32_t *misc = reinterpret_cast<uint32_t *>(mma_done + 1);  // [0] tmem, [1] abort
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -1173,9 +1171,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             mbar_init(acc_free + b, kEpiWarps);
         }
         mbar_init(mma_done, 1);
-        mbar_init(ld_bar, 1);
         misc[1] = 0;
-        misc[2] = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -1466,7 +1462,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         c.pack_ch = p.pack_ch;
         c.total_iters = p.total_iters;
         c.partials = p.partials;
-        volatile int *flag = reinterpret_cast<volatile int *>(misc + 2);
         if (p.decode)
             for (int q = c.etid; q < p.n; q += 128) perm_s[q] = p.perm[q];
         named_bar_sync(1, 128);
@@ -1475,8 +1470,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         db.ybuf_bytes = (uint32_t)p.ybuf_bytes;
         db.stage = smem;
         db.stage_bytes = (uint32_t)S * stage_bytes;
-        db.ld_bar = ld_bar;
-        db.ld_phase = 0;
         const uint32_t lane_off = (uint32_t)c.lane_base << 16;
         uint32_t bpar = 0;
         // wait for the B stage at ring slot kk (all 128 threads); false if the wait gave up
@@ -1534,7 +1527,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 ok = mbar_wait(acc_full + buf, use & 1, abort_flag, p.err);
                 if (named_bar_or(1, 128, !ok)) break;
                 tc_fence_after();
-                drain(c, cur, buf, true, nbs > 0, last, flag, abort_flag, db);
+                drain(c, cur, buf, true, nbs > 0, last, db);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acc_free + buf);
@@ -1596,7 +1589,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 ok = mbar_wait(acc_full + buf, use & 1, abort_flag, p.err);
                 if (named_bar_or(1, 128, !ok)) break;
                 tc_fence_after();
-                drain(c, cur, buf, true, false, !has_nxt, flag, abort_flag, db);
+                drain(c, cur, buf, true, false, !has_nxt, db);
                 tc_fence_before();
                 __syncwarp();
                 if (buf) ++use1; else ++use0;
@@ -1679,7 +1672,7 @@ __global__ void __launch_bounds__(kBM) finalize_kernel(const __grid_constant__ G
 size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes) {
     const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2;
     return 1024 + stage * n_stages + (size_t)ybuf_bytes + 4 * LORA_MAX_DECODE_ROWS + 4 * LORA_MAX_MODULES +
-           8 * (3 * (size_t)n_stages + 6) + 16;
+           8 * (3 * (size_t)n_stages + 5) + 16;
 }
 
 bool plan_gemm(GemmParams &gp, size_t *smem_bytes) {
