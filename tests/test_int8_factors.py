@@ -198,3 +198,33 @@ def test_int8_pool_refuses_what_it_does_not_serve():
         pool.segment_forward([(0, x, W, y)], ss, sa, 300, 1.0)  # grouped rows: bf16 pools only
     assert e.value.status == L.EUNSUPPORTED
     pool.close()
+
+
+@pytest.mark.gpu
+def test_int8_planned_forward_equals_own_grouping():
+    """int8 packs (128 ranks per stage) through the row plan give the same bits as a call that
+    groups its own rows, for fp32 and bf16 outputs."""
+    import torch
+    from harness import run_stage, to_dev_bf16
+    ranks = np.random.default_rng(8).choice(np.array([8, 16, 32, 64], np.int32), 24)
+    w = wl.custom("i8_plan", {"q": (2048, 2048), "o": (2048, 1024)}, [["q"], ["o"]], 77, ranks, 1.0, seed=9,
+                  ids=wl.random_ids(77, 24, 9, p_base=0.1))
+    q = _quantized(w, [int(a) for a in w.used_adapters()])
+    pool = _i8_pool(w, q)
+    names = w.module_names()
+    for y_dtype in (torch.float32, torch.bfloat16):
+        own = {}
+        for st in range(len(w.stages)):
+            own.update(run_stage(pool, w, st, y_dtype=y_dtype))
+        pool.plan_rows(torch.from_numpy(w.ids).cuda())
+        for st in range(len(w.stages)):
+            x = to_dev_bf16(w.x(st))
+            ios = []
+            for m in w.stages[st]:
+                y = torch.full((w.n_rows, w.modules[m][1]), float("nan"), dtype=y_dtype, device="cuda")
+                ios.append((names.index(m), x, to_dev_bf16(w.W(m)), y))
+            pool.layer_forward_planned(ios, w.scale)
+            for (mi, _, _, y), m in zip(ios, w.stages[st]):
+                torch.cuda.synchronize()
+                assert torch.equal(y, own[m]), (m, y_dtype)
+    pool.close()
