@@ -576,8 +576,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const 
     int m = 0;
     while (m + 1 < p.n_mod && p.split_begin[m + 1] <= (int)blockIdx.y) ++m;
     const int kc = blockIdx.y - p.split_begin[m];
-    const int ks = p.ksplit[m];
-    if (kc >= ks) return;
+    if (kc >= p.ksplit[m]) return;
     // one block per sorted position: rows of a shared adapter spread over blocks (its A is read
     // from L2 after the first), so blocks stay balanced
     const int u = blockIdx.x;
@@ -585,8 +584,19 @@ __global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const 
     const int qlo = u, qhi = u + 1;
     const int a = p.qadapter[u];
     const int d_in = p.d_in[m];
-    const int kbeg = kc * p.kc[m];
-    const int kend = min(d_in, kbeg + p.kc[m]);
+    if (a < 0) return;  // base-only position: no t row (every split of it returns here)
+    const PoolEntry *e = p.table[m] + a;
+    const int rp_u = e->rp;
+    // The split width was chosen for the largest storage rank in the pool (about 128 KiB of A
+    // per block); a lower-rank adapter takes proportionally wider splits, so fewer of them
+    // (blocks past its count leave at once).  Ranks are powers of two, so widths stay multiples
+    // of the 2048-wide step.
+    int kcw = p.kc[m];
+    for (int r2 = rp_u; r2 < p.rpmax && kcw < d_in; r2 <<= 1) kcw <<= 1;
+    const int ks = (d_in + kcw - 1) / kcw;
+    if (kc >= ks) return;
+    const int kbeg = kc * kcw;
+    const int kend = min(d_in, kbeg + kcw);
     const uint16_t *x = p.x[m];
     float *const T = p.T[m];
     const int32_t *const perm = p.perm;
@@ -600,8 +610,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const 
     int r = 0, rp = 0;
     const uint8_t *A = nullptr;  // bytes: bf16 elements or int8 codes
     const float *fold = nullptr;  // I8: scale of each of the adapter's rows
-    if (a >= 0) {
-        const PoolEntry *e = p.table[m] + a;
+    {
         r = e->rank;
         rp = e->rp;
         A = reinterpret_cast<const uint8_t *>(e->A);
