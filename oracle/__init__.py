@@ -17,6 +17,9 @@ GPU library (``adapter_serving_gb300``) and never imports it.
   "m07" section 6 "The cost is bandwidth, not compute"), ``base_bytes`` (base weights read
   once per step), ``lora_flop_ratio`` (the same section's ratio ``r(d_in+d_out)/(d_in d_out)``)
   and ``lora_extra_flops`` ("12. Adapter Serving ...", 2 x 2 x d x r per token).
+* quantized variants: ``quantize_rows_int8`` / ``adapted_linear_factors64`` (int8 adapter
+  factors) and ``quantize_rows_int4`` / ``adapted_linear_w4`` (an int4 base with bf16 or int8
+  adapters, "12. Adapter Serving ...", section "Quantization").
 """
 from __future__ import annotations
 
@@ -136,6 +139,42 @@ def quantize_rows_int8(bits):
 def dequantize_rows_int8(codes, scale):
     """The factor the int8 codes stand for, exactly: code * scale in fp64."""
     return np.asarray(codes, np.float64) * np.asarray(scale, np.float64)[:, None]
+
+
+def quantize_rows_int4(bits):
+    """Symmetric int4 base weights with one fp32 scale per output row ("12. Adapter Serving and
+    Multi-Tenant Customization", section "Quantization": the base model in INT4, the adapters in
+    BF16).  The pages fix neither the grouping nor the rounding; this follows the int8 rule with 7
+    in place of 127: scale = max|v| / 7 and code = round-half-even(v / scale), clipped to [-7, 7],
+    all in fp32 (a zero row gets scale 0 and codes 0).  ``bits``: uint16 bf16 bits [rows, cols];
+    returns (int8 [rows, cols] holding the codes, float32 [rows])."""
+    v = (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    v = v.reshape(np.shape(bits))
+    scale = (np.abs(v).max(axis=1) / np.float32(7.0)).astype(np.float32)
+    codes = np.zeros(v.shape, np.int8)
+    nz = scale > 0
+    q = np.rint(v[nz] / scale[nz, None])  # float32 / float32: one IEEE rounding, then half-to-even
+    codes[nz] = np.clip(q, -7, 7).astype(np.int8)
+    return codes, scale
+
+
+def adapted_linear_w4(x, codes, wscale, ids, A64, B64, scale, rows=None):
+    """fp64 ``y_i = W x_i + s * B_a (A_a x_i)`` with the base given as int4 codes and row scales:
+    W = codes * scale[:, None], exact in fp64 (the dequantised base of section "Quantization"), and
+    the factors as fp64 arrays (bf16 or int8 factors converted exactly; None where not used).
+    The plain definition in numpy fp64, the base term as one matrix product."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    rows = np.arange(len(ids), dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    W64 = np.asarray(codes, np.float64) * np.asarray(wscale, np.float64)[:, None]
+    xf = (np.ascontiguousarray(x, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    xf = xf.reshape(np.shape(x))[rows]
+    y = xf @ W64.T
+    for k, i in enumerate(rows):
+        a = int(ids[i])
+        if a < 0:
+            continue
+        y[k] += scale * (B64[a] @ (A64[a] @ xf[k]))
+    return y
 
 
 def adapted_linear_factors64(x, W, ids, A64, B64, scale, rows=None, threads=0):
