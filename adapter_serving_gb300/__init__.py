@@ -18,7 +18,7 @@ import os
 
 from . import build as _build
 
-__all__ = ["Pool", "AdapterCache", "LoraError", "build_segments", "form_batch", "quantize_rows_int8", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF16"]
+__all__ = ["Pool", "AdapterCache", "LoraError", "build_segments", "form_batch", "quantize_rows_int8", "quantize_w4", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF16"]
 
 LIB_PATH = _build.LIB
 if not os.path.exists(LIB_PATH):
@@ -46,6 +46,10 @@ class lora_module_io(ctypes.Structure):
     _fields_ = [("module", _I32), ("x", _P), ("W", _P), ("y", _P)]
 
 
+class lora_module_io_w4(ctypes.Structure):
+    _fields_ = [("module", _I32), ("x", _P), ("W_codes", _P), ("W_scale", _P), ("y", _P)]
+
+
 class lora_batch_policy(ctypes.Structure):
     _fields_ = [("max_batch", _I32), ("max_distinct", _I32), ("min_batch", _I32), ("tail_slots", _I32),
                 ("max_queue_ms", ctypes.c_double)]
@@ -64,6 +68,7 @@ _sig("lora_pool_load", ctypes.c_int, _P, _I32, _I32, _P, _P, _I32, _P)
 _sig("lora_pool_unload", ctypes.c_int, _P, _I32, _P)
 _sig("lora_pool_load_i8", ctypes.c_int, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P)
 _sig("lora_quantize_rows_int8", ctypes.c_int, _P, _I64, _I64, _P, _P)
+_sig("lora_quantize_w4", ctypes.c_int, _P, _I64, _I64, _P, _P)
 _sig("lora_pool_query", ctypes.c_int, _P, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I64))
 _sig("lora_pool_free_rows", ctypes.c_int, _P, _I32, ctypes.POINTER(_I64))
 _sig("lora_build_segments", ctypes.c_int, _P, _I32, _P, _P, _P, ctypes.POINTER(_I32))
@@ -79,6 +84,8 @@ _sig("lora_form_batch", ctypes.c_int, _P, _P, _I32, ctypes.POINTER(lora_batch_po
 _sig("lora_layer_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _I32, _F, _I32, _P)
 _sig("lora_plan_rows", ctypes.c_int, _P, _P, _I32, _P)
 _sig("lora_layer_forward_planned", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _F, _I32, _P)
+_sig("lora_layer_forward_w4", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io_w4), _P, _I32, _F, _I32, _P)
+_sig("lora_layer_forward_planned_w4", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io_w4), _F, _I32, _P)
 _sig("lora_linear_forward", ctypes.c_int, _P, _I32, _P, _P, _P, _I32, _F, _P, _I32, _P)
 _sig("lora_segment_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _P, _I32, _I32, _F,
      _I32, _P)
@@ -176,6 +183,24 @@ def quantize_rows_int8(bits):
     _check(lib.lora_quantize_rows_int8(b.ctypes.data, b.shape[0], b.shape[1], codes.ctypes.data, scales.ctypes.data),
            "lora_quantize_rows_int8")
     return codes, scales
+
+
+def quantize_w4(bits):
+    """Host int4 quantization of base weights, one fp32 scale per row (lora_quantize_w4): ``bits``
+    are bf16 values (uint16 numpy array or bf16 torch tensor) [rows, cols], cols a multiple of 8;
+    returns (packed uint8 [rows, cols // 2] in the kernel's layout, fp32 scales [rows])."""
+    import numpy as np
+    if hasattr(bits, "view") and not isinstance(bits, np.ndarray):  # torch bf16 tensor
+        import torch
+        bits = bits.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    if b.ndim != 2:
+        raise ValueError("need a 2-D array")
+    packed = np.empty((b.shape[0], b.shape[1] // 2), np.uint8)
+    scales = np.empty(b.shape[0], np.float32)
+    _check(lib.lora_quantize_w4(b.ctypes.data, b.shape[0], b.shape[1], packed.ctypes.data, scales.ctypes.data),
+           "lora_quantize_w4")
+    return packed, scales
 
 
 def form_batch(queue_adapter, queue_waited_ms, max_batch, max_distinct=32, min_batch=1, tail_slots=4,
@@ -337,6 +362,38 @@ class Pool:
             dt = d
             arr[i] = lora_module_io(int(module), x.data_ptr(), W.data_ptr(), y.data_ptr())
         return arr, dt
+
+    @staticmethod
+    def _ios_w4(ios):
+        import torch
+        arr = (lora_module_io_w4 * len(ios))()
+        dt = None
+        for i, (module, x, codes, wscale, y) in enumerate(ios):
+            _dev_bf16(x, "x")
+            if not (codes.is_cuda and codes.dtype == torch.uint8 and codes.is_contiguous()):
+                raise ValueError("W codes: need a contiguous CUDA uint8 tensor")
+            if not (wscale.is_cuda and wscale.dtype == torch.float32 and wscale.is_contiguous()):
+                raise ValueError("W scales: need a contiguous CUDA float32 tensor")
+            d = _y_dtype(y)
+            if dt is not None and d != dt:
+                raise ValueError("all outputs of one call share a dtype")
+            dt = d
+            arr[i] = lora_module_io_w4(int(module), x.data_ptr(), codes.data_ptr(), wscale.data_ptr(), y.data_ptr())
+        return arr, dt
+
+    def layer_forward_w4(self, ios, row_adapter_ids, scale, stream=None):
+        """int4 base: ios = [(module, x, W_codes, W_scale, y)] (quantize_w4's codes and scales on
+        the device), row_adapter_ids: CUDA int32 [n] (-1 = base only)."""
+        arr, dt = self._ios_w4(ios)
+        ids = _dev_i32(row_adapter_ids, "row_adapter_ids")
+        _check(lib.lora_layer_forward_w4(self.handle, len(ios), arr, _ptr(ids), ids.numel(), float(scale), dt,
+                                         _stream(stream)), "lora_layer_forward_w4")
+
+    def layer_forward_planned_w4(self, ios, scale, stream=None):
+        """int4 base on the rows of the last plan_rows: ios = [(module, x, W_codes, W_scale, y)]."""
+        arr, dt = self._ios_w4(ios)
+        _check(lib.lora_layer_forward_planned_w4(self.handle, len(ios), arr, float(scale), dt, _stream(stream)),
+               "lora_layer_forward_planned_w4")
 
     def layer_forward(self, ios, row_adapter_ids, scale, stream=None):
         """ios: [(module, x, W, y)], row_adapter_ids: CUDA int32 [n] (-1 = base only)."""

@@ -131,6 +131,29 @@ int lora::make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t col
     return LORA_OK;
 }
 
+// Bytes [rows, cols] (row-major; int4 base codes, two per byte), box {box_cols, box_rows}, no
+// swizzle: the shared-memory side is a dense [box_rows][box_cols] block.  256-byte L2 promotion, so
+// a 32-byte box row still brings whole DRAM bursts into L2.
+int lora::make_tmap_u8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled unavailable";
+        return LORA_ECUDA;
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled (int4 codes) failed (" + std::to_string((int)r) + ")";
+        return LORA_ECUDA;
+    }
+    return LORA_OK;
+}
+
 // Output y [n, d_out] (row-major, fp32 or bf16), box {128 outputs, 16 rows}, no swizzle: the
 // shared-memory side is a dense [16][128] block.  Rows past n and columns past d_out are clipped.
 int lora::make_tmap_y(CUtensorMap *tm, void *y, int64_t n, int64_t d_out, bool bf16) {
@@ -450,6 +473,36 @@ int lora_quantize_rows_int8(const void *src, int64_t rows, int64_t cols, int8_t 
     return LORA_OK;
 }
 
+int lora_quantize_w4(const void *src, int64_t rows, int64_t cols, uint8_t *packed, float *scales) {
+    if (rows < 0 || cols < 8 || cols % 8 != 0 || (rows > 0 && (!src || !packed || !scales))) return LORA_EINVAL;
+    const uint16_t *b = static_cast<const uint16_t *>(src);
+    auto f32 = [](uint16_t h) {
+        const uint32_t u = (uint32_t)h << 16;
+        float f;
+        std::memcpy(&f, &u, 4);
+        return f;
+    };
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *row = b + r * cols;
+        float mx = 0.f;
+        for (int64_t c = 0; c < cols; ++c) mx = std::max(mx, std::fabs(f32(row[c])));
+        const float sc = mx / 7.0f;
+        scales[r] = sc;
+        for (int64_t w = 0; w < cols / 8; ++w) {
+            uint32_t word = 0;
+            for (int e = 0; e < 8; ++e) {
+                float q = 0.f;
+                if (sc > 0.f) q = std::min(7.0f, std::max(-7.0f, std::nearbyint(f32(row[8 * w + e]) / sc)));
+                const uint32_t u = (uint32_t)((int)q + 8);  // 1..15
+                word |= u << ((e & 1) * 16 + (e >> 1) * 4);  // element 2s: nibble s; 2s + 1: nibble s of the high half
+            }
+            uint8_t *dst = packed + r * (cols / 2) + 4 * w;
+            for (int k = 0; k < 4; ++k) dst[k] = (uint8_t)(word >> (8 * k));  // little-endian, on any host
+        }
+    }
+    return LORA_OK;
+}
+
 int lora_pool_unload(lora_pool *p, int32_t a, lora_stream_t stream) {
     if (!p || a < 0 || a >= p->max_adapters) return LORA_EINVAL;
     ++p->gen;
@@ -572,9 +625,18 @@ extern "C" int lora_profile_read(lora_pool *p, int32_t kind, int32_t *launches, 
 // the packs of every module of the pool, nothing else), kUsePlan (shrink and gemm on the last plan)
 enum { kOwnGrouping = 0, kBuildPlan = 1, kUsePlan = 2 };
 
-static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const int32_t *ids,
+// One projection as the forward sees it: lora_module_io, or lora_module_io_w4 (w_scale set).
+struct IoDesc {
+    int32_t module;
+    const void *x;
+    const void *W;  // bf16 [d_out, d_in], or int4 codes [d_out, d_in / 2] bytes
+    const float *w_scale;
+    void *y;
+};
+
+static int forward_impl(lora_pool *p, int n_io, const IoDesc *io, const int32_t *ids,
                         const int32_t *seg_start, const int32_t *seg_adapter, int n_seg, int n, float scale,
-                        int y_dtype, cudaStream_t s, int mode = kOwnGrouping) {
+                        int y_dtype, cudaStream_t s, int mode = kOwnGrouping, bool w4 = false) {
     if (!p) return LORA_EINVAL;
     if (mode == kUsePlan) {
         if (p->plan_gen != p->gen) return LORA_EINVAL;  // no plan, or the pool changed since
@@ -598,9 +660,12 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     }
     if (n == 0) return LORA_OK;  // empty batch: nothing to read or write
     for (int i = 0; mode != kBuildPlan && i < n_io; ++i) {
-        const lora_module_io &m = io[i];
+        const IoDesc &m = io[i];
         if (m.module < 0 || m.module >= p->n_modules || !m.x || !m.W || !m.y) return LORA_EINVAL;
         if (!aligned16(m.x) || !aligned16(m.W) || !aligned16(m.y)) return LORA_EINVAL;
+        if (w4 && (!m.w_scale || (reinterpret_cast<uintptr_t>(m.w_scale) & 3))) return LORA_EINVAL;
+        // int4 codes: a packed row (d_in / 2 bytes) is a whole number of 16-byte TMA strides
+        if (w4 && p->mod[m.module].d_in % 32 != 0) return LORA_EUNSUPPORTED;
     }
     if (mode == kOwnGrouping && ids == nullptr && (!seg_start || !seg_adapter || n_seg < 1 || n_seg > n))
         return LORA_EINVAL;
@@ -609,7 +674,7 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     const int n_prep = mode == kBuildPlan ? p->n_modules : n_io;
     auto pool_module = [&](int i) { return mode == kBuildPlan ? i : io[i].module; };
     auto slot = [&](int i) { return mode == kOwnGrouping ? i : pool_module(i); };
-    if ((ids || p->i8) && !decode) return LORA_EUNSUPPORTED;
+    if ((ids || p->i8 || w4) && !decode) return LORA_EUNSUPPORTED;
     cudaError_t e;
 
     // ---- prep: row grouping / checks
@@ -709,13 +774,20 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     gp.rpmax = rpmax;
     gp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
     gp.i8 = p->i8 ? 1 : 0;
+    gp.w4 = w4 ? 1 : 0;
     gp.raster_group = 8;
     int64_t iters = 0;
     int tiles = 0;
     for (int i = 0; i < n_io; ++i) {
         const ModuleStore &ms = p->mod[io[i].module];
         GemmModule &gm = gp.mod[i];
-        int rc = make_tmap(&gm.tmW, io[i].W, ms.d_out, ms.d_in, kBM);
+        int rc;
+        if (w4) {
+            rc = make_tmap_u8(&gm.tmW, io[i].W, ms.d_out, ms.d_in / 2, kBK / 2, kBM);
+            gm.w_scale = io[i].w_scale;
+        } else {
+            rc = make_tmap(&gm.tmW, io[i].W, ms.d_out, ms.d_in, kBM);
+        }
         if (rc) return rc;
         rc = make_tmap(&gm.tmX, io[i].x, n, ms.d_in, gp.nt);
         if (rc) return rc;
@@ -767,15 +839,51 @@ static int forward_impl(lora_pool *p, int n_io, const lora_module_io *io, const 
     return LORA_OK;
 }
 
+namespace {
+// the projections of a call as IoDesc; false if n_io is out of range or io is missing
+bool io_descs(int32_t n_io, const lora_module_io *io, IoDesc (&d)[LORA_MAX_MODULES]) {
+    if (!io || n_io < 1 || n_io > LORA_MAX_MODULES) return false;
+    for (int i = 0; i < n_io; ++i) d[i] = IoDesc{io[i].module, io[i].x, io[i].W, nullptr, io[i].y};
+    return true;
+}
+bool io_descs(int32_t n_io, const lora_module_io_w4 *io, IoDesc (&d)[LORA_MAX_MODULES]) {
+    if (!io || n_io < 1 || n_io > LORA_MAX_MODULES) return false;
+    for (int i = 0; i < n_io; ++i) d[i] = IoDesc{io[i].module, io[i].x, io[i].W_codes, io[i].W_scale, io[i].y};
+    return true;
+}
+
+template <class Io>
+int layer_forward(lora_pool *p, int32_t n_io, const Io *io, const int32_t *ids, int32_t n, float scale,
+                  int32_t y_dtype, lora_stream_t stream, bool w4) {
+    IoDesc d[LORA_MAX_MODULES];
+    if (!io_descs(n_io, io, d)) return LORA_EINVAL;
+    if (!ids && n > 0) return LORA_EINVAL;
+    if (n == 0) return forward_impl(p, n_io, d, nullptr, nullptr, nullptr, 0, 0, scale, y_dtype, nullptr, kOwnGrouping, w4);
+    if (n > LORA_MAX_DECODE_ROWS) return LORA_EUNSUPPORTED;
+    return forward_impl(p, n_io, d, ids, nullptr, nullptr, 0, n, scale, y_dtype, reinterpret_cast<cudaStream_t>(stream),
+                        kOwnGrouping, w4);
+}
+
+template <class Io>
+int layer_forward_planned(lora_pool *p, int32_t n_io, const Io *io, float scale, int32_t y_dtype,
+                          lora_stream_t stream, bool w4) {
+    IoDesc d[LORA_MAX_MODULES];
+    if (!io_descs(n_io, io, d)) return LORA_EINVAL;
+    return forward_impl(p, n_io, d, nullptr, nullptr, nullptr, 0, 0, scale, y_dtype,
+                        reinterpret_cast<cudaStream_t>(stream), kUsePlan, w4);
+}
+}  // namespace
+
 extern "C" {
 
 int lora_layer_forward(lora_pool *p, int32_t n_io, const lora_module_io *io, const int32_t *ids, int32_t n,
                        float scale, int32_t y_dtype, lora_stream_t stream) {
-    if (!ids && n > 0) return LORA_EINVAL;
-    if (n == 0) return forward_impl(p, n_io, io, nullptr, nullptr, nullptr, 0, 0, scale, y_dtype, nullptr);
-    if (n > LORA_MAX_DECODE_ROWS) return LORA_EUNSUPPORTED;
-    return forward_impl(p, n_io, io, ids, nullptr, nullptr, 0, n, scale, y_dtype,
-                        reinterpret_cast<cudaStream_t>(stream));
+    return layer_forward(p, n_io, io, ids, n, scale, y_dtype, stream, false);
+}
+
+int lora_layer_forward_w4(lora_pool *p, int32_t n_io, const lora_module_io_w4 *io, const int32_t *ids, int32_t n,
+                          float scale, int32_t y_dtype, lora_stream_t stream) {
+    return layer_forward(p, n_io, io, ids, n, scale, y_dtype, stream, true);
 }
 
 int lora_linear_forward(lora_pool *p, int32_t module, const void *x, const void *W, const int32_t *ids, int32_t n,
@@ -791,16 +899,22 @@ int lora_plan_rows(lora_pool *p, const int32_t *ids, int32_t n, lora_stream_t st
 
 int lora_layer_forward_planned(lora_pool *p, int32_t n_io, const lora_module_io *io, float scale, int32_t y_dtype,
                                lora_stream_t stream) {
-    return forward_impl(p, n_io, io, nullptr, nullptr, nullptr, 0, 0, scale, y_dtype,
-                        reinterpret_cast<cudaStream_t>(stream), kUsePlan);
+    return layer_forward_planned(p, n_io, io, scale, y_dtype, stream, false);
+}
+
+int lora_layer_forward_planned_w4(lora_pool *p, int32_t n_io, const lora_module_io_w4 *io, float scale,
+                                  int32_t y_dtype, lora_stream_t stream) {
+    return layer_forward_planned(p, n_io, io, scale, y_dtype, stream, true);
 }
 
 int lora_segment_forward(lora_pool *p, int32_t n_io, const lora_module_io *io, const int32_t *seg_start,
                          const int32_t *seg_adapter, int32_t n_seg, int32_t n, float scale, int32_t y_dtype,
                          lora_stream_t stream) {
-    if (n == 0) return forward_impl(p, n_io, io, nullptr, nullptr, nullptr, 0, 0, scale, y_dtype, nullptr);
+    IoDesc d[LORA_MAX_MODULES];
+    if (!io_descs(n_io, io, d)) return LORA_EINVAL;
+    if (n == 0) return forward_impl(p, n_io, d, nullptr, nullptr, nullptr, 0, 0, scale, y_dtype, nullptr);
     if (!seg_start || !seg_adapter) return LORA_EINVAL;
-    return forward_impl(p, n_io, io, nullptr, seg_start, seg_adapter, n_seg, n, scale, y_dtype,
+    return forward_impl(p, n_io, d, nullptr, seg_start, seg_adapter, n_seg, n, scale, y_dtype,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -24,6 +24,10 @@ constexpr int kBM = 128;       // W rows per tile (MMA M)
 constexpr int kBK = 64;        // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kEpiWarps = 4;   // epilogue warps (one per TMEM lane quarter)
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+// int4 base weights: converter warps unpack each W k-block's codes into the bf16 tile the MMA reads
+constexpr int kConvWarps = 2;
+constexpr int kGemmThreadsW4 = kGemmThreads + 32 * kConvWarps;
+constexpr int kW4RawBytes = kBM * kBK / 2;  // packed codes of one W k-block (two per byte)
 constexpr int kMaxWin = 256;        // segments one tile's expand can touch (= max rows per tile)
 constexpr int kMaxStages = 8;
 constexpr int kShrinkThreads = 256;
@@ -97,6 +101,9 @@ struct GemmModule {
     CUtensorMap tmW;  // W [d_out, d_in]: box {64, 128}, 128B swizzle
     CUtensorMap tmX;  // X [n, d_in]:    box {64, nt},  128B swizzle
     CUtensorMap tmY;  // y [n, d_out]:   box {128, 16}, fp32 or bf16, no swizzle (epilogue stores)
+    // int4 base (GemmParams::w4): tmW is the packed codes [d_out, d_in / 2] bytes, box {32, 128},
+    // no swizzle (its 256-byte L2 promotion brings each row's next k-blocks into L2 with the first)
+    const float *w_scale;      // int4 base: [d_out] fp32 row scales
     void *y;
     const float *T;            // shrink result: decode packed per pack, grouped rows [n][rpmax]
     const PoolEntry *table;    // this module's entries [max_adapters]
@@ -122,6 +129,7 @@ struct GemmParams {
     int32_t rpmax;         // T row stride
     int32_t y_bf16;
     int32_t i8;            // factors are int8 codes (B stages carry 1-byte elements)
+    int32_t w4;            // base weights are int4 codes with one fp32 scale per output row (decode)
     int32_t n_stages;
     int32_t raster_group;  // W tiles per raster group (round robin)
     int32_t tmem_cols;
@@ -202,16 +210,18 @@ static_assert(sizeof(GemmParams) <= 32764, "gemm parameters exceed the kernel pa
 // tensor maps (lora_api.cu): bf16 [rows, cols] operand, box {64, box_rows}, 128-byte swizzle; and
 // the output y [n, d_out] (fp32 or bf16), box {128, 16}, for the epilogue's TMA stores
 int make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_rows);
+// bytes [rows, cols] (row-major), box {box_cols, box_rows}, no swizzle, 256-byte L2 promotion
+int make_tmap_u8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_cols, int box_rows);
 int make_tmap_y(CUtensorMap *tm, void *y, int64_t n, int64_t d_out, bool bf16);
 
 // launchers (lora_kernels.cu)
 cudaError_t launch_prep_decode(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_prep_segments(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStream_t s);
-cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s);  // p.i8 picks the instantiation
+cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s);  // p.i8, p.w4 pick the instantiation
 cudaError_t launch_finalize(const GemmParams &p, cudaStream_t s);  // decode: sum split tiles' pieces into y
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s);
-size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes);
+size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes, bool w4 = false);
 // TMEM buffers, stage count and shared memory of a gemm launch; false if no two stages fit
 bool plan_gemm(GemmParams &gp, size_t *smem_bytes);
 // decode packs of one module: at most one pack per slot

@@ -1008,17 +1008,17 @@ __device__ void expand_stage(const EpiCtx &c, const uint8_t *sa, const uint8_t *
     }
 }
 
-// This CTA's share of 16 columns of a tile: accumulator and/or expand delta, both TMEM loads in
-// flight before the one wait.
+// This CTA's share of 16 columns of a tile: accumulator (times the W row's scale, 1 for bf16
+// weights) and/or expand delta, both TMEM loads in flight before the one wait.
 __device__ __forceinline__ void own_cols16(uint32_t tacc, uint32_t tdel, bool with_acc, bool with_delta, int c0,
-                                           float (&v)[16]) {
+                                           float wsc, float (&v)[16]) {
     uint32_t r[16], d[16];
     if (with_acc) tmem_ld16(tacc + c0, r);
     if (with_delta) tmem_ld16(tdel + c0, d);
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        v[i] = (with_acc ? __uint_as_float(r[i]) : 0.f) + (with_delta ? __uint_as_float(d[i]) : 0.f);
+        v[i] = (with_acc ? __uint_as_float(r[i]) * wsc : 0.f) + (with_delta ? __uint_as_float(d[i]) : 0.f);
 }
 
 // Partial tiles (stream-K pieces) are kept in column quads: element (column c, lane o) at
@@ -1090,6 +1090,8 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool wi
         }
     };
     const bool o_ok = o0 + c.o < M.d_out;
+    // int4 base: the accumulator holds sum_k code[o, k] x[k]; the row's scale makes it W x
+    const float wsc = (c.p->w4 && o_ok) ? __ldg(c.p->mod[it.m].w_scale + o0 + c.o) : 1.f;
     // block c0 of y: into its slot of the current round; the round's stores go out when it is full
     auto emit = [&](int c0, const float (&v)[16]) {
         if (round_blocks == 0) {  // plain stores: lane o writes output o0 + o of 16 rows
@@ -1124,7 +1126,7 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool wi
         set_staging(0);
         for (int c0 = 0; c0 < ncols16; c0 += 16) {
             float v[16];
-            own_cols16(tacc, tdel, with_acc, with_delta, c0, v);
+            own_cols16(tacc, tdel, with_acc, with_delta, c0, wsc, v);
             emit(c0, v);
         }
         return;
@@ -1136,23 +1138,72 @@ __device__ void drain(EpiCtx &c, const Item &it, int buf, bool with_acc, bool wi
     float *dst = partials + ((size_t)blockIdx.x * 2 + ((b_c >= it.it0) ? 0 : 1)) * slot_elems;
     for (int c0 = 0; c0 < ncols16; c0 += 16) {
         float v[16];
-        own_cols16(tacc, tdel, with_acc, with_delta, c0, v);
+        own_cols16(tacc, tdel, with_acc, with_delta, c0, wsc, v);
         float4 *q = piece_quads(dst, c0, c.o);
 #pragma unroll
         for (int k = 0; k < 4; ++k) __stcg(q + k * kBM, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
     }
 }
 
+// ---- int4 base weights ------------------------------------------------------------------
+//
+// W is stored as 4-bit codes, two per byte, with one fp32 scale per output row ("12. Adapter
+// Serving and Multi-Tenant Customization", section "Quantization": an INT4 base with BF16
+// adapters, dequantised in the kernel, accumulated wide).  tcgen05's f16 kind takes bf16 on both sides, so the converter warps
+// turn every W k-block's codes into a bf16 tile of the integers themselves (exact: |code| <= 7)
+// between the TMA load and the MMA, and the drain multiplies the accumulator by the row's scale.
+//
+// Packing: a 32-bit word holds 8 consecutive k elements; nibble s (s = 0..3) of the low half is
+// element 2s and nibble s of the high half element 2s + 1, each stored as code + 8 (1..15).
+// (0x4300 | u) read as bf16 is 128 + u (u sits in the low mantissa bits), so one mask-or per pair
+// and one bf16x2 subtraction of 136 give a pair of codes.  A zero nibble (the TMA fill past d_in)
+// reads as -8 and meets x's zero fill there.
+__device__ __forceinline__ uint4 w4_bf16x8(uint32_t w) {
+    const __nv_bfloat162 off = __floats2bfloat162_rn(136.f, 136.f);
+    uint32_t r[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const uint32_t b = ((w >> (4 * s)) & 0x000F000Fu) | 0x43004300u;
+        const __nv_bfloat162 h = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&b), off);
+        r[s] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// One W k-block: the packed codes at `raw` ([128 rows][32 bytes], as TMA lays down the box) into
+// the bf16 tile at `dst` ([128 rows][64], 128-byte swizzle: the 16-byte chunk j of row r sits at
+// chunk j ^ (r % 8) of the row, as a TMA load with that swizzle would put it).  Thread ct of the
+// kConvWarps * 32 converter threads takes 16-byte pieces ct, ct + 64, ...: piece i is half i % 2 of
+// row i / 2, i.e. output chunks 4 (i % 2) .. 4 (i % 2) + 3.  A quarter warp reads 128 contiguous
+// bytes and writes eight different chunk columns of four rows: no bank conflicts.
+__device__ __forceinline__ void convert_w4_kblock(uint32_t raw, uint32_t dst, int ct) {
+#pragma unroll
+    for (int i = 0; i < (kBM * 2) / (kConvWarps * 32); ++i) {
+        const int idx = ct + i * kConvWarps * 32;
+        const int r = idx >> 1, h = idx & 1;
+        const uint4 w = lds_u128(raw + (uint32_t)idx * 16);
+        const uint32_t row = dst + (uint32_t)r * 128;
+        const uint32_t sw = (uint32_t)(r & 7);
+        sts_u128(row + (((uint32_t)(4 * h + 0) ^ sw) << 4), w4_bf16x8(w.x));
+        sts_u128(row + (((uint32_t)(4 * h + 1) ^ sw) << 4), w4_bf16x8(w.y));
+        sts_u128(row + (((uint32_t)(4 * h + 2) ^ sw) << 4), w4_bf16x8(w.z));
+        sts_u128(row + (((uint32_t)(4 * h + 3) ^ sw) << 4), w4_bf16x8(w.w));
+    }
+}
+
 // I8: the adapters' B factors are int8 codes (their scales are folded into t by the shrink).
-template <bool I8>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+// W4: the base weights are int4 codes with row scales (decode only); two more warps convert them.
+template <bool I8, bool W4>
+__global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.n_stages;
     const int NB = p.n_acc;
     const uint32_t a_bytes = kBM * kBK * 2;
     const uint32_t b_bytes = (uint32_t)p.nt * kBK * 2;
-    const uint32_t stage_bytes = a_bytes + b_bytes;
+    // W4: the stage also holds the k-block's packed codes after the x tile
+    const uint32_t stage_bytes = a_bytes + b_bytes + (W4 ? (uint32_t)kW4RawBytes : 0u);
+    const uint32_t w_tx = W4 ? (uint32_t)kW4RawBytes + b_bytes : a_bytes + b_bytes;  // bytes of one W fill
     uint8_t *ybuf = smem + (size_t)S * stage_bytes;  // epilogue y staging (may be empty)
     int32_t *perm_s = reinterpret_cast<int32_t *>(ybuf + p.ybuf_bytes);
     int32_t *npk = perm_s + LORA_MAX_DECODE_ROWS;  // [LORA_MAX_MODULES] packs per tile (decode)
@@ -1163,7 +1214,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     uint64_t *wfull = reinterpret_cast<uint64_t *>(npk + LORA_MAX_MODULES);
     uint64_t *bfull = wfull + S;
     uint64_t *empty = bfull + S;
-    uint64_t *acc_full = empty + S;
+    uint64_t *cfull = empty + S;  // W4: the slot's codes are converted (the MMA waits on this)
+    uint64_t *acc_full = cfull + (W4 ? S : 0);
     uint64_t *acc_free = acc_full + 2;
     uint64_t *mma_done = acc_free + 2;
     uint32_t *misc = reinterpret_cast<uint32_t *>(mma_done + 1);  // [0] tmem, [1] abort
@@ -1174,6 +1226,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             mbar_init(wfull + s, 1);
             mbar_init(bfull + s, 1);
             mbar_init(empty + s, 1);
+            if (W4) mbar_init(cfull + s, kConvWarps * 32);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
@@ -1235,12 +1288,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             note_fill(kk % S, false);
             if (lane == 0) {
                 uint8_t *sa = smem + (size_t)(kk % S) * stage_bytes;
-                mbar_arrive_expect_tx(wfull + kk % S, stage_bytes);
-                tma_load_2d(sa, &M.tmW, wfull + kk % S, kb * kBK, t.w_tile * kBM, pol_w);
+                mbar_arrive_expect_tx(wfull + kk % S, w_tx);
+                if (W4) tma_load_2d(sa + a_bytes + b_bytes, &M.tmW, wfull + kk % S, kb * (kBK / 2), t.w_tile * kBM, pol_w);
+                else tma_load_2d(sa, &M.tmW, wfull + kk % S, kb * kBK, t.w_tile * kBM, pol_w);
                 tma_load_2d(sa + a_bytes, &M.tmX, wfull + kk % S, kb * kBK, t.chunk * p.nt, pol_x);
             }
         };
-        if (I8 || p.stream_k) {  // int8 factors: decode only
+        if (I8 || W4 || p.stream_k) {  // int8 factors, int4 base: decode only
             // ---- decode: stream-K items, packs after their k-blocks
             while (ok && sc.next(p, npk, it)) {
                 const GemmModule &M = p.mod[it.m];
@@ -1275,7 +1329,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     }
                 }
             }
-        } else {
+        } else if constexpr (!W4) {
             // ---- grouped rows: whole tiles round robin, each tile's slots one per B stage: a
             // segment's rows in the chunk in runs of pf_ch (walked with sg / r)
             auto issue_b = [&](const Item &t, int &sg, int &r, uint32_t kk) {
@@ -1380,7 +1434,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             // one W k-block at stage k into accumulator column d
             auto mma_stage = [&](uint32_t d, bool accumulate) -> bool {
                 const int s = k % S;
-                if (!mbar_wait(wfull + s, (wpar >> s) & 1u, abort_flag, p.err)) return false;
+                if (!mbar_wait((W4 ? cfull : wfull) + s, (wpar >> s) & 1u, abort_flag, p.err)) return false;
                 wpar ^= 1u << s;
                 tc_fence_after();
                 const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
@@ -1392,7 +1446,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 umma_commit(empty + s);
                 return true;
             };
-            if (I8 || p.stream_k) {  // int8 factors: decode only
+            if (I8 || W4 || p.stream_k) {  // int8 factors, int4 base: decode only
                 Sched sc;
                 sc.begin(p, blockIdx.x);
                 Item it;
@@ -1416,7 +1470,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     if (buf) ++use1; else ++use0;
                     ++li;
                 }
-            } else {
+            } else if constexpr (!W4) {
                 // grouped rows: the epilogue writes each tile's expand into the accumulator first
                 // and then arrives on acc_free, so every k-block accumulates on top of it
                 Item cur, nxt;
@@ -1450,6 +1504,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             const uint32_t a = smem_u32(mma_done);
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(a, 0) && globaltimer() - t0 < kWaitBudgetNs) {
+            }
+        }
+    } else if (W4 && warp >= 2 + kEpiWarps) {
+        // ---------------------------------------------------------------- int4 converters
+        // walk the same fills as the MMA warp: every W k-block, skipping the B stages after it
+        const int ct = threadIdx.x - (64 + 32 * kEpiWarps);
+        Sched sc;
+        sc.begin(p, blockIdx.x);
+        Item it;
+        uint32_t k = 0, wpar = 0;
+        bool ok = true;
+        while (ok && sc.next(p, npk, it)) {
+            Mix mx;
+            mx.begin(it);
+            for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                const int s = k % S;
+                if (!mbar_wait(wfull + s, (wpar >> s) & 1u, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                wpar ^= 1u << s;
+                uint8_t *sa = smem + (size_t)s * stage_bytes;
+                convert_w4_kblock(smem_u32(sa + a_bytes + b_bytes), smem_u32(sa), ct);
+                fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
+                mbar_arrive(cfull + s);
+                k += 1 + (uint32_t)mx.after_w();
             }
         }
     } else {
@@ -1491,7 +1571,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         float z[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[i] = 0.f;
-        if (I8 || p.stream_k) {  // int8 factors: decode only
+        if (I8 || W4 || p.stream_k) {  // int8 factors, int4 base: decode only
             Sched sc;
             sc.begin(p, blockIdx.x);
             Item cur;
@@ -1544,7 +1624,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 has_cur = sc.next(p, npk, cur);
                 ++li;
             }
-        } else {
+        } else if constexpr (!W4) {
             // ---- grouped rows: the expand of tile j+1 is written into its accumulator (zeros +
             // delta) while tile j is multiplied, then acc_free tells the MMA warp to start on it.
             // A B stage is copied into the y buffer first, so its ring slot is given back at once.
@@ -1678,10 +1758,10 @@ __global__ void __launch_bounds__(kBM) finalize_kernel(const __grid_constant__ G
 
 // ====================================================================== launchers ==========
 
-size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes) {
-    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2;
+size_t gemm_smem_bytes(int nt, int n_stages, int ybuf_bytes, bool w4) {
+    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2 + (w4 ? kW4RawBytes : 0);
     return 1024 + stage * n_stages + (size_t)ybuf_bytes + 4 * LORA_MAX_DECODE_ROWS + 4 * LORA_MAX_MODULES +
-           8 * (3 * (size_t)n_stages + 5) + 16;
+           8 * ((w4 ? 4 : 3) * (size_t)n_stages + 5) + 16;
 }
 
 bool plan_gemm(GemmParams &gp, size_t *smem_bytes) {
@@ -1696,10 +1776,11 @@ bool plan_gemm(GemmParams &gp, size_t *smem_bytes) {
     // or store it plainly, which buys one more stage; grouped rows drain every tile while the next
     // one streams, so they keep a dedicated buffer
     gp.ybuf_bytes = gp.stream_k ? 0 : kYBufBytes;
-    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)gp.nt * kBK * 2;
-    const size_t fixed = gemm_smem_bytes(gp.nt, 0, gp.ybuf_bytes);
-    gp.n_stages = (int)std::min<size_t>(kMaxStages, (227 * 1024 - fixed - 24 * kMaxStages) / stage);
-    *smem_bytes = gemm_smem_bytes(gp.nt, gp.n_stages, gp.ybuf_bytes);
+    const bool w4 = gp.w4 != 0;
+    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)gp.nt * kBK * 2 + (w4 ? kW4RawBytes : 0);
+    const size_t fixed = gemm_smem_bytes(gp.nt, 0, gp.ybuf_bytes, w4);
+    gp.n_stages = (int)std::min<size_t>(kMaxStages, (227 * 1024 - fixed - (w4 ? 32 : 24) * kMaxStages) / stage);
+    *smem_bytes = gemm_smem_bytes(gp.nt, gp.n_stages, gp.ybuf_bytes, w4);
     return gp.n_stages >= 2;
 }
 
@@ -1738,15 +1819,17 @@ cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStr
 }
 
 cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s) {
-    static size_t configured[2] = {0, 0};
-    const int v = p.i8 ? 1 : 0;
-    auto kernel = p.i8 ? gemm_kernel<true> : gemm_kernel<false>;
+    static size_t configured[4] = {0, 0, 0, 0};
+    const int v = (p.i8 ? 1 : 0) + (p.w4 ? 2 : 0);
+    void (*const kernels[4])(GemmParams) = {gemm_kernel<false, false>, gemm_kernel<true, false>,
+                                            gemm_kernel<false, true>, gemm_kernel<true, true>};
+    auto kernel = kernels[v];
     if (smem_bytes > configured[v]) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
         if (e != cudaSuccess) return e;
         configured[v] = smem_bytes;
     }
-    return launch_pdl(kernel, dim3(p.n_cta), dim3(kGemmThreads), smem_bytes, s, p);
+    return launch_pdl(kernel, dim3(p.n_cta), dim3(p.w4 ? kGemmThreadsW4 : kGemmThreads), smem_bytes, s, p);
 }
 
 cudaError_t launch_finalize(const GemmParams &p, cudaStream_t s) {

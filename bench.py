@@ -60,23 +60,29 @@ WORKLOADS = {"attn70b": (wl.attn70b_decode, "decode"), "all70b": (wl.all70b_deco
              # the prefill path at a size a profiler capture can replay (8 requests, ~8.7k tokens)
              "prefill_small": (lambda: wl.prefill_segments(n_req=8), "prefill"),
              # the same decode batches with int8 adapter factors (codes + per-rank-row scales)
-             "attn70b_i8": (wl.attn70b_decode, "decode"), "all70b_i8": (wl.all70b_decode, "decode")}
+             "attn70b_i8": (wl.attn70b_decode, "decode"), "all70b_i8": (wl.all70b_decode, "decode"),
+             # the same decode batches with an int4 base (codes + one fp32 scale per output row)
+             "attn70b_w4": (wl.attn70b_decode, "decode"), "all70b_w4": (wl.all70b_decode, "decode")}
 INT8 = {"attn70b_i8", "all70b_i8"}
+W4 = {"attn70b_w4", "all70b_w4"}
 
 
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
-def algorithmic_bytes(w, int8=False):
-    """Algorithmic bytes of one step: W once, each distinct adapter's factors once (int8: one byte
-    per code plus the fp32 scale of each rank row, counted with A), x once per stage, y written
-    once (fp32)."""
+def algorithmic_bytes(w, int8=False, w4=False):
+    """Algorithmic bytes of one step: W once (int4 base: half a byte per weight plus one fp32
+    scale per output row), each distinct adapter's factors once (int8: one byte per code plus the
+    fp32 scale of each rank row, counted with A), x once per stage, y written once (fp32)."""
     ids = w.row_adapters()
     distinct = sorted(set(int(a) for a in ids if a >= 0))
     mods = w.module_names()
     e = 1 if int8 else 2
-    W = sum(w.modules[m][0] * w.modules[m][1] * 2 for m in mods)
+    if w4:
+        W = sum(w.modules[m][0] * w.modules[m][1] // 2 + 4 * w.modules[m][1] for m in mods)
+    else:
+        W = sum(w.modules[m][0] * w.modules[m][1] * 2 for m in mods)
     A = sum(int(w.ranks[a]) * (w.modules[m][0] * e + (4 if int8 else 0)) for a in distinct for m in mods)
     B = sum(int(w.ranks[a]) * w.modules[m][1] * e for a in distinct for m in mods)
     X = sum(w.n_rows * w.modules[st[0]][0] * 2 for st in w.stages)
@@ -253,7 +259,13 @@ def run_ours(args, w):
                 pool.load(int(a), mi, torch.from_numpy(A).view(torch.bfloat16), torch.from_numpy(B).view(torch.bfloat16))
     bf = lambda b: torch.from_numpy(b).view(torch.bfloat16).to(dev)
     xd = [bf(x) for x in xs]
-    Wd = {m: bf(Ws[m]) for m in names}
+    w4 = args.workload in W4
+    if w4:  # the library's quantizer: int4 codes, one fp32 scale per output row
+        Wq = {m: L.quantize_w4(Ws[m]) for m in names}
+        Wd = {m: (torch.from_numpy(Wq[m][0]).to(dev), torch.from_numpy(Wq[m][1]).to(dev)) for m in names}
+        del Wq
+    else:
+        Wd = {m: bf(Ws[m]) for m in names}
     yd = {m: torch.empty(w.n_rows, w.modules[m][1], device=dev) for m in names}
     grouped = w.ids is None
     if grouped:  # prefill: contiguous request segments; the base-only run gives every segment -1
@@ -262,8 +274,12 @@ def run_ours(args, w):
     else:
         ids = torch.from_numpy(w.ids).to(dev)
     ids_base = torch.full_like(ids, -1)
-    stage_io = [[(names.index(m), xd[st], Wd[m], yd[m]) for m in mods] for st, mods in enumerate(w.stages)]
+    def io_of(m, x, y):
+        return (names.index(m), x, *Wd[m], y) if w4 else (names.index(m), x, Wd[m], y)
+
+    stage_io = [[io_of(m, xd[st], yd[m]) for m in mods] for st, mods in enumerate(w.stages)]
     stream = torch.cuda.current_stream()
+    forward_planned = pool.layer_forward_planned_w4 if w4 else pool.layer_forward_planned
 
     def step(id_t):
         if not grouped:  # decode: one row grouping per batch serves every call of the step
@@ -272,7 +288,7 @@ def run_ours(args, w):
             if grouped:
                 pool.segment_forward(io, ss_d, id_t, w.n_rows, w.scale, stream=stream)
             else:
-                pool.layer_forward_planned(io, w.scale, stream=stream)
+                forward_planned(io, w.scale, stream=stream)
 
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -318,14 +334,17 @@ def run_ours(args, w):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    ab = algorithmic_bytes(w, int8)
+    ab = algorithmic_bytes(w, int8, w4)
     value = world * w.n_rows / (ms / 1e3)
     ranks = sorted(set(int(w.ranks[a]) for a in w.used_adapters()))
     line = {"metric": METRIC if args.workload == "attn70b" else f"{args.workload}: tokens/s", "value": value,
             "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16, int8 adapter factors" if int8 else "bf16", "data": "synthetic",
-            "config": {"workload": w.name + ("_int8_factors" if int8 else ""), "batch_rows": w.n_rows, "distinct_adapters": ab["distinct"],
+            "vs_baseline": None,
+            "dtype": "bf16, int8 adapter factors" if int8 else ("bf16, int4 base weights" if w4 else "bf16"),
+            "data": "synthetic",
+            "config": {"workload": w.name + ("_int8_factors" if int8 else "") + ("_int4_base" if w4 else ""),
+                       "batch_rows": w.n_rows, "distinct_adapters": ab["distinct"],
                        "ranks": ranks,
                        "projections": ", ".join(f"{m} {w.modules[m][0]}->{w.modules[m][1]}" for m in names),
                        "calls_per_step": len(w.stages), "output": "fp32",
@@ -386,7 +405,7 @@ def run_ours(args, w):
         for b in range(2):
             xb = [torch.empty_like(x) for x in xd]
             yb = {m: torch.empty_like(yd[m]) for m in names}
-            io_b = [[(names.index(m), xb[st], Wd[m], yb[m]) for m in mods] for st, mods in enumerate(w.stages)]
+            io_b = [[io_of(m, xb[st], yb[m]) for m in mods] for st, mods in enumerate(w.stages)]
             dbuf.append({"ids": torch.empty_like(ids), "x": xb, "y": yb, "io": io_b})
         hyb = [{m: torch.empty(w.n_rows, w.modules[m][1], dtype=torch.float32).pin_memory() for m in names}
                for _ in range(2)]
@@ -414,7 +433,7 @@ def run_ours(args, w):
                     stream.wait_event(outputs_free[b])
                 pool.plan_rows(B["ids"], stream=stream)
                 for st, io in enumerate(B["io"]):
-                    pool.layer_forward_planned(io, w.scale, stream=stream)
+                    forward_planned(io, w.scale, stream=stream)
                     done = torch.cuda.Event()
                     done.record(stream)
                     with torch.cuda.stream(down):  # this call's outputs
@@ -441,7 +460,9 @@ def run_ours(args, w):
         line["e2e"] = {"value": world * w.n_rows / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                        "timing": "steps back to back, host I/O of neighbouring steps overlapped; no L2 flush "
-                                 "(302 MB of W per step > 129 MB L2)"}
+                                 f"({ab['W'] / 1e6:.0f} MB of W per step"
+                                 + (" > 129 MB L2)" if ab["W"] > 129e6 else
+                                    ", less than the 129 MB L2: part of W may still be in L2 from the step before)")}
         code, detail = pool.last_device_error()
         if code:
             raise RuntimeError(f"device error {L.DEVERR.get(code)} at {detail}")

@@ -353,6 +353,46 @@ int lora_layer_forward_planned(lora_pool *pool, int32_t n_io, const lora_module_
                                int32_t y_dtype, lora_stream_t stream);
 
 /*
+ * int4 base weights with bf16 (or int8) adapters ("12. Adapter Serving ...", section
+ * "Quantization": the base quantized to INT4 while the adapters stay BF16; the kernel dequantizes
+ * the base, adds the adapter term and accumulates wide, and one batch mixes adapted and base-only
+ * rows).  W is symmetric int4 with one fp32 scale per output row:
+ *     W[o, k] = scale[o] * code[o, k],   code in [-7, 7],   scale[o] = max_k |W[o, k]| / 7
+ * and the forward computes y_i = scale * (code x_i) + s B_a A_a x_i with fp32 accumulation (the
+ * codes enter the tensor-core product as exact bf16 integers; the row scale multiplies the
+ * accumulator).
+ *
+ * lora_quantize_w4 -- host quantizer.  src: host bf16 [rows, cols] (cols a multiple of 8); writes
+ * packed [rows, cols / 2] bytes and scales [rows].  code = round-half-even(v / scale) in fp32,
+ * clipped to [-7, 7]; a zero row gets scale 0 and codes 0.  Packed layout: every 8 consecutive
+ * elements e0..e7 of a row form one little-endian 32-bit word; element 2s (s = 0..3) is stored at
+ * bits [4s, 4s + 4) and element 2s + 1 at bits [16 + 4s, 20 + 4s), each as code + 8 (1..15).
+ * Errors: EINVAL.
+ */
+int lora_quantize_w4(const void *src, int64_t rows, int64_t cols, uint8_t *packed, float *scales);
+
+/* One projection of an int4-base call. */
+typedef struct {
+    int32_t module;       /* pool module index */
+    const void *x;        /* device bf16 [n, d_in] */
+    const void *W_codes;  /* device [d_out, d_in / 2] bytes, lora_quantize_w4's layout; 16-byte aligned */
+    const float *W_scale; /* device fp32 [d_out] */
+    void *y;              /* device [n, d_out], fp32 or bf16 */
+} lora_module_io_w4;
+
+/*
+ * lora_layer_forward_w4 / lora_layer_forward_planned_w4 -- lora_layer_forward and
+ * lora_layer_forward_planned with int4 base weights.  Decode batches only (n <= 256); the module's
+ * d_in must be a multiple of 32.  The pool's factors may be bf16 or int8.  Same row ids, error
+ * word and errors as the bf16 calls (EUNSUPPORTED also for d_in % 32 != 0).
+ */
+int lora_layer_forward_w4(lora_pool *pool, int32_t n_io, const lora_module_io_w4 *io,
+                          const int32_t *row_adapter_ids, int32_t n, float scale, int32_t y_dtype,
+                          lora_stream_t stream);
+int lora_layer_forward_planned_w4(lora_pool *pool, int32_t n_io, const lora_module_io_w4 *io, float scale,
+                                  int32_t y_dtype, lora_stream_t stream);
+
+/*
  * lora_pool_last_segments -- synchronize the device and copy out the row grouping the most
  * recent forward on this pool used (computed on the device for lora_layer_forward; the
  * checked copy of the given table for lora_segment_forward).  Host outputs:
