@@ -375,7 +375,7 @@ def run_ours(args, w):
                             "bound": "hbm",
                             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                             "peak_source": src,
-                            "traffic": GEMM_DRAM_BYTES_PER_LAUNCH if args.workload == "attn70b" else None,
+                            "traffic": GEMM_DRAM_BYTES_PER_LAUNCH.get(args.workload),
                             "algorithmic_bytes_per_step": ab["gemm"], "launches_per_step": g_launch / args.steps}
         line["kernel_ms_per_step"] = {k: v[1] / args.steps for k, v in kt.items()}
         s_ms = kt["shrink"][1] / args.steps
@@ -484,11 +484,11 @@ def _build():
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per gemm launch, mean of the qkv and
-# o launches of this workload, from an ncu capture of the current gemm kernel; None whenever the
-# kernel has changed since the last capture.  The stream-K finish (finalize_kernel) is timed with
+# o launches of the workload, from an ncu capture of the current gemm kernel (bf16 base and int4
+# base); absent whenever the kernel has changed since the last capture.  The stream-K finish (finalize_kernel) is timed with
 # the gemm but its pieces are L2-resident in the live step, so its DRAM bytes are not added (under
 # ncu's cache control it re-reads them from DRAM).
-GEMM_DRAM_BYTES_PER_LAUNCH = 176_533_632
+GEMM_DRAM_BYTES_PER_LAUNCH = {"attn70b": 176_681_344, "attn70b_w4": 59_931_136}
 
 
 def main():
