@@ -1198,6 +1198,12 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.n_stages;
+    // Ring slot and round of fill k without an integer division in the loops (a runtime divide
+    // is tens of dependent instructions, and the producer issues one fill per few hundred
+    // cycles): k / S = umulhi(k, ceil(2^32 / S)), exact for k < 2^32 / 8 when S <= 8.
+    const uint32_t ring_m = 0xFFFFFFFFu / (uint32_t)S + 1u;
+    auto rround = [ring_m](uint32_t kk) -> uint32_t { return __umulhi(kk, ring_m); };
+    auto rslot = [ring_m, S](uint32_t kk) -> uint32_t { return kk - __umulhi(kk, ring_m) * (uint32_t)S; };
     const int NB = p.n_acc;
     const uint32_t a_bytes = kBM * kBK * 2;
     const uint32_t b_bytes = (uint32_t)p.nt * kBK * 2;
@@ -1279,19 +1285,20 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
         // one stage slot: wait until it is free (lane 0), the answer goes to the whole warp
         auto acquire = [&](uint32_t kk) -> bool {
             int got = 1;
-            if (lane == 0) got = mbar_wait(empty + kk % S, ((kk / S) & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
+            if (lane == 0) got = mbar_wait(empty + rslot(kk), (rround(kk) & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
             return __shfl_sync(0xffffffffu, got, 0) != 0;
         };
         // one W k-block of item t into stage kk
         auto issue_w = [&](const Item &t, int kb, uint32_t kk) {
             const GemmModule &M = p.mod[t.m];
-            note_fill(kk % S, false);
+            const uint32_t sl = rslot(kk);
+            note_fill((int)sl, false);
             if (lane == 0) {
-                uint8_t *sa = smem + (size_t)(kk % S) * stage_bytes;
-                mbar_arrive_expect_tx(wfull + kk % S, w_tx);
-                if (W4) tma_load_2d(sa + a_bytes + b_bytes, &M.tmW, wfull + kk % S, kb * (kBK / 2), t.w_tile * kBM, pol_w);
-                else tma_load_2d(sa, &M.tmW, wfull + kk % S, kb * kBK, t.w_tile * kBM, pol_w);
-                tma_load_2d(sa + a_bytes, &M.tmX, wfull + kk % S, kb * kBK, t.chunk * p.nt, pol_x);
+                uint8_t *sa = smem + (size_t)sl * stage_bytes;
+                mbar_arrive_expect_tx(wfull + sl, w_tx);
+                if (W4) tma_load_2d(sa + a_bytes + b_bytes, &M.tmW, wfull + sl, kb * (kBK / 2), t.w_tile * kBM, pol_w);
+                else tma_load_2d(sa, &M.tmW, wfull + sl, kb * kBK, t.w_tile * kBM, pol_w);
+                tma_load_2d(sa + a_bytes, &M.tmX, wfull + sl, kb * kBK, t.chunk * p.nt, pol_x);
             }
         };
         if (I8 || W4 || p.stream_k) {  // int8 factors, int4 base: decode only
@@ -1320,12 +1327,13 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
                             ok = false;
                             break;
                         }
-                        uint8_t *sa = smem + (size_t)(k % S) * stage_bytes;
-                        note_fill(k % S, true);
+                        const uint32_t sl = rslot(k);
+                        uint8_t *sa = smem + (size_t)sl * stage_bytes;
+                        note_fill((int)sl, true);
                         const uint4 cur = rec;
                         if (jb + 1 < b1 && lane <= kPackSlots)
                             rec = __ldcg(reinterpret_cast<const uint4 *>(M.packs + jb + 1) + lane);
-                        produce_pack(cur, M, o0, orows, p.pack_ch, sa, sa + a_bytes, bfull + k % S, lane, I8 ? 1 : 2);
+                        produce_pack(cur, M, o0, orows, p.pack_ch, sa, sa + a_bytes, bfull + sl, lane, I8 ? 1 : 2);
                     }
                 }
             }
@@ -1337,10 +1345,11 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
                 const int o0 = t.w_tile * kBM, row0 = t.chunk * p.nt;
                 const int orows = min(kBM, M.d_out - o0);
                 const int row1 = min(p.n, row0 + p.nt);
-                uint8_t *sa = smem + (size_t)(kk % S) * stage_bytes;
+                const uint32_t ring_s = rslot(kk);
+                uint8_t *sa = smem + (size_t)ring_s * stage_bytes;
                 uint8_t *sx = sa + a_bytes;
-                uint64_t *bar = bfull + kk % S;
-                note_fill(kk % S, true);
+                uint64_t *bar = bfull + ring_s;
+                note_fill((int)ring_s, true);
                 if (lane != 0) return;
                 const int ns = *p.n_seg;
                 int s1 = 0, a = -1;
@@ -1433,7 +1442,7 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
             bool ok = true;
             // one W k-block at stage k into accumulator column d
             auto mma_stage = [&](uint32_t d, bool accumulate) -> bool {
-                const int s = k % S;
+                const int s = (int)rslot(k);
                 if (!mbar_wait((W4 ? cfull : wfull) + s, (wpar >> s) & 1u, abort_flag, p.err)) return false;
                 wpar ^= 1u << s;
                 tc_fence_after();
@@ -1519,7 +1528,7 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
             Mix mx;
             mx.begin(it);
             for (int kb = it.kb0; kb < it.kb1; ++kb) {
-                const int s = k % S;
+                const int s = (int)rslot(k);
                 if (!mbar_wait(wfull + s, (wpar >> s) & 1u, abort_flag, p.err)) {
                     ok = false;
                     break;
@@ -1563,7 +1572,7 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
         uint32_t bpar = 0;
         // wait for the B stage at ring slot kk (all 128 threads); false if the wait gave up
         auto wait_b = [&](uint32_t kk) -> bool {
-            const int s = kk % S;
+            const int s = (int)rslot(kk);
             const bool ok = !named_bar_or(1, 128, !mbar_wait(bfull + s, (bpar >> s) & 1u, abort_flag, p.err));
             if (ok) bpar ^= 1u << s;
             return ok;
@@ -1598,7 +1607,7 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
                         ++k;  // the W k-block goes to the MMA warp
                         const int nb = mx.after_w();
                         for (int q = 0; q < nb; ++q, ++k) {
-                            const int s = k % S;
+                            const int s = (int)rslot(k);
                             ok = wait_b(k);
                             if (!ok) break;
                             const uint8_t *sa = smem + (size_t)s * stage_bytes;
@@ -1637,7 +1646,7 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
                 for (int q = 0; q < t.nbs; ++q) {
                     const uint32_t kk = k0 + (uint32_t)q;
                     if (!wait_b(kk)) return false;
-                    const uint8_t *sa = smem + (size_t)(kk % S) * stage_bytes;
+                    const uint8_t *sa = smem + (size_t)rslot(kk) * stage_bytes;
                     const uint8_t *sx = sa + a_bytes;
                     const BStageHdr *hdr = reinterpret_cast<const BStageHdr *>(sx);
                     // the slot's B rows ([128][rp], rank offset 0), then header and t rows
@@ -1650,7 +1659,7 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
                     for (uint32_t off = (uint32_t)c.etid * 16; off < kStageHdrBytes + tbytes; off += 128 * 16)
                         *reinterpret_cast<uint4 *>(ybuf + bbytes + off) = *reinterpret_cast<const uint4 *>(sx + off);
                     named_bar_sync(1, 128);  // the copy is complete: the slot goes back
-                    if (c.etid == 0) mbar_arrive(empty + kk % S);
+                    if (c.etid == 0) mbar_arrive(empty + rslot(kk));
                     expand_stage<I8>(c, ybuf, ybuf + bbytes, tacc, row0);
                     named_bar_sync(1, 128);  // before the buffer is overwritten
                 }
