@@ -55,7 +55,7 @@ typedef struct CUstream_st *lora_stream_t; /* == cudaStream_t */
 #define LORA_ENOTLOADED (-2)   /* adapter (or a module of it) is not resident */
 #define LORA_ENOMEM (-3)       /* no free pages in the pool, or a device allocation failed */
 #define LORA_ECUDA (-5)        /* a CUDA runtime call failed (see lora_last_cuda_error) */
-#define LORA_EUNSUPPORTED (-6) /* valid request this build does not handle (see each call) */
+#define LORA_EUNSUPPORTED (-6) /* valid request the library does not handle (see each call) */
 #define LORA_EDEVICE (-7)      /* a kernel recorded an error (see lora_last_device_error) */
 #define LORA_EPINNED (-8)      /* the adapter cache's pinning guard refuses a new adapter */
 
