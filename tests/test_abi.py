@@ -72,6 +72,10 @@ def test_host_argument_checks_without_gpu():
     assert L.lib.lora_pool_create(None, None) == L.EINVAL
     assert L.lib.lora_build_segments(None, -1, None, None, None, None) == L.EINVAL
     assert L.lib.lora_layer_forward(None, 1, None, None, 4, ctypes.c_float(1.0), 0, None) == L.EINVAL
+    assert L.lib.lora_layer_forward_w4(None, 1, None, None, 4, ctypes.c_float(1.0), 0, None) == L.EINVAL
+    assert L.lib.lora_layer_forward_planned_w4(None, 1, None, ctypes.c_float(1.0), 0, None) == L.EINVAL
+    assert L.lib.lora_layer_forward_planned(None, 0, None, ctypes.c_float(1.0), 0, None) == L.EINVAL
+    assert L.lib.lora_quantize_w4(None, 1, 8, None, None) == L.EINVAL
     assert L.lib.lora_pool_destroy(None) == L.EINVAL
     d_in = (ctypes.c_int32 * 1)(1000)
     d_out = (ctypes.c_int32 * 1)(1001)  # not a multiple of 8
@@ -88,3 +92,17 @@ def test_pool_create_fails_cleanly_without_gpu():
     with pytest.raises(L.LoraError) as e:
         L.Pool([1024], [1024], 4)
     assert e.value.status == L.ECUDA
+
+
+def test_ring_slot_without_division():
+    """The gemm's TMA ring finds fill k's slot and round as k - umulhi(k, ceil(2^32 / S)) * S and
+    umulhi(k, ceil(2^32 / S)) for S <= 8 stages: exact for every k below 2^32 / 8 (checked here on
+    a dense range and at the top of that range)."""
+    for S in range(2, 9):
+        m = 0xFFFFFFFF // S + 1
+        k = np.arange(0, 1 << 20, dtype=np.uint64)
+        q = (k * np.uint64(m)) >> np.uint64(32)
+        assert np.array_equal(q, k // np.uint64(S))
+        assert np.array_equal(k - q * np.uint64(S), k % np.uint64(S))
+        top = np.arange((1 << 29) - (1 << 16), 1 << 29, dtype=np.uint64)
+        assert np.array_equal((top * np.uint64(m)) >> np.uint64(32), top // np.uint64(S))
