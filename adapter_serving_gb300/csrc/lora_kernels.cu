@@ -1282,14 +1282,10 @@ __global__ void __launch_bounds__(W4 ? kGemmThreadsW4 : kGemmThreads, 1) gemm_ke
             filled |= bit;
             return par;
         };
-        // one stage slot: wait until it is free.  Usually it already is: every lane tests the barrier
-        // and one vote decides, with no divergent branch; otherwise lane 0 waits and its answer
-        // goes to the whole warp.
+        // one stage slot: wait until it is free (lane 0), the answer goes to the whole warp
         auto acquire = [&](uint32_t kk) -> bool {
-            const uint32_t sl = rslot(kk), par = (rround(kk) & 1u) ^ 1u;
-            if (__all_sync(0xffffffffu, mbar_try_wait(smem_u32(empty + sl), par))) return true;
             int got = 1;
-            if (lane == 0) got = mbar_wait(empty + sl, par, abort_flag, p.err) ? 1 : 0;
+            if (lane == 0) got = mbar_wait(empty + rslot(kk), (rround(kk) & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
             return __shfl_sync(0xffffffffu, got, 0) != 0;
         };
         // one W k-block of item t into stage kk
