@@ -1,0 +1,175 @@
+"""Planted mistakes: the oracle's pins must catch a plausible error anywhere in it.
+
+Each mutant is a plain fp64 restatement of an oracle function with one mistake planted in it (a
+dropped term, a wrong sign, a wrong index, a transposed operand, a wrong rounding or scale).  The
+test swaps it in for the oracle function, runs that function's pins, and requires at least one
+pin to fail.  The same restatement with no mistake passes every pin, so a failure comes from the
+planted mistake alone.  Everything here runs on the CPU; the GPU library is never involved.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import test_int4_base as Q
+import test_oracle_pins as P
+import workloads as wl
+
+
+def _f64(b):
+    return wl.bf16_bits_to_f32(np.asarray(b, np.uint16)).astype(np.float64)
+
+
+def _forward(x, W, ids, A, B, scale, rows=None, threads=0, return_t=False, bug=None):
+    """y_i = W x_i + s B_a (A_a x_i), row by row in fp64, with an optional planted mistake."""
+    xf, Wf = _f64(x), _f64(W)
+    if bug == "W_transposed_read":
+        Wf = Wf.reshape(Wf.shape[1], Wf.shape[0]).T
+    ids = np.asarray(ids, np.int32)
+    n_ad = len(A)
+    if np.any(ids < -1) or np.any(ids >= n_ad):
+        raise ValueError("adapter id out of range")
+    rows = np.arange(len(ids)) if rows is None else np.asarray(rows)
+    rmax = max([a.shape[0] for a in A if a is not None] + [1])
+    y = np.zeros((len(rows), Wf.shape[0]))
+    t_all = np.zeros((len(rows), rmax))
+    for k, i in enumerate(rows):
+        a = int(ids[i])
+        if bug == "base_skipped_for_adapted_rows" and a >= 0:
+            base = np.zeros(Wf.shape[0])
+        else:
+            base = Wf @ xf[i]
+        y[k] = base
+        if a < 0:
+            continue
+        if bug == "wrong_adapter":
+            a = (a + 1) % n_ad
+        Af, Bf = _f64(A[a]), _f64(B[a])
+        if bug == "B_transposed_read":
+            Bf = Bf.reshape(Bf.shape[1], Bf.shape[0]).T
+        if bug == "rank_truncated" and Af.shape[0] > 1:
+            Af, Bf = Af[:-1], Bf[:, :-1]
+        xi = xf[(i + 1) % len(ids)] if bug == "x_of_next_row_in_shrink" else xf[i]
+        t = Af @ xi
+        t_all[k, :len(t)] = t
+        if bug == "adapter_dropped":
+            continue
+        s = {"no_scale": 1.0, "minus_adapter": -scale}.get(bug, scale)
+        y[k] += s * (Bf @ t)
+    return (y, t_all) if return_t else y
+
+
+FORWARD_PINS = [P.test_hand_worked_example, P.test_bruteforce_exact_rationals, P.test_b_zero_is_base_layer,
+                P.test_one_adapter_equals_merged_weight, P.test_mixed_rows_match_their_merged_weight,
+                P.test_shrink_matches_matmul, P.test_base_only_rows, P.test_zero_padding_rank_changes_nothing,
+                P.test_row_permutation, P.test_adapter_is_sum_of_rank_one_pieces, P.test_linear_in_scale,
+                P.test_invalid_ids_rejected]
+FORWARD_BUGS = ["adapter_dropped", "minus_adapter", "no_scale", "wrong_adapter", "B_transposed_read",
+                "W_transposed_read", "rank_truncated", "x_of_next_row_in_shrink", "base_skipped_for_adapted_rows"]
+
+
+def _failing_pins(pins):
+    failed = []
+    for pin in pins:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    return failed
+
+
+def test_forward_restatement_passes_every_pin(monkeypatch):
+    monkeypatch.setattr(oracle, "adapted_linear", lambda *a, **k: _forward(*a, **k))
+    assert _failing_pins(FORWARD_PINS) == []
+
+
+@pytest.mark.parametrize("bug", FORWARD_BUGS)
+def test_forward_pins_catch_planted_mistake(monkeypatch, bug):
+    monkeypatch.setattr(oracle, "adapted_linear", lambda *a, **k: _forward(*a, bug=bug, **k))
+    assert _failing_pins(FORWARD_PINS), f"no pin caught {bug}"
+
+
+# ---------------------------------------------------------------------------- int4 base ---
+
+def _quantize4(bits, bug=None):
+    v = wl.bf16_bits_to_f32(np.asarray(bits, np.uint16))
+    levels = 8.0 if bug == "scale_over_8" else 7.0
+    scale = (np.abs(v).max(axis=1) / np.float32(levels)).astype(np.float32)
+    codes = np.zeros(v.shape, np.int8)
+    nz = scale > 0
+    q = v[nz] / scale[nz, None]
+    if bug == "truncate":
+        q = np.trunc(q)
+    elif bug == "half_away_from_zero":
+        q = np.sign(q) * np.floor(np.abs(q) + np.float32(0.5))
+    else:
+        q = np.rint(q)
+    codes[nz] = np.clip(q, -7, 7).astype(np.int8)
+    return codes, scale
+
+
+def _nearest_code_seed0():
+    Q.test_oracle_quantizer_rounds_to_the_nearest_code(0)
+
+
+def _nearest_code_seed1():
+    Q.test_oracle_quantizer_rounds_to_the_nearest_code(1)
+
+
+QUANT_PINS = [_nearest_code_seed0, _nearest_code_seed1, Q.test_oracle_quantizer_half_even_and_signs,
+              Q.test_power_of_two_base_round_trips]
+
+
+def test_int4_quantizer_restatement_passes_every_pin(monkeypatch):
+    monkeypatch.setattr(oracle, "quantize_rows_int4", lambda b: _quantize4(b))
+    assert _failing_pins(QUANT_PINS) == []
+
+
+@pytest.mark.parametrize("bug", ["scale_over_8", "truncate", "half_away_from_zero"])
+def test_int4_quantizer_pins_catch_planted_mistake(monkeypatch, bug):
+    monkeypatch.setattr(oracle, "quantize_rows_int4", lambda b: _quantize4(b, bug))
+    assert _failing_pins(QUANT_PINS), f"no pin caught {bug}"
+
+
+def _forward_w4(x, codes, wscale, ids, A64, B64, scale, rows=None, bug=None):
+    xf = _f64(x)
+    c = np.asarray(codes, np.float64)
+    sc = np.asarray(wscale, np.float64)
+    if bug == "row_scale_skipped":
+        W = c
+    elif bug == "scale_by_column":  # the row scales read along k (cycled when d_in > d_out)
+        W = c * np.resize(sc, c.shape[1])[None, :]
+    elif bug == "codes_left_offset":
+        W = (c + 8) * sc[:, None]
+    else:
+        W = c * sc[:, None]
+    ids = np.asarray(ids, np.int32)
+    rows = np.arange(len(ids)) if rows is None else np.asarray(rows)
+    y = np.zeros((len(rows), W.shape[0]))
+    for k, i in enumerate(rows):
+        y[k] = W @ xf[i]
+        a = int(ids[i])
+        if a >= 0 and bug != "adapter_dropped":
+            y[k] += scale * (B64[a] @ (A64[a] @ xf[i]))
+    return y
+
+
+def _w4_forward_seed0():
+    Q.test_oracle_w4_forward_matches_the_c_oracle(0)
+
+
+def _w4_forward_seed1():
+    Q.test_oracle_w4_forward_matches_the_c_oracle(1)
+
+
+W4_PINS = [_w4_forward_seed0, _w4_forward_seed1]
+
+
+def test_int4_forward_restatement_passes_every_pin(monkeypatch):
+    monkeypatch.setattr(oracle, "adapted_linear_w4", lambda *a, **k: _forward_w4(*a, **k))
+    assert _failing_pins(W4_PINS) == []
+
+
+@pytest.mark.parametrize("bug", ["row_scale_skipped", "scale_by_column", "codes_left_offset", "adapter_dropped"])
+def test_int4_forward_pins_catch_planted_mistake(monkeypatch, bug):
+    monkeypatch.setattr(oracle, "adapted_linear_w4", lambda *a, **k: _forward_w4(*a, bug=bug, **k))
+    assert _failing_pins(W4_PINS), f"no pin caught {bug}"
