@@ -39,6 +39,21 @@ def test_value_per_byte_keeps_the_hot_adapter_that_lru_would_evict():
     assert c.acquire("N", 200, 11.0) == ("ok", ["C"], True)
 
 
+def test_value_is_per_byte_not_per_adapter():
+    """A big adapter with more requests can still be worth less per byte: A holds 300 B for 3
+    requests (0.01 per byte), C holds 100 B for 2 (0.02 per byte), so A goes first and alone makes
+    the room; counting requests alone would evict C first and then A as well."""
+    c = OC.AdapterCache(400, guard_fraction=1.0)
+    for t in range(3):
+        c.acquire("A", 300, float(t))
+        c.release("A")
+    for t in (3.0, 4.0):
+        c.acquire("C", 100, t)
+        c.release("C")
+    assert c.acquire("N", 300, 5.0) == ("ok", ["A"], True)
+    assert c.resident == {"C", "N"}
+
+
 def test_referenced_adapter_is_never_evicted():
     c = OC.AdapterCache(300, guard_fraction=1.0)
     for t in range(10):
@@ -181,6 +196,22 @@ def test_library_matches_oracle_decision_for_decision(seed, guard, window):
     u, p, r = lib.stats()
     assert (u, p, r) == (ref.used_bytes(), ref.pinned_bytes(), len(ref.resident))
     lib.close()
+
+
+def test_library_value_is_per_byte():
+    """The library on the per-byte scenario above (ids 1 = A, 2 = C, 3 = N)."""
+    L = _lib()
+    c = L.AdapterCache(400, guard_fraction=1.0)
+    for t in range(3):
+        c.acquire(1, 300, float(t))
+        c.release(1)
+    for t in (3.0, 4.0):
+        c.acquire(2, 100, t)
+        c.release(2)
+    ev, load = c.acquire(3, 300, 5.0)
+    assert list(ev) == [1] and load
+    assert c.resident(2)[0] and not c.resident(1)[0]
+    c.close()
 
 
 def test_library_argument_checks():

@@ -173,3 +173,104 @@ def test_int4_forward_restatement_passes_every_pin(monkeypatch):
 def test_int4_forward_pins_catch_planted_mistake(monkeypatch, bug):
     monkeypatch.setattr(oracle, "adapted_linear_w4", lambda *a, **k: _forward_w4(*a, bug=bug, **k))
     assert _failing_pins(W4_PINS), f"no pin caught {bug}"
+
+
+# ------------------------------------------------------------------------- batch former ---
+
+import test_batch_former as TB  # noqa: E402
+from oracle import batch_former as OB  # noqa: E402
+
+_form_batch = OB.form_batch
+
+
+def _hand_worked_cases():
+    for case in TB._cases():
+        TB.test_oracle_hand_worked_cases(case)
+
+
+def _plain_grouping_properties():
+    for seed in range(4):
+        TB.test_oracle_properties_plain_grouping(seed)
+
+
+def _fairness_properties():
+    for seed in range(4):
+        TB.test_oracle_properties_fairness(seed)
+
+
+FORMER_PINS = [_hand_worked_cases, _plain_grouping_properties, _fairness_properties]
+
+
+def _former_mutant(bug):
+    def f(queue_adapter, queue_waited_ms, max_batch, max_distinct, min_batch=1, tail_slots=0, max_queue_ms=0.0):
+        if bug == "cap_ignored":
+            max_distinct = 10 ** 9
+        elif bug == "tail_slots_ignored":
+            tail_slots = 0
+        elif bug == "age_override_ignored":
+            max_queue_ms = 0.0
+        elif bug == "min_batch_ignored":
+            min_batch = 1
+        elif bug == "newest_first":  # the queue walked from its tail
+            n = len(queue_adapter)
+            batch, d = _form_batch(list(queue_adapter)[::-1], list(queue_waited_ms)[::-1], max_batch, max_distinct,
+                                   min_batch, tail_slots, max_queue_ms)
+            return [n - 1 - i for i in batch], d
+        return _form_batch(queue_adapter, queue_waited_ms, max_batch, max_distinct, min_batch, tail_slots,
+                           max_queue_ms)
+    return f
+
+
+def test_batch_former_wrapper_without_mistake_passes_every_pin(monkeypatch):
+    monkeypatch.setattr(OB, "form_batch", _former_mutant(None))
+    assert _failing_pins(FORMER_PINS) == []
+
+
+@pytest.mark.parametrize("bug", ["cap_ignored", "tail_slots_ignored", "age_override_ignored", "min_batch_ignored",
+                                 "newest_first"])
+def test_batch_former_pins_catch_planted_mistake(monkeypatch, bug):
+    monkeypatch.setattr(OB, "form_batch", _former_mutant(bug))
+    assert _failing_pins(FORMER_PINS), f"no pin caught {bug}"
+
+
+# ------------------------------------------------------------------------ adapter cache ---
+
+from fractions import Fraction  # noqa: E402
+
+import test_adapter_cache as TC  # noqa: E402
+from oracle import adapter_cache as OC  # noqa: E402
+
+
+def _cache_properties():
+    for seed in range(3):
+        TC.test_oracle_properties_on_zipf_traffic(seed)
+
+
+CACHE_PINS = [TC.test_value_per_byte_keeps_the_hot_adapter_that_lru_would_evict, TC.test_value_is_per_byte_not_per_adapter,
+              TC.test_referenced_adapter_is_never_evicted,
+              TC.test_pinning_guard_refuses_new_adapters_but_not_resident_ones, TC.test_value_counts_only_the_window,
+              TC.test_no_room_changes_nothing, TC.test_ties_go_to_the_older_latest_request_then_the_smaller_id,
+              TC.test_evicts_the_fewest_adapters_in_value_order, _cache_properties]
+
+CACHE_BUGS = {
+    # recency instead of value per byte
+    "lru": ("_value", lambda self, a, now: max(self.requests.get(a, [float("-inf")]))),
+    # requests counted, bytes ignored
+    "count_only": ("_value", lambda self, a, now: Fraction(
+        len([t for t in self.requests.get(a, []) if t > now - self.window]), 1)),
+    # every request counts, however old
+    "window_ignored": ("_value", lambda self, a, now: Fraction(len(self.requests.get(a, [])), self.bytes[a])),
+    # the guard never sees pinned bytes
+    "guard_blind": ("pinned_bytes", lambda self: 0),
+}
+
+
+def test_cache_pins_pass_unchanged():
+    assert _failing_pins(CACHE_PINS) == []
+
+
+@pytest.mark.parametrize("bug", sorted(CACHE_BUGS))
+def test_cache_pins_catch_planted_mistake(monkeypatch, bug):
+    name, fn = CACHE_BUGS[bug]
+    monkeypatch.setattr(OC.AdapterCache, name, fn)
+    assert _failing_pins(CACHE_PINS), f"no pin caught {bug}"
