@@ -274,3 +274,84 @@ def test_cache_pins_catch_planted_mistake(monkeypatch, bug):
     name, fn = CACHE_BUGS[bug]
     monkeypatch.setattr(OC.AdapterCache, name, fn)
     assert _failing_pins(CACHE_PINS), f"no pin caught {bug}"
+
+
+# ------------------------------------------------------------------ int8 adapter factors ---
+
+import test_int8_factors as T8  # noqa: E402
+
+
+def _quantize8(bits, bug=None):
+    v = wl.bf16_bits_to_f32(np.asarray(bits, np.uint16))
+    levels = 128.0 if bug == "scale_over_128" else 127.0
+    scale = (np.abs(v).max(axis=1) / np.float32(levels)).astype(np.float32)
+    codes = np.zeros(v.shape, np.int8)
+    nz = scale > 0
+    q = v[nz] / scale[nz, None]
+    q = np.trunc(q) if bug == "truncate" else np.rint(q)
+    if bug == "sign_lost":
+        q = np.abs(q)
+    codes[nz] = np.clip(q, -127, 127).astype(np.int8)
+    return codes, scale
+
+
+def _i8_nearest_seed0():
+    T8.test_oracle_quantizer_rounds_to_the_nearest_code(0)
+
+
+def _i8_nearest_seed1():
+    T8.test_oracle_quantizer_rounds_to_the_nearest_code(1)
+
+
+I8_QUANT_PINS = [_i8_nearest_seed0, _i8_nearest_seed1, T8.test_oracle_quantizer_signs_and_exact_multiples]
+
+
+def test_int8_quantizer_restatement_passes_every_pin(monkeypatch):
+    monkeypatch.setattr(oracle, "quantize_rows_int8", lambda b: _quantize8(b))
+    assert _failing_pins(I8_QUANT_PINS) == []
+
+
+@pytest.mark.parametrize("bug", ["scale_over_128", "truncate", "sign_lost"])
+def test_int8_quantizer_pins_catch_planted_mistake(monkeypatch, bug):
+    monkeypatch.setattr(oracle, "quantize_rows_int8", lambda b: _quantize8(b, bug))
+    assert _failing_pins(I8_QUANT_PINS), f"no pin caught {bug}"
+
+
+def _factors64(x, W, ids, A64, B64, scale, rows=None, threads=0, bug=None):
+    xf, Wf = _f64(x), _f64(W)
+    ids = np.asarray(ids, np.int32)
+    rows = np.arange(len(ids)) if rows is None else np.asarray(rows)
+    y = np.zeros((len(rows), Wf.shape[0]))
+    for k, i in enumerate(rows):
+        y[k] = Wf @ xf[i]
+        a = int(ids[i])
+        if a < 0:
+            continue
+        Bm = B64[a]
+        if bug == "B_transposed_read":
+            Bm = Bm.reshape(Bm.shape[1], Bm.shape[0]).T
+        t = A64[a] @ xf[i]
+        y[k] += (1.0 if bug == "t_not_scaled" else scale) * (Bm @ t)
+    return y
+
+
+def _f64_forward_seed0():
+    T8.test_oracle_fp64_factor_forward_matches_the_c_oracle(0)
+
+
+def _f64_forward_seed1():
+    T8.test_oracle_fp64_factor_forward_matches_the_c_oracle(1)
+
+
+F64_PINS = [_f64_forward_seed0, _f64_forward_seed1]
+
+
+def test_factor_forward_restatement_passes_every_pin(monkeypatch):
+    monkeypatch.setattr(oracle, "adapted_linear_factors64", lambda *a, **k: _factors64(*a, **k))
+    assert _failing_pins(F64_PINS) == []
+
+
+@pytest.mark.parametrize("bug", ["t_not_scaled", "B_transposed_read"])
+def test_factor_forward_pins_catch_planted_mistake(monkeypatch, bug):
+    monkeypatch.setattr(oracle, "adapted_linear_factors64", lambda *a, **k: _factors64(*a, bug=bug, **k))
+    assert _failing_pins(F64_PINS), f"no pin caught {bug}"
