@@ -355,3 +355,48 @@ def test_factor_forward_restatement_passes_every_pin(monkeypatch):
 def test_factor_forward_pins_catch_planted_mistake(monkeypatch, bug):
     monkeypatch.setattr(oracle, "adapted_linear_factors64", lambda *a, **k: _factors64(*a, bug=bug, **k))
     assert _failing_pins(F64_PINS), f"no pin caught {bug}"
+
+
+# ------------------------------------------------------------------------- row grouping ---
+
+def _segments(ids, bug=None):
+    ids = np.asarray(ids, np.int32)
+    n = len(ids)
+    if bug == "unstable":  # ties in reverse arrival order
+        perm = sorted(range(n), key=lambda i: (int(ids[i]), -i))
+    elif bug == "base_rows_last":
+        perm = sorted(range(n), key=lambda i: (int(ids[i]) < 0, int(ids[i])))
+    elif bug == "descending":
+        perm = sorted(range(n), key=lambda i: -int(ids[i]))
+    else:
+        perm = sorted(range(n), key=lambda i: int(ids[i]))
+    seg_start, seg_adapter = [0], []
+    for k, i in enumerate(perm):
+        if k == 0 or ids[i] != ids[perm[k - 1]]:
+            if k > 0:
+                seg_start.append(k)
+            seg_adapter.append(int(ids[i]))
+    if n:
+        seg_start.append(n)
+    if bug == "last_segment_dropped" and seg_adapter:
+        seg_adapter, seg_start = seg_adapter[:-1], seg_start[:-1]
+    return np.array(perm, np.int32), np.array(seg_start, np.int32), np.array(seg_adapter, np.int32)
+
+
+def _stable_sort_seeds():
+    for seed in range(6):
+        P.test_segments_stable_sort(seed)
+
+
+SEGMENT_PINS = [_stable_sort_seeds, P.test_segments_edge_cases]
+
+
+def test_segments_restatement_passes_every_pin(monkeypatch):
+    monkeypatch.setattr(oracle, "segments", lambda ids: _segments(ids))
+    assert _failing_pins(SEGMENT_PINS) == []
+
+
+@pytest.mark.parametrize("bug", ["unstable", "base_rows_last", "descending", "last_segment_dropped"])
+def test_segments_pins_catch_planted_mistake(monkeypatch, bug):
+    monkeypatch.setattr(oracle, "segments", lambda ids: _segments(ids, bug))
+    assert _failing_pins(SEGMENT_PINS), f"no pin caught {bug}"
