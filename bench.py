@@ -173,24 +173,33 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------------------
-def cpu_baseline(w, xs, Ws, factors, budget_s=10.0):
+def cpu_baseline(w, xs, Ws, factors, budget_s=10.0, single_core_s=3.0):
     """The oracle as it stands, on this host's cores: whole steps (every row, every projection)
-    repeated until ~budget_s of work; returns rows/s."""
+    repeated until ~budget_s of work; returns rows/s.  The same oracle on one core is timed too,
+    on the first 8 rows of the step, for ~single_core_s."""
     import oracle
-    rows = np.arange(w.n_rows)
-    t0 = time.perf_counter()
-    done = 0
-    while True:
-        for st, mods in enumerate(w.stages):
-            for m in mods:
-                oracle.workload_module(w, m, rows=rows, stage_x=xs[st], W=Ws[m], factors=factors)
-        done += w.n_rows
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": done / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{done // w.n_rows} full step(s) of the workload ({done} rows x 4 projections), fp64",
-            "seconds": round(dt, 2)}
+
+    def timed_rows(rows, threads, budget):
+        t0 = time.perf_counter()
+        done = 0
+        while True:
+            for st, mods in enumerate(w.stages):
+                for m in mods:
+                    oracle.workload_module(w, m, rows=rows, threads=threads, stage_x=xs[st], W=Ws[m], factors=factors)
+            done += len(rows)
+            if time.perf_counter() - t0 >= budget:
+                return done, time.perf_counter() - t0
+
+    done, dt = timed_rows(np.arange(w.n_rows), 0, budget_s)
+    n_proj = sum(len(mods) for mods in w.stages)
+    out = {"value": done / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+           "sample": f"{done // w.n_rows} full step(s) of the workload ({done} rows x {n_proj} projections), fp64",
+           "seconds": round(dt, 2)}
+    done1, dt1 = timed_rows(np.arange(min(8, w.n_rows)), 1, single_core_s)
+    out["single_core"] = {"value": done1 / dt1, "unit": UNIT, "cores": 1,
+                          "sample": f"{done1} rows (the step's first 8, repeated) x {n_proj} projections, fp64",
+                          "seconds": round(dt1, 2)}
+    return out
 
 
 def make_inputs(w):
