@@ -383,8 +383,10 @@ typedef struct {
 /*
  * lora_layer_forward_w4 / lora_layer_forward_planned_w4 -- lora_layer_forward and
  * lora_layer_forward_planned with int4 base weights.  Decode batches only (n <= 256); the module's
- * d_in must be a multiple of 32.  The pool's factors may be bf16 or int8.  Same row ids, error
- * word and errors as the bf16 calls (EUNSUPPORTED also for d_in % 32 != 0).
+ * d_in must be a multiple of 32.  The pool's factors may be bf16 or int8.  x, W_codes, W_scale and
+ * y are caller-owned device memory, borrowed for the call (x, W_codes, y 16-byte aligned, W_scale
+ * 4-byte aligned).  Same row ids, error word and errors as the bf16 calls: EINVAL also for a
+ * missing or misaligned W_scale, EUNSUPPORTED also for d_in % 32 != 0 or n > 256.
  */
 int lora_layer_forward_w4(lora_pool *pool, int32_t n_io, const lora_module_io_w4 *io,
                           const int32_t *row_adapter_ids, int32_t n, float scale, int32_t y_dtype,
