@@ -228,3 +228,30 @@ def test_int8_planned_forward_equals_own_grouping():
                 torch.cuda.synchronize()
                 assert torch.equal(y, own[m]), (m, y_dtype)
     pool.close()
+
+
+@pytest.mark.gpu
+def test_int8_full_size_attention_sampled_rows():
+    """The 70B attention decode batch (q/k/v/o, 128 rows, 128 distinct rank-8 adapters) with int8
+    factors, planned as the benchmark runs it, on rows the oracle computes one by one."""
+    import torch
+    from harness import check_close, to_dev_bf16
+    w = wl.attn70b_decode()
+    q = _quantized(w, [int(a) for a in w.used_adapters()])
+    pool = _i8_pool(w, q)
+    names = w.module_names()
+    rows = np.array([0, 1, 37, 64, 100, 127])
+    pool.plan_rows(torch.from_numpy(w.ids).cuda())
+    for st in range(len(w.stages)):
+        x = to_dev_bf16(w.x(st))
+        ios = []
+        for m in w.stages[st]:
+            y = torch.full((w.n_rows, w.modules[m][1]), float("nan"), dtype=torch.float32, device="cuda")
+            ios.append((names.index(m), x, to_dev_bf16(w.W(m)), y))
+        pool.layer_forward_planned(ios, w.scale)
+        torch.cuda.synchronize()
+        for (_, _, _, y), m in zip(ios, w.stages[st]):
+            check_close(y.cpu().double().numpy()[rows], _ref(w, q, m, st, rows=rows), what=f"attn70b int8/{m}")
+    code, _ = pool.last_device_error()
+    assert code == 0
+    pool.close()
