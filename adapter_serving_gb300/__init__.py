@@ -94,6 +94,7 @@ _sig("lora_linear_forward_static", ctypes.c_int, _P, _P, _I32, _I32, _P, _I32, _
 _sig("lora_pool_last_segments", ctypes.c_int, _P, _P, _P, _P, ctypes.POINTER(_I32), ctypes.POINTER(_I32))
 _sig("lora_last_device_error", ctypes.c_int, _P, ctypes.POINTER(_I32), ctypes.POINTER(_I32))
 _sig("lora_profile_enable", ctypes.c_int, _P, _I32)
+_sig("lora_pool_set_wait_budget", ctypes.c_int, _P, ctypes.c_uint64)
 _sig("lora_profile_read", ctypes.c_int, _P, _I32, ctypes.POINTER(_I32), ctypes.POINTER(ctypes.c_double))
 _sig("lora_last_cuda_error", ctypes.c_char_p)
 _sig("lora_status_string", ctypes.c_char_p, ctypes.c_int)
@@ -440,7 +441,11 @@ class Pool:
         decoded = n.value <= MAX_DECODE_ROWS
         return (perm[:n.value].copy() if decoded else None), ss, sa[:ns.value].copy()
 
-    KERNELS = {"prep": 0, "shrink": 1, "gemm": 2}
+    KERNELS = {"prep": 0, "shrink": 1, "gemm": 2, "finalize": 3}
+
+    def set_wait_budget(self, budget_ns):
+        """Budget of each bounded in-kernel wait (lora_pool_set_wait_budget); 0 = the 2 s default."""
+        _check(lib.lora_pool_set_wait_budget(self.handle, int(budget_ns)), "lora_pool_set_wait_budget")
 
     def profile(self, enable=True):
         _check(lib.lora_profile_enable(self.handle, 1 if enable else 0), "lora_profile_enable")

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "liblora_gb300.so")
-SOURCES = ["lora_kernels.cu", "lora_api.cu", "lora_static.cu", "batch_former.cpp", "adapter_cache.cpp"]
+SOURCES = ["lora_kernels.cu", "decode_kernels.cu", "lora_api.cu", "lora_static.cu", "batch_former.cpp", "adapter_cache.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

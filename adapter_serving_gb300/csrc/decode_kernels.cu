@@ -1,0 +1,941 @@
+// decode_kernels.cu -- the decode path of the adapted linear layer y_i = W x_i + s B_a (A_a x_i),
+// for a batch of at most 256 rows that each carry their own adapter id:
+//
+//   prep_decode_kernel      row grouping: stable sort of the rows by adapter id (the segments),
+//                           id checks, and per projection the gather list of the distinct
+//                           adapters' A rows (8-row groups)
+//   decode_gemm_kernel      one persistent tcgen05 GEMM per call over two tile spaces, each split
+//                           stream-K over the SMs: W tiles (128 rows of W: the base W x) and A tiles
+//                           (128 gathered rows of the distinct adapters' A: the shrink A_a x).  Both
+//                           multiply the same x k-blocks; base pieces go to the workspace, the
+//                           shrink's t values (row j against its own adapter's rows only) to per-CTA
+//                           partial buffers
+//   decode_finalize_kernel  per (W tile, 16 rows): the base pieces added in k order, t summed in k
+//                           order and scaled, the expand s B_a t on CUDA cores (B read once per
+//                           distinct adapter and tile), y written
+//
+// The forward is "m07 -- Multi-Adapter (LoRA) Serving", section 6 "Deep Dive A: Batching
+// Heterogeneous Adapters": one base GEMM shared by the batch plus a per-row adapter product
+// gathered through an index vector inside the kernel; "the cost is bandwidth, not compute": W is
+// read once per call and every distinct adapter's A and B once per call.  The shrink rides on the
+// tensor cores because the base GEMM's operand stream is already there: an A tile costs the same
+// bytes as the CUDA-core shrink and multiplies every row (the rows of other adapters are computed
+// and dropped), which is free at decode, where the tensor pipe idles.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <algorithm>
+#include <cstdint>
+
+#include "lora_internal.h"
+#include "prep_common.cuh"
+#include "ptx.cuh"
+
+namespace lora {
+
+// ============================================================================ prep ==========
+
+constexpr int kPrepGroups = 4;  // groups of 256 threads; group g builds projections g, g + 4
+
+// Exclusive prefix sum of 64-bit values over a group of 256 threads (8 warps) on named barrier
+// `bar`; `total` receives the sum.
+__device__ uint64_t group_scan256_u64(uint64_t v, uint64_t *s_warp, uint64_t &total, int bar) {
+    const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) & 7;
+    uint64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    named_bar_sync(bar, 256);
+    uint64_t before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint64_t t = s_warp[w];
+        before += w < warp ? t : 0;
+        tot += t;
+    }
+    named_bar_sync(bar, 256);  // s_warp may be reused
+    total = tot;
+    return before + x - v;
+}
+
+// Row grouping state the prep block keeps in shared memory (n <= 256 rows).
+struct PrepShared {
+    int id[LORA_MAX_DECODE_ROWS];                    // adapter id of row r (-1 = base only)
+    int sorted[LORA_MAX_DECODE_ROWS];                // adapter id at sorted position q
+    int perm[LORA_MAX_DECODE_ROWS];                  // row at sorted position q
+    int cnt[4][LORA_MAX_DECODE_ROWS];                // partial position counts
+    int seg_of[LORA_MAX_DECODE_ROWS];                // segment of position q
+    int seg_q0[LORA_MAX_DECODE_ROWS + 1];            // first position of segment s
+    int rank[LORA_MAX_MODULES][LORA_MAX_DECODE_ROWS];  // rank at position q (0 = none)
+    int arow[LORA_MAX_MODULES][LORA_MAX_DECODE_ROWS];  // first A-slab row of the adapter at q
+    int scan[8];
+};
+
+// The gather list of every projection: each segment with an adapter of rank r takes ceil(r / 8)
+// consecutive 8-row groups (its A rows in order), segments in sorted order; a row's t values sit
+// at slot rows [8 g0, 8 g0 + r) of its segment's first group g0.
+__device__ void build_groups(const PrepParams &p, const PrepShared &sh, int ns) {
+    __shared__ uint64_t s_warp_all[kPrepGroups][8];
+    __shared__ int s_g0_all[kPrepGroups][LORA_MAX_DECODE_ROWS];
+    const int g = threadIdx.x >> 8, tid = threadIdx.x & 255;
+    const int bar = 1 + g;
+    uint64_t *s_warp = s_warp_all[g];
+    int *s_g0 = s_g0_all[g];
+    for (int m = g; m < p.n_mod; m += kPrepGroups) {
+        int cnt = 0, q0 = 0, q1 = 0, r = 0, row = 0;
+        if (tid < ns) {
+            q0 = sh.seg_q0[tid];
+            q1 = sh.seg_q0[tid + 1];
+            r = sh.rank[m][q0];
+            row = sh.arow[m][q0];
+            if (sh.sorted[q0] >= 0 && r > 0) cnt = (r + kGroupRows - 1) / kGroupRows;
+        }
+        uint64_t tot = 0;
+        const int g0 = (int)group_scan256_u64((uint64_t)cnt, s_warp, tot, bar);
+        if (tid < ns) s_g0[tid] = cnt > 0 ? g0 : -1;
+        AGroup *G = p.groups[m];
+        for (int k = 0; k < cnt; ++k) {
+            AGroup a;
+            a.row = row + kGroupRows * k;
+            a.q0 = (int16_t)q0;
+            a.q1 = (int16_t)q1;
+            a.rbase = (int16_t)(kGroupRows * k);
+            a.rank = (int16_t)r;
+            a.pad_ = 0;
+            G[g0 + k] = a;
+        }
+        if (tid == 0) p.n_groups[m] = (int)tot;
+        named_bar_sync(bar, 256);
+        for (int q = tid; q < p.n; q += 256) {
+            const int gs = s_g0[sh.seg_of[q]];
+            p.rowinfo[m][sh.perm[q]].tslot = gs >= 0 ? gs * kGroupRows : -1;
+        }
+        named_bar_sync(bar, 256);  // s_g0 is reused by the group's next projection
+    }
+}
+
+// One block of 1024 threads, n <= 256 rows.  Position of row i in the stable order:
+// #{j : id_j < id_i} + #{j < i : id_j == id_i}, counted by four threads per row over a quarter
+// of the rows each.
+__global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const PrepParams p) {
+    __shared__ PrepShared sh;
+    const int tid = threadIdx.x;
+    const int n = p.n;
+    grid_dep_wait();
+    grid_dep_launch();
+    bool seg_ok = true;
+    if (p.ids == nullptr) {
+        seg_ok = segments_valid_block(p);
+        if (!seg_ok && tid == 0) report(p.err, LORA_DEVERR_BAD_SEGMENTS, 0);
+    }
+    // ---- ids, checked; every projection's rank and A row of the row's adapter (loads in flight first)
+    int id = -1;
+    int rank_row[LORA_MAX_MODULES], arow_row[LORA_MAX_MODULES], rp_row[LORA_MAX_MODULES];
+    const uint16_t *B_row[LORA_MAX_MODULES];
+    if (tid < n) {
+        int where = tid;
+        if (p.ids) {
+            id = p.ids[tid];
+        } else if (seg_ok) {
+            where = seg_of(p.seg_start_in, p.n_seg_in, tid);
+            id = p.seg_adapter_in[where];
+        }
+        if (id < -1 || id >= p.max_adapters) {
+            report(p.err, LORA_DEVERR_BAD_ADAPTER, where);
+            id = -1;
+        }
+#pragma unroll
+        for (int m = 0; m < LORA_MAX_MODULES; ++m) {
+            rank_row[m] = 1;
+            arow_row[m] = 0;
+            rp_row[m] = 0;
+            B_row[m] = nullptr;
+            if (id >= 0 && m < p.n_mod) {
+                const PoolEntry *e = p.table[m] + id;
+                rank_row[m] = e->rank;
+                arow_row[m] = (int)e->row_off;
+                rp_row[m] = e->rp;
+                B_row[m] = e->B;
+            }
+        }
+        bool ok = true;
+#pragma unroll
+        for (int m = 0; m < LORA_MAX_MODULES; ++m) ok = ok && rank_row[m] > 0;
+        if (!ok) {
+            report(p.err, LORA_DEVERR_NOT_LOADED, where);
+            id = -1;
+        }
+        if (id < 0) {
+#pragma unroll
+            for (int m = 0; m < LORA_MAX_MODULES; ++m) rank_row[m] = 0;
+        }
+        sh.id[tid] = id;
+        p.radapter[tid] = id;
+#pragma unroll
+        for (int m = 0; m < LORA_MAX_MODULES; ++m)
+            if (m < p.n_mod) {  // the slot row is filled in with the gather lists below
+                RowInfo ri;
+                ri.B = id >= 0 ? B_row[m] : nullptr;
+                ri.rank = (int16_t)(id >= 0 ? rank_row[m] : 0);
+                ri.rp = (int16_t)(id >= 0 ? rp_row[m] : 0);
+                ri.tslot = -1;
+                p.rowinfo[m][tid] = ri;
+            }
+    }
+    __syncthreads();
+    // ---- stable sort: four partial counts per row
+    {
+        const int row = tid & 255, part = tid >> 8;
+        if (row < n) {
+            const int v = sh.id[row];
+            const int j0 = part * n / 4, j1 = (part + 1) * n / 4;
+            int c = 0;
+            for (int j = j0; j < j1; ++j) {
+                const int u = sh.id[j];
+                c += (u < v) || (u == v && j < row);
+            }
+            sh.cnt[part][row] = c;
+        }
+    }
+    __syncthreads();
+    if (tid < n) {
+        const int pos = sh.cnt[0][tid] + sh.cnt[1][tid] + sh.cnt[2][tid] + sh.cnt[3][tid];
+        p.perm[pos] = tid;
+        p.qadapter[pos] = id;
+        sh.perm[pos] = tid;
+        sh.sorted[pos] = id;
+#pragma unroll
+        for (int m = 0; m < LORA_MAX_MODULES; ++m) {
+            sh.rank[m][pos] = rank_row[m];
+            sh.arow[m][pos] = arow_row[m];
+        }
+    }
+    __syncthreads();
+    // ---- segment starts: positions whose id differs from the one before; inclusive scan of the
+    // flags (warp shuffles, then the 8 warp totals)
+    int flag = 0;
+    if (tid < 256) flag = (tid < n) && (tid == 0 || sh.sorted[tid] != sh.sorted[tid - 1]);
+    int incl = flag;
+    const int lane = tid & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (tid < 256 && lane == 31) sh.scan[tid >> 5] = incl;
+    __syncthreads();
+    int before = 0, ns = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const int t = sh.scan[w];
+        before += w < (tid >> 5) ? t : 0;
+        ns += t;
+    }
+    if (tid < n) sh.seg_of[tid] = before + incl - 1;
+    if (flag) {
+        const int seg = before + incl - 1;
+        p.seg_start[seg] = tid;
+        p.seg_adapter[seg] = sh.sorted[tid];
+        sh.seg_q0[seg] = tid;
+    }
+    if (tid == 0) {
+        *p.n_seg = ns;
+        p.seg_start[ns] = n;
+        sh.seg_q0[ns] = n;
+    }
+    if (p.groups[0] != nullptr) {
+        __syncthreads();  // the segment table is complete
+        build_groups(p, sh, ns);
+    }
+}
+
+// ============================================================================ gemm ==========
+//
+// Two launches per call, each a programmatic dependent of the one before it.
+//
+// decode_gemm_kernel: one CTA per SM (at most), warp roles: warp 0 is the TMA producer, lane 0 of
+// warp 1 issues tcgen05.mma, warps 2-5 are the epilogue (TMEM lane quarter = warp % 4); with an
+// int4 base, warps 6-7 convert W codes to bf16 between the TMA load and the MMA.  MMA M = 128 rows of W or of the gathered A rows,
+// N = the batch (nt columns, column = row of the batch), K = d_in in 64-wide k-blocks.  Each of the
+// two tile spaces is split stream-K: CTA c takes k-blocks [c T / N, (c + 1) T / N) of the W space
+// (T = all W tiles' k-blocks, N = CTAs), then its share of the A space (whose size the prep decided
+// on the device).  Every item (a tile's k range held by one CTA) accumulates into one of two TMEM
+// buffers, so the drain of one overlaps the MMAs of the next.  W items leave base pieces in the
+// workspace; A items leave, for every row j, its share of t_j (the rows of its own adapter only),
+// and the last CTA to finish an A tile (a counter, no waiting) adds the tile's shares in k order.
+// The gemm lets its dependent launch at once: the finalize's blocks take the registers the gemm
+// leaves free and wait, so they start the moment the gemm's last CTA is done.
+//
+// decode_finalize_kernel: block (W tile, 16 rows of the batch), thread o = output row 128 tile + o:
+//   base  = the tile's pieces in k order (the piece from k-block 0, then every later CTA's)
+//   t_j   = the final t row the gemm's A-tile pass wrote, or the CUDA-core shrink's (int8 factors)
+//   y[j, o] = base + sum_r B_a(j)[o, r] t_j[r]
+// The rows' adapters and their B rows are fetched before the block waits for the gemm; after it,
+// one round of loads (t and the pieces), the dot products and the stores.  B is read as
+// the pool stores it ([d_out, rp]): a block reads one contiguous run of 128 rows of each row's
+// adapter.
+
+constexpr int kConvWarp0 = 2 + kEpiWarps;
+constexpr int kDecThreads = 32 * (kConvWarp0);
+constexpr int kDecThreadsW4 = 32 * (kConvWarp0 + kConvWarps);
+constexpr int kFinRows = 16;                   // rows of the batch per finalize block
+constexpr uint32_t kPreL2 = 12;                // W k-blocks asked of L2 before the wait
+
+// The A space of a call, computed from the prep's group counts (one thread).
+struct DecShared {
+    int32_t a_begin[LORA_MAX_MODULES + 1];  // first A-space k-block of each projection
+    int32_t n_groups[LORA_MAX_MODULES];
+    int32_t a_iters, a_ctas;
+};
+
+__device__ void dec_a_space(const DecodeParams &p, DecShared &d) {
+    int it = 0, kbn_max = 0;
+    for (int m = 0; m < p.n_mod; ++m) {
+        int g = p.shrink_tc ? *p.mod[m].n_groups : 0;
+        g = min(max(g, 0), kDecMaxGroups);
+        const int at = (g + kTileGroups - 1) / kTileGroups;
+        d.n_groups[m] = g;
+        d.a_begin[m] = it;
+        it += at * p.mod[m].k_blocks;
+        if (at > 0) kbn_max = max(kbn_max, p.mod[m].k_blocks);
+    }
+    d.a_begin[p.n_mod] = it;
+    d.a_iters = it;
+    d.a_ctas = decode_a_ctas(it, kbn_max, p.n_cta);
+}
+
+// The CTA whose range [c T / N, (c + 1) T / N) holds position x (32-bit arithmetic while T N
+// fits, as it does for every shape a pool can hold).
+__device__ __forceinline__ int cta_of(int64_t x, int64_t total, int n) {
+    if (total * n < 0x7fffffff) return (int)(((uint32_t)(x + 1) * (uint32_t)n - 1u) / (uint32_t)total);
+    return (int)(((x + 1) * n - 1) / total);
+}
+
+struct DItem {
+    int32_t a;         // 0: W tile, 1: A tile
+    int32_t m;         // projection
+    int32_t tile;      // tile within the projection (W: rows 128 tile..; A: groups 16 tile..)
+    int32_t kb0, kb1;  // the CTA's k-blocks of the tile
+    int32_t it0;       // the tile's first k-block in its space
+};
+
+// A CTA's items: its share of the A space first (so the shrink's t values are complete early and
+// the last CTA on each A tile adds them up while the W stream runs), then its W range.
+struct DSched {
+    int64_t x, e;
+    int32_t phase, cta;
+    // the W range only (before the wait, when the A space is not known yet)
+    __device__ void begin_w(const DecodeParams &p, int c) {
+        cta = c;
+        phase = 1;
+        x = (int64_t)c * p.w_iters / p.n_cta;
+        e = (int64_t)(c + 1) * p.w_iters / p.n_cta;
+    }
+    __device__ void begin(const DecodeParams &p, int c, const DecShared &d) {
+        cta = c;
+        phase = 0;
+        if (c < d.a_ctas) {
+            x = (int64_t)c * d.a_iters / d.a_ctas;
+            e = (int64_t)(c + 1) * d.a_iters / d.a_ctas;
+        } else {
+            x = e = 0;
+        }
+    }
+    __device__ bool next(const DecodeParams &p, const DecShared *d, DItem &it) {
+        if (phase == 0) {
+            if (x < e) {
+                int m = 0;
+                while (m + 1 < p.n_mod && d->a_begin[m + 1] <= x) ++m;
+                const int kbn = p.mod[m].k_blocks;
+                const int local = (int)(x - d->a_begin[m]);
+                const int at = local / kbn;
+                it.a = 1;
+                it.m = m;
+                it.tile = at;
+                it.kb0 = local - at * kbn;
+                it.kb1 = (e - x) < (int64_t)(kbn - it.kb0) ? it.kb0 + (int)(e - x) : kbn;
+                it.it0 = d->a_begin[m] + at * kbn;
+                x += it.kb1 - it.kb0;
+                return true;
+            }
+            begin_w(p, cta);
+        }
+        if (phase == 1 && x < e) {
+            int m = 0;
+            while (m + 1 < p.n_mod && p.mod[m + 1].w_iter_begin <= x) ++m;
+            const int kbn = p.mod[m].k_blocks;
+            const int local = (int)(x - p.mod[m].w_iter_begin);
+            const int lt = local / kbn;
+            it.a = 0;
+            it.m = m;
+            it.tile = lt;
+            it.kb0 = local - lt * kbn;
+            it.kb1 = (e - x) < (int64_t)(kbn - it.kb0) ? it.kb0 + (int)(e - x) : kbn;
+            it.it0 = p.mod[m].w_iter_begin + lt * kbn;
+            x += it.kb1 - it.kb0;
+            return true;
+        }
+        phase = 2;
+        return false;
+    }
+};
+
+// Base pieces are kept in column quads: element (column c, lane o) at ((c / 4) * 128 + o) * 4 +
+// c % 4.  A thread's 16 columns are four 16-byte vectors and a warp stores or loads 512
+// contiguous bytes per instruction.
+__device__ __forceinline__ float4 *piece_quads(float *piece, int c0, int o) {
+    return reinterpret_cast<float4 *>(piece) + (size_t)(c0 >> 2) * kBM + o;
+}
+__device__ __forceinline__ const float4 *piece_quads(const float *piece, int c0, int o) {
+    return reinterpret_cast<const float4 *>(piece) + (size_t)(c0 >> 2) * kBM + o;
+}
+
+// W4: the int4 codes of one W k-block ([128 rows][32 bytes] as the TMA lays the box down) into the
+// bf16 tile of the integers the MMA reads ([128 rows][64], 128-byte swizzle: the 16-byte chunk j of
+// row r sits at chunk j ^ (r % 8)).  Packing: a 32-bit word holds 8 consecutive k elements; nibble s
+// of the low half is element 2s and nibble s of the high half element 2s + 1, each stored as
+// code + 8.  (0x4300 | u) read as bf16 is 128 + u, so one mask-or per pair and one bf16x2
+// subtraction of 136 give two codes.  Thread ct of the kConvWarps * 32 converter threads takes
+// 16-byte pieces ct, ct + 64, ...: piece i is half i % 2 of row i / 2.
+__device__ __forceinline__ uint4 w4_bf16x8(uint32_t w) {
+    const __nv_bfloat162 off = __floats2bfloat162_rn(136.f, 136.f);
+    uint32_t r[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const uint32_t b = ((w >> (4 * s)) & 0x000F000Fu) | 0x43004300u;
+        const __nv_bfloat162 h = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&b), off);
+        r[s] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+__device__ __forceinline__ void convert_w4_kblock(uint32_t raw, uint32_t dst, int ct) {
+#pragma unroll
+    for (int i = 0; i < (kBM * 2) / (kConvWarps * 32); ++i) {
+        const int idx = ct + i * kConvWarps * 32;
+        const int r = idx >> 1, h = idx & 1;
+        const uint4 w = lds_u128(raw + (uint32_t)idx * 16);
+        const uint32_t row = dst + (uint32_t)r * 128;
+        const uint32_t sw = (uint32_t)(r & 7);
+        sts_u128(row + (((uint32_t)(4 * h + 0) ^ sw) << 4), w4_bf16x8(w.x));
+        sts_u128(row + (((uint32_t)(4 * h + 1) ^ sw) << 4), w4_bf16x8(w.y));
+        sts_u128(row + (((uint32_t)(4 * h + 2) ^ sw) << 4), w4_bf16x8(w.z));
+        sts_u128(row + (((uint32_t)(4 * h + 3) ^ sw) << 4), w4_bf16x8(w.w));
+    }
+}
+
+// 8 bf16 of B against 8 fp32 t values
+__device__ __forceinline__ float dot8_b(uint4 b, const float *t) {
+    float a0 = bf16lo(b.x) * t[0], a1 = bf16hi(b.x) * t[1];
+    a0 = fmaf(bf16lo(b.y), t[2], a0);
+    a1 = fmaf(bf16hi(b.y), t[3], a1);
+    a0 = fmaf(bf16lo(b.z), t[4], a0);
+    a1 = fmaf(bf16hi(b.z), t[5], a1);
+    a0 = fmaf(bf16lo(b.w), t[6], a0);
+    a1 = fmaf(bf16hi(b.w), t[7], a1);
+    return a0 + a1;
+}
+// 8 int8 codes of B against 8 fp32 t values (the int8 scales are already folded into t)
+__device__ __forceinline__ float dot8_b(uint2 b, const float *t) {
+    const float4 lo = i8x4(b.x), hi = i8x4(b.y);
+    float a0 = lo.x * t[0], a1 = lo.y * t[1];
+    a0 = fmaf(lo.z, t[2], a0);
+    a1 = fmaf(lo.w, t[3], a1);
+    a0 = fmaf(hi.x, t[4], a0);
+    a1 = fmaf(hi.y, t[5], a1);
+    a0 = fmaf(hi.z, t[6], a0);
+    a1 = fmaf(hi.w, t[7], a1);
+    return a0 + a1;
+}
+
+
+// W4: the base weights are int4 codes with one fp32 scale per output row ("12. Adapter Serving and
+// Multi-Tenant Customization", section "Quantization": an INT4 base dequantised in the kernel,
+// BF16 adapters, wide accumulation).  The codes enter the MMA as exact bf16 integers and the drain
+// multiplies the accumulator by the row's scale.
+template <bool W4>
+__global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_gemm_kernel(const __grid_constant__ DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ DecShared dsh;
+    __shared__ int32_t perm_s[LORA_MAX_DECODE_ROWS];
+    __shared__ int s_last;
+    const int S = p.n_stages;
+    // Ring slot and round of fill k without an integer division in the loops:
+    // k / S = umulhi(k, ceil(2^32 / S)), exact for k < 2^32 / 8 when S <= 8.
+    const uint32_t ring_m = 0xFFFFFFFFu / (uint32_t)S + 1u;
+    auto rround = [ring_m](uint32_t kk) -> uint32_t { return __umulhi(kk, ring_m); };
+    auto rslot = [ring_m, S](uint32_t kk) -> uint32_t { return kk - __umulhi(kk, ring_m) * (uint32_t)S; };
+    const int nt = p.nt;
+    const uint32_t a_bytes = kBM * kBK * 2;            // W or A tile of one k-block (bf16)
+    const uint32_t x_bytes = (uint32_t)nt * kBK * 2;   // x tile of one k-block
+    const uint32_t stage_bytes = a_bytes + x_bytes + (W4 ? (uint32_t)kW4RawBytes : 0u);
+    const uint32_t w_fill = W4 ? (uint32_t)kW4RawBytes : a_bytes;  // bytes of W one fill brings
+    const uint64_t wait_ns = p.wait_ns;
+    // Every fill (W or A k-block) completes one phase of its slot's wfull, so the phase of fill k
+    // is round(k) & 1 for every waiter; with an int4 base the converters arrive on cfull for every
+    // fill (converting W ones), and the MMA waits on cfull instead.
+    uint64_t *wfull = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);
+    uint64_t *cfull = wfull + S;
+    uint64_t *empty = cfull + S;
+    uint64_t *acc_full = empty + S;
+    uint64_t *acc_free = acc_full + 2;
+    uint64_t *mma_done = acc_free + 2;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(mma_done + 1);  // [0] tmem, [1] abort
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(wfull + s, 1);
+            mbar_init(cfull + s, kConvWarps * 32);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_free + b, kEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int m = 0; m < p.n_mod; ++m) {
+            tma_prefetch_desc(&p.mod[m].tmW);
+            tma_prefetch_desc(&p.mod[m].tmX);
+            if (p.shrink_tc) tma_prefetch_desc(&p.mod[m].tmA);
+        }
+    }
+    if (warp == 1) tmem_alloc(misc, (uint32_t)p.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = misc[0];
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    const uint64_t pol_w = l2_policy_evict_first();  // W and A: read once per call
+    const uint64_t pol_x = l2_policy_evict_last();   // x: read by every tile
+
+    // Before griddepcontrol.wait: L2 prefetches of the CTA's first W k-blocks.  W is the caller's
+    // weight and no kernel of this library writes it, so HBM can be busy with it while the
+    // previous kernel (the row plan, the previous call's finalize) drains; x, the gather list and
+    // the workspace are touched only after the wait.
+    if (warp == 0 && lane == 0) {
+        DSched sc;
+        sc.begin_w(p, blockIdx.x);
+        DItem it;
+        uint32_t nf = 0;
+        while (nf < kPreL2 && sc.next(p, nullptr, it)) {
+            const DecodeModule &M = p.mod[it.m];
+            for (int kb = it.kb0; kb < it.kb1 && nf < kPreL2; ++kb, ++nf)
+                tma_prefetch_2d(&M.tmW, W4 ? kb * (kBK / 2) : kb * kBK, it.tile * kBM);
+        }
+    }
+    grid_dep_wait();
+    // The finalize may launch now.  Every kernel before this one has completed, so the finalize
+    // may read the row plan (and the factors) before its own wait; it waits for this grid before
+    // reading anything this grid writes.
+    if (threadIdx.x == 0) grid_dep_launch();
+    if (threadIdx.x == 32) dec_a_space(p, dsh);
+    for (int q = threadIdx.x; q < p.n; q += blockDim.x) perm_s[q] = p.perm[q];
+    __syncthreads();
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer (warp)
+        DSched sc;
+        sc.begin(p, blockIdx.x, dsh);
+        DItem it;
+        uint32_t k = 0;  // stage fills issued
+        bool ok = true;
+        while (ok && sc.next(p, &dsh, it)) {
+            const DecodeModule &M = p.mod[it.m];
+            // A tile: lane l < 16 gathers group 16 tile + l (8 rows of one adapter's A)
+            int arow = 0;
+            bool mine = false;
+            uint32_t a_tx = 0;
+            if (it.a) {
+                const int g = it.tile * kTileGroups + lane;
+                mine = lane < kTileGroups && g < dsh.n_groups[it.m];
+                if (mine) arow = M.groups[g].row;
+                a_tx = (uint32_t)__popc(__ballot_sync(0xffffffffu, mine)) * (kGroupRows * kBK * 2);
+            }
+            for (int kb = it.kb0; kb < it.kb1; ++kb, ++k) {
+                const uint32_t sl = rslot(k);
+                uint8_t *sa = smem + (size_t)sl * stage_bytes;
+                {
+                    int got = 1;
+                    if (lane == 0) got = mbar_wait(empty + sl, (rround(k) & 1) ^ 1, abort_flag, p.err, wait_ns) ? 1 : 0;
+                    if (!__shfl_sync(0xffffffffu, got, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (it.a == 0) {
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(wfull + sl, w_fill + x_bytes);
+                            if (W4) tma_load_2d(sa + a_bytes + x_bytes, &M.tmW, wfull + sl, kb * (kBK / 2), it.tile * kBM, pol_w);
+                            else tma_load_2d(sa, &M.tmW, wfull + sl, kb * kBK, it.tile * kBM, pol_w);
+                        }
+                    } else {
+                        if (lane == 0) mbar_arrive_expect_tx(wfull + sl, a_tx + x_bytes);
+                        __syncwarp();
+                        if (mine) tma_load_2d(sa + lane * (kGroupRows * kBK * 2), &M.tmA, wfull + sl, kb * kBK, arow, pol_w);
+                    }
+                }
+                if (lane == 0) tma_load_2d(sa + a_bytes, &M.tmX, wfull + sl, kb * kBK, 0, pol_x);
+            }
+        }
+        // never leave the block with copies still landing in its shared memory: wait for the
+        // latest fill of every slot
+        const uint32_t issued = k;
+        if (lane == 0)
+            for (uint32_t q = 0; q < (uint32_t)S && q < issued; ++q) mbar_drain(wfull + q, ((issued - 1 - q) / (uint32_t)S) & 1u);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            const uint32_t idesc = idesc_bf16_f32(kBM, (uint32_t)nt);
+            DSched sc;
+            sc.begin(p, blockIdx.x, dsh);
+            DItem it;
+            uint32_t k = 0, li = 0;
+            bool ok = true;
+            while (ok && sc.next(p, &dsh, it)) {
+                const int buf = li & 1;
+                if (!mbar_wait(acc_free + buf, ((li >> 1) & 1) ^ 1, abort_flag, p.err, wait_ns)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(buf * nt);
+                for (int kb = it.kb0; kb < it.kb1; ++kb, ++k) {
+                    const uint32_t s = rslot(k);
+                    if (!mbar_wait((W4 ? cfull : wfull) + s, rround(k) & 1, abort_flag, p.err, wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+                    const uint64_t da = sdesc_kmajor_sw128(sa);
+                    const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        umma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, (kb > it.kb0 || kk > 0) ? 1u : 0u);
+                    umma_commit(empty + s);
+                }
+                if (!ok) break;
+                umma_commit(acc_full + buf);
+                ++li;
+            }
+            umma_commit(mma_done);
+            mbar_drain(mma_done, 0);
+        }
+    } else if (warp >= 2 && warp < 2 + kEpiWarps) {
+        // ---------------------------------------------------------------- epilogue
+        const int lane_base = (warp & 3) * 32;
+        const int o = lane_base + lane;  // TMEM lane = row of the tile
+        const uint32_t lane_off = (uint32_t)lane_base << 16;
+        const size_t slot_elems = (size_t)kBM * nt;
+        const int ncols16 = (p.n + 15) & ~15;
+        DSched sc;
+        sc.begin(p, blockIdx.x, dsh);
+        DItem it;
+        uint32_t li = 0;
+        while (sc.next(p, &dsh, it)) {
+            const int buf = li & 1;
+            const bool ok = mbar_wait(acc_full + buf, (li >> 1) & 1, abort_flag, p.err, wait_ns);
+            if (named_bar_or(1, 128, !ok)) break;
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + lane_off + (uint32_t)(buf * nt);
+            const DecodeModule &M = p.mod[it.m];
+            if (it.a == 0) {
+                // base piece -> its workspace slot
+                float *const piece = it.kb0 == 0 ? p.home + (size_t)(M.w_tile_begin + it.tile) * slot_elems
+                                                 : p.ctaw + (size_t)blockIdx.x * slot_elems;
+                const int orow = it.tile * kBM + o;
+                const float wsc = (W4 && orow < M.d_out) ? __ldg(M.w_scale + orow) : 1.f;
+                for (int c0 = 0; c0 < ncols16; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tacc + (uint32_t)c0, r);
+                    tmem_ld_wait();
+                    float4 *q = piece_quads(piece, c0, o);
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq)
+                        __stcg(q + kq * kBM, make_float4(__uint_as_float(r[4 * kq]) * wsc, __uint_as_float(r[4 * kq + 1]) * wsc,
+                                                         __uint_as_float(r[4 * kq + 2]) * wsc, __uint_as_float(r[4 * kq + 3]) * wsc));
+                }
+            } else {
+                // shrink piece: lane o is slot row 128 tile + o; only the columns of the rows whose
+                // adapter owns the slot row are kept (this CTA's part of their t values)
+                const int a_first = cta_of(it.it0, dsh.a_iters, dsh.a_ctas);
+                const int part = (int)blockIdx.x - a_first;
+                const size_t pstride = (size_t)p.tp_rows * LORA_MAX_RANK;
+                const int g = it.tile * kTileGroups + o / kGroupRows;  // this lane's group
+                const int ng = dsh.n_groups[it.m], kbn = M.k_blocks;
+                const bool gok = g < ng;
+                // the projection's pointers, copied out of the parameters before the stores below
+                float *const tpart = M.tpart, *const tfin = M.tfin;
+                const AGroup *const groups = M.groups;
+                int32_t *const acount = M.acount;
+                const float scale = p.scale;
+                for (int gg = 0; gg < 32 / kGroupRows; ++gg) {
+                    const int gw = it.tile * kTileGroups + (lane_base / kGroupRows) + gg;
+                    if (gw >= ng) break;  // warp-uniform
+                    const AGroup ag = groups[gw];
+                    const int r = ag.rbase + (lane & (kGroupRows - 1));
+                    const bool keep = (lane / kGroupRows) == gg && r < ag.rank;
+                    for (int q = ag.q0; q < ag.q1; ++q) {
+                        const int j = perm_s[q];
+                        const uint32_t v = tmem_ld1(tacc + (uint32_t)j);
+                        tmem_ld_wait();
+                        if (keep) tpart[part * pstride + (size_t)j * LORA_MAX_RANK + r] = __uint_as_float(v);
+                    }
+                }
+                // the tile's last CTA (a counter, no waiting) adds the parts in k order: t = s * sum
+                const int na = cta_of(it.it0 + kbn - 1, dsh.a_iters, dsh.a_ctas) - a_first + 1;
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (o == 0) s_last = atomicAdd(acount + it.tile, 1) == na - 1;
+                named_bar_sync(1, 128);
+                if (s_last) {
+                    __threadfence();
+                    if (gok) {
+                        const AGroup ag = groups[g];
+                        const int r = ag.rbase + (o & (kGroupRows - 1));
+                        if (r < ag.rank)
+                            for (int q = ag.q0; q < ag.q1; ++q) {
+                                const int j = perm_s[q];
+                                const float *tp = tpart + (size_t)j * LORA_MAX_RANK + r;
+                                float sum = 0.f;
+                                for (int cp = 0; cp < na; cp += 8) {  // eight parts' loads in flight, k order
+                                    float part[8];
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c) part[c] = cp + c < na ? __ldcg(tp + (cp + c) * pstride) : 0.f;
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c)
+                                        if (cp + c < na) sum = (cp + c == 0) ? part[c] : sum + part[c];
+                                }
+                                tfin[(size_t)j * LORA_MAX_RANK + r] = scale * sum;
+                            }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_free + buf);
+            ++li;
+        }
+    } else if (W4 && warp >= kConvWarp0) {
+        // ---------------------------------------------------------------- int4 converters
+        const int ct = threadIdx.x - 32 * kConvWarp0;
+        DSched sc;
+        sc.begin(p, blockIdx.x, dsh);
+        DItem it;
+        uint32_t k = 0;
+        bool ok = true;
+        while (ok && sc.next(p, &dsh, it)) {
+            for (int kb = it.kb0; kb < it.kb1; ++kb, ++k) {
+                const uint32_t s = rslot(k);
+                if (!mbar_wait(wfull + s, rround(k) & 1, abort_flag, p.err, wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (it.a == 0) {
+                    uint8_t *sa = smem + (size_t)s * stage_bytes;
+                    convert_w4_kblock(smem_u32(sa + a_bytes + x_bytes), smem_u32(sa), ct);
+                    fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
+                }
+                mbar_arrive(cfull + s);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+    }
+}
+
+template <bool I8>
+__global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_constant__ DecodeParams p) {
+    using BChunk = typename std::conditional<I8, uint2, uint4>::type;  // 8 elements of B
+    __shared__ __align__(16) float ts[kFinRows][LORA_MAX_RANK];
+    __shared__ __align__(16) BChunk sB[kFinRows][kBM];  // every row's first chunk of B, thread o at [k][o]
+    __shared__ RowInfo s_ri[kFinRows];
+    const int tid = threadIdx.x, tile = blockIdx.x, c0 = blockIdx.y * kFinRows;
+    int m = 0;
+    while (m + 1 < p.n_mod && p.mod[m + 1].w_tile_begin <= tile) ++m;
+    // the projection's fields, copied out of the parameters once: a runtime-indexed parameter is
+    // read through a generic pointer, which the compiler must reload after every store
+    const DecodeModule &Mp = p.mod[m];
+    const int w_tile_begin = Mp.w_tile_begin, k_blocks = Mp.k_blocks, d_out = Mp.d_out;
+    const int w_iter_begin = Mp.w_iter_begin, m_tiles = Mp.m_tiles;
+    const RowInfo *const rowinfo = Mp.rowinfo;
+    const float *const tfin = Mp.tfin;
+    const float *const Tm = Mp.T;
+    void *const yv_base = Mp.y;
+    const float *const home = p.home, *const ctaw = p.ctaw;
+    const int n = p.n, nt = p.nt, rpmax = p.rpmax, shrink_tc = p.shrink_tc, y_bf16 = p.y_bf16;
+    const int lt = tile - w_tile_begin;
+    if (lt >= m_tiles || c0 >= n) {
+        grid_dep_wait();
+        return;
+    }
+    const int orow = lt * kBM + tid;
+    const bool o_ok = orow < d_out;
+    // ---- before the gemm has finished: the rows' adapters (the row plan is complete: the gemm
+    // launched this grid only after its own wait) and every row's first chunk of B, in flight
+    if (tid < kFinRows) {
+        RowInfo ri{nullptr, 0, 0, -1};
+        if (c0 + tid < n) {
+            const uint4 raw = __ldcg(reinterpret_cast<const uint4 *>(rowinfo + c0 + tid));
+            ri = *reinterpret_cast<const RowInfo *>(&raw);
+        }
+        s_ri[tid] = ri;
+    }
+    __syncthreads();
+    if (o_ok) {  // copies that hold no registers while they fly
+#pragma unroll
+        for (int k = 0; k < kFinRows; ++k)
+            if (s_ri[k].rank > 0) {
+                const BChunk *src = reinterpret_cast<const BChunk *>(s_ri[k].B) + (size_t)orow * (s_ri[k].rp / 8);
+                if constexpr (I8) cp_async_8(smem_u32(&sB[k][tid]), src);
+                else cp_async_16cg(smem_u32(&sB[k][tid]), src);
+            }
+        cp_async_commit();
+    }
+    grid_dep_wait();
+    grid_dep_launch();
+    // the gemm is complete: its A-tile counters start the next call at zero (even after a call
+    // that gave up a wait)
+    if (blockIdx.x == 0 && blockIdx.y == 0 && shrink_tc)
+        for (int mm = 0; mm < p.n_mod; ++mm)
+            for (int i = tid; i < kDecMaxGroups / kTileGroups; i += kBM) p.mod[mm].acount[i] = 0;
+    // ---- after: t (thread: row jj, ranks tid % 8 + 8 i) and the tile's base pieces, in flight together
+    const int jj = tid >> 3, r8 = tid & 7, j = c0 + jj;
+    const RowInfo rj = s_ri[jj];
+    const float *trow = shrink_tc ? tfin + (size_t)j * LORA_MAX_RANK : Tm + (size_t)j * rpmax;
+    const float t8 = r8 < rj.rank ? __ldcg(trow + r8) : 0.f;
+    const size_t slot_elems = (size_t)kBM * nt;
+    const int it0 = w_iter_begin + lt * k_blocks;
+    const int c_first = cta_of(it0, p.w_iters, p.n_cta);
+    const int np = cta_of(it0 + k_blocks - 1, p.w_iters, p.n_cta) - c_first + 1;
+    float4 v4[4];
+    {
+        const float4 *q = piece_quads(home + (size_t)(w_tile_begin + lt) * slot_elems, c0, tid);
+        float4 f[2][4];
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) v4[kq] = __ldcg(q + kq * kBM);
+        for (int k = 1; k < np; k += 2) {  // later pieces two at a time, added in k order
+#pragma unroll
+            for (int w = 0; w < 2; ++w)
+                if (k + w < np) {
+                    const float4 *qq = piece_quads(ctaw + (size_t)(c_first + k + w) * slot_elems, c0, tid);
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq) f[w][kq] = __ldcg(qq + kq * kBM);
+                }
+#pragma unroll
+            for (int w = 0; w < 2; ++w)
+                if (k + w < np) {
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq) {
+                        v4[kq].x += f[w][kq].x;
+                        v4[kq].y += f[w][kq].y;
+                        v4[kq].z += f[w][kq].z;
+                        v4[kq].w += f[w][kq].w;
+                    }
+                }
+        }
+    }
+    ts[jj][r8] = t8;
+    for (int r = r8 + 8; r < rj.rp; r += 8) ts[jj][r] = r < rj.rank ? __ldcg(trow + r) : 0.f;
+    if (o_ok) cp_async_wait_all();
+    __syncthreads();
+    if (!o_ok) return;
+    // ---- expand and store (every index below is a compile-time constant: nothing goes through
+    // local memory, which the L1-light carve-out would send to L2)
+    const float v[kFinRows] = {v4[0].x, v4[0].y, v4[0].z, v4[0].w, v4[1].x, v4[1].y, v4[1].z, v4[1].w,
+                               v4[2].x, v4[2].y, v4[2].z, v4[2].w, v4[3].x, v4[3].y, v4[3].z, v4[3].w};
+    const int nrows = min(kFinRows, n - c0);
+    float out[kFinRows];
+#pragma unroll
+    for (int k = 0; k < kFinRows; ++k) {
+        float d = 0.f;
+        const RowInfo ri = s_ri[k];
+        if (ri.rank > 0) {
+            d = dot8_b(sB[k][tid], ts[k]);
+            const int nch = ri.rp / 8;
+            if (nch > 1) {
+                const BChunk *row = reinterpret_cast<const BChunk *>(ri.B) + (size_t)orow * nch;
+                for (int ch = 1; ch < nch; ++ch) d += dot8_b(__ldg(row + ch), ts[k] + 8 * ch);
+            }
+        }
+        out[k] = v[k] + d;
+    }
+    if (y_bf16) {
+        __nv_bfloat16 *yp = static_cast<__nv_bfloat16 *>(yv_base) + (size_t)c0 * d_out + orow;
+#pragma unroll
+        for (int k = 0; k < kFinRows; ++k)
+            if (k < nrows) yp[(size_t)k * d_out] = __float2bfloat16_rn(out[k]);
+    } else {
+        float *yp = static_cast<float *>(yv_base) + (size_t)c0 * d_out + orow;
+#pragma unroll
+        for (int k = 0; k < kFinRows; ++k)
+            if (k < nrows) yp[(size_t)k * d_out] = out[k];
+    }
+}
+
+// ====================================================================== launchers ==========
+
+static size_t decode_smem_bytes(int nt, int n_stages, bool w4) {
+    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2 + (w4 ? kW4RawBytes : 0);
+    return 1024 + stage * n_stages + 8 * (3 * (size_t)n_stages + 5) + 16;
+}
+
+bool plan_decode_gemm(DecodeParams &dp, size_t *smem_bytes) {
+    int cols = 32;
+    while (cols < 2 * dp.nt) cols <<= 1;  // two accumulators of nt columns
+    dp.tmem_cols = cols;
+    const bool w4 = dp.w4 != 0;
+    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)dp.nt * kBK * 2 + (w4 ? kW4RawBytes : 0);
+    // at most six stages: the rest of shared memory stays free for finalize blocks that wait beside
+    // the gemm's CTAs
+    const size_t budget = 227 * 1024 - 2048;  // static shared memory (perm copy, A space)
+    int s = (int)std::min<size_t>(6, (budget - decode_smem_bytes(dp.nt, 0, w4)) / stage);
+    dp.n_stages = s;
+    *smem_bytes = decode_smem_bytes(dp.nt, s, w4);
+    return s >= 2;
+}
+
+cudaError_t launch_prep_decode(const PrepParams &p, cudaStream_t s) {
+    return launch_pdl(prep_decode_kernel, dim3(1), dim3(256 * kPrepGroups), 0, s, p);
+}
+
+cudaError_t launch_decode_gemm(const DecodeParams &p, size_t smem_bytes, cudaStream_t s) {
+    static size_t configured[2] = {0, 0};
+    const int v = p.w4 ? 1 : 0;
+    void (*const kernels[2])(DecodeParams) = {decode_gemm_kernel<false>, decode_gemm_kernel<true>};
+    if (smem_bytes > configured[v]) {
+        cudaError_t e = cudaFuncSetAttribute(kernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+        if (e != cudaSuccess) return e;
+        configured[v] = smem_bytes;
+    }
+    return launch_pdl(kernels[v], dim3(p.n_cta), dim3(p.w4 ? kDecThreadsW4 : kDecThreads), smem_bytes, s, p);
+}
+
+cudaError_t launch_decode_finalize(const DecodeParams &p, cudaStream_t s) {
+    // The finalize's blocks land beside the gemm's CTAs (which hold most of shared memory), so
+    // they ask for the same split of the SM's memory between L1 and shared memory.
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_finalize_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_finalize_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const dim3 grid(p.w_tiles, (p.n + kFinRows - 1) / kFinRows);
+    if (p.i8) return launch_pdl(decode_finalize_kernel<true>, grid, dim3(kBM), 0, s, p);
+    return launch_pdl(decode_finalize_kernel<false>, grid, dim3(kBM), 0, s, p);
+}
+
+}  // namespace lora

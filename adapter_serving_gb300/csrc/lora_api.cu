@@ -89,6 +89,7 @@ struct ModuleStore {
     uint16_t *A = nullptr;  // [pages * 64, d_in] (bf16, or int8 codes in an int8 pool)
     uint16_t *B = nullptr;  // [pages * 64 * d_out] (rank-major runs of [d_out, rp])
     float *fold = nullptr;  // int8 pool: [pages * 64] scale of each stored row (A scale x B scale)
+    CUtensorMap tmA;        // bf16 pool: the A slab, box {64, 8} (the decode gemm's A-tile gathers)
     RowAllocator rows;
 };
 
@@ -194,21 +195,27 @@ struct lora_pool {
     // workspace
     int32_t *perm = nullptr, *seg_start = nullptr, *seg_adapter = nullptr, *n_seg = nullptr, *err = nullptr;
     int32_t *qadapter = nullptr;      // [max_rows] decode: adapter of each sorted position
-    float *T = nullptr;               // [LORA_MAX_MODULES][max_rows][64]
+    int32_t *radapter = nullptr;      // [256] decode: validated adapter of each row
+    float *T = nullptr;               // [LORA_MAX_MODULES][max_rows][64] CUDA-core shrink result
     float *shrink_part = nullptr;     // [LORA_MAX_MODULES][ks_cap][256][64]
     int32_t *shrink_cnt = nullptr;    // [LORA_MAX_MODULES][256]
-    float *gemm_part = nullptr;       // [num_sms][2][128 * 256]
-    BPackG *packs = nullptr;          // [LORA_MAX_MODULES][kMaxPacks] decode expand packs
-    int32_t *tpos = nullptr;          // [LORA_MAX_MODULES][256] decode: t row of each position
-    int32_t *n_packs = nullptr;       // [LORA_MAX_MODULES]
-    float *Tp = nullptr;              // [LORA_MAX_MODULES][kPackedTFloats] decode: packed t
+    AGroup *groups = nullptr;         // [LORA_MAX_MODULES][kDecMaxGroups] decode: A gather lists
+    int32_t *n_groups = nullptr;      // [LORA_MAX_MODULES]
+    RowInfo *rowinfo = nullptr;       // [LORA_MAX_MODULES][256] decode: each row's adapter (B, rank, slot)
+    float *tpart = nullptr;           // [LORA_MAX_MODULES][kDecMaxParts][tp_rows][64] t partial sums
+    float *tfin = nullptr;            // [LORA_MAX_MODULES][tp_rows][64] decode t
+    int32_t *acount = nullptr;        // [LORA_MAX_MODULES][kDecMaxGroups / 16] A-tile completion counters
+    float *home = nullptr;            // [w_tiles_cap][128 * nt_cap] decode base pieces from k-block 0
+    float *ctaw = nullptr;            // [num_sms][128 * nt_cap] decode base pieces from inside a tile
+    int tp_rows = 0, nt_cap = 0, w_tiles_cap = 0;
+    uint64_t wait_ns = kWaitBudgetNs;  // budget of one in-kernel wait
     int32_t *chunk_seg0 = nullptr;    // [chunk_cap] grouped rows: first segment of each chunk
     int32_t *chunk_nb = nullptr;      // [chunk_cap] grouped rows: expand slots of each chunk
     int chunk_cap = 0;
     int ks_cap = 0;
     // kernel timing: pending event pairs per kernel kind
     bool profiling = false;
-    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> prof_pending[3];
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> prof_pending[4];
     std::vector<cudaEvent_t> prof_free;
     int last_n = 0;                   // rows of the most recent forward
     bool last_decode = false;
@@ -325,28 +332,48 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
     p->ks_cap = (max_din + 511) / 512;
     const size_t R = (size_t)p->max_rows;
     p->chunk_cap = (int)(R / 256 + 2);  // row chunks of 256 (grouped rows)
+    const int dec_rows = std::min(p->max_rows, LORA_MAX_DECODE_ROWS);
+    p->tp_rows = dec_rows;
+    p->nt_cap = (dec_rows + 15) & ~15;
+    p->w_tiles_cap = 0;
+    for (int m = 0; m < p->n_modules; ++m) p->w_tiles_cap += (p->mod[m].d_out + kBM - 1) / kBM;
+    const size_t piece = (size_t)kBM * p->nt_cap * 4;
     if ((rc = dev_alloc(p, (void **)&p->perm, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->seg_start, (R + 2) * 4)) ||
         (rc = dev_alloc(p, (void **)&p->seg_adapter, (R + 1) * 4)) || (rc = dev_alloc(p, (void **)&p->n_seg, 16)) ||
         (rc = dev_alloc(p, (void **)&p->qadapter, (R + 1) * 4)) ||
+        (rc = dev_alloc(p, (void **)&p->radapter, (size_t)LORA_MAX_DECODE_ROWS * 4)) ||
         (rc = dev_alloc(p, (void **)&p->err, 16)) ||
         (rc = dev_alloc(p, (void **)&p->T, (size_t)LORA_MAX_MODULES * R * LORA_MAX_RANK * 4)) ||
         (rc = dev_alloc(p, (void **)&p->shrink_part,
                         (size_t)LORA_MAX_MODULES * p->ks_cap * LORA_MAX_DECODE_ROWS * LORA_MAX_RANK * 4)) ||
         (rc = dev_alloc(p, (void **)&p->shrink_cnt, (size_t)LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS * 4)) ||
-        (rc = dev_alloc(p, (void **)&p->gemm_part, (size_t)p->num_sms * 2 * kBM * 256 * 4)) ||
-        (rc = dev_alloc(p, (void **)&p->packs, sizeof(BPackG) * LORA_MAX_MODULES * kMaxPacks)) ||
-        (rc = dev_alloc(p, (void **)&p->tpos, (size_t)4 * LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS)) ||
-        (rc = dev_alloc(p, (void **)&p->n_packs, (size_t)4 * LORA_MAX_MODULES)) ||
-        (rc = dev_alloc(p, (void **)&p->Tp, (size_t)4 * LORA_MAX_MODULES * kPackedTFloats)) ||
+        (rc = dev_alloc(p, (void **)&p->groups, sizeof(AGroup) * LORA_MAX_MODULES * kDecMaxGroups)) ||
+        (rc = dev_alloc(p, (void **)&p->n_groups, (size_t)4 * LORA_MAX_MODULES)) ||
+        (rc = dev_alloc(p, (void **)&p->rowinfo, sizeof(RowInfo) * LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS)) ||
+        (rc = dev_alloc(p, (void **)&p->tpart,
+                        (size_t)4 * LORA_MAX_MODULES * kDecMaxParts * p->tp_rows * LORA_MAX_RANK)) ||
+        (rc = dev_alloc(p, (void **)&p->tfin, (size_t)4 * LORA_MAX_MODULES * p->tp_rows * LORA_MAX_RANK)) ||
+        (rc = dev_alloc(p, (void **)&p->acount, (size_t)4 * LORA_MAX_MODULES * (kDecMaxGroups / kTileGroups))) ||
+        (rc = dev_alloc(p, (void **)&p->home, piece * p->w_tiles_cap)) ||
+        (rc = dev_alloc(p, (void **)&p->ctaw, piece * p->num_sms)) ||
         (rc = dev_alloc(p, (void **)&p->chunk_seg0, (size_t)4 * p->chunk_cap)) ||
         (rc = dev_alloc(p, (void **)&p->chunk_nb, (size_t)4 * p->chunk_cap))) {
         lora_pool_destroy(p);
         return rc;
     }
+    // the decode gemm gathers A rows of a bf16 pool straight from the slab, 8 rows per box
+    for (int m = 0; m < p->n_modules && !p->i8; ++m) {
+        ModuleStore &ms = p->mod[m];
+        if (ms.pages > 0 && (rc = make_tmap(&ms.tmA, ms.A, (int64_t)ms.pages * LORA_PAGE_ROWS, ms.d_in, kGroupRows))) {
+            lora_pool_destroy(p);
+            return rc;
+        }
+    }
     cudaError_t e = cudaSuccess;
     if (e == cudaSuccess) e = cudaMemset(p->d_table, 0, tbytes);
     if (e == cudaSuccess) e = cudaMemset(p->err, 0, 16);
     if (e == cudaSuccess) e = cudaMemset(p->n_seg, 0, 16);
+    if (e == cudaSuccess) e = cudaMemset(p->acount, 0, (size_t)4 * LORA_MAX_MODULES * (kDecMaxGroups / kTileGroups));
     if (e == cudaSuccess) e = cudaMemset(p->shrink_cnt, 0, (size_t)LORA_MAX_MODULES * LORA_MAX_DECODE_ROWS * 4);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -595,6 +622,12 @@ static cudaError_t timed_launch(lora_pool *p, int kind, cudaStream_t s, F &&laun
     return e;
 }
 
+extern "C" int lora_pool_set_wait_budget(lora_pool *p, uint64_t budget_ns) {
+    if (!p) return LORA_EINVAL;
+    p->wait_ns = budget_ns ? budget_ns : kWaitBudgetNs;
+    return LORA_OK;
+}
+
 extern "C" int lora_profile_enable(lora_pool *p, int32_t enable) {
     if (!p) return LORA_EINVAL;
     p->profiling = enable != 0;
@@ -602,7 +635,7 @@ extern "C" int lora_profile_enable(lora_pool *p, int32_t enable) {
 }
 
 extern "C" int lora_profile_read(lora_pool *p, int32_t kind, int32_t *launches, double *total_ms) {
-    if (!p || kind < 0 || kind > 2) return LORA_EINVAL;
+    if (!p || kind < 0 || kind > 3) return LORA_EINVAL;
     LORA_CUDA(cudaSetDevice(p->device));
     LORA_CUDA(cudaDeviceSynchronize());
     double tot = 0;
@@ -621,8 +654,9 @@ extern "C" int lora_profile_read(lora_pool *p, int32_t kind, int32_t *launches, 
 
 // ------------------------------------------------------------------ forward ----------------
 
-// mode: kOwnGrouping (group the rows, then shrink and gemm), kBuildPlan (group the rows and build
-// the packs of every module of the pool, nothing else), kUsePlan (shrink and gemm on the last plan)
+// mode: kOwnGrouping (group the rows, then the call's kernels), kBuildPlan (group the rows and
+// build the gather lists of every module of the pool, nothing else), kUsePlan (the call's kernels
+// on the last plan)
 enum { kOwnGrouping = 0, kBuildPlan = 1, kUsePlan = 2 };
 
 // One projection as the forward sees it: lora_module_io, or lora_module_io_w4 (w_scale set).
@@ -633,6 +667,188 @@ struct IoDesc {
     const float *w_scale;
     void *y;
 };
+
+// Decode (n <= 256): prep (unless planned), the int8 shrink on CUDA cores (int8 pools), the gemm
+// (W tiles, and for bf16 pools the A tiles of the shrink), the finalize (expand, y).
+static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float scale, int y_dtype, cudaStream_t s,
+                       bool w4, const int *slot_of) {
+    cudaError_t e;
+    const int nt = (n + 15) & ~15;
+    const int rpmax = p->rpmax();
+    if (p->i8) {
+        ShrinkParams sp{};
+        sp.n_mod = n_io;
+        sp.n = n;
+        sp.rpmax = rpmax;
+        sp.by_segment = 1;
+        sp.max_units = LORA_MAX_DECODE_ROWS;
+        sp.ks_max = p->ks_cap;
+        sp.scale = scale;
+        sp.i8 = 1;
+        sp.perm = p->perm;
+        sp.qadapter = p->qadapter;
+        sp.partials = p->shrink_part;
+        sp.counters = p->shrink_cnt;
+        // split width: about 128 KiB of A codes per block, in whole 2048-wide steps
+        int kc_dec = kShrinkDecKC;
+        while (kc_dec * rpmax < 128 * 1024) kc_dec += kShrinkDecKC;
+        int splits = 0;
+        for (int i = 0; i < n_io; ++i) {
+            const ModuleStore &ms = p->mod[io[i].module];
+            sp.x[i] = static_cast<const uint16_t *>(io[i].x);
+            sp.table[i] = p->d_table + (size_t)io[i].module * p->max_adapters;
+            sp.fold[i] = ms.fold;
+            sp.T[i] = p->T + (size_t)slot_of[i] * p->max_rows * LORA_MAX_RANK;
+            sp.d_in[i] = ms.d_in;
+            sp.kc[i] = std::min(kc_dec, ms.d_in);
+            sp.ksplit[i] = (ms.d_in + sp.kc[i] - 1) / sp.kc[i];
+            if (sp.ksplit[i] > p->ks_cap) return LORA_EUNSUPPORTED;
+            sp.split_begin[i] = splits;
+            splits += sp.ksplit[i];
+        }
+        sp.split_begin[n_io] = splits;
+        e = timed_launch(p, LORA_KERNEL_SHRINK, s, [&] { return launch_shrink(sp, n, splits, s); });
+        if (e != cudaSuccess) return cuda_fail(e, "shrink kernel");
+    }
+
+    DecodeParams dp;
+    memset(&dp, 0, sizeof dp);
+    dp.n_mod = n_io;
+    dp.n = n;
+    dp.nt = nt;
+    dp.tp_rows = p->tp_rows;
+    dp.shrink_tc = p->i8 ? 0 : 1;
+    dp.w4 = w4 ? 1 : 0;
+    dp.i8 = p->i8 ? 1 : 0;
+    dp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
+    dp.rpmax = rpmax;
+    dp.scale = scale;
+    dp.perm = p->perm;
+    dp.radapter = p->radapter;
+    dp.home = p->home;
+    dp.ctaw = p->ctaw;
+    dp.err = p->err;
+    dp.wait_ns = p->wait_ns;
+    int iters = 0, tiles = 0;
+    for (int i = 0; i < n_io; ++i) {
+        const ModuleStore &ms = p->mod[io[i].module];
+        DecodeModule &dm = dp.mod[i];
+        int rc;
+        if (w4) {
+            rc = make_tmap_u8(&dm.tmW, io[i].W, ms.d_out, ms.d_in / 2, kBK / 2, kBM);
+            dm.w_scale = io[i].w_scale;
+        } else {
+            rc = make_tmap(&dm.tmW, io[i].W, ms.d_out, ms.d_in, kBM);
+        }
+        if (rc) return rc;
+        if ((rc = make_tmap(&dm.tmX, io[i].x, n, ms.d_in, nt))) return rc;
+        if (!p->i8) dm.tmA = ms.tmA;
+        const int sl = slot_of[i];
+        dm.groups = p->groups + (size_t)sl * kDecMaxGroups;
+        dm.n_groups = p->n_groups + sl;
+        dm.rowinfo = p->rowinfo + (size_t)sl * LORA_MAX_DECODE_ROWS;
+        dm.T = p->T + (size_t)sl * p->max_rows * LORA_MAX_RANK;
+        dm.tpart = p->tpart + (size_t)sl * kDecMaxParts * p->tp_rows * LORA_MAX_RANK;
+        dm.tfin = p->tfin + (size_t)sl * p->tp_rows * LORA_MAX_RANK;
+        dm.acount = p->acount + (size_t)sl * (kDecMaxGroups / kTileGroups);
+        dm.y = io[i].y;
+        dm.d_in = ms.d_in;
+        dm.d_out = ms.d_out;
+        dm.m_tiles = (ms.d_out + kBM - 1) / kBM;
+        dm.k_blocks = (ms.d_in + kBK - 1) / kBK;
+        dm.w_iter_begin = iters;
+        dm.w_tile_begin = tiles;
+        tiles += dm.m_tiles;
+        iters += dm.m_tiles * dm.k_blocks;
+    }
+    if (tiles > p->w_tiles_cap) return LORA_EUNSUPPORTED;  // a projection named twice in one call
+    dp.w_tiles = tiles;
+    dp.w_iters = iters;
+    // every CTA gets at least 4 k-blocks of the W space, so all its ranges are non-empty
+    dp.n_cta = std::max(1, std::min(p->num_sms, iters / 4));
+    size_t smem = 0;
+    if (!plan_decode_gemm(dp, &smem)) return LORA_EUNSUPPORTED;
+    e = timed_launch(p, LORA_KERNEL_GEMM, s, [&] { return launch_decode_gemm(dp, smem, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "gemm kernel");
+    e = timed_launch(p, LORA_KERNEL_FINALIZE, s, [&] { return launch_decode_finalize(dp, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "finalize kernel");
+    return LORA_OK;
+}
+
+// Grouped rows (n > 256, contiguous segments): prep, shrink, gemm with the expand in its ring.
+static int grouped_call(lora_pool *p, int n_io, const IoDesc *io, int n, float scale, int y_dtype, cudaStream_t s) {
+    cudaError_t e;
+    const int nt = 256;
+    const int rpmax = p->rpmax();
+    ShrinkParams sp{};
+    sp.n_mod = n_io;
+    sp.n = n;
+    sp.rpmax = rpmax;
+    sp.by_segment = 0;
+    sp.max_units = LORA_MAX_DECODE_ROWS;
+    sp.ks_max = p->ks_cap;
+    sp.scale = scale;
+    sp.seg_start = p->seg_start;
+    sp.seg_adapter = p->seg_adapter;
+    sp.n_seg = p->n_seg;
+    for (int i = 0; i < n_io; ++i) {
+        const ModuleStore &ms = p->mod[io[i].module];
+        sp.x[i] = static_cast<const uint16_t *>(io[i].x);
+        sp.table[i] = p->d_table + (size_t)io[i].module * p->max_adapters;
+        sp.T[i] = p->T + (size_t)i * p->max_rows * LORA_MAX_RANK;
+        sp.d_in[i] = ms.d_in;
+        sp.kc[i] = ms.d_in;
+        sp.ksplit[i] = 1;
+        sp.split_begin[i] = i;
+    }
+    sp.split_begin[n_io] = n_io;
+    const int units = (n + kShrinkGroupRows - 1) / kShrinkGroupRows;
+    e = timed_launch(p, LORA_KERNEL_SHRINK, s, [&] { return launch_shrink(sp, units, n_io, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "shrink kernel");
+
+    GemmParams gp;
+    memset(&gp, 0, sizeof gp);
+    gp.n_mod = n_io;
+    gp.n = n;
+    gp.nt = nt;
+    gp.n_chunks = (n + nt - 1) / nt;
+    gp.rpmax = rpmax;
+    gp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
+    gp.raster_group = 8;
+    gp.wait_ns = p->wait_ns;
+    int tiles = 0;
+    for (int i = 0; i < n_io; ++i) {
+        const ModuleStore &ms = p->mod[io[i].module];
+        GemmModule &gm = gp.mod[i];
+        int rc;
+        if ((rc = make_tmap(&gm.tmW, io[i].W, ms.d_out, ms.d_in, kBM))) return rc;
+        if ((rc = make_tmap(&gm.tmX, io[i].x, n, ms.d_in, nt))) return rc;
+        if ((rc = make_tmap_y(&gm.tmY, io[i].y, n, ms.d_out, y_dtype == LORA_DTYPE_BF16))) return rc;
+        gm.y = io[i].y;
+        gm.T = sp.T[i];
+        gm.table = sp.table[i];
+        gm.d_in = ms.d_in;
+        gm.d_out = ms.d_out;
+        gm.m_tiles = (ms.d_out + kBM - 1) / kBM;
+        gm.k_blocks = (ms.d_in + kBK - 1) / kBK;
+        gm.tile_begin = tiles;
+        tiles += gm.m_tiles * gp.n_chunks;
+    }
+    gp.total_tiles = tiles;
+    gp.n_cta = std::min(p->num_sms, tiles);
+    gp.chunk_seg0 = p->chunk_seg0;
+    gp.chunk_nb = p->chunk_nb;
+    gp.pf_ch = pf_ch(nt, rpmax);
+    size_t smem = 0;
+    if (!plan_gemm(gp, &smem)) return LORA_EUNSUPPORTED;
+    gp.seg_start = p->seg_start;
+    gp.seg_adapter = p->seg_adapter;
+    gp.n_seg = p->n_seg;
+    gp.err = p->err;
+    e = timed_launch(p, LORA_KERNEL_GEMM, s, [&] { return launch_gemm(gp, smem, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "gemm kernel");
+    return LORA_OK;
+}
 
 static int forward_impl(lora_pool *p, int n_io, const IoDesc *io, const int32_t *ids,
                         const int32_t *seg_start, const int32_t *seg_adapter, int n_seg, int n, float scale,
@@ -661,7 +877,7 @@ static int forward_impl(lora_pool *p, int n_io, const IoDesc *io, const int32_t 
     if (n == 0) return LORA_OK;  // empty batch: nothing to read or write
     for (int i = 0; mode != kBuildPlan && i < n_io; ++i) {
         const IoDesc &m = io[i];
-        if (m.module < 0 || m.module >= p->n_modules || !m.x || !m.W || !m.y) return LORA_EINVAL;
+        if (!m.x || !m.W || !m.y) return LORA_EINVAL;
         if (!aligned16(m.x) || !aligned16(m.W) || !aligned16(m.y)) return LORA_EINVAL;
         if (w4 && (!m.w_scale || (reinterpret_cast<uintptr_t>(m.w_scale) & 3))) return LORA_EINVAL;
         // int4 codes: a packed row (d_in / 2 bytes) is a whole number of 16-byte TMA strides
@@ -670,49 +886,46 @@ static int forward_impl(lora_pool *p, int n_io, const IoDesc *io, const int32_t 
     if (mode == kOwnGrouping && ids == nullptr && (!seg_start || !seg_adapter || n_seg < 1 || n_seg > n))
         return LORA_EINVAL;
     const bool decode = n <= LORA_MAX_DECODE_ROWS;
-    // the plan covers every module of the pool; a planned call finds module m's packs at slot m
-    const int n_prep = mode == kBuildPlan ? p->n_modules : n_io;
-    auto pool_module = [&](int i) { return mode == kBuildPlan ? i : io[i].module; };
-    auto slot = [&](int i) { return mode == kOwnGrouping ? i : pool_module(i); };
     if ((ids || p->i8 || w4) && !decode) return LORA_EUNSUPPORTED;
-    cudaError_t e;
+    // the plan covers every module of the pool; a planned call finds module m's lists at slot m
+    const int n_prep = mode == kBuildPlan ? p->n_modules : n_io;
+    int slot_of[LORA_MAX_MODULES];
+    for (int i = 0; i < n_prep; ++i) slot_of[i] = mode == kOwnGrouping ? i : (mode == kBuildPlan ? i : io[i].module);
+    auto pool_module = [&](int i) { return mode == kBuildPlan ? i : io[i].module; };
 
     // ---- prep: row grouping / checks
-    PrepParams pp{};
-    pp.ids = ids;
-    pp.seg_start_in = seg_start;
-    pp.seg_adapter_in = seg_adapter;
-    pp.n_seg_in = n_seg;
-    pp.n = n;
-    pp.max_adapters = p->max_adapters;
-    pp.n_mod = n_prep;
-    for (int i = 0; i < n_prep; ++i) pp.table[i] = p->d_table + (size_t)pool_module(i) * p->max_adapters;
-    pp.perm = p->perm;
-    pp.seg_start = p->seg_start;
-    pp.seg_adapter = p->seg_adapter;
-    pp.n_seg = p->n_seg;
-    pp.err = p->err;
-    pp.qadapter = p->qadapter;
-    const int nt = decode ? ((n + 15) & ~15) : 256;  // rows per MMA tile (MMA N)
-    const int rpmax = p->rpmax();
-    if (decode) {
-        for (int i = 0; i < n_prep; ++i) {
-            pp.packs[i] = p->packs + (size_t)slot(i) * kMaxPacks;
-            pp.tpos[i] = p->tpos + (size_t)slot(i) * LORA_MAX_DECODE_ROWS;
-        }
-        pp.n_packs = p->n_packs;
-        pp.pack_ranks = p->i8 ? kPackRanksI8 : kPackRanks;
-        pp.pack_ch = pack_ch(nt, pp.pack_ranks);
-    } else {
-        if ((n + nt - 1) / nt > p->chunk_cap) return LORA_EUNSUPPORTED;
-        pp.nt = nt;
-        pp.pf_ch = pf_ch(nt, rpmax);
-        pp.chunk_seg0 = p->chunk_seg0;
-        pp.chunk_nb = p->chunk_nb;
-    }
     if (mode != kUsePlan) {
-        e = timed_launch(p, LORA_KERNEL_PREP, s,
-                         [&] { return decode ? launch_prep_decode(pp, s) : launch_prep_segments(pp, s); });
+        PrepParams pp{};
+        pp.ids = ids;
+        pp.seg_start_in = seg_start;
+        pp.seg_adapter_in = seg_adapter;
+        pp.n_seg_in = n_seg;
+        pp.n = n;
+        pp.max_adapters = p->max_adapters;
+        pp.n_mod = n_prep;
+        for (int i = 0; i < n_prep; ++i) pp.table[i] = p->d_table + (size_t)pool_module(i) * p->max_adapters;
+        pp.perm = p->perm;
+        pp.seg_start = p->seg_start;
+        pp.seg_adapter = p->seg_adapter;
+        pp.n_seg = p->n_seg;
+        pp.err = p->err;
+        pp.qadapter = p->qadapter;
+        if (decode) {
+            pp.radapter = p->radapter;
+            pp.n_groups = p->n_groups;
+            for (int i = 0; i < n_prep; ++i) {
+                if (!p->i8) pp.groups[i] = p->groups + (size_t)slot_of[i] * kDecMaxGroups;
+                pp.rowinfo[i] = p->rowinfo + (size_t)slot_of[i] * LORA_MAX_DECODE_ROWS;
+            }
+        } else {
+            if ((n + 255) / 256 > p->chunk_cap) return LORA_EUNSUPPORTED;
+            pp.nt = 256;
+            pp.pf_ch = pf_ch(256, p->rpmax());
+            pp.chunk_seg0 = p->chunk_seg0;
+            pp.chunk_nb = p->chunk_nb;
+        }
+        cudaError_t e = timed_launch(p, LORA_KERNEL_PREP, s,
+                                     [&] { return decode ? launch_prep_decode(pp, s) : launch_prep_segments(pp, s); });
         if (e != cudaSuccess) return cuda_fail(e, "prep kernel");
         p->last_n = n;
         p->last_decode = decode;
@@ -722,121 +935,8 @@ static int forward_impl(lora_pool *p, int n_io, const IoDesc *io, const int32_t 
         p->plan_n = n;
         return LORA_OK;
     }
-
-    // ---- shrink: T[m][q][:] = s * A_a x_row(q)
-    ShrinkParams sp{};
-    sp.n_mod = n_io;
-    sp.n = n;
-    sp.rpmax = rpmax;
-    sp.by_segment = decode ? 1 : 0;
-    sp.max_units = LORA_MAX_DECODE_ROWS;
-    sp.ks_max = p->ks_cap;
-    sp.scale = scale;
-    sp.i8 = p->i8 ? 1 : 0;
-    sp.perm = decode ? p->perm : nullptr;
-    sp.seg_start = p->seg_start;
-    sp.seg_adapter = p->seg_adapter;
-    sp.n_seg = p->n_seg;
-    sp.qadapter = p->qadapter;
-    sp.partials = p->shrink_part;
-    sp.counters = p->shrink_cnt;
-    // decode split width: about 128 KiB of A per block, in whole 2048-wide steps
-    int kc_dec = kShrinkDecKC;
-    while (kc_dec * rpmax * (p->i8 ? 1 : 2) < 128 * 1024) kc_dec += kShrinkDecKC;
-    int splits = 0;
-    for (int i = 0; i < n_io; ++i) {
-        const ModuleStore &ms = p->mod[io[i].module];
-        sp.x[i] = static_cast<const uint16_t *>(io[i].x);
-        sp.table[i] = pp.table[i];
-        sp.fold[i] = ms.fold;
-        sp.T[i] = decode ? p->Tp + (size_t)i * kPackedTFloats : p->T + (size_t)i * p->max_rows * LORA_MAX_RANK;
-        sp.tpos[i] = decode ? pp.tpos[i] : nullptr;
-        sp.d_in[i] = ms.d_in;
-        sp.kc[i] = decode ? std::min(kc_dec, ms.d_in) : ms.d_in;
-        sp.ksplit[i] = (ms.d_in + sp.kc[i] - 1) / sp.kc[i];
-        sp.split_begin[i] = splits;
-        splits += sp.ksplit[i];
-    }
-    sp.split_begin[n_io] = splits;
-    const int units = decode ? n : (n + kShrinkGroupRows - 1) / kShrinkGroupRows;
-    e = timed_launch(p, LORA_KERNEL_SHRINK, s, [&] { return launch_shrink(sp, units, splits, s); });
-    if (e != cudaSuccess) return cuda_fail(e, "shrink kernel");
-
-    // ---- base + expand on tcgen05
-    GemmParams gp;
-    memset(&gp, 0, sizeof gp);
-    gp.n_mod = n_io;
-    gp.n = n;
-    gp.nt = nt;
-    gp.n_chunks = (n + gp.nt - 1) / gp.nt;
-    gp.decode = decode ? 1 : 0;
-    gp.stream_k = gp.n_chunks == 1 ? 1 : 0;
-    gp.rpmax = rpmax;
-    gp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
-    gp.i8 = p->i8 ? 1 : 0;
-    gp.w4 = w4 ? 1 : 0;
-    gp.raster_group = 8;
-    int64_t iters = 0;
-    int tiles = 0;
-    for (int i = 0; i < n_io; ++i) {
-        const ModuleStore &ms = p->mod[io[i].module];
-        GemmModule &gm = gp.mod[i];
-        int rc;
-        if (w4) {
-            rc = make_tmap_u8(&gm.tmW, io[i].W, ms.d_out, ms.d_in / 2, kBK / 2, kBM);
-            gm.w_scale = io[i].w_scale;
-        } else {
-            rc = make_tmap(&gm.tmW, io[i].W, ms.d_out, ms.d_in, kBM);
-        }
-        if (rc) return rc;
-        rc = make_tmap(&gm.tmX, io[i].x, n, ms.d_in, gp.nt);
-        if (rc) return rc;
-        rc = make_tmap_y(&gm.tmY, io[i].y, n, ms.d_out, y_dtype == LORA_DTYPE_BF16);
-        if (rc) return rc;
-        gm.y = io[i].y;
-        gm.T = sp.T[i];
-        gm.table = pp.table[i];
-        gm.packs = decode ? pp.packs[i] : nullptr;
-        gm.npk_index = slot(i);
-        gm.d_in = ms.d_in;
-        gm.d_out = ms.d_out;
-        gm.m_tiles = (ms.d_out + kBM - 1) / kBM;
-        gm.k_blocks = (ms.d_in + kBK - 1) / kBK;
-        gm.iter_begin = iters;
-        gm.tile_begin = tiles;
-        const int mt = gm.m_tiles * gp.n_chunks;
-        tiles += mt;
-        iters += (int64_t)mt * gm.k_blocks;
-    }
-    gp.total_tiles = tiles;
-    gp.total_iters = iters;
-    if (gp.stream_k) {
-        // every CTA gets at least 4 k-blocks, so all ranges are non-empty
-        gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(p->num_sms, iters / 4));
-    } else {
-        gp.n_cta = std::min(p->num_sms, tiles);
-    }
-    gp.n_packs = decode ? p->n_packs : nullptr;
-    gp.chunk_seg0 = decode ? nullptr : p->chunk_seg0;
-    gp.chunk_nb = decode ? nullptr : p->chunk_nb;
-    gp.pack_ch = pack_ch(nt, p->i8 ? kPackRanksI8 : kPackRanks);
-    gp.pf_ch = pf_ch(nt, rpmax);
-    size_t smem = 0;
-    if (!plan_gemm(gp, &smem)) return LORA_EUNSUPPORTED;
-    gp.perm = p->perm;
-    gp.seg_start = p->seg_start;
-    gp.seg_adapter = p->seg_adapter;
-    gp.n_seg = p->n_seg;
-    gp.partials = p->gemm_part;
-    gp.err = p->err;
-    // the decode gemm leaves split tiles to finalize_kernel (timed with it, as one gemm launch)
-    e = timed_launch(p, LORA_KERNEL_GEMM, s, [&] {
-        cudaError_t r = launch_gemm(gp, smem, s);
-        if (r == cudaSuccess && gp.stream_k) r = launch_finalize(gp, s);
-        return r;
-    });
-    if (e != cudaSuccess) return cuda_fail(e, "gemm kernel");
-    return LORA_OK;
+    return decode ? decode_call(p, n_io, io, n, scale, y_dtype, s, w4, slot_of)
+                  : grouped_call(p, n_io, io, n, scale, y_dtype, s);
 }
 
 namespace {

@@ -7,10 +7,10 @@
 // another framework whose allocation policy forbids raw device allocations.  Such callers also
 // keep their adapters in their own fixed buffers instead of in a lora_pool.  This entry point
 // serves them: the caller passes the inputs, the output and its stacked adapter factors, and
-// every piece of per-call scratch (row grouping, shrink result and partial sums, stream-K
-// partial tiles, counters, the factor table) lives in one file-scope device array, sized once,
-// that each GPU loading this library holds until the process exits.  It runs the same row
-// grouping, shrink and tcgen05 kernels as lora_linear_forward.
+// every piece of per-call scratch (row grouping, the A gather list, the shrink's partial t sums,
+// the base pieces of the stream-K split, the factor table) lives in one file-scope device array,
+// sized once, that each GPU loading this library holds until the process exits.  It runs the same
+// prep, tcgen05 gemm and finalize kernels as lora_linear_forward.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -28,30 +28,31 @@ namespace {
 
 // ---- limits of the static path and the scratch layout they imply -----------------------
 constexpr int kStMaxRows = 128;       // decode rows per call
-constexpr int kStMaxDin = 16384;      // shrink K splits: d_in / 2048 <= 8
-constexpr int kStMaxDout = 32768;     // stream-K tile counters: d_out / 128 <= 256
+constexpr int kStMaxDout = 16384;     // one base-piece slot per 128-row tile of W: d_out / 128 <= 128
 constexpr int kStMaxAdapters = 4096;  // factor table entries
-constexpr int kStMaxCta = 160;        // stream-K partial-tile slots
-constexpr int kStKsMax = kStMaxDin / kShrinkDecKC;
-constexpr int kStMaxUnits = LORA_MAX_DECODE_ROWS;  // shrink counter stride (one per segment)
+constexpr int kStMaxCta = 160;        // base pieces that start inside a tile: one slot per CTA
+constexpr int kStMaxTiles = kStMaxDout / kBM;
+constexpr int kStNt = kStMaxRows;     // MMA N for the largest batch
 
 constexpr size_t al(size_t v) { return (v + 255) & ~size_t(255); }
 constexpr size_t kOffTable = 0;
 constexpr size_t kOffPerm = al(kOffTable + sizeof(PoolEntry) * kStMaxAdapters);
-constexpr size_t kOffSegStart = al(kOffPerm + 4 * 256);
-constexpr size_t kOffSegAdapter = al(kOffSegStart + 4 * 272);
-constexpr size_t kOffNSeg = al(kOffSegAdapter + 4 * 256);
+constexpr size_t kOffSegStart = al(kOffPerm + 4 * (kStMaxRows + 1));
+constexpr size_t kOffSegAdapter = al(kOffSegStart + 4 * (kStMaxRows + 2));
+constexpr size_t kOffNSeg = al(kOffSegAdapter + 4 * (kStMaxRows + 1));
 constexpr size_t kOffQAdapter = al(kOffNSeg + 16);
-constexpr size_t kOffErr = al(kOffQAdapter + 4 * 256);                     // from here up to kOffT:
-constexpr size_t kOffShrinkCnt = al(kOffErr + 16);                // cleared at every call
-constexpr size_t kOffT = al(kOffShrinkCnt + 4 * kStMaxUnits);  // packed t of the expand
-constexpr size_t kOffPacks = al(kOffT + 4 * kPackedTFloats);
-constexpr size_t kOffTpos = al(kOffPacks + sizeof(BPackG) * kMaxPacks);
-constexpr size_t kOffNPacks = al(kOffTpos + 4 * LORA_MAX_DECODE_ROWS);
-constexpr size_t kOffShrinkPart = al(kOffNPacks + 16);
-constexpr size_t kOffGemmPart = al(kOffShrinkPart + 4 * (size_t)kStKsMax * kStMaxRows * LORA_MAX_RANK);
-constexpr size_t kStaticBytes = al(kOffGemmPart + 4 * (size_t)kStMaxCta * 2 * kBM * kStMaxRows);
-static_assert(kOffT % 256 == 0 && kOffShrinkPart % 256 == 0 && kOffGemmPart % 256 == 0, "alignment");
+constexpr size_t kOffRAdapter = al(kOffQAdapter + 4 * (kStMaxRows + 1));
+constexpr size_t kOffGroups = al(kOffRAdapter + 4 * (kStMaxRows + 1));
+constexpr size_t kOffNGroups = al(kOffGroups + sizeof(AGroup) * kStMaxRows * (LORA_MAX_RANK / kGroupRows));
+constexpr size_t kOffRowInfo = al(kOffNGroups + 16);
+constexpr size_t kOffErr = al(kOffRowInfo + sizeof(RowInfo) * kStMaxRows);  // cleared at every call
+constexpr size_t kOffTpart = al(kOffErr + 16);
+constexpr size_t kOffTfin = al(kOffTpart + 4 * (size_t)kDecMaxParts * kStMaxRows * LORA_MAX_RANK);
+constexpr size_t kOffACount = al(kOffTfin + 4 * (size_t)kStMaxRows * LORA_MAX_RANK);  // zero after every call
+constexpr size_t kOffHome = al(kOffACount + 4 * (size_t)(kDecMaxGroups / kTileGroups));
+constexpr size_t kOffCtaw = al(kOffHome + 4 * (size_t)kStMaxTiles * kBM * kStNt);
+constexpr size_t kStaticBytes = al(kOffCtaw + 4 * (size_t)kStMaxCta * kBM * kStNt);
+static_assert(kOffTpart % 256 == 0 && kOffHome % 256 == 0 && kOffCtaw % 256 == 0, "alignment");
 static_assert(kStaticBytes <= (24u << 20), "the static scratch stays at most 24 MiB");
 
 }  // namespace
@@ -70,7 +71,7 @@ __global__ void static_table_kernel(PoolEntry *table, const uint16_t *A, const u
                                     int rank, int d_in, int d_out) {
     const int a = blockIdx.x * blockDim.x + threadIdx.x;
     if (a < n_adapters)
-        table[a] = PoolEntry{A + (size_t)a * rank * d_in, B + (size_t)a * d_out * rank, rank, rank, 0};
+        table[a] = PoolEntry{A + (size_t)a * rank * d_in, B + (size_t)a * d_out * rank, rank, rank, (int64_t)a * rank};
 }
 
 // Returns `status` and leaves the reason where lora_last_cuda_error() reads it.
@@ -93,9 +94,8 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     if (d_in < 8 || d_out < 8 || d_in % 8 || d_out % 8) return fail(LORA_EINVAL, "d_in, d_out: multiples of 8");
     if (rank != 8 && rank != 16 && rank != 32 && rank != 64)
         return fail(LORA_EINVAL, "rank must be 8, 16, 32 or 64 (zero-pad other ranks)");
-    if (n > kStMaxRows || d_in > kStMaxDin || d_out > kStMaxDout || n_adapters < 0 || n_adapters > kStMaxAdapters)
-        return fail(LORA_EUNSUPPORTED, "exceeds the static scratch: n <= 128, d_in <= 16384, d_out <= 32768, "
-                                       "n_adapters <= 4096");
+    if (n > kStMaxRows || d_out > kStMaxDout || n_adapters < 0 || n_adapters > kStMaxAdapters)
+        return fail(LORA_EUNSUPPORTED, "exceeds the static scratch: n <= 128, d_out <= 16384, n_adapters <= 4096");
     const void *ptrs[] = {x, W, y, A_stack, B_stack};
     for (const void *ptr : ptrs)
         if (ptr && (reinterpret_cast<uintptr_t>(ptr) & 15)) return fail(LORA_EINVAL, "pointers: 16-byte aligned");
@@ -125,20 +125,13 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     }
     PoolEntry *table = reinterpret_cast<PoolEntry *>(scratch + kOffTable);
     int32_t *perm = reinterpret_cast<int32_t *>(scratch + kOffPerm);
-    int32_t *seg_start = reinterpret_cast<int32_t *>(scratch + kOffSegStart);
-    int32_t *seg_adapter = reinterpret_cast<int32_t *>(scratch + kOffSegAdapter);
-    int32_t *n_seg = reinterpret_cast<int32_t *>(scratch + kOffNSeg);
     int32_t *err = reinterpret_cast<int32_t *>(scratch + kOffErr);
-    int32_t *qadapter = reinterpret_cast<int32_t *>(scratch + kOffQAdapter);
-    float *T = reinterpret_cast<float *>(scratch + kOffT);
-    BPackG *packs = reinterpret_cast<BPackG *>(scratch + kOffPacks);
-    int32_t *tpos = reinterpret_cast<int32_t *>(scratch + kOffTpos);
-    int32_t *n_packs = reinterpret_cast<int32_t *>(scratch + kOffNPacks);
     const int nt = (n + 15) & ~15;
 
-    // the previous call leaves its contents behind: zero the counters and the error word
-    e = cudaMemsetAsync(scratch + kOffErr, 0, kOffT - kOffErr, s);
-    if (e != cudaSuccess) return fail(LORA_ECUDA, std::string("clear counters: ") + cudaGetErrorString(e));
+    // the previous call leaves its contents behind: clear the error word (everything else is
+    // written before it is read)
+    e = cudaMemsetAsync(scratch + kOffErr, 0, 16, s);
+    if (e != cudaSuccess) return fail(LORA_ECUDA, std::string("clear the error word: ") + cudaGetErrorString(e));
     if (n_adapters > 0) {
         static_table_kernel<<<(n_adapters + 127) / 128, 128, 0, s>>>(table, static_cast<const uint16_t *>(A_stack),
                                                                     static_cast<const uint16_t *>(B_stack),
@@ -154,88 +147,59 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     pp.n_mod = 1;
     pp.table[0] = table;
     pp.perm = perm;
-    pp.seg_start = seg_start;
-    pp.seg_adapter = seg_adapter;
-    pp.n_seg = n_seg;
+    pp.seg_start = reinterpret_cast<int32_t *>(scratch + kOffSegStart);
+    pp.seg_adapter = reinterpret_cast<int32_t *>(scratch + kOffSegAdapter);
+    pp.n_seg = reinterpret_cast<int32_t *>(scratch + kOffNSeg);
     pp.err = err;
-    pp.qadapter = qadapter;
-    pp.packs[0] = packs;
-    pp.tpos[0] = tpos;
-    pp.n_packs = n_packs;
-    pp.pack_ranks = kPackRanks;
-    pp.pack_ch = pack_ch(nt, kPackRanks);
+    pp.qadapter = reinterpret_cast<int32_t *>(scratch + kOffQAdapter);
+    pp.radapter = reinterpret_cast<int32_t *>(scratch + kOffRAdapter);
+    pp.groups[0] = reinterpret_cast<AGroup *>(scratch + kOffGroups);
+    pp.n_groups = reinterpret_cast<int32_t *>(scratch + kOffNGroups);
+    pp.rowinfo[0] = reinterpret_cast<RowInfo *>(scratch + kOffRowInfo);
     if ((e = launch_prep_decode(pp, s)) != cudaSuccess)
         return fail(LORA_ECUDA, std::string("prep kernel: ") + cudaGetErrorString(e));
 
-    const int rpmax = rank;
-    ShrinkParams sp{};
-    sp.n_mod = 1;
-    sp.n = n;
-    sp.rpmax = rpmax;
-    sp.by_segment = 1;
-    sp.max_units = kStMaxUnits;
-    sp.ks_max = kStKsMax;
-    sp.scale = scale;
-    sp.perm = perm;
-    sp.seg_start = seg_start;
-    sp.seg_adapter = seg_adapter;
-    sp.n_seg = n_seg;
-    sp.qadapter = qadapter;
-    sp.partials = reinterpret_cast<float *>(scratch + kOffShrinkPart);
-    sp.counters = reinterpret_cast<int32_t *>(scratch + kOffShrinkCnt);
-    sp.x[0] = static_cast<const uint16_t *>(x);
-    sp.table[0] = table;
-    sp.T[0] = T;
-    sp.tpos[0] = tpos;
-    sp.d_in[0] = d_in;
-    sp.kc[0] = std::min(kShrinkDecKC, d_in);
-    sp.ksplit[0] = (d_in + sp.kc[0] - 1) / sp.kc[0];
-    sp.split_begin[0] = 0;
-    sp.split_begin[1] = sp.ksplit[0];
-    if ((e = launch_shrink(sp, n, sp.ksplit[0], s)) != cudaSuccess)
-        return fail(LORA_ECUDA, std::string("shrink kernel: ") + cudaGetErrorString(e));
-
-    GemmParams gp;
-    memset(&gp, 0, sizeof gp);
-    gp.n_mod = 1;
-    gp.n = n;
-    gp.nt = nt;
-    gp.n_chunks = 1;
-    gp.decode = 1;
-    gp.stream_k = 1;
-    gp.rpmax = rpmax;
-    gp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
-    gp.raster_group = 8;
-    GemmModule &gm = gp.mod[0];
-    if (make_tmap(&gm.tmW, W, d_out, d_in, kBM) || make_tmap(&gm.tmX, x, n, d_in, gp.nt) ||
-        make_tmap_y(&gm.tmY, y, n, d_out, y_dtype == LORA_DTYPE_BF16))
+    DecodeParams dp;
+    memset(&dp, 0, sizeof dp);
+    dp.n_mod = 1;
+    dp.n = n;
+    dp.nt = nt;
+    dp.tp_rows = kStMaxRows;
+    dp.shrink_tc = 1;
+    dp.y_bf16 = y_dtype == LORA_DTYPE_BF16 ? 1 : 0;
+    dp.rpmax = rank;
+    dp.scale = scale;
+    dp.perm = perm;
+    dp.radapter = pp.radapter;
+    dp.home = reinterpret_cast<float *>(scratch + kOffHome);
+    dp.ctaw = reinterpret_cast<float *>(scratch + kOffCtaw);
+    dp.err = err;
+    dp.wait_ns = kWaitBudgetNs;
+    DecodeModule &dm = dp.mod[0];
+    // the stacked A factors are the slab the A tiles gather from: adapter a's rows start at a * rank
+    const int64_t a_rows = n_adapters > 0 ? (int64_t)n_adapters * rank : kGroupRows;
+    if (make_tmap(&dm.tmW, W, d_out, d_in, kBM) || make_tmap(&dm.tmX, x, n, d_in, nt) ||
+        make_tmap(&dm.tmA, n_adapters > 0 ? A_stack : W, a_rows, d_in, kGroupRows))
         return LORA_ECUDA;  // the reason is already recorded
-    gm.y = y;
-    gm.T = T;
-    gm.table = table;
-    gm.d_in = d_in;
-    gm.d_out = d_out;
-    gm.m_tiles = (d_out + kBM - 1) / kBM;
-    gm.k_blocks = (d_in + kBK - 1) / kBK;
-    gm.iter_begin = 0;
-    gm.tile_begin = 0;
-    gm.packs = packs;
-    gp.total_tiles = gm.m_tiles;
-    gp.total_iters = (int64_t)gm.m_tiles * gm.k_blocks;
-    gp.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, gp.total_iters / 4));
-    gp.n_packs = n_packs;
-    gp.pack_ch = pack_ch(nt, kPackRanks);
+    dm.groups = pp.groups[0];
+    dm.n_groups = pp.n_groups;
+    dm.rowinfo = pp.rowinfo[0];
+    dm.tpart = reinterpret_cast<float *>(scratch + kOffTpart);
+    dm.tfin = reinterpret_cast<float *>(scratch + kOffTfin);
+    dm.acount = reinterpret_cast<int32_t *>(scratch + kOffACount);
+    dm.y = y;
+    dm.d_in = d_in;
+    dm.d_out = d_out;
+    dm.m_tiles = (d_out + kBM - 1) / kBM;
+    dm.k_blocks = (d_in + kBK - 1) / kBK;
+    dp.w_tiles = dm.m_tiles;
+    dp.w_iters = dm.m_tiles * dm.k_blocks;
+    dp.n_cta = std::max(1, std::min(num_sms, dp.w_iters / 4));
     size_t smem = 0;
-    if (!plan_gemm(gp, &smem)) return fail(LORA_EUNSUPPORTED, "no two pipeline stages fit shared memory");
-    gp.perm = perm;
-    gp.seg_start = seg_start;
-    gp.seg_adapter = seg_adapter;
-    gp.n_seg = n_seg;
-    gp.partials = reinterpret_cast<float *>(scratch + kOffGemmPart);
-    gp.err = err;
-    if ((e = launch_gemm(gp, smem, s)) != cudaSuccess)
+    if (!plan_decode_gemm(dp, &smem)) return fail(LORA_EUNSUPPORTED, "no two pipeline stages fit shared memory");
+    if ((e = launch_decode_gemm(dp, smem, s)) != cudaSuccess)
         return fail(LORA_ECUDA, std::string("gemm kernel: ") + cudaGetErrorString(e));
-    if ((e = launch_finalize(gp, s)) != cudaSuccess)  // split tiles' pieces -> y
+    if ((e = launch_decode_finalize(dp, s)) != cudaSuccess)  // pieces + expand -> y
         return fail(LORA_ECUDA, std::string("finalize kernel: ") + cudaGetErrorString(e));
     return LORA_OK;
 }

@@ -7,9 +7,9 @@
 #include <cstdint>
 #include <cuda.h>
 
-namespace lora {
+#include "lora_internal.h"
 
-constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s: far above any legitimate wait
+namespace lora {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -61,21 +61,32 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity.  `abort_flag` (shared) lets one role
-// that gave up release the others quickly; `err` (global, may be null) records the timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int *err) {
+// Bounded wait for the phase with the given parity: gives up after `budget_ns` of wall-clock
+// time.  `abort_flag` (shared) lets one role that gave up release the others quickly; `err`
+// (global, may be null) records the timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err,
+                                          uint64_t budget_ns = kWaitBudgetNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait_sleep(a, parity, 20000)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitBudgetNs) {
+        if (globaltimer() - t0 > budget_ns) {
             *abort_flag = 1;
             if (err) atomicCAS(err, 0, 3 /* LORA_DEVERR_TIMEOUT */);
             return false;
         }
+    }
+}
+
+// Wait (bounded by kWaitBudgetNs, whatever the call's budget) for the phase of a barrier that
+// completes on its own: copies already issued, MMAs already committed.  A block never exits with
+// those still writing its shared memory or TMEM.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(a, parity) && globaltimer() - t0 < kWaitBudgetNs) {
     }
 }
 
@@ -106,6 +117,13 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, ui
         " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// L2 prefetch of the 2-D box {x: inner, y: outer} of a tensor map (no shared memory involved).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *tm, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+                 "r"(x), "r"(y)
+                 : "memory");
 }
 
 // 1-D bulk copy global -> shared (TMA engine), completing `bytes` of tx on `bar`.  Both
@@ -188,6 +206,14 @@ __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+// 8-byte global->shared copy (L2 only), full size.
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+// 16-byte global->shared copy through L2 only, full size.
+__device__ __forceinline__ void cp_async_16cg(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Wait until every cp.async this thread issued has landed.
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
@@ -231,6 +257,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+// 32 lanes x 1 column of 32-bit: thread t of the warp gets lane (base + t) of column c.
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
 }
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -298,5 +330,16 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Four signed bytes as floats, exactly: bias each code to 0..255 (xor 0x80), place it in the low
+// mantissa bits of 2^23 (byte permute), subtract 2^23 + 128.  Two full-rate operations per code.
+__device__ __forceinline__ float4 i8x4(uint32_t v) {
+    const uint32_t u = v ^ 0x80808080u;
+    constexpr float kBias = 8388736.0f;  // 2^23 + 128
+    return make_float4(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - kBias,
+                       __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - kBias,
+                       __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - kBias,
+                       __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - kBias);
+}
 
 }  // namespace lora

@@ -413,16 +413,35 @@ int lora_pool_last_segments(lora_pool *pool, int32_t *perm, int32_t *seg_start, 
 int lora_last_device_error(lora_pool *pool, int32_t *code, int32_t *detail);
 
 /*
+ * lora_pool_set_wait_budget -- the wall-clock budget of each bounded in-kernel wait of this pool's
+ * forwards (a wait for a TMA copy to land, for an MMA, for a free pipeline slot or accumulator).
+ * A wait that runs out records LORA_DEVERR_TIMEOUT in the device error word; the kernel stops
+ * issuing work, waits for the copies and MMAs it has already issued, frees its tensor memory and
+ * returns, so the context stays usable.  That call's outputs are undefined; later calls are not
+ * affected.  0 restores the default of 2 s, far above any legitimate wait.  A budget of a few
+ * microseconds makes a correct call give up: that is how the bounded waits are exercised without
+ * hanging or faulting a GPU.  Host-side setting, takes effect for forwards queued after it.
+ * Errors: EINVAL.
+ */
+int lora_pool_set_wait_budget(lora_pool *pool, uint64_t budget_ns);
+
+/*
  * Kernel timing.  While enabled, every forward on this pool records a CUDA event pair on its
- * stream around each kernel it launches (LORA_KERNEL_PREP: row grouping / checks,
- * LORA_KERNEL_SHRINK: t = s A x, LORA_KERNEL_GEMM: tcgen05 base + expand).
+ * stream around each kernel it launches:
+ *  LORA_KERNEL_PREP      row grouping / checks (and the decode gather lists)
+ *  LORA_KERNEL_SHRINK    t = s A x on CUDA cores (grouped rows; decode with int8 factors)
+ *  LORA_KERNEL_GEMM      tcgen05 base (decode: with the shrink's A tiles for bf16 factors;
+ *                        grouped rows: with the expand)
+ *  LORA_KERNEL_FINALIZE  decode: base pieces summed, the expand s B t, y written
  * lora_profile_read synchronizes, returns the number of launches and their summed device
  * time in milliseconds for one kind, and clears that kind.  Timing adds two event records
- * per launch; leave it off for throughput runs.  Errors: EINVAL, ECUDA.
+ * per launch and separates launches that otherwise overlap; leave it off for throughput
+ * runs.  Errors: EINVAL, ECUDA.
  */
 #define LORA_KERNEL_PREP 0
 #define LORA_KERNEL_SHRINK 1
 #define LORA_KERNEL_GEMM 2
+#define LORA_KERNEL_FINALIZE 3
 int lora_profile_enable(lora_pool *pool, int32_t enable);
 int lora_profile_read(lora_pool *pool, int32_t kernel, int32_t *launches, double *total_ms);
 
