@@ -426,6 +426,12 @@ __device__ __forceinline__ void convert_w4_kblock(uint32_t raw, uint32_t dst, in
     }
 }
 
+// two floats as a bf16x2 word (round to nearest even), the first in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 // 8 bf16 of B against 8 fp32 t values
 __device__ __forceinline__ float dot8_b(uint4 b, const float *t) {
     float a0 = bf16lo(b.x) * t[0], a1 = bf16hi(b.x) * t[1];
@@ -468,11 +474,21 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
     const uint32_t ring_m = 0xFFFFFFFFu / (uint32_t)S + 1u;
     auto rround = [ring_m](uint32_t kk) -> uint32_t { return __umulhi(kk, ring_m); };
     auto rslot = [ring_m, S](uint32_t kk) -> uint32_t { return kk - __umulhi(kk, ring_m) * (uint32_t)S; };
-    const int nt = p.nt;
-    const uint32_t a_bytes = kBM * kBK * 2;            // W or A tile of one k-block (bf16)
-    const uint32_t x_bytes = (uint32_t)nt * kBK * 2;   // x tile of one k-block
-    const uint32_t stage_bytes = a_bytes + x_bytes + (W4 ? (uint32_t)kW4RawBytes : 0u);
-    const uint32_t w_fill = W4 ? (uint32_t)kW4RawBytes : a_bytes;  // bytes of W one fill brings
+    const int nt = p.nt, kps = p.kps;
+    // A stage holds one k-step (kps k-blocks of 64): the W or A operand (kps blocks of [128][64]
+    // bf16), the x operand (kps blocks of [nt][64]), and with an int4 base the raw codes.  W
+    // sub-block q sits at q * 16 KiB; an A tile's group g (8 rows) at g * kps KiB, its sub-block q at
+    // + q KiB (so the 8-row atoms of one sub-block are kps KiB apart).
+    const uint32_t sub_a = kBM * kBK * 2, sub_x = (uint32_t)nt * kBK * 2;
+    const uint32_t a_bytes = (uint32_t)kps * sub_a;
+    const uint32_t x_bytes = (uint32_t)kps * sub_x;
+    const uint32_t stage_bytes = a_bytes + x_bytes + (W4 ? (uint32_t)(kps * kW4RawBytes) : 0u);
+    const uint32_t w_fill = W4 ? (uint32_t)(kps * kW4RawBytes) : a_bytes;  // bytes of W one fill brings
+    // one k-step's TMA box of a tensor map at (element or byte) column kx of k-step ks, row y
+    auto load = [kps](void *dst, const CUtensorMap *tm, uint64_t *bar, int ks, int kcols, int y, uint64_t pol) {
+        if (kps == 1) tma_load_2d(dst, tm, bar, ks * kcols, y, pol);
+        else tma_load_3d(dst, tm, bar, 0, y, ks * kps, pol);
+    };
     const uint64_t wait_ns = p.wait_ns;
     // Every fill (W or A k-block) completes one phase of its slot's wfull, so the phase of fill k
     // is round(k) & 1 for every waiter; with an int4 base the converters arrive on cfull for every
@@ -527,8 +543,10 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
         uint32_t nf = 0;
         while (nf < kPreL2 && sc.next(p, nullptr, it)) {
             const DecodeModule &M = p.mod[it.m];
-            for (int kb = it.kb0; kb < it.kb1 && nf < kPreL2; ++kb, ++nf)
-                tma_prefetch_2d(&M.tmW, W4 ? kb * (kBK / 2) : kb * kBK, it.tile * kBM);
+            for (int kb = it.kb0; kb < it.kb1 && nf < kPreL2; ++kb, ++nf) {
+                if (kps == 1) tma_prefetch_2d(&M.tmW, W4 ? kb * (kBK / 2) : kb * kBK, it.tile * kBM);
+                else tma_prefetch_3d(&M.tmW, 0, it.tile * kBM, kb * kps);
+            }
         }
     }
     grid_dep_wait();
@@ -557,7 +575,7 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 const int g = it.tile * kTileGroups + lane;
                 mine = lane < kTileGroups && g < dsh.n_groups[it.m];
                 if (mine) arow = M.groups[g].row;
-                a_tx = (uint32_t)__popc(__ballot_sync(0xffffffffu, mine)) * (kGroupRows * kBK * 2);
+                a_tx = (uint32_t)__popc(__ballot_sync(0xffffffffu, mine)) * (uint32_t)(kps * kGroupRows * kBK * 2);
             }
             for (int kb = it.kb0; kb < it.kb1; ++kb, ++k) {
                 const uint32_t sl = rslot(k);
@@ -572,16 +590,16 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                     if (it.a == 0) {
                         if (lane == 0) {
                             mbar_arrive_expect_tx(wfull + sl, w_fill + x_bytes);
-                            if (W4) tma_load_2d(sa + a_bytes + x_bytes, &M.tmW, wfull + sl, kb * (kBK / 2), it.tile * kBM, pol_w);
-                            else tma_load_2d(sa, &M.tmW, wfull + sl, kb * kBK, it.tile * kBM, pol_w);
+                            if (W4) load(sa + a_bytes + x_bytes, &M.tmW, wfull + sl, kb, kBK / 2, it.tile * kBM, pol_w);
+                            else load(sa, &M.tmW, wfull + sl, kb, kBK, it.tile * kBM, pol_w);
                         }
                     } else {
                         if (lane == 0) mbar_arrive_expect_tx(wfull + sl, a_tx + x_bytes);
                         __syncwarp();
-                        if (mine) tma_load_2d(sa + lane * (kGroupRows * kBK * 2), &M.tmA, wfull + sl, kb * kBK, arow, pol_w);
+                        if (mine) load(sa + lane * (kps * kGroupRows * kBK * 2), &M.tmA, wfull + sl, kb, kBK, arow, pol_w);
                     }
                 }
-                if (lane == 0) tma_load_2d(sa + a_bytes, &M.tmX, wfull + sl, kb * kBK, 0, pol_x);
+                if (lane == 0) load(sa + a_bytes, &M.tmX, wfull + sl, kb, kBK, 0, pol_x);
             }
         }
         // never leave the block with copies still landing in its shared memory: wait for the
@@ -611,11 +629,16 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-                    const uint64_t da = sdesc_kmajor_sw128(sa);
-                    const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes);
+                    for (int q = 0; q < kps; ++q) {
+                        // W: sub-block q at q * 16 KiB, 1 KiB atoms; A tile: at q KiB, atoms kps KiB apart
+                        const uint64_t da = it.a ? sdesc_kmajor_sw128(sa + (uint32_t)q * 1024u, (uint32_t)kps * 1024u)
+                                                 : sdesc_kmajor_sw128(sa + (uint32_t)q * sub_a);
+                        const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes + (uint32_t)q * sub_x);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        umma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, (kb > it.kb0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            umma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
+                                      (kb > it.kb0 || q > 0 || kk > 0) ? 1u : 0u);
+                    }
                     umma_commit(empty + s);
                 }
                 if (!ok) break;
@@ -737,7 +760,8 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 }
                 if (it.a == 0) {
                     uint8_t *sa = smem + (size_t)s * stage_bytes;
-                    convert_w4_kblock(smem_u32(sa + a_bytes + x_bytes), smem_u32(sa), ct);
+                    for (int q = 0; q < kps; ++q)
+                        convert_w4_kblock(smem_u32(sa + a_bytes + x_bytes + q * kW4RawBytes), smem_u32(sa + q * sub_a), ct);
                     fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
                 }
                 mbar_arrive(cfull + s);
@@ -848,7 +872,6 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     for (int r = r8 + 8; r < rj.rp; r += 8) ts[jj][r] = r < rj.rank ? __ldcg(trow + r) : 0.f;
     if (o_ok) cp_async_wait_all();
     __syncthreads();
-    if (!o_ok) return;
     // ---- expand and store (every index below is a compile-time constant: nothing goes through
     // local memory, which the L1-light carve-out would send to L2)
     const float v[kFinRows] = {v4[0].x, v4[0].y, v4[0].z, v4[0].w, v4[1].x, v4[1].y, v4[1].z, v4[1].w,
@@ -859,7 +882,7 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     for (int k = 0; k < kFinRows; ++k) {
         float d = 0.f;
         const RowInfo ri = s_ri[k];
-        if (ri.rank > 0) {
+        if (o_ok && ri.rank > 0) {
             d = dot8_b(sB[k][tid], ts[k]);
             const int nch = ri.rp / 8;
             if (nch > 1) {
@@ -869,24 +892,47 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
         }
         out[k] = v[k] + d;
     }
+    // y through shared memory (the B staging area, read by every thread above): each thread then
+    // writes 16-byte runs of one row, a warp 512 (fp32) or 256 (bf16) contiguous bytes per store
+    __syncthreads();
+    float(*ys)[kBM] = reinterpret_cast<float(*)[kBM]>(&sB[0][0]);
+#pragma unroll
+    for (int k = 0; k < kFinRows; ++k) ys[k][tid] = out[k];
+    __syncthreads();
+    const int o_base = lt * kBM;
     if (y_bf16) {
-        __nv_bfloat16 *yp = static_cast<__nv_bfloat16 *>(yv_base) + (size_t)c0 * d_out + orow;
+        // 16 rows x 16 runs of 8 outputs: two per thread
 #pragma unroll
-        for (int k = 0; k < kFinRows; ++k)
-            if (k < nrows) yp[(size_t)k * d_out] = __float2bfloat16_rn(out[k]);
+        for (int i = 0; i < 2; ++i) {
+            const int f = tid + kBM * i, k = f >> 4, c8 = (f & 15) * 8;
+            if (k < nrows && o_base + c8 < d_out) {
+                uint4 w;
+                w.x = pack_bf16x2(ys[k][c8], ys[k][c8 + 1]);
+                w.y = pack_bf16x2(ys[k][c8 + 2], ys[k][c8 + 3]);
+                w.z = pack_bf16x2(ys[k][c8 + 4], ys[k][c8 + 5]);
+                w.w = pack_bf16x2(ys[k][c8 + 6], ys[k][c8 + 7]);
+                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(yv_base) + (size_t)(c0 + k) * d_out + o_base + c8) = w;
+            }
+        }
     } else {
-        float *yp = static_cast<float *>(yv_base) + (size_t)c0 * d_out + orow;
+        // 16 rows x 32 runs of 4 outputs: four per thread
 #pragma unroll
-        for (int k = 0; k < kFinRows; ++k)
-            if (k < nrows) yp[(size_t)k * d_out] = out[k];
+        for (int i = 0; i < 4; ++i) {
+            const int f = tid + kBM * i, k = f >> 5, c4 = (f & 31) * 4;
+            if (k < nrows && o_base + c4 < d_out)
+                *reinterpret_cast<float4 *>(static_cast<float *>(yv_base) + (size_t)(c0 + k) * d_out + o_base + c4) =
+                    *reinterpret_cast<const float4 *>(&ys[k][c4]);
+        }
     }
 }
 
 // ====================================================================== launchers ==========
 
-static size_t decode_smem_bytes(int nt, int n_stages, bool w4) {
-    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2 + (w4 ? kW4RawBytes : 0);
-    return 1024 + stage * n_stages + 8 * (3 * (size_t)n_stages + 5) + 16;
+static size_t decode_stage_bytes(int nt, int kps, bool w4) {
+    return (size_t)kps * ((size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2 + (w4 ? kW4RawBytes : 0));
+}
+static size_t decode_smem_bytes(int nt, int kps, int n_stages, bool w4) {
+    return 1024 + decode_stage_bytes(nt, kps, w4) * n_stages + 8 * (3 * (size_t)n_stages + 5) + 16;
 }
 
 bool plan_decode_gemm(DecodeParams &dp, size_t *smem_bytes) {
@@ -894,13 +940,12 @@ bool plan_decode_gemm(DecodeParams &dp, size_t *smem_bytes) {
     while (cols < 2 * dp.nt) cols <<= 1;  // two accumulators of nt columns
     dp.tmem_cols = cols;
     const bool w4 = dp.w4 != 0;
-    const size_t stage = (size_t)kBM * kBK * 2 + (size_t)dp.nt * kBK * 2 + (w4 ? kW4RawBytes : 0);
-    // at most six stages: the rest of shared memory stays free for finalize blocks that wait beside
-    // the gemm's CTAs
+    const size_t stage = decode_stage_bytes(dp.nt, dp.kps, w4);
+    // at most six k-blocks of stages in flight
     const size_t budget = 227 * 1024 - 2048;  // static shared memory (perm copy, A space)
-    int s = (int)std::min<size_t>(6, (budget - decode_smem_bytes(dp.nt, 0, w4)) / stage);
+    int s = (int)std::min<size_t>(6 / dp.kps, (budget - decode_smem_bytes(dp.nt, dp.kps, 0, w4)) / stage);
     dp.n_stages = s;
-    *smem_bytes = decode_smem_bytes(dp.nt, s, w4);
+    *smem_bytes = decode_smem_bytes(dp.nt, dp.kps, s, w4);
     return s >= 2;
 }
 

@@ -89,7 +89,8 @@ struct ModuleStore {
     uint16_t *A = nullptr;  // [pages * 64, d_in] (bf16, or int8 codes in an int8 pool)
     uint16_t *B = nullptr;  // [pages * 64 * d_out] (rank-major runs of [d_out, rp])
     float *fold = nullptr;  // int8 pool: [pages * 64] scale of each stored row (A scale x B scale)
-    CUtensorMap tmA;        // bf16 pool: the A slab, box {64, 8} (the decode gemm's A-tile gathers)
+    CUtensorMap tmA[2];     // bf16 pool: the A slab for the decode gemm's A-tile gathers, box {64, 8}
+                            // ([0]: one k-block per box; [1]: two, when d_in % 64 == 0)
     RowAllocator rows;
 };
 
@@ -111,20 +112,36 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 }  // namespace
 
-// 2-D bf16 tensor [rows, cols] (row-major), box {64 cols, box_rows rows}, 128-byte swizzle.
-int lora::make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_rows) {
+// bf16 tensor [rows, cols] (row-major), 128-byte swizzle.  kps = 1: 2-D, box {64 cols, box_rows};
+// kps = 2 (cols a multiple of 64): the 3-D view {64, rows, cols / 64} (strides: row, 128 bytes), box
+// {64, box_rows, 2}: two consecutive k-blocks, each landing as a 2-D box would.
+int lora::make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_rows, int kps) {
     auto fn = encode_fn();
     if (!fn) {
         g_last_cuda_error = "cuTensorMapEncodeTiled unavailable";
         return LORA_ECUDA;
     }
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (kps == 1) {
+        cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+        r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        if (cols % 64 != 0) {
+            g_last_cuda_error = "two k-blocks per box need cols % 64 == 0";
+            return LORA_EINVAL;
+        }
+        cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+        cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+        cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)kps};
+        r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) {
         g_last_cuda_error = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
         return LORA_ECUDA;
@@ -132,22 +149,38 @@ int lora::make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t col
     return LORA_OK;
 }
 
-// Bytes [rows, cols] (row-major; int4 base codes, two per byte), box {box_cols, box_rows}, no
-// swizzle: the shared-memory side is a dense [box_rows][box_cols] block.  256-byte L2 promotion, so
-// a 32-byte box row still brings whole DRAM bursts into L2.
-int lora::make_tmap_u8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+// Bytes [rows, cols] (row-major; int4 base codes, two per byte), no swizzle: the shared-memory side
+// is a dense [box_rows][box_cols] block (kps = 2: two of them, for k-blocks kb and kb + 1, from the
+// 3-D view {box_cols, rows, cols / box_cols}).  256-byte L2 promotion, so a 32-byte box row still
+// brings whole DRAM bursts into L2.
+int lora::make_tmap_u8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_cols, int box_rows,
+                       int kps) {
     auto fn = encode_fn();
     if (!fn) {
         g_last_cuda_error = "cuTensorMapEncodeTiled unavailable";
         return LORA_ECUDA;
     }
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols};
-    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (kps == 1) {
+        cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)cols};
+        cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+        r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        if (cols % box_cols != 0) {
+            g_last_cuda_error = "two k-blocks per box need cols % box_cols == 0";
+            return LORA_EINVAL;
+        }
+        cuuint64_t dims[3] = {(cuuint64_t)box_cols, (cuuint64_t)rows, (cuuint64_t)(cols / box_cols)};
+        cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)box_cols};
+        cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, (cuuint32_t)kps};
+        r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) {
         g_last_cuda_error = "cuTensorMapEncodeTiled (int4 codes) failed (" + std::to_string((int)r) + ")";
         return LORA_ECUDA;
@@ -364,7 +397,9 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
     // the decode gemm gathers A rows of a bf16 pool straight from the slab, 8 rows per box
     for (int m = 0; m < p->n_modules && !p->i8; ++m) {
         ModuleStore &ms = p->mod[m];
-        if (ms.pages > 0 && (rc = make_tmap(&ms.tmA, ms.A, (int64_t)ms.pages * LORA_PAGE_ROWS, ms.d_in, kGroupRows))) {
+        const int64_t rows = (int64_t)ms.pages * LORA_PAGE_ROWS;
+        if (ms.pages > 0 && ((rc = make_tmap(&ms.tmA[0], ms.A, rows, ms.d_in, kGroupRows, 1)) ||
+                             (ms.d_in % 64 == 0 && (rc = make_tmap(&ms.tmA[1], ms.A, rows, ms.d_in, kGroupRows, 2))))) {
             lora_pool_destroy(p);
             return rc;
         }
@@ -729,20 +764,26 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
     dp.ctaw = p->ctaw;
     dp.err = p->err;
     dp.wait_ns = p->wait_ns;
+    // two k-blocks per pipeline stage (half the TMA requests, above all for the 8-row A gathers)
+    // when every projection's d_in is a whole number of k-blocks and the batch fills at most 128
+    // columns (a stage of a 256-row batch would leave only two in shared memory)
+    dp.kps = nt <= 128 ? 2 : 1;
+    for (int i = 0; i < n_io; ++i)
+        if (p->mod[io[i].module].d_in % 64 != 0) dp.kps = 1;
     int iters = 0, tiles = 0;
     for (int i = 0; i < n_io; ++i) {
         const ModuleStore &ms = p->mod[io[i].module];
         DecodeModule &dm = dp.mod[i];
         int rc;
         if (w4) {
-            rc = make_tmap_u8(&dm.tmW, io[i].W, ms.d_out, ms.d_in / 2, kBK / 2, kBM);
+            rc = make_tmap_u8(&dm.tmW, io[i].W, ms.d_out, ms.d_in / 2, kBK / 2, kBM, dp.kps);
             dm.w_scale = io[i].w_scale;
         } else {
-            rc = make_tmap(&dm.tmW, io[i].W, ms.d_out, ms.d_in, kBM);
+            rc = make_tmap(&dm.tmW, io[i].W, ms.d_out, ms.d_in, kBM, dp.kps);
         }
         if (rc) return rc;
-        if ((rc = make_tmap(&dm.tmX, io[i].x, n, ms.d_in, nt))) return rc;
-        if (!p->i8) dm.tmA = ms.tmA;
+        if ((rc = make_tmap(&dm.tmX, io[i].x, n, ms.d_in, nt, dp.kps))) return rc;
+        if (!p->i8) dm.tmA = ms.tmA[dp.kps - 1];
         const int sl = slot_of[i];
         dm.groups = p->groups + (size_t)sl * kDecMaxGroups;
         dm.n_groups = p->n_groups + sl;
@@ -755,7 +796,7 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
         dm.d_in = ms.d_in;
         dm.d_out = ms.d_out;
         dm.m_tiles = (ms.d_out + kBM - 1) / kBM;
-        dm.k_blocks = (ms.d_in + kBK - 1) / kBK;
+        dm.k_blocks = ((ms.d_in + kBK - 1) / kBK + dp.kps - 1) / dp.kps;  // k-steps
         dm.w_iter_begin = iters;
         dm.w_tile_begin = tiles;
         tiles += dm.m_tiles;

@@ -66,11 +66,15 @@ struct RowInfo {
 };
 static_assert(sizeof(RowInfo) == 16, "RowInfo layout");
 
+// Decode tensor maps cover kps 64-wide k-blocks per box (a "k-step", one pipeline stage).  With
+// kps = 1 they are 2-D ({k, row}); with kps = 2 they are 3-D views {64 elements, row, k-block}
+// (k-block stride 128 bytes), whose box {64, rows, 2} lands as two k-blocks one after the other,
+// each in the layout a 2-D box would give.
 struct DecodeModule {
-    CUtensorMap tmW;  // W [d_out, d_in] bf16, box {64, 128}, 128B swizzle; int4 base: codes
-                      // [d_out, d_in / 2] bytes, box {32, 128}, no swizzle
-    CUtensorMap tmX;  // x [n, d_in] bf16, box {64, nt}, 128B swizzle
-    CUtensorMap tmA;  // A slab [rows, d_in] bf16, box {64, 8}, 128B swizzle (bf16 factors)
+    CUtensorMap tmW;  // W [d_out, d_in] bf16, box {64, 128(, kps)}, 128B swizzle; int4 base: codes
+                      // [d_out, d_in / 2] bytes, box {32, 128(, kps)}, no swizzle
+    CUtensorMap tmX;  // x [n, d_in] bf16, box {64, nt(, kps)}, 128B swizzle
+    CUtensorMap tmA;  // A slab [rows, d_in] bf16, box {64, 8(, kps)}, 128B swizzle (bf16 factors)
     const float *w_scale;      // int4 base: [d_out] fp32 row scales
     const AGroup *groups;      // [kDecMaxGroups] this projection's gathered groups
     const int32_t *n_groups;   // device: number of groups
@@ -80,8 +84,9 @@ struct DecodeModule {
     float *tfin;               // [tp_rows][64] t = s * (sum of the parts), written by each A tile's last CTA
     int32_t *acount;           // [kDecMaxGroups / 16] CTAs done with each A tile (reset by the last one)
     void *y;
-    int32_t d_in, d_out, m_tiles, k_blocks;
-    int32_t w_iter_begin;      // first (W tile, k-block) index of this projection
+    int32_t d_in, d_out, m_tiles;
+    int32_t k_blocks;          // k-steps of a tile (kps k-blocks of 64 each)
+    int32_t w_iter_begin;      // first (W tile, k-step) index of this projection
     int32_t w_tile_begin;      // first W tile of this projection
 };
 
@@ -93,8 +98,9 @@ struct DecodeParams {
     int32_t tp_rows;      // row stride of tpart
     int32_t n_cta;
     int32_t n_stages;
+    int32_t kps;          // 64-wide k-blocks per pipeline stage (1 or 2)
     int32_t tmem_cols;
-    int32_t w_iters;      // W tile k-blocks of all projections (the W stream-K space)
+    int32_t w_iters;      // W tile k-steps of all projections (the W stream-K space)
     int32_t w_tiles;
     int32_t shrink_tc;    // 1: the shrink is the A tiles (bf16 factors); 0: t comes from T
     int32_t w4;
@@ -230,11 +236,12 @@ struct PrepParams {
 
 static_assert(sizeof(GemmParams) <= 32764, "gemm parameters exceed the kernel parameter space");
 
-// tensor maps (lora_api.cu): bf16 [rows, cols] operand, box {64, box_rows}, 128-byte swizzle; and
+// tensor maps (lora_api.cu): bf16 [rows, cols] operand, box {64, box_rows}, 128-byte swizzle (with
+// kps = 2: the 3-D view {64, rows, cols / 64}, box {64, box_rows, 2}); and
 // the output y [n, d_out] (fp32 or bf16), box {128, 16}, for the epilogue's TMA stores
-int make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_rows);
+int make_tmap(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_rows, int kps = 1);
 // bytes [rows, cols] (row-major), box {box_cols, box_rows}, no swizzle, 256-byte L2 promotion
-int make_tmap_u8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_cols, int box_rows);
+int make_tmap_u8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, int box_cols, int box_rows, int kps = 1);
 int make_tmap_y(CUtensorMap *tm, void *y, int64_t n, int64_t d_out, bool bf16);
 
 // launchers (lora_kernels.cu: grouped rows, shrink; decode_kernels.cu: decode)

@@ -176,10 +176,11 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     dp.err = err;
     dp.wait_ns = kWaitBudgetNs;
     DecodeModule &dm = dp.mod[0];
+    dp.kps = (d_in % 64 == 0) ? 2 : 1;  // two k-blocks per pipeline stage where d_in allows
     // the stacked A factors are the slab the A tiles gather from: adapter a's rows start at a * rank
     const int64_t a_rows = n_adapters > 0 ? (int64_t)n_adapters * rank : kGroupRows;
-    if (make_tmap(&dm.tmW, W, d_out, d_in, kBM) || make_tmap(&dm.tmX, x, n, d_in, nt) ||
-        make_tmap(&dm.tmA, n_adapters > 0 ? A_stack : W, a_rows, d_in, kGroupRows))
+    if (make_tmap(&dm.tmW, W, d_out, d_in, kBM, dp.kps) || make_tmap(&dm.tmX, x, n, d_in, nt, dp.kps) ||
+        make_tmap(&dm.tmA, n_adapters > 0 ? A_stack : W, a_rows, d_in, kGroupRows, dp.kps))
         return LORA_ECUDA;  // the reason is already recorded
     dm.groups = pp.groups[0];
     dm.n_groups = pp.n_groups;
@@ -191,7 +192,7 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     dm.d_in = d_in;
     dm.d_out = d_out;
     dm.m_tiles = (d_out + kBM - 1) / kBM;
-    dm.k_blocks = (d_in + kBK - 1) / kBK;
+    dm.k_blocks = ((d_in + kBK - 1) / kBK + dp.kps - 1) / dp.kps;  // k-steps
     dp.w_tiles = dm.m_tiles;
     dp.w_iters = dm.m_tiles * dm.k_blocks;
     dp.n_cta = std::max(1, std::min(num_sms, dp.w_iters / 4));

@@ -119,6 +119,22 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, ui
         : "memory");
 }
 
+// 3-D tiled load of box {x, y, z} into shared memory (dims in the tensor map's order),
+// completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, uint64_t *bar, int32_t x, int32_t y,
+                                            int32_t z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *tm, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // L2 prefetch of the 2-D box {x: inner, y: outer} of a tensor map (no shared memory involved).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *tm, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
@@ -290,13 +306,13 @@ __device__ __forceinline__ void tmem_st_wait() {
 // Shared-memory matrix descriptor: K-major operand staged by TMA with 128-byte swizzle
 // (rows of 64 bf16 = 128 B, 8-row atoms of 1024 B).  `saddr` must be 1024-byte aligned;
 // advancing K by 16 elements inside the atom adds 32 B to the start address.
-__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr, uint32_t atom_pitch = 1024) {
     uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);  // start address, 16-byte units
-    d |= (uint64_t)1 << 16;                   // leading byte offset (unused with this swizzle)
-    d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: 8-row atom pitch
-    d |= (uint64_t)1 << 46;                   // descriptor version for tcgen05
-    d |= (uint64_t)2 << 61;                   // 128-byte swizzle
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);   // start address, 16-byte units
+    d |= (uint64_t)1 << 16;                    // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(atom_pitch >> 4) << 32;    // stride byte offset: 8-row atom pitch
+    d |= (uint64_t)1 << 46;                    // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                    // 128-byte swizzle
     return d;
 }
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major, shape M x N.
