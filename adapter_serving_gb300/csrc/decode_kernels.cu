@@ -777,12 +777,53 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
     }
 }
 
+// Where chunk ch (8 B values) of output row o of a B tile sits in shared memory, in chunks from the
+// tile's start, for rows of nch chunks (nch = 1, 2, 4 or 8): the chunks of a row are XOR-rotated so
+// that 8 threads reading the same chunk of 8 consecutive rows hit 8 different 16-byte bank groups.
+__device__ __forceinline__ int bchunk_slot(int o, int ch, int nch) {
+    return o * nch + (ch ^ (((o * nch) >> 3) & (nch - 1)));
+}
+
+// The B tiles (output rows o_base .. o_base + tile_rows - 1) of the rows k0 .. k1 - 1 into `buf`,
+// every thread of the block copying consecutive chunks of each tile (coalesced), one cp.async group.
+// Out of line: the finalize is short-lived and starts cold, so its code is kept small.
 template <bool I8>
+__device__ __noinline__ void fin_stage(const RowInfo *s_ri, const int *s_off, int k0, int k1, uint8_t *buf,
+                                       int o_base, int tile_rows) {
+    using BChunk = typename std::conditional<I8, uint2, uint4>::type;
+    constexpr int cu = sizeof(BChunk);
+#pragma unroll 4
+    for (int k = k0; k < k1; ++k) {
+        const RowInfo ri = s_ri[k];
+        if (ri.rank <= 0) continue;
+        const int lg = __ffs(ri.rp >> 3) - 1, nch = 1 << lg;  // chunks per row: 1, 2, 4 or 8
+        const BChunk *src = reinterpret_cast<const BChunk *>(ri.B) + ((size_t)o_base << lg);
+        const uint32_t dst = smem_u32(buf + s_off[k]);
+        const int units = tile_rows << lg;
+        for (int u = threadIdx.x; u < units; u += kBM) {
+            const uint32_t d = dst + (uint32_t)bchunk_slot(u >> lg, u & (nch - 1), nch) * cu;
+            if constexpr (I8) cp_async_8(d, src + u);
+            else cp_async_16cg(d, src + u);
+        }
+    }
+    cp_async_commit();
+}
+
+// ONE: every B tile of the block fits one buffer (a single pass); the expand then runs fully unrolled
+// over the 16 rows with y in registers.  Otherwise passes through two buffers, y accumulating in
+// shared memory (compact code: the kernel is short-lived and starts with a cold instruction cache).
+template <bool I8, bool ONE>
 __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_constant__ DecodeParams p) {
     using BChunk = typename std::conditional<I8, uint2, uint4>::type;  // 8 elements of B
-    __shared__ __align__(16) float ts[kFinRows][LORA_MAX_RANK];
-    __shared__ __align__(16) BChunk sB[kFinRows][kBM];  // every row's first chunk of B, thread o at [k][o]
-    __shared__ RowInfo s_ri[kFinRows];
+    // B tile buffers (fin_nbuf of fin_buf bytes), y [16][128] (base, then + expand), t [16][rpmax],
+    // the rows' adapters, the pass plan
+    extern __shared__ __align__(16) uint8_t fsm[];
+    const int nbuf = p.fin_nbuf, buf_bytes = p.fin_buf, rpmax = p.rpmax;
+    float *ys = reinterpret_cast<float *>(fsm + (size_t)nbuf * buf_bytes);
+    float *ts = ys + kFinRows * kBM;
+    RowInfo *s_ri = reinterpret_cast<RowInfo *>(ts + kFinRows * rpmax);
+    int *s_off = reinterpret_cast<int *>(s_ri + kFinRows);  // [16] byte offset of row k's tile
+    int *s_pend = s_off + kFinRows;                        // [17] end row of pass i
     const int tid = threadIdx.x, tile = blockIdx.x, c0 = blockIdx.y * kFinRows;
     int m = 0;
     while (m + 1 < p.n_mod && p.mod[m + 1].w_tile_begin <= tile) ++m;
@@ -796,35 +837,49 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     const float *const Tm = Mp.T;
     void *const yv_base = Mp.y;
     const float *const home = p.home, *const ctaw = p.ctaw;
-    const int n = p.n, nt = p.nt, rpmax = p.rpmax, shrink_tc = p.shrink_tc, y_bf16 = p.y_bf16;
+    const int n = p.n, nt = p.nt, shrink_tc = p.shrink_tc, y_bf16 = p.y_bf16;
     const int lt = tile - w_tile_begin;
     if (lt >= m_tiles || c0 >= n) {
         grid_dep_wait();
         return;
     }
-    const int orow = lt * kBM + tid;
-    const bool o_ok = orow < d_out;
+    const int nrows = min(kFinRows, n - c0);
+    const int o_base = lt * kBM;
+    const bool o_ok = o_base + tid < d_out;
+    const int tile_rows = min(kBM, d_out - o_base);
     // ---- before the gemm has finished: the rows' adapters (the row plan is complete: the gemm
-    // launched this grid only after its own wait) and every row's first chunk of B, in flight
-    if (tid < kFinRows) {
+    // launched this grid only after its own wait), the pass plan, and the first passes' B tiles.
+    // Warp 0 plans in registers: lane k holds row k; passes are taken greedily in row order.
+    if (tid < 32) {
         RowInfo ri{nullptr, 0, 0, -1};
-        if (c0 + tid < n) {
+        if (tid < nrows) {
             const uint4 raw = __ldcg(reinterpret_cast<const uint4 *>(rowinfo + c0 + tid));
             ri = *reinterpret_cast<const RowInfo *>(&raw);
         }
-        s_ri[tid] = ri;
+        const int bytes = tid < nrows && ri.rank > 0 ? kBM * (ri.rp >> 3) * (int)sizeof(BChunk) : 0;
+        int used = 0, np = 0, off = 0;
+        for (int k = 0; k < nrows; ++k) {
+            const int b = __shfl_sync(0xffffffffu, bytes, k);
+            if (k > 0 && used + b > buf_bytes) {  // row k opens pass np + 1
+                if (tid == 0) s_pend[np] = k;
+                ++np;
+                used = 0;
+            }
+            if (tid == k) off = used;
+            used += b;
+        }
+        if (tid == 0) s_pend[np] = nrows;
+        if (tid > np && tid <= kFinRows) s_pend[tid] = -1;
+        if (tid < kFinRows) {
+            s_ri[tid] = ri;
+            s_off[tid] = off;
+        }
     }
     __syncthreads();
-    if (o_ok) {  // copies that hold no registers while they fly
-#pragma unroll
-        for (int k = 0; k < kFinRows; ++k)
-            if (s_ri[k].rank > 0) {
-                const BChunk *src = reinterpret_cast<const BChunk *>(s_ri[k].B) + (size_t)orow * (s_ri[k].rp / 8);
-                if constexpr (I8) cp_async_8(smem_u32(&sB[k][tid]), src);
-                else cp_async_16cg(smem_u32(&sB[k][tid]), src);
-            }
-        cp_async_commit();
-    }
+    int n_pass = 0;
+    while (n_pass < kFinRows && s_pend[n_pass] >= 0) ++n_pass;
+    for (int i = 0; i < min(nbuf, n_pass); ++i)
+        fin_stage<I8>(s_ri, s_off, i == 0 ? 0 : s_pend[i - 1], s_pend[i], fsm + (size_t)i * buf_bytes, o_base, tile_rows);
     grid_dep_wait();
     grid_dep_launch();
     // the gemm is complete: its A-tile counters start the next call at zero (even after a call
@@ -832,96 +887,133 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     if (blockIdx.x == 0 && blockIdx.y == 0 && shrink_tc)
         for (int mm = 0; mm < p.n_mod; ++mm)
             for (int i = tid; i < kDecMaxGroups / kTileGroups; i += kBM) p.mod[mm].acount[i] = 0;
-    // ---- after: t (thread: row jj, ranks tid % 8 + 8 i) and the tile's base pieces, in flight together
-    const int jj = tid >> 3, r8 = tid & 7, j = c0 + jj;
-    const RowInfo rj = s_ri[jj];
-    const float *trow = shrink_tc ? tfin + (size_t)j * LORA_MAX_RANK : Tm + (size_t)j * rpmax;
-    const float t8 = r8 < rj.rank ? __ldcg(trow + r8) : 0.f;
+    // ---- after: t (zero past each row's rank) and the tile's base pieces, all loads in flight
+    // together.  t: float4 e = tid, tid + 128 of [16 rows][rpmax / 4]
+    const int lq = __ffs(rpmax >> 2) - 1;  // log2(rpmax / 4)
+    float4 tv[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int e = tid + i * kBM, jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
+        tv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (jj < kFinRows && r < s_ri[jj].rank) {
+            const int j = c0 + jj;
+            const float *trow = shrink_tc ? tfin + (size_t)j * LORA_MAX_RANK : Tm + (size_t)j * rpmax;
+            tv[i] = __ldcg(reinterpret_cast<const float4 *>(trow + r));
+        }
+    }
     const size_t slot_elems = (size_t)kBM * nt;
     const int it0 = w_iter_begin + lt * k_blocks;
     const int c_first = cta_of(it0, p.w_iters, p.n_cta);
     const int np = cta_of(it0 + k_blocks - 1, p.w_iters, p.n_cta) - c_first + 1;
-    float4 v4[4];
+    // base: the columns c0 .. c0 + 15 of every piece (4 column quads per thread), added in k order
+    float4 v4[kFinRows / 4];
     {
         const float4 *q = piece_quads(home + (size_t)(w_tile_begin + lt) * slot_elems, c0, tid);
-        float4 f[2][4];
 #pragma unroll
-        for (int kq = 0; kq < 4; ++kq) v4[kq] = __ldcg(q + kq * kBM);
-        for (int k = 1; k < np; k += 2) {  // later pieces two at a time, added in k order
+        for (int kq = 0; kq < kFinRows / 4; ++kq) v4[kq] = __ldcg(q + kq * kBM);
+        for (int k = 1; k < np; ++k) {
+            const float4 *qq = piece_quads(ctaw + (size_t)(c_first + k) * slot_elems, c0, tid);
+            float4 f[kFinRows / 4];
 #pragma unroll
-            for (int w = 0; w < 2; ++w)
-                if (k + w < np) {
-                    const float4 *qq = piece_quads(ctaw + (size_t)(c_first + k + w) * slot_elems, c0, tid);
+            for (int kq = 0; kq < kFinRows / 4; ++kq) f[kq] = __ldcg(qq + kq * kBM);
 #pragma unroll
-                    for (int kq = 0; kq < 4; ++kq) f[w][kq] = __ldcg(qq + kq * kBM);
-                }
-#pragma unroll
-            for (int w = 0; w < 2; ++w)
-                if (k + w < np) {
-#pragma unroll
-                    for (int kq = 0; kq < 4; ++kq) {
-                        v4[kq].x += f[w][kq].x;
-                        v4[kq].y += f[w][kq].y;
-                        v4[kq].z += f[w][kq].z;
-                        v4[kq].w += f[w][kq].w;
-                    }
-                }
-        }
-    }
-    ts[jj][r8] = t8;
-    for (int r = r8 + 8; r < rj.rp; r += 8) ts[jj][r] = r < rj.rank ? __ldcg(trow + r) : 0.f;
-    if (o_ok) cp_async_wait_all();
-    __syncthreads();
-    // ---- expand and store (every index below is a compile-time constant: nothing goes through
-    // local memory, which the L1-light carve-out would send to L2)
-    const float v[kFinRows] = {v4[0].x, v4[0].y, v4[0].z, v4[0].w, v4[1].x, v4[1].y, v4[1].z, v4[1].w,
-                               v4[2].x, v4[2].y, v4[2].z, v4[2].w, v4[3].x, v4[3].y, v4[3].z, v4[3].w};
-    const int nrows = min(kFinRows, n - c0);
-    float out[kFinRows];
-#pragma unroll
-    for (int k = 0; k < kFinRows; ++k) {
-        float d = 0.f;
-        const RowInfo ri = s_ri[k];
-        if (o_ok && ri.rank > 0) {
-            d = dot8_b(sB[k][tid], ts[k]);
-            const int nch = ri.rp / 8;
-            if (nch > 1) {
-                const BChunk *row = reinterpret_cast<const BChunk *>(ri.B) + (size_t)orow * nch;
-                for (int ch = 1; ch < nch; ++ch) d += dot8_b(__ldg(row + ch), ts[k] + 8 * ch);
+            for (int kq = 0; kq < kFinRows / 4; ++kq) {
+                v4[kq].x += f[kq].x;
+                v4[kq].y += f[kq].y;
+                v4[kq].z += f[kq].z;
+                v4[kq].w += f[kq].w;
             }
         }
-        out[k] = v[k] + d;
     }
-    // y through shared memory (the B staging area, read by every thread above): each thread then
-    // writes 16-byte runs of one row, a warp 512 (fp32) or 256 (bf16) contiguous bytes per store
-    __syncthreads();
-    float(*ys)[kBM] = reinterpret_cast<float(*)[kBM]>(&sB[0][0]);
 #pragma unroll
-    for (int k = 0; k < kFinRows; ++k) ys[k][tid] = out[k];
+    for (int i = 0; i < 2; ++i) {
+        const int e = tid + i * kBM, jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
+        if (jj < kFinRows) {
+            const int rank = s_ri[jj].rank;
+            float4 v = tv[i];
+            if (r + 1 >= rank) v.y = 0.f;
+            if (r + 2 >= rank) v.z = 0.f;
+            if (r + 3 >= rank) v.w = 0.f;
+            *reinterpret_cast<float4 *>(ts + jj * rpmax + r) = v;
+        }
+    }
+    if constexpr (ONE) {
+        // ---- expand (every index into out[] is a compile-time constant: nothing goes through
+        // local memory, which the L1-light carve-out would send to L2)
+        const float v[kFinRows] = {v4[0].x, v4[0].y, v4[0].z, v4[0].w, v4[1].x, v4[1].y, v4[1].z, v4[1].w,
+                                   v4[2].x, v4[2].y, v4[2].z, v4[2].w, v4[3].x, v4[3].y, v4[3].z, v4[3].w};
+        cp_async_wait_all();
+        __syncthreads();  // the tiles and t visible to every thread
+        float out[kFinRows];
+#pragma unroll
+        for (int k = 0; k < kFinRows; ++k) {
+            float d = 0.f;
+            const RowInfo ri = s_ri[k];
+            if (o_ok && ri.rank > 0) {
+                const int nch = ri.rp >> 3;  // 1, or 2 for int8 rank 16
+                const BChunk *bk = reinterpret_cast<const BChunk *>(fsm + s_off[k]);
+                const float *tk = ts + k * rpmax;
+                d = dot8_b(bk[bchunk_slot(tid, 0, nch)], tk);
+                if (nch > 1) d += dot8_b(bk[bchunk_slot(tid, 1, nch)], tk + 8);
+            }
+            out[k] = v[k] + d;
+        }
+#pragma unroll
+        for (int k = 0; k < kFinRows; ++k) ys[k * kBM + tid] = out[k];
+    } else {
+#pragma unroll
+        for (int kq = 0; kq < kFinRows / 4; ++kq) {  // y column tid starts as the base
+            ys[(4 * kq) * kBM + tid] = v4[kq].x;
+            ys[(4 * kq + 1) * kBM + tid] = v4[kq].y;
+            ys[(4 * kq + 2) * kBM + tid] = v4[kq].z;
+            ys[(4 * kq + 3) * kBM + tid] = v4[kq].w;
+        }
+        // ---- expand, pass by pass: each thread adds B_a[o] . t to its own column of y
+        for (int i = 0; i < n_pass; ++i) {
+            if (i + 1 < n_pass) cp_async_wait_all_but_1();
+            else cp_async_wait_all();
+            __syncthreads();  // pass i's tiles (and, on the first pass, t) visible to every thread
+            const uint8_t *buf = fsm + (size_t)(i % nbuf) * buf_bytes;
+            if (o_ok)
+                for (int k = i == 0 ? 0 : s_pend[i - 1]; k < s_pend[i]; ++k) {
+                    const RowInfo ri = s_ri[k];
+                    if (ri.rank <= 0) continue;
+                    const int nch = ri.rp >> 3;
+                    const BChunk *bk = reinterpret_cast<const BChunk *>(buf + s_off[k]);
+                    const float *tk = ts + k * rpmax;
+                    float d = 0.f;
+                    for (int ch = 0; ch < nch; ++ch) d += dot8_b(bk[bchunk_slot(tid, ch, nch)], tk + 8 * ch);
+                    ys[k * kBM + tid] += d;
+                }
+            if (i + nbuf < n_pass) {
+                __syncthreads();  // every thread is done with this buffer
+                fin_stage<I8>(s_ri, s_off, s_pend[i + nbuf - 1], s_pend[i + nbuf], fsm + (size_t)(i % nbuf) * buf_bytes,
+                              o_base, tile_rows);
+            }
+        }
+    }
+    // ---- y: each thread writes 16-byte runs of one row, a warp 512 (fp32) or 256 (bf16)
+    // contiguous bytes per store
     __syncthreads();
-    const int o_base = lt * kBM;
     if (y_bf16) {
-        // 16 rows x 16 runs of 8 outputs: two per thread
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int f = tid + kBM * i, k = f >> 4, c8 = (f & 15) * 8;
-            if (k < nrows && o_base + c8 < d_out) {
+        for (int f = tid; f < nrows * 16; f += kBM) {  // runs of 8 outputs
+            const int k = f >> 4, c8 = (f & 15) * 8;
+            if (o_base + c8 < d_out) {
+                const float *src = ys + k * kBM + c8;
                 uint4 w;
-                w.x = pack_bf16x2(ys[k][c8], ys[k][c8 + 1]);
-                w.y = pack_bf16x2(ys[k][c8 + 2], ys[k][c8 + 3]);
-                w.z = pack_bf16x2(ys[k][c8 + 4], ys[k][c8 + 5]);
-                w.w = pack_bf16x2(ys[k][c8 + 6], ys[k][c8 + 7]);
+                w.x = pack_bf16x2(src[0], src[1]);
+                w.y = pack_bf16x2(src[2], src[3]);
+                w.z = pack_bf16x2(src[4], src[5]);
+                w.w = pack_bf16x2(src[6], src[7]);
                 *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(yv_base) + (size_t)(c0 + k) * d_out + o_base + c8) = w;
             }
         }
     } else {
-        // 16 rows x 32 runs of 4 outputs: four per thread
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int f = tid + kBM * i, k = f >> 5, c4 = (f & 31) * 4;
-            if (k < nrows && o_base + c4 < d_out)
+        for (int f = tid; f < nrows * 32; f += kBM) {  // runs of 4 outputs
+            const int k = f >> 5, c4 = (f & 31) * 4;
+            if (o_base + c4 < d_out)
                 *reinterpret_cast<float4 *>(static_cast<float *>(yv_base) + (size_t)(c0 + k) * d_out + o_base + c4) =
-                    *reinterpret_cast<const float4 *>(&ys[k][c4]);
+                    *reinterpret_cast<const float4 *>(ys + k * kBM + c4);
         }
     }
 }
@@ -965,22 +1057,39 @@ cudaError_t launch_decode_gemm(const DecodeParams &p, size_t smem_bytes, cudaStr
     return launch_pdl(kernels[v], dim3(p.n_cta), dim3(p.w4 ? kDecThreadsW4 : kDecThreads), smem_bytes, s, p);
 }
 
-cudaError_t launch_decode_finalize(const DecodeParams &p, cudaStream_t s) {
-    // The finalize's blocks land beside the gemm's CTAs (which hold most of shared memory), so
-    // they ask for the same split of the SM's memory between L1 and shared memory.
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_finalize_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+// The finalize's B buffers: one that holds a block's 16 tiles when they fit 32 KiB (one pass), else
+// two of 16 KiB (one rank-64 tile), filled and drained in turn (a pass takes the rows whose tiles
+// fit one buffer).  With y and t beside them a block holds at most 45 KiB: five blocks to an SM.
+void plan_decode_finalize(DecodeParams &dp, size_t *smem_bytes) {
+    const int cu = dp.i8 ? 8 : 16;
+    const int tile_max = kBM * std::max(1, dp.rpmax / 8) * cu;
+    const int all = kFinRows * tile_max;
+    constexpr int kOne = 32 * 1024, kTwo = 16 * 1024;
+    dp.fin_nbuf = all <= kOne ? 1 : 2;
+    dp.fin_buf = all <= kOne ? all : std::max(kTwo, tile_max);
+    *smem_bytes = (size_t)dp.fin_nbuf * dp.fin_buf + kFinRows * kBM * 4 + (size_t)kFinRows * dp.rpmax * 4 +
+                  kFinRows * sizeof(RowInfo) + (2 * kFinRows + 1) * sizeof(int);
+}
+
+cudaError_t launch_decode_finalize(const DecodeParams &p, size_t smem_bytes, cudaStream_t s) {
+    // The finalize's blocks may land beside a gemm's CTAs (which hold most of shared memory), so they
+    // ask for the same split of the SM's memory between L1 and shared memory.
+    static size_t configured[4] = {0, 0, 0, 0};
+    void (*const kernels[4])(DecodeParams) = {decode_finalize_kernel<false, false>, decode_finalize_kernel<true, false>,
+                                              decode_finalize_kernel<false, true>, decode_finalize_kernel<true, true>};
+    const int v = (p.i8 ? 1 : 0) + (p.fin_nbuf == 1 ? 2 : 0);
+    if (configured[v] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kernels[v], cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_finalize_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        configured = true;
+    }
+    if (smem_bytes > configured[v]) {
+        cudaError_t e = cudaFuncSetAttribute(kernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+        if (e != cudaSuccess) return e;
+        configured[v] = smem_bytes;
     }
     const dim3 grid(p.w_tiles, (p.n + kFinRows - 1) / kFinRows);
-    if (p.i8) return launch_pdl(decode_finalize_kernel<true>, grid, dim3(kBM), 0, s, p);
-    return launch_pdl(decode_finalize_kernel<false>, grid, dim3(kBM), 0, s, p);
+    return launch_pdl(kernels[v], grid, dim3(kBM), smem_bytes, s, p);
 }
 
 }  // namespace lora

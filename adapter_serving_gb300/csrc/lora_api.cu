@@ -811,7 +811,9 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
     if (!plan_decode_gemm(dp, &smem)) return LORA_EUNSUPPORTED;
     e = timed_launch(p, LORA_KERNEL_GEMM, s, [&] { return launch_decode_gemm(dp, smem, s); });
     if (e != cudaSuccess) return cuda_fail(e, "gemm kernel");
-    e = timed_launch(p, LORA_KERNEL_FINALIZE, s, [&] { return launch_decode_finalize(dp, s); });
+    size_t fsmem = 0;
+    plan_decode_finalize(dp, &fsmem);
+    e = timed_launch(p, LORA_KERNEL_FINALIZE, s, [&] { return launch_decode_finalize(dp, fsmem, s); });
     if (e != cudaSuccess) return cuda_fail(e, "finalize kernel");
     return LORA_OK;
 }

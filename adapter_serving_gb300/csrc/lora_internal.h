@@ -106,7 +106,9 @@ struct DecodeParams {
     int32_t w4;
     int32_t y_bf16;
     int32_t i8;           // factors are int8 codes (B read as bytes in the expand)
-    int32_t rpmax;        // row stride of T
+    int32_t rpmax;        // row stride of T; the largest storage rank in the pool
+    int32_t fin_nbuf;     // the finalize's B tile buffers (1 or 2)
+    int32_t fin_buf;      // bytes of one
     float scale;
     const int32_t *perm;      // sorted position -> row
     const int32_t *radapter;  // row -> validated adapter id (-1: base only)
@@ -250,7 +252,8 @@ cudaError_t launch_prep_segments(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_shrink(const ShrinkParams &p, int grid_x, int grid_y, cudaStream_t s);
 cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_decode_gemm(const DecodeParams &p, size_t smem_bytes, cudaStream_t s);
-cudaError_t launch_decode_finalize(const DecodeParams &p, cudaStream_t s);
+void plan_decode_finalize(DecodeParams &dp, size_t *smem_bytes);
+cudaError_t launch_decode_finalize(const DecodeParams &p, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s);
 // TMEM buffers, stage count and shared memory of a gemm launch; false if no two stages fit
 bool plan_gemm(GemmParams &gp, size_t *smem_bytes);

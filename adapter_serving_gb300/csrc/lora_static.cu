@@ -200,7 +200,9 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     if (!plan_decode_gemm(dp, &smem)) return fail(LORA_EUNSUPPORTED, "no two pipeline stages fit shared memory");
     if ((e = launch_decode_gemm(dp, smem, s)) != cudaSuccess)
         return fail(LORA_ECUDA, std::string("gemm kernel: ") + cudaGetErrorString(e));
-    if ((e = launch_decode_finalize(dp, s)) != cudaSuccess)  // pieces + expand -> y
+    size_t fsmem = 0;
+    plan_decode_finalize(dp, &fsmem);
+    if ((e = launch_decode_finalize(dp, fsmem, s)) != cudaSuccess)  // pieces + expand -> y
         return fail(LORA_ECUDA, std::string("finalize kernel: ") + cudaGetErrorString(e));
     return LORA_OK;
 }
