@@ -66,7 +66,6 @@ struct PrepShared {
     int sorted[LORA_MAX_DECODE_ROWS];                // adapter id at sorted position q
     int perm[LORA_MAX_DECODE_ROWS];                  // row at sorted position q
     int cnt[4][LORA_MAX_DECODE_ROWS];                // partial position counts
-    int seg_of[LORA_MAX_DECODE_ROWS];                // segment of position q
     int seg_q0[LORA_MAX_DECODE_ROWS + 1];            // first position of segment s
     int rank[LORA_MAX_MODULES][LORA_MAX_DECODE_ROWS];  // rank at position q (0 = none)
     int arow[LORA_MAX_MODULES][LORA_MAX_DECODE_ROWS];  // first A-slab row of the adapter at q
@@ -78,11 +77,9 @@ struct PrepShared {
 // at slot rows [8 g0, 8 g0 + r) of its segment's first group g0.
 __device__ void build_groups(const PrepParams &p, const PrepShared &sh, int ns) {
     __shared__ uint64_t s_warp_all[kPrepGroups][8];
-    __shared__ int s_g0_all[kPrepGroups][LORA_MAX_DECODE_ROWS];
     const int g = threadIdx.x >> 8, tid = threadIdx.x & 255;
     const int bar = 1 + g;
     uint64_t *s_warp = s_warp_all[g];
-    int *s_g0 = s_g0_all[g];
     for (int m = g; m < p.n_mod; m += kPrepGroups) {
         int cnt = 0, q0 = 0, q1 = 0, r = 0, row = 0;
         if (tid < ns) {
@@ -94,7 +91,6 @@ __device__ void build_groups(const PrepParams &p, const PrepShared &sh, int ns) 
         }
         uint64_t tot = 0;
         const int g0 = (int)group_scan256_u64((uint64_t)cnt, s_warp, tot, bar);
-        if (tid < ns) s_g0[tid] = cnt > 0 ? g0 : -1;
         AGroup *G = p.groups[m];
         for (int k = 0; k < cnt; ++k) {
             AGroup a;
@@ -107,12 +103,6 @@ __device__ void build_groups(const PrepParams &p, const PrepShared &sh, int ns) 
             G[g0 + k] = a;
         }
         if (tid == 0) p.n_groups[m] = (int)tot;
-        named_bar_sync(bar, 256);
-        for (int q = tid; q < p.n; q += 256) {
-            const int gs = s_g0[sh.seg_of[q]];
-            p.rowinfo[m][sh.perm[q]].tslot = gs >= 0 ? gs * kGroupRows : -1;
-        }
-        named_bar_sync(bar, 256);  // s_g0 is reused by the group's next projection
     }
 }
 
@@ -175,12 +165,12 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
         p.radapter[tid] = id;
 #pragma unroll
         for (int m = 0; m < LORA_MAX_MODULES; ++m)
-            if (m < p.n_mod) {  // the slot row is filled in with the gather lists below
+            if (m < p.n_mod) {
                 RowInfo ri;
                 ri.B = id >= 0 ? B_row[m] : nullptr;
                 ri.rank = (int16_t)(id >= 0 ? rank_row[m] : 0);
                 ri.rp = (int16_t)(id >= 0 ? rp_row[m] : 0);
-                ri.tslot = -1;
+                ri.pad_ = 0;
                 p.rowinfo[m][tid] = ri;
             }
     }
@@ -233,7 +223,6 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
         before += w < (tid >> 5) ? t : 0;
         ns += t;
     }
-    if (tid < n) sh.seg_of[tid] = before + incl - 1;
     if (flag) {
         const int seg = before + incl - 1;
         p.seg_start[seg] = tid;
@@ -606,7 +595,7 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
         // latest fill of every slot
         const uint32_t issued = k;
         if (lane == 0)
-            for (uint32_t q = 0; q < (uint32_t)S && q < issued; ++q) mbar_drain(wfull + q, ((issued - 1 - q) / (uint32_t)S) & 1u);
+            for (uint32_t q = 0; q < (uint32_t)S && q < issued; ++q) mbar_drain(wfull + q, ((issued - 1 - q) / (uint32_t)S) & 1u, p.err);
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
@@ -646,7 +635,7 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 ++li;
             }
             umma_commit(mma_done);
-            mbar_drain(mma_done, 0);
+            mbar_drain(mma_done, 0, p.err);
         }
     } else if (warp >= 2 && warp < 2 + kEpiWarps) {
         // ---------------------------------------------------------------- epilogue
@@ -851,7 +840,7 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     // launched this grid only after its own wait), the pass plan, and the first passes' B tiles.
     // Warp 0 plans in registers: lane k holds row k; passes are taken greedily in row order.
     if (tid < 32) {
-        RowInfo ri{nullptr, 0, 0, -1};
+        RowInfo ri{nullptr, 0, 0, 0};
         if (tid < nrows) {
             const uint4 raw = __ldcg(reinterpret_cast<const uint4 *>(rowinfo + c0 + tid));
             ri = *reinterpret_cast<const RowInfo *>(&raw);

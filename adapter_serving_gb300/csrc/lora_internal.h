@@ -62,7 +62,7 @@ static_assert(sizeof(AGroup) == 16, "AGroup layout");
 struct RowInfo {
     const uint16_t *B;  // the adapter's B [d_out, rp] (bytes for int8 factors); null: base only
     int16_t rank, rp;
-    int32_t tslot;      // first slot row of the adapter in the A tiles (-1: none)
+    int32_t pad_;
 };
 static_assert(sizeof(RowInfo) == 16, "RowInfo layout");
 

@@ -70,7 +70,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
-        if (mbar_try_wait_sleep(a, parity, 20000)) return true;
+        // each try may suspend the thread for up to 20 us, never for longer than the whole budget
+        if (mbar_try_wait_sleep(a, parity, budget_ns < 20000 ? (uint32_t)budget_ns : 20000u)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > budget_ns) {
             *abort_flag = 1;
@@ -83,10 +84,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 // Wait (bounded by kWaitBudgetNs, whatever the call's budget) for the phase of a barrier that
 // completes on its own: copies already issued, MMAs already committed.  A block never exits with
 // those still writing its shared memory or TMEM.
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, int *err) {
     const uint32_t a = smem_u32(bar);
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(a, parity) && globaltimer() - t0 < kWaitBudgetNs) {
+    while (!mbar_try_wait(a, parity)) {
+        if (globaltimer() - t0 > kWaitBudgetNs) {  // gave up: say so
+            if (err) atomicCAS(err, 0, 3 /* LORA_DEVERR_TIMEOUT */);
+            return;
+        }
     }
 }
 

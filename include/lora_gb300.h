@@ -314,14 +314,19 @@ int lora_segment_forward(lora_pool *pool, int32_t n_io, const lora_module_io *io
  *
  *  x, W, y        as lora_linear_forward (device, 16-byte aligned); d_in, d_out multiples of 8
  *  row_adapter_ids device int32 [n]; -1 = base only; an id outside [-1, n_adapters) is served
- *                 base only (this call has no device error report)
+ *                 base only
  *  A_stack        device bf16 [n_adapters, rank, d_in]   (adapter a's A at offset a*rank*d_in)
  *  B_stack        device bf16 [n_adapters, d_out, rank]  (adapter a's B at offset a*d_out*rank)
  *  rank           8, 16, 32 or 64, the same for every adapter (zero-pad smaller ranks)
- * Limits of the scratch: n <= 128, d_in <= 16384, d_out <= 32768, n_adapters <= 4096; larger
- * requests return LORA_EUNSUPPORTED, bad arguments LORA_EINVAL, and lora_last_cuda_error()
- * then names the reason.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) for that device, so make that first call before any stream capture.
+ * Limits of the scratch: n <= 128, d_out <= 16384 (one base-piece slot per 128 rows of W),
+ * n_adapters <= 4096; d_in is not limited.  Larger requests return LORA_EUNSUPPORTED, bad
+ * arguments LORA_EINVAL, and lora_last_cuda_error() then names the reason.
+ * This call has no device error report: unlike the pooled calls (lora_last_device_error), it
+ * does not say when a row named an out-of-range id (that row gets the base term) or when a
+ * bounded in-kernel wait ran out (after the 2 s budget the kernels return early and y is
+ * undefined).  LORA_OK means the work was queued, not that the device finished it cleanly.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) for
+ * that device, so make that first call before any stream capture.
  * All calls share the one array and it keeps the previous call's contents (the counters in it
  * are cleared by every call): calls that can overlap on the GPU -- on different streams, or
  * from several host threads -- race and corrupt each other's results; order them.

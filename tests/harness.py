@@ -88,6 +88,24 @@ def bf16_ulps(y_bits, ref):
     return np.abs(key(np.asarray(y_bits, np.uint16)) - key(ref_bits))
 
 
+BF16_FLOOR_MAG = 2.0 ** -6   # below this |oracle|, an fp32 sum's rounding may exceed a bf16 ulp
+BF16_FLOOR_ABS = 2.0 ** -13  # one bf16 ulp at that magnitude
+
+
+def bf16_gate(y_bits, ref):
+    """Outputs where the bf16 gate fails (an empty array when it holds).  A bf16 output is one
+    rounding of the fp32 result, so it lies within 1 bf16 ulp of the oracle rounded alike -- as long
+    as the fp32 result's own error (about 1e-6 of the magnitude of the summed terms) stays below
+    half an ulp.  Near zero, where terms cancel, that error can exceed the ulp of the tiny result:
+    outputs with |oracle| < 2^-6 are held to 2^-13 absolute instead (one ulp at 2^-6, ten times
+    the fp32 path's typical error)."""
+    ref = np.asarray(ref, np.float64)
+    y = wl.bf16_bits_to_f32(np.asarray(y_bits, np.uint16)).astype(np.float64)
+    ok = bf16_ulps(y_bits, ref) <= 1
+    ok |= (np.abs(ref) < BF16_FLOOR_MAG) & (np.abs(y - ref) <= BF16_FLOOR_ABS)
+    return np.argwhere(~ok)
+
+
 def oracle_rows(w, module, stage, rows=None, threads=0, x_bits=None, W_bits=None, factors=None):
     return oracle.workload_module(w, module, rows=rows, threads=threads, stage_x=x_bits, W=W_bits,
                                   factors=factors)

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads as wl
-from harness import (bf16_ulps, check_close, make_pool, oracle_rows, run_stage, to_dev_bf16, to_host_bf16)
+from harness import (bf16_gate, check_close, make_pool, oracle_rows, run_stage, to_dev_bf16, to_host_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,7 +35,8 @@ def _check_all(w, pool, factors, stages=None, rows=None, y_dtype=torch.float32, 
                 yb = outs[m].view(torch.int16).cpu().numpy().view(np.uint16)
                 if rows is not None:
                     yb = yb[np.asarray(rows)]
-                assert bf16_ulps(yb, ref).max() <= 1, f"{w.name}/{m}: bf16 output more than 1 ulp off"
+                bad = bf16_gate(yb, ref)
+                assert len(bad) == 0, f"{w.name}/{m}: bf16 outputs off at {bad[:4].tolist()}"
 
 
 def _with_ids(w, ids):
@@ -60,6 +61,26 @@ def _reduced_attn(n=100, n_ad=64, ranks=8, d=1024, kv=256, seed=3, p_base=0.1):
     r = np.full(n_ad, ranks, np.int32) if np.isscalar(ranks) else np.asarray(ranks, np.int32)
     return wl.custom("reduced_attn", {"q": (d, d), "k": (d, kv), "v": (d, kv), "o": (d, d)},
                      [["q", "k", "v"], ["o"]], n, r, 1.0, seed=seed, ids=ids)
+
+
+def test_bounded_waits_run_out_cleanly_and_the_next_call_is_correct():
+    """A wait budget of 100 ns is far below one TMA round trip, so the first wait of every gemm CTA
+    gives up: it records LORA_DEVERR_TIMEOUT, the CTA stops issuing, waits for the copies and MMAs
+    it already issued, frees its tensor memory and returns.  Nothing hangs or faults.  With the
+    default budget back, the next calls (which allocate tensor memory again) match the oracle."""
+    w = _reduced_attn(n=48, n_ad=12, seed=41)
+    pool, f = make_pool(w)
+    pool.set_wait_budget(100)
+    for st in range(len(w.stages)):
+        run_stage(pool, w, st)  # outputs undefined
+    code, _ = pool.last_device_error()
+    assert code == 3, f"expected an in-kernel wait timeout, got device error {code}"
+    pool.set_wait_budget(0)
+    for _ in range(2):
+        _check_all(w, pool, f)
+    code, _ = pool.last_device_error()
+    assert code == 0
+    pool.close()
 
 
 def test_reduced_attention_layer_ragged_batch():
@@ -249,10 +270,24 @@ def _sample_rows(n, k, seed):
     return np.sort(g.choice(n, size=min(k, n), replace=False))
 
 
-def test_attn70b_decode_full_size_sampled():
+def _rows_by_rank(w, k, seed):
+    """About k rows, spread over every rank class the batch uses (base-only rows count as one
+    class) and over the batch: each class gives its first and last row and evenly spaced ones."""
+    ids = w.row_adapters()
+    rk = np.where(ids >= 0, w.ranks[np.maximum(ids, 0)], 0)
+    classes = np.unique(rk)
+    per = max(2, k // len(classes))
+    out = []
+    for c in classes:
+        idx = np.flatnonzero(rk == c)
+        out.extend(idx[np.linspace(0, len(idx) - 1, min(per, len(idx))).round().astype(int)])
+    return np.unique(np.concatenate([np.array(out, np.int64), _sample_rows(w.n_rows, 4, seed)]))
+
+
+def test_attn70b_decode_full_size_all_rows():
     w = wl.attn70b_decode()
     pool, f = make_pool(w)
-    _check_all(w, pool, f, rows=_sample_rows(w.n_rows, 12, 1))
+    _check_all(w, pool, f)  # every row and every output
     perm, ss, sa = pool.last_segments()
     rp, rss, rsa = oracle.segments(w.ids)
     assert np.array_equal(perm, rp) and np.array_equal(ss, rss) and np.array_equal(sa, rsa)
@@ -261,7 +296,7 @@ def test_attn70b_decode_full_size_sampled():
 def test_all70b_decode_full_size_sampled():
     w = wl.all70b_decode()
     pool, f = make_pool(w)
-    _check_all(w, pool, f, rows=_sample_rows(w.n_rows, 6, 2))
+    _check_all(w, pool, f, rows=np.arange(0, w.n_rows, 4) + (np.arange(0, w.n_rows, 4) // 4) % 4)
 
 
 def test_zipf_pool_5000_adapters_sampled():
@@ -281,7 +316,8 @@ def test_zipf_pool_5000_adapters_sampled():
                 f[(int(a), m)] = (A, B)
             pool.load(int(a), mi, to_host_bf16(A), to_host_bf16(B))
     torch.cuda.synchronize()
-    rows = _sample_rows(w.n_rows, 10, 3)
+    rows = _rows_by_rank(w, 32, 3)
+    assert len(rows) >= 32
     _check_all(w, pool, f, rows=rows)
     perm, ss, sa = pool.last_segments()
     rp, rss, rsa = oracle.segments(w.ids)

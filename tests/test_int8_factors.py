@@ -68,6 +68,33 @@ def test_oracle_quantizer_signs_and_exact_multiples():
     assert codes[0].tolist() == [127, -64, 32, 1, -1, 0, 96, -127]
 
 
+def test_oracle_dequantize_rows_int8_hand_worked():
+    """Each code times its own row's scale, exactly in fp64.  Three rows with distinct scales on a
+    square matrix: a scale taken along the columns gives other values here."""
+    codes = np.array([[1, -2, 127], [0, 5, -127], [3, 3, 3]], np.int8)
+    scale = np.array([0.5, 0.25, 2.0], np.float32)
+    got = oracle.dequantize_rows_int8(codes, scale)
+    want = np.array([[0.5, -1.0, 63.5], [0.0, 1.25, -31.75], [6.0, 6.0, 6.0]])
+    assert got.dtype == np.float64 and got.shape == (3, 3)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_oracle_dequantize_round_trip(seed):
+    """Quantize then dequantize: every value is code x scale exactly (an int8 times an fp32 fits the
+    53-bit fp64 significand), and lies within half a step of the value it stands for."""
+    bits = _rows(seed, 5, 129)
+    v = _f32(bits).astype(np.float64)
+    codes, scale = oracle.quantize_rows_int8(bits)
+    deq = oracle.dequantize_rows_int8(codes, scale)
+    assert deq.shape == v.shape
+    for r in range(v.shape[0]):
+        s = Fraction(float(scale[r]))
+        for c in range(0, v.shape[1], 7):
+            assert Fraction(float(deq[r, c])) == int(codes[r, c]) * s
+        assert np.all(np.abs(deq[r] - v[r]) <= float(scale[r]) * (0.5 + 2**-17))
+
+
 def test_int8_halves_the_adapter_bytes():
     """Per adapter: r (d_in + d_out) one-byte codes plus two fp32 scales per rank index and
     projection, against 2 bytes per parameter in bf16."""
@@ -150,11 +177,19 @@ def test_int8_decode_parity(case):
     else:
         w = wl.custom("i8_qkv", {"q": (4096, 4096), "k": (4096, 512), "v": (4096, 512)}, [["q", "k", "v"]], 128,
                       np.full(128, 8, np.int32), 1.0, seed=5, ids=wl._perm_ids(128, 6))
+    import torch
+    from harness import bf16_gate
     q = _quantized(w, [int(a) for a in w.used_adapters()])
     pool = _i8_pool(w, q)
     outs = run_stage(pool, w, 0)
+    outs16 = run_stage(pool, w, 0, y_dtype=torch.bfloat16)
     for m in w.stages[0]:
-        check_close(outs[m].cpu().double().numpy(), _ref(w, q, m, 0), what=f"{case}/{m}")
+        ref = _ref(w, q, m, 0)
+        check_close(outs[m].cpu().double().numpy(), ref, what=f"{case}/{m}")
+        # bf16 output: one rounding of the fp32 result, within 1 bf16 ulp of the oracle rounded alike
+        yb = outs16[m].view(torch.int16).cpu().numpy().view(np.uint16)
+        bad = bf16_gate(yb, ref)
+        assert len(bad) == 0, f"{case}/{m}: bf16 outputs off at {bad[:4].tolist()}"
     code, _ = pool.last_device_error()
     assert code == 0
     pool.close()
@@ -240,7 +275,7 @@ def test_int8_full_size_attention_sampled_rows():
     q = _quantized(w, [int(a) for a in w.used_adapters()])
     pool = _i8_pool(w, q)
     names = w.module_names()
-    rows = np.array([0, 1, 37, 64, 100, 127])
+    rows = np.arange(0, w.n_rows, 4) + (np.arange(0, w.n_rows, 4) // 4) % 4  # 32 rows, every residue mod 4
     pool.plan_rows(torch.from_numpy(w.ids).cuda())
     for st in range(len(w.stages)):
         x = to_dev_bf16(w.x(st))

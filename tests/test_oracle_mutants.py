@@ -317,6 +317,36 @@ def test_int8_quantizer_pins_catch_planted_mistake(monkeypatch, bug):
     assert _failing_pins(I8_QUANT_PINS), f"no pin caught {bug}"
 
 
+def _dequant8(codes, scale, bug=None):
+    c = np.asarray(codes, np.float64)
+    s = np.asarray(scale, np.float64)
+    if bug == "codes_as_unsigned":
+        c = np.asarray(codes, np.int8).view(np.uint8).astype(np.float64)
+    if bug == "scale_rounded_to_bf16":
+        s = wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(np.asarray(scale, np.float32))).astype(np.float64)
+    if bug == "scale_along_columns":
+        return c * s[None, :]
+    return c * s[:, None]
+
+
+def _deq_round_trip_seed0():
+    T8.test_oracle_dequantize_round_trip(0)
+
+
+DEQ8_PINS = [T8.test_oracle_dequantize_rows_int8_hand_worked, _deq_round_trip_seed0]
+
+
+def test_int8_dequantizer_restatement_passes_every_pin(monkeypatch):
+    monkeypatch.setattr(oracle, "dequantize_rows_int8", lambda c, s: _dequant8(c, s))
+    assert _failing_pins(DEQ8_PINS) == []
+
+
+@pytest.mark.parametrize("bug", ["scale_along_columns", "codes_as_unsigned", "scale_rounded_to_bf16"])
+def test_int8_dequantizer_pins_catch_planted_mistake(monkeypatch, bug):
+    monkeypatch.setattr(oracle, "dequantize_rows_int8", lambda c, s: _dequant8(c, s, bug))
+    assert _failing_pins(DEQ8_PINS), f"no pin caught {bug}"
+
+
 def _factors64(x, W, ids, A64, B64, scale, rows=None, threads=0, bug=None):
     xf, Wf = _f64(x), _f64(W)
     ids = np.asarray(ids, np.int32)

@@ -294,3 +294,23 @@ def test_generators_are_reproducible():
     p = wl.prefill_segments()
     lens = np.diff(p.seg_start)
     assert len(lens) == 64 and lens.min() >= 128 and lens.max() <= 2048
+
+
+def test_bf16_output_gate():
+    """The bf16 output gate: 1 ulp of the oracle rounded to bf16, or 2^-13 absolute where the
+    oracle is below 2^-6 in magnitude."""
+    from harness import bf16_gate
+    ref = np.array([1.0, -3.0, 0.25, 1e-4, -2e-3, 0.5])
+    bits = wl.f32_to_bf16_bits(ref.astype(np.float32))
+    assert len(bf16_gate(bits, ref)) == 0
+    one_up = bits.copy()
+    one_up[0] += 1                      # 1 ulp above 1.0: allowed
+    assert len(bf16_gate(one_up, ref)) == 0
+    two_up = bits.copy()
+    two_up[1] += 2                      # 2 ulps off at -3.0: refused
+    assert bf16_gate(two_up, ref).ravel().tolist() == [1]
+    tiny = bits.copy()
+    tiny[3] += 3                        # 3 ulps off at 1e-4, but 3 * 2^-21 < 2^-13: allowed
+    assert len(bf16_gate(tiny, ref)) == 0
+    far = wl.f32_to_bf16_bits(np.array([1e-4 + 2 ** -12], np.float32))
+    assert bf16_gate(far, ref[3:4]).ravel().tolist() == [0]   # 2^-12 off near zero: refused
