@@ -50,6 +50,15 @@ class lora_module_io_w4(ctypes.Structure):
     _fields_ = [("module", _I32), ("x", _P), ("W_codes", _P), ("W_scale", _P), ("y", _P)]
 
 
+class lora_load_item(ctypes.Structure):
+    _fields_ = [("adapter", _I32), ("module", _I32), ("rank", _I32), ("A", _P), ("B", _P)]
+
+
+class lora_packed_item(ctypes.Structure):
+    _fields_ = [("adapter", _I32), ("module", _I32), ("rank", _I32), ("pad_", _I32), ("a_offset", _I64),
+                ("b_offset", _I64)]
+
+
 class lora_batch_policy(ctypes.Structure):
     _fields_ = [("max_batch", _I32), ("max_distinct", _I32), ("min_batch", _I32), ("tail_slots", _I32),
                 ("max_queue_ms", ctypes.c_double)]
@@ -65,6 +74,19 @@ def _sig(name, res, *args):
 _sig("lora_pool_create", ctypes.c_int, ctypes.POINTER(lora_pool_desc), ctypes.POINTER(_P))
 _sig("lora_pool_destroy", ctypes.c_int, _P)
 _sig("lora_pool_load", ctypes.c_int, _P, _I32, _I32, _P, _P, _I32, _P)
+_sig("lora_pool_load_many", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_load_item), ctypes.POINTER(_I32), _P)
+_sig("lora_pool_load_packed", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_packed_item), _P, _P, _I64,
+     ctypes.POINTER(_I32), _P)
+_sig("lora_pool_unload_many", ctypes.c_int, _P, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32), _P)
+_sig("lora_layer_step", ctypes.c_int, _P, _P, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(lora_module_io), _F,
+     _I32, _P)
+_sig("lora_layer_step_host", ctypes.c_int, _P, _P, _P, _I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(lora_module_io),
+     ctypes.POINTER(_P), ctypes.POINTER(_P), _F, _I32, _P)
+_sig("lora_pool_host_wait", ctypes.c_int, _P, _P)
+_sig("lora_layer_gate_create", ctypes.c_int, _I32, ctypes.POINTER(_P))
+_sig("lora_layer_gate_destroy", ctypes.c_int, _P)
+_sig("lora_layer_gate_mark", ctypes.c_int, _P, _I32, _P)
+_sig("lora_layer_gate_wait", ctypes.c_int, _P, _I32, _P)
 _sig("lora_pool_unload", ctypes.c_int, _P, _I32, _P)
 _sig("lora_pool_load_i8", ctypes.c_int, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P)
 _sig("lora_quantize_rows_int8", ctypes.c_int, _P, _I64, _I64, _P, _P)
@@ -222,6 +244,59 @@ def form_batch(queue_adapter, queue_waited_ms, max_batch, max_distinct=32, min_b
     return out[:n.value].copy(), d.value
 
 
+def pack_factors(entries, pin=True):
+    """Pack bf16 factors for lora_pool_load_packed: entries = [(adapter_id, module, A, B)] with A
+    [rank, d_in] and B [d_out, rank] bf16 (torch tensors or uint16 numpy arrays).  Returns (items,
+    blob): the items for Pool.load_packed and one pinned uint8 tensor holding every A at a 16-byte
+    aligned offset, each followed by its B (pin=False: ordinary host memory, for inspection)."""
+    import numpy as np
+    import torch
+    items, parts, off = [], [], 0
+    for a, m, A, B in entries:
+        A = A.view(torch.uint16).numpy() if hasattr(A, "numpy") else np.asarray(A, np.uint16)
+        B = B.view(torch.uint16).numpy() if hasattr(B, "numpy") else np.asarray(B, np.uint16)
+        pad = (-off) % 16
+        parts.append(np.zeros(pad, np.uint8))
+        off += pad
+        ao = off
+        parts.append(np.ascontiguousarray(A).view(np.uint8).ravel())
+        off += A.nbytes
+        bo = off
+        parts.append(np.ascontiguousarray(B).view(np.uint8).ravel())
+        off += B.nbytes
+        items.append((int(a), int(m), int(A.shape[0]), ao, bo))
+    blob = torch.from_numpy(np.concatenate(parts) if parts else np.zeros(0, np.uint8))
+    return items, (blob.pin_memory() if pin else blob)
+
+
+class LayerGate:
+    """One CUDA event per layer (lora_layer_gate_*): mark(l, copy_stream) after layer l's loads,
+    wait(l, compute_stream) before layer l's forward."""
+
+    def __init__(self, n_layers):
+        h = _P()
+        _check(lib.lora_layer_gate_create(int(n_layers), ctypes.byref(h)), "lora_layer_gate_create")
+        self.handle = h
+        self.n_layers = int(n_layers)
+
+    def mark(self, layer, stream=None):
+        _check(lib.lora_layer_gate_mark(self.handle, int(layer), _stream(stream)), "lora_layer_gate_mark")
+
+    def wait(self, layer, stream=None):
+        _check(lib.lora_layer_gate_wait(self.handle, int(layer), _stream(stream)), "lora_layer_gate_wait")
+
+    def close(self):
+        if self.handle:
+            lib.lora_layer_gate_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class AdapterCache:
     """Residency decisions for a pool (lora_cache_*): value-per-byte eviction, reference counts,
     the pinning guard.  Host only; the caller applies the decisions to the pool."""
@@ -314,6 +389,46 @@ class Pool:
             raise ValueError(f"factor shapes {tuple(A.shape)} / {tuple(B.shape)} do not match module {module}")
         _check(lib.lora_pool_load(self.handle, int(adapter_id), int(module), _ptr(A), _ptr(B), int(rank),
                                   _stream(stream)), "lora_pool_load")
+
+    def load_many(self, items, stream=None):
+        """items: [(adapter_id, module, A, B)] as for load (host tensors should be pinned for the
+        copies to run asynchronously); one call, one table-write launch per 64 items."""
+        import torch
+        arr = (lora_load_item * max(1, len(items)))()
+        for i, (a, m, A, B) in enumerate(items):
+            for t, nm in ((A, "A"), (B, "B")):
+                if t.dtype != torch.bfloat16 or not t.is_contiguous():
+                    raise ValueError(f"{nm}: need a contiguous bf16 tensor")
+            rank = A.shape[0]
+            if B.shape != (self.d_out[m], rank) or A.shape != (rank, self.d_in[m]):
+                raise ValueError(f"factor shapes {tuple(A.shape)} / {tuple(B.shape)} do not match module {m}")
+            arr[i] = lora_load_item(int(a), int(m), int(rank), A.data_ptr(), B.data_ptr())
+        done = _I32(0)
+        _check(lib.lora_pool_load_many(self.handle, len(items), arr, ctypes.byref(done), _stream(stream)),
+               "lora_pool_load_many")
+        return done.value
+
+    def load_packed(self, items, host_blob, dev_staging, stream=None):
+        """items: [(adapter_id, module, rank, a_offset, b_offset)], byte offsets of A [rank, d_in]
+        and B [d_out, rank] (bf16) in host_blob (a pinned uint8 tensor); dev_staging: a CUDA uint8
+        tensor at least as large.  One copy and one scatter launch (lora_pool_load_packed)."""
+        arr = (lora_packed_item * max(1, len(items)))()
+        for i, (a, m, r, ao, bo) in enumerate(items):
+            arr[i] = lora_packed_item(int(a), int(m), int(r), 0, int(ao), int(bo))
+        if dev_staging.numel() * dev_staging.element_size() < host_blob.numel() * host_blob.element_size():
+            raise ValueError("dev_staging is smaller than host_blob")
+        done = _I32(0)
+        _check(lib.lora_pool_load_packed(self.handle, len(items), arr, _ptr(host_blob), _ptr(dev_staging),
+                                         host_blob.numel() * host_blob.element_size(), ctypes.byref(done),
+                                         _stream(stream)), "lora_pool_load_packed")
+        return done.value
+
+    def unload_many(self, adapter_ids, stream=None):
+        ids = (_I32 * max(1, len(adapter_ids)))(*[int(a) for a in adapter_ids])
+        done = _I32(0)
+        _check(lib.lora_pool_unload_many(self.handle, len(adapter_ids), ids, ctypes.byref(done), _stream(stream)),
+               "lora_pool_unload_many")
+        return done.value
 
     def load_i8(self, adapter_id, module, qA, sA, qB, sB, stream=None):
         """int8 pool: qA int8 [rank, d_in], sA fp32 [rank], qB int8 [d_out, rank], sB fp32 [rank]
@@ -413,6 +528,38 @@ class Pool:
         arr, dt = self._ios(ios)
         _check(lib.lora_layer_forward_planned(self.handle, len(ios), arr, float(scale), dt, _stream(stream)),
                "lora_layer_forward_planned")
+
+    def layer_step(self, stages, row_adapter_ids, scale, stream=None):
+        """One decode layer in one call (lora_layer_step): plan the rows, then every stage in
+        order.  stages: [[(module, x, W, y), ...], ...] (a stage's projections share x)."""
+        flat = [io for st in stages for io in st]
+        arr, dt = self._ios(flat)
+        sn = (_I32 * max(1, len(stages)))(*[len(st) for st in stages])
+        ids = _dev_i32(row_adapter_ids, "row_adapter_ids")
+        _check(lib.lora_layer_step(self.handle, _ptr(ids), ids.numel(), len(stages), sn, arr, float(scale), dt,
+                                   _stream(stream)), "lora_layer_step")
+
+    def layer_step_host(self, stages, row_adapter_ids, host_ids, host_x, host_y, scale, stream=None):
+        """lora_layer_step_host: stages as for layer_step (device x, W, y; row_adapter_ids the
+        device ids buffer); host_ids: pinned int32 [n]; host_x[st]: pinned bf16 input of stage st;
+        host_y: pinned outputs, one per projection in stage order.  One call moves the step's
+        inputs in, runs it and moves its outputs out; the outputs are in host memory once `stream`
+        has passed a later host_wait()."""
+        import torch
+        flat = [io for st in stages for io in st]
+        arr, dt = self._ios(flat)
+        sn = (_I32 * max(1, len(stages)))(*[len(st) for st in stages])
+        ids = _dev_i32(row_adapter_ids, "row_adapter_ids")
+        if host_ids.dtype != torch.int32 or host_ids.numel() != ids.numel():
+            raise ValueError("host_ids: int32, one per row")
+        hx = (_P * max(1, len(stages)))(*[t.data_ptr() for t in host_x])
+        hy = (_P * max(1, len(flat)))(*[t.data_ptr() for t in host_y])
+        _check(lib.lora_layer_step_host(self.handle, _ptr(host_ids), _ptr(ids), ids.numel(), len(stages), sn, arr, hx,
+                                        hy, float(scale), dt, _stream(stream)), "lora_layer_step_host")
+
+    def host_wait(self, stream=None):
+        """Make `stream` wait for every download layer_step_host has queued (lora_pool_host_wait)."""
+        _check(lib.lora_pool_host_wait(self.handle, _stream(stream)), "lora_pool_host_wait")
 
     def linear_forward(self, module, x, W, row_adapter_ids, scale, y, stream=None):
         _dev_bf16(x, "x"), _dev_bf16(W, "W")

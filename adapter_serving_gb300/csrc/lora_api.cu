@@ -250,6 +250,20 @@ struct lora_pool {
     bool profiling = false;
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> prof_pending[4];
     std::vector<cudaEvent_t> prof_free;
+    // lora_layer_step_host: the stream the outputs go down on, and one event per stage
+    cudaStream_t d2h = nullptr, h2d = nullptr;
+    std::vector<cudaEvent_t> stage_done;
+    cudaEvent_t inputs_ready = nullptr, downloads_done = nullptr;
+    // per device buffer set (keyed by its ids buffer): the compute that last read its inputs, the
+    // downloads that last read its outputs -- the next call on the same set waits for those only
+    struct BufSet {
+        const void *key = nullptr;
+        cudaEvent_t in_free = nullptr, out_free = nullptr;
+        bool used = false;
+        uint64_t last = 0;
+    };
+    BufSet bufsets[4];
+    uint64_t host_calls = 0;
     int last_n = 0;                   // rows of the most recent forward
     bool last_decode = false;
     std::vector<void *> allocations;
@@ -306,6 +320,15 @@ int lora_pool_destroy(lora_pool *p) {
             cudaEventDestroy(e.second);
         }
     for (auto e : p->prof_free) cudaEventDestroy(e);
+    for (auto e : p->stage_done) cudaEventDestroy(e);
+    for (auto &b : p->bufsets) {
+        if (b.in_free) cudaEventDestroy(b.in_free);
+        if (b.out_free) cudaEventDestroy(b.out_free);
+    }
+    if (p->inputs_ready) cudaEventDestroy(p->inputs_ready);
+    if (p->downloads_done) cudaEventDestroy(p->downloads_done);
+    if (p->d2h) cudaStreamDestroy(p->d2h);
+    if (p->h2d) cudaStreamDestroy(p->h2d);
     delete p;
     return LORA_OK;
 }
@@ -442,19 +465,22 @@ static void release_entry(lora_pool *p, int m, int a) {
     e = PoolEntry{nullptr, nullptr, 0, 0, -1};
 }
 
-int lora_pool_load(lora_pool *p, int32_t a, int32_t m, const void *A, const void *B, int32_t rank,
-                   lora_stream_t stream) {
+// The copies and host bookkeeping of one bf16 load, queued on s; *dst / *val receive the table
+// write that publishes it (also on failure: the cleared entry).
+static int load_one(lora_pool *p, int32_t a, int32_t m, const void *A, const void *B, int32_t rank, cudaStream_t s,
+                    PoolEntry **dst, PoolEntry *val) {
+    *dst = nullptr;
     if (!p || !A || !B || m < 0 || m >= p->n_modules || a < 0 || a >= p->max_adapters) return LORA_EINVAL;
     if (rank < 1 || rank > p->max_rank || p->i8) return LORA_EINVAL;
     ++p->gen;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     ModuleStore &ms = p->mod[m];
     const int rp = storage_rank(rank);
     // a reload replaces the old factors; free first so the rows can be reused
     release_entry(p, m, a);
+    *dst = p->d_table + (size_t)m * p->max_adapters + a;
     const int64_t off = ms.rows.alloc(order_of(rp));
     if (off < 0) {
-        LORA_CUDA(launch_table_write(p->d_table + (size_t)m * p->max_adapters + a, p->entry(m, a), s));
+        *val = p->entry(m, a);
         return LORA_ENOMEM;
     }
     uint16_t *Ad = ms.A + (size_t)off * ms.d_in;
@@ -471,8 +497,131 @@ int lora_pool_load(lora_pool *p, int32_t a, int32_t m, const void *A, const void
     PoolEntry e{Ad, Bd, rank, rp, off};
     p->entry(m, a) = e;
     p->rp_count[order_of(rp)]++;
-    LORA_CUDA(launch_table_write(p->d_table + (size_t)m * p->max_adapters + a, e, s));
+    *val = e;
     return LORA_OK;
+}
+
+int lora_pool_load(lora_pool *p, int32_t a, int32_t m, const void *A, const void *B, int32_t rank,
+                   lora_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    PoolEntry *dst;
+    PoolEntry val;
+    const int rc = load_one(p, a, m, A, B, rank, s, &dst, &val);
+    if (dst) LORA_CUDA(launch_table_write(dst, val, s));
+    return rc;
+}
+
+int lora_pool_load_many(lora_pool *p, int32_t n, const lora_load_item *items, int32_t *n_done, lora_stream_t stream) {
+    if (n_done) *n_done = 0;
+    if (!p || n < 0 || (n > 0 && !items)) return LORA_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    TableWrites w;
+    w.n = 0;
+    int rc = LORA_OK, i = 0;
+    for (; i < n; ++i) {
+        PoolEntry *dst;
+        PoolEntry val;
+        const lora_load_item &it = items[i];
+        rc = load_one(p, it.adapter, it.module, it.A, it.B, it.rank, s, &dst, &val);
+        if (dst) {
+            w.dst[w.n] = dst;
+            w.v[w.n] = val;
+            if (++w.n == kTableWritesMax) {
+                LORA_CUDA(launch_table_write_many(w, s));
+                w.n = 0;
+            }
+        }
+        if (rc != LORA_OK) break;
+    }
+    LORA_CUDA(launch_table_write_many(w, s));
+    if (n_done) *n_done = i;
+    return rc;
+}
+
+int lora_pool_load_packed(lora_pool *p, int32_t n, const lora_packed_item *items, const void *host_blob,
+                          void *dev_staging, int64_t blob_bytes, int32_t *n_done, lora_stream_t stream) {
+    if (n_done) *n_done = 0;
+    if (!p || n < 0 || blob_bytes < 0 || (n > 0 && (!items || !host_blob || !dev_staging)) || p->i8) return LORA_EINVAL;
+    if (reinterpret_cast<uintptr_t>(dev_staging) & 15) return LORA_EINVAL;
+    for (int i = 0; i < n; ++i) {  // every item checked before anything is queued
+        const lora_packed_item &it = items[i];
+        if (it.module < 0 || it.module >= p->n_modules || it.adapter < 0 || it.adapter >= p->max_adapters) return LORA_EINVAL;
+        if (it.rank < 1 || it.rank > p->max_rank || it.a_offset < 0 || it.b_offset < 0) return LORA_EINVAL;
+        const ModuleStore &ms = p->mod[it.module];
+        if (it.a_offset % 16 || it.b_offset % 2 || it.a_offset + (int64_t)it.rank * ms.d_in * 2 > blob_bytes ||
+            it.b_offset + (int64_t)ms.d_out * it.rank * 2 > blob_bytes)
+            return LORA_EINVAL;
+    }
+    if (n == 0) return LORA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    LORA_CUDA(cudaMemcpyAsync(dev_staging, host_blob, (size_t)blob_bytes, cudaMemcpyHostToDevice, s));
+    const uint8_t *stage = static_cast<const uint8_t *>(dev_staging);
+    ++p->gen;
+    PackedJobs jobs;
+    jobs.n = 0;
+    int rc = LORA_OK, i = 0;
+    for (; i < n; ++i) {
+        const lora_packed_item &it = items[i];
+        ModuleStore &ms = p->mod[it.module];
+        const int rp = storage_rank(it.rank);
+        release_entry(p, it.module, it.adapter);  // a reload replaces the old factors
+        PoolEntry *dst = p->d_table + (size_t)it.module * p->max_adapters + it.adapter;
+        const int64_t off = ms.rows.alloc(order_of(rp));
+        if (off < 0) {
+            LORA_CUDA(launch_packed_load(jobs, s));
+            LORA_CUDA(launch_table_write(dst, p->entry(it.module, it.adapter), s));  // cleared
+            jobs.n = 0;
+            rc = LORA_ENOMEM;
+            break;
+        }
+        PoolEntry e{ms.A + (size_t)off * ms.d_in, ms.B + (size_t)off * ms.d_out, it.rank, rp, off};
+        p->entry(it.module, it.adapter) = e;
+        p->rp_count[order_of(rp)]++;
+        jobs.j[jobs.n++] = PackedJob{stage + it.a_offset, stage + it.b_offset, dst, e, ms.d_in, ms.d_out};
+        if (jobs.n == kPackedMax) {
+            LORA_CUDA(launch_packed_load(jobs, s));
+            jobs.n = 0;
+        }
+    }
+    LORA_CUDA(launch_packed_load(jobs, s));
+    if (n_done) *n_done = i;
+    return rc;
+}
+
+int lora_pool_unload_many(lora_pool *p, int32_t n, const int32_t *ids, int32_t *n_done, lora_stream_t stream) {
+    if (n_done) *n_done = 0;
+    if (!p || n < 0 || (n > 0 && !ids)) return LORA_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    ++p->gen;
+    TableWrites w;
+    w.n = 0;
+    int rc = LORA_OK, i = 0;
+    for (; i < n; ++i) {
+        const int a = ids[i];
+        if (a < 0 || a >= p->max_adapters) {
+            rc = LORA_EINVAL;
+            break;
+        }
+        bool any = false;
+        for (int m = 0; m < p->n_modules; ++m) {
+            if (p->entry(m, a).rank <= 0) continue;
+            any = true;
+            release_entry(p, m, a);
+            w.dst[w.n] = p->d_table + (size_t)m * p->max_adapters + a;
+            w.v[w.n] = p->entry(m, a);
+            if (++w.n == kTableWritesMax) {
+                LORA_CUDA(launch_table_write_many(w, s));
+                w.n = 0;
+            }
+        }
+        if (!any) {
+            rc = LORA_ENOTLOADED;
+            break;
+        }
+    }
+    LORA_CUDA(launch_table_write_many(w, s));
+    if (n_done) *n_done = i;
+    return rc;
 }
 
 int lora_pool_load_i8(lora_pool *p, int32_t a, int32_t m, const int8_t *qA, const float *sA, const int8_t *qB,
@@ -1050,6 +1199,95 @@ int lora_layer_forward_planned_w4(lora_pool *p, int32_t n_io, const lora_module_
     return layer_forward_planned(p, n_io, io, scale, y_dtype, stream, true);
 }
 
+int lora_layer_step(lora_pool *p, const int32_t *ids, int32_t n, int32_t n_stages, const int32_t *stage_n,
+                    const lora_module_io *io, float scale, int32_t y_dtype, lora_stream_t stream) {
+    if (!p || n_stages < 0 || (n_stages > 0 && (!stage_n || !io))) return LORA_EINVAL;
+    for (int st = 0; st < n_stages; ++st)
+        if (stage_n[st] < 1) return LORA_EINVAL;
+    int rc = lora_plan_rows(p, ids, n, stream);
+    if (rc != LORA_OK) return rc;
+    for (int st = 0, off = 0; st < n_stages; off += stage_n[st], ++st)
+        if ((rc = lora_layer_forward_planned(p, stage_n[st], io + off, scale, y_dtype, stream)) != LORA_OK) return rc;
+    return LORA_OK;
+}
+
+int lora_layer_step_host(lora_pool *p, const int32_t *host_ids, int32_t *row_adapter_ids, int32_t n, int32_t n_stages,
+                         const int32_t *stage_n, const lora_module_io *io, const void *const *host_x,
+                         void *const *host_y, float scale, int32_t y_dtype, lora_stream_t stream) {
+    if (!p || !host_ids || !row_adapter_ids || n < 0 || n_stages < 0 || (n_stages > 0 && (!stage_n || !io || !host_x || !host_y)))
+        return LORA_EINVAL;
+    if (y_dtype != LORA_DTYPE_F32 && y_dtype != LORA_DTYPE_BF16) return LORA_EINVAL;
+    int total = 0;
+    for (int st = 0; st < n_stages; ++st) {
+        if (stage_n[st] < 1) return LORA_EINVAL;
+        for (int i = total; i < total + stage_n[st]; ++i)
+            if (io[i].module < 0 || io[i].module >= p->n_modules || io[i].x != io[total].x || !host_y[i]) return LORA_EINVAL;
+        if (!host_x[st]) return LORA_EINVAL;
+        total += stage_n[st];
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    LORA_CUDA(cudaSetDevice(p->device));
+    if (!p->d2h) LORA_CUDA(cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking));
+    if (!p->h2d) LORA_CUDA(cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking));
+    if (!p->inputs_ready) LORA_CUDA(cudaEventCreateWithFlags(&p->inputs_ready, cudaEventDisableTiming));
+    if (!p->downloads_done) LORA_CUDA(cudaEventCreateWithFlags(&p->downloads_done, cudaEventDisableTiming));
+    while ((int)p->stage_done.size() < n_stages) {
+        cudaEvent_t e;
+        LORA_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        p->stage_done.push_back(e);
+    }
+    // the buffer set of this call (least recently used slot for a new one)
+    lora_pool::BufSet *bs = nullptr;
+    for (auto &b : p->bufsets)
+        if (b.key == row_adapter_ids) bs = &b;
+    if (!bs) {
+        bs = &p->bufsets[0];
+        for (auto &b : p->bufsets)
+            if (b.last < bs->last) bs = &b;
+        if (!bs->in_free) LORA_CUDA(cudaEventCreateWithFlags(&bs->in_free, cudaEventDisableTiming));
+        if (!bs->out_free) LORA_CUDA(cudaEventCreateWithFlags(&bs->out_free, cudaEventDisableTiming));
+        bs->key = row_adapter_ids;
+        bs->used = false;
+    }
+    bs->last = ++p->host_calls;
+    // inputs in, on the pool's upload stream: after the last compute that read this set's inputs,
+    // so they may go up while an earlier call (another set) still computes
+    if (bs->used) LORA_CUDA(cudaStreamWaitEvent(p->h2d, bs->in_free, 0));
+    LORA_CUDA(cudaMemcpyAsync(row_adapter_ids, host_ids, (size_t)n * 4, cudaMemcpyHostToDevice, p->h2d));
+    for (int st = 0, off = 0; st < n_stages; off += stage_n[st], ++st)
+        LORA_CUDA(cudaMemcpyAsync(const_cast<void *>(io[off].x), host_x[st], (size_t)n * p->mod[io[off].module].d_in * 2,
+                                  cudaMemcpyHostToDevice, p->h2d));
+    LORA_CUDA(cudaEventRecord(p->inputs_ready, p->h2d));
+    // the step on `stream`: once its inputs are in and this set's outputs of an earlier call are out
+    LORA_CUDA(cudaStreamWaitEvent(s, p->inputs_ready, 0));
+    if (bs->used) LORA_CUDA(cudaStreamWaitEvent(s, bs->out_free, 0));
+    int rc = lora_plan_rows(p, row_adapter_ids, n, stream);
+    if (rc != LORA_OK) return rc;
+    // each stage, then its outputs out on the pool's download stream while the next stage (or the
+    // next call) computes
+    const size_t esz = y_dtype == LORA_DTYPE_F32 ? 4 : 2;
+    for (int st = 0, off = 0; st < n_stages; off += stage_n[st], ++st) {
+        if ((rc = lora_layer_forward_planned(p, stage_n[st], io + off, scale, y_dtype, stream)) != LORA_OK) return rc;
+        LORA_CUDA(cudaEventRecord(p->stage_done[(size_t)st], s));
+        LORA_CUDA(cudaStreamWaitEvent(p->d2h, p->stage_done[(size_t)st], 0));
+        for (int i = off; i < off + stage_n[st]; ++i)
+            LORA_CUDA(cudaMemcpyAsync(host_y[i], io[i].y, (size_t)n * p->mod[io[i].module].d_out * esz,
+                                      cudaMemcpyDeviceToHost, p->d2h));
+    }
+    LORA_CUDA(cudaEventRecord(bs->in_free, s));
+    LORA_CUDA(cudaEventRecord(bs->out_free, p->d2h));
+    bs->used = true;
+    return LORA_OK;
+}
+
+int lora_pool_host_wait(lora_pool *p, lora_stream_t stream) {
+    if (!p) return LORA_EINVAL;
+    if (!p->d2h) return LORA_OK;
+    LORA_CUDA(cudaEventRecord(p->downloads_done, p->d2h));
+    LORA_CUDA(cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(stream), p->downloads_done, 0));
+    return LORA_OK;
+}
+
 int lora_segment_forward(lora_pool *p, int32_t n_io, const lora_module_io *io, const int32_t *seg_start,
                          const int32_t *seg_adapter, int32_t n_seg, int32_t n, float scale, int32_t y_dtype,
                          lora_stream_t stream) {
@@ -1062,3 +1300,55 @@ int lora_segment_forward(lora_pool *p, int32_t n_io, const lora_module_io *io, c
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ layer gates -----------
+
+struct lora_layer_gate {
+    int device = 0;
+    std::vector<cudaEvent_t> ev;
+};
+
+int lora_layer_gate_create(int32_t n_layers, lora_layer_gate **out) {
+    if (!out || n_layers < 1) return LORA_EINVAL;
+    *out = nullptr;
+    auto *g = new lora_layer_gate;
+    if (cudaGetDevice(&g->device) != cudaSuccess) {
+        delete g;
+        return cuda_fail(cudaGetLastError(), "cudaGetDevice");
+    }
+    g->ev.assign((size_t)n_layers, nullptr);
+    for (auto &e : g->ev) {
+        const cudaError_t ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+        if (ce != cudaSuccess) {
+            lora_layer_gate_destroy(g);
+            return cuda_fail(ce, "cudaEventCreateWithFlags");
+        }
+    }
+    *out = g;
+    return LORA_OK;
+}
+
+int lora_layer_gate_destroy(lora_layer_gate *g) {
+    if (!g) return LORA_EINVAL;
+    for (auto e : g->ev)
+        if (e) cudaEventDestroy(e);
+    delete g;
+    return LORA_OK;
+}
+
+int lora_layer_gate_mark(lora_layer_gate *g, int32_t layer, lora_stream_t copy_stream) {
+    if (!g || layer < 0 || layer >= (int32_t)g->ev.size()) return LORA_EINVAL;
+    LORA_CUDA(cudaEventRecord(g->ev[(size_t)layer], reinterpret_cast<cudaStream_t>(copy_stream)));
+    return LORA_OK;
+}
+
+int lora_layer_gate_wait(lora_layer_gate *g, int32_t layer, lora_stream_t compute_stream) {
+    if (!g || layer < 0 || layer >= (int32_t)g->ev.size()) return LORA_EINVAL;
+    // loads already finished need no wait: leaving it out keeps the compute stream's kernels
+    // back to back (each launches early on the one before, which a stream wait would prevent)
+    const cudaError_t q = cudaEventQuery(g->ev[(size_t)layer]);
+    if (q == cudaSuccess) return LORA_OK;
+    if (q != cudaErrorNotReady) return cuda_fail(q, "cudaEventQuery");
+    LORA_CUDA(cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(compute_stream), g->ev[(size_t)layer], 0));
+    return LORA_OK;
+}

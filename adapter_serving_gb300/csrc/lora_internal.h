@@ -255,6 +255,29 @@ cudaError_t launch_decode_gemm(const DecodeParams &p, size_t smem_bytes, cudaStr
 void plan_decode_finalize(DecodeParams &dp, size_t *smem_bytes);
 cudaError_t launch_decode_finalize(const DecodeParams &p, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s);
+// Up to kTableWritesMax table entries written by one launch (the entries ride in the parameters).
+constexpr int kTableWritesMax = 64;
+struct TableWrites {
+    PoolEntry *dst[kTableWritesMax];
+    PoolEntry v[kTableWritesMax];
+    int32_t n;
+};
+cudaError_t launch_table_write_many(const TableWrites &w, cudaStream_t s);
+// Packed loads: one item's factors from a device staging buffer into its pool rows, zero-padded
+// to the storage rank, then its table entry.  Up to kPackedMax items per launch (parameters).
+constexpr int kPackedMax = 96;
+struct PackedJob {
+    const uint8_t *srcA;  // bf16 [rank, d_in] in the staging buffer
+    const uint8_t *srcB;  // bf16 [d_out, rank]
+    PoolEntry *dst;       // the table entry to publish
+    PoolEntry val;        // its value (val.A, val.B: the rows in the pool)
+    int32_t d_in, d_out;
+};
+struct PackedJobs {
+    PackedJob j[kPackedMax];
+    int32_t n;
+};
+cudaError_t launch_packed_load(const PackedJobs &jobs, cudaStream_t s);
 // TMEM buffers, stage count and shared memory of a gemm launch; false if no two stages fit
 bool plan_gemm(GemmParams &gp, size_t *smem_bytes);
 bool plan_decode_gemm(DecodeParams &dp, size_t *smem_bytes);

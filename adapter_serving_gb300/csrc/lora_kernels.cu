@@ -93,6 +93,42 @@ __global__ void __launch_bounds__(1024) prep_segments_kernel(const PrepParams p)
 }
 
 __global__ void table_write_kernel(PoolEntry *dst, PoolEntry v) { *dst = v; }
+__global__ void table_write_many_kernel(const __grid_constant__ TableWrites w) {
+    if ((int)threadIdx.x < w.n) *w.dst[threadIdx.x] = w.v[threadIdx.x];
+}
+
+// Block (item, part): a share of the item's A rows and B rows.  A ([rp, d_in] bf16, d_in a
+// multiple of 8) moves in 16-byte chunks, the rows past the rank zeroed.  B ([d_out, rp]) moves in
+// 16-byte chunks too when the rank is the storage rank (its rows are then contiguous in both
+// places), else element by element with the columns past the rank zeroed.  Block (item, 0)
+// publishes the entry; later kernels on the stream see it only after the whole grid has finished.
+__global__ void __launch_bounds__(256) packed_load_kernel(const __grid_constant__ PackedJobs jobs) {
+    const PackedJob &J = jobs.j[blockIdx.x];
+    const int rank = J.val.rank, rp = J.val.rp, d_in = J.d_in, d_out = J.d_out;
+    const int stride = gridDim.y * blockDim.x, t0 = blockIdx.y * blockDim.x + threadIdx.x;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const int cpr = d_in / 8;  // 16-byte chunks per A row
+    const int a_live = rank * cpr, a_all = rp * cpr;
+    uint4 *dA = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(J.val.A));
+    const uint4 *sA = reinterpret_cast<const uint4 *>(J.srcA);
+    for (int c = t0; c < a_all; c += stride) dA[c] = c < a_live ? sA[c] : zero;
+    uint16_t *dB = const_cast<uint16_t *>(J.val.B);
+    const bool b_vec = rank == rp && (reinterpret_cast<uintptr_t>(J.srcB) & 15) == 0;
+    if (b_vec) {
+        const int b_chunks = d_out * rp / 8;
+        uint4 *d4 = reinterpret_cast<uint4 *>(dB);
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(J.srcB);
+        for (int c = t0; c < b_chunks; c += stride) d4[c] = s4[c];
+    } else {
+        const uint16_t *sB = reinterpret_cast<const uint16_t *>(J.srcB);
+        const int b_elems = d_out * rp;
+        for (int e = t0; e < b_elems; e += stride) {
+            const int r = e / rp, c = e - r * rp;
+            dB[e] = c < rank ? sB[r * rank + c] : (uint16_t)0;
+        }
+    }
+    if (blockIdx.y == 0 && threadIdx.x == 0) *J.dst = J.val;
+}
 
 // ========================================================================== shrink ==========
 //
@@ -839,6 +875,18 @@ cudaError_t launch_gemm(const GemmParams &p, size_t smem_bytes, cudaStream_t s) 
 
 cudaError_t launch_table_write(PoolEntry *dst, PoolEntry value, cudaStream_t s) {
     table_write_kernel<<<1, 1, 0, s>>>(dst, value);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_table_write_many(const TableWrites &w, cudaStream_t s) {
+    if (w.n <= 0) return cudaSuccess;
+    table_write_many_kernel<<<1, kTableWritesMax, 0, s>>>(w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_packed_load(const PackedJobs &jobs, cudaStream_t s) {
+    if (jobs.n <= 0) return cudaSuccess;
+    packed_load_kernel<<<dim3(jobs.n, 16), 256, 0, s>>>(jobs);
     return cudaGetLastError();
 }
 

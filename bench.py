@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="timed loop only (for profiler launch lists)")
-    ap.add_argument("--workload", default="attn70b", choices=sorted(WORKLOADS),
+    ap.add_argument("--workload", default="attn70b", choices=sorted(WORKLOADS) + ["layers8"],
                     help="attn70b (the headline) or another of the pages' configurations")
     return ap.parse_args()
 
@@ -421,74 +421,110 @@ def run_ours(args, w):
         h2d = sum(x.numel() * 2 for x in hx) + hid.numel() * 4
         d2h = sum(y.numel() * 4 for y in hy.values())
 
-        # A serving loop keeps the host I/O of neighbouring steps in flight: while step k computes,
-        # step k+1's ids and x go up and step k-1's y comes back.  Device buffers alternate
-        # between two sets; the host inputs are the same each step and the outputs alternate
-        # between two host sets.  All bytes of both directions of every step are inside the
-        # timed region (first upload to last download).  No L2 flush between steps: each step
-        # reads 302 MB of W, more than the 129 MB L2, so nothing carries over.
-        up = torch.cuda.Stream(device=dev)
-        down = torch.cuda.Stream(device=dev)
-        dbuf = []
-        for b in range(2):
-            xb = [torch.empty_like(x) for x in xd]
-            yb = {m: torch.empty_like(yd[m]) for m in names}
-            io_b = [[io_of(m, xb[st], yb[m]) for m in mods] for st, mods in enumerate(w.stages)]
-            dbuf.append({"ids": torch.empty_like(ids), "x": xb, "y": yb, "io": io_b})
-        hyb = [{m: torch.empty(w.n_rows, w.modules[m][1], dtype=torch.float32).pin_memory() for m in names}
-               for _ in range(2)]
+        if not w4:
+            # One library call per step with host buffers (lora_layer_step_host): the ids and the
+            # stages' x go up, the step runs, every y comes back (a stage's outputs while the next
+            # stage computes); the call's work ends when the last output has landed.  Steps run back
+            # to back on one stream, so all bytes of both directions are inside the timed region.
+            # No L2 flush between steps: each step reads W, more than the 129 MB L2 (see "timing").
+            sets = []
+            for b in range(2):  # two device buffer sets, alternating: step k+1's inputs go up while step k computes
+                xb = [torch.empty_like(x) for x in xd]
+                yb = {m: torch.empty_like(yd[m]) for m in names}
+                sets.append((torch.empty_like(ids), [[io_of(m, xb[st], yb[m]) for m in mods]
+                                                     for st, mods in enumerate(w.stages)]))
+            hy_sets = [[torch.empty_like(hy[m]).pin_memory() for mods in w.stages for m in mods] for _ in range(2)]
 
-        def e2e_run(k_steps):
-            """k_steps pipelined steps; returns device ms per step."""
-            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            inputs_free = [None, None]   # compute done with a buffer set's ids and x
-            outputs_free = [None, None]  # download done from a buffer set's y
-            start.record(up)
-            up.wait_stream(stream)
-            for k in range(k_steps):
-                b = k % 2
-                B = dbuf[b]
-                with torch.cuda.stream(up):  # this step's inputs
-                    if inputs_free[b] is not None:
-                        up.wait_event(inputs_free[b])
-                    B["ids"].copy_(hid, non_blocking=True)
-                    for st in range(len(hx)):
-                        B["x"][st].copy_(hx[st], non_blocking=True)
-                    ready = torch.cuda.Event()
-                    ready.record(up)
-                stream.wait_event(ready)
-                if outputs_free[b] is not None:
-                    stream.wait_event(outputs_free[b])
-                pool.plan_rows(B["ids"], stream=stream)
-                for st, io in enumerate(B["io"]):
-                    forward_planned(io, w.scale, stream=stream)
-                    done = torch.cuda.Event()
-                    done.record(stream)
-                    with torch.cuda.stream(down):  # this call's outputs
-                        down.wait_event(done)
-                        for m in w.stages[st]:
-                            hyb[b][m].copy_(B["y"][m], non_blocking=True)
-                inputs_free[b] = done
-                freed = torch.cuda.Event()
-                freed.record(down)
-                outputs_free[b] = freed
-            stream.wait_stream(up)
-            stream.wait_stream(down)
-            end.record(stream)
-            torch.cuda.synchronize()
-            return start.elapsed_time(end) / k_steps
+            def e2e_run(k_steps):
+                """k_steps steps, one call each; returns (device ms, host wall ms) per step."""
+                start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                start.record(stream)
+                for k in range(k_steps):
+                    ids_b, stages_b = sets[k % 2]
+                    pool.layer_step_host(stages_b, ids_b, hid, hx, hy_sets[k % 2], w.scale, stream=stream)
+                pool.host_wait(stream=stream)  # every step's outputs are in host memory
+                end.record(stream)
+                torch.cuda.synchronize()
+                return start.elapsed_time(end) / k_steps, (time.perf_counter() - t0) * 1e3 / k_steps
+            how = ("one lora_layer_step_host call per step (ids and x up, the step, every y down; pinned host "
+                   "buffers, two device buffer sets alternating, so a step's copies overlap its neighbours' "
+                   "compute)")
+        else:
+            # int4 base: the serving loop keeps the host I/O of neighbouring steps in flight: while
+            # step k computes, step k+1's ids and x go up and step k-1's y comes back.  Device
+            # buffers alternate between two sets; all bytes of both directions of every step are
+            # inside the timed region (first upload to last download).
+            up = torch.cuda.Stream(device=dev)
+            down = torch.cuda.Stream(device=dev)
+            dbuf = []
+            for b in range(2):
+                xb = [torch.empty_like(x) for x in xd]
+                yb = {m: torch.empty_like(yd[m]) for m in names}
+                io_b = [[io_of(m, xb[st], yb[m]) for m in mods] for st, mods in enumerate(w.stages)]
+                dbuf.append({"ids": torch.empty_like(ids), "x": xb, "y": yb, "io": io_b})
+            hyb = [{m: torch.empty(w.n_rows, w.modules[m][1], dtype=torch.float32).pin_memory() for m in names}
+                   for _ in range(2)]
+
+            def e2e_run(k_steps):
+                """k_steps pipelined steps; returns (device ms, host wall ms) per step."""
+                start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                inputs_free = [None, None]   # compute done with a buffer set's ids and x
+                outputs_free = [None, None]  # download done from a buffer set's y
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                start.record(up)
+                up.wait_stream(stream)
+                for k in range(k_steps):
+                    b = k % 2
+                    B = dbuf[b]
+                    with torch.cuda.stream(up):  # this step's inputs
+                        if inputs_free[b] is not None:
+                            up.wait_event(inputs_free[b])
+                        B["ids"].copy_(hid, non_blocking=True)
+                        for st in range(len(hx)):
+                            B["x"][st].copy_(hx[st], non_blocking=True)
+                        ready = torch.cuda.Event()
+                        ready.record(up)
+                    stream.wait_event(ready)
+                    if outputs_free[b] is not None:
+                        stream.wait_event(outputs_free[b])
+                    pool.plan_rows(B["ids"], stream=stream)
+                    for st, io in enumerate(B["io"]):
+                        forward_planned(io, w.scale, stream=stream)
+                        done = torch.cuda.Event()
+                        done.record(stream)
+                        with torch.cuda.stream(down):  # this call's outputs
+                            down.wait_event(done)
+                            for m in w.stages[st]:
+                                hyb[b][m].copy_(B["y"][m], non_blocking=True)
+                    inputs_free[b] = done
+                    freed = torch.cuda.Event()
+                    freed.record(down)
+                    outputs_free[b] = freed
+                stream.wait_stream(up)
+                stream.wait_stream(down)
+                end.record(stream)
+                torch.cuda.synchronize()
+                return start.elapsed_time(end) / k_steps, (time.perf_counter() - t0) * 1e3 / k_steps
+            how = "two buffer sets, host I/O of neighbouring steps overlapped with compute"
 
         e2e_run(4)  # warm-up
         barrier()
-        e_ms = e2e_run(args.steps)
+        runs = [e2e_run(args.steps) for _ in range(5)]
+        dev_ms = sorted(r[0] for r in runs)
+        wall_ms = sorted(r[1] for r in runs)
+        e_ms = dev_ms[2]  # median of 5
         if world > 1:
             t = torch.tensor([e_ms], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e_ms = float(t.item())
         line["e2e"] = {"value": world * w.n_rows / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-                       "timing": "steps back to back, host I/O of neighbouring steps overlapped; no L2 flush "
-                                 f"({ab['W'] / 1e6:.0f} MB of W per step"
+                       "ms_per_step_runs": dev_ms, "host_wall_ms_per_step_runs": wall_ms,
+                       "timing": f"{how}; median of 5 runs of {args.steps} steps (device time, first upload to "
+                                 f"last download); no L2 flush ({ab['W'] / 1e6:.0f} MB of W per step"
                                  + (" > 129 MB L2)" if ab["W"] > 129e6 else
                                     ", less than the 129 MB L2: part of W may still be in L2 from the step before)")}
         code, detail = pool.last_device_error()
@@ -501,6 +537,173 @@ def run_ours(args, w):
     pool.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_layers(args):
+    """Adapter loads pipelined across layers ("12. Adapter Serving and Multi-Tenant Customization",
+    section "Switching cost: I/O, not compute"): 8 layers of the 70B attention projections, one
+    pool per layer, 128 decode rows on 128 distinct rank-16 adapters.  Every step 4 cold adapters
+    arrive (and 4 leave): their factors for all 8 layers are loaded while the step runs.  Three
+    timings of the same forwards: every adapter already resident; the loads on a copy stream, layer
+    by layer, each layer's forward waiting for its own layer's loads only (lora_layer_gate); the
+    loads queued on the compute stream before each layer (no overlap)."""
+    import torch
+    import adapter_serving_gb300 as L
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n_layers, n, rank, n_cold = 8, 128, 16, 4
+    mods = {"q": (8192, 8192), "k": (8192, 1024), "v": (8192, 1024), "o": (8192, 8192)}
+    stages = [["q", "k", "v"], ["o"]]
+    names = list(mods)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+
+    def randn(*shape, std=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    Ws = [{m: randn(mods[m][1], mods[m][0], std=mods[m][0] ** -0.5) for m in names} for _ in range(n_layers)]
+    xs = [[randn(n, 8192) for _ in stages] for _ in range(n_layers)]
+    ys = [{m: torch.empty(n, mods[m][1], device=dev) for m in names} for _ in range(n_layers)]
+    total = 2 * (max(3, args.warmup) + args.steps) + 2  # pipelined and serial steps, each brings n_cold adapters
+    n_ad = 128 + n_cold * (total + 1)
+    live0 = 128
+    pages = [(live0 + 3 * n_cold) * rank // 64 + 2] * len(names)  # the batch's, the cold ones, those leaving
+    pools = [L.Pool([mods[m][0] for m in names], [mods[m][1] for m in names], n_ad, max_rank=64, pages=pages,
+                    max_rows=n) for _ in range(n_layers)]
+    # host factors: 8 pinned sets per layer, adapter a uses set a % 8 (the values do not matter here)
+    hf = [[{m: (randn(rank, mods[m][0], std=0.02).cpu().pin_memory(), randn(mods[m][1], rank, std=0.02).cpu().pin_memory())
+            for m in names} for _ in range(8)] for _ in range(n_layers)]
+
+    def items(l, adapters):
+        return [(a, names.index(m), *hf[l][a % 8][m]) for a in adapters for m in names]
+
+    for l in range(n_layers):
+        pools[l].load_many(items(l, range(live0)))
+    # a cold adapter's factors for a layer arrive as one packed pinned blob (what a loader reading
+    # them from host storage would hand over): blob h of layer l holds factor sets 4h .. 4h + 3,
+    # adapter a uses set a % 8, and the cold adapters of a step are 4 consecutive ids
+    packs = [[L.pack_factors([(i, names.index(m), *hf[l][4 * h + i][m]) for i in range(n_cold) for m in names])
+              for h in range(2)] for l in range(n_layers)]
+    staging = [torch.empty(packs[l][0][1].numel(), dtype=torch.uint8, device=dev) for l in range(n_layers)]
+    torch.cuda.synchronize()
+    load_bytes = sum(packs[l][0][1].numel() for l in range(n_layers))
+    compute = torch.cuda.current_stream()
+    # the loads' small kernels (table writes, the scatter of a packed blob) take SM slots as soon as
+    # any are free, ahead of the forwards' waiting blocks: a high-priority copy stream
+    copy_s = torch.cuda.Stream(device=dev, priority=-1)
+    gate = L.LayerGate(n_layers)
+    group = 4  # layers per gate wait
+    # the rows of step k with loads: the 128 adapters resident once its cold ones are in (all
+    # precomputed, so no host copy sits inside a step)
+    ids_k = torch.stack([torch.arange(n_cold * (k + 1), n_cold * (k + 1) + live0, dtype=torch.int32)
+                         for k in range(total)]).to(dev)
+    ids_res = torch.arange(live0, dtype=torch.int32, device=dev)
+    nxt = [live0]  # next cold adapter id
+    step_end = [None, None, None]  # compute done, per loads step (ring)
+
+    def layer_io(l):
+        return [[(names.index(m), xs[l][st], Ws[l][m], ys[l][m]) for m in mods_] for st, mods_ in enumerate(stages)]
+
+    ios = [layer_io(l) for l in range(n_layers)]
+
+    def step(mode):
+        """One 8-layer step; mode: 'resident', 'pipelined' or 'serial'."""
+        if mode == "resident":
+            for l in range(n_layers):
+                pools[l].layer_step(ios[l], ids_res, 1.0, stream=compute)
+            return
+        k = (nxt[0] - live0) // n_cold  # loads step k: live = [n_cold (k + 1), n_cold (k + 1) + 128)
+        ids_d = ids_k[k]
+        cold = list(range(nxt[0], nxt[0] + n_cold))
+        nxt[0] += n_cold
+        h = (cold[0] % 8) // n_cold
+
+        def load_layer(l, s):
+            if evict:
+                pools[l].unload_many(evict, stream=s)
+            its, blob = packs[l][h]
+            pools[l].load_packed([(cold[i], m, r, ao, bo) for i, m, r, ao, bo in its], blob, staging[l], stream=s)
+
+        if mode == "serial":
+            evict = list(range(n_cold * k, n_cold * (k + 1)))  # last used by the step before
+            for l in range(n_layers):
+                load_layer(l, compute)
+                pools[l].layer_step(ios[l], ids_d, 1.0, stream=compute)
+            return
+        # The adapters that left the batch a step ago were last read by step k - 2's forwards: their
+        # pages go back once that step is done (an event), so this step's loads need not wait for
+        # the step still computing and may run ahead of it (the pool keeps room for them).
+        evict = list(range(n_cold * (k - 1), n_cold * k)) if k > 0 else []
+        done_k2 = step_end[(k - 2) % 3] if k >= 2 else None
+        if done_k2 is not None:
+            copy_s.wait_event(done_k2)
+        elif k == 1:
+            copy_s.wait_stream(compute)
+
+        def loads(l):
+            load_layer(l, copy_s)
+            gate.mark(l, copy_s)
+
+        # the loads go up a group of layers ahead; the forwards wait once per group, before its first
+        # layer, for that group's loads (each stream wait keeps one forward from launching early)
+        for l in range(min(group, n_layers)):
+            loads(l)
+        for l in range(n_layers):
+            if l % group == 0:
+                for j in range(l + group, min(l + 2 * group, n_layers)):
+                    loads(j)  # the next group's loads, queued before this group's forwards
+                for j in range(l, min(l + group, n_layers)):
+                    gate.wait(j, compute)
+            pools[l].layer_step(ios[l], ids_d, 1.0, stream=compute)
+        ev = torch.cuda.Event()
+        ev.record(compute)
+        step_end[k % 3] = ev
+
+    def timed(mode, k):
+        """Per-step device times (events on the compute stream) and the host's ms per step."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        t0 = time.perf_counter()
+        for i in range(k):
+            ev[i][0].record(compute)
+            step(mode)
+            ev[i][1].record(compute)
+        host_ms = (time.perf_counter() - t0) * 1e3 / k
+        torch.cuda.synchronize()
+        return sorted(a.elapsed_time(b) for a, b in ev), host_ms
+
+    res, host = {}, {}
+    for mode in ("resident", "pipelined", "serial"):
+        for _ in range(max(3, args.warmup)):
+            step(mode)
+        torch.cuda.synchronize()
+        res[mode], host[mode] = timed(mode, args.steps)
+    for l in range(n_layers):
+        code, detail = pools[l].last_device_error()
+        if code:
+            raise RuntimeError(f"device error {L.DEVERR.get(code)} at {detail} (layer {l})")
+    med = {k: statistics.median(v) for k, v in res.items()}
+    line = {"metric": "layers8: 8-layer decode step with cold-adapter loads in flight, tokens/s", "value": n / (med["pipelined"] / 1e3),
+            "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": med["pipelined"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "layers8_attn70b_decode_b128_r16_4cold", "layers": n_layers, "batch_rows": n,
+                       "rank": rank, "cold_adapters_per_step": n_cold,
+                       "projections": ", ".join(f"{m} {mods[m][0]}->{mods[m][1]}" for m in names),
+                       "l2": "no flush: each layer reads 302 MB of W, more than the 129 MB L2"},
+            "gpu_launches": n_layers * (1 + 2 * len(stages)) * args.steps,
+            "loads": {"bytes_per_step": load_bytes,
+                      "ms_per_step_resident": med["resident"],
+                      "ms_per_step_pipelined": med["pipelined"],
+                      "ms_per_step_serial": med["serial"],
+                      "pipelined_over_resident": med["pipelined"] / med["resident"] - 1,
+                      "serial_over_resident": med["serial"] / med["resident"] - 1,
+                      "copy_gbs_if_hidden": load_bytes / (med["resident"] / 1e3) / 1e9,
+                      "host_ms_per_step": host,
+                      "timing": "per-step device time (events on the compute stream), median of the steps"}}
+    print(json.dumps(line), flush=True)
+    gate.close()
+    for pool in pools:
+        pool.close()
 
 
 def _build():
@@ -523,6 +726,12 @@ def main():
     args = parse()
     if args.impl == "ours":
         _build()
+    if args.workload == "layers8":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle has no layer pipeline to time"}))
+        else:
+            run_layers(args)
+        return
     w = WORKLOADS[args.workload][0]()
     if args.impl == "reference":
         run_reference(args, w)

@@ -129,6 +129,60 @@ int lora_pool_load(lora_pool *pool, int32_t adapter_id, int32_t module, const vo
                    const void *B, int32_t rank, lora_stream_t stream);
 
 /*
+ * lora_pool_load_many -- lora_pool_load for n items in one call: each item's copies are queued
+ * on `stream` in item order, and the table entries are then written by one kernel launch per 64
+ * items instead of one per item (the host cost of a load is its launches).  Items apply in order,
+ * so a later item for the same (adapter, module) replaces an earlier one.  The call stops at the
+ * first item that fails: the items before it are loaded and published, *n_done (may be null)
+ * counts them, and the failing item leaves its (adapter, module) entry as lora_pool_load would:
+ * untouched for EINVAL (bad id, module, rank or pointer), cleared for ENOMEM (no free rows).
+ */
+typedef struct {
+    int32_t adapter;
+    int32_t module;
+    int32_t rank;
+    const void *A;  /* host or device bf16 [rank, d_in] */
+    const void *B;  /* host or device bf16 [d_out, rank] */
+} lora_load_item;
+int lora_pool_load_many(lora_pool *pool, int32_t n, const lora_load_item *items, int32_t *n_done,
+                        lora_stream_t stream);
+
+/*
+ * lora_pool_load_packed -- many bf16 loads from one packed host buffer: a single host->device copy
+ * of the whole blob into the caller's device staging buffer, then one kernel (per 96 items) that
+ * scatters every item's factors into its pool rows, zero-padded to the storage rank, and
+ * publishes its table entry.  Two launches however many items: the form for loading a cold
+ * adapter's factors for a layer while other layers run (see lora_layer_gate).
+ *  host_blob    host bf16 factors, pinned for an asynchronous copy; item i's A ([rank, d_in],
+ *               row-major) starts at byte a_offset (a multiple of 16), its B ([d_out, rank])
+ *               at b_offset (even)
+ *  dev_staging  device buffer of at least blob_bytes, 16-byte aligned, the caller's; it must not
+ *               be written while the call's kernels may still read it (same stream: in order)
+ * Every item is checked before anything is queued (EINVAL: bad id, module, rank or offset; then
+ * nothing is loaded).  Items then apply in order; ENOMEM (no free rows) stops at that item, whose
+ * entry is left cleared; *n_done (may be null) counts the items loaded.  Same visibility as
+ * lora_pool_load: forwards queued later on `stream` see the adapters.
+ */
+typedef struct {
+    int32_t adapter;
+    int32_t module;
+    int32_t rank;
+    int32_t pad_;
+    int64_t a_offset;
+    int64_t b_offset;
+} lora_packed_item;
+int lora_pool_load_packed(lora_pool *pool, int32_t n, const lora_packed_item *items, const void *host_blob,
+                          void *dev_staging, int64_t blob_bytes, int32_t *n_done, lora_stream_t stream);
+
+/*
+ * lora_pool_unload_many -- lora_pool_unload for n adapters, the table entries cleared by one
+ * kernel launch per 64.  Stops at the first id that is out of range (EINVAL) or resident in no
+ * module (ENOTLOADED); *n_done (may be null) counts the adapters unloaded.
+ */
+int lora_pool_unload_many(lora_pool *pool, int32_t n, const int32_t *adapter_ids, int32_t *n_done,
+                          lora_stream_t stream);
+
+/*
  * lora_pool_unload -- release adapter `adapter_id` from every module.  The table entries
  * are cleared on `stream`; the rows return to the free lists at once, so a later load may
  * reuse them: order it after every forward that still reads the adapter.
@@ -256,6 +310,29 @@ int lora_cache_release(lora_cache *cache, int32_t adapter);
 int lora_cache_stats(const lora_cache *cache, int64_t *used_bytes, int64_t *pinned_bytes, int32_t *resident);
 int lora_cache_resident(const lora_cache *cache, int32_t adapter, int32_t *resident, int32_t *ref);
 
+/*
+ * Layer gates -- adapter loads pipelined across the layers of a forward pass ("12. Adapter
+ * Serving and Multi-Tenant Customization", section "Switching cost: I/O, not compute": a cold
+ * adapter's factors are a copy, not a computation, so the factors a later layer needs can arrive
+ * while the earlier layers run).  A gate holds one CUDA event per layer, each layer with its own
+ * pool.  The loader queues layer l's loads on a copy stream (lora_pool_load / _load_many on that
+ * layer's pool) and then calls lora_layer_gate_mark(gate, l, copy_stream); the forward queues
+ * lora_layer_gate_wait(gate, l, compute_stream) just before layer l's first call, so the compute
+ * stream waits for layer l's copies only, never for a later layer's.  A layer never marked, or
+ * whose copies have already finished when the wait is queued, adds no wait (a stream wait between
+ * two forwards keeps the second from launching early on the first).  One wait may also cover
+ * several layers: marks of layers l .. l + g - 1 waited for before layer l.  Marking a layer again replaces its event (the waits queued after see the
+ * newest mark).  Unloads that free pages a queued forward still reads must be ordered after it
+ * (e.g. the copy stream waits for the compute stream before the step's unloads).
+ * lora_layer_gate_create  n_layers >= 1; uses the current device.  Errors: EINVAL, ECUDA.
+ * lora_layer_gate_mark / _wait   Errors: EINVAL (layer out of range), ECUDA.
+ */
+typedef struct lora_layer_gate lora_layer_gate;
+int lora_layer_gate_create(int32_t n_layers, lora_layer_gate **out);
+int lora_layer_gate_destroy(lora_layer_gate *gate);
+int lora_layer_gate_mark(lora_layer_gate *gate, int32_t layer, lora_stream_t copy_stream);
+int lora_layer_gate_wait(lora_layer_gate *gate, int32_t layer, lora_stream_t compute_stream);
+
 /* One projection of a layer call. */
 typedef struct {
     int32_t module;  /* pool module index */
@@ -347,6 +424,40 @@ int lora_linear_forward_static(const void *x, const void *W, int32_t d_in, int32
  * _unload and every forward that groups its own rows end it.  Errors: EINVAL, ECUDA.
  */
 int lora_plan_rows(lora_pool *pool, const int32_t *row_adapter_ids, int32_t n, lora_stream_t stream);
+
+/*
+ * lora_layer_step -- one layer of a decode step in one call: lora_plan_rows on the batch, then
+ * lora_layer_forward_planned for each stage in order (stage st runs stage_n[st] >= 1 projections
+ * that share an input, e.g. q/k/v, then o).  io holds the stages' entries one after another.
+ * Same outputs, errors and error word as those calls; stops at the first error.
+ */
+int lora_layer_step(lora_pool *pool, const int32_t *row_adapter_ids, int32_t n, int32_t n_stages,
+                    const int32_t *stage_n, const lora_module_io *io, float scale, int32_t y_dtype,
+                    lora_stream_t stream);
+
+/*
+ * lora_layer_step_host -- lora_layer_step with the step's inputs and outputs in host memory, one
+ * call per step.  The ids (host_ids -> row_adapter_ids, device int32 [n]) and every stage's input
+ * (host_x[st] -> that stage's io[].x, bf16 [n, d_in]) go up on an upload stream of the pool's; the
+ * rows are planned and the stages run on `stream`; each stage's outputs (io[i].y -> host_y[i],
+ * [n, d_out] of y_dtype) come down on a download stream of the pool's while the next stage -- or
+ * the next call -- computes.  The projections of a stage share one device x.
+ * Serving loop: alternate two sets of device buffers (ids, x, y; a set is known by its ids
+ * buffer): a call's inputs then go up while the previous call computes, and its outputs come down
+ * while the next one does.  A call waits only for the earlier calls on the same set (its inputs
+ * consumed, its outputs downloaded).  The outputs are in host memory once `stream` has passed a
+ * later lora_pool_host_wait(pool, stream), which makes `stream` wait for every download queued so
+ * far.  Host buffers should be pinned (pageable memory makes the copies synchronous); the host
+ * inputs may be rewritten, and the host outputs read, only after that point.  The device buffers
+ * are the caller's, borrowed.  Errors: EINVAL, and those of lora_layer_step.
+ */
+int lora_layer_step_host(lora_pool *pool, const int32_t *host_ids, int32_t *row_adapter_ids, int32_t n,
+                         int32_t n_stages, const int32_t *stage_n, const lora_module_io *io,
+                         const void *const *host_x, void *const *host_y, float scale, int32_t y_dtype,
+                         lora_stream_t stream);
+
+/* lora_pool_host_wait -- make `stream` wait for every download lora_layer_step_host has queued. */
+int lora_pool_host_wait(lora_pool *pool, lora_stream_t stream);
 
 /*
  * lora_layer_forward_planned -- lora_layer_forward on the rows of the last lora_plan_rows (same

@@ -106,3 +106,21 @@ def test_ring_slot_without_division():
         assert np.array_equal(k - q * np.uint64(S), k % np.uint64(S))
         top = np.arange((1 << 29) - (1 << 16), 1 << 29, dtype=np.uint64)
         assert np.array_equal((top * np.uint64(m)) >> np.uint64(32), top // np.uint64(S))
+
+
+def test_pack_factors_layout():
+    """pack_factors: every A at a 16-byte aligned offset, its B right after, bytes unchanged."""
+    import torch
+    L = pytest.importorskip("adapter_serving_gb300")
+    g = np.random.default_rng(0)
+    entries = []
+    for a, (r, d_in, d_out) in enumerate([(5, 24, 40), (8, 64, 16), (3, 8, 8)]):
+        A = g.integers(0, 2**16, (r, d_in), dtype=np.uint16)
+        B = g.integers(0, 2**16, (d_out, r), dtype=np.uint16)
+        entries.append((a, a % 2, A, B))
+    items, blob = L.pack_factors(entries, pin=False)
+    raw = blob.numpy()
+    for (a, m, A, B), (ia, im, r, ao, bo) in zip(entries, items):
+        assert (ia, im, r) == (a, m, A.shape[0]) and ao % 16 == 0 and bo == ao + A.nbytes
+        assert np.array_equal(raw[ao:ao + A.nbytes].view(np.uint16).reshape(A.shape), A)
+        assert np.array_equal(raw[bo:bo + B.nbytes].view(np.uint16).reshape(B.shape), B)
