@@ -393,7 +393,8 @@ def run_ours(args, w):
         hbm, src = peaks()
         g_launch, g_ms = kt["gemm"]
         achieved = ab["gemm"] * args.steps / (g_ms / 1e3) / 1e9
-        line["roofline"] = {"kernel": "decode_gemm_kernel (tcgen05: W tiles and the shrink's gathered A tiles, stream-K)",
+        line["roofline"] = {"kernel": "decode_gemm_kernel (tcgen05: W tiles" + (
+                                "" if int8 else " and the shrink's gathered A tiles") + ", stream-K)",
                             "bound": "hbm",
                             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                             "frac_of_8tbs": achieved / 8000.0,
@@ -714,12 +715,11 @@ def _build():
     mod.build()
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per gemm launch, mean of the qkv and
-# o launches of the workload, from an ncu capture of the current gemm kernel (bf16 base and int4
-# base); absent whenever the kernel has changed since the last capture.  The stream-K finish (finalize_kernel) is timed with
-# the gemm but its pieces are L2-resident in the live step, so its DRAM bytes are not added (under
-# ncu's cache control it re-reads them from DRAM).
-GEMM_DRAM_BYTES_PER_LAUNCH = {}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per decode_gemm_kernel launch, the
+# mean of the q/k/v and o launches of the workload, from the ncu captures summarised in profiles/
+# (decode_gemm_kernel_*); absent for a workload without a capture, and to be removed whenever the
+# kernel changes.
+GEMM_DRAM_BYTES_PER_LAUNCH = {"attn70b": 190903168, "zipf": 246150144, "attn70b_w4": 75282304}
 
 
 def main():
