@@ -417,8 +417,10 @@ int lora_linear_forward_static(const void *x, const void *W, int32_t d_in, int32
 /*
  * lora_plan_rows -- group a decode batch's rows once for every projection of the pool (the
  * index vector of "m07", section 6, is one per batch): stable sort by adapter id, id checks
- * (device error word), and every module's expand packs.  Then lora_layer_forward_planned runs
- * any projections of the pool on that batch without grouping again.
+ * (device error word), each row's adapter per projection, and every projection's gather list of
+ * the batch's distinct adapters' A rows (8-row groups, the shrink's tiles).  Then
+ * lora_layer_forward_planned runs any projections of the pool on that batch without grouping
+ * again.
  *  row_adapter_ids  device int32 [n], -1 = base only; 0 <= n <= min(LORA_MAX_DECODE_ROWS, max_rows)
  * Asynchronous on `stream`.  The plan lives in the pool's workspace: lora_pool_load / _load_i8 /
  * _unload and every forward that groups its own rows end it.  Errors: EINVAL, ECUDA.
