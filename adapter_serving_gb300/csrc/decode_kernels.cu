@@ -556,15 +556,22 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
         bool ok = true;
         while (ok && sc.next(p, &dsh, it)) {
             const DecodeModule &M = p.mod[it.m];
-            // A tile: lane l < 16 gathers group 16 tile + l (8 rows of one adapter's A)
+            // A tile: lane l < 16 gathers group 16 tile + l (8 rows of one adapter's A) -- unless the
+            // tile's groups are consecutive rows of the slab (adapters stored one after another):
+            // then one 128-row box, laid out like a W tile (rows past the last group are computed
+            // and dropped; past the slab, the copy fills zeros)
             int arow = 0;
-            bool mine = false;
+            bool mine = false, runs = false;
             uint32_t a_tx = 0;
             if (it.a) {
                 const int g = it.tile * kTileGroups + lane;
                 mine = lane < kTileGroups && g < dsh.n_groups[it.m];
                 if (mine) arow = M.groups[g].row;
-                a_tx = (uint32_t)__popc(__ballot_sync(0xffffffffu, mine)) * (uint32_t)(kps * kGroupRows * kBK * 2);
+                const int arow0 = __shfl_sync(0xffffffffu, arow, 0);
+                runs = M.a_runs && __all_sync(0xffffffffu, !mine || arow == arow0 + kGroupRows * lane);
+                arow = runs ? arow0 : arow;
+                a_tx = runs ? (uint32_t)(kps * kBM * kBK * 2)
+                            : (uint32_t)__popc(__ballot_sync(0xffffffffu, mine)) * (uint32_t)(kps * kGroupRows * kBK * 2);
             }
             for (int kb = it.kb0; kb < it.kb1; ++kb, ++k) {
                 const uint32_t sl = rslot(k);
@@ -585,7 +592,11 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                     } else {
                         if (lane == 0) mbar_arrive_expect_tx(wfull + sl, a_tx + x_bytes);
                         __syncwarp();
-                        if (mine) load(sa + lane * (kps * kGroupRows * kBK * 2), &M.tmA, wfull + sl, kb, kBK, arow, pol_w);
+                        if (runs) {
+                            if (lane == 0) load(sa, &M.tmA128, wfull + sl, kb, kBK, arow, pol_w);
+                        } else if (mine) {
+                            load(sa + lane * (kps * kGroupRows * kBK * 2), &M.tmA, wfull + sl, kb, kBK, arow, pol_w);
+                        }
                     }
                 }
                 if (lane == 0) load(sa + a_bytes, &M.tmX, wfull + sl, kb, kBK, 0, pol_x);
@@ -607,6 +618,17 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
             bool ok = true;
             while (ok && sc.next(p, &dsh, it)) {
                 const int buf = li & 1;
+                // the producer's choice for an A tile: one 128-row box when its groups are
+                // consecutive slab rows (then laid out like a W tile), else 8-row gathers
+                bool gathered = false;
+                if (it.a) {
+                    const DecodeModule &Ma = p.mod[it.m];
+                    const int ng = dsh.n_groups[it.m], g0 = it.tile * kTileGroups;
+                    gathered = !Ma.a_runs;
+                    const int r0 = Ma.groups[g0].row;
+                    for (int i = 1; i < kTileGroups && g0 + i < ng && !gathered; ++i)
+                        gathered = Ma.groups[g0 + i].row != r0 + kGroupRows * i;
+                }
                 if (!mbar_wait(acc_free + buf, ((li >> 1) & 1) ^ 1, abort_flag, p.err, wait_ns)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * nt);
@@ -619,9 +641,10 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
                     for (int q = 0; q < kps; ++q) {
-                        // W: sub-block q at q * 16 KiB, 1 KiB atoms; A tile: at q KiB, atoms kps KiB apart
-                        const uint64_t da = it.a ? sdesc_kmajor_sw128(sa + (uint32_t)q * 1024u, (uint32_t)kps * 1024u)
-                                                 : sdesc_kmajor_sw128(sa + (uint32_t)q * sub_a);
+                        // W (and a contiguous A tile): sub-block q at q * 16 KiB, 1 KiB atoms; a gathered
+                        // A tile: at q KiB, atoms kps KiB apart
+                        const uint64_t da = gathered ? sdesc_kmajor_sw128(sa + (uint32_t)q * 1024u, (uint32_t)kps * 1024u)
+                                                     : sdesc_kmajor_sw128(sa + (uint32_t)q * sub_a);
                         const uint64_t db = sdesc_kmajor_sw128(sa + a_bytes + (uint32_t)q * sub_x);
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)

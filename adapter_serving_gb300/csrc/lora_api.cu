@@ -90,6 +90,8 @@ struct ModuleStore {
     uint16_t *B = nullptr;  // [pages * 64 * d_out] (rank-major runs of [d_out, rp])
     float *fold = nullptr;  // int8 pool: [pages * 64] scale of each stored row (A scale x B scale)
     CUtensorMap tmA[2];     // bf16 pool: the A slab for the decode gemm's A-tile gathers, box {64, 8}
+    CUtensorMap tmA128[2];  // the same slab, box {64, 128}: A tiles whose 16 groups are consecutive rows
+    bool a_runs = false;    // tmA128 made (the slab has at least 128 rows)
                             // ([0]: one k-block per box; [1]: two, when d_in % 64 == 0)
     RowAllocator rows;
 };
@@ -425,6 +427,14 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
                              (ms.d_in % 64 == 0 && (rc = make_tmap(&ms.tmA[1], ms.A, rows, ms.d_in, kGroupRows, 2))))) {
             lora_pool_destroy(p);
             return rc;
+        }
+        if (rows >= kBM) {
+            if ((rc = make_tmap(&ms.tmA128[0], ms.A, rows, ms.d_in, kBM, 1)) ||
+                (ms.d_in % 64 == 0 && (rc = make_tmap(&ms.tmA128[1], ms.A, rows, ms.d_in, kBM, 2)))) {
+                lora_pool_destroy(p);
+                return rc;
+            }
+            ms.a_runs = true;
         }
     }
     cudaError_t e = cudaSuccess;
@@ -932,7 +942,11 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
         }
         if (rc) return rc;
         if ((rc = make_tmap(&dm.tmX, io[i].x, n, ms.d_in, nt, dp.kps))) return rc;
-        if (!p->i8) dm.tmA = ms.tmA[dp.kps - 1];
+        if (!p->i8) {
+            dm.tmA = ms.tmA[dp.kps - 1];
+            dm.tmA128 = ms.tmA128[dp.kps - 1];
+            dm.a_runs = ms.a_runs ? 1 : 0;
+        }
         const int sl = slot_of[i];
         dm.groups = p->groups + (size_t)sl * kDecMaxGroups;
         dm.n_groups = p->n_groups + sl;

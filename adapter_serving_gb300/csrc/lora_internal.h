@@ -75,6 +75,7 @@ struct DecodeModule {
                       // [d_out, d_in / 2] bytes, box {32, 128(, kps)}, no swizzle
     CUtensorMap tmX;  // x [n, d_in] bf16, box {64, nt(, kps)}, 128B swizzle
     CUtensorMap tmA;  // A slab [rows, d_in] bf16, box {64, 8(, kps)}, 128B swizzle (bf16 factors)
+    CUtensorMap tmA128;  // the same slab, box {64, 128(, kps)}: an A tile whose groups are consecutive rows
     const float *w_scale;      // int4 base: [d_out] fp32 row scales
     const AGroup *groups;      // [kDecMaxGroups] this projection's gathered groups
     const int32_t *n_groups;   // device: number of groups
@@ -88,6 +89,7 @@ struct DecodeModule {
     int32_t k_blocks;          // k-steps of a tile (kps k-blocks of 64 each)
     int32_t w_iter_begin;      // first (W tile, k-step) index of this projection
     int32_t w_tile_begin;      // first W tile of this projection
+    int32_t a_runs;            // 1: tmA128 is valid (the slab has at least 128 rows)
 };
 
 struct DecodeParams {

@@ -182,6 +182,11 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     if (make_tmap(&dm.tmW, W, d_out, d_in, kBM, dp.kps) || make_tmap(&dm.tmX, x, n, d_in, nt, dp.kps) ||
         make_tmap(&dm.tmA, n_adapters > 0 ? A_stack : W, a_rows, d_in, kGroupRows, dp.kps))
         return LORA_ECUDA;  // the reason is already recorded
+    dm.a_runs = 0;
+    if (a_rows >= kBM) {  // A tiles of consecutive adapters' rows: one 128-row box
+        if (make_tmap(&dm.tmA128, A_stack, a_rows, d_in, kBM, dp.kps)) return LORA_ECUDA;
+        dm.a_runs = 1;
+    }
     dm.groups = pp.groups[0];
     dm.n_groups = pp.n_groups;
     dm.rowinfo = pp.rowinfo[0];
