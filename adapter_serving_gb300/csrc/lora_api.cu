@@ -869,8 +869,11 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
     cudaError_t e;
     const int nt = (n + 15) & ~15;
     const int rpmax = p->rpmax();
+    // int8 factors: the CUDA-core shrink, launched after the gemm (which needs no t) so that it
+    // runs beside the gemm's W stream; the finalize then waits for both
+    ShrinkParams sp{};
+    int shrink_splits = 0;
     if (p->i8) {
-        ShrinkParams sp{};
         sp.n_mod = n_io;
         sp.n = n;
         sp.rpmax = rpmax;
@@ -901,8 +904,7 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
             splits += sp.ksplit[i];
         }
         sp.split_begin[n_io] = splits;
-        e = timed_launch(p, LORA_KERNEL_SHRINK, s, [&] { return launch_shrink(sp, n, splits, s); });
-        if (e != cudaSuccess) return cuda_fail(e, "shrink kernel");
+        shrink_splits = splits;
     }
 
     DecodeParams dp;
@@ -974,6 +976,10 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
     if (!plan_decode_gemm(dp, &smem)) return LORA_EUNSUPPORTED;
     e = timed_launch(p, LORA_KERNEL_GEMM, s, [&] { return launch_decode_gemm(dp, smem, s); });
     if (e != cudaSuccess) return cuda_fail(e, "gemm kernel");
+    if (p->i8) {
+        e = timed_launch(p, LORA_KERNEL_SHRINK, s, [&] { return launch_shrink(sp, n, shrink_splits, s); });
+        if (e != cudaSuccess) return cuda_fail(e, "shrink kernel");
+    }
     size_t fsmem = 0;
     plan_decode_finalize(dp, &fsmem);
     e = timed_launch(p, LORA_KERNEL_FINALIZE, s, [&] { return launch_decode_finalize(dp, fsmem, s); });

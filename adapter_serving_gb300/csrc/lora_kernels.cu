@@ -268,10 +268,7 @@ __global__ void __launch_bounds__(kShrinkThreads) shrink_kernel(const __grid_con
 // 8-byte loads of A codes up front, then reads the row's x from L2.  Partial sums of the splits are
 // combined by the last block of the position, in split order.  t_j is scaled by s and by the rank
 // row's fold scale (A scale x B scale) and written to row perm[q] of T.
-__global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const __grid_constant__ ShrinkParams p) {
-    __shared__ int s_last;
-    grid_dep_wait();
-    grid_dep_launch();
+__device__ __forceinline__ void shrink_decode_body(const ShrinkParams &p, int &s_last) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int m = 0;
     while (m + 1 < p.n_mod && p.split_begin[m + 1] <= (int)blockIdx.y) ++m;
@@ -344,6 +341,18 @@ __global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const 
         trow[j] = j < r ? scale * fold[j] * v : 0.f;
     }
     if (tid == 0) p.counters[m * p.max_units + u] = 0;
+}
+
+// Launched right after the gemm (on the gemm's trigger, which follows the gemm's own wait for the
+// row plan), so it reads the plan, the pool and x without waiting, and runs on the resources the
+// persistent gemm leaves free while the gemm streams W.  It never reads the gemm's results.  Block
+// (0, 0) waits for the gemm before it exits: the grid then completes only after the gemm has, and
+// the finalize's one wait covers both.
+__global__ void __launch_bounds__(kShrinkThreads, 3) shrink_decode_kernel(const __grid_constant__ ShrinkParams p) {
+    __shared__ int s_last;
+    grid_dep_launch();
+    shrink_decode_body(p, s_last);
+    if (blockIdx.x == 0 && blockIdx.y == 0) grid_dep_wait();
 }
 
 // ============================================================================ gemm ==========
