@@ -280,10 +280,15 @@ struct DecShared {
 };
 
 __device__ void dec_a_space(const DecodeParams &p, DecShared &d) {
+    // every projection's group count in flight at once (one round trip, not one per projection)
+    int gs[LORA_MAX_MODULES];
+#pragma unroll
+    for (int m = 0; m < LORA_MAX_MODULES; ++m) gs[m] = (m < p.n_mod && p.shrink_tc) ? __ldcg(p.mod[m].n_groups) : 0;
     int it = 0, kbn_max = 0;
-    for (int m = 0; m < p.n_mod; ++m) {
-        int g = p.shrink_tc ? *p.mod[m].n_groups : 0;
-        g = min(max(g, 0), kDecMaxGroups);
+#pragma unroll
+    for (int m = 0; m < LORA_MAX_MODULES; ++m) {
+        if (m >= p.n_mod) break;
+        const int g = min(max(gs[m], 0), kDecMaxGroups);
         const int at = (g + kTileGroups - 1) / kTileGroups;
         d.n_groups[m] = g;
         d.a_begin[m] = it;
@@ -624,10 +629,13 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 if (it.a) {
                     const DecodeModule &Ma = p.mod[it.m];
                     const int ng = dsh.n_groups[it.m], g0 = it.tile * kTileGroups;
+                    int rows[kTileGroups];  // all loads in flight at once
+#pragma unroll
+                    for (int i = 0; i < kTileGroups; ++i) rows[i] = g0 + i < ng ? __ldg(&Ma.groups[g0 + i].row) : 0;
                     gathered = !Ma.a_runs;
-                    const int r0 = Ma.groups[g0].row;
-                    for (int i = 1; i < kTileGroups && g0 + i < ng && !gathered; ++i)
-                        gathered = Ma.groups[g0 + i].row != r0 + kGroupRows * i;
+#pragma unroll
+                    for (int i = 1; i < kTileGroups; ++i)
+                        gathered = gathered || (g0 + i < ng && rows[i] != rows[0] + kGroupRows * i);
                 }
                 if (!mbar_wait(acc_free + buf, ((li >> 1) & 1) ^ 1, abort_flag, p.err, wait_ns)) break;
                 tc_fence_after();
