@@ -564,8 +564,12 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
             // A tile: lane l < 16 gathers group 16 tile + l (8 rows of one adapter's A) -- unless the
             // tile's groups are consecutive rows of the slab (adapters stored one after another):
             // then one 128-row box, laid out like a W tile (rows past the last group are computed
-            // and dropped; past the slab, the copy fills zeros)
-            int arow = 0;
+            // and dropped)
+            // (rows past the slab, the copy fills zeros).  With one k-block per stage the gathers
+            // go one box per run of consecutive groups instead: a run of length L splits into boxes
+            // of L's binary digits, largest first (an adapter's groups are one run of 1, 2, 4 or 8),
+            // and the lane at a box's first group issues it (box = log2 of its groups, -1: none).
+            int arow = 0, box = -1;
             bool mine = false, runs = false;
             uint32_t a_tx = 0;
             if (it.a) {
@@ -573,10 +577,21 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 mine = lane < kTileGroups && g < dsh.n_groups[it.m];
                 if (mine) arow = M.groups[g].row;
                 const int arow0 = __shfl_sync(0xffffffffu, arow, 0);
+                const int prev = __shfl_up_sync(0xffffffffu, arow, 1);
                 runs = M.a_runs && __all_sync(0xffffffffu, !mine || arow == arow0 + kGroupRows * lane);
+                const unsigned valid = __ballot_sync(0xffffffffu, mine);
+                // runs are cut at group 8 too, so no box is longer than 8 groups (64 rows)
+                const unsigned starts = __ballot_sync(0xffffffffu, mine && (lane == 0 || lane == 8 || arow != prev + kGroupRows));
+                if (M.a_boxes && mine) {
+                    const unsigned upto = (2u << lane) - 1u;                  // lanes 0..lane
+                    const int s0 = 31 - __clz(starts & upto);                 // this run's first lane
+                    const int e = __ffs((starts | ~valid) & ~upto) - 1;       // the next run's (lanes >= 16 are not valid)
+                    const int len = e - s0, pos = lane - s0;
+                    const int tb = 31 - __clz(len - pos);                     // the box at pos, if one starts there
+                    box = pos == ((len >> (tb + 1)) << (tb + 1)) ? tb : -1;
+                }
                 arow = runs ? arow0 : arow;
-                a_tx = runs ? (uint32_t)(kps * kBM * kBK * 2)
-                            : (uint32_t)__popc(__ballot_sync(0xffffffffu, mine)) * (uint32_t)(kps * kGroupRows * kBK * 2);
+                a_tx = runs ? (uint32_t)(kps * kBM * kBK * 2) : (uint32_t)__popc(valid) * (uint32_t)(kps * kGroupRows * kBK * 2);
             }
             for (int kb = it.kb0; kb < it.kb1; ++kb, ++k) {
                 const uint32_t sl = rslot(k);
@@ -599,6 +614,9 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                         __syncwarp();
                         if (runs) {
                             if (lane == 0) load(sa, &M.tmA128, wfull + sl, kb, kBK, arow, pol_w);
+                        } else if (M.a_boxes) {
+                            if (box >= 0)
+                                load(sa + lane * (kGroupRows * kBK * 2), box == 0 ? &M.tmA : &M.tmAb[box - 1], wfull + sl, kb, kBK, arow, pol_w);
                         } else if (mine) {
                             load(sa + lane * (kps * kGroupRows * kBK * 2), &M.tmA, wfull + sl, kb, kBK, arow, pol_w);
                         }

@@ -92,6 +92,8 @@ struct ModuleStore {
     CUtensorMap tmA[2];     // bf16 pool: the A slab for the decode gemm's A-tile gathers, box {64, 8}
     CUtensorMap tmA128[2];  // the same slab, box {64, 128}: A tiles whose 16 groups are consecutive rows
     bool a_runs = false;    // tmA128 made (the slab has at least 128 rows)
+    CUtensorMap tmAb[3];    // the same slab, box {64, 16 / 32 / 64}, one k-block: runs of consecutive groups
+    bool a_boxes = false;   // tmAb made
                             // ([0]: one k-block per box; [1]: two, when d_in % 64 == 0)
     RowAllocator rows;
 };
@@ -435,6 +437,14 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
                 return rc;
             }
             ms.a_runs = true;
+        }
+        if (ms.pages > 0) {  // at least 64 rows
+            for (int j = 0; j < 3; ++j)
+                if ((rc = make_tmap(&ms.tmAb[j], ms.A, rows, ms.d_in, kGroupRows << (j + 1), 1))) {
+                    lora_pool_destroy(p);
+                    return rc;
+                }
+            ms.a_boxes = true;
         }
     }
     cudaError_t e = cudaSuccess;
@@ -948,6 +958,9 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
             dm.tmA = ms.tmA[dp.kps - 1];
             dm.tmA128 = ms.tmA128[dp.kps - 1];
             dm.a_runs = ms.a_runs ? 1 : 0;
+            dm.a_boxes = (dp.kps == 1 && ms.a_boxes) ? 1 : 0;
+            if (dm.a_boxes)
+                for (int j = 0; j < 3; ++j) dm.tmAb[j] = ms.tmAb[j];
         }
         const int sl = slot_of[i];
         dm.groups = p->groups + (size_t)sl * kDecMaxGroups;

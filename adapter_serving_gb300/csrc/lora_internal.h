@@ -76,6 +76,7 @@ struct DecodeModule {
     CUtensorMap tmX;  // x [n, d_in] bf16, box {64, nt(, kps)}, 128B swizzle
     CUtensorMap tmA;  // A slab [rows, d_in] bf16, box {64, 8(, kps)}, 128B swizzle (bf16 factors)
     CUtensorMap tmA128;  // the same slab, box {64, 128(, kps)}: an A tile whose groups are consecutive rows
+    CUtensorMap tmAb[3]; // kps = 1: the same slab, box {64, 16 / 32 / 64}: 2 / 4 / 8 consecutive groups
     const float *w_scale;      // int4 base: [d_out] fp32 row scales
     const AGroup *groups;      // [kDecMaxGroups] this projection's gathered groups
     const int32_t *n_groups;   // device: number of groups
@@ -90,6 +91,7 @@ struct DecodeModule {
     int32_t w_iter_begin;      // first (W tile, k-step) index of this projection
     int32_t w_tile_begin;      // first W tile of this projection
     int32_t a_runs;            // 1: tmA128 is valid (the slab has at least 128 rows)
+    int32_t a_boxes;           // 1: tmAb is valid and kps = 1 (gathers go as one box per run of groups)
 };
 
 struct DecodeParams {

@@ -183,6 +183,7 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
         make_tmap(&dm.tmA, n_adapters > 0 ? A_stack : W, a_rows, d_in, kGroupRows, dp.kps))
         return LORA_ECUDA;  // the reason is already recorded
     dm.a_runs = 0;
+    dm.a_boxes = 0;
     if (a_rows >= kBM) {  // A tiles of consecutive adapters' rows: one 128-row box
         if (make_tmap(&dm.tmA128, A_stack, a_rows, d_in, kBM, dp.kps)) return LORA_ECUDA;
         dm.a_runs = 1;
