@@ -734,18 +734,33 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 const AGroup *const groups = M.groups;
                 int32_t *const acount = M.acount;
                 const float scale = p.scale;
-                for (int gg = 0; gg < 32 / kGroupRows; ++gg) {
-                    const int gw = it.tile * kTileGroups + (lane_base / kGroupRows) + gg;
-                    if (gw >= ng) break;  // warp-uniform
-                    const AGroup ag = groups[gw];
-                    const int r = ag.rbase + (lane & (kGroupRows - 1));
-                    const bool keep = (lane / kGroupRows) == gg && r < ag.rank;
-                    for (int q = ag.q0; q < ag.q1; ++q) {
-                        const int j = perm_s[q];
-                        const uint32_t v = tmem_ld1(tacc + (uint32_t)j);
-                        tmem_ld_wait();
-                        if (keep) tpart[part * pstride + (size_t)j * LORA_MAX_RANK + r] = __uint_as_float(v);
+                // the lane's group and rank row; the groups are in segment order, so the batch rows
+                // (sorted positions) of a warp's four groups are one range [wq0, wq1)
+                int q0 = 0, q1 = 0, r = 0;
+                if (gok) {
+                    const AGroup ag = groups[g];
+                    q0 = ag.q0;
+                    q1 = ag.q1;
+                    r = ag.rbase + (o & (kGroupRows - 1));
+                    if (r >= ag.rank) q1 = q0;  // a padding row of the group: nothing to keep
+                }
+                const int wq0 = __shfl_sync(0xffffffffu, q0, 0);
+                const int wq1 = (int)__reduce_max_sync(0xffffffffu, (unsigned)q1);
+                // this CTA's part: per batch row of the range, one warp-wide TMEM load of its column
+                // (four in flight), kept by the lanes whose group owns the row
+                for (int qb = wq0; qb < wq1; qb += 4) {
+                    uint32_t v[4];
+                    int jc[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        jc[u] = perm_s[min(qb + u, wq1 - 1)];
+                        v[u] = tmem_ld1(tacc + (uint32_t)jc[u]);
                     }
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (qb + u >= q0 && qb + u < q1)
+                            tpart[part * pstride + (size_t)jc[u] * LORA_MAX_RANK + r] = __uint_as_float(v[u]);
                 }
                 // the tile's last CTA (a counter, no waiting) adds the parts in k order: t = s * sum
                 const int na = cta_of(it.it0 + kbn - 1, dsh.a_iters, dsh.a_ctas) - a_first + 1;
@@ -755,24 +770,33 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 named_bar_sync(1, 128);
                 if (s_last) {
                     __threadfence();
-                    if (gok) {
-                        const AGroup ag = groups[g];
-                        const int r = ag.rbase + (o & (kGroupRows - 1));
-                        if (r < ag.rank)
-                            for (int q = ag.q0; q < ag.q1; ++q) {
-                                const int j = perm_s[q];
-                                const float *tp = tpart + (size_t)j * LORA_MAX_RANK + r;
-                                float sum = 0.f;
-                                for (int cp = 0; cp < na; cp += 8) {  // eight parts' loads in flight, k order
-                                    float part[8];
+                    for (int qb = wq0; qb < wq1; qb += 2) {  // two rows' parts in flight
+                        bool own[2];
+                        int jr[2];
+                        float sum[2] = {0.f, 0.f};
 #pragma unroll
-                                    for (int c = 0; c < 8; ++c) part[c] = cp + c < na ? __ldcg(tp + (cp + c) * pstride) : 0.f;
+                        for (int u = 0; u < 2; ++u) {
+                            own[u] = qb + u >= q0 && qb + u < q1;
+                            jr[u] = own[u] ? perm_s[qb + u] : 0;
+                        }
+                        for (int cp = 0; cp < na; cp += 8) {  // eight parts per row in flight, k order
+                            float pt[2][8];
 #pragma unroll
-                                    for (int c = 0; c < 8; ++c)
-                                        if (cp + c < na) sum = (cp + c == 0) ? part[c] : sum + part[c];
-                                }
-                                tfin[(size_t)j * LORA_MAX_RANK + r] = scale * sum;
-                            }
+                            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    pt[u][c] = own[u] && cp + c < na
+                                                   ? __ldcg(tpart + (size_t)(cp + c) * pstride + (size_t)jr[u] * LORA_MAX_RANK + r)
+                                                   : 0.f;
+#pragma unroll
+                            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    if (cp + c < na) sum[u] = (cp + c == 0) ? pt[u][c] : sum[u] + pt[u][c];
+                        }
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+                            if (own[u]) tfin[(size_t)jr[u] * LORA_MAX_RANK + r] = scale * sum[u];
                     }
                 }
             }
