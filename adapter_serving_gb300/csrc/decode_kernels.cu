@@ -376,15 +376,10 @@ struct DSched {
     }
 };
 
-// Base pieces are kept in column quads: element (column c, lane o) at ((c / 4) * 128 + o) * 4 +
-// c % 4.  A thread's 16 columns are four 16-byte vectors and a warp stores or loads 512
-// contiguous bytes per instruction.
-__device__ __forceinline__ float4 *piece_quads(float *piece, int c0, int o) {
-    return reinterpret_cast<float4 *>(piece) + (size_t)(c0 >> 2) * kBM + o;
-}
-__device__ __forceinline__ const float4 *piece_quads(const float *piece, int c0, int o) {
-    return reinterpret_cast<const float4 *>(piece) + (size_t)(c0 >> 2) * kBM + o;
-}
+// Base pieces are kept by sorted position: the value of batch row j (the MMA's column j) for output
+// row o of the tile sits at (pos(j) * 128 + o), pos(j) being j's place in the adapter-sorted order.
+// A warp stores 128 contiguous bytes per column, and the finalize, which walks rows in sorted order,
+// reads 512 contiguous bytes per row.
 
 // W4: the int4 codes of one W k-block ([128 rows][32 bytes] as the TMA lays the box down) into the
 // bf16 tile of the integers the MMA reads ([128 rows][64], 128-byte swizzle: the 16-byte chunk j of
@@ -461,6 +456,7 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ DecShared dsh;
     __shared__ int32_t perm_s[LORA_MAX_DECODE_ROWS];
+    __shared__ int16_t pos_s[LORA_MAX_DECODE_ROWS];  // the inverse: sorted position of batch row j
     __shared__ int s_last;
     const int S = p.n_stages;
     // Ring slot and round of fill k without an integer division in the loops:
@@ -549,7 +545,11 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
     // reading anything this grid writes.
     if (threadIdx.x == 0) grid_dep_launch();
     if (threadIdx.x == 32) dec_a_space(p, dsh);
-    for (int q = threadIdx.x; q < p.n; q += blockDim.x) perm_s[q] = p.perm[q];
+    for (int q = threadIdx.x; q < p.n; q += blockDim.x) {
+        const int j = p.perm[q];
+        perm_s[q] = j;
+        pos_s[j] = (int16_t)q;
+    }
     __syncthreads();
 
     if (warp == 0) {
@@ -714,11 +714,9 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                     uint32_t r[16];
                     tmem_ld16(tacc + (uint32_t)c0, r);
                     tmem_ld_wait();
-                    float4 *q = piece_quads(piece, c0, o);
 #pragma unroll
-                    for (int kq = 0; kq < 4; ++kq)
-                        __stcg(q + kq * kBM, make_float4(__uint_as_float(r[4 * kq]) * wsc, __uint_as_float(r[4 * kq + 1]) * wsc,
-                                                         __uint_as_float(r[4 * kq + 2]) * wsc, __uint_as_float(r[4 * kq + 3]) * wsc));
+                    for (int i = 0; i < 16; ++i)
+                        if (c0 + i < p.n) __stcg(piece + (size_t)pos_s[c0 + i] * kBM + o, __uint_as_float(r[i]) * wsc);
                 }
             } else {
                 // shrink piece: lane o is slot row 128 tile + o; only the columns of the rows whose
@@ -846,18 +844,19 @@ __device__ __forceinline__ int bchunk_slot(int o, int ch, int nch) {
     return o * nch + (ch ^ (((o * nch) >> 3) & (nch - 1)));
 }
 
-// The B tiles (output rows o_base .. o_base + tile_rows - 1) of the rows k0 .. k1 - 1 into `buf`,
+// The B tiles (output rows o_base .. o_base + tile_rows - 1) of the rows k0 .. k1 - 1 (but those in
+// `skip`, whose tile another row stages) into `buf`,
 // every thread of the block copying consecutive chunks of each tile (coalesced), one cp.async group.
 // Out of line: the finalize is short-lived and starts cold, so its code is kept small.
 template <bool I8>
-__device__ __noinline__ void fin_stage(const RowInfo *s_ri, const int *s_off, int k0, int k1, uint8_t *buf,
+__device__ __noinline__ void fin_stage(const RowInfo *s_ri, const int *s_off, unsigned skip, int k0, int k1, uint8_t *buf,
                                        int o_base, int tile_rows) {
     using BChunk = typename std::conditional<I8, uint2, uint4>::type;
     constexpr int cu = sizeof(BChunk);
 #pragma unroll 4
     for (int k = k0; k < k1; ++k) {
         const RowInfo ri = s_ri[k];
-        if (ri.rank <= 0) continue;
+        if (ri.rank <= 0 || ((skip >> k) & 1u)) continue;
         const int lg = __ffs(ri.rp >> 3) - 1, nch = 1 << lg;  // chunks per row: 1, 2, 4 or 8
         const BChunk *src = reinterpret_cast<const BChunk *>(ri.B) + ((size_t)o_base << lg);
         const uint32_t dst = smem_u32(buf + s_off[k]);
@@ -886,6 +885,9 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     RowInfo *s_ri = reinterpret_cast<RowInfo *>(ts + kFinRows * rpmax);
     int *s_off = reinterpret_cast<int *>(s_ri + kFinRows);  // [16] byte offset of row k's tile
     int *s_pend = s_off + kFinRows;                        // [17] end row of pass i
+    int *s_j = s_pend + kFinRows + 1;                      // [16] batch row of row k
+    int *s_skip = s_j + kFinRows;                          // rows staged by an earlier row (bit k)
+    // the block's rows are the sorted positions c0 .. c0 + 15 (rows of one adapter are adjacent)
     const int tid = threadIdx.x, tile = blockIdx.x, c0 = blockIdx.y * kFinRows;
     int m = 0;
     while (m + 1 < p.n_mod && p.mod[m + 1].w_tile_begin <= tile) ++m;
@@ -911,23 +913,36 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     const int tile_rows = min(kBM, d_out - o_base);
     // ---- before the gemm has finished: the rows' adapters (the row plan is complete: the gemm
     // launched this grid only after its own wait), the pass plan, and the first passes' B tiles.
-    // Warp 0 plans in registers: lane k holds row k; passes are taken greedily in row order.
+    // Warp 0 plans in registers: lane k holds row k; passes are taken greedily in row order, and a
+    // row with the adapter of the row before it reads that row's tile.
     if (tid < 32) {
         RowInfo ri{nullptr, 0, 0, 0};
+        int j = 0;
         if (tid < nrows) {
-            const uint4 raw = __ldcg(reinterpret_cast<const uint4 *>(rowinfo + c0 + tid));
+            j = __ldcg(p.perm + c0 + tid);
+            const uint4 raw = __ldcg(reinterpret_cast<const uint4 *>(rowinfo + j));
             ri = *reinterpret_cast<const RowInfo *>(&raw);
         }
-        const int bytes = tid < nrows && ri.rank > 0 ? kBM * (ri.rp >> 3) * (int)sizeof(BChunk) : 0;
-        int used = 0, np = 0, off = 0;
+        const bool has = tid < nrows && ri.rank > 0;
+        const int bytes = has ? kBM * (ri.rp >> 3) * (int)sizeof(BChunk) : 0;
+        const unsigned long long bp = has ? reinterpret_cast<unsigned long long>(ri.B) : 0ull;
+        const unsigned long long bprev = __shfl_up_sync(0xffffffffu, bp, 1);
+        const bool same = has && tid > 0 && bprev == bp;  // the previous row's adapter
+        const unsigned same_mask = __ballot_sync(0xffffffffu, same);
+        int used = 0, np = 0, off = 0, last = 0;
         for (int k = 0; k < nrows; ++k) {
             const int b = __shfl_sync(0xffffffffu, bytes, k);
+            if ((same_mask >> k) & 1u) {  // same pass as row k - 1: its tile
+                if (tid == k) off = last;
+                continue;
+            }
             if (k > 0 && used + b > buf_bytes) {  // row k opens pass np + 1
                 if (tid == 0) s_pend[np] = k;
                 ++np;
                 used = 0;
             }
             if (tid == k) off = used;
+            last = used;
             used += b;
         }
         if (tid == 0) s_pend[np] = nrows;
@@ -935,13 +950,16 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
         if (tid < kFinRows) {
             s_ri[tid] = ri;
             s_off[tid] = off;
+            s_j[tid] = j;
         }
+        if (tid == 0) *s_skip = (int)same_mask;  // rows whose tile an earlier row stages
     }
     __syncthreads();
     int n_pass = 0;
     while (n_pass < kFinRows && s_pend[n_pass] >= 0) ++n_pass;
+    const unsigned skip = (unsigned)*s_skip;
     for (int i = 0; i < min(nbuf, n_pass); ++i)
-        fin_stage<I8>(s_ri, s_off, i == 0 ? 0 : s_pend[i - 1], s_pend[i], fsm + (size_t)i * buf_bytes, o_base, tile_rows);
+        fin_stage<I8>(s_ri, s_off, skip, i == 0 ? 0 : s_pend[i - 1], s_pend[i], fsm + (size_t)i * buf_bytes, o_base, tile_rows);
     grid_dep_wait();
     grid_dep_launch();
     // the gemm is complete: its A-tile counters start the next call at zero (even after a call
@@ -958,7 +976,7 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
         const int e = tid + i * kBM, jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
         tv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (jj < kFinRows && r < s_ri[jj].rank) {
-            const int j = c0 + jj;
+            const int j = s_j[jj];
             const float *trow = shrink_tc ? tfin + (size_t)j * LORA_MAX_RANK : Tm + (size_t)j * rpmax;
             tv[i] = __ldcg(reinterpret_cast<const float4 *>(trow + r));
         }
@@ -967,24 +985,19 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     const int it0 = w_iter_begin + lt * k_blocks;
     const int c_first = cta_of(it0, p.w_iters, p.n_cta);
     const int np = cta_of(it0 + k_blocks - 1, p.w_iters, p.n_cta) - c_first + 1;
-    // base: the columns c0 .. c0 + 15 of every piece (4 column quads per thread), added in k order
-    float4 v4[kFinRows / 4];
+    // base: the block's 16 sorted positions of every piece, added in k order
+    float v[kFinRows];
     {
-        const float4 *q = piece_quads(home + (size_t)(w_tile_begin + lt) * slot_elems, c0, tid);
+        const float *q = home + (size_t)(w_tile_begin + lt) * slot_elems + (size_t)c0 * kBM + tid;
 #pragma unroll
-        for (int kq = 0; kq < kFinRows / 4; ++kq) v4[kq] = __ldcg(q + kq * kBM);
-        for (int k = 1; k < np; ++k) {
-            const float4 *qq = piece_quads(ctaw + (size_t)(c_first + k) * slot_elems, c0, tid);
-            float4 f[kFinRows / 4];
+        for (int k = 0; k < kFinRows; ++k) v[k] = __ldcg(q + k * kBM);
+        for (int pc = 1; pc < np; ++pc) {
+            const float *qq = ctaw + (size_t)(c_first + pc) * slot_elems + (size_t)c0 * kBM + tid;
+            float f[kFinRows];
 #pragma unroll
-            for (int kq = 0; kq < kFinRows / 4; ++kq) f[kq] = __ldcg(qq + kq * kBM);
+            for (int k = 0; k < kFinRows; ++k) f[k] = __ldcg(qq + k * kBM);
 #pragma unroll
-            for (int kq = 0; kq < kFinRows / 4; ++kq) {
-                v4[kq].x += f[kq].x;
-                v4[kq].y += f[kq].y;
-                v4[kq].z += f[kq].z;
-                v4[kq].w += f[kq].w;
-            }
+            for (int k = 0; k < kFinRows; ++k) v[k] += f[k];
         }
     }
 #pragma unroll
@@ -1002,8 +1015,6 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     if constexpr (ONE) {
         // ---- expand (every index into out[] is a compile-time constant: nothing goes through
         // local memory, which the L1-light carve-out would send to L2)
-        const float v[kFinRows] = {v4[0].x, v4[0].y, v4[0].z, v4[0].w, v4[1].x, v4[1].y, v4[1].z, v4[1].w,
-                                   v4[2].x, v4[2].y, v4[2].z, v4[2].w, v4[3].x, v4[3].y, v4[3].z, v4[3].w};
         cp_async_wait_all();
         __syncthreads();  // the tiles and t visible to every thread
         float out[kFinRows];
@@ -1024,12 +1035,7 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
         for (int k = 0; k < kFinRows; ++k) ys[k * kBM + tid] = out[k];
     } else {
 #pragma unroll
-        for (int kq = 0; kq < kFinRows / 4; ++kq) {  // y column tid starts as the base
-            ys[(4 * kq) * kBM + tid] = v4[kq].x;
-            ys[(4 * kq + 1) * kBM + tid] = v4[kq].y;
-            ys[(4 * kq + 2) * kBM + tid] = v4[kq].z;
-            ys[(4 * kq + 3) * kBM + tid] = v4[kq].w;
-        }
+        for (int k = 0; k < kFinRows; ++k) ys[k * kBM + tid] = v[k];  // y column tid starts as the base
         // ---- expand, pass by pass: each thread adds B_a[o] . t to its own column of y
         for (int i = 0; i < n_pass; ++i) {
             if (i + 1 < n_pass) cp_async_wait_all_but_1();
@@ -1049,7 +1055,7 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
                 }
             if (i + nbuf < n_pass) {
                 __syncthreads();  // every thread is done with this buffer
-                fin_stage<I8>(s_ri, s_off, s_pend[i + nbuf - 1], s_pend[i + nbuf], fsm + (size_t)(i % nbuf) * buf_bytes,
+                fin_stage<I8>(s_ri, s_off, skip, s_pend[i + nbuf - 1], s_pend[i + nbuf], fsm + (size_t)(i % nbuf) * buf_bytes,
                               o_base, tile_rows);
             }
         }
@@ -1067,14 +1073,14 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
                 w.y = pack_bf16x2(src[2], src[3]);
                 w.z = pack_bf16x2(src[4], src[5]);
                 w.w = pack_bf16x2(src[6], src[7]);
-                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(yv_base) + (size_t)(c0 + k) * d_out + o_base + c8) = w;
+                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(yv_base) + (size_t)s_j[k] * d_out + o_base + c8) = w;
             }
         }
     } else {
         for (int f = tid; f < nrows * 32; f += kBM) {  // runs of 4 outputs
             const int k = f >> 5, c4 = (f & 31) * 4;
             if (o_base + c4 < d_out)
-                *reinterpret_cast<float4 *>(static_cast<float *>(yv_base) + (size_t)(c0 + k) * d_out + o_base + c4) =
+                *reinterpret_cast<float4 *>(static_cast<float *>(yv_base) + (size_t)s_j[k] * d_out + o_base + c4) =
                     *reinterpret_cast<const float4 *>(ys + k * kBM + c4);
         }
     }
@@ -1130,7 +1136,7 @@ void plan_decode_finalize(DecodeParams &dp, size_t *smem_bytes) {
     dp.fin_nbuf = all <= kOne ? 1 : 2;
     dp.fin_buf = all <= kOne ? all : std::max(kTwo, tile_max);
     *smem_bytes = (size_t)dp.fin_nbuf * dp.fin_buf + kFinRows * kBM * 4 + (size_t)kFinRows * dp.rpmax * 4 +
-                  kFinRows * sizeof(RowInfo) + (2 * kFinRows + 1) * sizeof(int);
+                  kFinRows * sizeof(RowInfo) + (3 * kFinRows + 2) * sizeof(int);
 }
 
 cudaError_t launch_decode_finalize(const DecodeParams &p, size_t smem_bytes, cudaStream_t s) {
