@@ -102,6 +102,9 @@ __device__ void build_groups(const PrepParams &p, const PrepShared &sh, int ns) 
             a.pad_ = 0;
             G[g0 + k] = a;
         }
+        // the segment's rows find their t parts through the first group
+        if (cnt > 0)
+            for (int q = q0; q < q1; ++q) p.rowinfo[m][sh.perm[q]].g0 = g0;
         if (tid == 0) p.n_groups[m] = (int)tot;
     }
 }
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
                 ri.B = id >= 0 ? B_row[m] : nullptr;
                 ri.rank = (int16_t)(id >= 0 ? rank_row[m] : 0);
                 ri.rp = (int16_t)(id >= 0 ? rp_row[m] : 0);
-                ri.pad_ = 0;
+                ri.g0 = 0;
                 p.rowinfo[m][tid] = ri;
             }
     }
@@ -315,19 +318,21 @@ struct DItem {
     int32_t it0;       // the tile's first k-block in its space
 };
 
-// A CTA's items: its share of the A space first (so the shrink's t values are complete early and
-// the last CTA on each A tile adds them up while the W stream runs), then its W range.
+// A CTA's items come in two ranges, walked one after the other: its W range (W tiles of every
+// projection, split evenly over the CTAs) and its share of the A space (known only from the row
+// plan).  Which comes first is the call's choice (see the kernel).
 struct DSched {
     int64_t x, e;
     int32_t phase, cta;
-    // the W range only (before the wait, when the A space is not known yet)
+    // the W range
     __device__ void begin_w(const DecodeParams &p, int c) {
         cta = c;
         phase = 1;
         x = (int64_t)c * p.w_iters / p.n_cta;
         e = (int64_t)(c + 1) * p.w_iters / p.n_cta;
     }
-    __device__ void begin(const DecodeParams &p, int c, const DecShared &d) {
+    // the share of the A space
+    __device__ void begin_a(const DecodeParams &p, int c, const DecShared &d) {
         cta = c;
         phase = 0;
         if (c < d.a_ctas) {
@@ -354,7 +359,8 @@ struct DSched {
                 x += it.kb1 - it.kb0;
                 return true;
             }
-            begin_w(p, cta);
+            phase = 2;
+            return false;
         }
         if (phase == 1 && x < e) {
             int m = 0;
@@ -376,10 +382,9 @@ struct DSched {
     }
 };
 
-// Base pieces are kept by sorted position: the value of batch row j (the MMA's column j) for output
-// row o of the tile sits at (pos(j) * 128 + o), pos(j) being j's place in the adapter-sorted order.
-// A warp stores 128 contiguous bytes per column, and the finalize, which walks rows in sorted order,
-// reads 512 contiguous bytes per row.
+// Base pieces are kept by batch row: the value of row j (the MMA's column j) for output row o of the
+// tile sits at j * 128 + o.  A warp stores 128 contiguous bytes per column, and the finalize, whatever
+// order it walks rows in, reads 512 contiguous bytes per row.
 
 // W4: the int4 codes of one W k-block ([128 rows][32 bytes] as the TMA lays the box down) into the
 // bf16 tile of the integers the MMA reads ([128 rows][64], 128-byte swizzle: the 16-byte chunk j of
@@ -456,7 +461,6 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ DecShared dsh;
     __shared__ int32_t perm_s[LORA_MAX_DECODE_ROWS];
-    __shared__ int16_t pos_s[LORA_MAX_DECODE_ROWS];  // the inverse: sorted position of batch row j
     __shared__ int s_last;
     const int S = p.n_stages;
     // Ring slot and round of fill k without an integer division in the loops:
@@ -489,7 +493,8 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
     uint64_t *acc_full = empty + S;
     uint64_t *acc_free = acc_full + 2;
     uint64_t *mma_done = acc_free + 2;
-    uint32_t *misc = reinterpret_cast<uint32_t *>(mma_done + 1);  // [0] tmem, [1] abort
+    uint64_t *plan_ready = mma_done + 1;  // the A space and the row order are in shared memory
+    uint32_t *misc = reinterpret_cast<uint32_t *>(plan_ready + 1);  // [0] tmem, [1] abort
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -503,6 +508,7 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
             mbar_init(acc_free + b, kEpiWarps);
         }
         mbar_init(mma_done, 1);
+        mbar_init(plan_ready, 1);
         misc[1] = 0;
         fence_mbar_init();
     }
@@ -522,11 +528,14 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
     const uint64_t pol_w = l2_policy_evict_first();  // W and A: read once per call
     const uint64_t pol_x = l2_policy_evict_last();   // x: read by every tile
 
-    // Before griddepcontrol.wait: L2 prefetches of the CTA's first W k-blocks.  W is the caller's
-    // weight and no kernel of this library writes it, so HBM can be busy with it while the
-    // previous kernel (the row plan, the previous call's finalize) drains; x, the gather list and
-    // the workspace are touched only after the wait.
-    if (warp == 0 && lane == 0) {
+    // The order of a CTA's items.  W first (p.w_first): the W tiles read only W, x and the workspace
+    // of this call's parity, none of which the kernel before this one (the row plan, or the previous
+    // call's finalize, which reads the other parity's pieces) writes -- the host checks that x is not
+    // the previous call's y -- so they run while that kernel drains, and only the A tiles, which
+    // read the row plan, wait for it (griddepcontrol.wait).  Otherwise every role waits first, the
+    // A tiles come first, and the CTA's first W k-blocks are asked of L2 before the wait.
+    const bool w_first = p.w_first != 0;
+    if (!w_first && warp == 0 && lane == 0) {
         DSched sc;
         sc.begin_w(p, blockIdx.x);
         DItem it;
@@ -539,26 +548,30 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
             }
         }
     }
-    grid_dep_wait();
-    // The finalize may launch now.  Every kernel before this one has completed, so the finalize
-    // may read the row plan (and the factors) before its own wait; it waits for this grid before
-    // reading anything this grid writes.
-    if (threadIdx.x == 0) grid_dep_launch();
-    if (threadIdx.x == 32) dec_a_space(p, dsh);
-    for (int q = threadIdx.x; q < p.n; q += blockDim.x) {
-        const int j = p.perm[q];
-        perm_s[q] = j;
-        pos_s[j] = (int16_t)q;
-    }
-    __syncthreads();
+    // the A range (and with A first, everything) waits for the plan, which the epilogue warps
+    // publish after their own griddepcontrol.wait
+    auto plan_wait = [&]() -> bool {
+        grid_dep_wait();
+        return mbar_wait(plan_ready, 0, abort_flag, p.err, wait_ns);
+    };
+    // item ranges in order: 0 = W (W first), 1 = A, 2 = W (A first)
+    const int ph0 = w_first ? 0 : 1, ph1 = w_first ? 2 : 3;
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer (warp)
-        DSched sc;
-        sc.begin(p, blockIdx.x, dsh);
         DItem it;
         uint32_t k = 0;  // stage fills issued
         bool ok = true;
+        for (int ph = ph0; ok && ph < ph1; ++ph) {
+        if (ph == 1) {
+            int got = 1;
+            grid_dep_wait();
+            if (lane == 0) got = mbar_wait(plan_ready, 0, abort_flag, p.err, wait_ns) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, got, 0)) break;
+        }
+        DSched sc;
+        if (ph == 1) sc.begin_a(p, blockIdx.x, dsh);
+        else sc.begin_w(p, blockIdx.x);
         while (ok && sc.next(p, &dsh, it)) {
             const DecodeModule &M = p.mod[it.m];
             // A tile: lane l < 16 gathers group 16 tile + l (8 rows of one adapter's A) -- unless the
@@ -625,6 +638,7 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 if (lane == 0) load(sa + a_bytes, &M.tmX, wfull + sl, kb, kBK, 0, pol_x);
             }
         }
+        }
         // never leave the block with copies still landing in its shared memory: wait for the
         // latest fill of every slot
         const uint32_t issued = k;
@@ -634,11 +648,14 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
             const uint32_t idesc = idesc_bf16_f32(kBM, (uint32_t)nt);
-            DSched sc;
-            sc.begin(p, blockIdx.x, dsh);
             DItem it;
             uint32_t k = 0, li = 0;
             bool ok = true;
+            for (int ph = ph0; ok && ph < ph1; ++ph) {
+            if (ph == 1 && !plan_wait()) break;
+            DSched sc;
+            if (ph == 1) sc.begin_a(p, blockIdx.x, dsh);
+            else sc.begin_w(p, blockIdx.x);
             while (ok && sc.next(p, &dsh, it)) {
                 const int buf = li & 1;
                 // the producer's choice for an A tile: one 128-row box when its groups are
@@ -683,6 +700,7 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 umma_commit(acc_full + buf);
                 ++li;
             }
+            }
             umma_commit(mma_done);
             mbar_drain(mma_done, 0, p.err);
         }
@@ -693,14 +711,32 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
         const uint32_t lane_off = (uint32_t)lane_base << 16;
         const size_t slot_elems = (size_t)kBM * nt;
         const int ncols16 = (p.n + 15) & ~15;
-        DSched sc;
-        sc.begin(p, blockIdx.x, dsh);
+        // The plan: these warps wait for the kernel before this one, publish the A space and the row
+        // order, and let the next kernel launch.  Every kernel before this one has completed, so
+        // the finalize may read the row plan (and the factors) before its own wait; it waits for
+        // this grid before reading anything this grid writes.
+        grid_dep_wait();
+        if (threadIdx.x == 64) {
+            grid_dep_launch();
+            dec_a_space(p, dsh);
+        }
+        for (int q = threadIdx.x - 64; q < p.n; q += 128) perm_s[q] = p.perm[q];
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 64) mbar_arrive(plan_ready);
         DItem it;
         uint32_t li = 0;
+        bool go = true;
+        for (int ph = ph0; go && ph < ph1; ++ph) {
+        DSched sc;
+        if (ph == 1) sc.begin_a(p, blockIdx.x, dsh);
+        else sc.begin_w(p, blockIdx.x);
         while (sc.next(p, &dsh, it)) {
             const int buf = li & 1;
             const bool ok = mbar_wait(acc_full + buf, (li >> 1) & 1, abort_flag, p.err, wait_ns);
-            if (named_bar_or(1, 128, !ok)) break;
+            if (named_bar_or(1, 128, !ok)) {
+                go = false;
+                break;
+            }
             tc_fence_after();
             const uint32_t tacc = tmem_base + lane_off + (uint32_t)(buf * nt);
             const DecodeModule &M = p.mod[it.m];
@@ -716,7 +752,7 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (c0 + i < p.n) __stcg(piece + (size_t)pos_s[c0 + i] * kBM + o, __uint_as_float(r[i]) * wsc);
+                        if (c0 + i < p.n) __stcg(piece + (size_t)(c0 + i) * kBM + o, __uint_as_float(r[i]) * wsc);
                 }
             } else {
                 // shrink piece: lane o is slot row 128 tile + o; only the columns of the rows whose
@@ -725,13 +761,10 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 const int part = (int)blockIdx.x - a_first;
                 const size_t pstride = (size_t)p.tp_rows * LORA_MAX_RANK;
                 const int g = it.tile * kTileGroups + o / kGroupRows;  // this lane's group
-                const int ng = dsh.n_groups[it.m], kbn = M.k_blocks;
-                const bool gok = g < ng;
+                const bool gok = g < dsh.n_groups[it.m];
                 // the projection's pointers, copied out of the parameters before the stores below
-                float *const tpart = M.tpart, *const tfin = M.tfin;
+                float *const tpart = M.tpart;
                 const AGroup *const groups = M.groups;
-                int32_t *const acount = M.acount;
-                const float scale = p.scale;
                 // the lane's group and rank row; the groups are in segment order, so the batch rows
                 // (sorted positions) of a warp's four groups are one range [wq0, wq1)
                 int q0 = 0, q1 = 0, r = 0;
@@ -760,41 +793,46 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                         if (qb + u >= q0 && qb + u < q1)
                             tpart[part * pstride + (size_t)jc[u] * LORA_MAX_RANK + r] = __uint_as_float(v[u]);
                 }
-                // the tile's last CTA (a counter, no waiting) adds the parts in k order: t = s * sum
-                const int na = cta_of(it.it0 + kbn - 1, dsh.a_iters, dsh.a_ctas) - a_first + 1;
-                __threadfence();
-                named_bar_sync(1, 128);
-                if (o == 0) s_last = atomicAdd(acount + it.tile, 1) == na - 1;
-                named_bar_sync(1, 128);
-                if (s_last) {
+                // t = s * (the parts added in k order): by the finalize (p.t_fin), else by the tile's
+                // last CTA (a counter, no waiting), two rows' parts in flight
+                if (!p.t_fin) {
+                    const int na = cta_of(it.it0 + M.k_blocks - 1, dsh.a_iters, dsh.a_ctas) - a_first + 1;
+                    float *const tfin = M.tfin;
+                    const float scale = p.scale;
                     __threadfence();
-                    for (int qb = wq0; qb < wq1; qb += 2) {  // two rows' parts in flight
-                        bool own[2];
-                        int jr[2];
-                        float sum[2] = {0.f, 0.f};
+                    named_bar_sync(1, 128);
+                    if (o == 0) s_last = atomicAdd(M.acount + it.tile, 1) == na - 1;
+                    named_bar_sync(1, 128);
+                    if (s_last) {
+                        __threadfence();
+                        for (int qb = wq0; qb < wq1; qb += 2) {
+                            bool own[2];
+                            int jr[2];
+                            float sum[2] = {0.f, 0.f};
 #pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            own[u] = qb + u >= q0 && qb + u < q1;
-                            jr[u] = own[u] ? perm_s[qb + u] : 0;
-                        }
-                        for (int cp = 0; cp < na; cp += 8) {  // eight parts per row in flight, k order
-                            float pt[2][8];
+                            for (int u = 0; u < 2; ++u) {
+                                own[u] = qb + u >= q0 && qb + u < q1;
+                                jr[u] = own[u] ? perm_s[qb + u] : 0;
+                            }
+                            for (int cp = 0; cp < na; cp += 8) {  // eight parts per row in flight, k order
+                                float pt[2][8];
+#pragma unroll
+                                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c)
+                                        pt[u][c] = own[u] && cp + c < na
+                                                       ? __ldcg(tpart + (size_t)(cp + c) * pstride + (size_t)jr[u] * LORA_MAX_RANK + r)
+                                                       : 0.f;
+#pragma unroll
+                                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c)
+                                        if (cp + c < na) sum[u] = (cp + c == 0) ? pt[u][c] : sum[u] + pt[u][c];
+                            }
 #pragma unroll
                             for (int u = 0; u < 2; ++u)
-#pragma unroll
-                                for (int c = 0; c < 8; ++c)
-                                    pt[u][c] = own[u] && cp + c < na
-                                                   ? __ldcg(tpart + (size_t)(cp + c) * pstride + (size_t)jr[u] * LORA_MAX_RANK + r)
-                                                   : 0.f;
-#pragma unroll
-                            for (int u = 0; u < 2; ++u)
-#pragma unroll
-                                for (int c = 0; c < 8; ++c)
-                                    if (cp + c < na) sum[u] = (cp + c == 0) ? pt[u][c] : sum[u] + pt[u][c];
+                                if (own[u]) tfin[(size_t)jr[u] * LORA_MAX_RANK + r] = scale * sum[u];
                         }
-#pragma unroll
-                        for (int u = 0; u < 2; ++u)
-                            if (own[u]) tfin[(size_t)jr[u] * LORA_MAX_RANK + r] = scale * sum[u];
                     }
                 }
             }
@@ -803,14 +841,18 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
             if (lane == 0) mbar_arrive(acc_free + buf);
             ++li;
         }
+        }
     } else if (W4 && warp >= kConvWarp0) {
         // ---------------------------------------------------------------- int4 converters
         const int ct = threadIdx.x - 32 * kConvWarp0;
-        DSched sc;
-        sc.begin(p, blockIdx.x, dsh);
         DItem it;
         uint32_t k = 0;
         bool ok = true;
+        for (int ph = ph0; ok && ph < ph1; ++ph) {
+        if (ph == 1 && !plan_wait()) break;
+        DSched sc;
+        if (ph == 1) sc.begin_a(p, blockIdx.x, dsh);
+        else sc.begin_w(p, blockIdx.x);
         while (ok && sc.next(p, &dsh, it)) {
             for (int kb = it.kb0; kb < it.kb1; ++kb, ++k) {
                 const uint32_t s = rslot(k);
@@ -826,6 +868,7 @@ __global__ void __launch_bounds__(W4 ? kDecThreadsW4 : kDecThreads, 1) decode_ge
                 }
                 mbar_arrive(cfull + s);
             }
+        }
         }
     }
     tc_fence_before();
@@ -873,12 +916,13 @@ __device__ __noinline__ void fin_stage(const RowInfo *s_ri, const int *s_off, un
 // ONE: every B tile of the block fits one buffer (a single pass); the expand then runs fully unrolled
 // over the 16 rows with y in registers.  Otherwise passes through two buffers, y accumulating in
 // shared memory (compact code: the kernel is short-lived and starts with a cold instruction cache).
-template <bool I8, bool ONE>
+template <bool I8, bool ONE, bool TF>
 __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_constant__ DecodeParams p) {
     using BChunk = typename std::conditional<I8, uint2, uint4>::type;  // 8 elements of B
     // B tile buffers (fin_nbuf of fin_buf bytes), y [16][128] (base, then + expand), t [16][rpmax],
     // the rows' adapters, the pass plan
     extern __shared__ __align__(16) uint8_t fsm[];
+    __shared__ DecShared fds;  // the call's A space (where each A tile's t parts are)
     const int nbuf = p.fin_nbuf, buf_bytes = p.fin_buf, rpmax = p.rpmax;
     float *ys = reinterpret_cast<float *>(fsm + (size_t)nbuf * buf_bytes);
     float *ts = ys + kFinRows * kBM;
@@ -897,7 +941,11 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     const int w_tile_begin = Mp.w_tile_begin, k_blocks = Mp.k_blocks, d_out = Mp.d_out;
     const int w_iter_begin = Mp.w_iter_begin, m_tiles = Mp.m_tiles;
     const RowInfo *const rowinfo = Mp.rowinfo;
+    const float *const tpart = Mp.tpart;
     const float *const tfin = Mp.tfin;
+    constexpr bool t_fin = TF;  // the call's p.t_fin
+    const size_t pstride = (size_t)p.tp_rows * LORA_MAX_RANK;
+    const float scale = p.scale;
     const float *const Tm = Mp.T;
     void *const yv_base = Mp.y;
     const float *const home = p.home, *const ctaw = p.ctaw;
@@ -916,6 +964,8 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     // Warp 0 plans in registers: lane k holds row k; passes are taken greedily in row order, and a
     // row with the adapter of the row before it reads that row's tile.
     if (tid < 32) {
+        // lane m: the group count of the call's projection m (the A space), in flight with the rows'
+        const int gm = (TF && shrink_tc && tid < p.n_mod) ? __ldcg(p.mod[tid].n_groups) : 0;
         RowInfo ri{nullptr, 0, 0, 0};
         int j = 0;
         if (tid < nrows) {
@@ -946,6 +996,26 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
             used += b;
         }
         if (tid == 0) s_pend[np] = nrows;
+        if (shrink_tc && t_fin) {
+            // the call's A space as the gemm lays it out: projection m's tiles of 16 groups, each
+            // k_blocks k-steps long, projections in order (lanes m < n_mod, a warp scan)
+            const int kbm = tid < p.n_mod ? p.mod[tid].k_blocks : 0;
+            const int at = (min(max(gm, 0), kDecMaxGroups) + kTileGroups - 1) / kTileGroups;
+            const int am = at * kbm;
+            int incl = am;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
+            }
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            const int kmax = (int)__reduce_max_sync(0xffffffffu, (unsigned)(at > 0 ? kbm : 0));
+            if (tid < p.n_mod) fds.a_begin[tid] = incl - am;
+            if (tid == 0) {
+                fds.a_begin[p.n_mod] = total;
+                fds.a_iters = total;
+                fds.a_ctas = decode_a_ctas(total, kmax, p.n_cta);
+            }
+        }
         if (tid > np && tid <= kFinRows) s_pend[tid] = -1;
         if (tid < kFinRows) {
             s_ri[tid] = ri;
@@ -964,46 +1034,94 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     grid_dep_launch();
     // the gemm is complete: its A-tile counters start the next call at zero (even after a call
     // that gave up a wait)
-    if (blockIdx.x == 0 && blockIdx.y == 0 && shrink_tc)
+    if (blockIdx.x == 0 && blockIdx.y == 0 && shrink_tc && !t_fin)
         for (int mm = 0; mm < p.n_mod; ++mm)
             for (int i = tid; i < kDecMaxGroups / kTileGroups; i += kBM) p.mod[mm].acount[i] = 0;
     // ---- after: t (zero past each row's rank) and the tile's base pieces, all loads in flight
-    // together.  t: float4 e = tid, tid + 128 of [16 rows][rpmax / 4]
+    // together.  t is [16 rows][rpmax / 4] float4 values; with fewer values than threads, tpv
+    // threads share one value's A-tile parts (each adds every tpv-th part in k order, then the
+    // partial sums are added in a fixed order), so that the parts' loads are in flight at once.
     const int lq = __ffs(rpmax >> 2) - 1;  // log2(rpmax / 4)
+    const int nv = kFinRows << lq;
+    const int tpv = TF && nv < kBM ? kBM / nv : 1, vpt = !TF ? 2 : nv > kBM ? nv / kBM : 1;
+    const int sub = tid & (tpv - 1);
     float4 tv[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        const int e = tid + i * kBM, jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
-        tv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (jj < kFinRows && r < s_ri[jj].rank) {
+        const int e = tid / tpv + i * (kBM / tpv), jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < vpt && jj < kFinRows && r < s_ri[jj].rank) {
             const int j = s_j[jj];
-            const float *trow = shrink_tc ? tfin + (size_t)j * LORA_MAX_RANK : Tm + (size_t)j * rpmax;
-            tv[i] = __ldcg(reinterpret_cast<const float4 *>(trow + r));
+            if (shrink_tc && !t_fin) {
+                if (sub == 0) acc = __ldcg(reinterpret_cast<const float4 *>(tfin + (size_t)j * LORA_MAX_RANK + r));
+            } else if (shrink_tc) {
+                // t = s * (the A tile's parts): the tile of the group holding rank rows r .. r + 3 of
+                // the row's adapter, and the CTAs that shared it
+                const int at = (s_ri[jj].g0 + r / kGroupRows) / kTileGroups;
+                const int ia = fds.a_begin[m] + at * k_blocks;
+                const int cf = cta_of(ia, fds.a_iters, fds.a_ctas);
+                const int na = cta_of(ia + k_blocks - 1, fds.a_iters, fds.a_ctas) - cf + 1;
+                const float *tp = tpart + (size_t)j * LORA_MAX_RANK + r;
+                for (int pc = sub; pc < na; pc += 4 * tpv) {  // four parts in flight
+                    float4 pt[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        pt[c] = pc + c * tpv < na ? __ldcg(reinterpret_cast<const float4 *>(tp + (size_t)(pc + c * tpv) * pstride))
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        acc.x += pt[c].x;
+                        acc.y += pt[c].y;
+                        acc.z += pt[c].z;
+                        acc.w += pt[c].w;
+                    }
+                }
+            } else if (sub == 0) {
+                acc = __ldcg(reinterpret_cast<const float4 *>(Tm + (size_t)j * rpmax + r));
+            }
         }
+        // the value's partial sums, lanes sub = 0 .. tpv - 1 (every lane takes part)
+        for (int off = 1; off < tpv; off <<= 1) {
+            acc.x += __shfl_down_sync(0xffffffffu, acc.x, off);
+            acc.y += __shfl_down_sync(0xffffffffu, acc.y, off);
+            acc.z += __shfl_down_sync(0xffffffffu, acc.z, off);
+            acc.w += __shfl_down_sync(0xffffffffu, acc.w, off);
+        }
+        tv[i] = shrink_tc && t_fin ? make_float4(scale * acc.x, scale * acc.y, scale * acc.z, scale * acc.w) : acc;
     }
     const size_t slot_elems = (size_t)kBM * nt;
     const int it0 = w_iter_begin + lt * k_blocks;
     const int c_first = cta_of(it0, p.w_iters, p.n_cta);
     const int np = cta_of(it0 + k_blocks - 1, p.w_iters, p.n_cta) - c_first + 1;
-    // base: the block's 16 sorted positions of every piece, added in k order
+    // base: the block's rows of every piece, added in k order; the first two pieces' loads (most
+    // tiles have at most two) in flight together
     float v[kFinRows];
     {
-        const float *q = home + (size_t)(w_tile_begin + lt) * slot_elems + (size_t)c0 * kBM + tid;
+        // row k's values at s_j[k] * 128 + tid (rows past n read row 0, unused)
+        const float *q = home + (size_t)(w_tile_begin + lt) * slot_elems + tid;
+        const float *q1 = ctaw + (size_t)(c_first + 1) * slot_elems + tid;
+        float f[kFinRows];
 #pragma unroll
-        for (int k = 0; k < kFinRows; ++k) v[k] = __ldcg(q + k * kBM);
-        for (int pc = 1; pc < np; ++pc) {
-            const float *qq = ctaw + (size_t)(c_first + pc) * slot_elems + (size_t)c0 * kBM + tid;
-            float f[kFinRows];
+        for (int k = 0; k < kFinRows; ++k) {
+            const int jo = s_j[k] * kBM;
+            v[k] = __ldcg(q + jo);
+            f[k] = np > 1 ? __ldcg(q1 + jo) : 0.f;
+        }
+        if (np > 1)
 #pragma unroll
-            for (int k = 0; k < kFinRows; ++k) f[k] = __ldcg(qq + k * kBM);
+            for (int k = 0; k < kFinRows; ++k) v[k] += f[k];
+        for (int pc = 2; pc < np; ++pc) {
+            const float *qq = ctaw + (size_t)(c_first + pc) * slot_elems + tid;
+#pragma unroll
+            for (int k = 0; k < kFinRows; ++k) f[k] = __ldcg(qq + s_j[k] * kBM);
 #pragma unroll
             for (int k = 0; k < kFinRows; ++k) v[k] += f[k];
         }
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        const int e = tid + i * kBM, jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
-        if (jj < kFinRows) {
+        const int e = tid / tpv + i * (kBM / tpv), jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
+        if (i < vpt && sub == 0 && jj < kFinRows) {
             const int rank = s_ri[jj].rank;
             float4 v = tv[i];
             if (r + 1 >= rank) v.y = 0.f;
@@ -1092,7 +1210,7 @@ static size_t decode_stage_bytes(int nt, int kps, bool w4) {
     return (size_t)kps * ((size_t)kBM * kBK * 2 + (size_t)nt * kBK * 2 + (w4 ? kW4RawBytes : 0));
 }
 static size_t decode_smem_bytes(int nt, int kps, int n_stages, bool w4) {
-    return 1024 + decode_stage_bytes(nt, kps, w4) * n_stages + 8 * (3 * (size_t)n_stages + 5) + 16;
+    return 1024 + decode_stage_bytes(nt, kps, w4) * n_stages + 8 * (3 * (size_t)n_stages + 6) + 16;
 }
 
 bool plan_decode_gemm(DecodeParams &dp, size_t *smem_bytes) {
@@ -1142,10 +1260,13 @@ void plan_decode_finalize(DecodeParams &dp, size_t *smem_bytes) {
 cudaError_t launch_decode_finalize(const DecodeParams &p, size_t smem_bytes, cudaStream_t s) {
     // The finalize's blocks may land beside a gemm's CTAs (which hold most of shared memory), so they
     // ask for the same split of the SM's memory between L1 and shared memory.
-    static size_t configured[4] = {0, 0, 0, 0};
-    void (*const kernels[4])(DecodeParams) = {decode_finalize_kernel<false, false>, decode_finalize_kernel<true, false>,
-                                              decode_finalize_kernel<false, true>, decode_finalize_kernel<true, true>};
-    const int v = (p.i8 ? 1 : 0) + (p.fin_nbuf == 1 ? 2 : 0);
+    static size_t configured[6] = {0, 0, 0, 0, 0, 0};
+    void (*const kernels[6])(DecodeParams) = {
+        decode_finalize_kernel<false, false, false>, decode_finalize_kernel<true, false, false>,
+        decode_finalize_kernel<false, true, false>,  decode_finalize_kernel<true, true, false>,
+        decode_finalize_kernel<false, false, true>,  decode_finalize_kernel<false, true, true>};
+    // int8 factors have no A tiles (t comes from the CUDA-core shrink)
+    const int v = p.t_fin && !p.i8 ? 4 + (p.fin_nbuf == 1 ? 1 : 0) : (p.i8 ? 1 : 0) + (p.fin_nbuf == 1 ? 2 : 0);
     if (configured[v] == 0) {
         cudaError_t e = cudaFuncSetAttribute(kernels[v], cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared);

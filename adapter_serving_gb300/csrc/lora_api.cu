@@ -18,6 +18,7 @@
 #include <mutex>
 #include <set>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "lora_internal.h"
@@ -240,10 +241,11 @@ struct lora_pool {
     int32_t *n_groups = nullptr;      // [LORA_MAX_MODULES]
     RowInfo *rowinfo = nullptr;       // [LORA_MAX_MODULES][256] decode: each row's adapter (B, rank, slot)
     float *tpart = nullptr;           // [LORA_MAX_MODULES][kDecMaxParts][tp_rows][64] t partial sums
-    float *tfin = nullptr;            // [LORA_MAX_MODULES][tp_rows][64] decode t
+    float *home = nullptr;            // [2][w_tiles_cap][128 * nt_cap] decode base pieces from k-block 0
+    float *ctaw = nullptr;            // [2][num_sms][128 * nt_cap] decode base pieces from inside a tile
+    int call_parity = 0;              // the half of home / ctaw the next decode call writes
+    float *tfin = nullptr;            // [LORA_MAX_MODULES][tp_rows][64] decode t (summed in the gemm)
     int32_t *acount = nullptr;        // [LORA_MAX_MODULES][kDecMaxGroups / 16] A-tile completion counters
-    float *home = nullptr;            // [w_tiles_cap][128 * nt_cap] decode base pieces from k-block 0
-    float *ctaw = nullptr;            // [num_sms][128 * nt_cap] decode base pieces from inside a tile
     int tp_rows = 0, nt_cap = 0, w_tiles_cap = 0;
     uint64_t wait_ns = kWaitBudgetNs;  // budget of one in-kernel wait
     int32_t *chunk_seg0 = nullptr;    // [chunk_cap] grouped rows: first segment of each chunk
@@ -414,8 +416,8 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
                         (size_t)4 * LORA_MAX_MODULES * kDecMaxParts * p->tp_rows * LORA_MAX_RANK)) ||
         (rc = dev_alloc(p, (void **)&p->tfin, (size_t)4 * LORA_MAX_MODULES * p->tp_rows * LORA_MAX_RANK)) ||
         (rc = dev_alloc(p, (void **)&p->acount, (size_t)4 * LORA_MAX_MODULES * (kDecMaxGroups / kTileGroups))) ||
-        (rc = dev_alloc(p, (void **)&p->home, piece * p->w_tiles_cap)) ||
-        (rc = dev_alloc(p, (void **)&p->ctaw, piece * p->num_sms)) ||
+        (rc = dev_alloc(p, (void **)&p->home, 2 * piece * p->w_tiles_cap)) ||
+        (rc = dev_alloc(p, (void **)&p->ctaw, 2 * piece * p->num_sms)) ||
         (rc = dev_alloc(p, (void **)&p->chunk_seg0, (size_t)4 * p->chunk_cap)) ||
         (rc = dev_alloc(p, (void **)&p->chunk_nb, (size_t)4 * p->chunk_cap))) {
         lora_pool_destroy(p);
@@ -858,6 +860,26 @@ extern "C" int lora_profile_read(lora_pool *p, int32_t kind, int32_t *launches, 
 
 // ------------------------------------------------------------------ forward ----------------
 
+namespace {
+std::mutex g_out_mu;
+std::unordered_map<cudaStream_t, std::vector<ByteRange>> g_out;  // guarded by g_out_mu
+}  // namespace
+
+void lora::note_stream_outputs(cudaStream_t s, const ByteRange *r, int n) {
+    std::lock_guard<std::mutex> lk(g_out_mu);
+    g_out[s].assign(r, r + n);
+}
+
+bool lora::overlaps_stream_outputs(cudaStream_t s, const ByteRange *r, int n) {
+    std::lock_guard<std::mutex> lk(g_out_mu);
+    auto it = g_out.find(s);
+    if (it == g_out.end()) return false;
+    for (const ByteRange &o : it->second)
+        for (int i = 0; i < n; ++i)
+            if (r[i].lo < o.hi && o.lo < r[i].hi) return true;
+    return false;
+}
+
 // mode: kOwnGrouping (group the rows, then the call's kernels), kBuildPlan (group the rows and
 // build the gather lists of every module of the pool, nothing else), kUsePlan (the call's kernels
 // on the last plan)
@@ -931,10 +953,26 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
     dp.scale = scale;
     dp.perm = p->perm;
     dp.radapter = p->radapter;
-    dp.home = p->home;
-    dp.ctaw = p->ctaw;
+    // base pieces in the workspace half of this call's parity: the previous call's finalize may
+    // still read the other half while this call's W tiles run
+    dp.home = p->home + (size_t)p->call_parity * p->w_tiles_cap * kBM * p->nt_cap;
+    dp.ctaw = p->ctaw + (size_t)p->call_parity * p->num_sms * kBM * p->nt_cap;
     dp.err = p->err;
     dp.wait_ns = p->wait_ns;
+    {
+        ByteRange xr[LORA_MAX_MODULES] = {};
+        for (int i = 0; i < n_io; ++i) {
+            const uintptr_t lo = reinterpret_cast<uintptr_t>(io[i].x);
+            xr[i] = ByteRange{lo, lo + (uintptr_t)n * p->mod[io[i].module].d_in * 2};
+        }
+        dp.w_first = overlaps_stream_outputs(s, xr, n_io) ? 0 : 1;
+    }
+    // Where the A tiles' t parts are added up.  In the finalize when a batch of more than 128 rows
+    // can put tens of rows on one adapter (a tile's last CTA would add them one row range after
+    // another, at the end of its W stream) or the ranks are small (few values per finalize block);
+    // otherwise once per tile in the gemm, so that the many finalize blocks of wide projections
+    // read t directly.
+    dp.t_fin = (nt > 128 || rpmax <= 16) ? 1 : 0;
     // two k-blocks per pipeline stage (half the TMA requests, above all for the 8-row A gathers)
     // when every projection's d_in is a whole number of k-blocks and the batch fills at most 128
     // columns (a stage of a 256-row batch would leave only two in shared memory)
@@ -997,6 +1035,7 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
     plan_decode_finalize(dp, &fsmem);
     e = timed_launch(p, LORA_KERNEL_FINALIZE, s, [&] { return launch_decode_finalize(dp, fsmem, s); });
     if (e != cudaSuccess) return cuda_fail(e, "finalize kernel");
+    p->call_parity ^= 1;
     return LORA_OK;
 }
 
@@ -1160,8 +1199,18 @@ static int forward_impl(lora_pool *p, int n_io, const IoDesc *io, const int32_t 
         p->plan_n = n;
         return LORA_OK;
     }
-    return decode ? decode_call(p, n_io, io, n, scale, y_dtype, s, w4, slot_of)
-                  : grouped_call(p, n_io, io, n, scale, y_dtype, s);
+    const int rc = decode ? decode_call(p, n_io, io, n, scale, y_dtype, s, w4, slot_of)
+                          : grouped_call(p, n_io, io, n, scale, y_dtype, s);
+    if (rc == LORA_OK) {
+        ByteRange yr[LORA_MAX_MODULES] = {};
+        const size_t es = y_dtype == LORA_DTYPE_BF16 ? 2 : 4;
+        for (int i = 0; i < n_io; ++i) {
+            const uintptr_t lo = reinterpret_cast<uintptr_t>(io[i].y);
+            yr[i] = ByteRange{lo, lo + (uintptr_t)((size_t)n * p->mod[io[i].module].d_out * es)};
+        }
+        note_stream_outputs(s, yr, n_io);
+    }
+    return rc;
 }
 
 namespace {

@@ -62,7 +62,7 @@ static_assert(sizeof(AGroup) == 16, "AGroup layout");
 struct RowInfo {
     const uint16_t *B;  // the adapter's B [d_out, rp] (bytes for int8 factors); null: base only
     int16_t rank, rp;
-    int32_t pad_;
+    int32_t g0;         // bf16 factors: the first gathered group of the row's adapter (its t parts)
 };
 static_assert(sizeof(RowInfo) == 16, "RowInfo layout");
 
@@ -83,8 +83,8 @@ struct DecodeModule {
     const RowInfo *rowinfo;    // [n] per row: its adapter's B, rank, slot row
     const float *T;            // int8 factors: t rows [n][rpmax] from the CUDA-core shrink
     float *tpart;              // [kDecMaxParts][tp_rows][64] t partial sums of the A tiles
-    float *tfin;               // [tp_rows][64] t = s * (sum of the parts), written by each A tile's last CTA
-    int32_t *acount;           // [kDecMaxGroups / 16] CTAs done with each A tile (reset by the last one)
+    float *tfin;               // [tp_rows][64] t = s * (sum of the parts), by each A tile's last CTA (t_fin = 0)
+    int32_t *acount;           // [kDecMaxGroups / 16] CTAs done with each A tile (t_fin = 0; the finalize resets it)
     void *y;
     int32_t d_in, d_out, m_tiles;
     int32_t k_blocks;          // k-steps of a tile (kps k-blocks of 64 each)
@@ -120,8 +120,19 @@ struct DecodeParams {
     float *ctaw;          // [n_cta][kBM * nt] base pieces that start inside their tile
     int32_t *err;         // [0] code, [1] detail
     uint64_t wait_ns;     // budget of one in-kernel wait
+    int32_t w_first;      // 1: each CTA runs its W range before it waits for the kernel before it
+    int32_t t_fin;        // 1: the finalize adds the A tiles' t parts; 0: each tile's last CTA does (tfin)
 };
 static_assert(sizeof(DecodeParams) <= 32764, "decode parameters exceed the kernel parameter space");
+
+// The outputs (y) of the library's last forward on a stream.  Its kernels let the next kernel on the
+// stream start before they finish, so a decode call reads its x before its griddepcontrol.wait only
+// when x overlaps none of them.
+struct ByteRange {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+void note_stream_outputs(cudaStream_t s, const ByteRange *r, int n);
+bool overlaps_stream_outputs(cudaStream_t s, const ByteRange *r, int n);
 
 // ========================================================== grouped rows (prefill) ==========
 //

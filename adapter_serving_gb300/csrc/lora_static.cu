@@ -47,9 +47,7 @@ constexpr size_t kOffNGroups = al(kOffGroups + sizeof(AGroup) * kStMaxRows * (LO
 constexpr size_t kOffRowInfo = al(kOffNGroups + 16);
 constexpr size_t kOffErr = al(kOffRowInfo + sizeof(RowInfo) * kStMaxRows);  // cleared at every call
 constexpr size_t kOffTpart = al(kOffErr + 16);
-constexpr size_t kOffTfin = al(kOffTpart + 4 * (size_t)kDecMaxParts * kStMaxRows * LORA_MAX_RANK);
-constexpr size_t kOffACount = al(kOffTfin + 4 * (size_t)kStMaxRows * LORA_MAX_RANK);  // zero after every call
-constexpr size_t kOffHome = al(kOffACount + 4 * (size_t)(kDecMaxGroups / kTileGroups));
+constexpr size_t kOffHome = al(kOffTpart + 4 * (size_t)kDecMaxParts * kStMaxRows * LORA_MAX_RANK);
 constexpr size_t kOffCtaw = al(kOffHome + 4 * (size_t)kStMaxTiles * kBM * kStNt);
 constexpr size_t kStaticBytes = al(kOffCtaw + 4 * (size_t)kStMaxCta * kBM * kStNt);
 static_assert(kOffTpart % 256 == 0 && kOffHome % 256 == 0 && kOffCtaw % 256 == 0, "alignment");
@@ -192,8 +190,7 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     dm.n_groups = pp.n_groups;
     dm.rowinfo = pp.rowinfo[0];
     dm.tpart = reinterpret_cast<float *>(scratch + kOffTpart);
-    dm.tfin = reinterpret_cast<float *>(scratch + kOffTfin);
-    dm.acount = reinterpret_cast<int32_t *>(scratch + kOffACount);
+    dp.t_fin = 1;  // the finalize adds the A tiles' t parts (no counters in the scratch)
     dm.y = y;
     dm.d_in = d_in;
     dm.d_out = d_out;
@@ -210,5 +207,8 @@ extern "C" int lora_linear_forward_static(const void *x, const void *W, int32_t 
     plan_decode_finalize(dp, &fsmem);
     if ((e = launch_decode_finalize(dp, fsmem, s)) != cudaSuccess)  // pieces + expand -> y
         return fail(LORA_ECUDA, std::string("finalize kernel: ") + cudaGetErrorString(e));
+    const uintptr_t ylo = reinterpret_cast<uintptr_t>(y);
+    const ByteRange yr{ylo, ylo + (uintptr_t)((size_t)n * d_out * (y_dtype == LORA_DTYPE_BF16 ? 2 : 4))};
+    note_stream_outputs(s, &yr, 1);
     return LORA_OK;
 }
