@@ -35,6 +35,13 @@
  *    stream are asynchronous with respect to the host.  All calls on one pool must be
  *    ordered with each other (one stream, or explicit events): the pool's workspace and
  *    table are shared by its calls.
+ *  - The forward kernels are programmatic dependents of the kernel before them on the stream
+ *    (they may start while it drains), and a decode call streams its W tiles -- reading W and
+ *    x -- before it waits for that kernel.  An x that the library's previous forward on the
+ *    same stream wrote is detected, and that call waits first.  An x or W produced by another
+ *    library's kernel that itself lets dependents start early
+ *    (cudaTriggerProgrammaticLaunchCompletion) before it has written them must be separated
+ *    from the forward by an event or a stream synchronisation.
  *  - Shapes: d_in and d_out must be multiples of 8; 1 <= rank <= 64.
  */
 #ifndef LORA_GB300_H
