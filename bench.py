@@ -719,7 +719,7 @@ def _build():
 # mean of the q/k/v and o launches of the workload, from the ncu captures summarised in profiles/
 # (decode_gemm_kernel_*); absent for a workload without a capture, and to be removed whenever the
 # kernel changes.
-GEMM_DRAM_BYTES_PER_LAUNCH = {"attn70b": 191129984, "zipf": 246029056, "attn70b_w4": 75305088}
+GEMM_DRAM_BYTES_PER_LAUNCH = {"attn70b": 191158528, "zipf": 246900992, "attn70b_w4": 76158208}
 
 
 def main():
