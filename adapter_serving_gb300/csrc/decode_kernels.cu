@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
 //
 // decode_gemm_kernel: one CTA per SM (at most), warp roles: warp 0 is the TMA producer, lane 0 of
 // warp 1 issues tcgen05.mma, warps 2-5 are the epilogue (TMEM lane quarter = warp % 4); with an
-// int4 base, warps 6-7 convert W codes to bf16 between the TMA load and the MMA.  MMA M = 128 rows of W or of the gathered A rows,
+// int4 base, warps 6-9 convert W codes to bf16 between the TMA load and the MMA.  MMA M = 128 rows of W or of the gathered A rows,
 // N = the batch (nt columns, column = row of the batch), K = d_in in 64-wide k-blocks.  Each of the
 // two tile spaces is split stream-K: CTA c takes k-blocks [c T / N, (c + 1) T / N) of the W space
 // (T = all W tiles' k-blocks, N = CTAs), then its share of the A space (whose size the prep decided

@@ -26,8 +26,7 @@ constexpr int kBK = 64;        // K per pipeline stage (one 128-byte swizzle row
 constexpr int kEpiWarps = 4;   // epilogue warps (one per TMEM lane quarter)
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 // int4 base weights: converter warps unpack each W k-block's codes into the bf16 tile the MMA reads
-constexpr int kConvWarps = 2;
-constexpr int kGemmThreadsW4 = kGemmThreads + 32 * kConvWarps;
+constexpr int kConvWarps = 4;
 constexpr int kW4RawBytes = kBM * kBK / 2;  // packed codes of one W k-block (two per byte)
 constexpr int kMaxStages = 8;
 constexpr int kShrinkThreads = 256;
