@@ -108,6 +108,8 @@ _sig("lora_plan_rows", ctypes.c_int, _P, _P, _I32, _P)
 _sig("lora_layer_forward_planned", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _F, _I32, _P)
 _sig("lora_layer_forward_w4", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io_w4), _P, _I32, _F, _I32, _P)
 _sig("lora_layer_forward_planned_w4", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io_w4), _F, _I32, _P)
+_sig("lora_layer_step_host_w4", ctypes.c_int, _P, _P, _P, _I32, _I32, ctypes.POINTER(_I32),
+     ctypes.POINTER(lora_module_io_w4), ctypes.POINTER(_P), ctypes.POINTER(_P), _F, _I32, _P)
 _sig("lora_linear_forward", ctypes.c_int, _P, _I32, _P, _P, _P, _I32, _F, _P, _I32, _P)
 _sig("lora_segment_forward", ctypes.c_int, _P, _I32, ctypes.POINTER(lora_module_io), _P, _P, _I32, _I32, _F,
      _I32, _P)
@@ -556,6 +558,21 @@ class Pool:
         hy = (_P * max(1, len(flat)))(*[t.data_ptr() for t in host_y])
         _check(lib.lora_layer_step_host(self.handle, _ptr(host_ids), _ptr(ids), ids.numel(), len(stages), sn, arr, hx,
                                         hy, float(scale), dt, _stream(stream)), "lora_layer_step_host")
+
+    def layer_step_host_w4(self, stages, row_adapter_ids, host_ids, host_x, host_y, scale, stream=None):
+        """lora_layer_step_host_w4: as layer_step_host, each stage's entries (module, x, W_codes,
+        W_scale, y) as for layer_forward_w4."""
+        import torch
+        flat = [io for st in stages for io in st]
+        arr, dt = self._ios_w4(flat)
+        sn = (_I32 * max(1, len(stages)))(*[len(st) for st in stages])
+        ids = _dev_i32(row_adapter_ids, "row_adapter_ids")
+        if host_ids.dtype != torch.int32 or host_ids.numel() != ids.numel():
+            raise ValueError("host_ids: int32, one per row")
+        hx = (_P * max(1, len(stages)))(*[t.data_ptr() for t in host_x])
+        hy = (_P * max(1, len(flat)))(*[t.data_ptr() for t in host_y])
+        _check(lib.lora_layer_step_host_w4(self.handle, _ptr(host_ids), _ptr(ids), ids.numel(), len(stages), sn, arr,
+                                           hx, hy, float(scale), dt, _stream(stream)), "lora_layer_step_host_w4")
 
     def host_wait(self, stream=None):
         """Make `stream` wait for every download layer_step_host has queued (lora_pool_host_wait)."""

@@ -1293,9 +1293,24 @@ int lora_layer_step(lora_pool *p, const int32_t *ids, int32_t n, int32_t n_stage
     return LORA_OK;
 }
 
-int lora_layer_step_host(lora_pool *p, const int32_t *host_ids, int32_t *row_adapter_ids, int32_t n, int32_t n_stages,
-                         const int32_t *stage_n, const lora_module_io *io, const void *const *host_x,
-                         void *const *host_y, float scale, int32_t y_dtype, lora_stream_t stream) {
+}  // extern "C"
+
+namespace {
+int planned_forward(lora_pool *p, int32_t n_io, const lora_module_io *io, float scale, int32_t y_dtype,
+                    lora_stream_t stream) {
+    return lora_layer_forward_planned(p, n_io, io, scale, y_dtype, stream);
+}
+int planned_forward(lora_pool *p, int32_t n_io, const lora_module_io_w4 *io, float scale, int32_t y_dtype,
+                    lora_stream_t stream) {
+    return lora_layer_forward_planned_w4(p, n_io, io, scale, y_dtype, stream);
+}
+
+// lora_layer_step_host and its int4-base twin: IO is lora_module_io or lora_module_io_w4 (module,
+// x and y are what this code reads of it)
+template <class IO>
+int step_host(lora_pool *p, const int32_t *host_ids, int32_t *row_adapter_ids, int32_t n, int32_t n_stages,
+              const int32_t *stage_n, const IO *io, const void *const *host_x, void *const *host_y, float scale,
+              int32_t y_dtype, lora_stream_t stream) {
     if (!p || !host_ids || !row_adapter_ids || n < 0 || n_stages < 0 || (n_stages > 0 && (!stage_n || !io || !host_x || !host_y)))
         return LORA_EINVAL;
     if (y_dtype != LORA_DTYPE_F32 && y_dtype != LORA_DTYPE_BF16) return LORA_EINVAL;
@@ -1349,7 +1364,7 @@ int lora_layer_step_host(lora_pool *p, const int32_t *host_ids, int32_t *row_ada
     // next call) computes
     const size_t esz = y_dtype == LORA_DTYPE_F32 ? 4 : 2;
     for (int st = 0, off = 0; st < n_stages; off += stage_n[st], ++st) {
-        if ((rc = lora_layer_forward_planned(p, stage_n[st], io + off, scale, y_dtype, stream)) != LORA_OK) return rc;
+        if ((rc = planned_forward(p, stage_n[st], io + off, scale, y_dtype, stream)) != LORA_OK) return rc;
         LORA_CUDA(cudaEventRecord(p->stage_done[(size_t)st], s));
         LORA_CUDA(cudaStreamWaitEvent(p->d2h, p->stage_done[(size_t)st], 0));
         for (int i = off; i < off + stage_n[st]; ++i)
@@ -1360,6 +1375,22 @@ int lora_layer_step_host(lora_pool *p, const int32_t *host_ids, int32_t *row_ada
     LORA_CUDA(cudaEventRecord(bs->out_free, p->d2h));
     bs->used = true;
     return LORA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int lora_layer_step_host(lora_pool *p, const int32_t *host_ids, int32_t *row_adapter_ids, int32_t n, int32_t n_stages,
+                         const int32_t *stage_n, const lora_module_io *io, const void *const *host_x,
+                         void *const *host_y, float scale, int32_t y_dtype, lora_stream_t stream) {
+    return step_host(p, host_ids, row_adapter_ids, n, n_stages, stage_n, io, host_x, host_y, scale, y_dtype, stream);
+}
+
+int lora_layer_step_host_w4(lora_pool *p, const int32_t *host_ids, int32_t *row_adapter_ids, int32_t n,
+                            int32_t n_stages, const int32_t *stage_n, const lora_module_io_w4 *io,
+                            const void *const *host_x, void *const *host_y, float scale, int32_t y_dtype,
+                            lora_stream_t stream) {
+    return step_host(p, host_ids, row_adapter_ids, n, n_stages, stage_n, io, host_x, host_y, scale, y_dtype, stream);
 }
 
 int lora_pool_host_wait(lora_pool *p, lora_stream_t stream) {

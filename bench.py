@@ -422,94 +422,36 @@ def run_ours(args, w):
         h2d = sum(x.numel() * 2 for x in hx) + hid.numel() * 4
         d2h = sum(y.numel() * 4 for y in hy.values())
 
-        if not w4:
-            # One library call per step with host buffers (lora_layer_step_host): the ids and the
-            # stages' x go up, the step runs, every y comes back (a stage's outputs while the next
-            # stage computes); the call's work ends when the last output has landed.  Steps run back
-            # to back on one stream, so all bytes of both directions are inside the timed region.
-            # No L2 flush between steps: each step reads W, more than the 129 MB L2 (see "timing").
-            sets = []
-            for b in range(2):  # two device buffer sets, alternating: step k+1's inputs go up while step k computes
-                xb = [torch.empty_like(x) for x in xd]
-                yb = {m: torch.empty_like(yd[m]) for m in names}
-                sets.append((torch.empty_like(ids), [[io_of(m, xb[st], yb[m]) for m in mods]
-                                                     for st, mods in enumerate(w.stages)]))
-            hy_sets = [[torch.empty_like(hy[m]).pin_memory() for mods in w.stages for m in mods] for _ in range(2)]
+        # One library call per step with host buffers (lora_layer_step_host, or its int4-base twin
+        # lora_layer_step_host_w4): the ids and the stages' x go up, the step runs, every y comes
+        # back (a stage's outputs while the next stage computes); the call's work ends when the
+        # last output has landed.  Steps run back to back on one stream, so all bytes of both
+        # directions are inside the timed region.  No L2 flush between steps (see "timing").
+        step_host = pool.layer_step_host_w4 if w4 else pool.layer_step_host
+        sets = []
+        for b in range(2):  # two device buffer sets, alternating: step k+1's inputs go up while step k computes
+            xb = [torch.empty_like(x) for x in xd]
+            yb = {m: torch.empty_like(yd[m]) for m in names}
+            sets.append((torch.empty_like(ids), [[io_of(m, xb[st], yb[m]) for m in mods]
+                                                 for st, mods in enumerate(w.stages)]))
+        hy_sets = [[torch.empty_like(hy[m]).pin_memory() for mods in w.stages for m in mods] for _ in range(2)]
 
-            def e2e_run(k_steps):
-                """k_steps steps, one call each; returns (device ms, host wall ms) per step."""
-                start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                torch.cuda.synchronize()
-                t0 = time.perf_counter()
-                start.record(stream)
-                for k in range(k_steps):
-                    ids_b, stages_b = sets[k % 2]
-                    pool.layer_step_host(stages_b, ids_b, hid, hx, hy_sets[k % 2], w.scale, stream=stream)
-                pool.host_wait(stream=stream)  # every step's outputs are in host memory
-                end.record(stream)
-                torch.cuda.synchronize()
-                return start.elapsed_time(end) / k_steps, (time.perf_counter() - t0) * 1e3 / k_steps
-            how = ("one lora_layer_step_host call per step (ids and x up, the step, every y down; pinned host "
-                   "buffers, two device buffer sets alternating, so a step's copies overlap its neighbours' "
-                   "compute)")
-        else:
-            # int4 base: the serving loop keeps the host I/O of neighbouring steps in flight: while
-            # step k computes, step k+1's ids and x go up and step k-1's y comes back.  Device
-            # buffers alternate between two sets; all bytes of both directions of every step are
-            # inside the timed region (first upload to last download).
-            up = torch.cuda.Stream(device=dev)
-            down = torch.cuda.Stream(device=dev)
-            dbuf = []
-            for b in range(2):
-                xb = [torch.empty_like(x) for x in xd]
-                yb = {m: torch.empty_like(yd[m]) for m in names}
-                io_b = [[io_of(m, xb[st], yb[m]) for m in mods] for st, mods in enumerate(w.stages)]
-                dbuf.append({"ids": torch.empty_like(ids), "x": xb, "y": yb, "io": io_b})
-            hyb = [{m: torch.empty(w.n_rows, w.modules[m][1], dtype=torch.float32).pin_memory() for m in names}
-                   for _ in range(2)]
-
-            def e2e_run(k_steps):
-                """k_steps pipelined steps; returns (device ms, host wall ms) per step."""
-                start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                inputs_free = [None, None]   # compute done with a buffer set's ids and x
-                outputs_free = [None, None]  # download done from a buffer set's y
-                torch.cuda.synchronize()
-                t0 = time.perf_counter()
-                start.record(up)
-                up.wait_stream(stream)
-                for k in range(k_steps):
-                    b = k % 2
-                    B = dbuf[b]
-                    with torch.cuda.stream(up):  # this step's inputs
-                        if inputs_free[b] is not None:
-                            up.wait_event(inputs_free[b])
-                        B["ids"].copy_(hid, non_blocking=True)
-                        for st in range(len(hx)):
-                            B["x"][st].copy_(hx[st], non_blocking=True)
-                        ready = torch.cuda.Event()
-                        ready.record(up)
-                    stream.wait_event(ready)
-                    if outputs_free[b] is not None:
-                        stream.wait_event(outputs_free[b])
-                    pool.plan_rows(B["ids"], stream=stream)
-                    for st, io in enumerate(B["io"]):
-                        forward_planned(io, w.scale, stream=stream)
-                        done = torch.cuda.Event()
-                        done.record(stream)
-                        with torch.cuda.stream(down):  # this call's outputs
-                            down.wait_event(done)
-                            for m in w.stages[st]:
-                                hyb[b][m].copy_(B["y"][m], non_blocking=True)
-                    inputs_free[b] = done
-                    freed = torch.cuda.Event()
-                    freed.record(down)
-                    outputs_free[b] = freed
-                stream.wait_stream(up)
-                stream.wait_stream(down)
-                end.record(stream)
-                torch.cuda.synchronize()
-                return start.elapsed_time(end) / k_steps, (time.perf_counter() - t0) * 1e3 / k_steps
-            how = "two buffer sets, host I/O of neighbouring steps overlapped with compute"
+        def e2e_run(k_steps):
+            """k_steps steps, one call each; returns (device ms, host wall ms) per step."""
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            start.record(stream)
+            for k in range(k_steps):
+                ids_b, stages_b = sets[k % 2]
+                step_host(stages_b, ids_b, hid, hx, hy_sets[k % 2], w.scale, stream=stream)
+            pool.host_wait(stream=stream)  # every step's outputs are in host memory
+            end.record(stream)
+            torch.cuda.synchronize()
+            return start.elapsed_time(end) / k_steps, (time.perf_counter() - t0) * 1e3 / k_steps
+        how = ("one lora_layer_step_host" + ("_w4" if w4 else "") + " call per step (ids and x up, the step, "
+               "every y down; pinned host buffers, two device buffer sets alternating, so a step's copies "
+               "overlap its neighbours' compute)")
 
         e2e_run(4)  # warm-up
         barrier()
@@ -719,7 +661,7 @@ def _build():
 # mean of the q/k/v and o launches of the workload, from the ncu captures summarised in profiles/
 # (decode_gemm_kernel_*); absent for a workload without a capture, and to be removed whenever the
 # kernel changes.
-GEMM_DRAM_BYTES_PER_LAUNCH = {"attn70b": 191158528, "zipf": 246900992, "attn70b_w4": 76158208}
+GEMM_DRAM_BYTES_PER_LAUNCH = {"attn70b": 191158528, "zipf": 246900992, "attn70b_w4": 76028672}
 
 
 def main():

@@ -520,6 +520,16 @@ int lora_layer_forward_planned_w4(lora_pool *pool, int32_t n_io, const lora_modu
                                   int32_t y_dtype, lora_stream_t stream);
 
 /*
+ * lora_layer_step_host_w4 -- lora_layer_step_host with int4 base weights: the same host I/O, buffer
+ * sets, streams and lora_pool_host_wait, each stage run by lora_layer_forward_planned_w4.  Errors:
+ * EINVAL, and those of lora_layer_forward_planned_w4.
+ */
+int lora_layer_step_host_w4(lora_pool *pool, const int32_t *host_ids, int32_t *row_adapter_ids, int32_t n,
+                            int32_t n_stages, const int32_t *stage_n, const lora_module_io_w4 *io,
+                            const void *const *host_x, void *const *host_y, float scale, int32_t y_dtype,
+                            lora_stream_t stream);
+
+/*
  * lora_pool_last_segments -- synchronize the device and copy out the row grouping the most
  * recent forward on this pool used (computed on the device for lora_layer_forward; the
  * checked copy of the given table for lora_segment_forward).  Host outputs:

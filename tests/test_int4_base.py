@@ -246,6 +246,42 @@ def test_w4_with_power_of_two_scales_is_the_bf16_path_bit_for_bit():
 
 
 @pytest.mark.gpu
+def test_w4_host_step_gives_the_device_step_bits():
+    """lora_layer_step_host_w4: ids and x from pinned host memory, y back to it, one call per step
+    on two alternating device buffer sets; the host outputs equal the planned device calls'."""
+    import torch
+    from harness import make_pool, to_dev_bf16, to_host_bf16
+    w = _case("qkv_like")
+    qw = _quantize_base(w)
+    pool, _ = make_pool(w)
+    names = w.module_names()
+    packed = {m: (torch.from_numpy(_pack_w4(qw[m][0])).cuda(), torch.from_numpy(qw[m][1]).cuda()) for m in names}
+    ref = {}
+    for st in range(len(w.stages)):
+        ref.update(_run_w4(pool, w, st, qw, planned=True))
+    order = [m for st in w.stages for m in st]
+    hid = torch.from_numpy(w.row_adapters()).pin_memory()
+    hx = [to_host_bf16(w.x(st)).pin_memory() for st in range(len(w.stages))]
+    sets = []
+    for b in range(2):
+        ids_d = torch.full((w.n_rows,), 12345, dtype=torch.int32, device="cuda")  # garbage until uploaded
+        xb = [torch.zeros_like(to_dev_bf16(w.x(st))) for st in range(len(w.stages))]
+        yb = {m: torch.full((w.n_rows, w.modules[m][1]), float("nan"), device="cuda") for m in names}
+        stages = [[(names.index(m), xb[st], *packed[m], yb[m]) for m in w.stages[st]] for st in range(len(w.stages))]
+        hy = [torch.full((w.n_rows, w.modules[m][1]), float("nan")).pin_memory() for m in order]
+        sets.append((ids_d, stages, hy))
+    for k in range(4):
+        ids_d, stages, hy = sets[k % 2]
+        pool.layer_step_host_w4(stages, ids_d, hid, hx, hy, w.scale)
+    pool.host_wait()
+    torch.cuda.current_stream().synchronize()
+    for _, _, hy in sets:
+        for m, y in zip(order, hy):
+            assert torch.equal(y, ref[m].cpu()), m
+    pool.close()
+
+
+@pytest.mark.gpu
 def test_w4_with_int8_factors():
     """The int4 base under int8 adapter factors (both quantized variants in one call)."""
     from harness import check_close
