@@ -1037,86 +1037,102 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     if (blockIdx.x == 0 && blockIdx.y == 0 && shrink_tc && !t_fin)
         for (int mm = 0; mm < p.n_mod; ++mm)
             for (int i = tid; i < kDecMaxGroups / kTileGroups; i += kBM) p.mod[mm].acount[i] = 0;
-    // ---- after: t (zero past each row's rank) and the tile's base pieces, all loads in flight
-    // together.  t is [16 rows][rpmax / 4] float4 values; with fewer values than threads, tpv
-    // threads share one value's A-tile parts (each adds every tpv-th part in k order, then the
-    // partial sums are added in a fixed order), so that the parts' loads are in flight at once.
-    const int lq = __ffs(rpmax >> 2) - 1;  // log2(rpmax / 4)
-    const int nv = kFinRows << lq;
-    const int tpv = TF && nv < kBM ? kBM / nv : 1, vpt = !TF ? 2 : nv > kBM ? nv / kBM : 1;
-    const int sub = tid & (tpv - 1);
-    float4 tv[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int e = tid / tpv + i * (kBM / tpv), jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < vpt && jj < kFinRows && r < s_ri[jj].rank) {
-            const int j = s_j[jj];
-            if (shrink_tc && !t_fin) {
-                if (sub == 0) acc = __ldcg(reinterpret_cast<const float4 *>(tfin + (size_t)j * LORA_MAX_RANK + r));
-            } else if (shrink_tc) {
-                // t = s * (the A tile's parts): the tile of the group holding rank rows r .. r + 3 of
-                // the row's adapter, and the CTAs that shared it
-                const int at = (s_ri[jj].g0 + r / kGroupRows) / kTileGroups;
-                const int ia = fds.a_begin[m] + at * k_blocks;
-                const int cf = cta_of(ia, fds.a_iters, fds.a_ctas);
-                const int na = cta_of(ia + k_blocks - 1, fds.a_iters, fds.a_ctas) - cf + 1;
-                const float *tp = tpart + (size_t)j * LORA_MAX_RANK + r;
-                for (int pc = sub; pc < na; pc += 4 * tpv) {  // four parts in flight
-                    float4 pt[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        pt[c] = pc + c * tpv < na ? __ldcg(reinterpret_cast<const float4 *>(tp + (size_t)(pc + c * tpv) * pstride))
-                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        acc.x += pt[c].x;
-                        acc.y += pt[c].y;
-                        acc.z += pt[c].z;
-                        acc.w += pt[c].w;
-                    }
-                }
-            } else if (sub == 0) {
-                acc = __ldcg(reinterpret_cast<const float4 *>(Tm + (size_t)j * rpmax + r));
-            }
-        }
-        // the value's partial sums, lanes sub = 0 .. tpv - 1 (every lane takes part)
-        for (int off = 1; off < tpv; off <<= 1) {
-            acc.x += __shfl_down_sync(0xffffffffu, acc.x, off);
-            acc.y += __shfl_down_sync(0xffffffffu, acc.y, off);
-            acc.z += __shfl_down_sync(0xffffffffu, acc.z, off);
-            acc.w += __shfl_down_sync(0xffffffffu, acc.w, off);
-        }
-        tv[i] = shrink_tc && t_fin ? make_float4(scale * acc.x, scale * acc.y, scale * acc.z, scale * acc.w) : acc;
-    }
+    // ---- after: the tile's base pieces and t (zero past each row's rank), the pieces' loads issued
+    // first so that they are in flight while t's are.
     const size_t slot_elems = (size_t)kBM * nt;
     const int it0 = w_iter_begin + lt * k_blocks;
     const int c_first = cta_of(it0, p.w_iters, p.n_cta);
     const int np = cta_of(it0 + k_blocks - 1, p.w_iters, p.n_cta) - c_first + 1;
-    // base: the block's rows of every piece, added in k order; the first two pieces' loads (most
-    // tiles have at most two) in flight together
-    float v[kFinRows];
+    // base: the block's rows of every piece, added in k order; row k's values at s_j[k] * 128 + tid
+    // (rows past n read row 0, unused); the first two pieces (most tiles have at most two) loaded here
+    float v[kFinRows], f[kFinRows];
     {
-        // row k's values at s_j[k] * 128 + tid (rows past n read row 0, unused)
         const float *q = home + (size_t)(w_tile_begin + lt) * slot_elems + tid;
         const float *q1 = ctaw + (size_t)(c_first + 1) * slot_elems + tid;
-        float f[kFinRows];
 #pragma unroll
         for (int k = 0; k < kFinRows; ++k) {
             const int jo = s_j[k] * kBM;
             v[k] = __ldcg(q + jo);
             f[k] = np > 1 ? __ldcg(q1 + jo) : 0.f;
         }
-        if (np > 1)
+    }
+    // t is [16 rows][rpmax / 4] float4 values; with fewer values than threads, tpv threads share one
+    // value's A-tile parts (each adds every tpv-th part in k order, then the partial sums are added
+    // in a fixed order), and both of a thread's values take their parts in one loop, so that the
+    // parts' loads are in flight together.
+    const int lq = __ffs(rpmax >> 2) - 1;  // log2(rpmax / 4)
+    const int nv = kFinRows << lq;
+    const int tpv = TF && nv < kBM ? kBM / nv : 1, vpt = !TF ? 2 : nv > kBM ? nv / kBM : 1;
+    const int sub = tid & (tpv - 1);
+    float4 tv[2];
+    {
+        float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+        const float *tp[2] = {tpart, tpart};
+        int na[2] = {0, 0};
 #pragma unroll
-            for (int k = 0; k < kFinRows; ++k) v[k] += f[k];
-        for (int pc = 2; pc < np; ++pc) {
-            const float *qq = ctaw + (size_t)(c_first + pc) * slot_elems + tid;
-#pragma unroll
-            for (int k = 0; k < kFinRows; ++k) f[k] = __ldcg(qq + s_j[k] * kBM);
-#pragma unroll
-            for (int k = 0; k < kFinRows; ++k) v[k] += f[k];
+        for (int i = 0; i < 2; ++i) {
+            const int e = tid / tpv + i * (kBM / tpv), jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
+            if (i < vpt && jj < kFinRows && r < s_ri[jj].rank) {
+                const int j = s_j[jj];
+                if (shrink_tc && !t_fin) {
+                    if (sub == 0) acc[i] = __ldcg(reinterpret_cast<const float4 *>(tfin + (size_t)j * LORA_MAX_RANK + r));
+                } else if (shrink_tc) {
+                    // t = s * (the A tile's parts): the tile of the group holding rank rows r .. r + 3
+                    // of the row's adapter, and the CTAs that shared it
+                    const int at = (s_ri[jj].g0 + r / kGroupRows) / kTileGroups;
+                    const int ia = fds.a_begin[m] + at * k_blocks;
+                    const int cf = cta_of(ia, fds.a_iters, fds.a_ctas);
+                    na[i] = cta_of(ia + k_blocks - 1, fds.a_iters, fds.a_ctas) - cf + 1;
+                    tp[i] = tpart + (size_t)j * LORA_MAX_RANK + r;
+                } else if (sub == 0) {
+                    acc[i] = __ldcg(reinterpret_cast<const float4 *>(Tm + (size_t)j * rpmax + r));
+                }
+            }
         }
+        if constexpr (TF) {
+            for (int pc = sub; pc < max(na[0], na[1]); pc += 4 * tpv) {  // four parts of each value in flight
+                float4 pt[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        pt[i][c] = pc + c * tpv < na[i]
+                                       ? __ldcg(reinterpret_cast<const float4 *>(tp[i] + (size_t)(pc + c * tpv) * pstride))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        acc[i].x += pt[i][c].x;
+                        acc[i].y += pt[i][c].y;
+                        acc[i].z += pt[i][c].z;
+                        acc[i].w += pt[i][c].w;
+                    }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            // the value's partial sums, lanes sub = 0 .. tpv - 1 (every lane takes part)
+            for (int off = 1; off < tpv; off <<= 1) {
+                acc[i].x += __shfl_down_sync(0xffffffffu, acc[i].x, off);
+                acc[i].y += __shfl_down_sync(0xffffffffu, acc[i].y, off);
+                acc[i].z += __shfl_down_sync(0xffffffffu, acc[i].z, off);
+                acc[i].w += __shfl_down_sync(0xffffffffu, acc[i].w, off);
+            }
+            tv[i] = shrink_tc && t_fin ? make_float4(scale * acc[i].x, scale * acc[i].y, scale * acc[i].z, scale * acc[i].w)
+                                       : acc[i];
+        }
+    }
+    // the pieces after the first two
+    if (np > 1)
+#pragma unroll
+        for (int k = 0; k < kFinRows; ++k) v[k] += f[k];
+    for (int pc = 2; pc < np; ++pc) {
+        const float *qq = ctaw + (size_t)(c_first + pc) * slot_elems + tid;
+#pragma unroll
+        for (int k = 0; k < kFinRows; ++k) f[k] = __ldcg(qq + s_j[k] * kBM);
+#pragma unroll
+        for (int k = 0; k < kFinRows; ++k) v[k] += f[k];
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
