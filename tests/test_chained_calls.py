@@ -51,3 +51,31 @@ def test_call_reading_the_previous_calls_output_sees_it_complete():
         assert bad.size == 0, f"up output, iteration {it}: {len(bad)} outputs outside the bf16 gate"
         ref_down = oracle_rows(w, "down", 1, x_bits=mid_bits, factors=fac)
         check_close(y.cpu().numpy(), ref_down, what=f"down on the up output, iteration {it}")
+
+
+def test_layer_step_whose_second_stage_reads_the_first_stages_output():
+    """The same inside one lora_layer_step call: stage 2's x is stage 1's y."""
+    import adapter_serving_gb300 as L  # noqa: F401
+    n_rows, n_ad = 48, 10
+    ranks = np.random.default_rng(5).choice(np.array([8, 16, 64], np.int32), n_ad)
+    mods = {"up": (256, 768), "down": (768, 384)}
+    w = wl.custom("chain_step", mods, [["up"], ["down"]], n_rows, ranks, 1.5, seed=23,
+                  ids=wl.random_ids(n_rows, n_ad, 23, p_base=0.2))
+    pool, fac = make_pool(w)
+    names = w.module_names()
+    Wu, Wd = to_dev_bf16(w.W("up")), to_dev_bf16(w.W("down"))
+    ids = torch.from_numpy(w.row_adapters()).cuda()
+    x = to_dev_bf16(w.x(0))
+    ref_up = oracle_rows(w, "up", 0, factors=fac)
+    for it in range(3):
+        mid = torch.full((n_rows, 768), float("nan"), dtype=torch.bfloat16, device="cuda")
+        y = torch.full((n_rows, 384), float("nan"), dtype=torch.bfloat16, device="cuda")
+        pool.layer_step([[(names.index("up"), x, Wu, mid)], [(names.index("down"), mid, Wd, y)]], ids, w.scale)
+        torch.cuda.synchronize()
+        mid_bits = mid.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert bf16_gate(mid_bits, ref_up).size == 0, f"up output, iteration {it}"
+        ref_down = oracle_rows(w, "down", 1, x_bits=mid_bits, factors=fac)
+        y_bits = y.view(torch.int16).cpu().numpy().view(np.uint16)
+        bad = bf16_gate(y_bits, ref_down)
+        assert bad.size == 0, f"down on the up output, iteration {it}: {len(bad)} outputs outside the bf16 gate"
+    pool.close()
