@@ -9,10 +9,11 @@
 //                           (128 gathered rows of the distinct adapters' A: the shrink A_a x).  Both
 //                           multiply the same x k-blocks; base pieces go to the workspace, the
 //                           shrink's t values (row j against its own adapter's rows only) to per-CTA
-//                           partial buffers
-//   decode_finalize_kernel  per (W tile, 16 rows): the base pieces added in k order, t summed in k
-//                           order and scaled, the expand s B_a t on CUDA cores (B read once per
-//                           distinct adapter and tile), y written
+//                           partial buffers.  The W tiles need no row plan and run first
+//   decode_finalize_kernel  per (W tile, 16 rows of the adapter-sorted batch): the base pieces added
+//                           in k order, t (the parts summed in k order and scaled, here or by the
+//                           gemm), the expand s B_a t on CUDA cores (B read once per adapter and
+//                           block), y written
 //
 // The forward is "m07 -- Multi-Adapter (LoRA) Serving", section 6 "Deep Dive A: Batching
 // Heterogeneous Adapters": one base GEMM shared by the batch plus a per-row adapter product
@@ -249,20 +250,23 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
 //
 // decode_gemm_kernel: one CTA per SM (at most), warp roles: warp 0 is the TMA producer, lane 0 of
 // warp 1 issues tcgen05.mma, warps 2-5 are the epilogue (TMEM lane quarter = warp % 4); with an
-// int4 base, warps 6-9 convert W codes to bf16 between the TMA load and the MMA.  MMA M = 128 rows of W or of the gathered A rows,
-// N = the batch (nt columns, column = row of the batch), K = d_in in 64-wide k-blocks.  Each of the
-// two tile spaces is split stream-K: CTA c takes k-blocks [c T / N, (c + 1) T / N) of the W space
-// (T = all W tiles' k-blocks, N = CTAs), then its share of the A space (whose size the prep decided
-// on the device).  Every item (a tile's k range held by one CTA) accumulates into one of two TMEM
-// buffers, so the drain of one overlaps the MMAs of the next.  W items leave base pieces in the
-// workspace; A items leave, for every row j, its share of t_j (the rows of its own adapter only),
-// and the last CTA to finish an A tile (a counter, no waiting) adds the tile's shares in k order.
-// The gemm lets its dependent launch at once: the finalize's blocks take the registers the gemm
-// leaves free and wait, so they start the moment the gemm's last CTA is done.
+// int4 base, warps 6-9 convert W codes to bf16 between the TMA load and the MMA.  MMA M = 128 rows
+// of W or of the gathered A rows, N = the batch (nt columns, column = row of the batch), K = d_in
+// in 64-wide k-blocks.  Each of the two tile spaces is split stream-K: CTA c takes k-blocks
+// [c T / N, (c + 1) T / N) of the W space (T = all W tiles' k-blocks, N = CTAs) and its share of
+// the A space (whose size the prep decided on the device): the W range first, before anything
+// waits for the row plan, unless x is the previous call's output.  Every item (a tile's k range
+// held by one CTA) accumulates into one of two TMEM buffers, so the drain of one overlaps the MMAs
+// of the next.  W items leave base pieces in the workspace half of the call's parity; A items
+// leave, for every row j, its share of t_j (the rows of its own adapter only), added up in k order
+// by the finalize or by the last CTA to finish the tile (a counter, no waiting).  The epilogue
+// warps, once they have waited for the kernel before, let the dependent launch: the finalize's
+// blocks take the resources the gemm leaves and wait, so they start the moment the gemm is done.
 //
 // decode_finalize_kernel: block (W tile, 16 rows of the batch), thread o = output row 128 tile + o:
 //   base  = the tile's pieces in k order (the piece from k-block 0, then every later CTA's)
-//   t_j   = the final t row the gemm's A-tile pass wrote, or the CUDA-core shrink's (int8 factors)
+//   t_j   = s * (the A tiles' parts in k order), summed here or by the gemm, or the CUDA-core
+//           shrink's row (int8 factors)
 //   y[j, o] = base + sum_r B_a(j)[o, r] t_j[r]
 // The rows' adapters and their B rows are fetched before the block waits for the gemm; after it,
 // one round of loads (t and the pieces), the dot products and the stores.  B is read as
