@@ -36,6 +36,7 @@ namespace lora {
 // ============================================================================ prep ==========
 
 constexpr int kPrepGroups = 4;  // groups of 256 threads; group g builds projections g, g + 4
+constexpr int kFinRows = 16;     // rows of the sorted batch per finalize block (a "row block")
 
 // Exclusive prefix sum of 64-bit values over a group of 256 threads (8 warps) on named barrier
 // `bar`; `total` receives the sum.
@@ -238,6 +239,26 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
         p.seg_start[ns] = n;
         sh.seg_q0[ns] = n;
     }
+    // The finalize's row blocks heaviest first (when its blocks take more than one wave, the ones
+    // with the most B to stage start first): a block's weight is the sum of the ranks of the
+    // distinct adapters among its 16 positions (the first projection's), ties in block order.
+    if (p.rb_order != nullptr) {
+        __shared__ int s_weight[LORA_MAX_DECODE_ROWS / kFinRows];
+        const int nrb = (n + kFinRows - 1) / kFinRows;
+        if (tid < nrb) {
+            int wgt = 0;
+            for (int q = tid * kFinRows; q < min(n, (tid + 1) * kFinRows); ++q)
+                if (sh.sorted[q] >= 0 && (q == tid * kFinRows || sh.sorted[q - 1] != sh.sorted[q])) wgt += sh.rank[0][q];
+            s_weight[tid] = wgt;
+        }
+        __syncthreads();
+        if (tid < nrb) {
+            const int wgt = s_weight[tid];
+            int pos = 0;
+            for (int b = 0; b < nrb; ++b) pos += (s_weight[b] > wgt) || (s_weight[b] == wgt && b < tid);
+            p.rb_order[pos] = tid;
+        }
+    }
     if (p.groups[0] != nullptr) {
         __syncthreads();  // the segment table is complete
         build_groups(p, sh, ns);
@@ -276,7 +297,6 @@ __global__ void __launch_bounds__(256 * kPrepGroups) prep_decode_kernel(const Pr
 constexpr int kConvWarp0 = 2 + kEpiWarps;
 constexpr int kDecThreads = 32 * (kConvWarp0);
 constexpr int kDecThreadsW4 = 32 * (kConvWarp0 + kConvWarps);
-constexpr int kFinRows = 16;                   // rows of the batch per finalize block
 constexpr uint32_t kPreL2 = 12;                // W k-blocks asked of L2 before the wait
 
 // The A space of a call, computed from the prep's group counts (one thread).
@@ -935,8 +955,10 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     int *s_pend = s_off + kFinRows;                        // [17] end row of pass i
     int *s_j = s_pend + kFinRows + 1;                      // [16] batch row of row k
     int *s_skip = s_j + kFinRows;                          // rows staged by an earlier row (bit k)
-    // the block's rows are the sorted positions c0 .. c0 + 15 (rows of one adapter are adjacent)
-    const int tid = threadIdx.x, tile = blockIdx.x, c0 = blockIdx.y * kFinRows;
+    // the block's rows are the sorted positions c0 .. c0 + 15 (rows of one adapter are adjacent);
+    // row blocks in the prep's order, heaviest first
+    const int tid = threadIdx.x, tile = blockIdx.x;
+    const int c0 = (p.rb_order != nullptr ? __ldcg(p.rb_order + blockIdx.y) : (int)blockIdx.y) * kFinRows;
     int m = 0;
     while (m + 1 < p.n_mod && p.mod[m + 1].w_tile_begin <= tile) ++m;
     // the projection's fields, copied out of the parameters once: a runtime-indexed parameter is

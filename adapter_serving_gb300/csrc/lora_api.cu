@@ -244,6 +244,7 @@ struct lora_pool {
     float *home = nullptr;            // [2][w_tiles_cap][128 * nt_cap] decode base pieces from k-block 0
     float *ctaw = nullptr;            // [2][num_sms][128 * nt_cap] decode base pieces from inside a tile
     int call_parity = 0;              // the half of home / ctaw the next decode call writes
+    int32_t *rb_order = nullptr;      // [16] the finalize's row blocks, heaviest first (written by the prep)
     float *tfin = nullptr;            // [LORA_MAX_MODULES][tp_rows][64] decode t (summed in the gemm)
     int32_t *acount = nullptr;        // [LORA_MAX_MODULES][kDecMaxGroups / 16] A-tile completion counters
     int tp_rows = 0, nt_cap = 0, w_tiles_cap = 0;
@@ -415,6 +416,7 @@ int lora_pool_create(const lora_pool_desc *d, lora_pool **out) {
         (rc = dev_alloc(p, (void **)&p->tpart,
                         (size_t)4 * LORA_MAX_MODULES * kDecMaxParts * p->tp_rows * LORA_MAX_RANK)) ||
         (rc = dev_alloc(p, (void **)&p->tfin, (size_t)4 * LORA_MAX_MODULES * p->tp_rows * LORA_MAX_RANK)) ||
+        (rc = dev_alloc(p, (void **)&p->rb_order, (size_t)4 * (LORA_MAX_DECODE_ROWS / 16))) ||
         (rc = dev_alloc(p, (void **)&p->acount, (size_t)4 * LORA_MAX_MODULES * (kDecMaxGroups / kTileGroups))) ||
         (rc = dev_alloc(p, (void **)&p->home, 2 * piece * p->w_tiles_cap)) ||
         (rc = dev_alloc(p, (void **)&p->ctaw, 2 * piece * p->num_sms)) ||
@@ -952,6 +954,7 @@ static int decode_call(lora_pool *p, int n_io, const IoDesc *io, int n, float sc
     dp.rpmax = rpmax;
     dp.scale = scale;
     dp.perm = p->perm;
+    dp.rb_order = p->rb_order;
     dp.radapter = p->radapter;
     // base pieces in the workspace half of this call's parity: the previous call's finalize may
     // still read the other half while this call's W tiles run
@@ -1176,6 +1179,7 @@ static int forward_impl(lora_pool *p, int n_io, const IoDesc *io, const int32_t 
         pp.qadapter = p->qadapter;
         if (decode) {
             pp.radapter = p->radapter;
+            pp.rb_order = p->rb_order;
             pp.n_groups = p->n_groups;
             for (int i = 0; i < n_prep; ++i) {
                 if (!p->i8) pp.groups[i] = p->groups + (size_t)slot_of[i] * kDecMaxGroups;

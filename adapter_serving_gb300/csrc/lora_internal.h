@@ -114,6 +114,7 @@ struct DecodeParams {
     int32_t fin_buf;      // bytes of one
     float scale;
     const int32_t *perm;      // sorted position -> row
+    const int32_t *rb_order;  // the finalize's row blocks (16 sorted positions each) in launch order; null: in order
     const int32_t *radapter;  // row -> validated adapter id (-1: base only)
     float *home;          // [w_tiles][kBM * nt] base pieces that start at k-block 0 of their tile
     float *ctaw;          // [n_cta][kBM * nt] base pieces that start inside their tile
@@ -243,6 +244,7 @@ struct PrepParams {
     AGroup *groups[LORA_MAX_MODULES];
     int32_t *n_groups;                // [n_mod]
     RowInfo *rowinfo[LORA_MAX_MODULES];  // decode: [n] per row: its adapter's B, rank, slot row
+    int32_t *rb_order;                // decode: [ceil(n / 16)] the finalize's row blocks, heaviest first (null: not built)
     // grouped rows: per row chunk of nt rows
     int32_t nt;
     int32_t pf_ch;
