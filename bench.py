@@ -71,6 +71,20 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def replica_rate(ms_local, rows_per_rank, world, device=None):
+    """Whole-job rate of `world` independent replicas: every rank processed rows_per_rank rows in
+    its own ms_local per step; the job's step is the slowest rank's (max over ranks, one
+    all-reduce), and the rate is all ranks' rows over it.  Returns (rows/s, the job's ms)."""
+    ms = float(ms_local)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return world * rows_per_rank / (ms / 1e3), ms
+
+
 def algorithmic_bytes(w, int8=False, w4=False):
     """Algorithmic bytes of one step: W once (int4 base: half a byte per weight plus one fp32
     scale per output row), each distinct adapter's factors once (int8: one byte per code plus the
@@ -349,13 +363,8 @@ def run_ours(args, w):
         while time.perf_counter() - t0 < 1.5:
             timed(20, ids)
         clocks = sampler.stop()
-    ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    value, ms = replica_rate(total_ms / args.steps, w.n_rows, world, dev)
     ab = algorithmic_bytes(w, int8, w4)
-    value = world * w.n_rows / (ms / 1e3)
     ranks = sorted(set(int(w.ranks[a]) for a in w.used_adapters()))
     line = {"metric": METRIC if args.workload == "attn70b" else f"{args.workload}: tokens/s", "value": value,
             "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -458,12 +467,8 @@ def run_ours(args, w):
         runs = [e2e_run(args.steps) for _ in range(5)]
         dev_ms = sorted(r[0] for r in runs)
         wall_ms = sorted(r[1] for r in runs)
-        e_ms = dev_ms[2]  # median of 5
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        line["e2e"] = {"value": world * w.n_rows / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e_value, e_ms = replica_rate(dev_ms[2], w.n_rows, world, dev)  # median of 5, max over ranks
+        line["e2e"] = {"value": e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                        "ms_per_step_runs": dev_ms, "host_wall_ms_per_step_runs": wall_ms,
                        "timing": f"{how}; median of 5 runs of {args.steps} steps (device time, first upload to "
