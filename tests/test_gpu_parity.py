@@ -27,6 +27,8 @@ def _check_all(w, pool, factors, stages=None, rows=None, y_dtype=torch.float32, 
             wv = w if ids is None else _with_ids(w, ids)
             ref = oracle_rows(wv, m, st, rows=rows, x_bits=x_bits, W_bits=W_bits[m], factors=factors)
             y = outs[m].float().cpu().numpy().astype(np.float64)
+            # every output is written (y starts as NaN), whichever rows the oracle checks
+            assert np.all(np.isfinite(y)), f"{w.name}/{m}: outputs left unwritten"
             if rows is not None:
                 y = y[np.asarray(rows)]
             if y_dtype == torch.float32:
@@ -316,7 +318,11 @@ def test_zipf_pool_5000_adapters_sampled():
                 f[(int(a), m)] = (A, B)
             pool.load(int(a), mi, to_host_bf16(A), to_host_bf16(B))
     torch.cuda.synchronize()
-    rows = _rows_by_rank(w, 32, 3)
+    # every rank class, and the first and last row of every 16-row block of the adapter-sorted
+    # batch (the finalize's blocks, launched in the prep's order)
+    perm_ref, _, _ = oracle.segments(w.ids)
+    ends = np.concatenate([np.arange(0, w.n_rows, 16), np.minimum(np.arange(15, w.n_rows + 15, 16), w.n_rows - 1)])
+    rows = np.unique(np.concatenate([_rows_by_rank(w, 32, 3), np.asarray(perm_ref)[ends]]))
     assert len(rows) >= 32
     _check_all(w, pool, f, rows=rows)
     perm, ss, sa = pool.last_segments()
