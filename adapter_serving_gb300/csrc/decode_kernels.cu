@@ -937,6 +937,14 @@ __device__ __noinline__ void fin_stage(const RowInfo *s_ri, const int *s_off, un
     cp_async_commit();
 }
 
+// The finalize's copy of the call's A space: where each projection's A tiles start, and how many CTAs
+// share it (the gemm's DecShared without the group counts, which the finalize does not keep: the
+// bytes count toward five blocks to an SM, see plan_decode_finalize).
+struct FinAShared {
+    int32_t a_begin[LORA_MAX_MODULES + 1];
+    int32_t a_iters, a_ctas;
+};
+
 // ONE: every B tile of the block fits one buffer (a single pass); the expand then runs fully unrolled
 // over the 16 rows with y in registers.  Otherwise passes through two buffers, y accumulating in
 // shared memory (compact code: the kernel is short-lived and starts with a cold instruction cache).
@@ -946,7 +954,7 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     // B tile buffers (fin_nbuf of fin_buf bytes), y [16][128] (base, then + expand), t [16][rpmax],
     // the rows' adapters, the pass plan
     extern __shared__ __align__(16) uint8_t fsm[];
-    __shared__ DecShared fds;  // the call's A space (where each A tile's t parts are)
+    __shared__ FinAShared fds;  // the call's A space (where each A tile's t parts are)
     const int nbuf = p.fin_nbuf, buf_bytes = p.fin_buf, rpmax = p.rpmax;
     float *ys = reinterpret_cast<float *>(fsm + (size_t)nbuf * buf_bytes);
     float *ts = ys + kFinRows * kBM;
@@ -1287,7 +1295,15 @@ cudaError_t launch_decode_gemm(const DecodeParams &p, size_t smem_bytes, cudaStr
 
 // The finalize's B buffers: one that holds a block's 16 tiles when they fit 32 KiB (one pass), else
 // two of 16 KiB (one rank-64 tile), filled and drained in turn (a pass takes the rows whose tiles
-// fit one buffer).  With y and t beside them a block holds at most 45 KiB: five blocks to an SM.
+// fit one buffer).  With y and t beside them a block holds at most 45,512 bytes of dynamic shared
+// memory.  An SM of this part offers 233,472 bytes to its blocks, each block's share (with the
+// 1 KiB the driver keeps per block) rounded up to 128 bytes: five blocks take 5 x 46,592 = 232,960.
+// Nine more bytes per block would round each share up by another 128 and leave four blocks to an
+// SM (the multi-pass launches of a batch of 256 rows then take a third wave).
+constexpr size_t kFinSmemMax = 2 * 16384 + (size_t)kFinRows * kBM * 4 + (size_t)kFinRows * LORA_MAX_RANK * 4 +
+                               kFinRows * sizeof(RowInfo) + (3 * kFinRows + 2) * sizeof(int);
+static_assert(5 * ((kFinSmemMax + (sizeof(FinAShared) + 15) / 16 * 16 + 1024 + 127) / 128 * 128) <= 233472,
+              "five finalize blocks to an SM");
 void plan_decode_finalize(DecodeParams &dp, size_t *smem_bytes) {
     const int cu = dp.i8 ? 8 : 16;
     const int tile_max = kBM * std::max(1, dp.rpmax / 8) * cu;
