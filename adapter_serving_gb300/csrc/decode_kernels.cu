@@ -1064,6 +1064,53 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     const unsigned skip = (unsigned)*s_skip;
     for (int i = 0; i < min(nbuf, n_pass); ++i)
         fin_stage<I8>(s_ri, s_off, skip, i == 0 ? 0 : s_pend[i - 1], s_pend[i], fsm + (size_t)i * buf_bytes, o_base, tile_rows);
+    // Where the gemm's outputs for this block are (not the outputs themselves), still before the
+    // wait: the blocks finish on the SMs the gemm left first, so what they issue after it is the
+    // tail of the call.
+    // base: the tile's stream-K pieces, the home slot and then CTAs c_first + 1 .. c_first + np - 1
+    const size_t slot_elems = (size_t)kBM * nt;
+    const int it0 = w_iter_begin + lt * k_blocks;
+    const int c_first = cta_of(it0, p.w_iters, p.n_cta);
+    const int np = cta_of(it0 + k_blocks - 1, p.w_iters, p.n_cta) - c_first + 1;
+    const float *const q = home + (size_t)(w_tile_begin + lt) * slot_elems + tid;
+    const float *const q1 = ctaw + (size_t)(c_first + 1) * slot_elems + tid;
+    // t is [16 rows][rpmax / 4] float4 values; with fewer values than threads, tpv threads share one
+    // value's A-tile parts (each adds every tpv-th part in k order, then the partial sums are added
+    // in a fixed order), and both of a thread's values take their parts in one loop, so that the
+    // parts' loads are in flight together.  A one-pass bf16 block has rank-8 rows only (16 tiles fill
+    // its 32 KiB), so 32 values: one per thread at most.
+    constexpr int kVals = (ONE && !I8) ? 1 : 2;
+    const int lq = __ffs(rpmax >> 2) - 1;  // log2(rpmax / 4)
+    const int nv = kFinRows << lq;
+    const int tpv = TF && nv < kBM ? kBM / nv : 1, vpt = !TF ? 2 : nv > kBM ? nv / kBM : 1;
+    const int sub = tid & (tpv - 1);
+    // value i: its first t part (TF: parts pstride apart) or its t, and how many (0: none)
+    const float *tp[2] = {tpart, tpart};
+    int na[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < kVals; ++i) {
+        const int e = tid / tpv + i * (kBM / tpv), jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
+        if (i < vpt && jj < kFinRows && r < s_ri[jj].rank) {
+            const int j = s_j[jj];
+            if (shrink_tc && !t_fin) {
+                if (sub == 0) {
+                    tp[i] = tfin + (size_t)j * LORA_MAX_RANK + r;
+                    na[i] = 1;
+                }
+            } else if (shrink_tc) {
+                // t = s * (the A tile's parts): the tile of the group holding rank rows r .. r + 3
+                // of the row's adapter, and the CTAs that shared it
+                const int at = (s_ri[jj].g0 + r / kGroupRows) / kTileGroups;
+                const int ia = fds.a_begin[m] + at * k_blocks;
+                const int cf = cta_of(ia, fds.a_iters, fds.a_ctas);
+                na[i] = cta_of(ia + k_blocks - 1, fds.a_iters, fds.a_ctas) - cf + 1;
+                tp[i] = tpart + (size_t)j * LORA_MAX_RANK + r;
+            } else if (sub == 0) {
+                tp[i] = Tm + (size_t)j * rpmax + r;
+                na[i] = 1;
+            }
+        }
+    }
     grid_dep_wait();
     grid_dep_launch();
     // the gemm is complete: its A-tile counters start the next call at zero (even after a call
@@ -1073,68 +1120,31 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
             for (int i = tid; i < kDecMaxGroups / kTileGroups; i += kBM) p.mod[mm].acount[i] = 0;
     // ---- after: the tile's base pieces and t (zero past each row's rank), the pieces' loads issued
     // first so that they are in flight while t's are.
-    const size_t slot_elems = (size_t)kBM * nt;
-    const int it0 = w_iter_begin + lt * k_blocks;
-    const int c_first = cta_of(it0, p.w_iters, p.n_cta);
-    const int np = cta_of(it0 + k_blocks - 1, p.w_iters, p.n_cta) - c_first + 1;
     // base: the block's rows of every piece, added in k order; row k's values at s_j[k] * 128 + tid
     // (rows past n read row 0, unused); the first two pieces (most tiles have at most two) loaded here
     float v[kFinRows], f[kFinRows];
-    {
-        const float *q = home + (size_t)(w_tile_begin + lt) * slot_elems + tid;
-        const float *q1 = ctaw + (size_t)(c_first + 1) * slot_elems + tid;
 #pragma unroll
-        for (int k = 0; k < kFinRows; ++k) {
-            const int jo = s_j[k] * kBM;
-            v[k] = __ldcg(q + jo);
-            f[k] = np > 1 ? __ldcg(q1 + jo) : 0.f;
-        }
+    for (int k = 0; k < kFinRows; ++k) {
+        const int jo = s_j[k] * kBM;
+        v[k] = __ldcg(q + jo);
+        f[k] = np > 1 ? __ldcg(q1 + jo) : 0.f;
     }
-    // t is [16 rows][rpmax / 4] float4 values; with fewer values than threads, tpv threads share one
-    // value's A-tile parts (each adds every tpv-th part in k order, then the partial sums are added
-    // in a fixed order), and both of a thread's values take their parts in one loop, so that the
-    // parts' loads are in flight together.
-    const int lq = __ffs(rpmax >> 2) - 1;  // log2(rpmax / 4)
-    const int nv = kFinRows << lq;
-    const int tpv = TF && nv < kBM ? kBM / nv : 1, vpt = !TF ? 2 : nv > kBM ? nv / kBM : 1;
-    const int sub = tid & (tpv - 1);
     float4 tv[2];
     {
         float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-        const float *tp[2] = {tpart, tpart};
-        int na[2] = {0, 0};
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int e = tid / tpv + i * (kBM / tpv), jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
-            if (i < vpt && jj < kFinRows && r < s_ri[jj].rank) {
-                const int j = s_j[jj];
-                if (shrink_tc && !t_fin) {
-                    if (sub == 0) acc[i] = __ldcg(reinterpret_cast<const float4 *>(tfin + (size_t)j * LORA_MAX_RANK + r));
-                } else if (shrink_tc) {
-                    // t = s * (the A tile's parts): the tile of the group holding rank rows r .. r + 3
-                    // of the row's adapter, and the CTAs that shared it
-                    const int at = (s_ri[jj].g0 + r / kGroupRows) / kTileGroups;
-                    const int ia = fds.a_begin[m] + at * k_blocks;
-                    const int cf = cta_of(ia, fds.a_iters, fds.a_ctas);
-                    na[i] = cta_of(ia + k_blocks - 1, fds.a_iters, fds.a_ctas) - cf + 1;
-                    tp[i] = tpart + (size_t)j * LORA_MAX_RANK + r;
-                } else if (sub == 0) {
-                    acc[i] = __ldcg(reinterpret_cast<const float4 *>(Tm + (size_t)j * rpmax + r));
-                }
-            }
-        }
         if constexpr (TF) {
-            for (int pc = sub; pc < max(na[0], na[1]); pc += 4 * tpv) {  // four parts of each value in flight
+            const int nmax = kVals > 1 ? max(na[0], na[1]) : na[0];
+            for (int pc = sub; pc < nmax; pc += 4 * tpv) {  // four parts of each value in flight
                 float4 pt[2][4];
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
+                for (int i = 0; i < kVals; ++i)
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         pt[i][c] = pc + c * tpv < na[i]
                                        ? __ldcg(reinterpret_cast<const float4 *>(tp[i] + (size_t)(pc + c * tpv) * pstride))
                                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
+                for (int i = 0; i < kVals; ++i)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         acc[i].x += pt[i][c].x;
@@ -1143,9 +1153,13 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
                         acc[i].w += pt[i][c].w;
                     }
             }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kVals; ++i)
+                if (na[i] > 0) acc[i] = __ldcg(reinterpret_cast<const float4 *>(tp[i]));
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kVals; ++i) {
             // the value's partial sums, lanes sub = 0 .. tpv - 1 (every lane takes part)
             for (int off = 1; off < tpv; off <<= 1) {
                 acc[i].x += __shfl_down_sync(0xffffffffu, acc[i].x, off);
@@ -1169,7 +1183,7 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
         for (int k = 0; k < kFinRows; ++k) v[k] += f[k];
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kVals; ++i) {
         const int e = tid / tpv + i * (kBM / tpv), jj = e >> lq, r = (e & ((1 << lq) - 1)) * 4;
         if (i < vpt && sub == 0 && jj < kFinRows) {
             const int rank = s_ri[jj].rank;
@@ -1191,7 +1205,7 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
             float d = 0.f;
             const RowInfo ri = s_ri[k];
             if (o_ok && ri.rank > 0) {
-                const int nch = ri.rp >> 3;  // 1, or 2 for int8 rank 16
+                const int nch = I8 ? ri.rp >> 3 : 1;  // 1, or 2 for int8 rank 16 (bf16: rank 8 only)
                 const BChunk *bk = reinterpret_cast<const BChunk *>(fsm + s_off[k]);
                 const float *tk = ts + k * rpmax;
                 d = dot8_b(bk[bchunk_slot(tid, 0, nch)], tk);
