@@ -1065,8 +1065,8 @@ __global__ void __launch_bounds__(kBM, 5) decode_finalize_kernel(const __grid_co
     for (int i = 0; i < min(nbuf, n_pass); ++i)
         fin_stage<I8>(s_ri, s_off, skip, i == 0 ? 0 : s_pend[i - 1], s_pend[i], fsm + (size_t)i * buf_bytes, o_base, tile_rows);
     // Where the gemm's outputs for this block are (not the outputs themselves), still before the
-    // wait: the blocks finish on the SMs the gemm left first, so what they issue after it is the
-    // tail of the call.
+    // wait: the blocks start as the gemm's CTAs leave their SMs and wait there for the whole gemm,
+    // so what they issue after the wait is the tail of the call.
     // base: the tile's stream-K pieces, the home slot and then CTAs c_first + 1 .. c_first + np - 1
     const size_t slot_elems = (size_t)kBM * nt;
     const int it0 = w_iter_begin + lt * k_blocks;
