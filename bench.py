@@ -38,6 +38,7 @@ import workloads as wl  # noqa: E402
 METRIC = "adapted-layer decode tokens/s & HBM GB/s at batch 128, distinct adapters, 1 GB300"
 UNIT = "tokens/s"
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
+L2_BYTES = 129e6  # the L2 of this part (bytes)
 
 
 def parse():
@@ -437,11 +438,20 @@ def run_ours(args, w):
         # last output has landed.  Steps run back to back on one stream, so all bytes of both
         # directions are inside the timed region.  No L2 flush between steps (see "timing").
         step_host = pool.layer_step_host_w4 if w4 else pool.layer_step_host
+        # A base that fits L2 (the int4 codes: 76 MB) could be found there by the next step; then
+        # each buffer set reads its own copy of W, so a step's W was last read two steps before.
+        w_fits_l2 = ab["W"] <= L2_BYTES
+        w_sets = [Wd, {m: (tuple(t.clone() for t in Wd[m]) if w4 else Wd[m].clone()) for m in names}
+                  if w_fits_l2 else Wd]
+
+        def io_w(m, x, y, Wm):
+            return (names.index(m), x, *Wm[m], y) if w4 else (names.index(m), x, Wm[m], y)
+
         sets = []
         for b in range(2):  # two device buffer sets, alternating: step k+1's inputs go up while step k computes
             xb = [torch.empty_like(x) for x in xd]
             yb = {m: torch.empty_like(yd[m]) for m in names}
-            sets.append((torch.empty_like(ids), [[io_of(m, xb[st], yb[m]) for m in mods]
+            sets.append((torch.empty_like(ids), [[io_w(m, xb[st], yb[m], w_sets[b]) for m in mods]
                                                  for st, mods in enumerate(w.stages)]))
         hy_sets = [[torch.empty_like(hy[m]).pin_memory() for mods in w.stages for m in mods] for _ in range(2)]
 
@@ -473,8 +483,10 @@ def run_ours(args, w):
                        "ms_per_step_runs": dev_ms, "host_wall_ms_per_step_runs": wall_ms,
                        "timing": f"{how}; median of 5 runs of {args.steps} steps (device time, first upload to "
                                  f"last download); no L2 flush ({ab['W'] / 1e6:.0f} MB of W per step"
-                                 + (" > 129 MB L2)" if ab["W"] > 129e6 else
-                                    ", less than the 129 MB L2: part of W may still be in L2 from the step before)")}
+                                 + (f" > {L2_BYTES / 1e6:.0f} MB L2)" if not w_fits_l2 else
+                                    f", less than the {L2_BYTES / 1e6:.0f} MB L2, so the two buffer sets read two "
+                                    f"copies of W: a step's W was last read two steps, {2 * ab['total'] / 1e6:.0f} MB "
+                                    "of traffic, before)")}
         code, detail = pool.last_device_error()
         if code:
             raise RuntimeError(f"device error {L.DEVERR.get(code)} at {detail}")
